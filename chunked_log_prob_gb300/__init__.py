@@ -1,0 +1,23 @@
+"""GB300 (sm_103a) selective log-prob + GRPO loss forward/backward library.
+
+Python face of the C ABI declared in ``include/grpo_gb300.h``; all compute
+runs in the CUDA library ``libgrpo_gb300.so`` built from ``csrc/``.
+"""
+
+from ._binding import (  # noqa: F401
+    EXPORTED,
+    GRPO_OK,
+    GrpoError,
+    GrpoParams,
+    GrpoShape,
+    alloc_workspace,
+    grpo_get_plan,
+    grpo_logp_fwd,
+    grpo_loss_fwd_bwd,
+    grpo_read_device_status,
+    grpo_workspace_size,
+    lib,
+    make_params,
+    make_shape,
+    status_string,
+)

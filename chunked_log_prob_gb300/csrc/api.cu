@@ -1,0 +1,506 @@
+// Host side of the C ABI: argument checks, work planning, TMA descriptor
+// encoding and the launch sequence of the forward and backward passes.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "grpo_gb300.h"
+#include "launch.h"
+
+namespace grpo {
+namespace {
+
+constexpr int kMaxSplits = 32;          // forward vocab splits (per-row partials)
+constexpr int kMaxAutoChunkBlocks = 32;  // automatic backward chunk <= 4096 rows
+constexpr int kAutoVocabBlock = 32768;   // automatic backward vocab block
+constexpr int kGroupRows = 8;            // row blocks per raster group
+constexpr size_t kHeaderBytes = 16384;   // status, counters, loss partials
+constexpr int kMaxDevices = 64;
+
+// Workspace header layout.
+constexpr size_t kOffStatus = 0;       // int
+constexpr size_t kOffCounter = 4;      // unsigned
+constexpr size_t kOffMsum = 8;         // double
+constexpr size_t kOffPartials = 64;    // double[kMaxFinalizeBlocks]
+static_assert(kOffPartials + kMaxFinalizeBlocks * sizeof(double) <= kHeaderBytes, "header");
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+struct Layout {
+  long long n, nr;  // rows, rows rounded up to BM
+  int T, D, V;
+  int nvt;          // vocab tiles
+  int chunk_rows;   // backward chunk (multiple of BM)
+  int vblock;       // backward vocab block (multiple of BN)
+  bool need_acc;    // more than one vocab block -> fp32 dH accumulator
+  size_t off_pm, off_ps, off_zy, off_lse, off_g, off_G, off_acc, total;
+};
+
+int auto_chunk_blocks(long long n_rb_total, int n_dt, int sms) {
+  // Row blocks per backward chunk: keep the dH GEMM's (row block x D tile)
+  // grid close to whole waves of the SMs; prefer larger chunks on ties.
+  const int hi = static_cast<int>(std::min<long long>(n_rb_total, kMaxAutoChunkBlocks));
+  int best = hi;
+  double best_eff = -1.0;
+  for (int nrb = hi; nrb >= 1; --nrb) {
+    const long long units = static_cast<long long>(nrb) * n_dt;
+    const long long waves = cdiv(units, sms);
+    const double eff = static_cast<double>(units) / static_cast<double>(waves * sms);
+    if (eff > best_eff + 0.02) {
+      best_eff = eff;
+      best = nrb;
+    }
+  }
+  return best;
+}
+
+int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
+  L->n = s->n_tokens;
+  L->nr = cdiv(std::max<long long>(s->n_tokens, 1), BM) * BM;
+  L->T = s->seq_len;
+  L->D = s->hidden;
+  L->V = s->vocab;
+  L->nvt = static_cast<int>(cdiv(s->vocab, BN));
+  const long long n_rb_total = L->nr / BM;
+  const int n_dt = static_cast<int>(cdiv(s->hidden, BN));
+  // chunk rows
+  long long crows;
+  if (p && p->chunk_tokens > 0) {
+    crows = cdiv(p->chunk_tokens, BM) * BM;
+  } else if (sms > 0) {
+    crows = static_cast<long long>(auto_chunk_blocks(n_rb_total, n_dt, sms)) * BM;
+  } else {  // sizing without a device: the largest automatic chunk
+    crows = std::min<long long>(n_rb_total, kMaxAutoChunkBlocks) * BM;
+  }
+  crows = std::min(crows, L->nr);
+  if (crows > INT_MAX / 2) return GRPO_ERR_UNSUPPORTED_SHAPE;
+  L->chunk_rows = static_cast<int>(crows);
+  long long vb = (p && p->vocab_block > 0) ? p->vocab_block : kAutoVocabBlock;
+  vb = cdiv(vb, BN) * BN;
+  vb = std::min<long long>(vb, static_cast<long long>(L->nvt) * BN);
+  L->vblock = static_cast<int>(vb);
+  L->need_acc = L->vblock < L->V;
+
+  size_t off = kHeaderBytes;
+  const size_t part = static_cast<size_t>(kMaxSplits) * L->nr * sizeof(float);
+  L->off_pm = off; off = align_up(off + part, 256);
+  L->off_ps = off; off = align_up(off + part, 256);
+  L->off_zy = off; off = align_up(off + L->nr * sizeof(float), 256);
+  L->off_lse = off; off = align_up(off + L->nr * sizeof(float), 256);
+  L->off_g = off; off = align_up(off + L->nr * sizeof(float), 256);
+  L->off_G = off; off = align_up(off + static_cast<size_t>(L->chunk_rows) * L->vblock * 2, 256);
+  L->off_acc = off;
+  if (L->need_acc) off = align_up(off + static_cast<size_t>(L->chunk_rows) * L->D * 4, 256);
+  L->total = off;
+  return GRPO_OK;
+}
+
+int check_shape(const grpo_shape* s, bool need_seq) {
+  if (!s) return GRPO_ERR_INVALID_ARG;
+  if (s->n_tokens < 0 || s->hidden <= 0 || s->vocab <= 0 || s->reserved != 0)
+    return GRPO_ERR_INVALID_ARG;
+  if (s->hidden % 8 != 0) return GRPO_ERR_UNSUPPORTED_SHAPE;
+  if (s->n_tokens > (1LL << 30)) return GRPO_ERR_UNSUPPORTED_SHAPE;
+  if (need_seq) {
+    if (s->seq_len <= 0) return GRPO_ERR_INVALID_ARG;
+    if (s->n_tokens % s->seq_len != 0) return GRPO_ERR_UNSUPPORTED_SHAPE;
+  }
+  return GRPO_OK;
+}
+
+int check_params(const grpo_params* p) {
+  if (!p) return GRPO_OK;
+  if (p->flags != 0 || p->reserved != 0 || p->chunk_tokens < 0 || p->vocab_block < 0)
+    return GRPO_ERR_INVALID_ARG;
+  if (!(p->eps_low >= 0.f) || !(p->eps_high >= 0.f) || !(p->beta >= 0.f))
+    return GRPO_ERR_INVALID_ARG;
+  return GRPO_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ------------------------------------------------------------ device ----
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceInfo {
+  bool ready = false;
+  int status = GRPO_OK;
+  int sms = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+
+int device_setup(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GRPO_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return GRPO_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    d.ready = true;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      d.status = GRPO_ERR_CUDA;
+    } else if (major != 10 || minor != 3) {
+      d.status = GRPO_ERR_UNSUPPORTED_DEVICE;
+    } else if (prepare_fwd_gemm() != cudaSuccess || prepare_bwd_gemms() != cudaSuccess) {
+      d.status = GRPO_ERR_CUDA;
+    }
+    if (d.status == GRPO_OK && g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        d.status = GRPO_ERR_CUDA;
+      } else {
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+      }
+    }
+  }
+  *sms = d.sms;
+  return d.status;
+}
+
+// 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows,
+// `pitch_elems` elements between rows; box {box_inner, box_outer}; 128B swizzle.
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch_elems * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct Ws {
+  uint8_t* base;
+  int* status;
+  unsigned* counter;
+  double* msum;
+  double* partials;
+  float *pm, *ps, *zy, *lse, *g, *acc;
+  __nv_bfloat16* G;
+};
+
+Ws carve(void* ws, const Layout& L) {
+  Ws w;
+  w.base = static_cast<uint8_t*>(ws);
+  w.status = reinterpret_cast<int*>(w.base + kOffStatus);
+  w.counter = reinterpret_cast<unsigned*>(w.base + kOffCounter);
+  w.msum = reinterpret_cast<double*>(w.base + kOffMsum);
+  w.partials = reinterpret_cast<double*>(w.base + kOffPartials);
+  w.pm = reinterpret_cast<float*>(w.base + L.off_pm);
+  w.ps = reinterpret_cast<float*>(w.base + L.off_ps);
+  w.zy = reinterpret_cast<float*>(w.base + L.off_zy);
+  w.lse = reinterpret_cast<float*>(w.base + L.off_lse);
+  w.g = reinterpret_cast<float*>(w.base + L.off_g);
+  w.G = reinterpret_cast<__nv_bfloat16*>(w.base + L.off_G);
+  w.acc = reinterpret_cast<float*>(w.base + L.off_acc);
+  return w;
+}
+
+TileArgs base_args(const Layout& L, const Ws& w) {
+  TileArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.vocab = L.V;
+  a.hidden = L.D;
+  a.status = w.status;
+  return a;
+}
+
+// Forward logit GEMM over all N rows: per-split (max, sum-exp) and z_y.
+int run_forward(const void* hidden, const void* W, const int32_t* ids, const uint8_t* mask,
+                const Layout& L, const Ws& w, int sms, int* splits_out, cudaStream_t st) {
+  CUtensorMap map_h, map_w;
+  if (!encode_2d(&map_h, hidden, L.D, L.n, L.D, BK, BM) ||
+      !encode_2d(&map_w, W, L.D, L.V, L.D, BK, BN))
+    return GRPO_ERR_CUDA;
+  TileArgs a = base_args(L, w);
+  a.rows = static_cast<int>(L.n);
+  a.row0 = 0;
+  a.n_rb = static_cast<int>(L.nr / BM);
+  a.k_iters = static_cast<int>(cdiv(L.D, BK));
+  a.group_rows = std::min(kGroupRows, a.n_rb);
+  int splits = std::max(1, sms / a.group_rows);
+  splits = std::min(splits, std::min(L.nvt, kMaxSplits));
+  a.n_cols = splits;
+  a.n_vtiles = L.nvt;
+  a.v0 = 0;
+  a.ids = ids;
+  a.mask = mask;
+  a.part_m = w.pm;
+  a.part_s = w.ps;
+  a.zy = w.zy;
+  a.part_ld = L.nr;
+  const long long units = static_cast<long long>(a.n_rb) * a.n_cols;
+  const int grid = static_cast<int>(std::min<long long>(units, sms));
+  if (launch_fwd_gemm(map_h, map_w, a, grid, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  *splits_out = splits;
+  return GRPO_OK;
+}
+
+int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH,
+                 const Layout& L, const Ws& w, int sms, cudaStream_t st) {
+  CUtensorMap map_h, map_w_k, map_w_mn;
+  if (!encode_2d(&map_h, hidden, L.D, L.n, L.D, BK, BM) ||
+      !encode_2d(&map_w_k, W, L.D, L.V, L.D, BK, BN) ||
+      !encode_2d(&map_w_mn, W, L.D, L.V, L.D, 64, BK))
+    return GRPO_ERR_CUDA;
+  const int n_dt = static_cast<int>(cdiv(L.D, BN));
+  for (long long c0 = 0; c0 < L.n; c0 += L.chunk_rows) {
+    const int rows_c = static_cast<int>(std::min<long long>(L.chunk_rows, L.n - c0));
+    const int n_rb = static_cast<int>(cdiv(rows_c, BM));
+    for (long long v0 = 0; v0 < L.V; v0 += L.vblock) {
+      const int width = static_cast<int>(std::min<long long>(L.vblock, L.V - v0));
+      const int ntile = static_cast<int>(cdiv(width, BN));
+      // (1) G = g (onehot - softmax) for this chunk x vocab block, bf16.
+      TileArgs a = base_args(L, w);
+      a.rows = rows_c;
+      a.row0 = static_cast<int>(c0);
+      a.n_rb = n_rb;
+      a.k_iters = static_cast<int>(cdiv(L.D, BK));
+      a.group_rows = std::min(kGroupRows, n_rb);
+      a.n_cols = ntile;
+      a.v0 = static_cast<int>(v0);
+      a.ids = ids;
+      a.lse = w.lse;
+      a.g = w.g;
+      a.G = w.G;
+      a.ldG = L.vblock;
+      long long units = static_cast<long long>(n_rb) * ntile;
+      if (launch_bwdg_gemm(map_h, map_w_k, a, static_cast<int>(std::min<long long>(units, sms)),
+                           st) != cudaSuccess)
+        return GRPO_ERR_CUDA;
+      // (2) dH_chunk (+)= G W[v0 : v0 + width].
+      CUtensorMap map_g;
+      if (!encode_2d(&map_g, w.G, width, rows_c, L.vblock, BK, BM)) return GRPO_ERR_CUDA;
+      TileArgs b = base_args(L, w);
+      b.rows = rows_c;
+      b.row0 = static_cast<int>(c0);
+      b.n_rb = n_rb;
+      b.k_iters = static_cast<int>(cdiv(width, BK));
+      b.group_rows = std::min(kGroupRows, n_rb);
+      b.n_cols = n_dt;
+      b.v0 = static_cast<int>(v0);
+      b.acc = w.acc;
+      b.dH = static_cast<__nv_bfloat16*>(dH);
+      b.first = v0 == 0;
+      b.last = v0 + L.vblock >= L.V;
+      units = static_cast<long long>(n_rb) * n_dt;
+      if (launch_dh_gemm(map_g, map_w_mn, b, static_cast<int>(std::min<long long>(units, sms)),
+                         st) != cudaSuccess)
+        return GRPO_ERR_CUDA;
+    }
+  }
+  return GRPO_OK;
+}
+
+}  // namespace
+}  // namespace grpo
+
+using namespace grpo;
+
+extern "C" {
+
+void grpo_default_params(grpo_params* p) {
+  if (!p) return;
+  std::memset(p, 0, sizeof(*p));
+  p->eps_low = 0.2f;
+  p->eps_high = 0.2f;
+  p->beta = 0.001f;
+  p->loss_denominator = 0.f;
+}
+
+int grpo_workspace_size(const grpo_shape* shape, const grpo_params* params, size_t* bytes) {
+  if (!bytes) return GRPO_ERR_INVALID_ARG;
+  int r = check_shape(shape, false);
+  if (r != GRPO_OK) return r;
+  if ((r = check_params(params)) != GRPO_OK) return r;
+  Layout L;
+  if ((r = make_layout(shape, params, 0, &L)) != GRPO_OK) return r;
+  *bytes = L.total;
+  return GRPO_OK;
+}
+
+int grpo_logp_fwd(const void* hidden, const void* W, const int32_t* ids, float* logp,
+                  float* lse_or_null, const grpo_shape* shape, const grpo_params* params,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+  int r = check_shape(shape, false);
+  if (r != GRPO_OK) return r;
+  if ((r = check_params(params)) != GRPO_OK) return r;
+  if (shape->n_tokens > 0 && (!hidden || !W || !ids || !logp || !workspace))
+    return GRPO_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(W, 16) || !aligned(workspace, 256) || !aligned(ids, 4) ||
+      !aligned(logp, 4) || !aligned(lse_or_null, 4))
+    return GRPO_ERR_MISALIGNED;
+  int sms = 0;
+  if ((r = device_setup(&sms)) != GRPO_OK) return r;
+  Layout L;
+  if ((r = make_layout(shape, params, sms, &L)) != GRPO_OK) return r;
+  Layout Lmax;
+  make_layout(shape, params, 0, &Lmax);
+  if (workspace_bytes < std::max(L.total, Lmax.total)) return GRPO_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, 64, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  if (L.n == 0) return GRPO_OK;
+  Ws w = carve(workspace, L);
+  int splits = 1;
+  if ((r = run_forward(hidden, W, ids, nullptr, L, w, sms, &splits, st)) != GRPO_OK) return r;
+  FinalizeArgs f;
+  std::memset(&f, 0, sizeof(f));
+  f.n = L.n;
+  f.splits = splits;
+  f.part_ld = L.nr;
+  f.vocab = L.V;
+  f.seq_len = 1;
+  f.loss_mode = 0;
+  f.part_m = w.pm;
+  f.part_s = w.ps;
+  f.zy = w.zy;
+  f.ids = ids;
+  f.lse_ws = w.lse;
+  f.lse_out = lse_or_null;
+  f.logp_out = logp;
+  f.status = w.status;
+  if (launch_finalize(f, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  return GRPO_OK;
+}
+
+int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
+                      const uint8_t* mask, const float* old_logp, const float* ref_logp,
+                      const float* adv, float* loss, float* logp_or_null, void* dH,
+                      const grpo_shape* shape, const grpo_params* params, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  int r = check_shape(shape, true);
+  if (r != GRPO_OK) return r;
+  if ((r = check_params(params)) != GRPO_OK) return r;
+  if (!loss || !workspace) return GRPO_ERR_INVALID_ARG;
+  if (shape->n_tokens > 0 &&
+      (!hidden || !W || !ids || !old_logp || !ref_logp || !adv || !dH))
+    return GRPO_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(W, 16) || !aligned(dH, 16) || !aligned(workspace, 256) ||
+      !aligned(ids, 4) || !aligned(old_logp, 4) || !aligned(ref_logp, 4) || !aligned(adv, 4) ||
+      !aligned(loss, 4) || !aligned(logp_or_null, 4))
+    return GRPO_ERR_MISALIGNED;
+  grpo_params prm;
+  if (params) prm = *params; else grpo_default_params(&prm);
+  int sms = 0;
+  if ((r = device_setup(&sms)) != GRPO_OK) return r;
+  Layout L;
+  if ((r = make_layout(shape, &prm, sms, &L)) != GRPO_OK) return r;
+  Layout Lmax;
+  make_layout(shape, &prm, 0, &Lmax);
+  if (workspace_bytes < std::max(L.total, Lmax.total)) return GRPO_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, 64, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  if (L.n == 0) {
+    if (cudaMemsetAsync(loss, 0, sizeof(float), st) != cudaSuccess) return GRPO_ERR_CUDA;
+    return GRPO_OK;
+  }
+  Ws w = carve(workspace, L);
+  if (launch_count_mask(mask, L.n, w.msum, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  int splits = 1;
+  if ((r = run_forward(hidden, W, ids, mask, L, w, sms, &splits, st)) != GRPO_OK) return r;
+  FinalizeArgs f;
+  std::memset(&f, 0, sizeof(f));
+  f.n = L.n;
+  f.splits = splits;
+  f.part_ld = L.nr;
+  f.vocab = L.V;
+  f.seq_len = L.T;
+  f.loss_mode = 1;
+  f.part_m = w.pm;
+  f.part_s = w.ps;
+  f.zy = w.zy;
+  f.ids = ids;
+  f.mask = mask;
+  f.old_logp = old_logp;
+  f.ref_logp = ref_logp;
+  f.adv = adv;
+  f.eps_low = prm.eps_low;
+  f.eps_high = prm.eps_high;
+  f.beta = prm.beta;
+  f.loss_den = prm.loss_denominator;
+  f.msum = w.msum;
+  f.lse_ws = w.lse;
+  f.logp_out = logp_or_null;
+  f.g_ws = w.g;
+  f.block_partials = w.partials;
+  f.counter = w.counter;
+  f.loss_out = loss;
+  f.status = w.status;
+  if (launch_finalize(f, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  return run_backward(hidden, W, ids, dH, L, w, sms, st);
+}
+
+int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_info* info) {
+  if (!info) return GRPO_ERR_INVALID_ARG;
+  int r = check_shape(shape, false);
+  if (r != GRPO_OK) return r;
+  if ((r = check_params(params)) != GRPO_OK) return r;
+  int sms = 0;
+  if ((r = device_setup(&sms)) != GRPO_OK) return r;
+  Layout L, Lmax;
+  if ((r = make_layout(shape, params, sms, &L)) != GRPO_OK) return r;
+  make_layout(shape, params, 0, &Lmax);
+  std::memset(info, 0, sizeof(*info));
+  info->chunk_rows = L.chunk_rows;
+  info->vocab_block = L.vblock;
+  info->n_chunks = static_cast<int32_t>(cdiv(L.n, L.chunk_rows));
+  info->n_vocab_blocks = static_cast<int32_t>(cdiv(L.V, L.vblock));
+  const int n_rb = static_cast<int>(L.nr / BM);
+  const int grp = std::min(kGroupRows, n_rb);
+  info->fwd_splits = std::min(std::max(1, sms / grp), std::min(L.nvt, kMaxSplits));
+  info->launches_logp = L.n > 0 ? 2 : 0;
+  info->launches_loss = L.n > 0 ? 3 + 2 * info->n_chunks * info->n_vocab_blocks : 0;
+  info->workspace_bytes = std::max(L.total, Lmax.total);
+  return GRPO_OK;
+}
+
+int grpo_read_device_status(const void* workspace, int* device_status, void* stream) {
+  if (!workspace || !device_status) return GRPO_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return GRPO_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, static_cast<const uint8_t*>(workspace) + kOffStatus, sizeof(int),
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GRPO_ERR_CUDA;
+  *device_status = v;
+  return GRPO_OK;
+}
+
+const char* grpo_status_string(int s) {
+  switch (s) {
+    case GRPO_OK: return "ok";
+    case GRPO_ERR_INVALID_ARG: return "invalid argument";
+    case GRPO_ERR_MISALIGNED: return "pointer not aligned (hidden/W/dH need 16 bytes, workspace 256)";
+    case GRPO_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (hidden % 8, N % seq_len, or too large)";
+    case GRPO_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case GRPO_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs sm_103 / GB300)";
+    case GRPO_ERR_CUDA: return "CUDA runtime or driver error";
+    case GRPO_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case GRPO_ERR_BAD_TOKEN_ID: return "token id outside [0, vocab) on an unmasked row";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,413 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a with three fused
+// epilogues. One CTA per SM, 192 threads:
+//   warp 0      TMA producer (one elected thread) filling a 4-stage smem ring
+//   warp 1      TMEM allocator + MMA issuer (one elected thread)
+//   warps 2..5  epilogue: 128 threads <-> the 128 TMEM lanes (= tile rows)
+// The fp32 accumulator lives in TMEM, double buffered (2 x 256 columns), so
+// the epilogue of tile j overlaps the MMAs of tile j+1.
+//
+// Tile: 128 rows x 256 columns, K step 64 (one 128-byte swizzle atom of
+// bf16). Modes:
+//   MODE_FWD   S = H W^T over a run of vocab tiles; epilogue keeps an online
+//              max / sum-exp per row (base-2 domain) and picks the target logit.
+//   MODE_BWDG  S = H W^T for one vocab tile; epilogue writes
+//              G = g (onehot(y) - exp(S - lse)) in bf16 to the chunk workspace.
+//   MODE_DH    dH_tile (+)= G W over one vocab block (B operand MN-major);
+//              epilogue accumulates in fp32 and writes bf16 on the last block.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace grpo {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int GEMM_THREADS = 192;
+constexpr int GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment slack
+constexpr int TMEM_COLS = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum GemmMode { MODE_FWD = 0, MODE_BWDG = 1, MODE_DH = 2 };
+
+struct TileArgs {
+  int rows;        // valid A rows in this launch
+  int row0;        // FWD/BWDG: global H row of local row 0; DH: global dH row
+  int n_rb;        // ceil(rows / BM)
+  int k_iters;     // ceil(K / BK)
+  int group_rows;  // row blocks per raster group
+  int n_cols;      // FWD: vocab splits; BWDG: vocab tiles in block; DH: D tiles
+  int n_vtiles;    // FWD: vocab tiles in total
+  int v0;          // BWDG/DH: first vocab column of the block (0 for FWD)
+  int vocab;
+  int hidden;
+  const int32_t* ids;    // indexed by global row
+  const uint8_t* mask;   // FWD: optional; masked rows' ids are never read
+  // MODE_FWD
+  float* part_m;         // [n_cols][part_ld] running max (log2 units)
+  float* part_s;         // [n_cols][part_ld] running sum of 2^(x - max)
+  float* zy;             // [rows] target logit
+  long long part_ld;
+  // MODE_BWDG
+  const float* lse;      // indexed by global row
+  const float* g;        // indexed by global row
+  __nv_bfloat16* G;      // [rows][ldG] chunk workspace
+  long long ldG;
+  // MODE_DH
+  float* acc;            // [rows][hidden] fp32 accumulator
+  __nv_bfloat16* dH;     // [N][hidden] output, indexed by global row
+  int first;
+  int last;
+  int* status;
+};
+
+__device__ __forceinline__ void decode_unit(int u, int n_rb, int n_cols, int R, int& rb,
+                                            int& col) {
+  const int per_group = R * n_cols;
+  const int grp = u / per_group;
+  const int rem = u - grp * per_group;
+  const int rows_in_g = min(R, n_rb - grp * R);
+  col = rem / rows_in_g;
+  rb = grp * R + (rem - col * rows_in_g);
+}
+
+template <int MODE>
+__device__ __forceinline__ void unit_tiles(const TileArgs& a, int col, int& t0, int& t1) {
+  if (MODE == MODE_FWD) {
+    t0 = static_cast<int>((static_cast<long long>(col) * a.n_vtiles) / a.n_cols);
+    t1 = static_cast<int>((static_cast<long long>(col + 1) * a.n_vtiles) / a.n_cols);
+  } else {
+    t0 = col;
+    t1 = col + 1;
+  }
+}
+
+// Blocking wait that ignores the abort flag (used only to drain in-flight
+// async work on the abort path); bounded like every other wait.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitLimitCycles) return;
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                   const __grid_constant__ CUtensorMap map_b, const TileArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t tfull_bar[2];
+  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  // The 128-byte swizzle pattern is a function of address bits [4:9], so each
+  // stage starts on a 1024-byte boundary.
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int* abort_flag = &abort_sh;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], 4);
+    }
+    mbar_init(&drain_bar, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&map_a);
+    tma_prefetch_desc(&map_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_sh;
+
+  const int n_units = args.n_rb * args.n_cols;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      const uint64_t pol_a = policy_evict_last();
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        int rb, col, t0, t1;
+        decode_unit(u, args.n_rb, args.n_cols, args.group_rows, rb, col);
+        unit_tiles<MODE>(args, col, t0, t1);
+        const int a_row = (MODE == MODE_DH ? 0 : args.row0) + rb * BM;
+        for (int t = t0; t < t1 && ok; ++t) {
+          for (int k = 0; k < args.k_iters; ++k, ++it) {
+            const int s = it % STAGES;
+            const uint32_t round = it / STAGES;
+            if (!mbar_wait(&empty_bar[s], (round & 1u) ^ 1u, abort_flag, args.status)) {
+              ok = false;
+              break;
+            }
+            uint8_t* a_dst = smem + s * STAGE_BYTES;
+            uint8_t* b_dst = a_dst + A_BYTES;
+            mbar_arrive_expect_tx(&full_bar[s], STAGE_BYTES);
+            tma_load_2d_hint(a_dst, &map_a, &full_bar[s], k * BK, a_row, pol_a);
+            if (MODE == MODE_DH) {
+              // W[v0 + k*64 .. +64, d0 .. d0+256) as four 64x64 MN-major boxes.
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                tma_load_2d(b_dst + j * (BK * 64 * 2), &map_b, &full_bar[s],
+                            t * BN + j * 64, args.v0 + k * BK);
+            } else {
+              tma_load_2d(b_dst, &map_b, &full_bar[s], k * BK, args.v0 + t * BN);
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // Abort path: let the copies already issued land before the CTA exits.
+        for (uint32_t j = (it >= STAGES ? it - STAGES : 0); j < it; ++j)
+          drain_wait(&full_bar[j % STAGES], (j / STAGES) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BM, BN, false, MODE == MODE_DH);
+      uint32_t it = 0, tile_it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        int rb, col, t0, t1;
+        decode_unit(u, args.n_rb, args.n_cols, args.group_rows, rb, col);
+        unit_tiles<MODE>(args, col, t0, t1);
+        for (int t = t0; t < t1 && ok; ++t, ++tile_it) {
+          const uint32_t buf = tile_it & 1u;
+          const uint32_t use = tile_it >> 1;
+          if (!mbar_wait(&tempty_bar[buf], (use & 1u) ^ 1u, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + buf * BN;
+          for (int k = 0; k < args.k_iters; ++k, ++it) {
+            const int s = it % STAGES;
+            const uint32_t round = it / STAGES;
+            if (!mbar_wait(&full_bar[s], round & 1u, abort_flag, args.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(smem + s * STAGE_BYTES);
+            const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              // K-major, 128B swizzle: K advances by 32 bytes inside the atom;
+              // 8-row groups are 1024 bytes apart.
+              const uint64_t adesc = sdesc_sw128(a_addr + kk * 32, 16, 1024);
+              uint64_t bdesc;
+              if (MODE == MODE_DH) {
+                // MN-major, 128B swizzle: 64-wide N blocks 8 KB apart (LBO),
+                // 8-deep K groups 1 KB apart (SBO); K advances 16 rows.
+                bdesc = sdesc_sw128(b_addr + kk * 2048, BK * 64 * 2, 1024);
+              } else {
+                bdesc = sdesc_sw128(b_addr + kk * 32, 16, 1024);
+              }
+              tc_mma_bf16(d_tmem, adesc, bdesc, idesc, (k | kk) != 0 ? 1u : 0u);
+            }
+            tc_commit(&empty_bar[s]);
+          }
+          if (!ok) break;
+          tc_commit(&tfull_bar[buf]);
+        }
+      }
+      // Make sure every MMA issued by this thread has finished before TMEM is
+      // released (matters only on the abort path).
+      tc_commit(&drain_bar);
+      drain_wait(&drain_bar, 0);
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue --
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int lrow_in_tile = q * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t tile_it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      int rb, col, t0, t1;
+      decode_unit(u, args.n_rb, args.n_cols, args.group_rows, rb, col);
+      unit_tiles<MODE>(args, col, t0, t1);
+      const int lrow = rb * BM + lrow_in_tile;
+      const bool valid = lrow < args.rows;
+      const int grow = args.row0 + lrow;
+
+      // Per-row state.
+      float m2 = -INFINITY, ssum = 0.f;  // FWD
+      int y = -1;
+      float lse2 = 0.f, gval = 0.f;      // BWDG
+      if (MODE == MODE_FWD) {
+        if (valid && (args.mask == nullptr || args.mask[grow] != 0)) y = args.ids[grow];
+      } else if (MODE == MODE_BWDG) {
+        if (valid) {
+          gval = args.g[grow];
+          lse2 = args.lse[grow] * kLog2e;
+          if (gval != 0.f) y = args.ids[grow];
+        }
+      }
+
+      for (int t = t0; t < t1; ++t, ++tile_it) {
+        const uint32_t buf = tile_it & 1u;
+        const uint32_t use = tile_it >> 1;
+        if (!mbar_wait(&tfull_bar[buf], use & 1u, abort_flag, args.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + lane_addr + buf * BN;
+
+        if (MODE == MODE_FWD) {
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            const int col0 = t * BN + c * 32;
+            if (col0 >= args.vocab) break;  // warp-uniform
+            float v[32];
+            tmem_ld32(tbase + c * 32, v);
+            if (col0 + 32 > args.vocab) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (col0 + j >= args.vocab) v[j] = -INFINITY;
+            }
+            const unsigned off = static_cast<unsigned>(y - col0);
+            if (off < 32u) {
+              float z = 0.f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (static_cast<unsigned>(j) == off) z = v[j];
+              args.zy[lrow] = z;
+            }
+            float mx0 = fmaxf(v[0], v[1]), mx1 = fmaxf(v[2], v[3]);
+#pragma unroll
+            for (int j = 4; j < 32; j += 4) {
+              mx0 = fmaxf(mx0, fmaxf(v[j], v[j + 1]));
+              mx1 = fmaxf(mx1, fmaxf(v[j + 2], v[j + 3]));
+            }
+            const float mn = fmaxf(m2, fmaxf(mx0, mx1) * kLog2e);
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              s0 += ex2(fmaf(v[j], kLog2e, -mn));
+              s1 += ex2(fmaf(v[j + 1], kLog2e, -mn));
+              s2 += ex2(fmaf(v[j + 2], kLog2e, -mn));
+              s3 += ex2(fmaf(v[j + 3], kLog2e, -mn));
+            }
+            ssum = fmaf(ssum, ex2(m2 - mn), (s0 + s1) + (s2 + s3));
+            m2 = mn;
+          }
+        } else if (MODE == MODE_BWDG) {
+          __nv_bfloat16* grow_ptr = args.G + static_cast<long long>(lrow) * args.ldG + t * BN;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            const int col0 = args.v0 + t * BN + c * 32;  // global vocab index
+            float v[32];
+            tmem_ld32(tbase + c * 32, v);
+            const float ng = -gval;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = ng * ex2(fmaf(v[j], kLog2e, -lse2));
+            const unsigned off = static_cast<unsigned>(y - col0);
+            if (off < 32u) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (static_cast<unsigned>(j) == off) v[j] += gval;
+            }
+            if (col0 + 32 > args.vocab) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (col0 + j >= args.vocab) v[j] = 0.f;
+            }
+            if (valid) {
+              uint32_t p[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) p[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+              __nv_bfloat16* dst = grow_ptr + c * 32;
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                st_global_v4(dst + j * 8, p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+            }
+          }
+        } else {  // MODE_DH
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            const int d0 = t * BN + c * 32;
+            if (d0 >= args.hidden) break;  // warp-uniform
+            float v[32];
+            tmem_ld32(tbase + c * 32, v);
+            if (valid) {
+              float* accp = args.acc + static_cast<long long>(lrow) * args.hidden + d0;
+              __nv_bfloat16* outp =
+                  args.dH + static_cast<long long>(grow) * args.hidden + d0;
+#pragma unroll
+              for (int j8 = 0; j8 < 4; ++j8) {
+                if (d0 + j8 * 8 >= args.hidden) break;
+                float* a8 = accp + j8 * 8;
+                if (!args.first) {
+                  const float4 x0 = *reinterpret_cast<const float4*>(a8);
+                  const float4 x1 = *reinterpret_cast<const float4*>(a8 + 4);
+                  v[j8 * 8 + 0] += x0.x;
+                  v[j8 * 8 + 1] += x0.y;
+                  v[j8 * 8 + 2] += x0.z;
+                  v[j8 * 8 + 3] += x0.w;
+                  v[j8 * 8 + 4] += x1.x;
+                  v[j8 * 8 + 5] += x1.y;
+                  v[j8 * 8 + 6] += x1.z;
+                  v[j8 * 8 + 7] += x1.w;
+                }
+                if (args.last) {
+                  st_global_v4(outp + j8 * 8, pack_bf16x2(v[j8 * 8 + 0], v[j8 * 8 + 1]),
+                               pack_bf16x2(v[j8 * 8 + 2], v[j8 * 8 + 3]),
+                               pack_bf16x2(v[j8 * 8 + 4], v[j8 * 8 + 5]),
+                               pack_bf16x2(v[j8 * 8 + 6], v[j8 * 8 + 7]));
+                } else {
+                  *reinterpret_cast<float4*>(a8) =
+                      make_float4(v[j8 * 8 + 0], v[j8 * 8 + 1], v[j8 * 8 + 2], v[j8 * 8 + 3]);
+                  *reinterpret_cast<float4*>(a8 + 4) =
+                      make_float4(v[j8 * 8 + 4], v[j8 * 8 + 5], v[j8 * 8 + 6], v[j8 * 8 + 7]);
+                }
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+      }
+      if (MODE == MODE_FWD && ok && valid) {
+        args.part_m[static_cast<long long>(col) * args.part_ld + lrow] = m2;
+        args.part_s[static_cast<long long>(col) * args.part_ld + lrow] = ssum;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+}  // namespace grpo

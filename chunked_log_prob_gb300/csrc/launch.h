@@ -1,0 +1,54 @@
+// Internal launch interface between the host ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gemm_tc.cuh"
+
+namespace grpo {
+
+struct FinalizeArgs {
+  long long n;           // rows
+  int splits;            // vocab splits of the forward pass
+  long long part_ld;     // leading dimension of the split partials
+  int vocab;
+  int seq_len;
+  int loss_mode;         // 0: logp only; 1: logp + GRPO loss + g
+  const float* part_m;
+  const float* part_s;
+  const float* zy;
+  const int32_t* ids;
+  const uint8_t* mask;   // may be null (every row counts)
+  const float* old_logp;
+  const float* ref_logp;
+  const float* adv;
+  float eps_low, eps_high, beta, loss_den;
+  const double* msum;    // device sum of the mask
+  float* lse_ws;         // [n]
+  float* lse_out;        // optional
+  float* logp_out;       // optional
+  float* g_ws;           // [n] (loss mode)
+  double* block_partials;
+  unsigned* counter;
+  float* loss_out;
+  int* status;
+};
+
+constexpr int kFinalizeThreads = 256;
+constexpr int kMaxFinalizeBlocks = 1024;
+
+// Each launcher lives in the translation unit that instantiates its kernel.
+cudaError_t prepare_fwd_gemm();   // opt-in to the large dynamic smem
+cudaError_t prepare_bwd_gemms();
+cudaError_t launch_fwd_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
+                            const TileArgs& args, int grid, cudaStream_t stream);
+cudaError_t launch_bwdg_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
+                             const TileArgs& args, int grid, cudaStream_t stream);
+cudaError_t launch_dh_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
+                           const TileArgs& args, int grid, cudaStream_t stream);
+cudaError_t launch_count_mask(const uint8_t* mask, long long n, double* out,
+                              cudaStream_t stream);
+cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t stream);
+
+}  // namespace grpo

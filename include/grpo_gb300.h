@@ -1,0 +1,151 @@
+/*
+ * grpo_gb300.h - C ABI of the GB300 (sm_103a) selective log-prob / GRPO loss
+ * library.
+ *
+ * What it computes (the web pages this library restates are cited by title
+ * and section):
+ *
+ *   logp_t = h_t . W[y_t] - logsumexp_v(h_t . W_v)
+ *
+ * straight from the final hidden states h [N, D] and the lm_head weight
+ * W [V, D], without ever holding the N x V logits ("GRPO with 7x longer
+ * context", Unsloth docs, section "Flattened sequence length chunking" and
+ * its chunked_hidden_states_selective_log_softmax call). On top of it, the
+ * masked token-mean GRPO loss with a clipped importance ratio against the
+ * old policy and a beta-weighted k3 reverse-KL term against the reference
+ * policy ("Unsloth internals", section "The relationship to TRL"; "Train
+ * reasoning models with 5GB VRAM", section "Under the Hood"), and its
+ * gradient to the hidden states, obtained by recomputing the logit tiles
+ * (same Unsloth docs page, section "Offloading activations for log-softmax").
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor arguments are DEVICE pointers on the current CUDA device,
+ *     row-major and densely packed, 16-byte aligned:
+ *       hidden  bf16  [N, D]       W     bf16 [V, D]
+ *       ids     int32 [N]          mask  uint8 [N] (nonzero = token counts)
+ *       old_logp, ref_logp fp32 [N]
+ *       adv     fp32  [N / T]      (advantage of completion b = t / T)
+ *   - The caller owns every buffer, including the workspace; the library
+ *     allocates no device memory. Calls are asynchronous on `stream`
+ *     (a cudaStream_t; NULL = the legacy default stream).
+ *   - Return value: GRPO_OK (0) or a negative grpo_status. Argument checks
+ *     happen on the host before anything is launched; problems found on the
+ *     device (out-of-range token ids, a timed-out wait) are recorded in the
+ *     workspace's status word, read back with grpo_read_device_status.
+ *   - Two calls that share a workspace must not overlap on the GPU.
+ *   - Requires an sm_103 device (GB300).
+ */
+#ifndef GRPO_GB300_H_
+#define GRPO_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum grpo_status {
+  GRPO_OK = 0,
+  GRPO_ERR_INVALID_ARG = -1,       /* null pointer, negative size, bad param  */
+  GRPO_ERR_MISALIGNED = -2,        /* a pointer is not 16-byte aligned        */
+  GRPO_ERR_UNSUPPORTED_SHAPE = -3, /* D % 8 != 0, N % T != 0, size too large  */
+  GRPO_ERR_WORKSPACE_TOO_SMALL = -4,
+  GRPO_ERR_UNSUPPORTED_DEVICE = -5, /* not an sm_103 GPU                      */
+  GRPO_ERR_CUDA = -6,               /* a CUDA runtime/driver call failed      */
+  GRPO_ERR_DEVICE_TIMEOUT = -7,     /* (device) a bounded wait ran out        */
+  GRPO_ERR_BAD_TOKEN_ID = -8        /* (device) unmasked id outside [0, V)   */
+} grpo_status;
+
+typedef struct grpo_shape {
+  int64_t n_tokens; /* N = B * T flattened tokens (rows of hidden)           */
+  int32_t seq_len;  /* T: tokens per completion; row t is completion t / T    */
+  int32_t hidden;   /* D: hidden size, a multiple of 8                        */
+  int32_t vocab;    /* V: vocabulary size (rows of W)                         */
+  int32_t reserved; /* must be 0                                              */
+} grpo_shape;
+
+typedef struct grpo_params {
+  float eps_low;          /* ratio clip: lower bound 1 - eps_low (0.2)         */
+  float eps_high;         /* ratio clip: upper bound 1 + eps_high (0.2)        */
+  float beta;             /* weight of the k3 KL term (0.001)                  */
+  float loss_denominator; /* <= 0: divide by sum(mask); > 0: divide by this    */
+  int32_t chunk_tokens;   /* rows per backward chunk; 0 = automatic            */
+  int32_t vocab_block;    /* vocab columns per backward block; 0 = automatic   */
+  uint32_t flags;         /* must be 0                                         */
+  uint32_t reserved;      /* must be 0                                         */
+} grpo_params;
+
+/* Defaults: eps 0.2/0.2, beta 0.001 (the pages' corrected GRPO default,
+ * "How does Unsloth implement GRPO", section "Corrected hyperparameters"),
+ * token-mean denominator, automatic chunking. Host only. */
+void grpo_default_params(grpo_params* params);
+
+/* Bytes of device workspace that grpo_logp_fwd and grpo_loss_fwd_bwd need for
+ * this shape and these params. Host only, touches no GPU. The size grows with
+ * N (a few fp32 per token) and with chunk_tokens x vocab_block, never with
+ * N x V. Returns GRPO_OK or GRPO_ERR_INVALID_ARG / _UNSUPPORTED_SHAPE. */
+int grpo_workspace_size(const grpo_shape* shape, const grpo_params* params, size_t* bytes);
+
+/* Selective log-softmax ("GRPO with 7x longer context", section "Flattened
+ * sequence length chunking"):
+ *   logp[t] = h_t . W[ids[t]] - lse[t],  lse[t] = logsumexp_v h_t . W_v,
+ * for every t in [0, N). logits are accumulated and reduced in fp32.
+ *   logp:        fp32 [N] output (required)
+ *   lse_or_null: fp32 [N] output, or NULL
+ * params: only chunk/vocab fields are read (may be NULL for defaults).
+ * ids outside [0, V) give logp = NaN and GRPO_ERR_BAD_TOKEN_ID in the device
+ * status word. */
+int grpo_logp_fwd(const void* hidden, const void* W, const int32_t* ids, float* logp,
+                  float* lse_or_null, const grpo_shape* shape, const grpo_params* params,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Fused GRPO loss forward + backward to the hidden states.
+ *   r_t   = exp(logp_t - old_logp_t)
+ *   surr  = min(r_t A_b, clamp(r_t, 1 - eps_low, 1 + eps_high) A_b)
+ *   kl_t  = exp(ref_t - logp_t) - (ref_t - logp_t) - 1
+ *   l_t   = -surr + beta kl_t
+ *   loss  = sum_t mask_t l_t / M,  M = sum_t mask_t (or loss_denominator > 0)
+ *   dH_t  = dloss/dh_t = g_t (W[y_t] - sum_v softmax(h_t W^T)_v W_v),
+ *           g_t = dloss/dlogp_t
+ * ("Unsloth internals", section "The relationship to TRL"; "Train reasoning
+ * models with 5GB VRAM", section "Under the Hood"; "GRPO with 7x longer
+ * context", section "Offloading activations for log-softmax").
+ *   loss:         fp32 [1] device scalar output (sum accumulated in fp64)
+ *   logp_or_null: fp32 [N] output (0 on masked rows), or NULL
+ *   dH:           bf16 [N, D] output; masked rows are exactly 0
+ * M = 0 gives loss = 0 and dH = 0. Ids of masked rows are never read. */
+int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
+                      const uint8_t* mask, const float* old_logp, const float* ref_logp,
+                      const float* adv, float* loss, float* logp_or_null, void* dH,
+                      const grpo_shape* shape, const grpo_params* params, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* How a call with this shape and these params is carried out on the current
+ * device (host only; reads the device's SM count, launches nothing). */
+typedef struct grpo_plan_info {
+  int32_t chunk_rows;        /* rows per backward chunk                      */
+  int32_t vocab_block;       /* vocab columns per backward block             */
+  int32_t n_chunks;          /* backward chunks                              */
+  int32_t n_vocab_blocks;    /* backward vocab blocks per chunk              */
+  int32_t fwd_splits;        /* forward vocab splits (partials per row)      */
+  int32_t launches_logp;     /* kernel launches of one grpo_logp_fwd call    */
+  int32_t launches_loss;     /* kernel launches of one grpo_loss_fwd_bwd     */
+  int32_t reserved;
+  uint64_t workspace_bytes;  /* same as grpo_workspace_size                  */
+} grpo_plan_info;
+
+int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_info* info);
+
+/* Synchronises `stream`, then copies the device status word of the last call
+ * that used `workspace` into *device_status (GRPO_OK or a negative code). */
+int grpo_read_device_status(const void* workspace, int* device_status, void* stream);
+
+/* Static text for a status code. */
+const char* grpo_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GRPO_GB300_H_ */

@@ -1,0 +1,126 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and the host-only calls (workspace sizing, status strings,
+argument checks that fail before any GPU work) behave. No compute call runs.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def clp():
+    __graft_entry__.build()
+    import chunked_log_prob_gb300 as m
+
+    return m
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "grpo_gb300.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(grpo_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(clp):
+    declared = _declared_functions()
+    assert declared == sorted(clp.EXPORTED)
+    lib = ctypes.CDLL(clp._binding.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_library_is_loaded_in_process(clp):
+    maps = open("/proc/self/maps").read()
+    assert "libgrpo_gb300.so" in maps
+
+
+def test_status_strings(clp):
+    for code in range(0, -9, -1):
+        assert clp.status_string(code) != "unknown status"
+    assert clp.status_string(-99) == "unknown status"
+
+
+def test_default_params(clp):
+    p = clp.make_params()
+    assert abs(p.eps_low - 0.2) < 1e-7 and abs(p.eps_high - 0.2) < 1e-7
+    assert abs(p.beta - 0.001) < 1e-9 and p.flags == 0
+
+
+def test_workspace_independent_of_vocab_times_tokens(clp):
+    # Grows with N (a few fp32 per row) and with chunk x vocab block, never N x V.
+    p = clp.make_params(chunk_tokens=1024, vocab_block=8192)
+    sizes = [clp.grpo_workspace_size(n, 4096, 128256, 1, p) for n in (4096, 16384, 65536)]
+    per_row = (sizes[2] - sizes[1]) / (65536 - 16384)
+    assert per_row < 64 * 4 * 2 + 64  # split partials + a few fp32 per row
+    fixed = 1024 * 8192 * 2 + 1024 * 4096 * 4
+    assert sizes[0] < fixed + 4096 * 300 + 65536
+    assert sizes[2] < 65536 * 128256 * 4 / 100  # far below the N x V fp32 logits
+
+
+def test_workspace_grows_with_chunk(clp):
+    a = clp.grpo_workspace_size(16384, 4096, 128256, 1, clp.make_params(chunk_tokens=1024))
+    b = clp.grpo_workspace_size(16384, 4096, 128256, 1, clp.make_params(chunk_tokens=4096))
+    assert b > a
+
+
+def test_single_vocab_block_needs_no_accumulator(clp):
+    big = clp.grpo_workspace_size(1024, 4096, 4096, 1, clp.make_params(chunk_tokens=1024,
+                                                                       vocab_block=4096))
+    small = clp.grpo_workspace_size(1024, 4096, 4096, 1, clp.make_params(chunk_tokens=1024,
+                                                                         vocab_block=2048))
+    assert small - big > 1024 * 4096 * 4 - 1024 * 2048 * 2 - 4096
+
+
+@pytest.mark.parametrize("n,d,v,want", [
+    (100, 12, 50, -3),   # hidden % 8 != 0
+    (-1, 16, 50, -1),    # negative N
+    (10, 16, 0, -1),     # empty vocabulary
+])
+def test_workspace_size_rejects_bad_shapes(clp, n, d, v, want):
+    with pytest.raises(clp.GrpoError) as e:
+        clp.grpo_workspace_size(n, d, v)
+    assert e.value.code == want
+
+
+def test_bad_params_rejected(clp):
+    p = clp.make_params()
+    p.flags = 1
+    with pytest.raises(clp.GrpoError) as e:
+        clp.grpo_workspace_size(10, 16, 50, 1, p)
+    assert e.value.code == -1
+
+
+def test_null_pointers_rejected_before_launch(clp):
+    shape = clp.make_shape(10, 5, 16, 50)
+    rc = clp.lib.grpo_loss_fwd_bwd(None, None, None, None, None, None, None, None, None, None,
+                                   ctypes.byref(shape), None, None, 0, None)
+    assert rc == -1
+    rc = clp.lib.grpo_logp_fwd(None, None, None, None, None, ctypes.byref(shape), None, None, 0,
+                               None)
+    assert rc == -1
+
+
+def test_sequence_length_must_divide_tokens(clp):
+    shape = clp.make_shape(10, 3, 16, 50)
+    buf = ctypes.create_string_buffer(4096)
+    addr = (ctypes.addressof(buf) + 255) // 256 * 256
+    rc = clp.lib.grpo_loss_fwd_bwd(addr, addr, addr, addr, addr, addr, addr, addr, None, addr,
+                                   ctypes.byref(shape), None, addr, 1024, None)
+    assert rc == -3
+
+
+def test_misaligned_pointers_rejected(clp):
+    shape = clp.make_shape(8, 8, 16, 50)
+    buf = ctypes.create_string_buffer(8192)
+    a = (ctypes.addressof(buf) + 255) // 256 * 256
+    rc = clp.lib.grpo_logp_fwd(a + 8, a, a, a, None, ctypes.byref(shape), None, a, 4096, None)
+    assert rc == -2
+    rc = clp.lib.grpo_logp_fwd(a, a, a, a, None, ctypes.byref(shape), None, a + 16, 4096, None)
+    assert rc == -2

@@ -1,0 +1,214 @@
+"""GPU parity: the CUDA library (called through the C ABI) against the fp64
+oracle on identical seeded bf16 inputs.
+
+Gates: |d logp| <= 1e-2 absolute, relative loss error <= 1e-3, relative
+Frobenius error of dH over unmasked rows <= 2e-2. Masked rows: logp = 0 and
+dH exactly 0.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+LOGP_TOL = 1e-2
+LOSS_RTOL = 1e-3
+DH_RTOL = 2e-2
+
+
+@pytest.fixture(scope="module")
+def clp():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import chunked_log_prob_gb300 as m
+
+    return m
+
+
+DEV = "cuda:0"
+
+
+def _to(t):
+    return t.to(DEV) if t is not None else None
+
+
+def gpu_loss(clp, p, old, ref, params=None, mask=None, ids=None, hidden=None, weight=None):
+    mask = p.mask if mask is None else mask
+    ids = p.ids if ids is None else ids
+    hidden = p.hidden if hidden is None else hidden
+    weight = p.weight if weight is None else weight
+    ws = clp.alloc_workspace(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, params, DEV)
+    loss, logp, dH = clp.grpo_loss_fwd_bwd(
+        _to(hidden), _to(weight), _to(ids), _to(mask), _to(old), _to(ref), _to(p.adv),
+        p.seq_len, params=params, workspace=ws)
+    st = clp.grpo_read_device_status(ws)
+    return (loss.item(), logp.cpu().double().numpy(), dH.cpu().double().numpy(), st)
+
+
+def oracle_case(p, mask=None, base=None, eps=None, beta=None):
+    mask = p.mask if mask is None else mask
+    if base is None:
+        base, _ = oracle.selective_logp(p.hidden, p.weight, p.ids.numpy())
+    old, ref = p.old_ref(torch.from_numpy(np.asarray(base)))
+    want = oracle.loss_fwd_bwd(p.hidden, p.weight, p.ids.numpy(), mask.numpy(), old, ref, p.adv,
+                               p.seq_len, p.eps_low if eps is None else eps,
+                               p.eps_high if eps is None else eps,
+                               p.beta if beta is None else beta)
+    return old, ref, want
+
+
+def check(got, want, mask, tag=""):
+    L, logp, dH, st = got
+    m = mask.numpy().astype(bool)
+    assert st == 0, f"{tag} device status {st}"
+    dl = np.abs(logp - want["logp"])
+    rel_loss = abs(L - want["L"]) / max(abs(want["L"]), 1e-30)
+    num = np.linalg.norm(dH[m] - want["dH"][m])
+    den = np.linalg.norm(want["dH"][m])
+    rel_dh = num / den if den > 0 else num
+    print(f"{tag}: max|dlogp|={dl.max():.3e} rms={np.sqrt((dl ** 2).mean()):.3e} "
+          f"rel_loss={rel_loss:.3e} (L={want['L']:.6e}) rel_dH={rel_dh:.3e}")
+    assert dl.max() <= LOGP_TOL
+    assert rel_loss <= LOSS_RTOL
+    assert rel_dh <= DH_RTOL
+    assert np.all(logp[~m] == 0.0)
+    assert np.all(dH[~m] == 0.0)
+
+
+def test_logp_fwd_tiny(clp):
+    p = synth.make_problem("tiny", seed=0)
+    logp, lse = clp.grpo_logp_fwd(_to(p.hidden), _to(p.weight), _to(p.ids), want_lse=True)
+    want, want_lse = oracle.selective_logp(p.hidden, p.weight, p.ids.numpy())
+    d = np.abs(logp.cpu().double().numpy() - want)
+    dl = np.abs(lse.cpu().double().numpy() - want_lse)
+    print(f"logp tiny: max={d.max():.3e} rms={np.sqrt((d ** 2).mean()):.3e} lse max={dl.max():.3e}")
+    assert d.max() <= LOGP_TOL and dl.max() <= LOGP_TOL
+
+
+def test_loss_fwd_bwd_tiny(clp):
+    p = synth.make_problem("tiny", seed=0)
+    old, ref, want = oracle_case(p)
+    check(gpu_loss(clp, p, old, ref), want, p.mask, "tiny")
+
+
+# N, T, D, V, chunk_tokens, vocab_block, padded
+RAGGED = [
+    (300, 75, 200, 1000, 128, 512, True),     # tails in every dim; 3 chunks x 2 vocab blocks
+    (129, 129, 64, 257, 0, 0, False),         # one row past a tile, one column past a tile
+    (1000, 250, 136, 3000, 256, 1024, True),  # D not a multiple of 64
+    (256, 64, 2880, 2000, 0, 0, True),        # gpt-oss hidden size
+    (512, 128, 1536, 5000, 0, 768, True),     # Qwen2.5-1.5B hidden size, 7 vocab blocks
+    (640, 640, 4096, 777, 0, 0, False),       # Llama hidden size, vocab < 1K
+]
+
+
+@pytest.mark.parametrize("N,T,D,V,chunk,vblock,padded", RAGGED)
+def test_ragged_shapes(clp, N, T, D, V, chunk, vblock, padded):
+    G = 4 if (N // T) % 4 == 0 else 1
+    p = synth.make_problem("tiny", seed=N + D + V, prompts=(N // T) // G, G=G, T=T, D=D, V=V,
+                           lengths=(max(1, T // 3), T) if padded else None)
+    old, ref, want = oracle_case(p)
+    params = clp.make_params(chunk_tokens=chunk, vocab_block=vblock)
+    check(gpu_loss(clp, p, old, ref, params), want, p.mask, f"ragged {N}x{D}x{V}")
+
+
+def test_logp_fwd_ragged(clp):
+    p = synth.make_problem("tiny", seed=3, T=75, prompts=1, G=4, D=200, V=1000)
+    logp, _ = clp.grpo_logp_fwd(_to(p.hidden), _to(p.weight), _to(p.ids))
+    want, _ = oracle.selective_logp(p.hidden, p.weight, p.ids.numpy())
+    assert np.abs(logp.cpu().double().numpy() - want).max() <= LOGP_TOL
+
+
+def test_chunking_does_not_change_results(clp):
+    # "No loss of accuracy" from chunking: the forward never depends on the
+    # backward chunking; dH rows depend on the chunk size not at all, and on
+    # the vocab block only through fp32 accumulation order.
+    p = synth.make_problem("tiny", seed=11, T=128, prompts=1, G=4, D=256, V=3000,
+                           lengths=(40, 128))
+    old, ref, _ = oracle_case(p)
+    runs = {}
+    for chunk, vb in ((128, 0), (256, 0), (512, 0), (0, 256), (0, 1024), (128, 512)):
+        runs[(chunk, vb)] = gpu_loss(clp, p, old, ref, clp.make_params(chunk_tokens=chunk,
+                                                                      vocab_block=vb))
+    L0, lp0, dH0, _ = runs[(128, 0)]
+    for key, (L, lp, dH, st) in runs.items():
+        assert st == 0
+        assert L == L0 and np.array_equal(lp, lp0), key
+        if key[1] == 0:
+            assert np.array_equal(dH, dH0), key
+        else:
+            assert np.linalg.norm(dH - dH0) <= 1e-2 * np.linalg.norm(dH0), key
+
+
+def test_all_masked_gives_zero(clp):
+    p = synth.make_problem("tiny", seed=4)
+    mask = torch.zeros_like(p.mask)
+    old = torch.zeros(p.n_tokens)
+    L, logp, dH, st = gpu_loss(clp, p, old, old, mask=mask)
+    assert st == 0 and L == 0.0
+    assert np.all(logp == 0) and np.all(dH == 0)
+
+
+def test_masked_ids_are_never_read(clp):
+    p = synth.make_problem("tiny", seed=5, lengths=(10, 64))
+    ids = p.ids.clone()
+    ids[p.mask == 0] = -12345  # would be out of range if read
+    old, ref, want = oracle_case(p)
+    check(gpu_loss(clp, p, old, ref, ids=ids), want, p.mask, "masked ids")
+
+
+def test_bad_token_id_sets_status(clp):
+    p = synth.make_problem("tiny", seed=6)
+    ids = p.ids.clone()
+    ids[7] = p.vocab  # unmasked and out of range
+    old = torch.full((p.n_tokens,), -8.0)
+    L, logp, dH, st = gpu_loss(clp, p, old, old, ids=ids)
+    assert st == clp.STATUS_BAD_TOKEN_ID if hasattr(clp, "STATUS_BAD_TOKEN_ID") else st == -8
+    assert math.isnan(logp[7]) and math.isnan(L)
+
+
+def test_zero_weight_gives_uniform(clp):
+    p = synth.make_problem("tiny", seed=7)
+    W = torch.zeros_like(p.weight)
+    logp, lse = clp.grpo_logp_fwd(_to(p.hidden), _to(W), _to(p.ids), want_lse=True)
+    assert np.abs(logp.cpu().double().numpy() + math.log(p.vocab)).max() < 1e-5
+    old = torch.full((p.n_tokens,), -math.log(p.vocab)) + 0.01
+    L, lp, dH, st = gpu_loss(clp, p, old, old, weight=W)
+    assert st == 0 and np.all(dH == 0)
+
+
+def test_on_policy_identity(clp):
+    # old = ref = logp: ratio 1 and zero KL, so loss = -mean masked advantage.
+    p = synth.make_problem("tiny", seed=8, lengths=(20, 64))
+    base, _ = oracle.selective_logp(p.hidden, p.weight, p.ids.numpy())
+    lp = torch.from_numpy(base).float()
+    L, _, _, st = gpu_loss(clp, p, lp, lp)
+    A = p.adv.double().numpy()[np.arange(p.n_tokens) // p.seq_len]
+    m = p.mask.double().numpy()
+    want = -(A * m).sum() / m.sum()
+    assert st == 0 and abs(L - want) <= 1e-4 * max(1.0, abs(want))
+
+
+def test_vocab_of_one(clp):
+    p = synth.make_problem("tiny", seed=9, V=1)
+    p.ids.zero_()
+    logp, _ = clp.grpo_logp_fwd(_to(p.hidden), _to(p.weight), _to(p.ids))
+    assert np.abs(logp.cpu().numpy()).max() < 1e-6
+
+
+def test_empty_batch(clp):
+    h = torch.empty(0, 64, dtype=torch.bfloat16, device=DEV)
+    W = torch.randn(100, 64, device=DEV).to(torch.bfloat16)
+    e = torch.empty(0, dtype=torch.int32, device=DEV)
+    f = torch.empty(0, dtype=torch.float32, device=DEV)
+    loss, logp, dH = clp.grpo_loss_fwd_bwd(h, W, e, torch.empty(0, dtype=torch.uint8, device=DEV),
+                                           f, f, torch.empty(0, dtype=torch.float32, device=DEV),
+                                           1)
+    assert loss.item() == 0.0 and dH.numel() == 0
