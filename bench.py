@@ -1,0 +1,413 @@
+#!/usr/bin/env python
+"""Benchmark of the fused GRPO selective-log-prob loss forward + backward.
+
+One step = one grpo_loss_fwd_bwd call over one synthetic batch: the logit GEMM
+with online log-sum-exp over the whole vocabulary, the loss / dlogp epilogue,
+and the chunked backward (recomputed logit tiles -> G -> dH). Default workload:
+the Llama-3.1-8B lm_head shape (N = 1 x 4 x 4096 tokens, D = 4096,
+V = 128256, bf16), inputs resident in HBM and larger than L2 (W is 1.05 GB,
+hidden 134 MB), so no L2 flush is needed between steps.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Prints one JSON line (rank 0). Under torchrun each rank runs its own
+independent batch (weak scaling, no collective on the data path); the time is
+the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s & % bf16 tensor peak, GRPO logp+loss fwd+bwd (Llama-3.1-8B shape)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama-3.1-8b")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--chunk-tokens", type=int, default=0)
+    ap.add_argument("--vocab-block", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- helpers ----
+
+def flops_per_token(D, V):
+    # 2DV forward + 4DV backward (recomputed logits + G W), per valid token.
+    return 6.0 * D * V
+
+
+def oracle_rows_per_second(p, target_s, seed, cores_note):
+    """Time the fp64 oracle on a seeded sample of valid rows of workload `p`."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    rng = np.random.default_rng(seed)
+    valid = torch.nonzero(p.mask.cpu() != 0).flatten().numpy()
+    W64 = p.weight.float().cpu().numpy().astype(np.float64)  # input preparation
+    h = p.hidden.cpu()
+    ids = p.ids.cpu().numpy()
+    base = torch.full((p.n_tokens,), -math.log(p.vocab))
+    old, ref = (x.cpu() for x in p.old_ref(base.to(p.old_noise.device)))
+    adv = p.adv.cpu()
+    M = float(len(valid))
+
+    def run(n_rows):
+        rows = np.sort(rng.choice(valid, size=min(n_rows, len(valid)), replace=False))
+        t0 = time.perf_counter()
+        oracle.rows_fwd_bwd(h, W64, ids, rows, old, ref, adv, p.seq_len, M,
+                            p.eps_low, p.eps_high, p.beta)
+        return len(rows), time.perf_counter() - t0
+
+    n0, t0 = run(8)
+    per_row = t0 / n0
+    n_rows = int(max(8, min(len(valid), target_s / max(per_row, 1e-6))))
+    n, t = run(n_rows)
+    return n, t
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- ours ----
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import chunked_log_prob_gb300 as clp
+    import synth
+
+    p = synth.make_problem(args.workload, seed=args.seed + rank, device=dev)
+    N, D, V, T = p.n_tokens, p.hidden_size, p.vocab, p.seq_len
+    params = clp.make_params(p.eps_low, p.eps_high, p.beta, 0.0, args.chunk_tokens,
+                             args.vocab_block)
+    plan = clp.grpo_get_plan(N, D, V, T, params)
+    ws = clp.alloc_workspace(N, D, V, T, params, dev)
+    # old/ref: the policy's own log-probs (as a GRPO trainer gets them) + noise.
+    base, _ = clp.grpo_logp_fwd(p.hidden, p.weight, p.ids, workspace=ws)
+    old, ref = p.old_ref(base)
+    valid = p.n_valid
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    logp = torch.empty(N, dtype=torch.float32, device=dev)
+    dH = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
+
+    def step():
+        clp.grpo_loss_fwd_bwd(p.hidden, p.weight, p.ids, p.mask, old, ref, p.adv, T,
+                              params=params, workspace=ws, loss=loss, logp=logp, dH=dH)
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    status = clp.grpo_read_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status} ({clp.status_string(status)})")
+
+    gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    gpu_id = f"GPU-{gpu_id}" if gpu_id is not None else str(local)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(gpu_id) as clocks:
+        time.sleep(0.3)  # let the sampler start
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms_t = torch.tensor([ms], device=dev, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+
+    # Forward alone (one logit GEMM launch + finalize), timed on the same stream.
+    fwd_ms = None
+    if rank == 0:
+        for _ in range(3):
+            clp.grpo_logp_fwd(p.hidden, p.weight, p.ids, workspace=ws, logp=logp)
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        reps = max(5, args.steps // 2)
+        for _ in range(reps):
+            clp.grpo_logp_fwd(p.hidden, p.weight, p.ids, workspace=ws, logp=logp)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        fwd_ms = ev0.elapsed_time(ev1) / reps
+
+    # End to end through the public API with host buffers: pinned H2D of the
+    # step's inputs, the call, D2H of its results (loss, dH), every step.
+    e2e = None
+    if not args.no_e2e:
+        hh = p.hidden.cpu().pin_memory()
+        host_in = [hh, p.ids.cpu().pin_memory(), p.mask.cpu().pin_memory(),
+                   old.cpu().pin_memory(), ref.cpu().pin_memory(), p.adv.cpu().pin_memory()]
+        dev_in = [torch.empty_like(x, device=dev) for x in host_in]
+        loss_h = torch.empty(1, dtype=torch.float32).pin_memory()
+        dH_h = torch.empty(N, D, dtype=torch.bfloat16).pin_memory()
+
+        def e2e_step():
+            for d_, h_ in zip(dev_in, host_in):
+                d_.copy_(h_, non_blocking=True)
+            clp.grpo_loss_fwd_bwd(dev_in[0], p.weight, dev_in[1], dev_in[2], dev_in[3],
+                                  dev_in[4], dev_in[5], T, params=params, workspace=ws,
+                                  loss=loss, logp=None, dH=dH, want_logp=False)
+            loss_h.copy_(loss, non_blocking=True)
+            dH_h.copy_(dH, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = torch.tensor([ev0.elapsed_time(ev1) / args.steps], device=dev,
+                            dtype=torch.float64)
+        if world > 1:
+            dist.all_reduce(e_ms, op=dist.ReduceOp.MAX)
+        h2d = sum(x.numel() * x.element_size() for x in host_in)
+        d2h = loss_h.numel() * 4 + dH_h.numel() * 2
+        e2e = {"value": world * valid / (float(e_ms.item()) / 1e3), "unit": "tokens/s",
+               "ms_per_step": float(e_ms.item()), "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h,
+               "note": "pinned host hidden/ids/mask/old/ref/adv in, loss + dH out; "
+                       "lm_head W resident on the device"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    fl = flops_per_token(D, V) * valid
+    tflops = fl / (ms_max / 1e3) / 1e12
+    peak_sus = peaks["bf16_tflops_sustained"]
+    peak_burst = peaks["bf16_tflops"]
+    out = {
+        "metric": METRIC,
+        "value": world * valid / (ms_max / 1e3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": p.name, "n_tokens": N, "valid_tokens": valid, "hidden": D,
+            "vocab": V, "seq_len": T, "completions": p.n_seqs,
+            "chunk_rows": plan["chunk_rows"], "vocab_block": plan["vocab_block"],
+            "l2": "inputs larger than L2 (W %.2f GB, hidden %.0f MB); no flush" % (
+                V * D * 2 / 1e9, N * D * 2 / 1e6),
+            "parallelism": "replicas: one independent batch per GPU" if world > 1 else "1 GPU",
+        },
+        "tflops": tflops,
+        "pct_bf16_peak": 100.0 * tflops / peak_sus,
+        "roofline": {
+            "bound": "tensor", "achieved": tflops, "peak": peak_sus, "unit": "TFLOP/s",
+            "frac": tflops / peak_sus, "frac_of_burst_peak": tflops / peak_burst,
+            "peak_source": f"{peak_src} bf16 sustained (cuBLAS loop)",
+            "kernel": "grpo_loss_fwd_bwd: %d launches per call (logit GEMM, finalize, "
+                      "%d x %d backward G/dH GEMM pairs)" % (
+                          plan["launches_loss"], plan["n_chunks"], plan["n_vocab_blocks"]),
+            "flops_per_call": fl, "traffic": None,
+        },
+        "fwd_only": None if fwd_ms is None else {
+            "ms": fwd_ms, "tflops": 2.0 * D * V * N / (fwd_ms / 1e3) / 1e12,
+            "frac_of_burst_peak": 2.0 * D * V * N / (fwd_ms / 1e3) / 1e12 / peak_burst,
+            "scope": "grpo_logp_fwd: logit GEMM + finalize over all N rows"},
+        "e2e": e2e,
+        "clocks": clocks.summary(),
+        "gpu_launches": plan["launches_loss"] * args.steps,
+        "workspace_bytes": plan["workspace_bytes"],
+        "cpu_baseline": None,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        n, t = oracle_rows_per_second(p, args.cpu_seconds, args.seed, None)
+        out["cpu_baseline"] = {
+            "value": n / t, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{n} seeded valid rows of {p.name} (logp, g, dH per row; 6DV fp64 "
+                      f"flops each), {t:.1f} s on the host cores (numpy/OpenBLAS threads)"}
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------- reference ----
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    import oracle
+    import synth
+
+    p = synth.make_problem(args.workload, seed=args.seed, device="cpu")
+    W64 = p.weight.float().numpy().astype(np.float64)
+    valid = torch.nonzero(p.mask != 0).flatten().numpy()
+    base = torch.full((p.n_tokens,), -math.log(p.vocab))
+    old, ref = p.old_ref(base)
+    M = float(len(valid))
+    rng = np.random.default_rng(args.seed)
+    # Rows per step: about 3 s of oracle work, calibrated on 8 rows.
+    t0 = time.perf_counter()
+    oracle.rows_fwd_bwd(p.hidden, W64, p.ids.numpy(), valid[:8], old, ref, p.adv, p.seq_len, M)
+    per_row = (time.perf_counter() - t0) / 8
+    rows_per_step = int(max(4, min(len(valid), 3.0 / max(per_row, 1e-6))))
+
+    def step():
+        rows = np.sort(rng.choice(valid, size=rows_per_step, replace=False))
+        oracle.rows_fwd_bwd(p.hidden, W64, p.ids.numpy(), rows, old, ref, p.adv, p.seq_len, M,
+                            p.eps_low, p.eps_high, p.beta)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = rows_per_step / dt
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": p.name, "n_tokens": p.n_tokens, "hidden": p.hidden_size,
+                   "vocab": p.vocab, "seq_len": p.seq_len},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(),
+                         "kind": "oracle",
+                         "sample": f"{rows_per_step} seeded valid rows per step of {p.name}"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    a = parse_args()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)
