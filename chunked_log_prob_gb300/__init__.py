@@ -7,12 +7,14 @@ runs in the CUDA library ``libgrpo_gb300.so`` built from ``csrc/``.
 from ._binding import (  # noqa: F401
     EXPORTED,
     GRPO_OK,
+    NOALLOC_MAX_TOKENS,
     GrpoError,
     GrpoParams,
     GrpoShape,
     alloc_workspace,
     grpo_get_plan,
     grpo_logp_fwd,
+    grpo_logp_fwd_noalloc,
     grpo_loss_fwd_bwd,
     grpo_read_device_status,
     grpo_workspace_size,

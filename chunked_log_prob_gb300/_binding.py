@@ -71,6 +71,8 @@ def _load():
     lib.grpo_get_plan.restype = ctypes.c_int
     lib.grpo_read_device_status.argtypes = [vp, P(ctypes.c_int), vp]
     lib.grpo_read_device_status.restype = ctypes.c_int
+    lib.grpo_logp_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, P(GrpoShape), vp]
+    lib.grpo_logp_fwd_noalloc.restype = ctypes.c_int
     lib.grpo_status_string.argtypes = [ctypes.c_int]
     lib.grpo_status_string.restype = ctypes.c_char_p
     return lib
@@ -80,7 +82,10 @@ lib = _load()
 
 EXPORTED = ("grpo_default_params", "grpo_workspace_size", "grpo_logp_fwd",
             "grpo_loss_fwd_bwd", "grpo_get_plan", "grpo_read_device_status",
-            "grpo_status_string")
+            "grpo_logp_fwd_noalloc", "grpo_status_string")
+
+# Largest batch of the workspace-free forward (its static device scratch).
+NOALLOC_MAX_TOKENS = 8192
 
 
 def status_string(code: int) -> str:
@@ -217,3 +222,27 @@ def grpo_read_device_status(workspace) -> int:
     if rc != GRPO_OK:
         raise GrpoError(rc, "grpo_read_device_status")
     return int(st.value)
+
+
+def grpo_logp_fwd_noalloc(hidden, W, ids, logp, lse=None):
+    """Workspace-free forward for callers that cannot allocate device memory.
+
+    Same results as grpo_logp_fwd; scratch is a static device array inside the
+    library (n_tokens <= NOALLOC_MAX_TOKENS). The caller passes the outputs.
+    Calls that overlap on the GPU race on the shared scratch.
+    """
+    dev = hidden.device
+    N, D = hidden.shape
+    V = W.shape[0]
+    _check(hidden, "hidden", torch.bfloat16, (N, D), dev)
+    _check(W, "W", torch.bfloat16, (V, D), dev)
+    _check(ids, "ids", torch.int32, (N,), dev)
+    _check(logp, "logp", torch.float32, (N,), dev)
+    if lse is not None:
+        _check(lse, "lse", torch.float32, (N,), dev)
+    shape = make_shape(N, 1, D, V)
+    rc = lib.grpo_logp_fwd_noalloc(_ptr(hidden), _ptr(W), _ptr(ids), _ptr(logp), _ptr(lse),
+                                   ctypes.byref(shape), _stream(dev))
+    if rc != GRPO_OK:
+        raise GrpoError(rc, "grpo_logp_fwd_noalloc")
+    return logp, lse

@@ -504,3 +504,85 @@ const char* grpo_status_string(int s) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Workspace-free forward for callers that cannot allocate device memory (see
+// grpo_logp_fwd_noalloc in the header). Its scratch is this file-scope device
+// array; host code reaches it only through the address that
+// cudaGetSymbolAddress returns for the current device (the array's name on the
+// host is a stand-in, not a device address).
+static __device__ __align__(256) unsigned char g_grpo_noalloc_scratch[GRPO_NOALLOC_SCRATCH_BYTES];
+
+namespace grpo {
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the static scratch on the current device; looked up once
+// per device, with that device current.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GRPO_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return GRPO_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_grpo_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return GRPO_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return GRPO_OK;
+}
+
+}  // namespace
+}  // namespace grpo
+
+extern "C" int grpo_logp_fwd_noalloc(const void* hidden, const void* W, const int32_t* ids,
+                                     float* logp, float* lse_or_null, const grpo_shape* shape,
+                                     void* stream) {
+  int r = check_shape(shape, false);
+  if (r != GRPO_OK) return r;
+  if (shape->n_tokens > GRPO_NOALLOC_MAX_TOKENS) return GRPO_ERR_UNSUPPORTED_SHAPE;
+  if (shape->n_tokens > 0 && (!hidden || !W || !ids || !logp)) return GRPO_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(W, 16) || !aligned(ids, 4) || !aligned(logp, 4) ||
+      !aligned(lse_or_null, 4))
+    return GRPO_ERR_MISALIGNED;
+  int sms = 0;
+  if ((r = device_setup(&sms)) != GRPO_OK) return r;
+  Layout L;
+  if ((r = make_layout(shape, nullptr, sms, &L)) != GRPO_OK) return r;
+  // The forward uses the workspace only up to the backward's G block.
+  if (L.off_G > GRPO_NOALLOC_SCRATCH_BYTES) return GRPO_ERR_UNSUPPORTED_SHAPE;
+  void* scratch = nullptr;
+  if ((r = noalloc_scratch(&scratch)) != GRPO_OK) return r;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // Status word and reduction counter must start at zero; the rest is fully
+  // overwritten before it is read.
+  if (cudaMemsetAsync(scratch, 0, 64, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  if (L.n == 0) return GRPO_OK;
+  Ws w = carve(scratch, L);
+  w.G = nullptr;  // beyond the forward's part of the scratch; never used here
+  w.acc = nullptr;
+  int splits = 1;
+  if ((r = run_forward(hidden, W, ids, nullptr, L, w, sms, &splits, st)) != GRPO_OK) return r;
+  FinalizeArgs f;
+  std::memset(&f, 0, sizeof(f));
+  f.n = L.n;
+  f.splits = splits;
+  f.part_ld = L.nr;
+  f.vocab = L.V;
+  f.seq_len = 1;
+  f.loss_mode = 0;
+  f.part_m = w.pm;
+  f.part_s = w.ps;
+  f.zy = w.zy;
+  f.ids = ids;
+  f.lse_ws = w.lse;
+  f.lse_out = lse_or_null;
+  f.logp_out = logp;
+  f.status = w.status;
+  if (launch_finalize(f, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  return GRPO_OK;
+}

@@ -141,6 +141,35 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
  * that used `workspace` into *device_status (GRPO_OK or a negative code). */
 int grpo_read_device_status(const void* workspace, int* device_status, void* stream);
 
+/* Workspace-free selective log-softmax. The pages have no counterpart to this
+ * call: it exists for callers that cannot allocate device memory themselves,
+ * for instance a plugin running inside a host framework that owns every byte
+ * of device memory through its own pool and forbids side allocations, or a
+ * latency-critical caller that cannot accept cudaMalloc's implicit device
+ * synchronisation or its failure under memory pressure.
+ *
+ * Computes exactly what grpo_logp_fwd computes (same kernels, same results),
+ * but its scratch lives in a file-scope device array of
+ * GRPO_NOALLOC_SCRATCH_BYTES (2.25 MiB) inside the library instead of a
+ * caller workspace. Every GPU on which the library's device code is loaded
+ * holds that array until the process exits. The caller still passes the
+ * inputs and the outputs (logp, optional lse) as device pointers.
+ *   - n_tokens is limited to GRPO_NOALLOC_MAX_TOKENS (8192); larger sizes
+ *     return GRPO_ERR_UNSUPPORTED_SHAPE before anything is launched.
+ *   - Allocates nothing: no cudaMalloc/cudaFree, no allocating library call.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins.
+ *   - All calls share the one array, which keeps the previous call's
+ *     contents; each call clears the parts that must start at zero. Two calls
+ *     that overlap on the GPU (different streams, no ordering between them)
+ *     race on the array and give wrong results: order them, e.g. on one stream.
+ *   - Out-of-range ids give logp = NaN; there is no caller-visible status word. */
+#define GRPO_NOALLOC_MAX_TOKENS 8192
+#define GRPO_NOALLOC_SCRATCH_BYTES 2359296
+int grpo_logp_fwd_noalloc(const void* hidden, const void* W, const int32_t* ids, float* logp,
+                          float* lse_or_null, const grpo_shape* shape, void* stream);
+
 /* Static text for a status code. */
 const char* grpo_status_string(int status);
 
