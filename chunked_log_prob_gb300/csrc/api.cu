@@ -26,6 +26,7 @@ constexpr int kMaxDevices = 64;
 constexpr size_t kOffStatus = 0;       // int
 constexpr size_t kOffCounter = 4;      // unsigned
 constexpr size_t kOffMsum = 8;         // double
+constexpr size_t kOffActive = 16;      // int: length of the active row-block list
 constexpr size_t kOffPartials = 64;    // double[kMaxFinalizeBlocks]
 static_assert(kOffPartials + kMaxFinalizeBlocks * sizeof(double) <= kHeaderBytes, "header");
 
@@ -39,7 +40,7 @@ struct Layout {
   int chunk_rows;   // backward chunk (multiple of BM)
   int vblock;       // backward vocab block (multiple of BN)
   bool need_acc;    // more than one vocab block -> fp32 dH accumulator
-  size_t off_pm, off_ps, off_zy, off_lse, off_g, off_G, off_acc, total;
+  size_t off_pm, off_ps, off_zy, off_lse, off_g, off_rbl, off_G, off_acc, total;
 };
 
 int auto_chunk_blocks(long long n_rb_total, int n_dt, int sms) {
@@ -94,6 +95,7 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   L->off_zy = off; off = align_up(off + L->nr * sizeof(float), 256);
   L->off_lse = off; off = align_up(off + L->nr * sizeof(float), 256);
   L->off_g = off; off = align_up(off + L->nr * sizeof(float), 256);
+  L->off_rbl = off; off = align_up(off + (L->nr / BM) * sizeof(int), 256);
   L->off_G = off; off = align_up(off + static_cast<size_t>(L->chunk_rows) * L->vblock * 2, 256);
   L->off_acc = off;
   if (L->need_acc) off = align_up(off + static_cast<size_t>(L->chunk_rows) * L->D * 4, 256);
@@ -197,6 +199,8 @@ struct Ws {
   unsigned* counter;
   double* msum;
   double* partials;
+  int* n_active;
+  int* rb_list;
   float *pm, *ps, *zy, *lse, *g, *acc;
   __nv_bfloat16* G;
 };
@@ -208,6 +212,8 @@ Ws carve(void* ws, const Layout& L) {
   w.counter = reinterpret_cast<unsigned*>(w.base + kOffCounter);
   w.msum = reinterpret_cast<double*>(w.base + kOffMsum);
   w.partials = reinterpret_cast<double*>(w.base + kOffPartials);
+  w.n_active = reinterpret_cast<int*>(w.base + kOffActive);
+  w.rb_list = reinterpret_cast<int*>(w.base + L.off_rbl);
   w.pm = reinterpret_cast<float*>(w.base + L.off_pm);
   w.ps = reinterpret_cast<float*>(w.base + L.off_ps);
   w.zy = reinterpret_cast<float*>(w.base + L.off_zy);
@@ -227,17 +233,21 @@ TileArgs base_args(const Layout& L, const Ws& w) {
   return a;
 }
 
-// Forward logit GEMM over all N rows: per-split (max, sum-exp) and z_y.
+// Forward logit GEMM: per-split (max, sum-exp) and z_y for every row of the
+// row blocks in `rb_list` (all row blocks when it is null).
 int run_forward(const void* hidden, const void* W, const int32_t* ids, const uint8_t* mask,
-                const Layout& L, const Ws& w, int sms, int* splits_out, cudaStream_t st) {
+                const int* rb_list, const int* n_active, const Layout& L, const Ws& w, int sms,
+                int* splits_out, cudaStream_t st) {
   CUtensorMap map_h, map_w;
   if (!encode_2d(&map_h, hidden, L.D, L.n, L.D, BK, BM) ||
       !encode_2d(&map_w, W, L.D, L.V, L.D, BK, BN))
     return GRPO_ERR_CUDA;
   TileArgs a = base_args(L, w);
-  a.rows = static_cast<int>(L.n);
-  a.row0 = 0;
+  a.n_total = L.n;
   a.n_rb = static_cast<int>(L.nr / BM);
+  a.rb_offset = 0;
+  a.rb_list = rb_list;
+  a.n_active = n_active;
   a.k_iters = static_cast<int>(cdiv(L.D, BK));
   a.group_rows = std::min(kGroupRows, a.n_rb);
   int splits = std::max(1, sms / a.group_rows);
@@ -258,6 +268,9 @@ int run_forward(const void* hidden, const void* W, const int32_t* ids, const uin
   return GRPO_OK;
 }
 
+// Backward over the active row blocks, in chunks of chunk_rows / BM list
+// entries: G block, then dH accumulation, per vocab block. Chunks past the
+// device-side list length find no work and return at once.
 int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH,
                  const Layout& L, const Ws& w, int sms, cudaStream_t st) {
   CUtensorMap map_h, map_w_k, map_w_mn;
@@ -266,17 +279,20 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
       !encode_2d(&map_w_mn, W, L.D, L.V, L.D, 64, BK))
     return GRPO_ERR_CUDA;
   const int n_dt = static_cast<int>(cdiv(L.D, BN));
-  for (long long c0 = 0; c0 < L.n; c0 += L.chunk_rows) {
-    const int rows_c = static_cast<int>(std::min<long long>(L.chunk_rows, L.n - c0));
-    const int n_rb = static_cast<int>(cdiv(rows_c, BM));
+  const int n_rb_total = static_cast<int>(L.nr / BM);
+  const int rb_per_chunk = L.chunk_rows / BM;
+  for (int rb0 = 0; rb0 < n_rb_total; rb0 += rb_per_chunk) {
+    const int n_rb = std::min(rb_per_chunk, n_rb_total - rb0);
     for (long long v0 = 0; v0 < L.V; v0 += L.vblock) {
       const int width = static_cast<int>(std::min<long long>(L.vblock, L.V - v0));
       const int ntile = static_cast<int>(cdiv(width, BN));
       // (1) G = g (onehot - softmax) for this chunk x vocab block, bf16.
       TileArgs a = base_args(L, w);
-      a.rows = rows_c;
-      a.row0 = static_cast<int>(c0);
+      a.n_total = L.n;
       a.n_rb = n_rb;
+      a.rb_offset = rb0;
+      a.rb_list = w.rb_list;
+      a.n_active = w.n_active;
       a.k_iters = static_cast<int>(cdiv(L.D, BK));
       a.group_rows = std::min(kGroupRows, n_rb);
       a.n_cols = ntile;
@@ -292,11 +308,14 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
         return GRPO_ERR_CUDA;
       // (2) dH_chunk (+)= G W[v0 : v0 + width].
       CUtensorMap map_g;
-      if (!encode_2d(&map_g, w.G, width, rows_c, L.vblock, BK, BM)) return GRPO_ERR_CUDA;
+      if (!encode_2d(&map_g, w.G, width, static_cast<uint64_t>(n_rb) * BM, L.vblock, BK, BM))
+        return GRPO_ERR_CUDA;
       TileArgs b = base_args(L, w);
-      b.rows = rows_c;
-      b.row0 = static_cast<int>(c0);
+      b.n_total = L.n;
       b.n_rb = n_rb;
+      b.rb_offset = rb0;
+      b.rb_list = w.rb_list;
+      b.n_active = w.n_active;
       b.k_iters = static_cast<int>(cdiv(width, BK));
       b.group_rows = std::min(kGroupRows, n_rb);
       b.n_cols = n_dt;
@@ -364,7 +383,7 @@ int grpo_logp_fwd(const void* hidden, const void* W, const int32_t* ids, float* 
   if (L.n == 0) return GRPO_OK;
   Ws w = carve(workspace, L);
   int splits = 1;
-  if ((r = run_forward(hidden, W, ids, nullptr, L, w, sms, &splits, st)) != GRPO_OK) return r;
+  if ((r = run_forward(hidden, W, ids, nullptr, nullptr, nullptr, L, w, sms, &splits, st)) != GRPO_OK) return r;
   FinalizeArgs f;
   std::memset(&f, 0, sizeof(f));
   f.n = L.n;
@@ -417,9 +436,14 @@ int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
     return GRPO_OK;
   }
   Ws w = carve(workspace, L);
-  if (launch_count_mask(mask, L.n, w.msum, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  const int n_rb_total = static_cast<int>(L.nr / BM);
+  if (launch_row_plan(mask, L.n, n_rb_total, w.rb_list, w.n_active, w.msum, st) != cudaSuccess ||
+      launch_zero_padding_blocks(mask, L.n, n_rb_total, L.D, dH, sms, st) != cudaSuccess)
+    return GRPO_ERR_CUDA;
   int splits = 1;
-  if ((r = run_forward(hidden, W, ids, mask, L, w, sms, &splits, st)) != GRPO_OK) return r;
+  if ((r = run_forward(hidden, W, ids, mask, w.rb_list, w.n_active, L, w, sms, &splits, st)) !=
+      GRPO_OK)
+    return r;
   FinalizeArgs f;
   std::memset(&f, 0, sizeof(f));
   f.n = L.n;
@@ -471,7 +495,7 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
   const int grp = std::min(kGroupRows, n_rb);
   info->fwd_splits = std::min(std::max(1, sms / grp), std::min(L.nvt, kMaxSplits));
   info->launches_logp = L.n > 0 ? 2 : 0;
-  info->launches_loss = L.n > 0 ? 3 + 2 * info->n_chunks * info->n_vocab_blocks : 0;
+  info->launches_loss = L.n > 0 ? 4 + 2 * info->n_chunks * info->n_vocab_blocks : 0;
   info->workspace_bytes = std::max(L.total, Lmax.total);
   return GRPO_OK;
 }
@@ -566,7 +590,7 @@ extern "C" int grpo_logp_fwd_noalloc(const void* hidden, const void* W, const in
   w.G = nullptr;  // beyond the forward's part of the scratch; never used here
   w.acc = nullptr;
   int splits = 1;
-  if ((r = run_forward(hidden, W, ids, nullptr, L, w, sms, &splits, st)) != GRPO_OK) return r;
+  if ((r = run_forward(hidden, W, ids, nullptr, nullptr, nullptr, L, w, sms, &splits, st)) != GRPO_OK) return r;
   FinalizeArgs f;
   std::memset(&f, 0, sizeof(f));
   f.n = L.n;

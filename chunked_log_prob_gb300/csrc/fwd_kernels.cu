@@ -2,6 +2,8 @@
 // the mask count, and the per-row finalisation (log-sum-exp combine,
 // selective log-prob, GRPO token loss and its derivative, deterministic
 // fp64 loss reduction).
+#include <algorithm>
+
 #include "launch.h"
 
 namespace grpo {
@@ -17,22 +19,87 @@ cudaError_t launch_fwd_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
   return cudaGetLastError();
 }
 
-__global__ void __launch_bounds__(1024) count_mask_kernel(const uint8_t* __restrict__ mask,
-                                                          long long n, double* out) {
-  __shared__ unsigned long long warp_sums[32];
-  unsigned long long s = 0;
-  if (mask == nullptr) {
-    s = threadIdx.x == 0 ? static_cast<unsigned long long>(n) : 0ull;
-  } else {
-    for (long long i = threadIdx.x; i < n; i += blockDim.x) s += mask[i] != 0;
+// Row plan of a loss call (one block of 1024 threads): the list of row blocks
+// (BM rows each) holding at least one unmasked token, in increasing order, its
+// length, and the number of unmasked tokens. Blocks of pure padding are then
+// skipped by every GEMM of the call.
+__global__ void __launch_bounds__(1024) row_plan_kernel(const uint8_t* __restrict__ mask,
+                                                        long long n, int n_rb,
+                                                        int* __restrict__ rb_list,
+                                                        int* __restrict__ n_active,
+                                                        double* __restrict__ msum) {
+  __shared__ int warp_off[32];
+  __shared__ int chunk_total;
+  __shared__ unsigned long long warp_tok[32];
+  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  const int n_warps = blockDim.x >> 5;
+  int base = 0;
+  unsigned long long tokens = 0;
+  for (int b0 = 0; b0 < n_rb; b0 += blockDim.x) {
+    const int rb = b0 + threadIdx.x;
+    int cnt = 0;
+    if (rb < n_rb) {
+      const long long r0 = static_cast<long long>(rb) * BM;
+      const long long r1 = min(r0 + BM, n);
+      if (mask == nullptr) {
+        cnt = static_cast<int>(r1 - r0);
+      } else {
+        for (long long r = r0; r < r1; ++r) cnt += mask[r] != 0;
+      }
+    }
+    tokens += static_cast<unsigned long long>(cnt);
+    const bool active = cnt > 0;
+    const unsigned bal = __ballot_sync(0xffffffffu, active);
+    const int pre = __popc(bal & ((1u << lane) - 1u));
+    if (lane == 0) warp_off[w] = __popc(bal);
+    __syncthreads();
+    if (w == 0) {
+      const int v = lane < n_warps ? warp_off[lane] : 0;
+      int incl = v;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+      }
+      if (lane < n_warps) warp_off[lane] = incl - v;
+      if (lane == 31) chunk_total = incl;
+    }
+    __syncthreads();
+    if (active) rb_list[base + warp_off[w] + pre] = rb;
+    base += chunk_total;
+    __syncthreads();
   }
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
-  if ((threadIdx.x & 31) == 0) warp_sums[threadIdx.x >> 5] = s;
+  for (int o = 16; o > 0; o >>= 1) tokens += __shfl_down_sync(0xffffffffu, tokens, o);
+  if (lane == 0) warp_tok[w] = tokens;
   __syncthreads();
-  if (threadIdx.x < 32) {
-    s = threadIdx.x < (blockDim.x >> 5) ? warp_sums[threadIdx.x] : 0ull;
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
-    if (threadIdx.x == 0) *out = static_cast<double>(s);
+  if (threadIdx.x == 0) {
+    unsigned long long t = 0;
+    for (int i = 0; i < n_warps; ++i) t += warp_tok[i];
+    *msum = static_cast<double>(t);
+    *n_active = base;
+  }
+}
+
+// dH rows of row blocks without any unmasked token are never touched by the
+// backward GEMMs; they are written as exact zeros here.
+__global__ void __launch_bounds__(256) zero_padding_blocks_kernel(
+    const uint8_t* __restrict__ mask, long long n, int n_rb, int hidden,
+    __nv_bfloat16* __restrict__ dH) {
+  __shared__ int any;
+  for (int rb = blockIdx.x; rb < n_rb; rb += gridDim.x) {
+    if (threadIdx.x == 0) any = 0;
+    __syncthreads();
+    const long long r0 = static_cast<long long>(rb) * BM;
+    const long long r1 = min(r0 + BM, n);
+    if (r0 + threadIdx.x < r1 && mask[r0 + threadIdx.x] != 0) any = 1;
+    __syncthreads();
+    if (!any) {
+      // hidden % 8 == 0: 16-byte stores of 8 bf16.
+      const long long vecs = (r1 - r0) * (hidden / 8);
+      uint4* dst = reinterpret_cast<uint4*>(dH + r0 * hidden);
+      for (long long i = threadIdx.x; i < vecs; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
   }
 }
 
@@ -59,17 +126,21 @@ __global__ void __launch_bounds__(kFinalizeThreads) finalize_kernel(const Finali
   double local = 0.0;
   for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < a.n;
        t += static_cast<long long>(gridDim.x) * blockDim.x) {
-    // log-sum-exp from the per-split (max, sum) pairs, base-2 domain.
-    float m2 = -INFINITY;
-    for (int s = 0; s < a.splits; ++s) m2 = fmaxf(m2, a.part_m[s * a.part_ld + t]);
-    float ssum = 0.f;
-    for (int s = 0; s < a.splits; ++s)
-      ssum += a.part_s[s * a.part_ld + t] * exp2f(a.part_m[s * a.part_ld + t] - m2);
-    const float lse = (m2 + log2f(ssum)) * 0.69314718055994531f;
+    const bool counted = !a.loss_mode || a.mask == nullptr || a.mask[t] != 0;
+    // log-sum-exp from the per-split (max, sum) pairs, base-2 domain. Masked
+    // rows of a loss call may sit in skipped row blocks with no partials.
+    float lse = 0.f;
+    if (counted) {
+      float m2 = -INFINITY;
+      for (int s = 0; s < a.splits; ++s) m2 = fmaxf(m2, a.part_m[s * a.part_ld + t]);
+      float ssum = 0.f;
+      for (int s = 0; s < a.splits; ++s)
+        ssum += a.part_s[s * a.part_ld + t] * exp2f(a.part_m[s * a.part_ld + t] - m2);
+      lse = (m2 + log2f(ssum)) * 0.69314718055994531f;
+    }
     a.lse_ws[t] = lse;
     if (a.lse_out) a.lse_out[t] = lse;
 
-    const bool counted = !a.loss_mode || a.mask == nullptr || a.mask[t] != 0;
     float logp = 0.f;
     float gval = 0.f;
     if (counted) {
@@ -125,9 +196,18 @@ __global__ void __launch_bounds__(kFinalizeThreads) finalize_kernel(const Finali
   }
 }
 
-cudaError_t launch_count_mask(const uint8_t* mask, long long n, double* out,
-                              cudaStream_t stream) {
-  count_mask_kernel<<<1, 1024, 0, stream>>>(mask, n, out);
+cudaError_t launch_row_plan(const uint8_t* mask, long long n, int n_rb, int* rb_list,
+                            int* n_active, double* msum, cudaStream_t stream) {
+  row_plan_kernel<<<1, 1024, 0, stream>>>(mask, n, n_rb, rb_list, n_active, msum);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_padding_blocks(const uint8_t* mask, long long n, int n_rb, int hidden,
+                                       void* dH, int sms, cudaStream_t stream) {
+  if (mask == nullptr || n_rb <= 0) return cudaSuccess;
+  const int grid = std::min(n_rb, 4 * std::max(sms, 1));
+  zero_padding_blocks_kernel<<<grid, 256, 0, stream>>>(mask, n, n_rb, hidden,
+                                                       static_cast<__nv_bfloat16*>(dH));
   return cudaGetLastError();
 }
 

@@ -37,9 +37,12 @@ constexpr float kLog2e = 1.4426950408889634f;
 enum GemmMode { MODE_FWD = 0, MODE_BWDG = 1, MODE_DH = 2 };
 
 struct TileArgs {
-  int rows;        // valid A rows in this launch
-  int row0;        // FWD/BWDG: global H row of local row 0; DH: global dH row
-  int n_rb;        // ceil(rows / BM)
+  long long n_total;     // N: rows of hidden / dH; global rows >= N are padding
+  int n_rb;              // row blocks this launch may cover (host-side bound)
+  int rb_offset;         // first entry of the row-block list this launch covers
+  const int* rb_list;    // global indices of the row blocks to compute, or null
+                         // (then local block i is global block rb_offset + i)
+  const int* n_active;   // device-side length of rb_list, or null (= all)
   int k_iters;     // ceil(K / BK)
   int group_rows;  // row blocks per raster group
   int n_cols;      // FWD: vocab splits; BWDG: vocab tiles in block; DH: D tiles
@@ -52,15 +55,15 @@ struct TileArgs {
   // MODE_FWD
   float* part_m;         // [n_cols][part_ld] running max (log2 units)
   float* part_s;         // [n_cols][part_ld] running sum of 2^(x - max)
-  float* zy;             // [rows] target logit
+  float* zy;             // [N] target logit, indexed by global row
   long long part_ld;
   // MODE_BWDG
   const float* lse;      // indexed by global row
   const float* g;        // indexed by global row
-  __nv_bfloat16* G;      // [rows][ldG] chunk workspace
+  __nv_bfloat16* G;      // [local rows][ldG] chunk workspace
   long long ldG;
   // MODE_DH
-  float* acc;            // [rows][hidden] fp32 accumulator
+  float* acc;            // [local rows][hidden] fp32 accumulator
   __nv_bfloat16* dH;     // [N][hidden] output, indexed by global row
   int first;
   int last;
@@ -75,6 +78,18 @@ __device__ __forceinline__ void decode_unit(int u, int n_rb, int n_cols, int R, 
   const int rows_in_g = min(R, n_rb - grp * R);
   col = rem / rows_in_g;
   rb = grp * R + (rem - col * rows_in_g);
+}
+
+// Global row block of the launch's local row block `li`.
+__device__ __forceinline__ int global_rb(const TileArgs& a, int li) {
+  return a.rb_list != nullptr ? a.rb_list[a.rb_offset + li] : a.rb_offset + li;
+}
+
+// Row blocks this launch actually covers (the active list may be shorter
+// than the host-side bound).
+__device__ __forceinline__ int launch_row_blocks(const TileArgs& a) {
+  if (a.n_active == nullptr) return a.n_rb;
+  return max(0, min(a.n_rb, *a.n_active - a.rb_offset));
 }
 
 template <int MODE>
@@ -145,7 +160,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
 
-  const int n_units = args.n_rb * args.n_cols;
+  const int n_rb = launch_row_blocks(args);
+  const int n_units = n_rb * args.n_cols;
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
@@ -154,10 +170,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       bool ok = true;
       const uint64_t pol_a = policy_evict_last();
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        int rb, col, t0, t1;
-        decode_unit(u, args.n_rb, args.n_cols, args.group_rows, rb, col);
+        int li, col, t0, t1;
+        decode_unit(u, n_rb, args.n_cols, args.group_rows, li, col);
         unit_tiles<MODE>(args, col, t0, t1);
-        const int a_row = (MODE == MODE_DH ? 0 : args.row0) + rb * BM;
+        const int a_row = (MODE == MODE_DH ? li : global_rb(args, li)) * BM;
         for (int t = t0; t < t1 && ok; ++t) {
           for (int k = 0; k < args.k_iters; ++k, ++it) {
             const int s = it % STAGES;
@@ -195,8 +211,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t it = 0, tile_it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        int rb, col, t0, t1;
-        decode_unit(u, args.n_rb, args.n_cols, args.group_rows, rb, col);
+        int li, col, t0, t1;
+        decode_unit(u, n_rb, args.n_cols, args.group_rows, li, col);
         unit_tiles<MODE>(args, col, t0, t1);
         for (int t = t0; t < t1 && ok; ++t, ++tile_it) {
           const uint32_t buf = tile_it & 1u;
@@ -251,12 +267,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     uint32_t tile_it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      int rb, col, t0, t1;
-      decode_unit(u, args.n_rb, args.n_cols, args.group_rows, rb, col);
+      int li, col, t0, t1;
+      decode_unit(u, n_rb, args.n_cols, args.group_rows, li, col);
       unit_tiles<MODE>(args, col, t0, t1);
-      const int lrow = rb * BM + lrow_in_tile;
-      const bool valid = lrow < args.rows;
-      const int grow = args.row0 + lrow;
+      const int lrow = li * BM + lrow_in_tile;  // row of the chunk workspace
+      const long long grow = static_cast<long long>(global_rb(args, li)) * BM + lrow_in_tile;
+      const bool valid = grow < args.n_total;
 
       // Per-row state.
       float m2 = -INFINITY, ssum = 0.f;  // FWD
@@ -300,7 +316,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
               for (int j = 0; j < 32; ++j)
                 if (static_cast<unsigned>(j) == off) z = v[j];
-              args.zy[lrow] = z;
+              args.zy[grow] = z;
             }
             float mx0 = fmaxf(v[0], v[1]), mx1 = fmaxf(v[2], v[3]);
 #pragma unroll
@@ -398,8 +414,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (lane == 0) mbar_arrive(&tempty_bar[buf]);
       }
       if (MODE == MODE_FWD && ok && valid) {
-        args.part_m[static_cast<long long>(col) * args.part_ld + lrow] = m2;
-        args.part_s[static_cast<long long>(col) * args.part_ld + lrow] = ssum;
+        args.part_m[static_cast<long long>(col) * args.part_ld + grow] = m2;
+        args.part_s[static_cast<long long>(col) * args.part_ld + grow] = ssum;
       }
     }
   }

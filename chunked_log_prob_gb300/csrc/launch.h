@@ -47,8 +47,10 @@ cudaError_t launch_bwdg_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
                              const TileArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_dh_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
                            const TileArgs& args, int grid, cudaStream_t stream);
-cudaError_t launch_count_mask(const uint8_t* mask, long long n, double* out,
-                              cudaStream_t stream);
+cudaError_t launch_row_plan(const uint8_t* mask, long long n, int n_rb, int* rb_list,
+                            int* n_active, double* msum, cudaStream_t stream);
+cudaError_t launch_zero_padding_blocks(const uint8_t* mask, long long n, int n_rb, int hidden,
+                                       void* dH, int sms, cudaStream_t stream);
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t stream);
 
 }  // namespace grpo

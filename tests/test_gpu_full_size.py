@@ -1,0 +1,130 @@
+"""Full-size GPU parity on the four large workloads, in the launch configuration
+bench.py times (default plan).
+
+The oracle cannot afford all N x V logits in fp64 at these sizes, so:
+  * logp and dH are compared on a seeded sample of rows. Given the loss
+    denominator M, a row's logp, g and dH depend on that row alone, so the
+    oracle's values for sampled rows are exact, not estimates.
+  * the loss is compared exactly in a second call whose mask keeps only the
+    sampled rows (M = sample size), same shapes and hidden states;
+  * for the Llama-3.1-8B shape (the bench workload) the oracle also computes
+    every row's logp, so the loss of the full call is compared exactly.
+Masked rows in the sample must have logp = 0 and dH exactly 0.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+LOGP_TOL = 1e-2
+LOSS_RTOL = 1e-3
+DH_RTOL = 2e-2
+DEV = "cuda:0"
+N_SAMPLE = 192
+N_SAMPLE_MASKED = 32
+
+
+@pytest.fixture(scope="module")
+def clp():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import chunked_log_prob_gb300 as m
+
+    return m
+
+
+def _sample_rows(p, seed):
+    rng = np.random.default_rng(seed)
+    m = p.mask.numpy().astype(bool)
+    valid = np.nonzero(m)[0]
+    masked = np.nonzero(~m)[0]
+    rows = rng.choice(valid, size=min(N_SAMPLE, len(valid)), replace=False)
+    mrows = rng.choice(masked, size=min(N_SAMPLE_MASKED, len(masked)), replace=False)
+    # Always include the first and last valid rows (tile and chunk edges).
+    rows = np.unique(np.concatenate([rows, valid[:1], valid[-1:]]))
+    return np.sort(rows), np.sort(mrows)
+
+
+def _run(clp, p, mask, old, ref):
+    dev = torch.device(DEV)
+    args = [t.to(dev) for t in (p.hidden, p.weight, p.ids, mask, old, ref, p.adv)]
+    ws = clp.alloc_workspace(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, None, dev)
+    loss, logp, dH = clp.grpo_loss_fwd_bwd(*args, p.seq_len, workspace=ws)
+    st = clp.grpo_read_device_status(ws)
+    return loss.item(), logp.cpu(), dH, st
+
+
+@pytest.mark.parametrize("name", ["qwen2.5-1.5b", "llama-3.1-8b", "qwen3-8b-long",
+                                  "gpt-oss-20b-long"])
+def test_full_size_sampled_rows(clp, name):
+    p = synth.make_problem(name, seed=1)
+    rows, mrows = _sample_rows(p, seed=2)
+    W64 = p.weight.float().numpy().astype(np.float64)
+    lp_rows, _ = oracle.selective_logp(p.hidden[rows], W64, p.ids.numpy()[rows])
+    base = torch.full((p.n_tokens,), -math.log(p.vocab), dtype=torch.float64)
+    base[rows] = torch.from_numpy(lp_rows)
+    old, ref = p.old_ref(base)
+    M = float(p.mask.sum())
+
+    # (1) the workload itself: sampled rows of logp and dH.
+    L, logp, dH, st = _run(clp, p, p.mask, old, ref)
+    assert st == 0
+    want = oracle.rows_fwd_bwd(p.hidden, W64, p.ids.numpy(), rows, old, ref, p.adv,
+                               p.seq_len, M, p.eps_low, p.eps_high, p.beta)
+    got_lp = logp.double().numpy()[rows]
+    got_dh = dH[torch.from_numpy(rows).to(DEV)].double().cpu().numpy()
+    dl = np.abs(got_lp - want["logp"]).max()
+    rel_dh = np.linalg.norm(got_dh - want["dH"]) / np.linalg.norm(want["dH"])
+    print(f"{name}: rows={len(rows)} max|dlogp|={dl:.3e} rel_dH={rel_dh:.3e}")
+    assert dl <= LOGP_TOL and rel_dh <= DH_RTOL
+    if len(mrows):
+        assert torch.all(logp[mrows] == 0)
+        assert torch.all(dH[torch.from_numpy(mrows).to(DEV)] == 0)
+    assert math.isfinite(L)
+
+    # (2) same shapes, mask = sampled rows only: the loss is exact.
+    mask2 = torch.zeros_like(p.mask)
+    mask2[rows] = 1
+    L2, logp2, dH2, st2 = _run(clp, p, mask2, old, ref)
+    assert st2 == 0
+    lp_full = np.zeros(p.n_tokens)
+    lp_full[rows] = lp_rows
+    L_want, _, _, M2 = oracle.grpo_loss(lp_full, old, ref, p.adv, mask2, p.seq_len,
+                                        p.eps_low, p.eps_high, p.beta)
+    rel_loss = abs(L2 - L_want) / abs(L_want)
+    got_dh2 = dH2[torch.from_numpy(rows).to(DEV)].double().cpu().numpy()
+    want_dh2 = want["dH"] * (M / M2)  # dH is linear in g, and g scales as 1/M
+    rel_dh2 = np.linalg.norm(got_dh2 - want_dh2) / np.linalg.norm(want_dh2)
+    print(f"{name}: sampled-mask loss={L2:.6e} want={L_want:.6e} rel={rel_loss:.3e} "
+          f"rel_dH={rel_dh2:.3e}")
+    assert rel_loss <= LOSS_RTOL and rel_dh2 <= DH_RTOL
+    other = torch.ones(p.n_tokens, dtype=torch.bool)
+    other[rows] = False
+    assert torch.all(logp2[other] == 0)
+    assert int((dH2[other.to(DEV)] != 0).sum()) == 0
+
+
+def test_llama_full_loss_exact(clp):
+    # Every row through the oracle (about 1.7e13 fp64 flops): the loss of the
+    # bench's own workload, exactly, with old/ref = oracle logp + noise.
+    p = synth.make_problem("llama-3.1-8b", seed=3)
+    W64 = p.weight.float().numpy().astype(np.float64)
+    lp, _ = oracle.selective_logp(p.hidden, W64, p.ids.numpy(), row_block=256)
+    old, ref = p.old_ref(torch.from_numpy(lp))
+    L, logp, dH, st = _run(clp, p, p.mask, old, ref)
+    assert st == 0
+    L_want, g, _, _ = oracle.grpo_loss(lp, old, ref, p.adv, p.mask, p.seq_len,
+                                       p.eps_low, p.eps_high, p.beta)
+    d = np.abs(logp.double().numpy() - lp)
+    rel = abs(L - L_want) / abs(L_want)
+    print(f"llama full: max|dlogp|={d.max():.3e} rms={np.sqrt((d ** 2).mean()):.3e} "
+          f"loss={L:.6e} want={L_want:.6e} rel={rel:.3e}")
+    assert d.max() <= LOGP_TOL and rel <= LOSS_RTOL

@@ -170,7 +170,7 @@ def test_bad_token_id_sets_status(clp):
     ids[7] = p.vocab  # unmasked and out of range
     old = torch.full((p.n_tokens,), -8.0)
     L, logp, dH, st = gpu_loss(clp, p, old, old, ids=ids)
-    assert st == clp.STATUS_BAD_TOKEN_ID if hasattr(clp, "STATUS_BAD_TOKEN_ID") else st == -8
+    assert st == -8  # GRPO_ERR_BAD_TOKEN_ID
     assert math.isnan(logp[7]) and math.isnan(L)
 
 
@@ -212,3 +212,22 @@ def test_empty_batch(clp):
                                            f, f, torch.empty(0, dtype=torch.float32, device=DEV),
                                            1)
     assert loss.item() == 0.0 and dH.numel() == 0
+
+
+@pytest.mark.parametrize("chunk", [256, 0])
+def test_padding_blocks_are_skipped_and_zeroed(clp, chunk):
+    # Completions of 512 slots with 1..512 valid tokens: most 128-row blocks are
+    # pure padding, skipped by every GEMM; their dH rows must still come out 0.
+    p = synth.make_problem("tiny", seed=21 + chunk, prompts=2, G=4, T=512, D=256, V=3000,
+                           lengths=(1, 512))
+    old, ref, want = oracle_case(p)
+    params = clp.make_params(chunk_tokens=chunk, vocab_block=1024)
+    ws = clp.alloc_workspace(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, params, DEV)
+    dH = torch.full((p.n_tokens, p.hidden_size), float("nan"), dtype=torch.bfloat16, device=DEV)
+    logp = torch.full((p.n_tokens,), float("nan"), device=DEV)
+    loss, logp, dH = clp.grpo_loss_fwd_bwd(
+        _to(p.hidden), _to(p.weight), _to(p.ids), _to(p.mask), _to(old), _to(ref), _to(p.adv),
+        p.seq_len, params=params, workspace=ws, dH=dH, logp=logp)
+    st = clp.grpo_read_device_status(ws)
+    got = (loss.item(), logp.cpu().double().numpy(), dH.cpu().double().numpy(), st)
+    check(got, want, p.mask, f"padding chunk={chunk}")
