@@ -18,7 +18,7 @@ namespace {
 constexpr int kMaxSplits = 32;          // forward vocab splits (per-row partials)
 constexpr int kMaxAutoChunkBlocks = 32;  // automatic backward chunk <= 4096 rows
 constexpr int kAutoVocabBlock = 32768;   // automatic backward vocab block
-constexpr int kGroupRows = 8;            // row blocks per raster group
+constexpr int kSplitsTarget = 8;        // forward vocab splits per raster group
 constexpr size_t kHeaderBytes = 16384;   // status, counters, loss partials
 constexpr int kMaxDevices = 64;
 
@@ -101,6 +101,14 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   if (L->need_acc) off = align_up(off + static_cast<size_t>(L->chunk_rows) * L->D * 4, 256);
   L->total = off;
   return GRPO_OK;
+}
+
+// Row blocks per raster group: the CTAs in flight (one per SM) cover
+// group_rows row blocks x (sms / group_rows) vocab tiles or splits, so each
+// W tile fetched from HBM is shared through L2 by group_rows CTAs and each row
+// block's hidden states by the others.
+int group_rows_for(int n_rb, int sms) {
+  return std::max(1, std::min(n_rb, std::max(1, sms) / kSplitsTarget));
 }
 
 int check_shape(const grpo_shape* s, bool need_seq) {
@@ -249,7 +257,7 @@ int run_forward(const void* hidden, const void* W, const int32_t* ids, const uin
   a.rb_list = rb_list;
   a.n_active = n_active;
   a.k_iters = static_cast<int>(cdiv(L.D, BK));
-  a.group_rows = std::min(kGroupRows, a.n_rb);
+  a.group_rows = group_rows_for(a.n_rb, sms);
   int splits = std::max(1, sms / a.group_rows);
   splits = std::min(splits, std::min(L.nvt, kMaxSplits));
   a.n_cols = splits;
@@ -294,7 +302,7 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
       a.rb_list = w.rb_list;
       a.n_active = w.n_active;
       a.k_iters = static_cast<int>(cdiv(L.D, BK));
-      a.group_rows = std::min(kGroupRows, n_rb);
+      a.group_rows = group_rows_for(n_rb, sms);
       a.n_cols = ntile;
       a.v0 = static_cast<int>(v0);
       a.ids = ids;
@@ -317,7 +325,7 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
       b.rb_list = w.rb_list;
       b.n_active = w.n_active;
       b.k_iters = static_cast<int>(cdiv(width, BK));
-      b.group_rows = std::min(kGroupRows, n_rb);
+      b.group_rows = group_rows_for(n_rb, sms);
       b.n_cols = n_dt;
       b.v0 = static_cast<int>(v0);
       b.acc = w.acc;
@@ -375,9 +383,8 @@ int grpo_logp_fwd(const void* hidden, const void* W, const int32_t* ids, float* 
   if ((r = device_setup(&sms)) != GRPO_OK) return r;
   Layout L;
   if ((r = make_layout(shape, params, sms, &L)) != GRPO_OK) return r;
-  Layout Lmax;
-  make_layout(shape, params, 0, &Lmax);
-  if (workspace_bytes < std::max(L.total, Lmax.total)) return GRPO_ERR_WORKSPACE_TOO_SMALL;
+  // The forward uses the workspace only up to the backward's G block.
+  if (workspace_bytes < L.off_G) return GRPO_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(workspace, 0, 64, st) != cudaSuccess) return GRPO_ERR_CUDA;
   if (L.n == 0) return GRPO_OK;
@@ -492,7 +499,7 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
   info->n_chunks = static_cast<int32_t>(cdiv(L.n, L.chunk_rows));
   info->n_vocab_blocks = static_cast<int32_t>(cdiv(L.V, L.vblock));
   const int n_rb = static_cast<int>(L.nr / BM);
-  const int grp = std::min(kGroupRows, n_rb);
+  const int grp = group_rows_for(n_rb, sms);
   info->fwd_splits = std::min(std::max(1, sms / grp), std::min(L.nvt, kMaxSplits));
   info->launches_logp = L.n > 0 ? 2 : 0;
   info->launches_loss = L.n > 0 ? 4 + 2 * info->n_chunks * info->n_vocab_blocks : 0;

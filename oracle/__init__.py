@@ -7,6 +7,8 @@ an independent library routine; no function is "parity unpinned".
 """
 
 from .grpo_oracle import (  # noqa: F401
+    IDENTITY,
+    Transform,
     broadcast_advantage,
     grad_hidden,
     grpo_loss,

@@ -44,6 +44,12 @@ notes of the repository):
 * sequence b of token t is t // T (completions of length T laid end to end);
   the advantage of the sequence is broadcast over its tokens.
 * masked rows get logp = 0 and a zero gradient row.
+* logit transforms ("GRPO with 7x longer context", notes under the
+  chunked_hidden_states_selective_log_softmax call: softcapping, temperature
+  and the logit scale multiply/divide): applied to the raw logit z in the
+  order the call lists them, z' = f(z) = s(z * mult / div) / temperature with
+  s(x) = cap * tanh(x / cap) when a softcap is set, else s(x) = x. logp is the
+  log-softmax of z'; the chain rule adds f'(z_v) to every vocab term of dH.
 """
 
 from __future__ import annotations
@@ -53,6 +59,36 @@ import numpy as np
 # Rows per block when whole logit rows are materialised; bounds the float64
 # temporary to ROW_BLOCK * V * 8 bytes.
 ROW_BLOCK = 64
+
+
+class Transform:
+    """Logit transform z' = s(z * mult / div) / temperature (identity by default)."""
+
+    def __init__(self, scale_mul=1.0, scale_div=1.0, softcap=0.0, temperature=1.0):
+        self.scale_mul = float(scale_mul)
+        self.scale_div = float(scale_div)
+        self.softcap = float(softcap)
+        self.temperature = float(temperature)
+
+    @property
+    def identity(self):
+        return (self.scale_mul == 1.0 and self.scale_div == 1.0 and self.softcap == 0.0
+                and self.temperature == 1.0)
+
+    def apply(self, z):
+        """Returns (z', dz'/dz), both float64 arrays shaped like z."""
+        x = z * self.scale_mul / self.scale_div
+        dx = self.scale_mul / self.scale_div
+        if self.softcap > 0.0:
+            u = np.tanh(x / self.softcap)
+            x = self.softcap * u
+            d = dx * (1.0 - u * u)
+        else:
+            d = np.full_like(z, dx)
+        return x / self.temperature, d / self.temperature
+
+
+IDENTITY = Transform()
 
 
 def _f64(x) -> np.ndarray:
@@ -75,7 +111,7 @@ def logsumexp_rows(z: np.ndarray) -> np.ndarray:
     return mx + np.log(np.exp(z - mx[:, None]).sum(axis=1))
 
 
-def selective_logp(hidden, W, ids, row_block: int = ROW_BLOCK):
+def selective_logp(hidden, W, ids, row_block: int = ROW_BLOCK, xf: Transform = IDENTITY):
     """Selective log-softmax of the sampled tokens, from hidden states.
 
     ("GRPO with 7x longer context", section "Flattened sequence length
@@ -94,6 +130,8 @@ def selective_logp(hidden, W, ids, row_block: int = ROW_BLOCK):
     for r0 in range(0, n, row_block):
         r1 = min(n, r0 + row_block)
         z = logits_rows(h[r0:r1], Wd)
+        if not xf.identity:
+            z = xf.apply(z)[0]
         l = logsumexp_rows(z)
         lse[r0:r1] = l
         logp[r0:r1] = z[np.arange(r1 - r0), y[r0:r1]] - l
@@ -156,7 +194,7 @@ def grpo_loss(logp, old, ref, adv_per_seq, mask, seq_len, eps_low=0.2,
     return L, g, loss_tok, M
 
 
-def grad_hidden(hidden, W, ids, g, row_block: int = ROW_BLOCK):
+def grad_hidden(hidden, W, ids, g, row_block: int = ROW_BLOCK, xf: Transform = IDENTITY):
     """dH_t = g_t * (W[y_t] - sum_v softmax(z_t)_v W_v), float64.
 
     ("GRPO with 7x longer context", section "Offloading activations for
@@ -176,29 +214,37 @@ def grad_hidden(hidden, W, ids, g, row_block: int = ROW_BLOCK):
         if rows.size == 0:
             continue
         z = logits_rows(h[rows], Wd)
-        p = np.exp(z - logsumexp_rows(z)[:, None])
-        dH[rows] = gd[rows, None] * (Wd[y[rows]] - p @ Wd)
+        if xf.identity:
+            p = np.exp(z - logsumexp_rows(z)[:, None])
+            dH[rows] = gd[rows, None] * (Wd[y[rows]] - p @ Wd)
+        else:
+            # d logp_t / d z_v = (onehot_v(y_t) - softmax(z')_v) f'(z_v)
+            zt, dz = xf.apply(z)
+            jac = -np.exp(zt - logsumexp_rows(zt)[:, None])
+            jac[np.arange(len(rows)), y[rows]] += 1.0
+            dH[rows] = gd[rows, None] * ((jac * dz) @ Wd)
     return dH
 
 
 def loss_fwd_bwd(hidden, W, ids, mask, old, ref, adv_per_seq, seq_len,
-                 eps_low=0.2, eps_high=0.2, beta=0.001, loss_denominator=0.0):
+                 eps_low=0.2, eps_high=0.2, beta=0.001, loss_denominator=0.0,
+                 xf: Transform = IDENTITY):
     """The whole path: logp, the loss, and the gradient to the hidden states.
 
     Returns a dict with L, logp (masked rows 0), lse, g, dH, M.
     """
     m = _f64(mask)
-    logp, lse = selective_logp(hidden, W, ids)
+    logp, lse = selective_logp(hidden, W, ids, xf=xf)
     logp = np.where(m > 0, logp, 0.0)
     L, g, loss_tok, M = grpo_loss(logp, old, ref, adv_per_seq, mask, seq_len,
                                   eps_low, eps_high, beta, loss_denominator)
-    dH = grad_hidden(hidden, W, ids, g)
+    dH = grad_hidden(hidden, W, ids, g, xf=xf)
     return {"L": L, "logp": logp, "lse": lse, "g": g, "dH": dH, "M": M,
             "loss_tok": loss_tok}
 
 
 def rows_fwd_bwd(hidden, W, ids, rows, old, ref, adv_per_seq, seq_len, M,
-                 eps_low=0.2, eps_high=0.2, beta=0.001):
+                 eps_low=0.2, eps_high=0.2, beta=0.001, xf: Transform = IDENTITY):
     """logp, g and dH for a chosen set of (unmasked) rows only.
 
     Given the loss denominator M, everything about a row depends on that row
@@ -207,10 +253,10 @@ def rows_fwd_bwd(hidden, W, ids, rows, old, ref, adv_per_seq, seq_len, M,
     rows = np.asarray(rows, dtype=np.int64)
     h = _f64(hidden)[rows] if not hasattr(hidden, "detach") else _f64(hidden[rows])
     y = np.asarray(ids, dtype=np.int64)[rows]
-    logp, lse = selective_logp(h, W, y)
+    logp, lse = selective_logp(h, W, y, xf=xf)
     A = _f64(adv_per_seq)[rows // seq_len]
     _, dloss_tok, _, _ = token_terms(logp, _f64(old)[rows], _f64(ref)[rows], A,
                                      eps_low, eps_high, beta)
     g = dloss_tok / M
-    dH = grad_hidden(h, W, y, g)
+    dH = grad_hidden(h, W, y, g, xf=xf)
     return {"logp": logp, "lse": lse, "g": g, "dH": dH}

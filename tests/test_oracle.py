@@ -391,3 +391,85 @@ def test_generator_is_deterministic():
     b = synth.make_problem("tiny", seed=9)
     assert torch.equal(a.hidden, b.hidden) and torch.equal(a.weight, b.weight)
     assert torch.equal(a.ids, b.ids) and torch.equal(a.adv, b.adv)
+
+
+# ------------------------------------------------------ logit transforms ---
+
+def test_temperature_and_scale_equal_rescaled_weights():
+    # z / T = h . (W / T) and z * a / b = h . (W * a / b): exact identities.
+    h = _rand((7, 12), 40)
+    W = _rand((60, 12), 41, 0.5)
+    y = np.arange(7) * 8
+    lp_t, _ = oracle.selective_logp(h, W, y, xf=oracle.Transform(temperature=0.7))
+    lp_w, _ = oracle.selective_logp(h, W / 0.7, y)
+    assert np.allclose(lp_t, lp_w, rtol=0, atol=1e-12)
+    lp_s, _ = oracle.selective_logp(h, W, y, xf=oracle.Transform(scale_mul=3.0, scale_div=2.0))
+    lp_w2, _ = oracle.selective_logp(h, W * 1.5, y)
+    assert np.allclose(lp_s, lp_w2, rtol=0, atol=1e-12)
+
+
+def test_softcap_saturation_closed_form():
+    # Two entries with logits far beyond the cap: z' = +-cap / T, so
+    # logp(y=0) = -log1p(exp(-2 cap / T)).
+    cap, T = 5.0, 0.8
+    h = np.array([[1.0, 0.0]])
+    W = np.array([[1e4, 0.0], [-1e4, 0.0]])
+    lp, _ = oracle.selective_logp(h, W, [0], xf=oracle.Transform(softcap=cap, temperature=T))
+    assert abs(lp[0] - (-math.log1p(math.exp(-2 * cap / T)))) < 1e-14
+
+
+def test_large_softcap_tends_to_identity():
+    h = _rand((5, 10), 42)
+    W = _rand((30, 10), 43, 0.3)
+    y = np.arange(5)
+    a, _ = oracle.selective_logp(h, W, y)
+    b, _ = oracle.selective_logp(h, W, y, xf=oracle.Transform(softcap=1e7))
+    assert np.allclose(a, b, rtol=0, atol=1e-11)
+
+
+def test_transform_matches_torch_fp64():
+    h = _rand((6, 16), 44)
+    W = _rand((50, 16), 45, 0.8)
+    y = np.random.default_rng(46).integers(0, 50, 6)
+    xf = oracle.Transform(scale_mul=1.5, scale_div=2.0, softcap=3.0, temperature=0.6)
+    lp, _ = oracle.selective_logp(h, W, y, xf=xf)
+    z = torch.tensor(h) @ torch.tensor(W).T
+    zt = 3.0 * torch.tanh(z * 0.75 / 3.0) / 0.6
+    ref = torch.log_softmax(zt, 1).gather(1, torch.tensor(y)[:, None])[:, 0]
+    assert np.allclose(lp, ref.numpy(), rtol=0, atol=1e-12)
+
+
+def _L_of_h_xf(h, W, y, mask, old, ref, adv, T, eps, beta, xf):
+    lp, _ = oracle.selective_logp(h, W, y, xf=xf)
+    return oracle.grpo_loss(lp, old, ref, adv, mask, T, eps, eps, beta)[0]
+
+
+@pytest.mark.parametrize("xf", [
+    oracle.Transform(softcap=2.0),
+    oracle.Transform(scale_mul=2.0, scale_div=3.0, softcap=1.5, temperature=0.7),
+    oracle.Transform(temperature=1.3)])
+def test_transformed_dH_matches_finite_differences(xf):
+    rng = np.random.default_rng(47)
+    N, D, V, T = 6, 8, 40, 3
+    h = rng.standard_normal((N, D))
+    W = rng.standard_normal((V, D)) * 0.5
+    y = rng.integers(0, V, N)
+    mask = np.ones(N)
+    lp, _ = oracle.selective_logp(h, W, y, xf=xf)
+    old = lp + rng.normal(0, 0.1, N)
+    ref = lp + rng.normal(0, 0.1, N)
+    adv = rng.standard_normal(N // T)
+    out = oracle.loss_fwd_bwd(h, W, y, mask, old, ref, adv, T, 0.2, 0.2, 0.05, xf=xf)
+    fd = np.zeros_like(h)
+    step = 1e-6
+    for t in range(N):
+        for d in range(D):
+            hp, hm = h.copy(), h.copy()
+            hp[t, d] += step
+            hm[t, d] -= step
+            fd[t, d] = (_L_of_h_xf(hp, W, y, mask, old, ref, adv, T, 0.2, 0.05, xf)
+                        - _L_of_h_xf(hm, W, y, mask, old, ref, adv, T, 0.2, 0.05, xf)) / (2 * step)
+    assert np.linalg.norm(fd - out["dH"]) / np.linalg.norm(out["dH"]) < 1e-6
+    # A backward that forgets the transform's derivative is caught.
+    no_chain = oracle.grad_hidden(h, W, y, out["g"])
+    assert np.linalg.norm(fd - no_chain) / np.linalg.norm(fd) > 1e-2
