@@ -34,7 +34,9 @@ class GrpoParams(ctypes.Structure):
     _fields_ = [("eps_low", ctypes.c_float), ("eps_high", ctypes.c_float),
                 ("beta", ctypes.c_float), ("loss_denominator", ctypes.c_float),
                 ("chunk_tokens", ctypes.c_int32), ("vocab_block", ctypes.c_int32),
-                ("flags", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
+                ("flags", ctypes.c_uint32), ("reserved", ctypes.c_uint32),
+                ("logit_scale_multiply", ctypes.c_float), ("logit_scale_divide", ctypes.c_float),
+                ("logit_softcapping", ctypes.c_float), ("temperature", ctypes.c_float)]
 
 
 class GrpoPlanInfo(ctypes.Structure):
@@ -93,12 +95,17 @@ def status_string(code: int) -> str:
 
 
 def make_params(eps_low=0.2, eps_high=0.2, beta=0.001, loss_denominator=0.0,
-                chunk_tokens=0, vocab_block=0) -> GrpoParams:
+                chunk_tokens=0, vocab_block=0, *, logit_scale_multiply=0.0,
+                logit_scale_divide=0.0, logit_softcapping=0.0, temperature=0.0,
+                flags=0) -> GrpoParams:
     p = GrpoParams()
     lib.grpo_default_params(ctypes.byref(p))
     p.eps_low, p.eps_high, p.beta = eps_low, eps_high, beta
     p.loss_denominator = loss_denominator
     p.chunk_tokens, p.vocab_block = chunk_tokens, vocab_block
+    p.logit_scale_multiply, p.logit_scale_divide = logit_scale_multiply, logit_scale_divide
+    p.logit_softcapping, p.temperature = logit_softcapping, temperature
+    p.flags = flags
     return p
 
 

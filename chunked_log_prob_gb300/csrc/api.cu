@@ -130,7 +130,30 @@ int check_params(const grpo_params* p) {
     return GRPO_ERR_INVALID_ARG;
   if (!(p->eps_low >= 0.f) || !(p->eps_high >= 0.f) || !(p->beta >= 0.f))
     return GRPO_ERR_INVALID_ARG;
+  if (!(p->logit_scale_multiply >= 0.f) || !(p->logit_scale_divide >= 0.f) ||
+      !(p->logit_softcapping >= 0.f) || !(p->temperature >= 0.f))
+    return GRPO_ERR_INVALID_ARG;
   return GRPO_OK;
+}
+
+// Logit transform constants for the epilogues (see TileArgs::xmode).
+void set_transform(TileArgs* a, const grpo_params* p) {
+  a->xmode = 0;
+  a->k0 = a->k1 = a->k2 = 1.f;
+  if (!p) return;
+  const double mul = p->logit_scale_multiply > 0.f ? p->logit_scale_multiply : 1.0;
+  const double div = p->logit_scale_divide > 0.f ? p->logit_scale_divide : 1.0;
+  const double temp = p->temperature > 0.f ? p->temperature : 1.0;
+  const double cap = p->logit_softcapping;
+  const double scale = mul / div;
+  a->k0 = static_cast<float>(scale / temp);
+  if (cap > 0.0) {
+    a->xmode = 2;
+    a->k1 = static_cast<float>(scale / cap);
+    a->k2 = static_cast<float>(cap / temp);
+  } else if (scale / temp != 1.0) {
+    a->xmode = 1;
+  }
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -244,13 +267,14 @@ TileArgs base_args(const Layout& L, const Ws& w) {
 // Forward logit GEMM: per-split (max, sum-exp) and z_y for every row of the
 // row blocks in `rb_list` (all row blocks when it is null).
 int run_forward(const void* hidden, const void* W, const int32_t* ids, const uint8_t* mask,
-                const int* rb_list, const int* n_active, const Layout& L, const Ws& w, int sms,
-                int* splits_out, cudaStream_t st) {
+                const int* rb_list, const int* n_active, const grpo_params* prm,
+                const Layout& L, const Ws& w, int sms, int* splits_out, cudaStream_t st) {
   CUtensorMap map_h, map_w;
   if (!encode_2d(&map_h, hidden, L.D, L.n, L.D, BK, BM) ||
       !encode_2d(&map_w, W, L.D, L.V, L.D, BK, BN))
     return GRPO_ERR_CUDA;
   TileArgs a = base_args(L, w);
+  set_transform(&a, prm);
   a.n_total = L.n;
   a.n_rb = static_cast<int>(L.nr / BM);
   a.rb_offset = 0;
@@ -280,7 +304,8 @@ int run_forward(const void* hidden, const void* W, const int32_t* ids, const uin
 // entries: G block, then dH accumulation, per vocab block. Chunks past the
 // device-side list length find no work and return at once.
 int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH,
-                 const Layout& L, const Ws& w, int sms, cudaStream_t st) {
+                 const grpo_params* prm, const Layout& L, const Ws& w, int sms,
+                 cudaStream_t st) {
   CUtensorMap map_h, map_w_k, map_w_mn;
   if (!encode_2d(&map_h, hidden, L.D, L.n, L.D, BK, BM) ||
       !encode_2d(&map_w_k, W, L.D, L.V, L.D, BK, BN) ||
@@ -296,6 +321,7 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
       const int ntile = static_cast<int>(cdiv(width, BN));
       // (1) G = g (onehot - softmax) for this chunk x vocab block, bf16.
       TileArgs a = base_args(L, w);
+      set_transform(&a, prm);
       a.n_total = L.n;
       a.n_rb = n_rb;
       a.rb_offset = rb0;
@@ -390,7 +416,7 @@ int grpo_logp_fwd(const void* hidden, const void* W, const int32_t* ids, float* 
   if (L.n == 0) return GRPO_OK;
   Ws w = carve(workspace, L);
   int splits = 1;
-  if ((r = run_forward(hidden, W, ids, nullptr, nullptr, nullptr, L, w, sms, &splits, st)) != GRPO_OK) return r;
+  if ((r = run_forward(hidden, W, ids, nullptr, nullptr, nullptr, params, L, w, sms, &splits, st)) != GRPO_OK) return r;
   FinalizeArgs f;
   std::memset(&f, 0, sizeof(f));
   f.n = L.n;
@@ -448,8 +474,8 @@ int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
       launch_zero_padding_blocks(mask, L.n, n_rb_total, L.D, dH, sms, st) != cudaSuccess)
     return GRPO_ERR_CUDA;
   int splits = 1;
-  if ((r = run_forward(hidden, W, ids, mask, w.rb_list, w.n_active, L, w, sms, &splits, st)) !=
-      GRPO_OK)
+  if ((r = run_forward(hidden, W, ids, mask, w.rb_list, w.n_active, &prm, L, w, sms, &splits,
+                       st)) != GRPO_OK)
     return r;
   FinalizeArgs f;
   std::memset(&f, 0, sizeof(f));
@@ -480,7 +506,7 @@ int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
   f.loss_out = loss;
   f.status = w.status;
   if (launch_finalize(f, st) != cudaSuccess) return GRPO_ERR_CUDA;
-  return run_backward(hidden, W, ids, dH, L, w, sms, st);
+  return run_backward(hidden, W, ids, dH, &prm, L, w, sms, st);
 }
 
 int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_info* info) {
@@ -597,7 +623,7 @@ extern "C" int grpo_logp_fwd_noalloc(const void* hidden, const void* W, const in
   w.G = nullptr;  // beyond the forward's part of the scratch; never used here
   w.acc = nullptr;
   int splits = 1;
-  if ((r = run_forward(hidden, W, ids, nullptr, nullptr, nullptr, L, w, sms, &splits, st)) != GRPO_OK) return r;
+  if ((r = run_forward(hidden, W, ids, nullptr, nullptr, nullptr, nullptr, L, w, sms, &splits, st)) != GRPO_OK) return r;
   FinalizeArgs f;
   std::memset(&f, 0, sizeof(f));
   f.n = L.n;

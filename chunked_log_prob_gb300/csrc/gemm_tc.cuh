@@ -50,6 +50,10 @@ struct TileArgs {
   int v0;          // BWDG/DH: first vocab column of the block (0 for FWD)
   int vocab;
   int hidden;
+  // Logit transform z' = f(S) applied before the log-softmax (FWD, BWDG):
+  //   xmode 0: z' = S;  1: z' = k0 S;  2: z' = k2 tanh(k1 S), f'(S) = k0 (1 - tanh^2)
+  int xmode;
+  float k0, k1, k2;
   const int32_t* ids;    // indexed by global row
   const uint8_t* mask;   // FWD: optional; masked rows' ids are never read
   // MODE_FWD
@@ -109,6 +113,25 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (clock64() - t0 > kWaitLimitCycles) return;
+  }
+}
+
+// tanh(x) = 1 - 2 / (1 + e^{2x}), with the SFU exponential; absolute error a
+// few 1e-7 over the whole range, saturating cleanly to +-1.
+__device__ __forceinline__ float tanh_sfu(float x) {
+  const float e = ex2(x * 2.8853900817779268f);  // e^{2x} = 2^{2x log2 e}
+  return 1.f - __fdividef(2.f, 1.f + e);
+}
+
+// Applies the logit transform to 32 raw logits in place; returns nothing when
+// the transform is the identity (xmode 0).
+__device__ __forceinline__ void logit_transform(const TileArgs& a, float (&v)[32]) {
+  if (a.xmode == 1) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= a.k0;
+  } else if (a.xmode == 2) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = a.k2 * tanh_sfu(v[j] * a.k1);
   }
 }
 
@@ -305,6 +328,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (col0 >= args.vocab) break;  // warp-uniform
             float v[32];
             tmem_ld32(tbase + c * 32, v);
+            logit_transform(args, v);
             if (col0 + 32 > args.vocab) {
 #pragma unroll
               for (int j = 0; j < 32; ++j)
@@ -344,13 +368,32 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             float v[32];
             tmem_ld32(tbase + c * 32, v);
             const float ng = -gval;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = ng * ex2(fmaf(v[j], kLog2e, -lse2));
             const unsigned off = static_cast<unsigned>(y - col0);
-            if (off < 32u) {
+            if (args.xmode != 2) {
+              // z' = k S (k = 1 without a transform): G = k g (onehot - p).
+              const float k = args.xmode == 1 ? args.k0 : 1.f;
+              const float kl = k * kLog2e;
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (static_cast<unsigned>(j) == off) v[j] += gval;
+              for (int j = 0; j < 32; ++j) v[j] = ng * ex2(fmaf(v[j], kl, -lse2));
+              if (off < 32u) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (static_cast<unsigned>(j) == off) v[j] += gval;
+              }
+              if (args.xmode == 1) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] *= k;
+              }
+            } else {
+              // Softcap: z' = k2 u, u = tanh(k1 S), dz'/dS = k0 (1 - u^2).
+              const float k2l = args.k2 * kLog2e;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float u = tanh_sfu(v[j] * args.k1);
+                const float d = args.k0 * fmaf(-u, u, 1.f);
+                const float pg = ng * ex2(fmaf(u, k2l, -lse2));
+                v[j] = (static_cast<unsigned>(j) == off ? pg + gval : pg) * d;
+              }
             }
             if (col0 + 32 > args.vocab) {
 #pragma unroll

@@ -74,15 +74,26 @@ typedef struct grpo_params {
   int32_t vocab_block;    /* vocab columns per backward block; 0 = automatic   */
   uint32_t flags;         /* must be 0                                         */
   uint32_t reserved;      /* must be 0                                         */
+  /* Logit transforms ("GRPO with 7x longer context", the options of the
+   * selective log-softmax call: logit scale multiply/divide, softcapping,
+   * temperature), applied to the raw logit z in that order:
+   *   z' = s(z * logit_scale_multiply / logit_scale_divide) / temperature,
+   *   s(x) = logit_softcapping * tanh(x / logit_softcapping)  (x when 0).
+   * logp and the loss use z'; dH carries dz'/dz. 0 in any field = unused. */
+  float logit_scale_multiply;
+  float logit_scale_divide;
+  float logit_softcapping;
+  float temperature;
 } grpo_params;
 
 /* Defaults: eps 0.2/0.2, beta 0.001 (the pages' corrected GRPO default,
  * "How does Unsloth implement GRPO", section "Corrected hyperparameters"),
- * token-mean denominator, automatic chunking. Host only. */
+ * token-mean denominator, automatic chunking, no logit transform. Host only. */
 void grpo_default_params(grpo_params* params);
 
-/* Bytes of device workspace that grpo_logp_fwd and grpo_loss_fwd_bwd need for
- * this shape and these params. Host only, touches no GPU. The size grows with
+/* Bytes of device workspace that grpo_loss_fwd_bwd needs for this shape and
+ * these params (enough for grpo_logp_fwd too, which needs only the part that
+ * does not depend on the chunking). Host only, touches no GPU. The size grows with
  * N (a few fp32 per token) and with chunk_tokens x vocab_block, never with
  * N x V. Returns GRPO_OK or GRPO_ERR_INVALID_ARG / _UNSUPPORTED_SHAPE. */
 int grpo_workspace_size(const grpo_shape* shape, const grpo_params* params, size_t* bytes);
@@ -93,7 +104,7 @@ int grpo_workspace_size(const grpo_shape* shape, const grpo_params* params, size
  * for every t in [0, N). logits are accumulated and reduced in fp32.
  *   logp:        fp32 [N] output (required)
  *   lse_or_null: fp32 [N] output, or NULL
- * params: only chunk/vocab fields are read (may be NULL for defaults).
+ * params: the chunk/vocab and logit-transform fields are read (NULL = defaults).
  * ids outside [0, V) give logp = NaN and GRPO_ERR_BAD_TOKEN_ID in the device
  * status word. */
 int grpo_logp_fwd(const void* hidden, const void* W, const int32_t* ids, float* logp,

@@ -231,3 +231,32 @@ def test_padding_blocks_are_skipped_and_zeroed(clp, chunk):
     st = clp.grpo_read_device_status(ws)
     got = (loss.item(), logp.cpu().double().numpy(), dH.cpu().double().numpy(), st)
     check(got, want, p.mask, f"padding chunk={chunk}")
+
+
+XFORMS = [
+    dict(temperature=0.7),
+    dict(logit_softcapping=30.0),
+    dict(logit_softcapping=2.0),
+    dict(logit_scale_multiply=1.5, logit_scale_divide=2.0, logit_softcapping=3.0,
+         temperature=0.9),
+    dict(logit_scale_multiply=0.5),
+]
+
+
+@pytest.mark.parametrize("kw", XFORMS)
+def test_logit_transforms(clp, kw):
+    # Logit std ~2.8 (W ~ N(0, 0.2^2), D = 200) so that softcaps of 2-3 saturate.
+    p = synth.make_problem("tiny", seed=31, T=75, prompts=1, G=4, D=200, V=3000,
+                           lengths=(20, 75), weight_std=0.2)
+    xf = oracle.Transform(scale_mul=kw.get("logit_scale_multiply", 1.0),
+                          scale_div=kw.get("logit_scale_divide", 1.0),
+                          softcap=kw.get("logit_softcapping", 0.0),
+                          temperature=kw.get("temperature", 1.0))
+    base, _ = oracle.selective_logp(p.hidden, p.weight, p.ids.numpy(), xf=xf)
+    old, ref = p.old_ref(torch.from_numpy(base))
+    want = oracle.loss_fwd_bwd(p.hidden, p.weight, p.ids.numpy(), p.mask.numpy(), old, ref,
+                               p.adv, p.seq_len, p.eps_low, p.eps_high, p.beta, xf=xf)
+    params = clp.make_params(chunk_tokens=128, vocab_block=1024, **kw)
+    check(gpu_loss(clp, p, old, ref, params), want, p.mask, f"transform {kw}")
+    lp, _ = clp.grpo_logp_fwd(_to(p.hidden), _to(p.weight), _to(p.ids), params=params)
+    assert np.abs(lp.cpu().double().numpy() - base).max() <= LOGP_TOL
