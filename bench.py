@@ -42,8 +42,15 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama-3.1-8b")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="override tokens per completion (small profiling cases)")
     ap.add_argument("--chunk-tokens", type=int, default=0)
     ap.add_argument("--vocab-block", type=int, default=0)
+    ap.add_argument("--backward", default="stored", choices=["stored", "recompute"],
+                    help="stored: the backward reads fp16 logits kept per chunk (4NDV "
+                         "executed); recompute: it recomputes the logit tiles (6NDV)")
+    ap.add_argument("--no-variant", action="store_true",
+                    help="skip timing the other backward variant")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -186,23 +193,36 @@ def run_ours(args):
     import chunked_log_prob_gb300 as clp
     import synth
 
-    p = synth.make_problem(args.workload, seed=args.seed + rank, device=dev)
+    over = {"T": args.seq_len} if args.seq_len > 0 else {}
+    if args.seq_len > 0 and synth.WORKLOADS[args.workload]["lengths"] is not None:
+        lo, hi = synth.WORKLOADS[args.workload]["lengths"]
+        over["lengths"] = (min(lo, args.seq_len), args.seq_len)
+    p = synth.make_problem(args.workload, seed=args.seed + rank, device=dev, **over)
+    torch.cuda.empty_cache()  # drop the generator's fp32 temporaries
     N, D, V, T = p.n_tokens, p.hidden_size, p.vocab, p.seq_len
-    params = clp.make_params(p.eps_low, p.eps_high, p.beta, 0.0, args.chunk_tokens,
-                             args.vocab_block)
+    stored = args.backward == "stored"
+
+    def make(flag):
+        return clp.make_params(p.eps_low, p.eps_high, p.beta, 0.0, args.chunk_tokens,
+                               args.vocab_block, flags=flag)
+
+    params = make(1 if stored else 0)
+    other = make(0 if stored else 1)
     plan = clp.grpo_get_plan(N, D, V, T, params)
-    ws = clp.alloc_workspace(N, D, V, T, params, dev)
+    ws_bytes = max(clp.grpo_workspace_size(N, D, V, T, params),
+                   0 if args.no_variant else clp.grpo_workspace_size(N, D, V, T, other))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     # old/ref: the policy's own log-probs (as a GRPO trainer gets them) + noise.
-    base, _ = clp.grpo_logp_fwd(p.hidden, p.weight, p.ids, workspace=ws)
+    base, _ = clp.grpo_logp_fwd(p.hidden, p.weight, p.ids, params=params, workspace=ws)
     old, ref = p.old_ref(base)
     valid = p.n_valid
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     logp = torch.empty(N, dtype=torch.float32, device=dev)
     dH = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
 
-    def step():
+    def step(prm=params):
         clp.grpo_loss_fwd_bwd(p.hidden, p.weight, p.ids, p.mask, old, ref, p.adv, T,
-                              params=params, workspace=ws, loss=loss, logp=logp, dH=dH)
+                              params=prm, workspace=ws, loss=loss, logp=logp, dH=dH)
 
     stream = torch.cuda.current_stream(dev)
     for _ in range(max(args.warmup, 3)):
@@ -233,16 +253,39 @@ def run_ours(args):
         dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
     ms_max = float(ms_t.item())
 
+    # The other backward variant on the same inputs (reported beside the headline).
+    variant = None
+    if not args.no_variant:
+        for _ in range(3):
+            step(other)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step(other)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        v_ms = torch.tensor([ev0.elapsed_time(ev1) / args.steps], device=dev, dtype=torch.float64)
+        if world > 1:
+            dist.all_reduce(v_ms, op=dist.ReduceOp.MAX)
+        v_ms = float(v_ms.item())
+        v_exec = (6.0 if stored else 4.0) * D * V * p.n_valid
+        variant = {"backward": "recomputed logits" if stored else "stored fp16 logits",
+                   "ms_per_step": v_ms, "value": world * p.n_valid / (v_ms / 1e3),
+                   "tflops_executed": v_exec / (v_ms / 1e3) / 1e12,
+                   "launches_per_call": clp.grpo_get_plan(N, D, V, T, other)["launches_loss"]}
+
     # Forward alone (one logit GEMM launch + finalize), timed on the same stream.
     fwd_ms = None
     if rank == 0:
         for _ in range(3):
-            clp.grpo_logp_fwd(p.hidden, p.weight, p.ids, workspace=ws, logp=logp)
+            clp.grpo_logp_fwd(p.hidden, p.weight, p.ids, params=params, workspace=ws, logp=logp)
         torch.cuda.synchronize(dev)
         ev0.record(stream)
         reps = max(5, args.steps // 2)
         for _ in range(reps):
-            clp.grpo_logp_fwd(p.hidden, p.weight, p.ids, workspace=ws, logp=logp)
+            clp.grpo_logp_fwd(p.hidden, p.weight, p.ids, params=params, workspace=ws, logp=logp)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
         fwd_ms = ev0.elapsed_time(ev1) / reps
@@ -297,6 +340,10 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
     fl = flops_per_token(D, V) * valid
     tflops = fl / (ms_max / 1e3) / 1e12
+    # Executed tensor work: 6NDV with the recomputed backward, 4NDV when the
+    # backward reads the stored fp16 logits instead of a second logit GEMM.
+    fl_exec = (4.0 if stored else 6.0) * D * V * valid
+    tflops_exec = fl_exec / (ms_max / 1e3) / 1e12
     peak_sus = peaks["bf16_tflops_sustained"]
     peak_burst = peaks["bf16_tflops"]
     out = {
@@ -321,15 +368,18 @@ def run_ours(args):
             "parallelism": "replicas: one independent batch per GPU" if world > 1 else "1 GPU",
         },
         "tflops": tflops,
-        "pct_bf16_peak": 100.0 * tflops / peak_sus,
+        "tflops_executed": tflops_exec,
+        "pct_bf16_peak": 100.0 * tflops_exec / peak_sus,
+        "backward": "stored fp16 logits" if stored else "recomputed logits",
+        "variant": variant,
         "roofline": {
-            "bound": "tensor", "achieved": tflops, "peak": peak_sus, "unit": "TFLOP/s",
-            "frac": tflops / peak_sus, "frac_of_burst_peak": tflops / peak_burst,
+            "bound": "tensor", "achieved": tflops_exec, "peak": peak_sus, "unit": "TFLOP/s",
+            "frac": tflops_exec / peak_sus, "frac_of_burst_peak": tflops_exec / peak_burst,
+            "counted_tflops_6NDV": tflops,
             "peak_source": f"{peak_src} bf16 sustained (cuBLAS loop)",
-            "kernel": "grpo_loss_fwd_bwd: %d launches per call (logit GEMM, finalize, "
-                      "%d x %d backward G/dH GEMM pairs)" % (
-                          plan["launches_loss"], plan["n_chunks"], plan["n_vocab_blocks"]),
-            "flops_per_call": fl, "traffic": None,
+            "kernel": "grpo_loss_fwd_bwd: %d launches per call, %d chunks x %d vocab blocks" % (
+                plan["launches_loss"], plan["n_chunks"], plan["n_vocab_blocks"]),
+            "flops_per_call": fl_exec, "traffic": None,
         },
         "fwd_only": None if fwd_ms is None else {
             "ms": fwd_ms, "tflops": 2.0 * D * V * N / (fwd_ms / 1e3) / 1e12,

@@ -18,6 +18,8 @@ namespace {
 constexpr int kMaxSplits = 32;          // forward vocab splits (per-row partials)
 constexpr int kMaxAutoChunkBlocks = 32;  // automatic backward chunk <= 4096 rows
 constexpr int kAutoVocabBlock = 32768;   // automatic backward vocab block
+constexpr int kMaxStoredChunkBlocks = 64;                   // stored-logit chunk bound
+constexpr size_t kMaxStoredChunkBytes = size_t(2) << 30;    // 2 GiB of fp16 logits
 constexpr int kSplitsTarget = 8;        // forward vocab splits per raster group
 constexpr size_t kHeaderBytes = 16384;   // status, counters, loss partials
 constexpr int kMaxDevices = 64;
@@ -34,13 +36,15 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
 struct Layout {
+  bool stored;      // stored-logit backward (GRPO_FLAG_STORED_LOGITS)
+  long long ldS;    // stored mode: elements per row of the chunk logit block
   long long n, nr;  // rows, rows rounded up to BM
   int T, D, V;
   int nvt;          // vocab tiles
   int chunk_rows;   // backward chunk (multiple of BM)
   int vblock;       // backward vocab block (multiple of BN)
   bool need_acc;    // more than one vocab block -> fp32 dH accumulator
-  size_t off_pm, off_ps, off_zy, off_lse, off_g, off_rbl, off_G, off_acc, total;
+  size_t off_pm, off_ps, off_zy, off_lse, off_g, off_rbl, off_lt, off_G, off_acc, total;
 };
 
 int auto_chunk_blocks(long long n_rb_total, int n_dt, int sms) {
@@ -61,7 +65,69 @@ int auto_chunk_blocks(long long n_rb_total, int n_dt, int sms) {
   return best;
 }
 
+// Stored-logit backward: largest chunk (row blocks) whose fp16 logit block
+// stays within kMaxStoredChunkBytes.
+int stored_max_blocks(long long ldS) {
+  const long long by_mem = static_cast<long long>(kMaxStoredChunkBytes / (BM * ldS * 2));
+  return static_cast<int>(std::max(1LL, std::min<long long>(kMaxStoredChunkBlocks, by_mem)));
+}
+
+// Fraction of SM time a launch of `units` equal units keeps busy.
+double wave_eff(long long units, int sms) {
+  const long long waves = cdiv(units, sms);
+  return static_cast<double>(units) / static_cast<double>(waves * sms);
+}
+
+// Forward vocab splits for a chunk of nrb row blocks: whole waves of
+// (row block x split) units, and splits of even length in vocab tiles.
+int stored_fwd_splits(int nrb, int nvt, int sms, double* eff_out) {
+  int best = 1;
+  double best_eff = -1.0;
+  for (int sp = 1; sp <= std::min(nvt, kMaxSplits); ++sp) {
+    const double even = (static_cast<double>(nvt) / sp) / static_cast<double>(cdiv(nvt, sp));
+    const double eff = wave_eff(static_cast<long long>(nrb) * sp, sms) * even;
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = sp;
+    }
+  }
+  if (eff_out) *eff_out = best_eff;
+  return best;
+}
+
+// Row blocks per chunk for the stored-logit backward. Each chunk runs a
+// forward launch of (row blocks x splits) units and a dH launch of
+// (row blocks x D tiles) units; the score is the ideal SM time of the whole
+// schedule (every chunk, including a shorter last one) over its wave-rounded
+// time, forward and dH weighted equally. Near-ties go to the larger chunk.
+int auto_stored_chunk_blocks(long long n_rb_total, int n_dt, int nvt, int sms, long long ldS) {
+  const int hi = static_cast<int>(std::min<long long>(n_rb_total, stored_max_blocks(ldS)));
+  int best = hi;
+  double best_score = -1.0;
+  for (int nrb = hi; nrb >= 1; --nrb) {
+    double ideal = 0.0, actual = 0.0;
+    for (long long r0 = 0; r0 < n_rb_total; r0 += nrb) {
+      const int n = static_cast<int>(std::min<long long>(nrb, n_rb_total - r0));
+      const int sp = stored_fwd_splits(n, nvt, sms, nullptr);
+      // forward: waves x tiles per unit (the longest unit sets the pace)
+      ideal += static_cast<double>(n) * nvt / sms;
+      actual += static_cast<double>(cdiv(static_cast<long long>(n) * sp, sms)) * cdiv(nvt, sp);
+      // dH: units of equal K; scaled to the forward's per-row work
+      ideal += static_cast<double>(n) * nvt / sms;
+      actual += static_cast<double>(cdiv(static_cast<long long>(n) * n_dt, sms)) * nvt / n_dt;
+    }
+    const double score = ideal / actual;
+    if (score > best_score + 0.005) {
+      best_score = score;
+      best = nrb;
+    }
+  }
+  return best;
+}
+
 int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
+  L->stored = p != nullptr && (p->flags & GRPO_FLAG_STORED_LOGITS) != 0;
+  L->ldS = cdiv(std::max(s->vocab, 1), 8) * 8;
   L->n = s->n_tokens;
   L->nr = cdiv(std::max<long long>(s->n_tokens, 1), BM) * BM;
   L->T = s->seq_len;
@@ -74,6 +140,11 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   long long crows;
   if (p && p->chunk_tokens > 0) {
     crows = cdiv(p->chunk_tokens, BM) * BM;
+  } else if (L->stored) {
+    crows = static_cast<long long>(
+                sms > 0 ? auto_stored_chunk_blocks(n_rb_total, n_dt, L->nvt, sms, L->ldS)
+                        : std::min<long long>(n_rb_total, stored_max_blocks(L->ldS))) *
+            BM;
   } else if (sms > 0) {
     crows = static_cast<long long>(auto_chunk_blocks(n_rb_total, n_dt, sms)) * BM;
   } else {  // sizing without a device: the largest automatic chunk
@@ -86,7 +157,8 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   vb = cdiv(vb, BN) * BN;
   vb = std::min<long long>(vb, static_cast<long long>(L->nvt) * BN);
   L->vblock = static_cast<int>(vb);
-  L->need_acc = L->vblock < L->V;
+  L->need_acc = !L->stored && L->vblock < L->V;
+  if (L->stored) L->vblock = static_cast<int>(L->ldS);
 
   size_t off = kHeaderBytes;
   const size_t part = static_cast<size_t>(kMaxSplits) * L->nr * sizeof(float);
@@ -96,6 +168,9 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   L->off_lse = off; off = align_up(off + L->nr * sizeof(float), 256);
   L->off_g = off; off = align_up(off + L->nr * sizeof(float), 256);
   L->off_rbl = off; off = align_up(off + (L->nr / BM) * sizeof(int), 256);
+  L->off_lt = off; off = align_up(off + L->nr * sizeof(double), 256);
+  // Backward chunk block: bf16 G [C x V_b] (recompute path) or the chunk's
+  // fp16 logits, rewritten in place as bf16 G [C x ldS] (stored path).
   L->off_G = off; off = align_up(off + static_cast<size_t>(L->chunk_rows) * L->vblock * 2, 256);
   L->off_acc = off;
   if (L->need_acc) off = align_up(off + static_cast<size_t>(L->chunk_rows) * L->D * 4, 256);
@@ -126,7 +201,8 @@ int check_shape(const grpo_shape* s, bool need_seq) {
 
 int check_params(const grpo_params* p) {
   if (!p) return GRPO_OK;
-  if (p->flags != 0 || p->reserved != 0 || p->chunk_tokens < 0 || p->vocab_block < 0)
+  if ((p->flags & ~GRPO_FLAG_STORED_LOGITS) != 0 || p->reserved != 0 || p->chunk_tokens < 0 ||
+      p->vocab_block < 0)
     return GRPO_ERR_INVALID_ARG;
   if (!(p->eps_low >= 0.f) || !(p->eps_high >= 0.f) || !(p->beta >= 0.f))
     return GRPO_ERR_INVALID_ARG;
@@ -190,7 +266,8 @@ int device_setup(int* sms) {
       d.status = GRPO_ERR_CUDA;
     } else if (major != 10 || minor != 3) {
       d.status = GRPO_ERR_UNSUPPORTED_DEVICE;
-    } else if (prepare_fwd_gemm() != cudaSuccess || prepare_bwd_gemms() != cudaSuccess) {
+    } else if (prepare_fwd_gemm() != cudaSuccess || prepare_bwd_gemms() != cudaSuccess ||
+               prepare_fwds_gemm() != cudaSuccess) {
       d.status = GRPO_ERR_CUDA;
     }
     if (d.status == GRPO_OK && g_encode == nullptr) {
@@ -230,6 +307,7 @@ struct Ws {
   unsigned* counter;
   double* msum;
   double* partials;
+  double* lt;
   int* n_active;
   int* rb_list;
   float *pm, *ps, *zy, *lse, *g, *acc;
@@ -245,6 +323,7 @@ Ws carve(void* ws, const Layout& L) {
   w.partials = reinterpret_cast<double*>(w.base + kOffPartials);
   w.n_active = reinterpret_cast<int*>(w.base + kOffActive);
   w.rb_list = reinterpret_cast<int*>(w.base + L.off_rbl);
+  w.lt = reinterpret_cast<double*>(w.base + L.off_lt);
   w.pm = reinterpret_cast<float*>(w.base + L.off_pm);
   w.ps = reinterpret_cast<float*>(w.base + L.off_ps);
   w.zy = reinterpret_cast<float*>(w.base + L.off_zy);
@@ -367,6 +446,122 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
   return GRPO_OK;
 }
 
+// Stored-logit path of a loss call, chunk by chunk over the active row
+// blocks: forward GEMM that also stores the chunk's fp16 logits; per-row
+// finish (lse, logp, token loss, g) rewriting the logits in place as bf16 G;
+// dH GEMM over the whole vocabulary. A closing kernel reduces the loss.
+int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint8_t* mask,
+               const float* old_logp, const float* ref_logp, const float* adv, float* loss,
+               float* logp_out, void* dH, const grpo_params* prm, const Layout& L, const Ws& w,
+               int sms, cudaStream_t st) {
+  CUtensorMap map_h, map_w_k, map_w_mn;
+  if (!encode_2d(&map_h, hidden, L.D, L.n, L.D, BK, BM) ||
+      !encode_2d(&map_w_k, W, L.D, L.V, L.D, BK, BN) ||
+      !encode_2d(&map_w_mn, W, L.D, L.V, L.D, 64, BK))
+    return GRPO_ERR_CUDA;
+  const int n_dt = static_cast<int>(cdiv(L.D, BN));
+  const int n_rb_total = static_cast<int>(L.nr / BM);
+  const int rb_per_chunk = L.chunk_rows / BM;
+  uint16_t* S = reinterpret_cast<uint16_t*>(w.G);
+  for (int rb0 = 0; rb0 < n_rb_total; rb0 += rb_per_chunk) {
+    const int n_rb = std::min(rb_per_chunk, n_rb_total - rb0);
+    const int splits = stored_fwd_splits(n_rb, L.nvt, sms, nullptr);
+    // (1) logits of the chunk: online LSE partials, z_y, fp16 copy.
+    TileArgs a = base_args(L, w);
+    set_transform(&a, prm);
+    a.n_total = L.n;
+    a.n_rb = n_rb;
+    a.rb_offset = rb0;
+    a.rb_list = w.rb_list;
+    a.n_active = w.n_active;
+    a.k_iters = static_cast<int>(cdiv(L.D, BK));
+    a.group_rows = n_rb;
+    a.n_cols = splits;
+    a.n_vtiles = L.nvt;
+    a.v0 = 0;
+    a.ids = ids;
+    a.mask = mask;
+    a.part_m = w.pm;
+    a.part_s = w.ps;
+    a.zy = w.zy;
+    a.part_ld = L.nr;
+    a.S = S;
+    a.ldS = L.ldS;
+    long long units = static_cast<long long>(n_rb) * splits;
+    if (launch_fwds_gemm(map_h, map_w_k, a, static_cast<int>(std::min<long long>(units, sms)),
+                         st) != cudaSuccess)
+      return GRPO_ERR_CUDA;
+    // (2) per-row finish; the chunk block becomes G.
+    GformArgs f;
+    std::memset(&f, 0, sizeof(f));
+    f.n_total = L.n;
+    f.n_rb = n_rb;
+    f.rb_offset = rb0;
+    f.rb_list = w.rb_list;
+    f.n_active = w.n_active;
+    f.splits = splits;
+    f.part_ld = L.nr;
+    f.vocab = L.V;
+    f.seq_len = L.T;
+    f.part_m = w.pm;
+    f.part_s = w.ps;
+    f.zy = w.zy;
+    f.ids = ids;
+    f.mask = mask;
+    f.old_logp = old_logp;
+    f.ref_logp = ref_logp;
+    f.adv = adv;
+    f.eps_low = prm->eps_low;
+    f.eps_high = prm->eps_high;
+    f.beta = prm->beta;
+    f.loss_den = prm->loss_denominator;
+    f.msum = w.msum;
+    f.logp_out = logp_out;
+    f.lt = w.lt;
+    f.S = S;
+    f.ldS = L.ldS;
+    f.xmode = a.xmode;
+    f.k0 = a.k0;
+    f.k2 = a.k2;
+    f.status = w.status;
+    if (launch_finalize_gform(f, n_rb * BM, st) != cudaSuccess) return GRPO_ERR_CUDA;
+    // (3) dH rows of the chunk = G W over the whole vocabulary.
+    CUtensorMap map_g;
+    if (!encode_2d(&map_g, S, L.V, static_cast<uint64_t>(n_rb) * BM, L.ldS, BK, BM))
+      return GRPO_ERR_CUDA;
+    TileArgs b = base_args(L, w);
+    b.n_total = L.n;
+    b.n_rb = n_rb;
+    b.rb_offset = rb0;
+    b.rb_list = w.rb_list;
+    b.n_active = w.n_active;
+    b.k_iters = static_cast<int>(cdiv(L.V, BK));
+    b.group_rows = group_rows_for(n_rb, sms);
+    b.n_cols = n_dt;
+    b.v0 = 0;
+    b.dH = static_cast<__nv_bfloat16*>(dH);
+    b.first = 1;
+    b.last = 1;
+    units = static_cast<long long>(n_rb) * n_dt;
+    if (launch_dh_gemm(map_g, map_w_mn, b, static_cast<int>(std::min<long long>(units, sms)),
+                       st) != cudaSuccess)
+      return GRPO_ERR_CUDA;
+  }
+  FinishArgs fin;
+  std::memset(&fin, 0, sizeof(fin));
+  fin.n = L.n;
+  fin.mask = mask;
+  fin.lt = w.lt;
+  fin.logp_out = logp_out;
+  fin.loss_den = prm->loss_denominator;
+  fin.msum = w.msum;
+  fin.block_partials = w.partials;
+  fin.counter = w.counter;
+  fin.loss_out = loss;
+  if (launch_finish_loss(fin, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  return GRPO_OK;
+}
+
 }  // namespace
 }  // namespace grpo
 
@@ -473,6 +668,9 @@ int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
   if (launch_row_plan(mask, L.n, n_rb_total, w.rb_list, w.n_active, w.msum, st) != cudaSuccess ||
       launch_zero_padding_blocks(mask, L.n, n_rb_total, L.D, dH, sms, st) != cudaSuccess)
     return GRPO_ERR_CUDA;
+  if (L.stored)
+    return run_stored(hidden, W, ids, mask, old_logp, ref_logp, adv, loss, logp_or_null, dH,
+                      &prm, L, w, sms, st);
   int splits = 1;
   if ((r = run_forward(hidden, W, ids, mask, w.rb_list, w.n_active, &prm, L, w, sms, &splits,
                        st)) != GRPO_OK)
@@ -528,7 +726,13 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
   const int grp = group_rows_for(n_rb, sms);
   info->fwd_splits = std::min(std::max(1, sms / grp), std::min(L.nvt, kMaxSplits));
   info->launches_logp = L.n > 0 ? 2 : 0;
-  info->launches_loss = L.n > 0 ? 4 + 2 * info->n_chunks * info->n_vocab_blocks : 0;
+  info->launches_loss = L.n <= 0 ? 0
+                      : L.stored ? 3 + 3 * info->n_chunks
+                                 : 4 + 2 * info->n_chunks * info->n_vocab_blocks;
+  if (L.stored) {
+    info->n_vocab_blocks = 1;
+    info->fwd_splits = stored_fwd_splits(L.chunk_rows / BM, L.nvt, sms, nullptr);
+  }
   info->workspace_bytes = std::max(L.total, Lmax.total);
   return GRPO_OK;
 }

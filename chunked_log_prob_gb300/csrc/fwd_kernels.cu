@@ -2,6 +2,8 @@
 // the mask count, and the per-row finalisation (log-sum-exp combine,
 // selective log-prob, GRPO token loss and its derivative, deterministic
 // fp64 loss reduction).
+#include <cuda_fp16.h>
+
 #include <algorithm>
 
 #include "launch.h"
@@ -216,6 +218,170 @@ cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t stream) {
   if (blocks < 1) blocks = 1;
   if (blocks > kMaxFinalizeBlocks) blocks = kMaxFinalizeBlocks;
   finalize_kernel<<<static_cast<int>(blocks), kFinalizeThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace grpo
+
+// ---------------------------------------------------------------------------
+// Stored-logit backward: per chunk, the forward GEMM also keeps the chunk's
+// logits in fp16; this kernel finishes each row (log-sum-exp, logp, token
+// loss, g) and rewrites the row in place as the bf16 G row that the dH GEMM
+// consumes: G_v = g (onehot_v(y) - exp(z'_v - lse)) f'(z_v). One CTA per row.
+namespace grpo {
+
+cudaError_t launch_fwds_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
+                             const TileArgs& args, int grid, cudaStream_t stream) {
+  tc_gemm_kernel<MODE_FWDS><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, stream>>>(map_a, map_b,
+                                                                             args);
+  return cudaGetLastError();
+}
+
+cudaError_t prepare_fwds_gemm() {
+  return cudaFuncSetAttribute(tc_gemm_kernel<MODE_FWDS>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint32_t h16) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h16)));
+}
+
+__global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const GformArgs a) {
+  __shared__ float sh_lse2, sh_g;
+  __shared__ int sh_y;
+  const int lrow = blockIdx.x;
+  const int li = lrow / BM;
+  int n_rb = a.n_rb;
+  if (a.n_active != nullptr) n_rb = max(0, min(a.n_rb, *a.n_active - a.rb_offset));
+  if (li >= n_rb) return;  // whole block: uniform
+  const int rb = a.rb_list != nullptr ? a.rb_list[a.rb_offset + li] : a.rb_offset + li;
+  const long long grow = static_cast<long long>(rb) * BM + (lrow - li * BM);
+
+  if (threadIdx.x == 0) {
+    float g = 0.f, lse = 0.f;
+    int y = -1;
+    const bool counted = grow < a.n_total && (a.mask == nullptr || a.mask[grow] != 0);
+    if (counted) {
+      float m2 = -INFINITY;
+      for (int s = 0; s < a.splits; ++s) m2 = fmaxf(m2, a.part_m[s * a.part_ld + grow]);
+      float ssum = 0.f;
+      for (int s = 0; s < a.splits; ++s)
+        ssum += a.part_s[s * a.part_ld + grow] * exp2f(a.part_m[s * a.part_ld + grow] - m2);
+      lse = (m2 + log2f(ssum)) * 0.69314718055994531f;
+      y = a.ids[grow];
+      float logp;
+      if (y < 0 || y >= a.vocab) {
+        atomicCAS(a.status, 0, GRPO_ERR_BAD_TOKEN_ID);
+        logp = __int_as_float(0x7fc00000);
+        y = -1;
+      } else {
+        logp = a.zy[grow] - lse;
+      }
+      const double mden = a.loss_den > 0.f ? static_cast<double>(a.loss_den) : *a.msum;
+      const double lp = logp;
+      const double A = a.adv[grow / a.seq_len];
+      const double r = exp(lp - static_cast<double>(a.old_logp[grow]));
+      const double lo = 1.0 - static_cast<double>(a.eps_low);
+      const double hi = 1.0 + static_cast<double>(a.eps_high);
+      const double c = fmin(fmax(r, lo), hi);
+      const double surr = fmin(r * A, c * A);
+      const double d = static_cast<double>(a.ref_logp[grow]) - lp;
+      const double ed = exp(d);
+      a.lt[grow] = -surr + static_cast<double>(a.beta) * (ed - d - 1.0);
+      const bool clipped = (A > 0.0 && r > hi) || (A < 0.0 && r < lo);
+      const double dl = -(clipped ? 0.0 : A * r) + static_cast<double>(a.beta) * (1.0 - ed);
+      g = mden != 0.0 ? static_cast<float>(dl / mden) : 0.f;
+      if (a.logp_out) a.logp_out[grow] = logp;
+    }
+    sh_lse2 = lse * kLog2e;
+    sh_g = g;
+    sh_y = y;
+  }
+  __syncthreads();
+  const float lse2 = sh_lse2, g = sh_g;
+  const int y = sh_y;
+  uint4* row = reinterpret_cast<uint4*>(a.S + static_cast<long long>(lrow) * a.ldS);
+  const int n_vec = static_cast<int>(a.ldS / 8);
+  if (g == 0.f) {
+    for (int i = threadIdx.x; i < n_vec; i += blockDim.x) row[i] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const float ng = -g;
+  for (int i = threadIdx.x; i < n_vec; i += blockDim.x) {
+    const uint4 in = row[i];
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float gv[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int v = i * 8 + k * 2 + h;
+        const float z = half_bits_to_float(h == 0 ? (w[k] & 0xffffu) : (w[k] >> 16));
+        float d = 1.f;  // dz'/dz recovered from the stored z'
+        if (a.xmode == 1) {
+          d = a.k0;
+        } else if (a.xmode == 2) {
+          const float u = z / a.k2;
+          d = a.k0 * fmaf(-u, u, 1.f);
+        }
+        float val = ng * ex2(fmaf(z, kLog2e, -lse2));
+        if (v == y) val += g;
+        gv[h] = v < a.vocab ? val * d : 0.f;
+      }
+      o[k] = pack_bf16x2(gv[0], gv[1]);
+    }
+    row[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Closing reduction of a stored-logit call: masked rows get logp = 0, and the
+// token losses of unmasked rows are summed in a fixed order (fp64).
+__global__ void __launch_bounds__(kFinalizeThreads) finish_loss_kernel(const FinishArgs a) {
+  __shared__ double sh[32];
+  __shared__ bool is_last;
+  double local = 0.0;
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < a.n;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const bool counted = a.mask == nullptr || a.mask[t] != 0;
+    if (counted) {
+      local += a.lt[t];
+    } else if (a.logp_out) {
+      a.logp_out[t] = 0.f;
+    }
+  }
+  const double bsum = block_sum(local, sh);
+  if (threadIdx.x == 0) {
+    a.block_partials[blockIdx.x] = bsum;
+    __threadfence();
+    const unsigned done = atomicAdd(a.counter, 1u);
+    is_last = (done == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (is_last) {
+    __threadfence();
+    double v = 0.0;
+    for (unsigned i = threadIdx.x; i < gridDim.x; i += blockDim.x)
+      v += reinterpret_cast<volatile double*>(a.block_partials)[i];
+    const double tot = block_sum(v, sh);
+    if (threadIdx.x == 0) {
+      const double mden = a.loss_den > 0.f ? static_cast<double>(a.loss_den) : *a.msum;
+      *a.loss_out = mden != 0.0 ? static_cast<float>(tot / mden) : 0.f;
+      *a.counter = 0;
+    }
+  }
+}
+
+cudaError_t launch_finalize_gform(const GformArgs& a, int rows, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  finalize_gform_kernel<<<rows, kGformThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finish_loss(const FinishArgs& a, cudaStream_t stream) {
+  long long blocks = (a.n + kFinalizeThreads - 1) / kFinalizeThreads;
+  blocks = std::max(1LL, std::min<long long>(blocks, kMaxFinalizeBlocks));
+  finish_loss_kernel<<<static_cast<int>(blocks), kFinalizeThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

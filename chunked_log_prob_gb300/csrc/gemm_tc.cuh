@@ -14,6 +14,9 @@
 //              G = g (onehot(y) - exp(S - lse)) in bf16 to the chunk workspace.
 //   MODE_DH    dH_tile (+)= G W over one vocab block (B operand MN-major);
 //              epilogue accumulates in fp32 and writes bf16 on the last block.
+//   MODE_FWDS  MODE_FWD over the rows of one backward chunk that also stores
+//              the (transformed) logits in fp16 to the chunk workspace, for a
+//              backward that needs no second logit GEMM.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -34,7 +37,9 @@ constexpr int GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment sla
 constexpr int TMEM_COLS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
-enum GemmMode { MODE_FWD = 0, MODE_BWDG = 1, MODE_DH = 2 };
+enum GemmMode { MODE_FWD = 0, MODE_BWDG = 1, MODE_DH = 2, MODE_FWDS = 3 };
+
+__host__ __device__ constexpr bool is_fwd(int mode) { return mode == MODE_FWD || mode == MODE_FWDS; }
 
 struct TileArgs {
   long long n_total;     // N: rows of hidden / dH; global rows >= N are padding
@@ -66,6 +71,9 @@ struct TileArgs {
   const float* g;        // indexed by global row
   __nv_bfloat16* G;      // [local rows][ldG] chunk workspace
   long long ldG;
+  // MODE_FWDS
+  uint16_t* S;           // [local rows][ldS] fp16 logits of the chunk
+  long long ldS;
   // MODE_DH
   float* acc;            // [local rows][hidden] fp32 accumulator
   __nv_bfloat16* dH;     // [N][hidden] output, indexed by global row
@@ -98,7 +106,7 @@ __device__ __forceinline__ int launch_row_blocks(const TileArgs& a) {
 
 template <int MODE>
 __device__ __forceinline__ void unit_tiles(const TileArgs& a, int col, int& t0, int& t1) {
-  if (MODE == MODE_FWD) {
+  if (is_fwd(MODE)) {
     t0 = static_cast<int>((static_cast<long long>(col) * a.n_vtiles) / a.n_cols);
     t1 = static_cast<int>((static_cast<long long>(col + 1) * a.n_vtiles) / a.n_cols);
   } else {
@@ -301,7 +309,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       float m2 = -INFINITY, ssum = 0.f;  // FWD
       int y = -1;
       float lse2 = 0.f, gval = 0.f;      // BWDG
-      if (MODE == MODE_FWD) {
+      if (is_fwd(MODE)) {
         if (valid && (args.mask == nullptr || args.mask[grow] != 0)) y = args.ids[grow];
       } else if (MODE == MODE_BWDG) {
         if (valid) {
@@ -321,7 +329,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         tc_fence_after();
         const uint32_t tbase = tmem_base + lane_addr + buf * BN;
 
-        if (MODE == MODE_FWD) {
+        if (is_fwd(MODE)) {
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
             const int col0 = t * BN + c * 32;
@@ -329,6 +337,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             float v[32];
             tmem_ld32(tbase + c * 32, v);
             logit_transform(args, v);
+            if (MODE == MODE_FWDS && valid) {
+              uint16_t* dst = args.S + static_cast<long long>(lrow) * args.ldS + col0;
+              if (col0 + 32 <= args.vocab) {
+                uint32_t hpk[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) hpk[j] = pack_f16x2(v[2 * j], v[2 * j + 1]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  st_global_v4(dst + j * 8, hpk[4 * j], hpk[4 * j + 1], hpk[4 * j + 2],
+                               hpk[4 * j + 3]);
+              } else {
+                for (int j = 0; j < 32 && col0 + j < args.vocab; ++j)
+                  dst[j] = static_cast<uint16_t>(pack_f16x2(v[j], 0.f) & 0xffffu);
+              }
+            }
             if (col0 + 32 > args.vocab) {
 #pragma unroll
               for (int j = 0; j < 32; ++j)
@@ -456,7 +479,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty_bar[buf]);
       }
-      if (MODE == MODE_FWD && ok && valid) {
+      if (is_fwd(MODE) && ok && valid) {
         args.part_m[static_cast<long long>(col) * args.part_ld + grow] = m2;
         args.part_s[static_cast<long long>(col) * args.part_ld + grow] = ssum;
       }

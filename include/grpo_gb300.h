@@ -65,6 +65,15 @@ typedef struct grpo_shape {
   int32_t reserved; /* must be 0                                              */
 } grpo_shape;
 
+/* grpo_params.flags bit: backward without a second logit GEMM. Per chunk of
+ * rows, the forward GEMM also keeps the chunk's (transformed) logits in fp16
+ * in the workspace; a row-wise pass turns them into G once lse and g are
+ * known, and the dH GEMM runs over the whole vocabulary. Executes 4 N D V
+ * instead of 6 N D V flops, for a workspace of chunk x V x 2 bytes (capped at
+ * 2 GiB) instead of chunk x vocab_block x 2 (vocab_block is then ignored).
+ * Logits must stay within fp16 range (|z'| < 65504). */
+#define GRPO_FLAG_STORED_LOGITS 1u
+
 typedef struct grpo_params {
   float eps_low;          /* ratio clip: lower bound 1 - eps_low (0.2)         */
   float eps_high;         /* ratio clip: upper bound 1 + eps_high (0.2)        */
@@ -72,7 +81,7 @@ typedef struct grpo_params {
   float loss_denominator; /* <= 0: divide by sum(mask); > 0: divide by this    */
   int32_t chunk_tokens;   /* rows per backward chunk; 0 = automatic            */
   int32_t vocab_block;    /* vocab columns per backward block; 0 = automatic   */
-  uint32_t flags;         /* must be 0                                         */
+  uint32_t flags;         /* 0 or GRPO_FLAG_STORED_LOGITS                      */
   uint32_t reserved;      /* must be 0                                         */
   /* Logit transforms ("GRPO with 7x longer context", the options of the
    * selective log-softmax call: logit scale multiply/divide, softcapping,
@@ -141,7 +150,8 @@ typedef struct grpo_plan_info {
   int32_t n_vocab_blocks;    /* backward vocab blocks per chunk              */
   int32_t fwd_splits;        /* forward vocab splits (partials per row)      */
   int32_t launches_logp;     /* kernel launches of one grpo_logp_fwd call    */
-  int32_t launches_loss;     /* kernel launches of one grpo_loss_fwd_bwd     */
+  int32_t launches_loss;     /* kernel launches of one grpo_loss_fwd_bwd
+                                (with a mask; one fewer without)          */
   int32_t reserved;
   uint64_t workspace_bytes;  /* same as grpo_workspace_size                  */
 } grpo_plan_info;

@@ -91,7 +91,7 @@ def test_workspace_size_rejects_bad_shapes(clp, n, d, v, want):
 
 def test_bad_params_rejected(clp):
     p = clp.make_params()
-    p.flags = 1
+    p.flags = 2  # not a defined flag bit
     with pytest.raises(clp.GrpoError) as e:
         clp.grpo_workspace_size(10, 16, 50, 1, p)
     assert e.value.code == -1
@@ -124,3 +124,17 @@ def test_misaligned_pointers_rejected(clp):
     assert rc == -2
     rc = clp.lib.grpo_logp_fwd(a, a, a, a, None, ctypes.byref(shape), None, a + 16, 4096, None)
     assert rc == -2
+
+
+def test_stored_logit_workspace_is_chunk_times_vocab(clp):
+    # Stored-logit backward: one fp16 logit block of chunk x V (V padded to 8),
+    # still independent of N.
+    p = clp.make_params(chunk_tokens=2048, flags=1)
+    a = clp.grpo_workspace_size(16384, 4096, 128256, 1, p)
+    b = clp.grpo_workspace_size(65536, 4096, 128256, 1, p)
+    block = 2048 * 128256 * 2
+    assert block < a < block + 16384 * 400
+    assert (b - a) / (65536 - 16384) < 64 * 4 * 2 + 64
+    # Automatic chunk without a device: bounded by 2 GiB of logits.
+    auto = clp.grpo_workspace_size(131072, 2880, 201088, 1, clp.make_params(flags=1))
+    assert auto < (2 << 30) + 131072 * 400

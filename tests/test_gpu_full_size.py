@@ -53,18 +53,20 @@ def _sample_rows(p, seed):
     return np.sort(rows), np.sort(mrows)
 
 
-def _run(clp, p, mask, old, ref):
+def _run(clp, p, mask, old, ref, flags=0):
     dev = torch.device(DEV)
     args = [t.to(dev) for t in (p.hidden, p.weight, p.ids, mask, old, ref, p.adv)]
-    ws = clp.alloc_workspace(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, None, dev)
-    loss, logp, dH = clp.grpo_loss_fwd_bwd(*args, p.seq_len, workspace=ws)
+    params = clp.make_params(flags=flags)
+    ws = clp.alloc_workspace(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, params, dev)
+    loss, logp, dH = clp.grpo_loss_fwd_bwd(*args, p.seq_len, params=params, workspace=ws)
     st = clp.grpo_read_device_status(ws)
     return loss.item(), logp.cpu(), dH, st
 
 
+@pytest.mark.parametrize("flags", [0, 1], ids=["recompute", "stored"])
 @pytest.mark.parametrize("name", ["qwen2.5-1.5b", "llama-3.1-8b", "qwen3-8b-long",
                                   "gpt-oss-20b-long"])
-def test_full_size_sampled_rows(clp, name):
+def test_full_size_sampled_rows(clp, name, flags):
     p = synth.make_problem(name, seed=1)
     rows, mrows = _sample_rows(p, seed=2)
     W64 = p.weight.float().numpy().astype(np.float64)
@@ -75,7 +77,7 @@ def test_full_size_sampled_rows(clp, name):
     M = float(p.mask.sum())
 
     # (1) the workload itself: sampled rows of logp and dH.
-    L, logp, dH, st = _run(clp, p, p.mask, old, ref)
+    L, logp, dH, st = _run(clp, p, p.mask, old, ref, flags)
     assert st == 0
     want = oracle.rows_fwd_bwd(p.hidden, W64, p.ids.numpy(), rows, old, ref, p.adv,
                                p.seq_len, M, p.eps_low, p.eps_high, p.beta)
@@ -93,7 +95,7 @@ def test_full_size_sampled_rows(clp, name):
     # (2) same shapes, mask = sampled rows only: the loss is exact.
     mask2 = torch.zeros_like(p.mask)
     mask2[rows] = 1
-    L2, logp2, dH2, st2 = _run(clp, p, mask2, old, ref)
+    L2, logp2, dH2, st2 = _run(clp, p, mask2, old, ref, flags)
     assert st2 == 0
     lp_full = np.zeros(p.n_tokens)
     lp_full[rows] = lp_rows

@@ -260,3 +260,75 @@ def test_logit_transforms(clp, kw):
     check(gpu_loss(clp, p, old, ref, params), want, p.mask, f"transform {kw}")
     lp, _ = clp.grpo_logp_fwd(_to(p.hidden), _to(p.weight), _to(p.ids), params=params)
     assert np.abs(lp.cpu().double().numpy() - base).max() <= LOGP_TOL
+
+
+# ---------------------------------------------- stored-logit backward ------
+
+STORED = 1  # GRPO_FLAG_STORED_LOGITS
+
+
+@pytest.mark.parametrize("N,T,D,V,chunk,vblock,padded", RAGGED)
+def test_stored_logits_ragged(clp, N, T, D, V, chunk, vblock, padded):
+    G = 4 if (N // T) % 4 == 0 else 1
+    p = synth.make_problem("tiny", seed=N + D + V + 1, prompts=(N // T) // G, G=G, T=T, D=D,
+                           V=V, lengths=(max(1, T // 3), T) if padded else None)
+    old, ref, want = oracle_case(p)
+    params = clp.make_params(chunk_tokens=chunk, flags=STORED)
+    check(gpu_loss(clp, p, old, ref, params), want, p.mask, f"stored {N}x{D}x{V}")
+
+
+@pytest.mark.parametrize("kw", XFORMS)
+def test_stored_logits_transforms(clp, kw):
+    p = synth.make_problem("tiny", seed=32, T=75, prompts=1, G=4, D=200, V=3000,
+                           lengths=(20, 75), weight_std=0.2)
+    xf = oracle.Transform(scale_mul=kw.get("logit_scale_multiply", 1.0),
+                          scale_div=kw.get("logit_scale_divide", 1.0),
+                          softcap=kw.get("logit_softcapping", 0.0),
+                          temperature=kw.get("temperature", 1.0))
+    base, _ = oracle.selective_logp(p.hidden, p.weight, p.ids.numpy(), xf=xf)
+    old, ref = p.old_ref(torch.from_numpy(base))
+    want = oracle.loss_fwd_bwd(p.hidden, p.weight, p.ids.numpy(), p.mask.numpy(), old, ref,
+                               p.adv, p.seq_len, p.eps_low, p.eps_high, p.beta, xf=xf)
+    params = clp.make_params(chunk_tokens=128, flags=STORED, **kw)
+    check(gpu_loss(clp, p, old, ref, params), want, p.mask, f"stored transform {kw}")
+
+
+@pytest.mark.parametrize("chunk", [256, 0])
+def test_stored_logits_padding_blocks(clp, chunk):
+    p = synth.make_problem("tiny", seed=41 + chunk, prompts=2, G=4, T=512, D=256, V=3000,
+                           lengths=(1, 512))
+    old, ref, want = oracle_case(p)
+    params = clp.make_params(chunk_tokens=chunk, flags=STORED)
+    ws = clp.alloc_workspace(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, params, DEV)
+    dH = torch.full((p.n_tokens, p.hidden_size), float("nan"), dtype=torch.bfloat16, device=DEV)
+    logp = torch.full((p.n_tokens,), float("nan"), device=DEV)
+    loss, logp, dH = clp.grpo_loss_fwd_bwd(
+        _to(p.hidden), _to(p.weight), _to(p.ids), _to(p.mask), _to(old), _to(ref), _to(p.adv),
+        p.seq_len, params=params, workspace=ws, dH=dH, logp=logp)
+    st = clp.grpo_read_device_status(ws)
+    got = (loss.item(), logp.cpu().double().numpy(), dH.cpu().double().numpy(), st)
+    check(got, want, p.mask, f"stored padding chunk={chunk}")
+
+
+def test_stored_and_recomputed_backward_agree(clp):
+    p = synth.make_problem("tiny", seed=12, T=128, prompts=2, G=4, D=256, V=5000,
+                           lengths=(30, 128))
+    old, ref, _ = oracle_case(p)
+    L1, lp1, dH1, s1 = gpu_loss(clp, p, old, ref, clp.make_params(flags=0))
+    L2, lp2, dH2, s2 = gpu_loss(clp, p, old, ref, clp.make_params(flags=STORED))
+    assert s1 == 0 and s2 == 0
+    assert np.abs(lp1 - lp2).max() <= 1e-5
+    assert abs(L1 - L2) <= 1e-5 * abs(L1)
+    assert np.linalg.norm(dH1 - dH2) <= 1e-2 * np.linalg.norm(dH1)
+
+
+def test_stored_logits_bad_id_and_all_masked(clp):
+    p = synth.make_problem("tiny", seed=13)
+    params = clp.make_params(flags=STORED)
+    ids = p.ids.clone()
+    ids[9] = -3
+    old = torch.full((p.n_tokens,), -8.0)
+    L, logp, dH, st = gpu_loss(clp, p, old, old, params, ids=ids)
+    assert st == -8 and math.isnan(logp[9]) and math.isnan(L)
+    L, logp, dH, st = gpu_loss(clp, p, old, old, params, mask=torch.zeros_like(p.mask))
+    assert st == 0 and L == 0.0 and np.all(logp == 0) and np.all(dH == 0)
