@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--backward", default="stored", choices=["stored", "recompute"],
                     help="stored: the backward reads fp16 logits kept per chunk (4NDV "
                          "executed); recompute: it recomputes the logit tiles (6NDV)")
+    ap.add_argument("--single-cta", action="store_true",
+                    help="one CTA per 128-row GEMM tile instead of CTA pairs")
     ap.add_argument("--no-variant", action="store_true",
                     help="skip timing the other backward variant")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -204,7 +206,7 @@ def run_ours(args):
 
     def make(flag):
         return clp.make_params(p.eps_low, p.eps_high, p.beta, 0.0, args.chunk_tokens,
-                               args.vocab_block, flags=flag)
+                               args.vocab_block, flags=flag | (2 if args.single_cta else 0))
 
     params = make(1 if stored else 0)
     other = make(0 if stored else 1)

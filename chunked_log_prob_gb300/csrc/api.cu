@@ -36,6 +36,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
 struct Layout {
+  int ctas;         // 2: CTA-pair GEMMs (default); 1: single-CTA GEMMs
   bool stored;      // stored-logit backward (GRPO_FLAG_STORED_LOGITS)
   long long ldS;    // stored mode: elements per row of the chunk logit block
   long long n, nr;  // rows, rows rounded up to BM
@@ -47,10 +48,10 @@ struct Layout {
   size_t off_pm, off_ps, off_zy, off_lse, off_g, off_rbl, off_lt, off_G, off_acc, total;
 };
 
-int auto_chunk_blocks(long long n_rb_total, int n_dt, int sms) {
+int auto_chunk_blocks(long long n_rb_total, int n_dt, int sms, int max_units) {
   // Row blocks per backward chunk: keep the dH GEMM's (row block x D tile)
   // grid close to whole waves of the SMs; prefer larger chunks on ties.
-  const int hi = static_cast<int>(std::min<long long>(n_rb_total, kMaxAutoChunkBlocks));
+  const int hi = static_cast<int>(std::min<long long>(n_rb_total, max_units));
   int best = hi;
   double best_eff = -1.0;
   for (int nrb = hi; nrb >= 1; --nrb) {
@@ -100,8 +101,8 @@ int stored_fwd_splits(int nrb, int nvt, int sms, double* eff_out) {
 // (row blocks x D tiles) units; the score is the ideal SM time of the whole
 // schedule (every chunk, including a shorter last one) over its wave-rounded
 // time, forward and dH weighted equally. Near-ties go to the larger chunk.
-int auto_stored_chunk_blocks(long long n_rb_total, int n_dt, int nvt, int sms, long long ldS) {
-  const int hi = static_cast<int>(std::min<long long>(n_rb_total, stored_max_blocks(ldS)));
+int auto_stored_chunk_blocks(long long n_rb_total, int n_dt, int nvt, int sms, int max_units) {
+  const int hi = static_cast<int>(std::min<long long>(n_rb_total, max_units));
   int best = hi;
   double best_score = -1.0;
   for (int nrb = hi; nrb >= 1; --nrb) {
@@ -126,6 +127,7 @@ int auto_stored_chunk_blocks(long long n_rb_total, int n_dt, int nvt, int sms, l
 }
 
 int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
+  L->ctas = (p != nullptr && (p->flags & GRPO_FLAG_SINGLE_CTA) != 0) ? 1 : 2;
   L->stored = p != nullptr && (p->flags & GRPO_FLAG_STORED_LOGITS) != 0;
   L->ldS = cdiv(std::max(s->vocab, 1), 8) * 8;
   L->n = s->n_tokens;
@@ -134,23 +136,26 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   L->D = s->hidden;
   L->V = s->vocab;
   L->nvt = static_cast<int>(cdiv(s->vocab, BN));
-  const long long n_rb_total = L->nr / BM;
   const int n_dt = static_cast<int>(cdiv(s->hidden, BN));
-  // chunk rows
+  // Chunks are whole row units (BM * ctas rows: what one CTA pair covers).
+  const long long ru_rows = static_cast<long long>(BM) * L->ctas;
+  const long long n_ru_total = cdiv(L->nr, ru_rows);
+  const int slots = sms / L->ctas;
+  const int max_stored_units = std::max(1, stored_max_blocks(L->ldS) / L->ctas);
   long long crows;
   if (p && p->chunk_tokens > 0) {
-    crows = cdiv(p->chunk_tokens, BM) * BM;
+    crows = cdiv(p->chunk_tokens, ru_rows) * ru_rows;
   } else if (L->stored) {
-    crows = static_cast<long long>(
-                sms > 0 ? auto_stored_chunk_blocks(n_rb_total, n_dt, L->nvt, sms, L->ldS)
-                        : std::min<long long>(n_rb_total, stored_max_blocks(L->ldS))) *
-            BM;
+    crows = (sms > 0 ? auto_stored_chunk_blocks(n_ru_total, n_dt, L->nvt, slots,
+                                                max_stored_units)
+                     : std::min<long long>(n_ru_total, max_stored_units)) *
+            ru_rows;
   } else if (sms > 0) {
-    crows = static_cast<long long>(auto_chunk_blocks(n_rb_total, n_dt, sms)) * BM;
+    crows = auto_chunk_blocks(n_ru_total, n_dt, slots, kMaxAutoChunkBlocks / L->ctas) * ru_rows;
   } else {  // sizing without a device: the largest automatic chunk
-    crows = std::min<long long>(n_rb_total, kMaxAutoChunkBlocks) * BM;
+    crows = std::min<long long>(n_ru_total, kMaxAutoChunkBlocks / L->ctas) * ru_rows;
   }
-  crows = std::min(crows, L->nr);
+  crows = std::min(crows, n_ru_total * ru_rows);
   if (crows > INT_MAX / 2) return GRPO_ERR_UNSUPPORTED_SHAPE;
   L->chunk_rows = static_cast<int>(crows);
   long long vb = (p && p->vocab_block > 0) ? p->vocab_block : kAutoVocabBlock;
@@ -201,7 +206,7 @@ int check_shape(const grpo_shape* s, bool need_seq) {
 
 int check_params(const grpo_params* p) {
   if (!p) return GRPO_OK;
-  if ((p->flags & ~GRPO_FLAG_STORED_LOGITS) != 0 || p->reserved != 0 || p->chunk_tokens < 0 ||
+  if ((p->flags & ~(GRPO_FLAG_STORED_LOGITS | GRPO_FLAG_SINGLE_CTA)) != 0 || p->reserved != 0 || p->chunk_tokens < 0 ||
       p->vocab_block < 0)
     return GRPO_ERR_INVALID_ARG;
   if (!(p->eps_low >= 0.f) || !(p->eps_high >= 0.f) || !(p->beta >= 0.f))
@@ -349,8 +354,9 @@ int run_forward(const void* hidden, const void* W, const int32_t* ids, const uin
                 const int* rb_list, const int* n_active, const grpo_params* prm,
                 const Layout& L, const Ws& w, int sms, int* splits_out, cudaStream_t st) {
   CUtensorMap map_h, map_w;
+  const int slots = std::max(1, sms / L.ctas);
   if (!encode_2d(&map_h, hidden, L.D, L.n, L.D, BK, BM) ||
-      !encode_2d(&map_w, W, L.D, L.V, L.D, BK, BN))
+      !encode_2d(&map_w, W, L.D, L.V, L.D, BK, BN / L.ctas))
     return GRPO_ERR_CUDA;
   TileArgs a = base_args(L, w);
   set_transform(&a, prm);
@@ -360,8 +366,9 @@ int run_forward(const void* hidden, const void* W, const int32_t* ids, const uin
   a.rb_list = rb_list;
   a.n_active = n_active;
   a.k_iters = static_cast<int>(cdiv(L.D, BK));
-  a.group_rows = group_rows_for(a.n_rb, sms);
-  int splits = std::max(1, sms / a.group_rows);
+  const int n_ru = static_cast<int>(cdiv(a.n_rb, L.ctas));
+  a.group_rows = group_rows_for(n_ru, slots);
+  int splits = std::max(1, slots / a.group_rows);
   splits = std::min(splits, std::min(L.nvt, kMaxSplits));
   a.n_cols = splits;
   a.n_vtiles = L.nvt;
@@ -372,9 +379,9 @@ int run_forward(const void* hidden, const void* W, const int32_t* ids, const uin
   a.part_s = w.ps;
   a.zy = w.zy;
   a.part_ld = L.nr;
-  const long long units = static_cast<long long>(a.n_rb) * a.n_cols;
-  const int grid = static_cast<int>(std::min<long long>(units, sms));
-  if (launch_fwd_gemm(map_h, map_w, a, grid, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  const long long units = static_cast<long long>(n_ru) * a.n_cols;
+  const int grid = L.ctas * static_cast<int>(std::min<long long>(units, slots));
+  if (launch_fwd_gemm(L.ctas, map_h, map_w, a, grid, st) != cudaSuccess) return GRPO_ERR_CUDA;
   *splits_out = splits;
   return GRPO_OK;
 }
@@ -386,8 +393,9 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
                  const grpo_params* prm, const Layout& L, const Ws& w, int sms,
                  cudaStream_t st) {
   CUtensorMap map_h, map_w_k, map_w_mn;
+  const int slots = std::max(1, sms / L.ctas);
   if (!encode_2d(&map_h, hidden, L.D, L.n, L.D, BK, BM) ||
-      !encode_2d(&map_w_k, W, L.D, L.V, L.D, BK, BN) ||
+      !encode_2d(&map_w_k, W, L.D, L.V, L.D, BK, BN / L.ctas) ||
       !encode_2d(&map_w_mn, W, L.D, L.V, L.D, 64, BK))
     return GRPO_ERR_CUDA;
   const int n_dt = static_cast<int>(cdiv(L.D, BN));
@@ -395,6 +403,7 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
   const int rb_per_chunk = L.chunk_rows / BM;
   for (int rb0 = 0; rb0 < n_rb_total; rb0 += rb_per_chunk) {
     const int n_rb = std::min(rb_per_chunk, n_rb_total - rb0);
+    const int n_ru = static_cast<int>(cdiv(n_rb, L.ctas));
     for (long long v0 = 0; v0 < L.V; v0 += L.vblock) {
       const int width = static_cast<int>(std::min<long long>(L.vblock, L.V - v0));
       const int ntile = static_cast<int>(cdiv(width, BN));
@@ -407,7 +416,7 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
       a.rb_list = w.rb_list;
       a.n_active = w.n_active;
       a.k_iters = static_cast<int>(cdiv(L.D, BK));
-      a.group_rows = group_rows_for(n_rb, sms);
+      a.group_rows = group_rows_for(n_ru, slots);
       a.n_cols = ntile;
       a.v0 = static_cast<int>(v0);
       a.ids = ids;
@@ -415,8 +424,9 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
       a.g = w.g;
       a.G = w.G;
       a.ldG = L.vblock;
-      long long units = static_cast<long long>(n_rb) * ntile;
-      if (launch_bwdg_gemm(map_h, map_w_k, a, static_cast<int>(std::min<long long>(units, sms)),
+      long long units = static_cast<long long>(n_ru) * ntile;
+      if (launch_bwdg_gemm(L.ctas, map_h, map_w_k, a,
+                           L.ctas * static_cast<int>(std::min<long long>(units, slots)),
                            st) != cudaSuccess)
         return GRPO_ERR_CUDA;
       // (2) dH_chunk (+)= G W[v0 : v0 + width].
@@ -430,15 +440,16 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
       b.rb_list = w.rb_list;
       b.n_active = w.n_active;
       b.k_iters = static_cast<int>(cdiv(width, BK));
-      b.group_rows = group_rows_for(n_rb, sms);
+      b.group_rows = group_rows_for(n_ru, slots);
       b.n_cols = n_dt;
       b.v0 = static_cast<int>(v0);
       b.acc = w.acc;
       b.dH = static_cast<__nv_bfloat16*>(dH);
       b.first = v0 == 0;
       b.last = v0 + L.vblock >= L.V;
-      units = static_cast<long long>(n_rb) * n_dt;
-      if (launch_dh_gemm(map_g, map_w_mn, b, static_cast<int>(std::min<long long>(units, sms)),
+      units = static_cast<long long>(n_ru) * n_dt;
+      if (launch_dh_gemm(L.ctas, map_g, map_w_mn, b,
+                         L.ctas * static_cast<int>(std::min<long long>(units, slots)),
                          st) != cudaSuccess)
         return GRPO_ERR_CUDA;
     }
@@ -455,8 +466,9 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
                float* logp_out, void* dH, const grpo_params* prm, const Layout& L, const Ws& w,
                int sms, cudaStream_t st) {
   CUtensorMap map_h, map_w_k, map_w_mn;
+  const int slots = std::max(1, sms / L.ctas);
   if (!encode_2d(&map_h, hidden, L.D, L.n, L.D, BK, BM) ||
-      !encode_2d(&map_w_k, W, L.D, L.V, L.D, BK, BN) ||
+      !encode_2d(&map_w_k, W, L.D, L.V, L.D, BK, BN / L.ctas) ||
       !encode_2d(&map_w_mn, W, L.D, L.V, L.D, 64, BK))
     return GRPO_ERR_CUDA;
   const int n_dt = static_cast<int>(cdiv(L.D, BN));
@@ -465,7 +477,8 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
   uint16_t* S = reinterpret_cast<uint16_t*>(w.G);
   for (int rb0 = 0; rb0 < n_rb_total; rb0 += rb_per_chunk) {
     const int n_rb = std::min(rb_per_chunk, n_rb_total - rb0);
-    const int splits = stored_fwd_splits(n_rb, L.nvt, sms, nullptr);
+    const int n_ru = static_cast<int>(cdiv(n_rb, L.ctas));
+    const int splits = stored_fwd_splits(n_ru, L.nvt, slots, nullptr);
     // (1) logits of the chunk: online LSE partials, z_y, fp16 copy.
     TileArgs a = base_args(L, w);
     set_transform(&a, prm);
@@ -475,7 +488,7 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     a.rb_list = w.rb_list;
     a.n_active = w.n_active;
     a.k_iters = static_cast<int>(cdiv(L.D, BK));
-    a.group_rows = n_rb;
+    a.group_rows = n_ru;
     a.n_cols = splits;
     a.n_vtiles = L.nvt;
     a.v0 = 0;
@@ -487,8 +500,9 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     a.part_ld = L.nr;
     a.S = S;
     a.ldS = L.ldS;
-    long long units = static_cast<long long>(n_rb) * splits;
-    if (launch_fwds_gemm(map_h, map_w_k, a, static_cast<int>(std::min<long long>(units, sms)),
+    long long units = static_cast<long long>(n_ru) * splits;
+    if (launch_fwds_gemm(L.ctas, map_h, map_w_k, a,
+                         L.ctas * static_cast<int>(std::min<long long>(units, slots)),
                          st) != cudaSuccess)
       return GRPO_ERR_CUDA;
     // (2) per-row finish; the chunk block becomes G.
@@ -536,14 +550,15 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     b.rb_list = w.rb_list;
     b.n_active = w.n_active;
     b.k_iters = static_cast<int>(cdiv(L.V, BK));
-    b.group_rows = group_rows_for(n_rb, sms);
+    b.group_rows = group_rows_for(n_ru, slots);
     b.n_cols = n_dt;
     b.v0 = 0;
     b.dH = static_cast<__nv_bfloat16*>(dH);
     b.first = 1;
     b.last = 1;
-    units = static_cast<long long>(n_rb) * n_dt;
-    if (launch_dh_gemm(map_g, map_w_mn, b, static_cast<int>(std::min<long long>(units, sms)),
+    units = static_cast<long long>(n_ru) * n_dt;
+    if (launch_dh_gemm(L.ctas, map_g, map_w_mn, b,
+                       L.ctas * static_cast<int>(std::min<long long>(units, slots)),
                        st) != cudaSuccess)
       return GRPO_ERR_CUDA;
   }
@@ -723,15 +738,17 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
   info->n_chunks = static_cast<int32_t>(cdiv(L.n, L.chunk_rows));
   info->n_vocab_blocks = static_cast<int32_t>(cdiv(L.V, L.vblock));
   const int n_rb = static_cast<int>(L.nr / BM);
-  const int grp = group_rows_for(n_rb, sms);
-  info->fwd_splits = std::min(std::max(1, sms / grp), std::min(L.nvt, kMaxSplits));
+  const int slots = std::max(1, sms / L.ctas);
+  const int grp = group_rows_for(static_cast<int>(cdiv(n_rb, L.ctas)), slots);
+  info->fwd_splits = std::min(std::max(1, slots / grp), std::min(L.nvt, kMaxSplits));
   info->launches_logp = L.n > 0 ? 2 : 0;
   info->launches_loss = L.n <= 0 ? 0
                       : L.stored ? 3 + 3 * info->n_chunks
                                  : 4 + 2 * info->n_chunks * info->n_vocab_blocks;
   if (L.stored) {
     info->n_vocab_blocks = 1;
-    info->fwd_splits = stored_fwd_splits(L.chunk_rows / BM, L.nvt, sms, nullptr);
+    info->fwd_splits =
+        stored_fwd_splits(L.chunk_rows / (BM * L.ctas), L.nvt, slots, nullptr);
   }
   info->workspace_bytes = std::max(L.total, Lmax.total);
   return GRPO_OK;

@@ -1,29 +1,28 @@
 // Backward-side GEMM launchers: the G tile (recomputed logits -> bf16
-// softmax-Jacobian rows) and the dH accumulation.
+// softmax-Jacobian rows) and the dH accumulation, each in the single-CTA and
+// the CTA-pair variant.
 #include "launch.h"
 
 namespace grpo {
 
 cudaError_t prepare_bwd_gemms() {
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE_BWDG>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       GEMM_SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(tc_gemm_kernel<MODE_DH>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
+  cudaError_t e = prepare_gemm_variant<MODE_BWDG, 1>();
+  if (e == cudaSuccess) e = prepare_gemm_variant<MODE_BWDG, 2>();
+  if (e == cudaSuccess) e = prepare_gemm_variant<MODE_DH, 1>();
+  if (e == cudaSuccess) e = prepare_gemm_variant<MODE_DH, 2>();
+  return e;
 }
 
-cudaError_t launch_bwdg_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
+cudaError_t launch_bwdg_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                              const TileArgs& args, int grid, cudaStream_t stream) {
-  tc_gemm_kernel<MODE_BWDG><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, stream>>>(map_a, map_b,
-                                                                             args);
-  return cudaGetLastError();
+  return ctas == 2 ? launch_gemm_variant<MODE_BWDG, 2>(map_a, map_b, args, grid, stream)
+                   : launch_gemm_variant<MODE_BWDG, 1>(map_a, map_b, args, grid, stream);
 }
 
-cudaError_t launch_dh_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
+cudaError_t launch_dh_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                            const TileArgs& args, int grid, cudaStream_t stream) {
-  tc_gemm_kernel<MODE_DH><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, stream>>>(map_a, map_b, args);
-  return cudaGetLastError();
+  return ctas == 2 ? launch_gemm_variant<MODE_DH, 2>(map_a, map_b, args, grid, stream)
+                   : launch_gemm_variant<MODE_DH, 1>(map_a, map_b, args, grid, stream);
 }
 
 }  // namespace grpo

@@ -11,20 +11,16 @@
 namespace grpo {
 
 cudaError_t prepare_fwd_gemm() {
-  return cudaFuncSetAttribute(tc_gemm_kernel<MODE_FWD>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
+  cudaError_t e = prepare_gemm_variant<MODE_FWD, 1>();
+  return e == cudaSuccess ? prepare_gemm_variant<MODE_FWD, 2>() : e;
 }
 
-cudaError_t launch_fwd_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
+cudaError_t launch_fwd_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                             const TileArgs& args, int grid, cudaStream_t stream) {
-  tc_gemm_kernel<MODE_FWD><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, stream>>>(map_a, map_b, args);
-  return cudaGetLastError();
+  return ctas == 2 ? launch_gemm_variant<MODE_FWD, 2>(map_a, map_b, args, grid, stream)
+                   : launch_gemm_variant<MODE_FWD, 1>(map_a, map_b, args, grid, stream);
 }
 
-// Row plan of a loss call (one block of 1024 threads): the list of row blocks
-// (BM rows each) holding at least one unmasked token, in increasing order, its
-// length, and the number of unmasked tokens. Blocks of pure padding are then
-// skipped by every GEMM of the call.
 __global__ void __launch_bounds__(1024) row_plan_kernel(const uint8_t* __restrict__ mask,
                                                         long long n, int n_rb,
                                                         int* __restrict__ rb_list,
@@ -230,16 +226,15 @@ cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t stream) {
 // consumes: G_v = g (onehot_v(y) - exp(z'_v - lse)) f'(z_v). One CTA per row.
 namespace grpo {
 
-cudaError_t launch_fwds_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
+cudaError_t launch_fwds_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                              const TileArgs& args, int grid, cudaStream_t stream) {
-  tc_gemm_kernel<MODE_FWDS><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, stream>>>(map_a, map_b,
-                                                                             args);
-  return cudaGetLastError();
+  return ctas == 2 ? launch_gemm_variant<MODE_FWDS, 2>(map_a, map_b, args, grid, stream)
+                   : launch_gemm_variant<MODE_FWDS, 1>(map_a, map_b, args, grid, stream);
 }
 
 cudaError_t prepare_fwds_gemm() {
-  return cudaFuncSetAttribute(tc_gemm_kernel<MODE_FWDS>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
+  cudaError_t e = prepare_gemm_variant<MODE_FWDS, 1>();
+  return e == cudaSuccess ? prepare_gemm_variant<MODE_FWDS, 2>() : e;
 }
 
 __device__ __forceinline__ float half_bits_to_float(uint32_t h16) {

@@ -143,13 +143,28 @@ __device__ __forceinline__ void logit_transform(const TileArgs& a, float (&v)[32
   }
 }
 
-template <int MODE>
+// Per-variant geometry. CTAS = 1: one CTA computes a 128 x 256 tile. CTAS = 2:
+// a CTA pair computes a 256 x 256 tile with tcgen05 cta_group::2; each CTA
+// loads its own 128 A rows and half of the B tile (128 of its 256 rows/cols),
+// the leader issues the MMAs, and each CTA's TMEM holds its 128 rows.
+template <int CTAS>
+struct PairCfg {
+  static constexpr int kBRows = BN / CTAS;             // B rows (cols) per CTA
+  static constexpr int kBBytes = kBRows * BK * 2;
+  static constexpr int kStageBytes = A_BYTES + kBBytes;
+  static constexpr int kStages = CTAS == 2 ? 6 : STAGES;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+};
+
+template <int MODE, int CTAS>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b, const TileArgs args) {
+  using C = PairCfg<CTAS>;
+  constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[STAGES];
-  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t full_bar[kStages];
+  __shared__ __align__(8) uint64_t empty_bar[kStages];
   __shared__ __align__(8) uint64_t tfull_bar[2];
   __shared__ __align__(8) uint64_t tempty_bar[2];
   __shared__ __align__(8) uint64_t drain_bar;
@@ -164,15 +179,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int* abort_flag = &abort_sh;
+  const uint32_t rank = CTAS == 2 ? cluster_ctarank() : 0u;
+  const int cta_slot = static_cast<int>(blockIdx.x) / CTAS;  // pair index
+  const int n_slots = static_cast<int>(gridDim.x) / CTAS;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full_bar[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], CTAS);  // pair: both CTAs' producers arrive (leader's)
       mbar_init(&empty_bar[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull_bar[b], 1);
-      mbar_init(&tempty_bar[b], 4);
+      mbar_init(&tempty_bar[b], 4 * CTAS);  // every epilogue warp of the pair
     }
     mbar_init(&drain_bar, 1);
     abort_sh = 0;
@@ -183,16 +201,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tma_prefetch_desc(&map_b);
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_base_sh, TMEM_COLS);
-    tmem_relinquish();
+    if (CTAS == 2) {
+      tmem_alloc_pair(&tmem_base_sh, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&tmem_base_sh, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (CTAS == 2) cluster_sync(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
 
   const int n_rb = launch_row_blocks(args);
-  const int n_units = n_rb * args.n_cols;
+  const int n_ru = (n_rb + CTAS - 1) / CTAS;  // row units: 128 * CTAS rows each
+  const int n_units = n_ru * args.n_cols;
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
@@ -200,50 +224,73 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t it = 0;
       bool ok = true;
       const uint64_t pol_a = policy_evict_last();
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        int li, col, t0, t1;
-        decode_unit(u, n_rb, args.n_cols, args.group_rows, li, col);
+      for (int u = cta_slot; u < n_units && ok; u += n_slots) {
+        int ru, col, t0, t1;
+        decode_unit(u, n_ru, args.n_cols, args.group_rows, ru, col);
         unit_tiles<MODE>(args, col, t0, t1);
+        // A CTA whose row block lies past the list computes its partner's rows
+        // again and stores nothing.
+        int li = ru * CTAS + static_cast<int>(rank);
+        if (li >= n_rb) li = ru * CTAS;
         const int a_row = (MODE == MODE_DH ? li : global_rb(args, li)) * BM;
         for (int t = t0; t < t1 && ok; ++t) {
           for (int k = 0; k < args.k_iters; ++k, ++it) {
-            const int s = it % STAGES;
-            const uint32_t round = it / STAGES;
+            const int s = it % kStages;
+            const uint32_t round = it / kStages;
             if (!mbar_wait(&empty_bar[s], (round & 1u) ^ 1u, abort_flag, args.status)) {
               ok = false;
               break;
             }
-            uint8_t* a_dst = smem + s * STAGE_BYTES;
+            uint8_t* a_dst = smem + s * C::kStageBytes;
             uint8_t* b_dst = a_dst + A_BYTES;
-            mbar_arrive_expect_tx(&full_bar[s], STAGE_BYTES);
-            tma_load_2d_hint(a_dst, &map_a, &full_bar[s], k * BK, a_row, pol_a);
-            if (MODE == MODE_DH) {
-              // W[v0 + k*64 .. +64, d0 .. d0+256) as four 64x64 MN-major boxes.
+            if (CTAS == 2) {
+              // Both CTAs count their bytes on the leader's barrier.
+              const uint32_t lead = mapa_shared(smem_u32(&full_bar[s]), 0);
+              mbar_arrive_expect_tx_cluster(lead, C::kStageBytes);
+              tma_load_2d_pair(a_dst, &map_a, lead, k * BK, a_row, pol_a);
+              if (MODE == MODE_DH) {
 #pragma unroll
-              for (int j = 0; j < 4; ++j)
-                tma_load_2d(b_dst + j * (BK * 64 * 2), &map_b, &full_bar[s],
-                            t * BN + j * 64, args.v0 + k * BK);
+                for (int j = 0; j < C::kBRows / 64; ++j)
+                  tma_load_2d_pair_nohint(b_dst + j * (BK * 64 * 2), &map_b, lead,
+                                          t * BN + static_cast<int>(rank) * C::kBRows + j * 64,
+                                          args.v0 + k * BK);
+              } else {
+                tma_load_2d_pair_nohint(b_dst, &map_b, lead, k * BK,
+                                        args.v0 + t * BN + static_cast<int>(rank) * C::kBRows);
+              }
             } else {
-              tma_load_2d(b_dst, &map_b, &full_bar[s], k * BK, args.v0 + t * BN);
+              mbar_arrive_expect_tx(&full_bar[s], C::kStageBytes);
+              tma_load_2d_hint(a_dst, &map_a, &full_bar[s], k * BK, a_row, pol_a);
+              if (MODE == MODE_DH) {
+                // W[v0 + k*64 .. +64, d0 .. d0+256) as four 64x64 MN-major boxes.
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  tma_load_2d(b_dst + j * (BK * 64 * 2), &map_b, &full_bar[s],
+                              t * BN + j * 64, args.v0 + k * BK);
+              } else {
+                tma_load_2d(b_dst, &map_b, &full_bar[s], k * BK, args.v0 + t * BN);
+              }
             }
           }
         }
       }
-      if (!ok) {
-        // Abort path: let the copies already issued land before the CTA exits.
-        for (uint32_t j = (it >= STAGES ? it - STAGES : 0); j < it; ++j)
-          drain_wait(&full_bar[j % STAGES], (j / STAGES) & 1u);
+      if (!ok && rank == 0) {
+        // Abort path: let the copies already issued land before the CTA exits
+        // (the leader's barriers count the pair's copies; the peer passes the
+        // closing cluster barrier only after this).
+        for (uint32_t j = (it >= kStages ? it - kStages : 0); j < it; ++j)
+          drain_wait(&full_bar[j % kStages], (j / kStages) & 1u);
       }
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(BM, BN, false, MODE == MODE_DH);
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BM * CTAS, BN, false, MODE == MODE_DH);
       uint32_t it = 0, tile_it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        int li, col, t0, t1;
-        decode_unit(u, n_rb, args.n_cols, args.group_rows, li, col);
+      for (int u = cta_slot; u < n_units && ok; u += n_slots) {
+        int ru, col, t0, t1;
+        decode_unit(u, n_ru, args.n_cols, args.group_rows, ru, col);
         unit_tiles<MODE>(args, col, t0, t1);
         for (int t = t0; t < t1 && ok; ++t, ++tile_it) {
           const uint32_t buf = tile_it & 1u;
@@ -255,14 +302,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + buf * BN;
           for (int k = 0; k < args.k_iters; ++k, ++it) {
-            const int s = it % STAGES;
-            const uint32_t round = it / STAGES;
+            const int s = it % kStages;
+            const uint32_t round = it / kStages;
             if (!mbar_wait(&full_bar[s], round & 1u, abort_flag, args.status)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t a_addr = smem_u32(smem + s * STAGE_BYTES);
+            const uint32_t a_addr = smem_u32(smem + s * C::kStageBytes);
             const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
@@ -277,17 +324,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               } else {
                 bdesc = sdesc_sw128(b_addr + kk * 32, 16, 1024);
               }
-              tc_mma_bf16(d_tmem, adesc, bdesc, idesc, (k | kk) != 0 ? 1u : 0u);
+              const uint32_t acc = (k | kk) != 0 ? 1u : 0u;
+              if (CTAS == 2) tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, acc);
+              else tc_mma_bf16(d_tmem, adesc, bdesc, idesc, acc);
             }
-            tc_commit(&empty_bar[s]);
+            if (CTAS == 2) tc_commit_pair_multicast(&empty_bar[s], 0x3);
+            else tc_commit(&empty_bar[s]);
           }
           if (!ok) break;
-          tc_commit(&tfull_bar[buf]);
+          if (CTAS == 2) tc_commit_pair_multicast(&tfull_bar[buf], 0x3);
+          else tc_commit(&tfull_bar[buf]);
         }
       }
       // Make sure every MMA issued by this thread has finished before TMEM is
       // released (matters only on the abort path).
-      tc_commit(&drain_bar);
+      if (CTAS == 2) tc_commit_pair(&drain_bar); else tc_commit(&drain_bar);
       drain_wait(&drain_bar, 0);
     }
   } else {
@@ -297,13 +348,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     uint32_t tile_it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      int li, col, t0, t1;
-      decode_unit(u, n_rb, args.n_cols, args.group_rows, li, col);
+    // Where this CTA's epilogue warps report a drained accumulator: the
+    // leader's barrier (pair) or the CTA's own.
+    const uint32_t tempty_addr0 =
+        CTAS == 2 ? mapa_shared(smem_u32(&tempty_bar[0]), 0) : smem_u32(&tempty_bar[0]);
+    for (int u = cta_slot; u < n_units && ok; u += n_slots) {
+      int ru, col, t0, t1;
+      decode_unit(u, n_ru, args.n_cols, args.group_rows, ru, col);
       unit_tiles<MODE>(args, col, t0, t1);
+      const int li = ru * CTAS + static_cast<int>(rank);
+      const bool block_ok = li < n_rb;
       const int lrow = li * BM + lrow_in_tile;  // row of the chunk workspace
-      const long long grow = static_cast<long long>(global_rb(args, li)) * BM + lrow_in_tile;
-      const bool valid = grow < args.n_total;
+      const long long grow =
+          block_ok ? static_cast<long long>(global_rb(args, li)) * BM + lrow_in_tile : 0;
+      const bool valid = block_ok && grow < args.n_total;
 
       // Per-row state.
       float m2 = -INFINITY, ssum = 0.f;  // FWD
@@ -348,8 +406,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                   st_global_v4(dst + j * 8, hpk[4 * j], hpk[4 * j + 1], hpk[4 * j + 2],
                                hpk[4 * j + 3]);
               } else {
-                for (int j = 0; j < 32 && col0 + j < args.vocab; ++j)
-                  dst[j] = static_cast<uint16_t>(pack_f16x2(v[j], 0.f) & 0xffffu);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (col0 + j < args.vocab)
+                    dst[j] = static_cast<uint16_t>(pack_f16x2(v[j], 0.f) & 0xffffu);
               }
             }
             if (col0 + 32 > args.vocab) {
@@ -477,7 +537,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+        if (lane == 0) {
+          if (CTAS == 2) mbar_arrive_cluster(tempty_addr0 + buf * 8u);
+          else mbar_arrive(&tempty_bar[buf]);
+        }
       }
       if (is_fwd(MODE) && ok && valid) {
         args.part_m[static_cast<long long>(col) * args.part_ld + grow] = m2;
@@ -487,9 +550,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if (CTAS == 2) cluster_sync(); else __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+  if (warp == 1) {
+    if (CTAS == 2) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
+  }
 }
 
 }  // namespace grpo

@@ -79,14 +79,44 @@ constexpr int kGformThreads = 256;
 constexpr int kFinalizeThreads = 256;
 constexpr int kMaxFinalizeBlocks = 1024;
 
-// Each launcher lives in the translation unit that instantiates its kernel.
+// Launch of one GEMM variant; a CTA pair (CTAS = 2) runs as a 2-CTA cluster.
+// `grid` counts CTAs (a multiple of CTAS).
+template <int MODE, int CTAS>
+cudaError_t launch_gemm_variant(const CUtensorMap& map_a, const CUtensorMap& map_b,
+                                const TileArgs& args, int grid, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = PairCfg<CTAS>::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (CTAS == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, CTAS>, map_a, map_b, args);
+}
+
+template <int MODE, int CTAS>
+cudaError_t prepare_gemm_variant() {
+  return cudaFuncSetAttribute(tc_gemm_kernel<MODE, CTAS>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              PairCfg<CTAS>::kSmemBytes);
+}
+
+// Each launcher lives in the translation unit that instantiates its kernels;
+// ctas selects the single-CTA (1) or CTA-pair (2) variant.
 cudaError_t prepare_fwd_gemm();   // opt-in to the large dynamic smem
 cudaError_t prepare_bwd_gemms();
-cudaError_t launch_fwd_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
+cudaError_t launch_fwd_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                             const TileArgs& args, int grid, cudaStream_t stream);
-cudaError_t launch_bwdg_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
+cudaError_t launch_bwdg_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                              const TileArgs& args, int grid, cudaStream_t stream);
-cudaError_t launch_dh_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
+cudaError_t launch_dh_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                            const TileArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_row_plan(const uint8_t* mask, long long n, int n_rb, int* rb_list,
                             int* n_active, double* msum, cudaStream_t stream);
@@ -94,7 +124,7 @@ cudaError_t launch_zero_padding_blocks(const uint8_t* mask, long long n, int n_r
                                        void* dH, int sms, cudaStream_t stream);
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t stream);
 cudaError_t prepare_fwds_gemm();
-cudaError_t launch_fwds_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
+cudaError_t launch_fwds_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                              const TileArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_finalize_gform(const GformArgs& a, int rows, cudaStream_t stream);
 cudaError_t launch_finish_loss(const FinishArgs& a, cudaStream_t stream);

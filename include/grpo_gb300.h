@@ -74,6 +74,11 @@ typedef struct grpo_shape {
  * Logits must stay within fp16 range (|z'| < 65504). */
 #define GRPO_FLAG_STORED_LOGITS 1u
 
+/* grpo_params.flags bit: run every GEMM as one CTA per 128-row tile instead
+ * of the default CTA pair per 256-row tile (tcgen05 cta_group::2). Same
+ * results up to fp32 summation order; kept for comparison and debugging. */
+#define GRPO_FLAG_SINGLE_CTA 2u
+
 typedef struct grpo_params {
   float eps_low;          /* ratio clip: lower bound 1 - eps_low (0.2)         */
   float eps_high;         /* ratio clip: upper bound 1 + eps_high (0.2)        */
@@ -81,7 +86,7 @@ typedef struct grpo_params {
   float loss_denominator; /* <= 0: divide by sum(mask); > 0: divide by this    */
   int32_t chunk_tokens;   /* rows per backward chunk; 0 = automatic            */
   int32_t vocab_block;    /* vocab columns per backward block; 0 = automatic   */
-  uint32_t flags;         /* 0 or GRPO_FLAG_STORED_LOGITS                      */
+  uint32_t flags;         /* GRPO_FLAG_* bits, or 0                           */
   uint32_t reserved;      /* must be 0                                         */
   /* Logit transforms ("GRPO with 7x longer context", the options of the
    * selective log-softmax call: logit scale multiply/divide, softcapping,

@@ -91,7 +91,7 @@ def test_workspace_size_rejects_bad_shapes(clp, n, d, v, want):
 
 def test_bad_params_rejected(clp):
     p = clp.make_params()
-    p.flags = 2  # not a defined flag bit
+    p.flags = 8  # not a defined flag bit
     with pytest.raises(clp.GrpoError) as e:
         clp.grpo_workspace_size(10, 16, 50, 1, p)
     assert e.value.code == -1

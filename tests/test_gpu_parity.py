@@ -332,3 +332,31 @@ def test_stored_logits_bad_id_and_all_masked(clp):
     assert st == -8 and math.isnan(logp[9]) and math.isnan(L)
     L, logp, dH, st = gpu_loss(clp, p, old, old, params, mask=torch.zeros_like(p.mask))
     assert st == 0 and L == 0.0 and np.all(logp == 0) and np.all(dH == 0)
+
+
+# -------------------------------------- single-CTA GEMMs (flag) vs pairs ---
+
+SINGLE = 2  # GRPO_FLAG_SINGLE_CTA
+
+
+@pytest.mark.parametrize("flags", [SINGLE, SINGLE | STORED])
+@pytest.mark.parametrize("N,T,D,V,chunk,vblock,padded", RAGGED[:4])
+def test_single_cta_gemms(clp, flags, N, T, D, V, chunk, vblock, padded):
+    G = 4 if (N // T) % 4 == 0 else 1
+    p = synth.make_problem("tiny", seed=N + D + V + 2, prompts=(N // T) // G, G=G, T=T, D=D,
+                           V=V, lengths=(max(1, T // 3), T) if padded else None)
+    old, ref, want = oracle_case(p)
+    params = clp.make_params(chunk_tokens=chunk, vocab_block=vblock, flags=flags)
+    check(gpu_loss(clp, p, old, ref, params), want, p.mask, f"single {flags} {N}x{D}x{V}")
+
+
+def test_pair_and_single_cta_agree(clp):
+    # Odd number of 128-row blocks: the last CTA pair has one real row block.
+    p = synth.make_problem("tiny", seed=14, T=640, prompts=1, G=1, D=256, V=3000)
+    old, ref, _ = oracle_case(p)
+    for extra in (0, STORED):
+        L1, lp1, dH1, s1 = gpu_loss(clp, p, old, ref, clp.make_params(flags=extra))
+        L2, lp2, dH2, s2 = gpu_loss(clp, p, old, ref, clp.make_params(flags=extra | SINGLE))
+        assert s1 == 0 and s2 == 0
+        assert np.abs(lp1 - lp2).max() <= 1e-5 and abs(L1 - L2) <= 1e-5 * abs(L1)
+        assert np.linalg.norm(dH1 - dH2) <= 1e-2 * np.linalg.norm(dH1)
