@@ -168,6 +168,31 @@ def oracle_rows_per_second(p, target_s, seed, cores_note):
     return n, t
 
 
+def kernel_source_hash():
+    """Hash of the CUDA sources: DRAM traffic recorded for other sources is stale."""
+    import hashlib
+
+    csrc = os.path.join(ROOT, "chunked_log_prob_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, backward):
+    """DRAM bytes per call from a committed ncu summary, if it matches these sources."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}_{backward}.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_call")
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -381,7 +406,9 @@ def run_ours(args):
             "peak_source": f"{peak_src} bf16 sustained (cuBLAS loop)",
             "kernel": "grpo_loss_fwd_bwd: %d launches per call, %d chunks x %d vocab blocks" % (
                 plan["launches_loss"], plan["n_chunks"], plan["n_vocab_blocks"]),
-            "flops_per_call": fl_exec, "traffic": None,
+            "flops_per_call": fl_exec,
+            "traffic": recorded_traffic(p.name, "stored" if stored else "recompute"),
+            "traffic_unit": "DRAM bytes per call (ncu dram__bytes_read.sum + write.sum)",
         },
         "fwd_only": None if fwd_ms is None else {
             "ms": fwd_ms, "tflops": 2.0 * D * V * N / (fwd_ms / 1e3) / 1e12,
