@@ -132,6 +132,30 @@ class ClockSampler:
 
 # ------------------------------------------------------------- helpers ----
 
+def rank_env():
+    """(world size, rank, local rank) as torch.distributed.run sets them."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(seed, rank):
+    """Each replica draws its own batch: the job's work grows with the ranks (weak scaling)."""
+    return seed + rank
+
+
+def max_over_ranks(x):
+    """The job's time is its slowest rank's: max of a float over all ranks."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def flops_per_token(D, V):
     # 2DV forward + 4DV backward (recomputed logits + G W), per valid token.
     return 6.0 * D * V
@@ -206,9 +230,7 @@ def run_ours(args):
     import torch
     import torch.distributed as dist
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     torch.cuda.set_device(local)
@@ -224,7 +246,7 @@ def run_ours(args):
     if args.seq_len > 0 and synth.WORKLOADS[args.workload]["lengths"] is not None:
         lo, hi = synth.WORKLOADS[args.workload]["lengths"]
         over["lengths"] = (min(lo, args.seq_len), args.seq_len)
-    p = synth.make_problem(args.workload, seed=args.seed + rank, device=dev, **over)
+    p = synth.make_problem(args.workload, seed=rank_seed(args.seed, rank), device=dev, **over)
     torch.cuda.empty_cache()  # drop the generator's fp32 temporaries
     N, D, V, T = p.n_tokens, p.hidden_size, p.vocab, p.seq_len
     stored = args.backward == "stored"
@@ -274,11 +296,7 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    ms_t = torch.tensor([ms], device=dev, dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
+    ms_max = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
 
     # The other backward variant on the same inputs (reported beside the headline).
     variant = None
@@ -293,10 +311,7 @@ def run_ours(args):
             step(other)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
-        v_ms = torch.tensor([ev0.elapsed_time(ev1) / args.steps], device=dev, dtype=torch.float64)
-        if world > 1:
-            dist.all_reduce(v_ms, op=dist.ReduceOp.MAX)
-        v_ms = float(v_ms.item())
+        v_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
         v_exec = (6.0 if stored else 4.0) * D * V * p.n_valid
         variant = {"backward": "recomputed logits" if stored else "stored fp16 logits",
                    "ms_per_step": v_ms, "value": world * p.n_valid / (v_ms / 1e3),
@@ -347,14 +362,11 @@ def run_ours(args):
             e2e_step()
         ev1.record(stream)
         torch.cuda.synchronize(dev)
-        e_ms = torch.tensor([ev0.elapsed_time(ev1) / args.steps], device=dev,
-                            dtype=torch.float64)
-        if world > 1:
-            dist.all_reduce(e_ms, op=dist.ReduceOp.MAX)
+        e_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
         h2d = sum(x.numel() * x.element_size() for x in host_in)
         d2h = loss_h.numel() * 4 + dH_h.numel() * 2
-        e2e = {"value": world * valid / (float(e_ms.item()) / 1e3), "unit": "tokens/s",
-               "ms_per_step": float(e_ms.item()), "h2d_bytes_per_step": h2d,
+        e2e = {"value": world * valid / (e_ms / 1e3), "unit": "tokens/s",
+               "ms_per_step": e_ms, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h,
                "note": "pinned host hidden/ids/mask/old/ref/adv in, loss + dH out; "
                        "lm_head W resident on the device"}
@@ -434,7 +446,8 @@ def run_ours(args):
 # ----------------------------------------------------------- reference ----
 
 def run_reference(args):
-    rank = int(os.environ.get("RANK", "0"))
+    # The oracle runs on rank 0's host cores only; other ranks exit without work.
+    _, rank, _ = rank_env()
     if rank != 0:
         return
     import numpy as np
