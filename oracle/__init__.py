@@ -18,4 +18,5 @@ from .grpo_oracle import (  # noqa: F401
     rows_fwd_bwd,
     selective_logp,
     token_terms,
+    token_weights,
 )

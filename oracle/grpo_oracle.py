@@ -44,6 +44,11 @@ notes of the repository):
 * sequence b of token t is t // T (completions of length T laid end to end);
   the advantage of the sequence is broadcast over its tokens.
 * masked rows get logp = 0 and a zero gradient row.
+* per-sequence aggregation (optional, a reading of the GRPO objective's
+  per-completion normalisation; the pages name no aggregation at all):
+  L = (1/B') sum_b (1/len_b) sum_{t in b} m_t l_t with len_b = sum_{t in b} m_t
+  and B' the number of completions with len_b > 0 (or a caller-given
+  denominator > 0 in place of B').
 * logit transforms ("GRPO with 7x longer context", notes under the
   chunked_hidden_states_selective_log_softmax call: softcapping, temperature
   and the logit scale multiply/divide): applied to the raw logit z in the
@@ -170,16 +175,44 @@ def broadcast_advantage(adv_per_seq, n_tokens: int, seq_len: int) -> np.ndarray:
     return a[np.arange(n_tokens) // seq_len]
 
 
-def grpo_loss(logp, old, ref, adv_per_seq, mask, seq_len, eps_low=0.2,
-              eps_high=0.2, beta=0.001, loss_denominator=0.0):
-    """Masked token-mean GRPO loss L and g_t = dL/dlogp_t.
+def token_weights(mask, seq_len, aggregation="token", loss_denominator=0.0):
+    """w_t with L = sum_t w_t l_t: m_t / M (token mean) or m_t / (len_b B')
+    (mean over completions of the per-completion token mean)."""
+    m = _f64(mask)
+    n = m.shape[0]
+    if aggregation == "token":
+        M = float(loss_denominator) if loss_denominator > 0 else float(m.sum())
+        return (m / M if M != 0.0 else np.zeros(n)), M
+    lens = m.reshape(-1, seq_len).sum(axis=1)
+    B = float(loss_denominator) if loss_denominator > 0 else float((lens > 0).sum())
+    if B == 0.0:
+        return np.zeros(n), B
+    len_tok = np.repeat(lens, seq_len)
+    w = np.where(m > 0, m / np.where(len_tok > 0, len_tok, 1.0) / B, 0.0)
+    return w, B
 
-    Returns (L, g [N], loss_tok [N], M). Masked tokens have g_t = 0.
+
+def grpo_loss(logp, old, ref, adv_per_seq, mask, seq_len, eps_low=0.2,
+              eps_high=0.2, beta=0.001, loss_denominator=0.0, aggregation="token"):
+    """Masked GRPO loss L and g_t = dL/dlogp_t.
+
+    aggregation "token": L = sum_t m_t l_t / M; "sequence": mean over
+    completions of each completion's token mean. Returns (L, g [N],
+    loss_tok [N], M) with M the token count (token) or completion count
+    (sequence) used as denominator. Masked tokens have g_t = 0.
     """
     logp = _f64(logp)
     n = logp.shape[0]
     m = _f64(mask)
     A = broadcast_advantage(adv_per_seq, n, seq_len)
+    if aggregation != "token":
+        w, B = token_weights(mask, seq_len, aggregation, loss_denominator)
+        lp = np.where(m > 0, logp, 0.0)
+        od = np.where(m > 0, _f64(old), 0.0)
+        rf = np.where(m > 0, _f64(ref), 0.0)
+        loss_tok, dloss_tok, _, _ = token_terms(lp, od, rf, A, eps_low, eps_high, beta)
+        L = float(np.sum(np.where(w > 0, w * loss_tok, 0.0)))
+        return L, np.where(w > 0, w * dloss_tok, 0.0), np.where(m > 0, loss_tok, 0.0), B
     M = float(loss_denominator) if loss_denominator > 0 else float(m.sum())
     # Masked tokens contribute nothing; their logp (written as 0) never enters
     # the arithmetic, so their inputs may hold anything.
@@ -228,7 +261,7 @@ def grad_hidden(hidden, W, ids, g, row_block: int = ROW_BLOCK, xf: Transform = I
 
 def loss_fwd_bwd(hidden, W, ids, mask, old, ref, adv_per_seq, seq_len,
                  eps_low=0.2, eps_high=0.2, beta=0.001, loss_denominator=0.0,
-                 xf: Transform = IDENTITY):
+                 xf: Transform = IDENTITY, aggregation="token"):
     """The whole path: logp, the loss, and the gradient to the hidden states.
 
     Returns a dict with L, logp (masked rows 0), lse, g, dH, M.
@@ -237,7 +270,7 @@ def loss_fwd_bwd(hidden, W, ids, mask, old, ref, adv_per_seq, seq_len,
     logp, lse = selective_logp(hidden, W, ids, xf=xf)
     logp = np.where(m > 0, logp, 0.0)
     L, g, loss_tok, M = grpo_loss(logp, old, ref, adv_per_seq, mask, seq_len,
-                                  eps_low, eps_high, beta, loss_denominator)
+                                  eps_low, eps_high, beta, loss_denominator, aggregation)
     dH = grad_hidden(hidden, W, ids, g, xf=xf)
     return {"L": L, "logp": logp, "lse": lse, "g": g, "dH": dH, "M": M,
             "loss_tok": loss_tok}

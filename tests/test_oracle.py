@@ -473,3 +473,52 @@ def test_transformed_dH_matches_finite_differences(xf):
     # A backward that forgets the transform's derivative is caught.
     no_chain = oracle.grad_hidden(h, W, y, out["g"])
     assert np.linalg.norm(fd - no_chain) / np.linalg.norm(fd) > 1e-2
+
+
+# ------------------------------------------------- per-sequence aggregation --
+
+def test_sequence_mean_equals_token_mean_without_padding():
+    logp, adv, mask, T, eps = _loss_case(50)
+    rng = np.random.default_rng(51)
+    old = logp + rng.normal(0, 0.1, 12)
+    ref = logp + rng.normal(0, 0.1, 12)
+    a = oracle.grpo_loss(logp, old, ref, adv, mask, T, eps, eps, 0.02)
+    b = oracle.grpo_loss(logp, old, ref, adv, mask, T, eps, eps, 0.02, aggregation="sequence")
+    assert abs(a[0] - b[0]) < 1e-15 and np.allclose(a[1], b[1], atol=1e-17)
+
+
+def test_sequence_mean_hand_case():
+    # Two completions of T = 3: lengths 1 and 3, on-policy, beta = 0:
+    # l_t = -A_b, so L = (1/2) * (-A_0 + (-A_1)) whatever the lengths.
+    logp = np.array([-1.0, -2.0, -3.0, -1.5, -2.5, -0.5])
+    mask = np.array([1, 0, 0, 1, 1, 1])
+    adv = np.array([0.7, -0.3])
+    L, g, _, B = oracle.grpo_loss(logp, logp, logp, adv, mask, 3, 0.2, 0.2, 0.0,
+                                  aggregation="sequence")
+    assert B == 2.0 and abs(L - (-(0.7 - 0.3) / 2)) < 1e-15
+    assert np.allclose(g, [-0.7 / 2, 0, 0, 0.3 / 6, 0.3 / 6, 0.3 / 6], atol=1e-16)
+    # Token mean weighs the long completion three times as much.
+    Lt, _, _, _ = oracle.grpo_loss(logp, logp, logp, adv, mask, 3, 0.2, 0.2, 0.0)
+    assert abs(Lt - (-(0.7 - 3 * 0.3) / 4)) < 1e-15
+
+
+def test_sequence_mean_empty_completion_and_fd():
+    rng = np.random.default_rng(52)
+    T = 4
+    logp = -rng.uniform(1, 5, 12)
+    mask = np.array([1, 1, 0, 0, 0, 0, 0, 0, 1, 1, 1, 0])  # completion 1 is empty
+    adv = rng.standard_normal(3)
+    old = logp + rng.normal(0, 0.1, 12)
+    ref = logp + rng.normal(0, 0.1, 12)
+    L, g, _, B = oracle.grpo_loss(logp, old, ref, adv, mask, T, 0.2, 0.2, 0.05,
+                                  aggregation="sequence")
+    assert B == 2.0
+    step = 1e-6
+    for t in range(12):
+        p_, m_ = logp.copy(), logp.copy()
+        p_[t] += step
+        m_[t] -= step
+        fd = (oracle.grpo_loss(p_, old, ref, adv, mask, T, 0.2, 0.2, 0.05, aggregation="sequence")[0]
+              - oracle.grpo_loss(m_, old, ref, adv, mask, T, 0.2, 0.2, 0.05,
+                                 aggregation="sequence")[0]) / (2 * step)
+        assert abs(fd - g[t]) < 1e-8
