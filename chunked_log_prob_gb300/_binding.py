@@ -36,7 +36,8 @@ class GrpoParams(ctypes.Structure):
                 ("chunk_tokens", ctypes.c_int32), ("vocab_block", ctypes.c_int32),
                 ("flags", ctypes.c_uint32), ("reserved", ctypes.c_uint32),
                 ("logit_scale_multiply", ctypes.c_float), ("logit_scale_divide", ctypes.c_float),
-                ("logit_softcapping", ctypes.c_float), ("temperature", ctypes.c_float)]
+                ("logit_softcapping", ctypes.c_float), ("temperature", ctypes.c_float),
+                ("workspace_limit_bytes", ctypes.c_uint64)]
 
 
 class GrpoPlanInfo(ctypes.Structure):
@@ -86,6 +87,11 @@ EXPORTED = ("grpo_default_params", "grpo_workspace_size", "grpo_logp_fwd",
             "grpo_loss_fwd_bwd", "grpo_get_plan", "grpo_read_device_status",
             "grpo_logp_fwd_noalloc", "grpo_status_string")
 
+FLAG_STORED_LOGITS = 1
+FLAG_SINGLE_CTA = 2
+FLAG_SEQUENCE_MEAN = 4
+FLAG_FIT_FREE_MEMORY = 8
+
 # Largest batch of the workspace-free forward (its static device scratch).
 NOALLOC_MAX_TOKENS = 8192
 
@@ -97,7 +103,7 @@ def status_string(code: int) -> str:
 def make_params(eps_low=0.2, eps_high=0.2, beta=0.001, loss_denominator=0.0,
                 chunk_tokens=0, vocab_block=0, *, logit_scale_multiply=0.0,
                 logit_scale_divide=0.0, logit_softcapping=0.0, temperature=0.0,
-                flags=0) -> GrpoParams:
+                flags=0, workspace_limit_bytes=0) -> GrpoParams:
     p = GrpoParams()
     lib.grpo_default_params(ctypes.byref(p))
     p.eps_low, p.eps_high, p.beta = eps_low, eps_high, beta
@@ -106,6 +112,7 @@ def make_params(eps_low=0.2, eps_high=0.2, beta=0.001, loss_denominator=0.0,
     p.logit_scale_multiply, p.logit_scale_divide = logit_scale_multiply, logit_scale_divide
     p.logit_softcapping, p.temperature = logit_softcapping, temperature
     p.flags = flags
+    p.workspace_limit_bytes = int(workspace_limit_bytes)
     return p
 
 

@@ -29,6 +29,7 @@ constexpr size_t kOffStatus = 0;       // int
 constexpr size_t kOffCounter = 4;      // unsigned
 constexpr size_t kOffMsum = 8;         // double
 constexpr size_t kOffActive = 16;      // int: length of the active row-block list
+constexpr size_t kOffNonempty = 20;    // int: completions with any unmasked token
 constexpr size_t kOffPartials = 64;    // double[kMaxFinalizeBlocks]
 static_assert(kOffPartials + kMaxFinalizeBlocks * sizeof(double) <= kHeaderBytes, "header");
 
@@ -45,7 +46,7 @@ struct Layout {
   int chunk_rows;   // backward chunk (multiple of BM)
   int vblock;       // backward vocab block (multiple of BN)
   bool need_acc;    // more than one vocab block -> fp32 dH accumulator
-  size_t off_pm, off_ps, off_zy, off_lse, off_g, off_rbl, off_lt, off_G, off_acc, total;
+  size_t off_pm, off_ps, off_zy, off_lse, off_g, off_rbl, off_lt, off_seq, off_G, off_acc, total;
 };
 
 int auto_chunk_blocks(long long n_rb_total, int n_dt, int sms, int max_units) {
@@ -126,6 +127,21 @@ int auto_stored_chunk_blocks(long long n_rb_total, int n_dt, int nvt, int sms, i
   return best;
 }
 
+// Workspace budget of a call in bytes (0 = none): the caller's limit, or half
+// of the device's free memory with GRPO_FLAG_FIT_FREE_MEMORY.
+size_t workspace_budget(const grpo_params* p) {
+  if (p == nullptr) return 0;
+  size_t budget = static_cast<size_t>(p->workspace_limit_bytes);
+  if ((p->flags & GRPO_FLAG_FIT_FREE_MEMORY) != 0) {
+    size_t free_b = 0, total_b = 0;
+    if (cudaMemGetInfo(&free_b, &total_b) == cudaSuccess) {
+      const size_t half = free_b / 2;
+      budget = budget == 0 ? half : std::min(budget, half);
+    }
+  }
+  return budget;
+}
+
 int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   L->ctas = (p != nullptr && (p->flags & GRPO_FLAG_SINGLE_CTA) != 0) ? 1 : 2;
   L->stored = p != nullptr && (p->flags & GRPO_FLAG_STORED_LOGITS) != 0;
@@ -137,34 +153,13 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   L->V = s->vocab;
   L->nvt = static_cast<int>(cdiv(s->vocab, BN));
   const int n_dt = static_cast<int>(cdiv(s->hidden, BN));
-  // Chunks are whole row units (BM * ctas rows: what one CTA pair covers).
-  const long long ru_rows = static_cast<long long>(BM) * L->ctas;
-  const long long n_ru_total = cdiv(L->nr, ru_rows);
-  const int slots = sms / L->ctas;
-  const int max_stored_units = std::max(1, stored_max_blocks(L->ldS) / L->ctas);
-  long long crows;
-  if (p && p->chunk_tokens > 0) {
-    crows = cdiv(p->chunk_tokens, ru_rows) * ru_rows;
-  } else if (L->stored) {
-    crows = (sms > 0 ? auto_stored_chunk_blocks(n_ru_total, n_dt, L->nvt, slots,
-                                                max_stored_units)
-                     : std::min<long long>(n_ru_total, max_stored_units)) *
-            ru_rows;
-  } else if (sms > 0) {
-    crows = auto_chunk_blocks(n_ru_total, n_dt, slots, kMaxAutoChunkBlocks / L->ctas) * ru_rows;
-  } else {  // sizing without a device: the largest automatic chunk
-    crows = std::min<long long>(n_ru_total, kMaxAutoChunkBlocks / L->ctas) * ru_rows;
-  }
-  crows = std::min(crows, n_ru_total * ru_rows);
-  if (crows > INT_MAX / 2) return GRPO_ERR_UNSUPPORTED_SHAPE;
-  L->chunk_rows = static_cast<int>(crows);
   long long vb = (p && p->vocab_block > 0) ? p->vocab_block : kAutoVocabBlock;
   vb = cdiv(vb, BN) * BN;
   vb = std::min<long long>(vb, static_cast<long long>(L->nvt) * BN);
-  L->vblock = static_cast<int>(vb);
+  L->vblock = L->stored ? static_cast<int>(L->ldS) : static_cast<int>(vb);
   L->need_acc = !L->stored && L->vblock < L->V;
-  if (L->stored) L->vblock = static_cast<int>(L->ldS);
 
+  // Everything before the backward chunk block depends on N only.
   size_t off = kHeaderBytes;
   const size_t part = static_cast<size_t>(kMaxSplits) * L->nr * sizeof(float);
   L->off_pm = off; off = align_up(off + part, 256);
@@ -174,12 +169,50 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   L->off_g = off; off = align_up(off + L->nr * sizeof(float), 256);
   L->off_rbl = off; off = align_up(off + (L->nr / BM) * sizeof(int), 256);
   L->off_lt = off; off = align_up(off + L->nr * sizeof(double), 256);
+  L->off_seq = off; off = align_up(off + L->nr * sizeof(int), 256);  // >= N / T lengths
+  L->off_G = off;
+
+  // Chunks are whole row units (BM * ctas rows: what one CTA pair covers).
+  const long long ru_rows = static_cast<long long>(BM) * L->ctas;
+  const long long n_ru_total = cdiv(L->nr, ru_rows);
+  const int slots = sms / L->ctas;
+  // Bytes of the chunk block per row unit: bf16 G (+ fp32 dH accumulator) or
+  // fp16 logits.
+  const size_t unit_bytes = static_cast<size_t>(ru_rows) *
+                            (static_cast<size_t>(L->vblock) * 2 + (L->need_acc ? L->D * 4 : 0));
+  long long max_units = L->stored ? std::max(1, stored_max_blocks(L->ldS) / L->ctas)
+                                  : kMaxAutoChunkBlocks / L->ctas;
+  const size_t budget = workspace_budget(p);
+  if (budget > 0) {
+    const long long fit =
+        budget > off + 512 ? static_cast<long long>((budget - off - 512) / unit_bytes) : 0;
+    if (fit < 1) return GRPO_ERR_WORKSPACE_TOO_SMALL;
+    max_units = std::min(max_units, fit);
+  }
+  long long crows;
+  if (p && p->chunk_tokens > 0) {
+    crows = cdiv(p->chunk_tokens, ru_rows) * ru_rows;
+  } else if (L->stored) {
+    crows = (sms > 0 ? auto_stored_chunk_blocks(n_ru_total, n_dt, L->nvt, slots,
+                                                static_cast<int>(max_units))
+                     : std::min<long long>(n_ru_total, max_units)) *
+            ru_rows;
+  } else if (sms > 0) {
+    crows = auto_chunk_blocks(n_ru_total, n_dt, slots, static_cast<int>(max_units)) * ru_rows;
+  } else {  // sizing without a device: the largest automatic chunk
+    crows = std::min<long long>(n_ru_total, max_units) * ru_rows;
+  }
+  crows = std::min(crows, n_ru_total * ru_rows);
+  if (crows > INT_MAX / 2) return GRPO_ERR_UNSUPPORTED_SHAPE;
+  L->chunk_rows = static_cast<int>(crows);
+
   // Backward chunk block: bf16 G [C x V_b] (recompute path) or the chunk's
   // fp16 logits, rewritten in place as bf16 G [C x ldS] (stored path).
-  L->off_G = off; off = align_up(off + static_cast<size_t>(L->chunk_rows) * L->vblock * 2, 256);
+  off = align_up(off + static_cast<size_t>(L->chunk_rows) * L->vblock * 2, 256);
   L->off_acc = off;
   if (L->need_acc) off = align_up(off + static_cast<size_t>(L->chunk_rows) * L->D * 4, 256);
   L->total = off;
+  if (budget > 0 && L->total > budget) return GRPO_ERR_WORKSPACE_TOO_SMALL;
   return GRPO_OK;
 }
 
@@ -206,7 +239,8 @@ int check_shape(const grpo_shape* s, bool need_seq) {
 
 int check_params(const grpo_params* p) {
   if (!p) return GRPO_OK;
-  if ((p->flags & ~(GRPO_FLAG_STORED_LOGITS | GRPO_FLAG_SINGLE_CTA)) != 0 || p->reserved != 0 || p->chunk_tokens < 0 ||
+  if ((p->flags & ~(GRPO_FLAG_STORED_LOGITS | GRPO_FLAG_SINGLE_CTA | GRPO_FLAG_SEQUENCE_MEAN |
+                    GRPO_FLAG_FIT_FREE_MEMORY)) != 0 || p->reserved != 0 || p->chunk_tokens < 0 ||
       p->vocab_block < 0)
     return GRPO_ERR_INVALID_ARG;
   if (!(p->eps_low >= 0.f) || !(p->eps_high >= 0.f) || !(p->beta >= 0.f))
@@ -314,6 +348,8 @@ struct Ws {
   double* partials;
   double* lt;
   int* n_active;
+  int* n_nonempty;
+  int* seq_lens;
   int* rb_list;
   float *pm, *ps, *zy, *lse, *g, *acc;
   __nv_bfloat16* G;
@@ -327,6 +363,8 @@ Ws carve(void* ws, const Layout& L) {
   w.msum = reinterpret_cast<double*>(w.base + kOffMsum);
   w.partials = reinterpret_cast<double*>(w.base + kOffPartials);
   w.n_active = reinterpret_cast<int*>(w.base + kOffActive);
+  w.n_nonempty = reinterpret_cast<int*>(w.base + kOffNonempty);
+  w.seq_lens = reinterpret_cast<int*>(w.base + L.off_seq);
   w.rb_list = reinterpret_cast<int*>(w.base + L.off_rbl);
   w.lt = reinterpret_cast<double*>(w.base + L.off_lt);
   w.pm = reinterpret_cast<float*>(w.base + L.off_pm);
@@ -530,6 +568,9 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     f.beta = prm->beta;
     f.loss_den = prm->loss_denominator;
     f.msum = w.msum;
+    f.seq_mode = (prm->flags & GRPO_FLAG_SEQUENCE_MEAN) != 0;
+    f.seq_lens = w.seq_lens;
+    f.n_nonempty = w.n_nonempty;
     f.logp_out = logp_out;
     f.lt = w.lt;
     f.S = S;
@@ -568,8 +609,6 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
   fin.mask = mask;
   fin.lt = w.lt;
   fin.logp_out = logp_out;
-  fin.loss_den = prm->loss_denominator;
-  fin.msum = w.msum;
   fin.block_partials = w.partials;
   fin.counter = w.counter;
   fin.loss_out = loss;
@@ -683,6 +722,9 @@ int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
   if (launch_row_plan(mask, L.n, n_rb_total, w.rb_list, w.n_active, w.msum, st) != cudaSuccess ||
       launch_zero_padding_blocks(mask, L.n, n_rb_total, L.D, dH, sms, st) != cudaSuccess)
     return GRPO_ERR_CUDA;
+  if ((prm.flags & GRPO_FLAG_SEQUENCE_MEAN) != 0 &&
+      launch_seq_lens(mask, L.n, L.T, w.seq_lens, w.n_nonempty, st) != cudaSuccess)
+    return GRPO_ERR_CUDA;
   if (L.stored)
     return run_stored(hidden, W, ids, mask, old_logp, ref_logp, adv, loss, logp_or_null, dH,
                       &prm, L, w, sms, st);
@@ -711,6 +753,9 @@ int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
   f.beta = prm.beta;
   f.loss_den = prm.loss_denominator;
   f.msum = w.msum;
+  f.seq_mode = (prm.flags & GRPO_FLAG_SEQUENCE_MEAN) != 0;
+  f.seq_lens = w.seq_lens;
+  f.n_nonempty = w.n_nonempty;
   f.lse_ws = w.lse;
   f.logp_out = logp_or_null;
   f.g_ws = w.g;
@@ -745,6 +790,8 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
   info->launches_loss = L.n <= 0 ? 0
                       : L.stored ? 3 + 3 * info->n_chunks
                                  : 4 + 2 * info->n_chunks * info->n_vocab_blocks;
+  if (L.n > 0 && params != nullptr && (params->flags & GRPO_FLAG_SEQUENCE_MEAN) != 0)
+    info->launches_loss += 1;
   if (L.stored) {
     info->n_vocab_blocks = 1;
     info->fwd_splits =

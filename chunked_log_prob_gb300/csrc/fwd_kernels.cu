@@ -116,11 +116,53 @@ __device__ double block_sum(double v, double* sh) {
   return r;  // valid in thread 0
 }
 
+// Unmasked tokens per completion (b = t / seq_len) and the number of
+// completions that have any; one block per completion (grid-stride).
+__global__ void __launch_bounds__(256) seq_lens_kernel(const uint8_t* __restrict__ mask,
+                                                       long long n, int seq_len,
+                                                       int* __restrict__ lens,
+                                                       int* __restrict__ n_nonempty) {
+  __shared__ int warp_cnt[8];
+  const long long n_seq = n / seq_len;
+  for (long long b = blockIdx.x; b < n_seq; b += gridDim.x) {
+    int c = 0;
+    const long long r0 = b * seq_len;
+    if (mask == nullptr) {
+      c = threadIdx.x == 0 ? seq_len : 0;
+    } else {
+      for (long long r = r0 + threadIdx.x; r < r0 + seq_len; r += blockDim.x) c += mask[r] != 0;
+    }
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_down_sync(0xffffffffu, c, o);
+    if ((threadIdx.x & 31) == 0) warp_cnt[threadIdx.x >> 5] = c;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int tot = 0;
+      for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) tot += warp_cnt[w];
+      lens[b] = tot;
+      if (tot > 0) atomicAdd(n_nonempty, 1);
+    }
+    __syncthreads();
+  }
+}
+
+// Weight of an unmasked token in the loss: 1 / M for the token mean, or
+// 1 / (len_b B') for the mean over completions of their token means.
+__device__ __forceinline__ double token_weight(int seq_mode, float loss_den, const double* msum,
+                                               const int* seq_lens, const int* n_nonempty,
+                                               long long t, int seq_len) {
+  double den;
+  if (seq_mode) {
+    const double bcount = loss_den > 0.f ? static_cast<double>(loss_den) : *n_nonempty;
+    den = static_cast<double>(seq_lens[t / seq_len]) * bcount;
+  } else {
+    den = loss_den > 0.f ? static_cast<double>(loss_den) : *msum;
+  }
+  return den != 0.0 ? 1.0 / den : 0.0;
+}
+
 __global__ void __launch_bounds__(kFinalizeThreads) finalize_kernel(const FinalizeArgs a) {
   __shared__ double sh[32];
   __shared__ bool is_last;
-  const double mden = a.loss_mode ? (a.loss_den > 0.f ? static_cast<double>(a.loss_den) : *a.msum)
-                                  : 0.0;
   double local = 0.0;
   for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < a.n;
        t += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -160,10 +202,12 @@ __global__ void __launch_bounds__(kFinalizeThreads) finalize_kernel(const Finali
         const double d = static_cast<double>(a.ref_logp[t]) - lp;
         const double ed = exp(d);
         const double kl = ed - d - 1.0;
-        local += -surr + static_cast<double>(a.beta) * kl;
+        const double wt = token_weight(a.seq_mode, a.loss_den, a.msum, a.seq_lens,
+                                       a.n_nonempty, t, a.seq_len);
+        local += (-surr + static_cast<double>(a.beta) * kl) * wt;
         const bool clipped = (A > 0.0 && r > hi) || (A < 0.0 && r < lo);
         const double dl = -(clipped ? 0.0 : A * r) + static_cast<double>(a.beta) * (1.0 - ed);
-        gval = mden != 0.0 ? static_cast<float>(dl / mden) : 0.f;
+        gval = static_cast<float>(dl * wt);
       }
     }
     if (a.logp_out) a.logp_out[t] = logp;
@@ -188,10 +232,19 @@ __global__ void __launch_bounds__(kFinalizeThreads) finalize_kernel(const Finali
       v += reinterpret_cast<volatile double*>(a.block_partials)[i];
     const double tot = block_sum(v, sh);
     if (threadIdx.x == 0) {
-      *a.loss_out = mden != 0.0 ? static_cast<float>(tot / mden) : 0.f;
+      *a.loss_out = static_cast<float>(tot);
       *a.counter = 0;
     }
   }
+}
+
+cudaError_t launch_seq_lens(const uint8_t* mask, long long n, int seq_len, int* lens,
+                            int* n_nonempty, cudaStream_t stream) {
+  const long long n_seq = n / seq_len;
+  if (n_seq <= 0) return cudaSuccess;
+  seq_lens_kernel<<<static_cast<int>(std::min<long long>(n_seq, 4096)), 256, 0, stream>>>(
+      mask, n, seq_len, lens, n_nonempty);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_row_plan(const uint8_t* mask, long long n, int n_rb, int* rb_list,
@@ -272,7 +325,8 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
       } else {
         logp = a.zy[grow] - lse;
       }
-      const double mden = a.loss_den > 0.f ? static_cast<double>(a.loss_den) : *a.msum;
+      const double wt = token_weight(a.seq_mode, a.loss_den, a.msum, a.seq_lens, a.n_nonempty,
+                                     grow, a.seq_len);
       const double lp = logp;
       const double A = a.adv[grow / a.seq_len];
       const double r = exp(lp - static_cast<double>(a.old_logp[grow]));
@@ -282,10 +336,10 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
       const double surr = fmin(r * A, c * A);
       const double d = static_cast<double>(a.ref_logp[grow]) - lp;
       const double ed = exp(d);
-      a.lt[grow] = -surr + static_cast<double>(a.beta) * (ed - d - 1.0);
+      a.lt[grow] = (-surr + static_cast<double>(a.beta) * (ed - d - 1.0)) * wt;
       const bool clipped = (A > 0.0 && r > hi) || (A < 0.0 && r < lo);
       const double dl = -(clipped ? 0.0 : A * r) + static_cast<double>(a.beta) * (1.0 - ed);
-      g = mden != 0.0 ? static_cast<float>(dl / mden) : 0.f;
+      g = static_cast<float>(dl * wt);
       if (a.logp_out) a.logp_out[grow] = logp;
     }
     sh_lse2 = lse * kLog2e;
@@ -360,8 +414,7 @@ __global__ void __launch_bounds__(kFinalizeThreads) finish_loss_kernel(const Fin
       v += reinterpret_cast<volatile double*>(a.block_partials)[i];
     const double tot = block_sum(v, sh);
     if (threadIdx.x == 0) {
-      const double mden = a.loss_den > 0.f ? static_cast<double>(a.loss_den) : *a.msum;
-      *a.loss_out = mden != 0.0 ? static_cast<float>(tot / mden) : 0.f;
+      *a.loss_out = static_cast<float>(tot);
       *a.counter = 0;
     }
   }

@@ -25,6 +25,9 @@ struct FinalizeArgs {
   const float* adv;
   float eps_low, eps_high, beta, loss_den;
   const double* msum;    // device sum of the mask
+  int seq_mode;          // 1: per-completion mean (weights 1 / (len_b B'))
+  const int* seq_lens;   // [n / seq_len] unmasked tokens per completion
+  const int* n_nonempty; // completions with len_b > 0
   float* lse_ws;         // [n]
   float* lse_out;        // optional
   float* logp_out;       // optional
@@ -54,8 +57,11 @@ struct GformArgs {
   const float* adv;
   float eps_low, eps_high, beta, loss_den;
   const double* msum;
+  int seq_mode;
+  const int* seq_lens;
+  const int* n_nonempty;
   float* logp_out;       // optional
-  double* lt;            // [N] token loss of unmasked rows
+  double* lt;            // [N] weighted token loss w_t l_t of unmasked rows
   uint16_t* S;           // [chunk rows][ldS]: fp16 logits in, bf16 G out
   long long ldS;
   int xmode;
@@ -68,8 +74,6 @@ struct FinishArgs {
   const uint8_t* mask;
   const double* lt;
   float* logp_out;
-  float loss_den;
-  const double* msum;
   double* block_partials;
   unsigned* counter;
   float* loss_out;
@@ -120,6 +124,8 @@ cudaError_t launch_dh_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap
                            const TileArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_row_plan(const uint8_t* mask, long long n, int n_rb, int* rb_list,
                             int* n_active, double* msum, cudaStream_t stream);
+cudaError_t launch_seq_lens(const uint8_t* mask, long long n, int seq_len, int* lens,
+                            int* n_nonempty, cudaStream_t stream);
 cudaError_t launch_zero_padding_blocks(const uint8_t* mask, long long n, int n_rb, int hidden,
                                        void* dH, int sms, cudaStream_t stream);
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t stream);

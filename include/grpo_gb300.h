@@ -79,6 +79,19 @@ typedef struct grpo_shape {
  * results up to fp32 summation order; kept for comparison and debugging. */
 #define GRPO_FLAG_SINGLE_CTA 2u
 
+/* grpo_params.flags bit: loss = mean over completions of each completion's
+ * masked token mean, L = (1/B') sum_b (1/len_b) sum_{t in b} m_t l_t, with
+ * len_b the unmasked tokens of completion b (b = t / seq_len) and B' the
+ * completions with len_b > 0 (loss_denominator > 0 replaces B'). Without the
+ * flag: token mean over the batch. */
+#define GRPO_FLAG_SEQUENCE_MEAN 4u
+
+/* grpo_params.flags bit: size the chunk from the current device's free memory
+ * (budget = half of what cudaMemGetInfo reports, or workspace_limit_bytes if
+ * smaller) - the pages' "adjust to the available VRAM". With this flag
+ * grpo_workspace_size queries the current device (no allocation, no launch). */
+#define GRPO_FLAG_FIT_FREE_MEMORY 8u
+
 typedef struct grpo_params {
   float eps_low;          /* ratio clip: lower bound 1 - eps_low (0.2)         */
   float eps_high;         /* ratio clip: upper bound 1 + eps_high (0.2)        */
@@ -98,6 +111,11 @@ typedef struct grpo_params {
   float logit_scale_divide;
   float logit_softcapping;
   float temperature;
+  /* Upper bound on the workspace in bytes (0 = none). The automatic chunk is
+   * the largest that keeps the whole workspace within it; an explicit
+   * chunk_tokens over the budget, or a budget below the chunk-independent
+   * part, gives GRPO_ERR_WORKSPACE_TOO_SMALL. */
+  uint64_t workspace_limit_bytes;
 } grpo_params;
 
 /* Defaults: eps 0.2/0.2, beta 0.001 (the pages' corrected GRPO default,
@@ -130,7 +148,8 @@ int grpo_logp_fwd(const void* hidden, const void* W, const int32_t* ids, float* 
  *   surr  = min(r_t A_b, clamp(r_t, 1 - eps_low, 1 + eps_high) A_b)
  *   kl_t  = exp(ref_t - logp_t) - (ref_t - logp_t) - 1
  *   l_t   = -surr + beta kl_t
- *   loss  = sum_t mask_t l_t / M,  M = sum_t mask_t (or loss_denominator > 0)
+ *   loss  = sum_t mask_t l_t / M,  M = sum_t mask_t (or loss_denominator > 0);
+ *           per-completion mean with GRPO_FLAG_SEQUENCE_MEAN
  *   dH_t  = dloss/dh_t = g_t (W[y_t] - sum_v softmax(h_t W^T)_v W_v),
  *           g_t = dloss/dlogp_t
  * ("Unsloth internals", section "The relationship to TRL"; "Train reasoning

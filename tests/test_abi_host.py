@@ -91,7 +91,7 @@ def test_workspace_size_rejects_bad_shapes(clp, n, d, v, want):
 
 def test_bad_params_rejected(clp):
     p = clp.make_params()
-    p.flags = 8  # not a defined flag bit
+    p.flags = 16  # not a defined flag bit
     with pytest.raises(clp.GrpoError) as e:
         clp.grpo_workspace_size(10, 16, 50, 1, p)
     assert e.value.code == -1
@@ -138,3 +138,35 @@ def test_stored_logit_workspace_is_chunk_times_vocab(clp):
     # Automatic chunk without a device: bounded by 2 GiB of logits.
     auto = clp.grpo_workspace_size(131072, 2880, 201088, 1, clp.make_params(flags=1))
     assert auto < (2 << 30) + 131072 * 400
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_workspace_budget_caps_the_chunk(clp, flags):
+    n, d, v = 65536, 4096, 128256
+    free = clp.grpo_workspace_size(n, d, v, 1, clp.make_params(flags=flags))
+    for limit in (free // 2, free // 4):
+        got = clp.grpo_workspace_size(n, d, v, 1, clp.make_params(flags=flags,
+                                                                 workspace_limit_bytes=limit))
+        assert got <= limit
+    # A generous budget changes nothing.
+    same = clp.grpo_workspace_size(n, d, v, 1, clp.make_params(flags=flags,
+                                                              workspace_limit_bytes=free * 4))
+    assert same == free
+
+
+def test_workspace_budget_too_small_is_an_error(clp):
+    with pytest.raises(clp.GrpoError) as e:
+        clp.grpo_workspace_size(65536, 4096, 128256, 1,
+                                clp.make_params(workspace_limit_bytes=1 << 20))
+    assert e.value.code == -4
+    # An explicit chunk that does not fit the budget is refused too.
+    with pytest.raises(clp.GrpoError) as e:
+        clp.grpo_workspace_size(65536, 4096, 128256, 1,
+                                clp.make_params(flags=1, chunk_tokens=16384,
+                                                workspace_limit_bytes=1 << 30))
+    assert e.value.code == -4
+
+
+def test_sequence_mean_flag_is_accepted(clp):
+    assert clp.grpo_workspace_size(1024, 64, 100, 256,
+                                   clp.make_params(flags=clp._binding.FLAG_SEQUENCE_MEAN)) > 0

@@ -360,3 +360,36 @@ def test_pair_and_single_cta_agree(clp):
         assert s1 == 0 and s2 == 0
         assert np.abs(lp1 - lp2).max() <= 1e-5 and abs(L1 - L2) <= 1e-5 * abs(L1)
         assert np.linalg.norm(dH1 - dH2) <= 1e-2 * np.linalg.norm(dH1)
+
+
+# ------------------------------------- aggregation and workspace budgets ---
+
+SEQMEAN = 4  # GRPO_FLAG_SEQUENCE_MEAN
+FITFREE = 8  # GRPO_FLAG_FIT_FREE_MEMORY
+
+
+@pytest.mark.parametrize("flags", [SEQMEAN, SEQMEAN | STORED, SEQMEAN | SINGLE])
+def test_sequence_mean_aggregation(clp, flags):
+    p = synth.make_problem("tiny", seed=60, T=100, prompts=2, G=4, D=256, V=3000,
+                           lengths=(5, 100))
+    p.mask[300:400] = 0  # completion 3 has no token at all
+    base, _ = oracle.selective_logp(p.hidden, p.weight, p.ids.numpy())
+    old, ref = p.old_ref(torch.from_numpy(base))
+    want = oracle.loss_fwd_bwd(p.hidden, p.weight, p.ids.numpy(), p.mask.numpy(), old, ref,
+                               p.adv, p.seq_len, p.eps_low, p.eps_high, p.beta,
+                               aggregation="sequence")
+    check(gpu_loss(clp, p, old, ref, clp.make_params(flags=flags)), want, p.mask,
+          f"sequence mean {flags}")
+
+
+@pytest.mark.parametrize("flags,limit", [(FITFREE, 0), (STORED | FITFREE, 0),
+                                         (STORED, 24 << 20), (0, 24 << 20)])
+def test_workspace_budget_plans_give_same_results(clp, flags, limit):
+    p = synth.make_problem("tiny", seed=61, T=512, prompts=2, G=4, D=512, V=6000,
+                           lengths=(100, 512))
+    old, ref, want = oracle_case(p)
+    params = clp.make_params(flags=flags, workspace_limit_bytes=limit)
+    if limit:
+        assert clp.grpo_workspace_size(p.n_tokens, p.hidden_size, p.vocab, p.seq_len,
+                                       params) <= limit
+    check(gpu_loss(clp, p, old, ref, params), want, p.mask, f"budget {flags} {limit}")
