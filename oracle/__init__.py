@@ -11,6 +11,7 @@ from .grpo_oracle import (  # noqa: F401
     Transform,
     broadcast_advantage,
     grad_hidden,
+    grad_weight,
     grpo_loss,
     logits_rows,
     logsumexp_rows,

@@ -259,6 +259,31 @@ def grad_hidden(hidden, W, ids, g, row_block: int = ROW_BLOCK, xf: Transform = I
     return dH
 
 
+def grad_weight(hidden, W, ids, g, row_block: int = ROW_BLOCK, xf: Transform = IDENTITY):
+    """dW = dL/dW: dW_v = sum_t g_t (onehot_v(y_t) - softmax(z'_t)_v) f'(z_tv) h_t.
+
+    The lm_head gradient (needed only when the head is trained; frozen under
+    LoRA). Same Jacobian rows as grad_hidden, contracted with h instead of W.
+    Returns float64 [V, D].
+    """
+    h = _f64(hidden)
+    Wd = _f64(W)
+    y = np.asarray(ids, dtype=np.int64)
+    gd = _f64(g)
+    dW = np.zeros_like(Wd)
+    for r0 in range(0, h.shape[0], row_block):
+        r1 = min(h.shape[0], r0 + row_block)
+        rows = np.nonzero(gd[r0:r1] != 0.0)[0] + r0
+        if rows.size == 0:
+            continue
+        z = logits_rows(h[rows], Wd)
+        zt, dz = xf.apply(z) if not xf.identity else (z, np.ones_like(z))
+        jac = -np.exp(zt - logsumexp_rows(zt)[:, None])
+        jac[np.arange(len(rows)), y[rows]] += 1.0
+        dW += ((gd[rows, None] * jac * dz).T) @ h[rows]
+    return dW
+
+
 def loss_fwd_bwd(hidden, W, ids, mask, old, ref, adv_per_seq, seq_len,
                  eps_low=0.2, eps_high=0.2, beta=0.001, loss_denominator=0.0,
                  xf: Transform = IDENTITY, aggregation="token"):

@@ -522,3 +522,47 @@ def test_sequence_mean_empty_completion_and_fd():
               - oracle.grpo_loss(m_, old, ref, adv, mask, T, 0.2, 0.2, 0.05,
                                  aggregation="sequence")[0]) / (2 * step)
         assert abs(fd - g[t]) < 1e-8
+
+
+# ------------------------------------------------------ lm_head gradient ---
+
+@pytest.mark.parametrize("xf", [oracle.IDENTITY, oracle.Transform(softcap=2.0, temperature=0.8)])
+def test_dW_matches_finite_differences(xf):
+    h, W, y, mask, old, ref, adv, T, eps, beta = _tiny_full(70, N=8, D=5, V=12)
+    out = oracle.loss_fwd_bwd(h, W, y, mask, old, ref, adv, T, eps, eps, beta, xf=xf)
+    dW = oracle.grad_weight(h, W, y, out["g"], xf=xf)
+    step = 1e-6
+    fd = np.zeros_like(W)
+    for v in range(W.shape[0]):
+        for d in range(W.shape[1]):
+            Wp, Wm = W.copy(), W.copy()
+            Wp[v, d] += step
+            Wm[v, d] -= step
+            fd[v, d] = (_L_of_h_xf(h, Wp, y, mask, old, ref, adv, T, eps, beta, xf)
+                        - _L_of_h_xf(h, Wm, y, mask, old, ref, adv, T, eps, beta, xf)) / (2 * step)
+    assert np.linalg.norm(fd - dW) / np.linalg.norm(fd) < 1e-6
+
+
+def test_dW_columns_sum_to_zero():
+    # sum_v (onehot - softmax)_v = 0 for every token, so sum_v dW_v = 0.
+    h, W, y, mask, old, ref, adv, T, eps, beta = _tiny_full(71)
+    out = oracle.loss_fwd_bwd(h, W, y, mask, old, ref, adv, T, eps, eps, beta)
+    dW = oracle.grad_weight(h, W, y, out["g"])
+    assert np.abs(dW.sum(axis=0)).max() < 1e-14 * max(1.0, np.abs(dW).max()) * W.shape[0]
+    assert np.abs(dW).max() > 1e-6
+
+
+def test_dW_matches_torch_autograd():
+    h, W, y, mask, old, ref, adv, T, eps, beta = _tiny_full(72)
+    out = oracle.loss_fwd_bwd(h, W, y, mask, old, ref, adv, T, eps, eps, beta)
+    dW = oracle.grad_weight(h, W, y, out["g"])
+    Wt = torch.tensor(W, requires_grad=True)
+    lp = torch.log_softmax(torch.tensor(h) @ Wt.T, 1).gather(1, torch.tensor(y)[:, None])[:, 0]
+    A = torch.tensor(adv)[torch.arange(len(y)) // T]
+    r = torch.exp(lp - torch.tensor(old))
+    surr = torch.minimum(r * A, torch.clamp(r, 1 - eps, 1 + eps) * A)
+    dl = torch.tensor(ref) - lp
+    m = torch.tensor(mask)
+    L = ((-surr + beta * (torch.exp(dl) - dl - 1)) * m).sum() / m.sum()
+    L.backward()
+    assert np.allclose(Wt.grad.numpy(), dW, rtol=1e-10, atol=1e-14)
