@@ -51,6 +51,8 @@ def parse_args():
                          "executed); recompute: it recomputes the logit tiles (6NDV)")
     ap.add_argument("--single-cta", action="store_true",
                     help="one CTA per 128-row GEMM tile instead of CTA pairs")
+    ap.add_argument("--with-dw", action="store_true",
+                    help="also compute the lm_head gradient dW (full fine-tuning; +2NDV)")
     ap.add_argument("--no-variant", action="store_true",
                     help="skip timing the other backward variant")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -268,10 +270,11 @@ def run_ours(args):
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     logp = torch.empty(N, dtype=torch.float32, device=dev)
     dH = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
+    dW = torch.empty(V, D, dtype=torch.float32, device=dev) if args.with_dw else None
 
     def step(prm=params):
         clp.grpo_loss_fwd_bwd(p.hidden, p.weight, p.ids, p.mask, old, ref, p.adv, T,
-                              params=prm, workspace=ws, loss=loss, logp=logp, dH=dH)
+                              params=prm, workspace=ws, loss=loss, logp=logp, dH=dH, dW=dW)
 
     stream = torch.cuda.current_stream(dev)
     for _ in range(max(args.warmup, 3)):
@@ -312,11 +315,13 @@ def run_ours(args):
         ev1.record(stream)
         torch.cuda.synchronize(dev)
         v_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
-        v_exec = (6.0 if stored else 4.0) * D * V * p.n_valid
+        v_exec = ((6.0 if stored else 4.0) + (2.0 if args.with_dw else 0.0)) * D * V * p.n_valid
         variant = {"backward": "recomputed logits" if stored else "stored fp16 logits",
                    "ms_per_step": v_ms, "value": world * p.n_valid / (v_ms / 1e3),
                    "tflops_executed": v_exec / (v_ms / 1e3) / 1e12,
-                   "launches_per_call": clp.grpo_get_plan(N, D, V, T, other)["launches_loss"]}
+                   "launches_per_call": clp.grpo_get_plan(N, D, V, T, other)["launches_loss"]
+            + (clp.grpo_get_plan(N, D, V, T, other)["n_chunks"]
+               * clp.grpo_get_plan(N, D, V, T, other)["n_vocab_blocks"] if args.with_dw else 0)}
 
     # Forward alone (one logit GEMM launch + finalize), timed on the same stream.
     fwd_ms = None
@@ -381,7 +386,7 @@ def run_ours(args):
     tflops = fl / (ms_max / 1e3) / 1e12
     # Executed tensor work: 6NDV with the recomputed backward, 4NDV when the
     # backward reads the stored fp16 logits instead of a second logit GEMM.
-    fl_exec = (4.0 if stored else 6.0) * D * V * valid
+    fl_exec = ((4.0 if stored else 6.0) + (2.0 if args.with_dw else 0.0)) * D * V * valid
     tflops_exec = fl_exec / (ms_max / 1e3) / 1e12
     peak_sus = peaks["bf16_tflops_sustained"]
     peak_burst = peaks["bf16_tflops"]
@@ -409,7 +414,8 @@ def run_ours(args):
         "tflops": tflops,
         "tflops_executed": tflops_exec,
         "pct_bf16_peak": 100.0 * tflops_exec / peak_sus,
-        "backward": "stored fp16 logits" if stored else "recomputed logits",
+        "backward": ("stored fp16 logits" if stored else "recomputed logits") + (
+            " + lm_head dW" if args.with_dw else ""),
         "variant": variant,
         "roofline": {
             "bound": "tensor", "achieved": tflops_exec, "peak": peak_sus, "unit": "TFLOP/s",
@@ -428,7 +434,8 @@ def run_ours(args):
             "scope": "grpo_logp_fwd: logit GEMM + finalize over all N rows"},
         "e2e": e2e,
         "clocks": clocks.summary(),
-        "gpu_launches": plan["launches_loss"] * args.steps,
+        "gpu_launches": (plan["launches_loss"] + (plan["n_chunks"] * plan["n_vocab_blocks"]
+                                                  if args.with_dw else 0)) * args.steps,
         "workspace_bytes": plan["workspace_bytes"],
         "cpu_baseline": None,
     }

@@ -67,7 +67,7 @@ def _load():
     lib.grpo_workspace_size.restype = ctypes.c_int
     lib.grpo_logp_fwd.argtypes = [vp, vp, vp, vp, vp, P(GrpoShape), P(GrpoParams), vp, sz, vp]
     lib.grpo_logp_fwd.restype = ctypes.c_int
-    lib.grpo_loss_fwd_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+    lib.grpo_loss_fwd_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                       P(GrpoShape), P(GrpoParams), vp, sz, vp]
     lib.grpo_loss_fwd_bwd.restype = ctypes.c_int
     lib.grpo_get_plan.argtypes = [P(GrpoShape), P(GrpoParams), P(GrpoPlanInfo)]
@@ -195,8 +195,12 @@ def grpo_logp_fwd(hidden, W, ids, *, params: GrpoParams | None = None, workspace
 
 def grpo_loss_fwd_bwd(hidden, W, ids, mask, old_logp, ref_logp, adv, seq_len, *,
                       params: GrpoParams | None = None, workspace=None, want_logp=True,
-                      loss=None, logp=None, dH=None):
-    """Fused GRPO loss forward + backward to hidden. Returns (loss[1], logp[N] | None, dH[N, D])."""
+                      loss=None, logp=None, dH=None, dW=None, want_dW=False):
+    """Fused GRPO loss forward + backward to hidden (and to the lm_head weight).
+
+    Returns (loss[1], logp[N] | None, dH[N, D]) or, with want_dW / dW given,
+    (loss, logp, dH, dW[V, D] fp32).
+    """
     dev = hidden.device
     N, D = hidden.shape
     V = W.shape[0]
@@ -216,16 +220,22 @@ def grpo_loss_fwd_bwd(hidden, W, ids, mask, old_logp, ref_logp, adv, seq_len, *,
         logp = torch.empty(N, dtype=torch.float32, device=dev)
     if dH is None:
         dH = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
+    if want_dW and dW is None:
+        dW = torch.empty(V, D, dtype=torch.float32, device=dev)
+    if dW is not None:
+        _check(dW, "dW", torch.float32, (V, D), dev)
     if workspace is None:
         workspace = alloc_workspace(N, D, V, seq_len, params, dev)
     shape = make_shape(N, seq_len, D, V)
     rc = lib.grpo_loss_fwd_bwd(_ptr(hidden), _ptr(W), _ptr(ids), _ptr(mask), _ptr(old_logp),
                                _ptr(ref_logp), _ptr(adv), _ptr(loss), _ptr(logp), _ptr(dH),
-                               ctypes.byref(shape),
+                               _ptr(dW), ctypes.byref(shape),
                                ctypes.byref(params) if params is not None else None,
                                _ptr(workspace), workspace.numel(), _stream(dev))
     if rc != GRPO_OK:
         raise GrpoError(rc, "grpo_loss_fwd_bwd")
+    if dW is not None:
+        return loss, logp, dH, dW
     return loss, logp, dH
 
 

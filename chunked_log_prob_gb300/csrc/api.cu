@@ -424,10 +424,42 @@ int run_forward(const void* hidden, const void* W, const int32_t* ids, const uin
   return GRPO_OK;
 }
 
+// dW[v0 : v0 + width) (+)= G^T H over the chunk's active row blocks; G is the
+// chunk block (pitch ldG elements). first: this chunk starts the sum.
+int launch_dw(const void* hidden, const __nv_bfloat16* G, long long ldG, int v0, int width,
+              int rb0, int n_rb, float* dW, bool first, const Layout& L, const Ws& w, int sms,
+              cudaStream_t st) {
+  const int slots = std::max(1, sms / L.ctas);
+  CUtensorMap map_gt, map_h_mn;
+  if (!encode_2d(&map_gt, G, width, static_cast<uint64_t>(n_rb) * BM, ldG, 64, BK) ||
+      !encode_2d(&map_h_mn, hidden, L.D, L.n, L.D, 64, BK))
+    return GRPO_ERR_CUDA;
+  TileArgs a = base_args(L, w);
+  a.n_total = L.n;
+  a.n_rb = n_rb;
+  a.rb_offset = rb0;
+  a.rb_list = w.rb_list;
+  a.n_active = w.n_active;
+  const int n_vu = static_cast<int>(cdiv(width, static_cast<long long>(BM) * L.ctas));
+  const int n_dt = static_cast<int>(cdiv(L.D, BN));
+  a.group_rows = group_rows_for(n_vu, slots);
+  a.n_cols = n_dt;
+  a.v0 = v0;
+  a.dw_rows = width;
+  a.dW = dW;
+  a.first = first ? 1 : 0;
+  const long long units = static_cast<long long>(n_vu) * n_dt;
+  if (launch_dw_gemm(L.ctas, map_gt, map_h_mn, a,
+                     L.ctas * static_cast<int>(std::min<long long>(units, slots)),
+                     st) != cudaSuccess)
+    return GRPO_ERR_CUDA;
+  return GRPO_OK;
+}
+
 // Backward over the active row blocks, in chunks of chunk_rows / BM list
 // entries: G block, then dH accumulation, per vocab block. Chunks past the
 // device-side list length find no work and return at once.
-int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH,
+int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH, float* dW,
                  const grpo_params* prm, const Layout& L, const Ws& w, int sms,
                  cudaStream_t st) {
   CUtensorMap map_h, map_w_k, map_w_mn;
@@ -490,6 +522,12 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
                          L.ctas * static_cast<int>(std::min<long long>(units, slots)),
                          st) != cudaSuccess)
         return GRPO_ERR_CUDA;
+      // (3) optional lm_head gradient rows [v0, v0 + width) from the same G block.
+      if (dW != nullptr) {
+        const int r = launch_dw(hidden, w.G, L.vblock, static_cast<int>(v0), width, rb0, n_rb,
+                                dW, rb0 == 0, L, w, sms, st);
+        if (r != GRPO_OK) return r;
+      }
     }
   }
   return GRPO_OK;
@@ -501,8 +539,8 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
 // dH GEMM over the whole vocabulary. A closing kernel reduces the loss.
 int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint8_t* mask,
                const float* old_logp, const float* ref_logp, const float* adv, float* loss,
-               float* logp_out, void* dH, const grpo_params* prm, const Layout& L, const Ws& w,
-               int sms, cudaStream_t st) {
+               float* logp_out, void* dH, float* dW, const grpo_params* prm, const Layout& L,
+               const Ws& w, int sms, cudaStream_t st) {
   CUtensorMap map_h, map_w_k, map_w_mn;
   const int slots = std::max(1, sms / L.ctas);
   if (!encode_2d(&map_h, hidden, L.D, L.n, L.D, BK, BM) ||
@@ -602,6 +640,12 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
                        L.ctas * static_cast<int>(std::min<long long>(units, slots)),
                        st) != cudaSuccess)
       return GRPO_ERR_CUDA;
+    // (4) optional lm_head gradient from the same G block.
+    if (dW != nullptr) {
+      const int r = launch_dw(hidden, reinterpret_cast<const __nv_bfloat16*>(S), L.ldS, 0, L.V,
+                              rb0, n_rb, dW, rb0 == 0, L, w, sms, st);
+      if (r != GRPO_OK) return r;
+    }
   }
   FinishArgs fin;
   std::memset(&fin, 0, sizeof(fin));
@@ -689,8 +733,8 @@ int grpo_logp_fwd(const void* hidden, const void* W, const int32_t* ids, float* 
 int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
                       const uint8_t* mask, const float* old_logp, const float* ref_logp,
                       const float* adv, float* loss, float* logp_or_null, void* dH,
-                      const grpo_shape* shape, const grpo_params* params, void* workspace,
-                      size_t workspace_bytes, void* stream) {
+                      float* dW_or_null, const grpo_shape* shape, const grpo_params* params,
+                      void* workspace, size_t workspace_bytes, void* stream) {
   int r = check_shape(shape, true);
   if (r != GRPO_OK) return r;
   if ((r = check_params(params)) != GRPO_OK) return r;
@@ -700,7 +744,7 @@ int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
     return GRPO_ERR_INVALID_ARG;
   if (!aligned(hidden, 16) || !aligned(W, 16) || !aligned(dH, 16) || !aligned(workspace, 256) ||
       !aligned(ids, 4) || !aligned(old_logp, 4) || !aligned(ref_logp, 4) || !aligned(adv, 4) ||
-      !aligned(loss, 4) || !aligned(logp_or_null, 4))
+      !aligned(loss, 4) || !aligned(logp_or_null, 4) || !aligned(dW_or_null, 16))
     return GRPO_ERR_MISALIGNED;
   grpo_params prm;
   if (params) prm = *params; else grpo_default_params(&prm);
@@ -715,6 +759,10 @@ int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
   if (cudaMemsetAsync(workspace, 0, 64, st) != cudaSuccess) return GRPO_ERR_CUDA;
   if (L.n == 0) {
     if (cudaMemsetAsync(loss, 0, sizeof(float), st) != cudaSuccess) return GRPO_ERR_CUDA;
+    if (dW_or_null != nullptr &&
+        cudaMemsetAsync(dW_or_null, 0, static_cast<size_t>(L.V) * L.D * sizeof(float), st) !=
+            cudaSuccess)
+      return GRPO_ERR_CUDA;
     return GRPO_OK;
   }
   Ws w = carve(workspace, L);
@@ -727,7 +775,7 @@ int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
     return GRPO_ERR_CUDA;
   if (L.stored)
     return run_stored(hidden, W, ids, mask, old_logp, ref_logp, adv, loss, logp_or_null, dH,
-                      &prm, L, w, sms, st);
+                      dW_or_null, &prm, L, w, sms, st);
   int splits = 1;
   if ((r = run_forward(hidden, W, ids, mask, w.rb_list, w.n_active, &prm, L, w, sms, &splits,
                        st)) != GRPO_OK)
@@ -764,7 +812,7 @@ int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
   f.loss_out = loss;
   f.status = w.status;
   if (launch_finalize(f, st) != cudaSuccess) return GRPO_ERR_CUDA;
-  return run_backward(hidden, W, ids, dH, &prm, L, w, sms, st);
+  return run_backward(hidden, W, ids, dH, dW_or_null, &prm, L, w, sms, st);
 }
 
 int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_info* info) {

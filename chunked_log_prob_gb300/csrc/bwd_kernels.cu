@@ -10,7 +10,15 @@ cudaError_t prepare_bwd_gemms() {
   if (e == cudaSuccess) e = prepare_gemm_variant<MODE_BWDG, 2>();
   if (e == cudaSuccess) e = prepare_gemm_variant<MODE_DH, 1>();
   if (e == cudaSuccess) e = prepare_gemm_variant<MODE_DH, 2>();
+  if (e == cudaSuccess) e = prepare_gemm_variant<MODE_DW, 1>();
+  if (e == cudaSuccess) e = prepare_gemm_variant<MODE_DW, 2>();
   return e;
+}
+
+cudaError_t launch_dw_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                           const TileArgs& args, int grid, cudaStream_t stream) {
+  return ctas == 2 ? launch_gemm_variant<MODE_DW, 2>(map_a, map_b, args, grid, stream)
+                   : launch_gemm_variant<MODE_DW, 1>(map_a, map_b, args, grid, stream);
 }
 
 cudaError_t launch_bwdg_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,

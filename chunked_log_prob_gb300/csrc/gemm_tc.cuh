@@ -14,6 +14,9 @@
 //              G = g (onehot(y) - exp(S - lse)) in bf16 to the chunk workspace.
 //   MODE_DH    dH_tile (+)= G W over one vocab block (B operand MN-major);
 //              epilogue accumulates in fp32 and writes bf16 on the last block.
+//   MODE_DW    dW[v0 + m, n] (+)= sum over the chunk's rows of G[row, m] H[row, n]:
+//              the lm_head gradient; A (G^T) and B (H) are both MN-major, K runs
+//              over the chunk's active row blocks; fp32 RMW on the output.
 //   MODE_FWDS  MODE_FWD over the rows of one backward chunk that also stores
 //              the (transformed) logits in fp16 to the chunk workspace, for a
 //              backward that needs no second logit GEMM.
@@ -37,7 +40,7 @@ constexpr int GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment sla
 constexpr int TMEM_COLS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
-enum GemmMode { MODE_FWD = 0, MODE_BWDG = 1, MODE_DH = 2, MODE_FWDS = 3 };
+enum GemmMode { MODE_FWD = 0, MODE_BWDG = 1, MODE_DH = 2, MODE_FWDS = 3, MODE_DW = 4 };
 
 __host__ __device__ constexpr bool is_fwd(int mode) { return mode == MODE_FWD || mode == MODE_FWDS; }
 
@@ -74,6 +77,9 @@ struct TileArgs {
   // MODE_FWDS
   uint16_t* S;           // [local rows][ldS] fp16 logits of the chunk
   long long ldS;
+  // MODE_DW
+  float* dW;             // [V][hidden] fp32 output / accumulator
+  int dw_rows;           // vocab rows of dW this launch covers (from v0)
   // MODE_DH
   float* acc;            // [local rows][hidden] fp32 accumulator
   __nv_bfloat16* dH;     // [N][hidden] output, indexed by global row
@@ -156,6 +162,21 @@ struct PairCfg {
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
 };
 
+// One TMA box into this CTA's stage; its bytes are counted on the leader's
+// barrier (pair) or this CTA's own.
+template <int CTAS>
+__device__ __forceinline__ void load_box(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                         uint32_t lead, int c0, int c1, bool hint,
+                                         uint64_t pol) {
+  if (CTAS == 2) {
+    if (hint) tma_load_2d_pair(dst, map, lead, c0, c1, pol);
+    else tma_load_2d_pair_nohint(dst, map, lead, c0, c1);
+  } else {
+    if (hint) tma_load_2d_hint(dst, map, bar, c0, c1, pol);
+    else tma_load_2d(dst, map, bar, c0, c1);
+  }
+}
+
 template <int MODE, int CTAS>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
@@ -214,9 +235,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
 
+  // Row blocks of the active list this launch covers. For MODE_DW they are the
+  // K dimension; its units are vocab rows instead.
   const int n_rb = launch_row_blocks(args);
-  const int n_ru = (n_rb + CTAS - 1) / CTAS;  // row units: 128 * CTAS rows each
+  const int n_ru = MODE == MODE_DW ? (args.dw_rows + BM * CTAS - 1) / (BM * CTAS)
+                                   : (n_rb + CTAS - 1) / CTAS;  // units of 128*CTAS rows
   const int n_units = n_ru * args.n_cols;
+  const int k_iters = MODE == MODE_DW ? n_rb * (BM / BK) : args.k_iters;
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
@@ -232,9 +257,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // again and stores nothing.
         int li = ru * CTAS + static_cast<int>(rank);
         if (li >= n_rb) li = ru * CTAS;
-        const int a_row = (MODE == MODE_DH ? li : global_rb(args, li)) * BM;
+        const int a_row =
+            MODE == MODE_DW ? 0 : (MODE == MODE_DH ? li : global_rb(args, li)) * BM;
+        const int a_m0 = (ru * CTAS + static_cast<int>(rank)) * BM;  // MODE_DW: vocab row
         for (int t = t0; t < t1 && ok; ++t) {
-          for (int k = 0; k < args.k_iters; ++k, ++it) {
+          for (int k = 0; k < k_iters; ++k, ++it) {
             const int s = it % kStages;
             const uint32_t round = it / kStages;
             if (!mbar_wait(&empty_bar[s], (round & 1u) ^ 1u, abort_flag, args.status)) {
@@ -243,7 +270,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             uint8_t* a_dst = smem + s * C::kStageBytes;
             uint8_t* b_dst = a_dst + A_BYTES;
-            if (CTAS == 2) {
+            if (MODE == MODE_DW) {
+              const uint32_t lead = CTAS == 2 ? mapa_shared(smem_u32(&full_bar[s]), 0) : 0u;
+              if (CTAS == 2) mbar_arrive_expect_tx_cluster(lead, C::kStageBytes);
+              else mbar_arrive_expect_tx(&full_bar[s], C::kStageBytes);
+              const int kr = k * BK;  // chunk-local row of this K step
+              const int grow_k = global_rb(args, kr / BM) * BM + kr % BM;
+              // A = G^T: 128 vocab rows (two 64-wide MN blocks) x 64 chunk rows.
+#pragma unroll
+              for (int j = 0; j < 2; ++j)
+                load_box<CTAS>(a_dst + j * (BK * 64 * 2), &map_a, &full_bar[s], lead,
+                               a_m0 + j * 64, kr, true, pol_a);
+              // B = H: this CTA's D columns x the same 64 rows, in 64-wide blocks.
+#pragma unroll
+              for (int j = 0; j < C::kBRows / 64; ++j)
+                load_box<CTAS>(b_dst + j * (BK * 64 * 2), &map_b, &full_bar[s], lead,
+                               t * BN + static_cast<int>(rank) * C::kBRows + j * 64, grow_k,
+                               false, 0);
+            } else if (CTAS == 2) {
               // Both CTAs count their bytes on the leader's barrier.
               const uint32_t lead = mapa_shared(smem_u32(&full_bar[s]), 0);
               mbar_arrive_expect_tx_cluster(lead, C::kStageBytes);
@@ -285,7 +329,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer --
     if (lane == 0 && rank == 0) {
-      constexpr uint32_t idesc = idesc_bf16(BM * CTAS, BN, false, MODE == MODE_DH);
+      constexpr uint32_t idesc =
+          idesc_bf16(BM * CTAS, BN, MODE == MODE_DW, MODE == MODE_DH || MODE == MODE_DW);
       uint32_t it = 0, tile_it = 0;
       bool ok = true;
       for (int u = cta_slot; u < n_units && ok; u += n_slots) {
@@ -301,7 +346,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + buf * BN;
-          for (int k = 0; k < args.k_iters; ++k, ++it) {
+          for (int k = 0; k < k_iters; ++k, ++it) {
             const int s = it % kStages;
             const uint32_t round = it / kStages;
             if (!mbar_wait(&full_bar[s], round & 1u, abort_flag, args.status)) {
@@ -315,9 +360,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int kk = 0; kk < BK / 16; ++kk) {
               // K-major, 128B swizzle: K advances by 32 bytes inside the atom;
               // 8-row groups are 1024 bytes apart.
-              const uint64_t adesc = sdesc_sw128(a_addr + kk * 32, 16, 1024);
+              const uint64_t adesc = MODE == MODE_DW
+                                         ? sdesc_sw128(a_addr + kk * 2048, BK * 64 * 2, 1024)
+                                         : sdesc_sw128(a_addr + kk * 32, 16, 1024);
               uint64_t bdesc;
-              if (MODE == MODE_DH) {
+              if (MODE == MODE_DH || MODE == MODE_DW) {
                 // MN-major, 128B swizzle: 64-wide N blocks 8 KB apart (LBO),
                 // 8-deep K groups 1 KB apart (SBO); K advances 16 rows.
                 bdesc = sdesc_sw128(b_addr + kk * 2048, BK * 64 * 2, 1024);
@@ -483,7 +530,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               for (int j = 0; j < 32; ++j)
                 if (col0 + j >= args.vocab) v[j] = 0.f;
             }
-            if (valid) {
+            // Rows past N in an active block come out exactly 0 (zero-filled
+            // hidden rows, g = 0); they are written too, so that the G block
+            // holds no stale bytes for the dW GEMM.
+            if (block_ok) {
               uint32_t p[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) p[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
@@ -491,6 +541,44 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
               for (int j = 0; j < 4; ++j)
                 st_global_v4(dst + j * 8, p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+            }
+          }
+        } else if (MODE == MODE_DW) {
+          const int vrow = ru * CTAS * BM + static_cast<int>(rank) * BM + lrow_in_tile;
+          const bool vvalid = vrow < args.dw_rows;
+          float* out = args.dW + (static_cast<long long>(args.v0) + vrow) * args.hidden;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            const int d0 = t * BN + c * 32;
+            if (d0 >= args.hidden) break;  // warp-uniform
+            float v[32];
+            tmem_ld32(tbase + c * 32, v);
+            if (k_iters == 0) {  // no row of the chunk is active: nothing accumulated
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
+            if (vvalid) {
+#pragma unroll
+              for (int j8 = 0; j8 < 4; ++j8) {
+                if (d0 + j8 * 8 >= args.hidden) break;
+                float* o8 = out + d0 + j8 * 8;
+                if (!args.first) {
+                  const float4 x0 = *reinterpret_cast<const float4*>(o8);
+                  const float4 x1 = *reinterpret_cast<const float4*>(o8 + 4);
+                  v[j8 * 8 + 0] += x0.x;
+                  v[j8 * 8 + 1] += x0.y;
+                  v[j8 * 8 + 2] += x0.z;
+                  v[j8 * 8 + 3] += x0.w;
+                  v[j8 * 8 + 4] += x1.x;
+                  v[j8 * 8 + 5] += x1.y;
+                  v[j8 * 8 + 6] += x1.z;
+                  v[j8 * 8 + 7] += x1.w;
+                }
+                *reinterpret_cast<float4*>(o8) =
+                    make_float4(v[j8 * 8 + 0], v[j8 * 8 + 1], v[j8 * 8 + 2], v[j8 * 8 + 3]);
+                *reinterpret_cast<float4*>(o8 + 4) =
+                    make_float4(v[j8 * 8 + 4], v[j8 * 8 + 5], v[j8 * 8 + 6], v[j8 * 8 + 7]);
+              }
             }
           }
         } else {  // MODE_DH

@@ -122,6 +122,8 @@ cudaError_t launch_bwdg_gemm(int ctas, const CUtensorMap& map_a, const CUtensorM
                              const TileArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_dh_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                            const TileArgs& args, int grid, cudaStream_t stream);
+cudaError_t launch_dw_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                           const TileArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_row_plan(const uint8_t* mask, long long n, int n_rb, int* rb_list,
                             int* n_active, double* msum, cudaStream_t stream);
 cudaError_t launch_seq_lens(const uint8_t* mask, long long n, int seq_len, int* lens,

@@ -158,12 +158,16 @@ int grpo_logp_fwd(const void* hidden, const void* W, const int32_t* ids, float* 
  *   loss:         fp32 [1] device scalar output (sum accumulated in fp64)
  *   logp_or_null: fp32 [N] output (0 on masked rows), or NULL
  *   dH:           bf16 [N, D] output; masked rows are exactly 0
+ *   dW_or_null:   fp32 [V, D] output, the lm_head gradient
+ *                 dW_v = sum_t g_t (onehot_v(y_t) - softmax_v) f'(z_tv) h_t
+ *                 (overwritten, 16-byte aligned), or NULL when the head is
+ *                 frozen (the LoRA case); costs one more GEMM of 2 N D V flops
  * M = 0 gives loss = 0 and dH = 0. Ids of masked rows are never read. */
 int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
                       const uint8_t* mask, const float* old_logp, const float* ref_logp,
                       const float* adv, float* loss, float* logp_or_null, void* dH,
-                      const grpo_shape* shape, const grpo_params* params, void* workspace,
-                      size_t workspace_bytes, void* stream);
+                      float* dW_or_null, const grpo_shape* shape, const grpo_params* params,
+                      void* workspace, size_t workspace_bytes, void* stream);
 
 /* How a call with this shape and these params is carried out on the current
  * device (host only; reads the device's SM count, launches nothing). */

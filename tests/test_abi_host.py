@@ -100,7 +100,7 @@ def test_bad_params_rejected(clp):
 def test_null_pointers_rejected_before_launch(clp):
     shape = clp.make_shape(10, 5, 16, 50)
     rc = clp.lib.grpo_loss_fwd_bwd(None, None, None, None, None, None, None, None, None, None,
-                                   ctypes.byref(shape), None, None, 0, None)
+                                   None, ctypes.byref(shape), None, None, 0, None)
     assert rc == -1
     rc = clp.lib.grpo_logp_fwd(None, None, None, None, None, ctypes.byref(shape), None, None, 0,
                                None)
@@ -112,7 +112,7 @@ def test_sequence_length_must_divide_tokens(clp):
     buf = ctypes.create_string_buffer(4096)
     addr = (ctypes.addressof(buf) + 255) // 256 * 256
     rc = clp.lib.grpo_loss_fwd_bwd(addr, addr, addr, addr, addr, addr, addr, addr, None, addr,
-                                   ctypes.byref(shape), None, addr, 1024, None)
+                                   None, ctypes.byref(shape), None, addr, 1024, None)
     assert rc == -3
 
 

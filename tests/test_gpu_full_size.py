@@ -130,3 +130,19 @@ def test_llama_full_loss_exact(clp):
     print(f"llama full: max|dlogp|={d.max():.3e} rms={np.sqrt((d ** 2).mean()):.3e} "
           f"loss={L:.6e} want={L_want:.6e} rel={rel:.3e}")
     assert d.max() <= LOGP_TOL and rel <= LOSS_RTOL
+
+
+def test_llama_lm_head_gradient_column_sums(clp):
+    # sum_v (onehot - softmax)_v = 0 per token, so the columns of dW sum to ~0 at
+    # any size: a full-size property check of the dW GEMM (both backward modes).
+    p = synth.make_problem("llama-3.1-8b", seed=4)
+    old = torch.full((p.n_tokens,), -12.0)
+    dev = torch.device(DEV)
+    args = [t.to(dev) for t in (p.hidden, p.weight, p.ids, p.mask, old, old, p.adv)]
+    for flags in (0, 1):
+        params = clp.make_params(flags=flags)
+        _, _, _, dW = clp.grpo_loss_fwd_bwd(*args, p.seq_len, params=params, want_dW=True)
+        colsum = dW.double().sum(dim=0).abs().max().item()
+        scale = dW.double().abs().sum(dim=0).max().item()
+        print(f"llama dW flags={flags}: max|col sum|={colsum:.3e} vs col |.| sum {scale:.3e}")
+        assert torch.isfinite(dW).all() and colsum <= 2e-2 * scale

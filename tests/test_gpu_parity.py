@@ -393,3 +393,70 @@ def test_workspace_budget_plans_give_same_results(clp, flags, limit):
         assert clp.grpo_workspace_size(p.n_tokens, p.hidden_size, p.vocab, p.seq_len,
                                        params) <= limit
     check(gpu_loss(clp, p, old, ref, params), want, p.mask, f"budget {flags} {limit}")
+
+
+# ----------------------------------------------------- lm_head gradient dW --
+
+DW_CASES = [
+    # N, T, D, V, chunk, vblock, padded, flags
+    (256, 64, 256, 4096, 0, 0, False, 0),
+    (256, 64, 256, 4096, 0, 0, False, STORED),
+    (300, 75, 200, 1000, 128, 512, True, 0),
+    (300, 75, 200, 1000, 128, 512, True, STORED),
+    (300, 75, 200, 1000, 128, 512, True, SINGLE),
+    (300, 75, 200, 1000, 128, 512, True, SINGLE | STORED),
+    (4096, 512, 256, 3000, 256, 1024, True, STORED),   # many skipped blocks, empty chunks
+    (4096, 512, 256, 3000, 256, 1024, True, 0),
+]
+
+
+@pytest.mark.parametrize("N,T,D,V,chunk,vblock,padded,flags", DW_CASES)
+def test_lm_head_gradient(clp, N, T, D, V, chunk, vblock, padded, flags):
+    G = 4 if (N // T) % 4 == 0 else 1
+    p = synth.make_problem("tiny", seed=N + V + flags, prompts=(N // T) // G, G=G, T=T, D=D,
+                           V=V, lengths=(1 if N >= 4096 else T // 3, T) if padded else None)
+    old, ref, want = oracle_case(p)
+    want_dW = oracle.grad_weight(p.hidden, p.weight, p.ids.numpy(), want["g"])
+    params = clp.make_params(chunk_tokens=chunk, vocab_block=vblock, flags=flags)
+    ws = clp.alloc_workspace(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, params, DEV)
+    dW = torch.full((V, D), float("nan"), device=DEV)
+    loss, logp, dH, dW = clp.grpo_loss_fwd_bwd(
+        _to(p.hidden), _to(p.weight), _to(p.ids), _to(p.mask), _to(old), _to(ref), _to(p.adv),
+        p.seq_len, params=params, workspace=ws, dW=dW)
+    st = clp.grpo_read_device_status(ws)
+    check((loss.item(), logp.cpu().double().numpy(), dH.cpu().double().numpy(), st), want,
+          p.mask, f"dW case {N}x{D}x{V} flags={flags}")
+    got = dW.cpu().double().numpy()
+    rel = np.linalg.norm(got - want_dW) / np.linalg.norm(want_dW)
+    print(f"   dW rel={rel:.3e}")
+    assert np.all(np.isfinite(got)) and rel <= DH_RTOL
+
+
+def test_lm_head_gradient_all_masked_is_zero(clp):
+    p = synth.make_problem("tiny", seed=62)
+    dW = torch.full((p.vocab, p.hidden_size), float("nan"), device=DEV)
+    for flags in (0, STORED):
+        _, _, _, dW = clp.grpo_loss_fwd_bwd(
+            _to(p.hidden), _to(p.weight), _to(p.ids), _to(torch.zeros_like(p.mask)),
+            _to(torch.zeros(p.n_tokens)), _to(torch.zeros(p.n_tokens)), _to(p.adv), p.seq_len,
+            params=clp.make_params(flags=flags), dW=dW)
+        assert torch.all(dW == 0)
+
+
+def test_lm_head_gradient_with_transform(clp):
+    p = synth.make_problem("tiny", seed=63, T=75, prompts=1, G=4, D=200, V=3000,
+                           lengths=(20, 75), weight_std=0.2)
+    xf = oracle.Transform(softcap=2.0, temperature=0.8)
+    base, _ = oracle.selective_logp(p.hidden, p.weight, p.ids.numpy(), xf=xf)
+    old, ref = p.old_ref(torch.from_numpy(base))
+    want = oracle.loss_fwd_bwd(p.hidden, p.weight, p.ids.numpy(), p.mask.numpy(), old, ref,
+                               p.adv, p.seq_len, p.eps_low, p.eps_high, p.beta, xf=xf)
+    want_dW = oracle.grad_weight(p.hidden, p.weight, p.ids.numpy(), want["g"], xf=xf)
+    for flags in (0, STORED):
+        params = clp.make_params(chunk_tokens=128, flags=flags, logit_softcapping=2.0,
+                                 temperature=0.8)
+        _, _, _, dW = clp.grpo_loss_fwd_bwd(
+            _to(p.hidden), _to(p.weight), _to(p.ids), _to(p.mask), _to(old), _to(ref),
+            _to(p.adv), p.seq_len, params=params, want_dW=True)
+        rel = np.linalg.norm(dW.cpu().double().numpy() - want_dW) / np.linalg.norm(want_dW)
+        assert rel <= DH_RTOL, (flags, rel)
