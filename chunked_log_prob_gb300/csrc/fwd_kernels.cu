@@ -356,8 +356,8 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
     return;
   }
   const float ng = -g;
-  for (int i = threadIdx.x; i < n_vec; i += blockDim.x) {
-    const uint4 in = row[i];
+  // G_v from the stored z'_v: g (onehot_v(y) - exp(z'_v - lse)) f'(z_v).
+  auto convert = [&](const uint4 in, int i) {
     const uint32_t w[4] = {in.x, in.y, in.z, in.w};
     uint32_t o[4];
 #pragma unroll
@@ -380,8 +380,18 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
       }
       o[k] = pack_bf16x2(gv[0], gv[1]);
     }
-    row[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  };
+  // Two 16-byte vectors per thread per step keep more loads in flight.
+  const int step = 2 * blockDim.x;
+  int i = threadIdx.x;
+  for (; i + blockDim.x < n_vec; i += step) {
+    const uint4 in0 = row[i];
+    const uint4 in1 = row[i + blockDim.x];
+    row[i] = convert(in0, i);
+    row[i + blockDim.x] = convert(in1, i + blockDim.x);
   }
+  if (i < n_vec) row[i] = convert(row[i], i);
 }
 
 // Closing reduction of a stored-logit call: masked rows get logp = 0, and the

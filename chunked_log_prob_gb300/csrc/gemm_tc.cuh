@@ -158,7 +158,7 @@ struct PairCfg {
   static constexpr int kBRows = BN / CTAS;             // B rows (cols) per CTA
   static constexpr int kBBytes = kBRows * BK * 2;
   static constexpr int kStageBytes = A_BYTES + kBBytes;
-  static constexpr int kStages = CTAS == 2 ? 6 : STAGES;
+  static constexpr int kStages = CTAS == 2 ? 7 : STAGES;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
 };
 
