@@ -34,7 +34,7 @@ class GrpoParams(ctypes.Structure):
     _fields_ = [("eps_low", ctypes.c_float), ("eps_high", ctypes.c_float),
                 ("beta", ctypes.c_float), ("loss_denominator", ctypes.c_float),
                 ("chunk_tokens", ctypes.c_int32), ("vocab_block", ctypes.c_int32),
-                ("flags", ctypes.c_uint32), ("reserved", ctypes.c_uint32),
+                ("flags", ctypes.c_uint32), ("raster_rows", ctypes.c_int32),
                 ("logit_scale_multiply", ctypes.c_float), ("logit_scale_divide", ctypes.c_float),
                 ("logit_softcapping", ctypes.c_float), ("temperature", ctypes.c_float),
                 ("workspace_limit_bytes", ctypes.c_uint64)]
@@ -103,7 +103,7 @@ def status_string(code: int) -> str:
 def make_params(eps_low=0.2, eps_high=0.2, beta=0.001, loss_denominator=0.0,
                 chunk_tokens=0, vocab_block=0, *, logit_scale_multiply=0.0,
                 logit_scale_divide=0.0, logit_softcapping=0.0, temperature=0.0,
-                flags=0, workspace_limit_bytes=0) -> GrpoParams:
+                flags=0, workspace_limit_bytes=0, raster_rows=0) -> GrpoParams:
     p = GrpoParams()
     lib.grpo_default_params(ctypes.byref(p))
     p.eps_low, p.eps_high, p.beta = eps_low, eps_high, beta
@@ -113,6 +113,7 @@ def make_params(eps_low=0.2, eps_high=0.2, beta=0.001, loss_denominator=0.0,
     p.logit_softcapping, p.temperature = logit_softcapping, temperature
     p.flags = flags
     p.workspace_limit_bytes = int(workspace_limit_bytes)
+    p.raster_rows = int(raster_rows)
     return p
 
 

@@ -216,12 +216,23 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   return GRPO_OK;
 }
 
-// Row blocks per raster group: the CTAs in flight (one per SM) cover
-// group_rows row blocks x (sms / group_rows) vocab tiles or splits, so each
-// W tile fetched from HBM is shared through L2 by group_rows CTAs and each row
-// block's hidden states by the others.
+// Row units per raster group: the slots in flight (one per SM pair) cover
+// group_rows row units x (slots / group_rows) vocab tiles or splits, so each
+// W tile fetched from HBM is shared through L2 by group_rows slots and each
+// row unit's hidden states by the others.
 int group_rows_for(int n_rb, int sms) {
   return std::max(1, std::min(n_rb, std::max(1, sms) / kSplitsTarget));
+}
+
+// Same, with group_rows a divisor of the slot count (at least 4 columns per
+// group): a group is then exactly one round of the persistent grid, and the
+// slots that share a W range all run in the same round.
+int group_rows_exact(int n_ru, int slots) {
+  slots = std::max(1, slots);
+  const int cap = std::max(1, std::min(n_ru, slots / 4));
+  for (int r = cap; r > 1; --r)
+    if (slots % r == 0) return r;
+  return 1;
 }
 
 int check_shape(const grpo_shape* s, bool need_seq) {
@@ -240,7 +251,7 @@ int check_shape(const grpo_shape* s, bool need_seq) {
 int check_params(const grpo_params* p) {
   if (!p) return GRPO_OK;
   if ((p->flags & ~(GRPO_FLAG_STORED_LOGITS | GRPO_FLAG_SINGLE_CTA | GRPO_FLAG_SEQUENCE_MEAN |
-                    GRPO_FLAG_FIT_FREE_MEMORY)) != 0 || p->reserved != 0 || p->chunk_tokens < 0 ||
+                    GRPO_FLAG_FIT_FREE_MEMORY)) != 0 || p->raster_rows < 0 || p->chunk_tokens < 0 ||
       p->vocab_block < 0)
     return GRPO_ERR_INVALID_ARG;
   if (!(p->eps_low >= 0.f) || !(p->eps_high >= 0.f) || !(p->beta >= 0.f))
@@ -405,7 +416,8 @@ int run_forward(const void* hidden, const void* W, const int32_t* ids, const uin
   a.n_active = n_active;
   a.k_iters = static_cast<int>(cdiv(L.D, BK));
   const int n_ru = static_cast<int>(cdiv(a.n_rb, L.ctas));
-  a.group_rows = group_rows_for(n_ru, slots);
+  a.group_rows = (prm != nullptr && prm->raster_rows > 0) ? std::min(prm->raster_rows, n_ru)
+                                                         : group_rows_exact(n_ru, slots);
   int splits = std::max(1, slots / a.group_rows);
   splits = std::min(splits, std::min(L.nvt, kMaxSplits));
   a.n_cols = splits;
@@ -486,7 +498,8 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
       a.rb_list = w.rb_list;
       a.n_active = w.n_active;
       a.k_iters = static_cast<int>(cdiv(L.D, BK));
-      a.group_rows = group_rows_for(n_ru, slots);
+      a.group_rows = (prm != nullptr && prm->raster_rows > 0) ? std::min(prm->raster_rows, n_ru)
+                                                             : group_rows_exact(n_ru, slots);
       a.n_cols = ntile;
       a.v0 = static_cast<int>(v0);
       a.ids = ids;
@@ -832,7 +845,7 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
   info->n_vocab_blocks = static_cast<int32_t>(cdiv(L.V, L.vblock));
   const int n_rb = static_cast<int>(L.nr / BM);
   const int slots = std::max(1, sms / L.ctas);
-  const int grp = group_rows_for(static_cast<int>(cdiv(n_rb, L.ctas)), slots);
+  const int grp = group_rows_exact(static_cast<int>(cdiv(n_rb, L.ctas)), slots);
   info->fwd_splits = std::min(std::max(1, slots / grp), std::min(L.nvt, kMaxSplits));
   info->launches_logp = L.n > 0 ? 2 : 0;
   info->launches_loss = L.n <= 0 ? 0

@@ -100,7 +100,8 @@ typedef struct grpo_params {
   int32_t chunk_tokens;   /* rows per backward chunk; 0 = automatic            */
   int32_t vocab_block;    /* vocab columns per backward block; 0 = automatic   */
   uint32_t flags;         /* GRPO_FLAG_* bits, or 0                           */
-  uint32_t reserved;      /* must be 0                                         */
+  int32_t raster_rows;    /* row units per raster group of the persistent GEMM
+                             grids (a tuning knob; 0 = automatic)             */
   /* Logit transforms ("GRPO with 7x longer context", the options of the
    * selective log-softmax call: logit scale multiply/divide, softcapping,
    * temperature), applied to the raw logit z in that order:
