@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     grpo_logp_fwd_noalloc,
     grpo_loss_fwd_bwd,
     grpo_read_device_status,
+    grpo_selftest_bounded_wait,
     grpo_workspace_size,
     lib,
     make_params,

@@ -76,6 +76,8 @@ def _load():
     lib.grpo_read_device_status.restype = ctypes.c_int
     lib.grpo_logp_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, P(GrpoShape), vp]
     lib.grpo_logp_fwd_noalloc.restype = ctypes.c_int
+    lib.grpo_selftest_bounded_wait.argtypes = [vp, sz, vp]
+    lib.grpo_selftest_bounded_wait.restype = ctypes.c_int
     lib.grpo_status_string.argtypes = [ctypes.c_int]
     lib.grpo_status_string.restype = ctypes.c_char_p
     return lib
@@ -85,7 +87,7 @@ lib = _load()
 
 EXPORTED = ("grpo_default_params", "grpo_workspace_size", "grpo_logp_fwd",
             "grpo_loss_fwd_bwd", "grpo_get_plan", "grpo_read_device_status",
-            "grpo_logp_fwd_noalloc", "grpo_status_string")
+            "grpo_logp_fwd_noalloc", "grpo_selftest_bounded_wait", "grpo_status_string")
 
 FLAG_STORED_LOGITS = 1
 FLAG_SINGLE_CTA = 2
@@ -271,3 +273,12 @@ def grpo_logp_fwd_noalloc(hidden, W, ids, logp, lse=None):
     if rc != GRPO_OK:
         raise GrpoError(rc, "grpo_logp_fwd_noalloc")
     return logp, lse
+
+
+def grpo_selftest_bounded_wait(workspace) -> int:
+    """Runs the bounded-wait self-test; returns the device status it left (-7 expected)."""
+    rc = lib.grpo_selftest_bounded_wait(_ptr(workspace), workspace.numel(),
+                                        _stream(workspace.device))
+    if rc != GRPO_OK:
+        raise GrpoError(rc, "grpo_selftest_bounded_wait")
+    return grpo_read_device_status(workspace)

@@ -874,6 +874,22 @@ int grpo_read_device_status(const void* workspace, int* device_status, void* str
   return GRPO_OK;
 }
 
+int grpo_selftest_bounded_wait(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes < 64) return GRPO_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return GRPO_ERR_MISALIGNED;
+  int sms = 0;
+  int r = device_setup(&sms);
+  if (r != GRPO_OK) return r;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  if (cudaMemsetAsync(workspace, 0, 64, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  if (launch_bounded_wait_selftest(reinterpret_cast<int*>(base + kOffStatus),
+                                   reinterpret_cast<int*>(base + kOffCounter), st) !=
+      cudaSuccess)
+    return GRPO_ERR_CUDA;
+  return GRPO_OK;
+}
+
 const char* grpo_status_string(int s) {
   switch (s) {
     case GRPO_OK: return "ok";

@@ -444,3 +444,32 @@ cudaError_t launch_finish_loss(const FinishArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace grpo
+
+// ---------------------------------------------------------------------------
+// Self-test of the bounded waits: one thread waits, with the same routine the
+// GEMM roles use, on an mbarrier that nothing ever arrives on. The wait must
+// run out, record GRPO_ERR_DEVICE_TIMEOUT in the status word and return; the
+// kernel then exits normally and the context stays usable.
+namespace grpo {
+
+__global__ void bounded_wait_selftest_kernel(int* status, int* waited_out) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_sh;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const bool ok = mbar_wait(&bar, 0, &abort_sh, status);  // phase 0 never completes
+    *waited_out = ok ? 0 : 1;
+  }
+}
+
+cudaError_t launch_bounded_wait_selftest(int* status, int* waited_out, cudaStream_t stream) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(status, waited_out);
+  return cudaGetLastError();
+}
+
+}  // namespace grpo

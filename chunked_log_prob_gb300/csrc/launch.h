@@ -136,5 +136,6 @@ cudaError_t launch_fwds_gemm(int ctas, const CUtensorMap& map_a, const CUtensorM
                              const TileArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_finalize_gform(const GformArgs& a, int rows, cudaStream_t stream);
 cudaError_t launch_finish_loss(const FinishArgs& a, cudaStream_t stream);
+cudaError_t launch_bounded_wait_selftest(int* status, int* waited_out, cudaStream_t stream);
 
 }  // namespace grpo

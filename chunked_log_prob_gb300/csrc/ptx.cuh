@@ -1,7 +1,7 @@
 // Inline-PTX building blocks for sm_103a: mbarriers with bounded waits, TMA
 // tile loads, tcgen05 MMA / TMEM access and shared-memory matrix descriptors.
 //
-// Every wait here is bounded: after ~2 s of spinning the waiting thread sets
+// Every wait here is bounded: after ~1 s of spinning the waiting thread sets
 // the CTA's abort flag and the device status word, and returns false. Callers
 // then skip the rest of their work and fall through to the kernel's exit path,
 // so no wait can hang the GPU.
@@ -53,8 +53,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// ~2 s at the GB300's clocks: far beyond any legitimate wait in these kernels.
-constexpr long long kWaitLimitCycles = 4000000000LL;
+// About 1 s at the GB300's clocks (1.0-1.4 s between 2.07 and 1.4 GHz): far
+// beyond any legitimate wait in these kernels (a stage or a tile: us to ms).
+constexpr long long kWaitLimitCycles = 2000000000LL;
 
 // Waits for the phase of `bar` with the given parity to complete. Returns
 // false (and raises the abort flag and the status word) on timeout, or when

@@ -220,6 +220,15 @@ int grpo_read_device_status(const void* workspace, int* device_status, void* str
 int grpo_logp_fwd_noalloc(const void* hidden, const void* W, const int32_t* ids, float* logp,
                           float* lse_or_null, const grpo_shape* shape, void* stream);
 
+/* Self-test of the device-side failure detection. Launches one tiny kernel
+ * that waits, with the same bounded wait every GEMM role uses, on an mbarrier
+ * that nothing ever arrives on: after about one second the wait gives up,
+ * records GRPO_ERR_DEVICE_TIMEOUT in the status word of `workspace` (>= 64
+ * bytes, 256-byte aligned) and the kernel returns normally - no trap, no
+ * hang, the context stays usable. Read the outcome with
+ * grpo_read_device_status. Returns GRPO_OK if the launch went through. */
+int grpo_selftest_bounded_wait(void* workspace, size_t workspace_bytes, void* stream);
+
 /* Static text for a status code. */
 const char* grpo_status_string(int status);
 
