@@ -44,6 +44,7 @@ struct Layout {
   int T, D, V;
   int nvt;          // vocab tiles
   int chunk_rows;   // backward chunk (multiple of BM)
+  int n_sbuf;       // stored path: logit blocks (2 = double-buffered chunks)
   int vblock;       // backward vocab block (multiple of BN)
   bool need_acc;    // more than one vocab block -> fp32 dH accumulator
   size_t off_pm, off_ps, off_zy, off_lse, off_g, off_rbl, off_lt, off_seq, off_G, off_acc, total;
@@ -178,8 +179,11 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   const int slots = sms / L->ctas;
   // Bytes of the chunk block per row unit: bf16 G (+ fp32 dH accumulator) or
   // fp16 logits.
+  // The stored path keeps two chunk blocks when there is more than one chunk
+  // (one being turned into G while the next chunk's logits are computed).
   const size_t unit_bytes = static_cast<size_t>(ru_rows) *
-                            (static_cast<size_t>(L->vblock) * 2 + (L->need_acc ? L->D * 4 : 0));
+                            (static_cast<size_t>(L->vblock) * 2 * (L->stored ? 2 : 1) +
+                             (L->need_acc ? L->D * 4 : 0));
   long long max_units = L->stored ? std::max(1, stored_max_blocks(L->ldS) / L->ctas)
                                   : kMaxAutoChunkBlocks / L->ctas;
   const size_t budget = workspace_budget(p);
@@ -205,10 +209,12 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   crows = std::min(crows, n_ru_total * ru_rows);
   if (crows > INT_MAX / 2) return GRPO_ERR_UNSUPPORTED_SHAPE;
   L->chunk_rows = static_cast<int>(crows);
+  L->n_sbuf = (L->stored && cdiv(L->nr, L->chunk_rows) > 1) ? 2 : 1;
 
   // Backward chunk block: bf16 G [C x V_b] (recompute path) or the chunk's
-  // fp16 logits, rewritten in place as bf16 G [C x ldS] (stored path).
-  off = align_up(off + static_cast<size_t>(L->chunk_rows) * L->vblock * 2, 256);
+  // fp16 logits, rewritten in place as bf16 G [C x ldS] (stored path; two of
+  // them when double-buffered).
+  off = align_up(off + static_cast<size_t>(L->n_sbuf) * L->chunk_rows * L->vblock * 2, 256);
   L->off_acc = off;
   if (L->need_acc) off = align_up(off + static_cast<size_t>(L->chunk_rows) * L->D * 4, 256);
   L->total = off;
@@ -295,6 +301,12 @@ struct DeviceInfo {
   bool ready = false;
   int status = GRPO_OK;
   int sms = 0;
+  // Side stream for the stored path's row-wise G formation, which overlaps
+  // the next chunk's logit GEMM; events order it against the caller's stream.
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_main = nullptr;
+  cudaEvent_t ev_fwd[2] = {nullptr, nullptr};
+  cudaEvent_t ev_g[2] = {nullptr, nullptr};
 };
 
 std::mutex g_mu;
@@ -320,6 +332,14 @@ int device_setup(int* sms) {
                prepare_fwds_gemm() != cudaSuccess) {
       d.status = GRPO_ERR_CUDA;
     }
+    if (d.status == GRPO_OK) {
+      bool okc = cudaStreamCreateWithFlags(&d.side, cudaStreamNonBlocking) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&d.ev_main, cudaEventDisableTiming) == cudaSuccess;
+      for (int i = 0; i < 2 && okc; ++i)
+        okc = cudaEventCreateWithFlags(&d.ev_fwd[i], cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&d.ev_g[i], cudaEventDisableTiming) == cudaSuccess;
+      if (!okc) d.status = GRPO_ERR_CUDA;
+    }
     if (d.status == GRPO_OK && g_encode == nullptr) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -334,6 +354,12 @@ int device_setup(int* sms) {
   }
   *sms = d.sms;
   return d.status;
+}
+
+DeviceInfo* current_device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  return &g_dev[dev];
 }
 
 // 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows,
@@ -549,7 +575,10 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
 // Stored-logit path of a loss call, chunk by chunk over the active row
 // blocks: forward GEMM that also stores the chunk's fp16 logits; per-row
 // finish (lse, logp, token loss, g) rewriting the logits in place as bf16 G;
-// dH GEMM over the whole vocabulary. A closing kernel reduces the loss.
+// dH GEMM over the whole vocabulary (and dW, when asked). With two chunk
+// blocks the per-row finish of chunk c runs on a side stream while chunk c+1's
+// logits are computed; the caller's stream sees one ordered sequence:
+//   FWDS(0) FWDS(1) DH(0) FWDS(2) DH(1) ... DH(n-1), then the loss reduction.
 int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint8_t* mask,
                const float* old_logp, const float* ref_logp, const float* adv, float* loss,
                float* logp_out, void* dH, float* dW, const grpo_params* prm, const Layout& L,
@@ -560,20 +589,29 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
       !encode_2d(&map_w_k, W, L.D, L.V, L.D, BK, BN / L.ctas) ||
       !encode_2d(&map_w_mn, W, L.D, L.V, L.D, 64, BK))
     return GRPO_ERR_CUDA;
+  DeviceInfo* di = current_device_info();
+  if (di == nullptr) return GRPO_ERR_CUDA;
+  const bool overlap = L.n_sbuf == 2;
   const int n_dt = static_cast<int>(cdiv(L.D, BN));
   const int n_rb_total = static_cast<int>(L.nr / BM);
   const int rb_per_chunk = L.chunk_rows / BM;
-  uint16_t* S = reinterpret_cast<uint16_t*>(w.G);
-  for (int rb0 = 0; rb0 < n_rb_total; rb0 += rb_per_chunk) {
-    const int n_rb = std::min(rb_per_chunk, n_rb_total - rb0);
+  const int n_chunks = static_cast<int>(cdiv(n_rb_total, rb_per_chunk));
+  auto sbuf = [&](int c) {
+    return reinterpret_cast<uint16_t*>(w.G) +
+           (overlap ? static_cast<size_t>(c & 1) * L.chunk_rows * L.ldS : 0);
+  };
+  auto chunk_rbs = [&](int c) { return std::min(rb_per_chunk, n_rb_total - c * rb_per_chunk); };
+
+  // (1) logits of chunk c: online LSE partials, z_y, fp16 copy.
+  auto fwds = [&](int c, int* splits_out) -> int {
+    const int n_rb = chunk_rbs(c);
     const int n_ru = static_cast<int>(cdiv(n_rb, L.ctas));
     const int splits = stored_fwd_splits(n_ru, L.nvt, slots, nullptr);
-    // (1) logits of the chunk: online LSE partials, z_y, fp16 copy.
     TileArgs a = base_args(L, w);
     set_transform(&a, prm);
     a.n_total = L.n;
     a.n_rb = n_rb;
-    a.rb_offset = rb0;
+    a.rb_offset = c * rb_per_chunk;
     a.rb_list = w.rb_list;
     a.n_active = w.n_active;
     a.k_iters = static_cast<int>(cdiv(L.D, BK));
@@ -587,19 +625,24 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     a.part_s = w.ps;
     a.zy = w.zy;
     a.part_ld = L.nr;
-    a.S = S;
+    a.S = sbuf(c);
     a.ldS = L.ldS;
-    long long units = static_cast<long long>(n_ru) * splits;
-    if (launch_fwds_gemm(L.ctas, map_h, map_w_k, a,
-                         L.ctas * static_cast<int>(std::min<long long>(units, slots)),
-                         st) != cudaSuccess)
-      return GRPO_ERR_CUDA;
-    // (2) per-row finish; the chunk block becomes G.
+    const long long units = static_cast<long long>(n_ru) * splits;
+    *splits_out = splits;
+    return launch_fwds_gemm(L.ctas, map_h, map_w_k, a,
+                            L.ctas * static_cast<int>(std::min<long long>(units, slots)),
+                            st) == cudaSuccess
+               ? GRPO_OK
+               : GRPO_ERR_CUDA;
+  };
+  // (2) per-row finish of chunk c; its block becomes G.
+  auto gform = [&](int c, int splits, cudaStream_t s2) -> int {
+    const int n_rb = chunk_rbs(c);
     GformArgs f;
     std::memset(&f, 0, sizeof(f));
     f.n_total = L.n;
     f.n_rb = n_rb;
-    f.rb_offset = rb0;
+    f.rb_offset = c * rb_per_chunk;
     f.rb_list = w.rb_list;
     f.n_active = w.n_active;
     f.splits = splits;
@@ -624,21 +667,27 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     f.n_nonempty = w.n_nonempty;
     f.logp_out = logp_out;
     f.lt = w.lt;
-    f.S = S;
+    f.S = sbuf(c);
     f.ldS = L.ldS;
-    f.xmode = a.xmode;
-    f.k0 = a.k0;
-    f.k2 = a.k2;
+    TileArgs t = base_args(L, w);
+    set_transform(&t, prm);
+    f.xmode = t.xmode;
+    f.k0 = t.k0;
+    f.k2 = t.k2;
     f.status = w.status;
-    if (launch_finalize_gform(f, n_rb * BM, st) != cudaSuccess) return GRPO_ERR_CUDA;
-    // (3) dH rows of the chunk = G W over the whole vocabulary.
+    return launch_finalize_gform(f, n_rb * BM, s2) == cudaSuccess ? GRPO_OK : GRPO_ERR_CUDA;
+  };
+  // (3) dH rows of chunk c = G W over the whole vocabulary; (4) dW.
+  auto dh = [&](int c) -> int {
+    const int n_rb = chunk_rbs(c);
+    const int n_ru = static_cast<int>(cdiv(n_rb, L.ctas));
     CUtensorMap map_g;
-    if (!encode_2d(&map_g, S, L.V, static_cast<uint64_t>(n_rb) * BM, L.ldS, BK, BM))
+    if (!encode_2d(&map_g, sbuf(c), L.V, static_cast<uint64_t>(n_rb) * BM, L.ldS, BK, BM))
       return GRPO_ERR_CUDA;
     TileArgs b = base_args(L, w);
     b.n_total = L.n;
     b.n_rb = n_rb;
-    b.rb_offset = rb0;
+    b.rb_offset = c * rb_per_chunk;
     b.rb_list = w.rb_list;
     b.n_active = w.n_active;
     b.k_iters = static_cast<int>(cdiv(L.V, BK));
@@ -648,18 +697,51 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     b.dH = static_cast<__nv_bfloat16*>(dH);
     b.first = 1;
     b.last = 1;
-    units = static_cast<long long>(n_ru) * n_dt;
+    const long long units = static_cast<long long>(n_ru) * n_dt;
     if (launch_dh_gemm(L.ctas, map_g, map_w_mn, b,
                        L.ctas * static_cast<int>(std::min<long long>(units, slots)),
                        st) != cudaSuccess)
       return GRPO_ERR_CUDA;
-    // (4) optional lm_head gradient from the same G block.
-    if (dW != nullptr) {
-      const int r = launch_dw(hidden, reinterpret_cast<const __nv_bfloat16*>(S), L.ldS, 0, L.V,
-                              rb0, n_rb, dW, rb0 == 0, L, w, sms, st);
-      if (r != GRPO_OK) return r;
+    if (dW != nullptr)
+      return launch_dw(hidden, reinterpret_cast<const __nv_bfloat16*>(sbuf(c)), L.ldS, 0, L.V,
+                       c * rb_per_chunk, n_rb, dW, c == 0, L, w, sms, st);
+    return GRPO_OK;
+  };
+
+  int r = GRPO_OK;
+  if (!overlap) {
+    for (int c = 0; c < n_chunks && r == GRPO_OK; ++c) {
+      int splits = 1;
+      r = fwds(c, &splits);
+      if (r == GRPO_OK) r = gform(c, splits, st);
+      if (r == GRPO_OK) r = dh(c);
+    }
+  } else {
+    // The side stream starts after everything already on the caller's stream.
+    if (cudaEventRecord(di->ev_main, st) != cudaSuccess ||
+        cudaStreamWaitEvent(di->side, di->ev_main, 0) != cudaSuccess)
+      return GRPO_ERR_CUDA;
+    auto fwd_then_gform = [&](int c) -> int {
+      int splits = 1;
+      int rr = fwds(c, &splits);
+      if (rr != GRPO_OK) return rr;
+      if (cudaEventRecord(di->ev_fwd[c & 1], st) != cudaSuccess ||
+          cudaStreamWaitEvent(di->side, di->ev_fwd[c & 1], 0) != cudaSuccess)
+        return GRPO_ERR_CUDA;
+      rr = gform(c, splits, di->side);
+      if (rr != GRPO_OK) return rr;
+      return cudaEventRecord(di->ev_g[c & 1], di->side) == cudaSuccess ? GRPO_OK
+                                                                        : GRPO_ERR_CUDA;
+    };
+    r = fwd_then_gform(0);
+    for (int c = 0; c < n_chunks && r == GRPO_OK; ++c) {
+      if (c + 1 < n_chunks) r = fwd_then_gform(c + 1);  // buffer (c+1)&1: free after dh(c-1)
+      if (r != GRPO_OK) break;
+      if (cudaStreamWaitEvent(st, di->ev_g[c & 1], 0) != cudaSuccess) return GRPO_ERR_CUDA;
+      r = dh(c);
     }
   }
+  if (r != GRPO_OK) return r;
   FinishArgs fin;
   std::memset(&fin, 0, sizeof(fin));
   fin.n = L.n;

@@ -127,17 +127,19 @@ def test_misaligned_pointers_rejected(clp):
 
 
 def test_stored_logit_workspace_is_chunk_times_vocab(clp):
-    # Stored-logit backward: one fp16 logit block of chunk x V (V padded to 8),
-    # still independent of N.
+    # Stored-logit backward: two fp16 logit blocks of chunk x V (V padded to 8;
+    # double-buffered when there is more than one chunk), independent of N.
     p = clp.make_params(chunk_tokens=2048, flags=1)
     a = clp.grpo_workspace_size(16384, 4096, 128256, 1, p)
     b = clp.grpo_workspace_size(65536, 4096, 128256, 1, p)
     block = 2048 * 128256 * 2
-    assert block < a < block + 16384 * 400
+    assert 2 * block < a < 2 * block + 16384 * 400
+    one = clp.grpo_workspace_size(2048, 4096, 128256, 1, p)  # a single chunk: one block
+    assert block < one < block + 2048 * 400
     assert (b - a) / (65536 - 16384) < 64 * 4 * 2 + 64
     # Automatic chunk without a device: bounded by 2 GiB of logits.
     auto = clp.grpo_workspace_size(131072, 2880, 201088, 1, clp.make_params(flags=1))
-    assert auto < (2 << 30) + 131072 * 400
+    assert auto < 2 * (2 << 30) + 131072 * 400
 
 
 @pytest.mark.parametrize("flags", [0, 1])
