@@ -36,6 +36,9 @@ static_assert(kOffPartials + kMaxFinalizeBlocks * sizeof(double) <= kHeaderBytes
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
+// D columns per dH unit, in units of 256: the pair kernel covers 512.
+int dh_accumulators(int ctas) { return ctas == 2 ? 2 : 1; }
+
 struct Layout {
   int ctas;         // 2: CTA-pair GEMMs (default); 1: single-CTA GEMMs
   bool stored;      // stored-logit backward (GRPO_FLAG_STORED_LOGITS)
@@ -153,7 +156,8 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   L->D = s->hidden;
   L->V = s->vocab;
   L->nvt = static_cast<int>(cdiv(s->vocab, BN));
-  const int n_dt = static_cast<int>(cdiv(s->hidden, BN));
+  L->ctas = (p != nullptr && (p->flags & GRPO_FLAG_SINGLE_CTA) != 0) ? 1 : 2;
+  const int n_dt = static_cast<int>(cdiv(s->hidden, BN * dh_accumulators(L->ctas)));
   long long vb = (p && p->vocab_block > 0) ? p->vocab_block : kAutoVocabBlock;
   vb = cdiv(vb, BN) * BN;
   vb = std::min<long long>(vb, static_cast<long long>(L->nvt) * BN);
@@ -507,6 +511,8 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
       !encode_2d(&map_w_mn, W, L.D, L.V, L.D, 64, BK))
     return GRPO_ERR_CUDA;
   const int n_dt = static_cast<int>(cdiv(L.D, BN));
+  const int n_dt_dh = static_cast<int>(cdiv(L.D, BN * dh_accumulators(L.ctas)));
+  (void)n_dt;
   const int n_rb_total = static_cast<int>(L.nr / BM);
   const int rb_per_chunk = L.chunk_rows / BM;
   for (int rb0 = 0; rb0 < n_rb_total; rb0 += rb_per_chunk) {
@@ -550,13 +556,13 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
       b.n_active = w.n_active;
       b.k_iters = static_cast<int>(cdiv(width, BK));
       b.group_rows = group_rows_for(n_ru, slots);
-      b.n_cols = n_dt;
+      b.n_cols = n_dt_dh;
       b.v0 = static_cast<int>(v0);
       b.acc = w.acc;
       b.dH = static_cast<__nv_bfloat16*>(dH);
       b.first = v0 == 0;
       b.last = v0 + L.vblock >= L.V;
-      units = static_cast<long long>(n_ru) * n_dt;
+      units = static_cast<long long>(n_ru) * n_dt_dh;
       if (launch_dh_gemm(L.ctas, map_g, map_w_mn, b,
                          L.ctas * static_cast<int>(std::min<long long>(units, slots)),
                          st) != cudaSuccess)
@@ -592,7 +598,7 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
   DeviceInfo* di = current_device_info();
   if (di == nullptr) return GRPO_ERR_CUDA;
   const bool overlap = L.n_sbuf == 2;
-  const int n_dt = static_cast<int>(cdiv(L.D, BN));
+  const int n_dt_dh = static_cast<int>(cdiv(L.D, BN * dh_accumulators(L.ctas)));
   const int n_rb_total = static_cast<int>(L.nr / BM);
   const int rb_per_chunk = L.chunk_rows / BM;
   const int n_chunks = static_cast<int>(cdiv(n_rb_total, rb_per_chunk));
@@ -692,12 +698,12 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     b.n_active = w.n_active;
     b.k_iters = static_cast<int>(cdiv(L.V, BK));
     b.group_rows = group_rows_for(n_ru, slots);
-    b.n_cols = n_dt;
+    b.n_cols = n_dt_dh;
     b.v0 = 0;
     b.dH = static_cast<__nv_bfloat16*>(dH);
     b.first = 1;
     b.last = 1;
-    const long long units = static_cast<long long>(n_ru) * n_dt;
+    const long long units = static_cast<long long>(n_ru) * n_dt_dh;
     if (launch_dh_gemm(L.ctas, map_g, map_w_mn, b,
                        L.ctas * static_cast<int>(std::min<long long>(units, slots)),
                        st) != cudaSuccess)

@@ -153,12 +153,21 @@ __device__ __forceinline__ void logit_transform(const TileArgs& a, float (&v)[32
 // a CTA pair computes a 256 x 256 tile with tcgen05 cta_group::2; each CTA
 // loads its own 128 A rows and half of the B tile (128 of its 256 rows/cols),
 // the leader issues the MMAs, and each CTA's TMEM holds its 128 rows.
-template <int CTAS>
+// The pair's dH GEMM runs units of 512 D columns: two 256-column accumulators
+// fill TMEM (no double buffering; its units are whole-vocabulary K loops, so
+// the single epilogue per unit costs ~1 %), and every A tile of G feeds twice
+// the MMA work.
+template <int MODE, int CTAS>
 struct PairCfg {
-  static constexpr int kBRows = BN / CTAS;             // B rows (cols) per CTA
-  static constexpr int kBBytes = kBRows * BK * 2;
+  static constexpr int kNAcc = (MODE == MODE_DH && CTAS == 2) ? 2 : 1;  // accumulators
+  static constexpr int kNBuf = kNAcc == 2 ? 1 : 2;     // TMEM buffers (of kNAcc x 256)
+  static constexpr int kTileN = BN * kNAcc;            // N columns per unit
+  static constexpr int kBRows = BN / CTAS;             // B rows (cols) per CTA and MMA
+  static constexpr int kBBytes = kNAcc * kBRows * BK * 2;
   static constexpr int kStageBytes = A_BYTES + kBBytes;
-  static constexpr int kStages = CTAS == 2 ? 7 : STAGES;
+  static constexpr int kMaxDynSmem = 232448 - 1024 - 1024;  // 227 KB less slack and statics
+  static constexpr int kStages =
+      CTAS == 2 ? (kMaxDynSmem / kStageBytes < 7 ? kMaxDynSmem / kStageBytes : 7) : STAGES;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
 };
 
@@ -181,7 +190,7 @@ template <int MODE, int CTAS>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b, const TileArgs args) {
-  using C = PairCfg<CTAS>;
+  using C = PairCfg<MODE, CTAS>;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
@@ -293,10 +302,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               mbar_arrive_expect_tx_cluster(lead, C::kStageBytes);
               tma_load_2d_pair(a_dst, &map_a, lead, k * BK, a_row, pol_a);
               if (MODE == MODE_DH) {
+                // Per accumulator, this CTA's 128 of its 256 D columns.
+                constexpr int kBoxes = C::kBRows / 64;
 #pragma unroll
-                for (int j = 0; j < C::kBRows / 64; ++j)
+                for (int j = 0; j < C::kNAcc * kBoxes; ++j)
                   tma_load_2d_pair_nohint(b_dst + j * (BK * 64 * 2), &map_b, lead,
-                                          t * BN + static_cast<int>(rank) * C::kBRows + j * 64,
+                                          t * C::kTileN + (j / kBoxes) * BN +
+                                              static_cast<int>(rank) * C::kBRows +
+                                              (j % kBoxes) * 64,
                                           args.v0 + k * BK);
               } else {
                 tma_load_2d_pair_nohint(b_dst, &map_b, lead, k * BK,
@@ -338,8 +351,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         decode_unit(u, n_ru, args.n_cols, args.group_rows, ru, col);
         unit_tiles<MODE>(args, col, t0, t1);
         for (int t = t0; t < t1 && ok; ++t, ++tile_it) {
-          const uint32_t buf = tile_it & 1u;
-          const uint32_t use = tile_it >> 1;
+          const uint32_t buf = tile_it % C::kNBuf;
+          const uint32_t use = tile_it / C::kNBuf;
           if (!mbar_wait(&tempty_bar[buf], (use & 1u) ^ 1u, abort_flag, args.status)) {
             ok = false;
             break;
@@ -372,8 +385,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 bdesc = sdesc_sw128(b_addr + kk * 32, 16, 1024);
               }
               const uint32_t acc = (k | kk) != 0 ? 1u : 0u;
-              if (CTAS == 2) tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, acc);
-              else tc_mma_bf16(d_tmem, adesc, bdesc, idesc, acc);
+#pragma unroll
+              for (int na = 0; na < C::kNAcc; ++na) {
+                // Accumulator na: B columns na*256.. (its own B boxes), TMEM columns na*256..
+                const uint64_t bd = bdesc + ((static_cast<uint64_t>(na) * C::kBRows * BK * 2) >> 4);
+                if (CTAS == 2) tc_mma_bf16_pair(d_tmem + na * BN, adesc, bd, idesc, acc);
+                else tc_mma_bf16(d_tmem + na * BN, adesc, bd, idesc, acc);
+              }
             }
             if (CTAS == 2) tc_commit_pair_multicast(&empty_bar[s], 0x3);
             else tc_commit(&empty_bar[s]);
@@ -425,8 +443,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       }
 
       for (int t = t0; t < t1; ++t, ++tile_it) {
-        const uint32_t buf = tile_it & 1u;
-        const uint32_t use = tile_it >> 1;
+        const uint32_t buf = tile_it % C::kNBuf;
+        const uint32_t use = tile_it / C::kNBuf;
         if (!mbar_wait(&tfull_bar[buf], use & 1u, abort_flag, args.status)) {
           ok = false;
           break;
@@ -583,8 +601,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
         } else {  // MODE_DH
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            const int d0 = t * BN + c * 32;
+          for (int c = 0; c < C::kTileN / 32; ++c) {
+            const int d0 = t * C::kTileN + c * 32;
             if (d0 >= args.hidden) break;  // warp-uniform
             float v[32];
             tmem_ld32(tbase + c * 32, v);

@@ -91,7 +91,7 @@ cudaError_t launch_gemm_variant(const CUtensorMap& map_a, const CUtensorMap& map
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = PairCfg<CTAS>::kSmemBytes;
+  cfg.dynamicSmemBytes = PairCfg<MODE, CTAS>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   if (CTAS == 2) {
@@ -109,7 +109,7 @@ template <int MODE, int CTAS>
 cudaError_t prepare_gemm_variant() {
   return cudaFuncSetAttribute(tc_gemm_kernel<MODE, CTAS>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              PairCfg<CTAS>::kSmemBytes);
+                              PairCfg<MODE, CTAS>::kSmemBytes);
 }
 
 // Each launcher lives in the translation unit that instantiates its kernels;
