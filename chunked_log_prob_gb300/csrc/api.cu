@@ -311,6 +311,11 @@ struct DeviceInfo {
   cudaEvent_t ev_main = nullptr;
   cudaEvent_t ev_fwd[2] = {nullptr, nullptr};
   cudaEvent_t ev_g[2] = {nullptr, nullptr};
+  // Held while one call enqueues its work on the side stream: the events are
+  // shared, and each record must be followed by its own waits before another
+  // call records again (cudaStreamWaitEvent takes the record current at the
+  // time it is enqueued).
+  std::mutex side_mu;
 };
 
 std::mutex g_mu;
@@ -723,6 +728,7 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
       if (r == GRPO_OK) r = dh(c);
     }
   } else {
+    std::lock_guard<std::mutex> side_lock(di->side_mu);
     // The side stream starts after everything already on the caller's stream.
     if (cudaEventRecord(di->ev_main, st) != cudaSuccess ||
         cudaStreamWaitEvent(di->side, di->ev_main, 0) != cudaSuccess)
@@ -746,7 +752,7 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
       if (cudaStreamWaitEvent(st, di->ev_g[c & 1], 0) != cudaSuccess) return GRPO_ERR_CUDA;
       r = dh(c);
     }
-  }
+  }  // side_lock released: this call's records and waits are all enqueued
   if (r != GRPO_OK) return r;
   FinishArgs fin;
   std::memset(&fin, 0, sizeof(fin));

@@ -32,7 +32,11 @@
  *     happen on the host before anything is launched; problems found on the
  *     device (out-of-range token ids, a timed-out wait) are recorded in the
  *     workspace's status word, read back with grpo_read_device_status.
- *   - Two calls that share a workspace must not overlap on the GPU.
+ *   - Two calls that share a workspace must not overlap on the GPU. Calls
+ *     with separate workspaces may run concurrently from several host
+ *     threads; the stored-logit path's side stream (one per device, created
+ *     on first use together with a few events; no device memory) is then
+ *     shared, which orders their row-wise G passes one after another.
  *   - Requires an sm_103 device (GB300).
  */
 #ifndef GRPO_GB300_H_

@@ -460,3 +460,51 @@ def test_lm_head_gradient_with_transform(clp):
             _to(p.adv), p.seq_len, params=params, want_dW=True)
         rel = np.linalg.norm(dW.cpu().double().numpy() - want_dW) / np.linalg.norm(want_dW)
         assert rel <= DH_RTOL, (flags, rel)
+
+
+def test_concurrent_calls_from_two_threads(clp):
+    # Separate workspaces and streams, stored path with several chunks (so the
+    # shared side stream is used): results equal the same calls made serially.
+    import threading
+
+    probs = [synth.make_problem("tiny", seed=90 + i, prompts=2, G=4, T=256, D=256, V=3000,
+                                lengths=(64, 256)) for i in range(2)]
+    params = clp.make_params(chunk_tokens=512, flags=STORED)
+
+    def args_of(p):
+        base, _ = oracle.selective_logp(p.hidden, p.weight, p.ids.numpy())
+        old, ref = p.old_ref(torch.from_numpy(base))
+        return [_to(x) for x in (p.hidden, p.weight, p.ids, p.mask, old, ref, p.adv)]
+
+    inputs = [args_of(p) for p in probs]
+    serial = []
+    for p, a in zip(probs, inputs):
+        loss, logp, dH = clp.grpo_loss_fwd_bwd(*a, p.seq_len, params=params)
+        torch.cuda.synchronize()
+        serial.append((loss.clone(), logp.clone(), dH.clone()))
+
+    out = [None, None]
+    errors = []
+
+    def worker(i):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                ws = clp.alloc_workspace(probs[i].n_tokens, 256, 3000, probs[i].seq_len, params,
+                                         DEV)
+                for _ in range(3):
+                    r = clp.grpo_loss_fwd_bwd(*inputs[i], probs[i].seq_len, params=params,
+                                              workspace=ws)
+                s.synchronize()
+                out[i] = r
+        except Exception as e:  # surfaced below
+            errors.append(e)
+
+    th = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    assert not errors
+    for (l0, lp0, d0), (l1, lp1, d1) in zip(serial, out):
+        assert torch.equal(l0, l1) and torch.equal(lp0, lp1) and torch.equal(d0, d1)
