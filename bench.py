@@ -438,6 +438,8 @@ def run_ours(args):
         "tflops_executed": tflops_exec,
         "pct_bf16_peak": 100.0 * tflops_exec / peak_sus,
         "backward": ("stored fp16 logits" if stored else "recomputed logits") + (
+            ", G formed inside the dH GEMM" if stored and plan["g_in_dh_gemm"]
+            and not args.with_dw else ", G formed in its own pass" if stored else "") + (
             " + lm_head dW" if args.with_dw else ""),
         "variant": variant,
         "roofline": {

@@ -44,7 +44,7 @@ class GrpoPlanInfo(ctypes.Structure):
     _fields_ = [("chunk_rows", ctypes.c_int32), ("vocab_block", ctypes.c_int32),
                 ("n_chunks", ctypes.c_int32), ("n_vocab_blocks", ctypes.c_int32),
                 ("fwd_splits", ctypes.c_int32), ("launches_logp", ctypes.c_int32),
-                ("launches_loss", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("launches_loss", ctypes.c_int32), ("g_in_dh_gemm", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_uint64)]
 
 

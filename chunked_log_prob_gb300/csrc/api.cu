@@ -20,6 +20,14 @@ constexpr int kMaxAutoChunkBlocks = 32;  // automatic backward chunk <= 4096 row
 constexpr int kAutoVocabBlock = 32768;   // automatic backward vocab block
 constexpr int kMaxStoredChunkBlocks = 64;                   // stored-logit chunk bound
 constexpr size_t kMaxStoredChunkBytes = size_t(2) << 30;    // 2 GiB of fp16 logits
+// Hidden sizes up to which the stored-logit backward forms G inside the dH
+// GEMM (MODE_DHS) rather than in a pass of its own over the logit block.
+// Measured on GB300: the separate pass costs about 1/D of the dH GEMM and
+// mostly hides behind the next chunk's GEMMs; the in-GEMM conversion costs a
+// roughly constant share of the dH GEMM (its shared-memory traffic competes
+// with the CTA-pair MMA operand reads). At D = 1536 fusing is 7-12 % faster
+// per call, at D = 2880 and 4096 the overlapped separate pass is faster.
+constexpr int kFusedMaxHidden = 2048;
 constexpr int kSplitsTarget = 8;        // forward vocab splits per raster group
 constexpr size_t kHeaderBytes = 16384;   // status, counters, loss partials
 constexpr int kMaxDevices = 64;
@@ -48,6 +56,8 @@ struct Layout {
   int nvt;          // vocab tiles
   int chunk_rows;   // backward chunk (multiple of BM)
   int n_sbuf;       // stored path: logit blocks (2 = double-buffered chunks)
+  bool fused;       // stored path, D <= kFusedMaxHidden: G formed inside the dH
+                    // GEMM, one logit block (the dW variant then runs unoverlapped)
   int vblock;       // backward vocab block (multiple of BN)
   bool need_acc;    // more than one vocab block -> fp32 dH accumulator
   size_t off_pm, off_ps, off_zy, off_lse, off_g, off_rbl, off_lt, off_seq, off_G, off_acc, total;
@@ -72,10 +82,13 @@ int auto_chunk_blocks(long long n_rb_total, int n_dt, int sms, int max_units) {
 }
 
 // Stored-logit backward: largest chunk (row blocks) whose fp16 logit block
-// stays within kMaxStoredChunkBytes.
-int stored_max_blocks(long long ldS) {
-  const long long by_mem = static_cast<long long>(kMaxStoredChunkBytes / (BM * ldS * 2));
-  return static_cast<int>(std::max(1LL, std::min<long long>(kMaxStoredChunkBlocks, by_mem)));
+// stays within kMaxStoredChunkBytes (twice that when there is only one block).
+int stored_max_blocks(long long ldS, int n_sbuf) {
+  // One block may take the room (and the row bound) of two.
+  const int f = n_sbuf == 1 ? 2 : 1;
+  const long long by_mem = static_cast<long long>(f * kMaxStoredChunkBytes / (BM * ldS * 2));
+  return static_cast<int>(
+      std::max(1LL, std::min<long long>(f * kMaxStoredChunkBlocks, by_mem)));
 }
 
 // Fraction of SM time a launch of `units` equal units keeps busy.
@@ -163,6 +176,7 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   vb = std::min<long long>(vb, static_cast<long long>(L->nvt) * BN);
   L->vblock = L->stored ? static_cast<int>(L->ldS) : static_cast<int>(vb);
   L->need_acc = !L->stored && L->vblock < L->V;
+  L->fused = L->stored && L->D <= kFusedMaxHidden;
 
   // Everything before the backward chunk block depends on N only.
   size_t off = kHeaderBytes;
@@ -184,11 +198,13 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   // Bytes of the chunk block per row unit: bf16 G (+ fp32 dH accumulator) or
   // fp16 logits.
   // The stored path keeps two chunk blocks when there is more than one chunk
-  // (one being turned into G while the next chunk's logits are computed).
+  // (one being turned into G while the next chunk's logits are computed),
+  // one when the dH GEMM forms G itself.
+  const int sbufs = L->stored && !L->fused ? 2 : 1;
   const size_t unit_bytes = static_cast<size_t>(ru_rows) *
-                            (static_cast<size_t>(L->vblock) * 2 * (L->stored ? 2 : 1) +
+                            (static_cast<size_t>(L->vblock) * 2 * sbufs +
                              (L->need_acc ? L->D * 4 : 0));
-  long long max_units = L->stored ? std::max(1, stored_max_blocks(L->ldS) / L->ctas)
+  long long max_units = L->stored ? std::max(1, stored_max_blocks(L->ldS, sbufs) / L->ctas)
                                   : kMaxAutoChunkBlocks / L->ctas;
   const size_t budget = workspace_budget(p);
   if (budget > 0) {
@@ -213,7 +229,7 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   crows = std::min(crows, n_ru_total * ru_rows);
   if (crows > INT_MAX / 2) return GRPO_ERR_UNSUPPORTED_SHAPE;
   L->chunk_rows = static_cast<int>(crows);
-  L->n_sbuf = (L->stored && cdiv(L->nr, L->chunk_rows) > 1) ? 2 : 1;
+  L->n_sbuf = (sbufs == 2 && cdiv(L->nr, L->chunk_rows) > 1) ? 2 : 1;
 
   // Backward chunk block: bf16 G [C x V_b] (recompute path) or the chunk's
   // fp16 logits, rewritten in place as bf16 G [C x ldS] (stored path; two of
@@ -515,9 +531,7 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
       !encode_2d(&map_w_k, W, L.D, L.V, L.D, BK, BN / L.ctas) ||
       !encode_2d(&map_w_mn, W, L.D, L.V, L.D, 64, BK))
     return GRPO_ERR_CUDA;
-  const int n_dt = static_cast<int>(cdiv(L.D, BN));
   const int n_dt_dh = static_cast<int>(cdiv(L.D, BN * dh_accumulators(L.ctas)));
-  (void)n_dt;
   const int n_rb_total = static_cast<int>(L.nr / BM);
   const int rb_per_chunk = L.chunk_rows / BM;
   for (int rb0 = 0; rb0 < n_rb_total; rb0 += rb_per_chunk) {
@@ -646,8 +660,8 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
                ? GRPO_OK
                : GRPO_ERR_CUDA;
   };
-  // (2) per-row finish of chunk c; its block becomes G.
-  auto gform = [&](int c, int splits, cudaStream_t s2) -> int {
+  // (2) per-row finish of chunk c: lse, logp, token loss and g.
+  auto row_args = [&](int c, int splits) -> GformArgs {
     const int n_rb = chunk_rbs(c);
     GformArgs f;
     std::memset(&f, 0, sizeof(f));
@@ -686,7 +700,22 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     f.k0 = t.k0;
     f.k2 = t.k2;
     f.status = w.status;
-    return launch_finalize_gform(f, n_rb * BM, s2) == cudaSuccess ? GRPO_OK : GRPO_ERR_CUDA;
+    f.lse_out = w.lse;
+    f.g_out = w.g;
+    return f;
+  };
+  // (2a) ... and its logit block rewritten in place as G (hidden sizes above
+  // kFusedMaxHidden, and dW, which reads G too).
+  auto gform = [&](int c, int splits, cudaStream_t s2) -> int {
+    return launch_finalize_gform(row_args(c, splits), chunk_rbs(c) * BM, s2) == cudaSuccess
+               ? GRPO_OK
+               : GRPO_ERR_CUDA;
+  };
+  // (2b) ... or the row values alone, for the dH GEMM that forms G itself.
+  auto rowfin = [&](int c, int splits) -> int {
+    return launch_finalize_rows(row_args(c, splits), chunk_rbs(c) * BM, st) == cudaSuccess
+               ? GRPO_OK
+               : GRPO_ERR_CUDA;
   };
   // (3) dH rows of chunk c = G W over the whole vocabulary; (4) dW.
   auto dh = [&](int c) -> int {
@@ -719,8 +748,51 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     return GRPO_OK;
   };
 
+  // (3') dH rows of chunk c straight from its stored logits: the GEMM's
+  // epilogue warps turn each landed A stage into G in shared memory.
+  auto dhs = [&](int c) -> int {
+    const int n_rb = chunk_rbs(c);
+    const int n_ru = static_cast<int>(cdiv(n_rb, L.ctas));
+    CUtensorMap map_s;
+    if (!encode_2d(&map_s, sbuf(c), L.V, static_cast<uint64_t>(n_rb) * BM, L.ldS, BK, BM))
+      return GRPO_ERR_CUDA;
+    TileArgs b = base_args(L, w);
+    set_transform(&b, prm);
+    b.n_total = L.n;
+    b.n_rb = n_rb;
+    b.rb_offset = c * rb_per_chunk;
+    b.rb_list = w.rb_list;
+    b.n_active = w.n_active;
+    b.k_iters = static_cast<int>(cdiv(L.V, BK));
+    b.group_rows = group_rows_for(n_ru, slots);
+    b.n_cols = n_dt_dh;
+    b.v0 = 0;
+    b.ids = ids;
+    b.lse = w.lse;
+    b.g = w.g;
+    b.zy = w.zy;
+    b.dH = static_cast<__nv_bfloat16*>(dH);
+    b.first = 1;
+    b.last = 1;
+    const long long units = static_cast<long long>(n_ru) * n_dt_dh;
+    return launch_dhs_gemm(L.ctas, map_s, map_w_mn, b,
+                           L.ctas * static_cast<int>(std::min<long long>(units, slots)),
+                           st) == cudaSuccess
+               ? GRPO_OK
+               : GRPO_ERR_CUDA;
+  };
+
   int r = GRPO_OK;
-  if (!overlap) {
+  if (dW == nullptr && L.fused) {
+    // G never materialises: logits, row values, dH, chunk after chunk on the
+    // caller's stream.
+    for (int c = 0; c < n_chunks && r == GRPO_OK; ++c) {
+      int splits = 1;
+      r = fwds(c, &splits);
+      if (r == GRPO_OK) r = rowfin(c, splits);
+      if (r == GRPO_OK) r = dhs(c);
+    }
+  } else if (!overlap) {
     for (int c = 0; c < n_chunks && r == GRPO_OK; ++c) {
       int splits = 1;
       r = fwds(c, &splits);
@@ -952,6 +1024,7 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
     info->fwd_splits =
         stored_fwd_splits(L.chunk_rows / (BM * L.ctas), L.nvt, slots, nullptr);
   }
+  info->g_in_dh_gemm = L.fused ? 1 : 0;
   info->workspace_bytes = std::max(L.total, Lmax.total);
   return GRPO_OK;
 }

@@ -1,6 +1,7 @@
 // Backward-side GEMM launchers: the G tile (recomputed logits -> bf16
-// softmax-Jacobian rows) and the dH accumulation, each in the single-CTA and
-// the CTA-pair variant.
+// softmax-Jacobian rows), the dH accumulation from a G block or straight
+// from a stored fp16 logit block, and the lm_head gradient, each in the
+// single-CTA and the CTA-pair variant.
 #include "launch.h"
 
 namespace grpo {
@@ -12,6 +13,8 @@ cudaError_t prepare_bwd_gemms() {
   if (e == cudaSuccess) e = prepare_gemm_variant<MODE_DH, 2>();
   if (e == cudaSuccess) e = prepare_gemm_variant<MODE_DW, 1>();
   if (e == cudaSuccess) e = prepare_gemm_variant<MODE_DW, 2>();
+  if (e == cudaSuccess) e = prepare_gemm_variant<MODE_DHS, 1>();
+  if (e == cudaSuccess) e = prepare_gemm_variant<MODE_DHS, 2>();
   return e;
 }
 
@@ -31,6 +34,12 @@ cudaError_t launch_dh_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap
                            const TileArgs& args, int grid, cudaStream_t stream) {
   return ctas == 2 ? launch_gemm_variant<MODE_DH, 2>(map_a, map_b, args, grid, stream)
                    : launch_gemm_variant<MODE_DH, 1>(map_a, map_b, args, grid, stream);
+}
+
+cudaError_t launch_dhs_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                            const TileArgs& args, int grid, cudaStream_t stream) {
+  return ctas == 2 ? launch_gemm_variant<MODE_DHS, 2>(map_a, map_b, args, grid, stream)
+                   : launch_gemm_variant<MODE_DHS, 1>(map_a, map_b, args, grid, stream);
 }
 
 }  // namespace grpo

@@ -294,54 +294,71 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t h16) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h16)));
 }
 
+// Per-row finish of a stored-logit chunk: combines the forward's split
+// partials into lse, writes logp and the weighted token loss, and returns
+// g = dL/dlogp (0 for rows that do not count), lse and the target id (-1 when
+// the row does not count or its id is out of range).
+__device__ __forceinline__ void finish_row(const GformArgs& a, long long grow, float& lse,
+                                           float& g, int& y) {
+  g = 0.f;
+  lse = 0.f;
+  y = -1;
+  const bool counted = grow < a.n_total && (a.mask == nullptr || a.mask[grow] != 0);
+  if (!counted) return;
+  float m2 = -INFINITY;
+  for (int s = 0; s < a.splits; ++s) m2 = fmaxf(m2, a.part_m[s * a.part_ld + grow]);
+  float ssum = 0.f;
+  for (int s = 0; s < a.splits; ++s)
+    ssum += a.part_s[s * a.part_ld + grow] * exp2f(a.part_m[s * a.part_ld + grow] - m2);
+  lse = (m2 + log2f(ssum)) * 0.69314718055994531f;
+  y = a.ids[grow];
+  float logp;
+  if (y < 0 || y >= a.vocab) {
+    atomicCAS(a.status, 0, GRPO_ERR_BAD_TOKEN_ID);
+    logp = __int_as_float(0x7fc00000);
+    y = -1;
+  } else {
+    logp = a.zy[grow] - lse;
+  }
+  const double wt = token_weight(a.seq_mode, a.loss_den, a.msum, a.seq_lens, a.n_nonempty,
+                                 grow, a.seq_len);
+  const double lp = logp;
+  const double A = a.adv[grow / a.seq_len];
+  const double r = exp(lp - static_cast<double>(a.old_logp[grow]));
+  const double lo = 1.0 - static_cast<double>(a.eps_low);
+  const double hi = 1.0 + static_cast<double>(a.eps_high);
+  const double c = fmin(fmax(r, lo), hi);
+  const double surr = fmin(r * A, c * A);
+  const double d = static_cast<double>(a.ref_logp[grow]) - lp;
+  const double ed = exp(d);
+  a.lt[grow] = (-surr + static_cast<double>(a.beta) * (ed - d - 1.0)) * wt;
+  const bool clipped = (A > 0.0 && r > hi) || (A < 0.0 && r < lo);
+  const double dl = -(clipped ? 0.0 : A * r) + static_cast<double>(a.beta) * (1.0 - ed);
+  g = static_cast<float>(dl * wt);
+  if (a.logp_out) a.logp_out[grow] = logp;
+}
+
+// Global row of local row `lrow` of the chunk, or -1 past the active list.
+__device__ __forceinline__ long long chunk_row(const GformArgs& a, int lrow) {
+  const int li = lrow / BM;
+  int n_rb = a.n_rb;
+  if (a.n_active != nullptr) n_rb = max(0, min(a.n_rb, *a.n_active - a.rb_offset));
+  if (li >= n_rb) return -1;
+  const int rb = a.rb_list != nullptr ? a.rb_list[a.rb_offset + li] : a.rb_offset + li;
+  return static_cast<long long>(rb) * BM + (lrow - li * BM);
+}
+
 __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const GformArgs a) {
   __shared__ float sh_lse2, sh_g;
   __shared__ int sh_y;
   const int lrow = blockIdx.x;
-  const int li = lrow / BM;
-  int n_rb = a.n_rb;
-  if (a.n_active != nullptr) n_rb = max(0, min(a.n_rb, *a.n_active - a.rb_offset));
-  if (li >= n_rb) return;  // whole block: uniform
-  const int rb = a.rb_list != nullptr ? a.rb_list[a.rb_offset + li] : a.rb_offset + li;
-  const long long grow = static_cast<long long>(rb) * BM + (lrow - li * BM);
+  const long long grow = chunk_row(a, lrow);
+  if (grow < 0) return;  // whole block: uniform
 
   if (threadIdx.x == 0) {
-    float g = 0.f, lse = 0.f;
-    int y = -1;
-    const bool counted = grow < a.n_total && (a.mask == nullptr || a.mask[grow] != 0);
-    if (counted) {
-      float m2 = -INFINITY;
-      for (int s = 0; s < a.splits; ++s) m2 = fmaxf(m2, a.part_m[s * a.part_ld + grow]);
-      float ssum = 0.f;
-      for (int s = 0; s < a.splits; ++s)
-        ssum += a.part_s[s * a.part_ld + grow] * exp2f(a.part_m[s * a.part_ld + grow] - m2);
-      lse = (m2 + log2f(ssum)) * 0.69314718055994531f;
-      y = a.ids[grow];
-      float logp;
-      if (y < 0 || y >= a.vocab) {
-        atomicCAS(a.status, 0, GRPO_ERR_BAD_TOKEN_ID);
-        logp = __int_as_float(0x7fc00000);
-        y = -1;
-      } else {
-        logp = a.zy[grow] - lse;
-      }
-      const double wt = token_weight(a.seq_mode, a.loss_den, a.msum, a.seq_lens, a.n_nonempty,
-                                     grow, a.seq_len);
-      const double lp = logp;
-      const double A = a.adv[grow / a.seq_len];
-      const double r = exp(lp - static_cast<double>(a.old_logp[grow]));
-      const double lo = 1.0 - static_cast<double>(a.eps_low);
-      const double hi = 1.0 + static_cast<double>(a.eps_high);
-      const double c = fmin(fmax(r, lo), hi);
-      const double surr = fmin(r * A, c * A);
-      const double d = static_cast<double>(a.ref_logp[grow]) - lp;
-      const double ed = exp(d);
-      a.lt[grow] = (-surr + static_cast<double>(a.beta) * (ed - d - 1.0)) * wt;
-      const bool clipped = (A > 0.0 && r > hi) || (A < 0.0 && r < lo);
-      const double dl = -(clipped ? 0.0 : A * r) + static_cast<double>(a.beta) * (1.0 - ed);
-      g = static_cast<float>(dl * wt);
-      if (a.logp_out) a.logp_out[grow] = logp;
-    }
+    float lse, g;
+    int y;
+    finish_row(a, grow, lse, g, y);
     sh_lse2 = lse * kLog2e;
     sh_g = g;
     sh_y = y;
@@ -433,6 +450,28 @@ __global__ void __launch_bounds__(kFinalizeThreads) finish_loss_kernel(const Fin
 cudaError_t launch_finalize_gform(const GformArgs& a, int rows, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
   finalize_gform_kernel<<<rows, kGformThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// The row values alone (one thread per row of the chunk), for the dH GEMM
+// that turns the stored logits into G itself.
+__global__ void __launch_bounds__(kFinalizeThreads) finalize_rows_kernel(const GformArgs a,
+                                                                         int rows) {
+  const int lrow = blockIdx.x * blockDim.x + threadIdx.x;
+  if (lrow >= rows) return;
+  const long long grow = chunk_row(a, lrow);
+  if (grow < 0) return;
+  float lse, g;
+  int y;
+  finish_row(a, grow, lse, g, y);
+  a.lse_out[grow] = lse;
+  a.g_out[grow] = g;
+}
+
+cudaError_t launch_finalize_rows(const GformArgs& a, int rows, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  finalize_rows_kernel<<<(rows + kFinalizeThreads - 1) / kFinalizeThreads, kFinalizeThreads, 0,
+                         stream>>>(a, rows);
   return cudaGetLastError();
 }
 

@@ -1,8 +1,9 @@
-// Persistent, warp-specialised tcgen05 GEMM for sm_103a with three fused
-// epilogues. One CTA per SM, 192 threads:
-//   warp 0      TMA producer (one elected thread) filling a 4-stage smem ring
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a with fused
+// epilogues. One CTA per SM, 192 threads (320 for MODE_DHS):
+//   warp 0      TMA producer (one elected thread) filling the smem stage ring
 //   warp 1      TMEM allocator + MMA issuer (one elected thread)
 //   warps 2..5  epilogue: 128 threads <-> the 128 TMEM lanes (= tile rows)
+//   warps 6..9  MODE_DHS only: converter warps (the second half of each row)
 // The fp32 accumulator lives in TMEM, double buffered (2 x 256 columns), so
 // the epilogue of tile j overlaps the MMAs of tile j+1.
 //
@@ -20,6 +21,11 @@
 //   MODE_FWDS  MODE_FWD over the rows of one backward chunk that also stores
 //              the (transformed) logits in fp16 to the chunk workspace, for a
 //              backward that needs no second logit GEMM.
+//   MODE_DHS   MODE_DH whose A operand is that stored fp16 logit block: the
+//              epilogue warps, idle during the long vocabulary K loop, and four
+//              converter-only warps rewrite each landed A stage in place as
+//              bf16 G (the softmax-Jacobian row, scaled by dL/dlogp) before the
+//              MMA reads it, so G never goes through HBM.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -31,18 +37,17 @@ namespace grpo {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int STAGES = 4;                 // pipeline depth of the single-CTA kernels
+constexpr int A_BYTES = BM * BK * 2;      // 16 KB
 constexpr int GEMM_THREADS = 192;
-constexpr int GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment slack
 constexpr int TMEM_COLS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
-enum GemmMode { MODE_FWD = 0, MODE_BWDG = 1, MODE_DH = 2, MODE_FWDS = 3, MODE_DW = 4 };
+enum GemmMode { MODE_FWD = 0, MODE_BWDG = 1, MODE_DH = 2, MODE_FWDS = 3, MODE_DW = 4,
+                MODE_DHS = 5 };
 
 __host__ __device__ constexpr bool is_fwd(int mode) { return mode == MODE_FWD || mode == MODE_FWDS; }
+__host__ __device__ constexpr bool is_dh(int mode) { return mode == MODE_DH || mode == MODE_DHS; }
 
 struct TileArgs {
   long long n_total;     // N: rows of hidden / dH; global rows >= N are padding
@@ -69,7 +74,7 @@ struct TileArgs {
   float* part_s;         // [n_cols][part_ld] running sum of 2^(x - max)
   float* zy;             // [N] target logit, indexed by global row
   long long part_ld;
-  // MODE_BWDG
+  // MODE_BWDG, MODE_DHS
   const float* lse;      // indexed by global row
   const float* g;        // indexed by global row
   __nv_bfloat16* G;      // [local rows][ldG] chunk workspace
@@ -80,7 +85,7 @@ struct TileArgs {
   // MODE_DW
   float* dW;             // [V][hidden] fp32 output / accumulator
   int dw_rows;           // vocab rows of dW this launch covers (from v0)
-  // MODE_DH
+  // MODE_DH, MODE_DHS
   float* acc;            // [local rows][hidden] fp32 accumulator
   __nv_bfloat16* dH;     // [N][hidden] output, indexed by global row
   int first;
@@ -149,6 +154,90 @@ __device__ __forceinline__ void logit_transform(const TileArgs& a, float (&v)[32
   }
 }
 
+// f'(S) recovered from the transformed logit z' (1 without a transform).
+__device__ __forceinline__ float dz_of_logit(const TileArgs& a, float z) {
+  if (a.xmode == 1) return a.k0;
+  if (a.xmode == 2) {
+    const float u = z / a.k2;
+    return a.k0 * fmaf(-u, u, 1.f);
+  }
+  return 1.f;
+}
+
+// Byte offset of stage column c (0..63) of row r in a 128B-swizzled A stage:
+// 16-byte chunk j of row r sits at chunk j ^ (r & 7).
+__device__ __forceinline__ int swz_offset(int r, int c) {
+  return r * 128 + ((((c >> 3) ^ r) & 7) << 4) + (c & 7) * 2;
+}
+
+// MODE_DHS: rewrites chunks jb..jb+NCH-1 (8 columns each) of row r of a
+// landed A stage (64 fp16 logits z' of vocab columns vbase..) in place as the
+// bf16 G values,
+//   G_v = g (onehot_v(y) - 2^(z'_v log2e - lse2)) f'(S_v).
+// Rows with g = 0 (masked, padding, past N) become zeros whatever the buffer
+// held; columns at or past the vocabulary size become zeros. The main loop
+// runs over logical chunks, so the 8 lanes of a shared-memory phase (8
+// consecutive rows, same chunk) touch 8 different physical chunks: no bank
+// conflicts. The target column (at most once per row and unit) and the
+// vocabulary edge (the last stage) are fixed up afterwards, off the hot path;
+// the target uses the fp32 z'_y the logit GEMM recorded.
+template <int NCH>
+__device__ __forceinline__ void logits_to_g_row(const TileArgs& a, uint8_t* tile, int r, int jb,
+                                                int vbase, int y, float g, float lse2,
+                                                float zy) {
+  uint4* row = reinterpret_cast<uint4*>(tile + r * 128);
+  const int sw = r & 7;
+  if (g == 0.f) {
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) row[(jb + j) ^ sw] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  const float ng = -g;
+  if (a.xmode == 0) {
+    uint4 in[NCH];
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) in[j] = row[(jb + j) ^ sw];
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const uint32_t w[4] = {in[j].x, in[j].y, in[j].z, in[j].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float z0, z1;
+        unpack_f16x2(w[e], z0, z1);
+        o[e] = pack_bf16x2(ng * ex2(fmaf(z0, kLog2e, -lse2)), ng * ex2(fmaf(z1, kLog2e, -lse2)));
+      }
+      row[(jb + j) ^ sw] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  } else {
+#pragma unroll 1
+    for (int j = jb; j < jb + NCH; ++j) {
+      const uint4 x = row[j ^ sw];
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float z0, z1;
+        unpack_f16x2(w[e], z0, z1);
+        o[e] = pack_bf16x2(ng * ex2(fmaf(z0, kLog2e, -lse2)) * dz_of_logit(a, z0),
+                           ng * ex2(fmaf(z1, kLog2e, -lse2)) * dz_of_logit(a, z1));
+      }
+      row[j ^ sw] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+  const unsigned yoff = static_cast<unsigned>(y - vbase - jb * 8);
+  if (yoff < static_cast<unsigned>(NCH * 8) && y < a.vocab) {
+    const float val = (ng * ex2(fmaf(zy, kLog2e, -lse2)) + g) * dz_of_logit(a, zy);
+    *reinterpret_cast<uint16_t*>(tile + swz_offset(r, jb * 8 + static_cast<int>(yoff))) =
+        static_cast<uint16_t>(pack_bf16x2(val, 0.f) & 0xffffu);
+  }
+  if (vbase + (jb + NCH) * 8 > a.vocab) {
+#pragma unroll 1
+    for (int c = max(jb * 8, a.vocab - vbase); c < (jb + NCH) * 8; ++c)
+      *reinterpret_cast<uint16_t*>(tile + swz_offset(r, c)) = 0;
+  }
+}
+
 // Per-variant geometry. CTAS = 1: one CTA computes a 128 x 256 tile. CTAS = 2:
 // a CTA pair computes a 256 x 256 tile with tcgen05 cta_group::2; each CTA
 // loads its own 128 A rows and half of the B tile (128 of its 256 rows/cols),
@@ -159,7 +248,7 @@ __device__ __forceinline__ void logit_transform(const TileArgs& a, float (&v)[32
 // the MMA work.
 template <int MODE, int CTAS>
 struct PairCfg {
-  static constexpr int kNAcc = (MODE == MODE_DH && CTAS == 2) ? 2 : 1;  // accumulators
+  static constexpr int kNAcc = (is_dh(MODE) && CTAS == 2) ? 2 : 1;  // accumulators
   static constexpr int kNBuf = kNAcc == 2 ? 1 : 2;     // TMEM buffers (of kNAcc x 256)
   static constexpr int kTileN = BN * kNAcc;            // N columns per unit
   static constexpr int kBRows = BN / CTAS;             // B rows (cols) per CTA and MMA
@@ -169,6 +258,10 @@ struct PairCfg {
   static constexpr int kStages =
       CTAS == 2 ? (kMaxDynSmem / kStageBytes < 7 ? kMaxDynSmem / kStageBytes : 7) : STAGES;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+  // Warp groups that convert A stages (MODE_DHS): the epilogue warps and a
+  // second group of converter-only warps, each group half of every row.
+  static constexpr int kCvtGroups = MODE == MODE_DHS ? 2 : 1;
+  static constexpr int kThreads = 64 + 128 * kCvtGroups;
 };
 
 // One TMA box into this CTA's stage; its bytes are counted on the leader's
@@ -187,7 +280,7 @@ __device__ __forceinline__ void load_box(void* dst, const CUtensorMap* map, uint
 }
 
 template <int MODE, int CTAS>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b, const TileArgs args) {
   using C = PairCfg<MODE, CTAS>;
@@ -198,6 +291,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   __shared__ __align__(8) uint64_t tfull_bar[2];
   __shared__ __align__(8) uint64_t tempty_bar[2];
   __shared__ __align__(8) uint64_t drain_bar;
+  // MODE_DHS: this CTA's A stage has landed (its own barrier); the stage has
+  // been converted to G by the pair's epilogue warps (the leader's barrier).
+  __shared__ __align__(8) uint64_t afull_bar[MODE == MODE_DHS ? kStages : 1];
+  __shared__ __align__(8) uint64_t cvt_bar[MODE == MODE_DHS ? kStages : 1];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -223,6 +320,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       mbar_init(&tempty_bar[b], 4 * CTAS);  // every epilogue warp of the pair
     }
     mbar_init(&drain_bar, 1);
+    if constexpr (MODE == MODE_DHS) {
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(&afull_bar[s], 1);
+        mbar_init(&cvt_bar[s], 4 * C::kCvtGroups * CTAS);  // every converter warp of the pair
+      }
+    }
     abort_sh = 0;
     fence_mbar_init();
   }
@@ -267,7 +370,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         int li = ru * CTAS + static_cast<int>(rank);
         if (li >= n_rb) li = ru * CTAS;
         const int a_row =
-            MODE == MODE_DW ? 0 : (MODE == MODE_DH ? li : global_rb(args, li)) * BM;
+            MODE == MODE_DW ? 0 : (is_dh(MODE) ? li : global_rb(args, li)) * BM;
         const int a_m0 = (ru * CTAS + static_cast<int>(rank)) * BM;  // MODE_DW: vocab row
         for (int t = t0; t < t1 && ok; ++t) {
           for (int k = 0; k < k_iters; ++k, ++it) {
@@ -279,7 +382,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             uint8_t* a_dst = smem + s * C::kStageBytes;
             uint8_t* b_dst = a_dst + A_BYTES;
-            if (MODE == MODE_DW) {
+            if constexpr (MODE == MODE_DHS) {
+              // A (the stored fp16 logits) into this CTA's stage, counted on
+              // its own barrier: the epilogue warps turn it into G in place.
+              mbar_arrive_expect_tx(&afull_bar[s], A_BYTES);
+              tma_load_2d_hint(a_dst, &map_a, &afull_bar[s], k * BK, a_row, pol_a);
+              // B (W, MN-major): per accumulator, this CTA's kBRows of its 256
+              // D columns, counted on the leader's barrier (pair) or its own.
+              constexpr int kBoxes = C::kBRows / 64;
+              const uint32_t lead = CTAS == 2 ? mapa_shared(smem_u32(&full_bar[s]), 0) : 0u;
+              if (CTAS == 2) mbar_arrive_expect_tx_cluster(lead, C::kBBytes);
+              else mbar_arrive_expect_tx(&full_bar[s], C::kBBytes);
+#pragma unroll
+              for (int j = 0; j < C::kNAcc * kBoxes; ++j)
+                load_box<CTAS>(b_dst + j * (BK * 64 * 2), &map_b, &full_bar[s], lead,
+                               t * C::kTileN + (j / kBoxes) * BN +
+                                   static_cast<int>(rank) * C::kBRows + (j % kBoxes) * 64,
+                               args.v0 + k * BK, false, 0);
+            } else if (MODE == MODE_DW) {
               const uint32_t lead = CTAS == 2 ? mapa_shared(smem_u32(&full_bar[s]), 0) : 0u;
               if (CTAS == 2) mbar_arrive_expect_tx_cluster(lead, C::kStageBytes);
               else mbar_arrive_expect_tx(&full_bar[s], C::kStageBytes);
@@ -331,19 +451,23 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
         }
       }
-      if (!ok && rank == 0) {
+      if (!ok) {
         // Abort path: let the copies already issued land before the CTA exits
         // (the leader's barriers count the pair's copies; the peer passes the
-        // closing cluster barrier only after this).
-        for (uint32_t j = (it >= kStages ? it - kStages : 0); j < it; ++j)
-          drain_wait(&full_bar[j % kStages], (j / kStages) & 1u);
+        // closing cluster barrier only after this). MODE_DHS counts each
+        // CTA's A copies on its own barriers.
+        for (uint32_t j = (it >= kStages ? it - kStages : 0); j < it; ++j) {
+          if (rank == 0) drain_wait(&full_bar[j % kStages], (j / kStages) & 1u);
+          if constexpr (MODE == MODE_DHS)
+            drain_wait(&afull_bar[j % kStages], (j / kStages) & 1u);
+        }
       }
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer --
     if (lane == 0 && rank == 0) {
       constexpr uint32_t idesc =
-          idesc_bf16(BM * CTAS, BN, MODE == MODE_DW, MODE == MODE_DH || MODE == MODE_DW);
+          idesc_bf16(BM * CTAS, BN, MODE == MODE_DW, is_dh(MODE) || MODE == MODE_DW);
       uint32_t it = 0, tile_it = 0;
       bool ok = true;
       for (int u = cta_slot; u < n_units && ok; u += n_slots) {
@@ -366,6 +490,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               ok = false;
               break;
             }
+            if constexpr (MODE == MODE_DHS) {
+              if (!mbar_wait(&cvt_bar[s], round & 1u, abort_flag, args.status)) {
+                ok = false;
+                break;
+              }
+            }
             tc_fence_after();
             const uint32_t a_addr = smem_u32(smem + s * C::kStageBytes);
             const uint32_t b_addr = a_addr + A_BYTES;
@@ -377,7 +507,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                          ? sdesc_sw128(a_addr + kk * 2048, BK * 64 * 2, 1024)
                                          : sdesc_sw128(a_addr + kk * 32, 16, 1024);
               uint64_t bdesc;
-              if (MODE == MODE_DH || MODE == MODE_DW) {
+              if (is_dh(MODE) || MODE == MODE_DW) {
                 // MN-major, 128B swizzle: 64-wide N blocks 8 KB apart (LBO),
                 // 8-deep K groups 1 KB apart (SBO); K advances 16 rows.
                 bdesc = sdesc_sw128(b_addr + kk * 2048, BK * 64 * 2, 1024);
@@ -410,6 +540,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // ---------------------------------------------------------- epilogue --
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int lrow_in_tile = q * 32 + lane;
+    const int part = (warp - 2) >> 2;  // 0: epilogue warps; 1: converter-only (MODE_DHS)
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     uint32_t tile_it = 0;
     bool ok = true;
@@ -417,6 +548,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // leader's barrier (pair) or the CTA's own.
     const uint32_t tempty_addr0 =
         CTAS == 2 ? mapa_shared(smem_u32(&tempty_bar[0]), 0) : smem_u32(&tempty_bar[0]);
+    const uint32_t cvt_addr0 =
+        CTAS == 2 ? mapa_shared(smem_u32(&cvt_bar[0]), 0) : smem_u32(&cvt_bar[0]);
+    uint32_t cit = 0;  // MODE_DHS: A stages converted so far
     for (int u = cta_slot; u < n_units && ok; u += n_slots) {
       int ru, col, t0, t1;
       decode_unit(u, n_ru, args.n_cols, args.group_rows, ru, col);
@@ -431,15 +565,42 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       // Per-row state.
       float m2 = -INFINITY, ssum = 0.f;  // FWD
       int y = -1;
-      float lse2 = 0.f, gval = 0.f;      // BWDG
+      float lse2 = 0.f, gval = 0.f;      // BWDG, DHS
+      float zyv = 0.f;                   // DHS: fp32 target logit
       if (is_fwd(MODE)) {
         if (valid && (args.mask == nullptr || args.mask[grow] != 0)) y = args.ids[grow];
-      } else if (MODE == MODE_BWDG) {
+      } else if (MODE == MODE_BWDG || MODE == MODE_DHS) {
         if (valid) {
           gval = args.g[grow];
           lse2 = args.lse[grow] * kLog2e;
-          if (gval != 0.f) y = args.ids[grow];
+          if (gval != 0.f) {
+            y = args.ids[grow];
+            if (MODE == MODE_DHS) zyv = args.zy[grow];
+          }
         }
+      }
+
+      if constexpr (MODE == MODE_DHS) {
+        // Every A stage of this unit, as it lands: fp16 logits -> bf16 G in
+        // place (this thread's part of its row), then tell the MMA issuer.
+        for (int k = 0; k < k_iters; ++k, ++cit) {
+          const int s = static_cast<int>(cit % kStages);
+          if (!mbar_wait(&afull_bar[s], (cit / kStages) & 1u, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          constexpr int kNch = 8 / C::kCvtGroups;
+          logits_to_g_row<kNch>(args, smem + s * C::kStageBytes, lrow_in_tile, part * kNch,
+                                args.v0 + k * BK, y, gval, lse2, zyv);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (CTAS == 2) mbar_arrive_cluster(cvt_addr0 + static_cast<uint32_t>(s) * 8u);
+            else mbar_arrive(&cvt_bar[s]);
+          }
+        }
+        if (!ok) break;
+        if (part != 0) continue;  // converter-only warps: no epilogue
       }
 
       for (int t = t0; t < t1; ++t, ++tile_it) {

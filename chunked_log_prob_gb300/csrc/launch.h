@@ -38,7 +38,9 @@ struct FinalizeArgs {
   int* status;
 };
 
-// Stored-logit backward: per-row finish + in-place G formation.
+// Stored-logit backward: per-row finish (lse, logp, token loss, g), and
+// either in-place G formation (finalize_gform) or the row values alone for
+// the dH GEMM that converts the logits itself (finalize_rows).
 struct GformArgs {
   long long n_total;
   int n_rb, rb_offset;
@@ -62,6 +64,8 @@ struct GformArgs {
   const int* n_nonempty;
   float* logp_out;       // optional
   double* lt;            // [N] weighted token loss w_t l_t of unmasked rows
+  float* lse_out;        // finalize_rows: [rows] lse (natural log), by global row
+  float* g_out;          // finalize_rows: [rows] dL/dlogp (0 for rows that do not count)
   uint16_t* S;           // [chunk rows][ldS]: fp16 logits in, bf16 G out
   long long ldS;
   int xmode;
@@ -90,7 +94,7 @@ cudaError_t launch_gemm_variant(const CUtensorMap& map_a, const CUtensorMap& map
                                 const TileArgs& args, int grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+  cfg.blockDim = dim3(PairCfg<MODE, CTAS>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = PairCfg<MODE, CTAS>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -122,6 +126,8 @@ cudaError_t launch_bwdg_gemm(int ctas, const CUtensorMap& map_a, const CUtensorM
                              const TileArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_dh_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                            const TileArgs& args, int grid, cudaStream_t stream);
+cudaError_t launch_dhs_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                            const TileArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_dw_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                            const TileArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_row_plan(const uint8_t* mask, long long n, int n_rb, int* rb_list,
@@ -135,6 +141,7 @@ cudaError_t prepare_fwds_gemm();
 cudaError_t launch_fwds_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                              const TileArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_finalize_gform(const GformArgs& a, int rows, cudaStream_t stream);
+cudaError_t launch_finalize_rows(const GformArgs& a, int rows, cudaStream_t stream);
 cudaError_t launch_finish_loss(const FinishArgs& a, cudaStream_t stream);
 cudaError_t launch_bounded_wait_selftest(int* status, int* waited_out, cudaStream_t stream);
 

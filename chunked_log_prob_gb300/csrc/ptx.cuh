@@ -246,6 +246,20 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
+// Cluster-scope release: for an arrive that announces this thread's own
+// shared-memory writes to a consumer in the peer CTA.
+__device__ __forceinline__ void mbar_arrive_cluster_rel(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                   cluster_addr)
+               : "memory");
+}
+
+// Orders this thread's generic-proxy writes to shared memory before later
+// async-proxy reads of it (tcgen05.mma operands).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // TMA tile load into this CTA's shared memory whose completion is counted on
 // an mbarrier that may sit in the peer CTA of the pair.
 __device__ __forceinline__ void tma_load_2d_pair_nohint(void* dst, const CUtensorMap* map,
@@ -326,6 +340,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Two fp16 (low half first) widened to fp32.
+__device__ __forceinline__ void unpack_f16x2(uint32_t w, float& lo, float& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.f32.f16 %0, l;\n\t"
+      "cvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(w));
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {

@@ -185,7 +185,9 @@ typedef struct grpo_plan_info {
   int32_t launches_logp;     /* kernel launches of one grpo_logp_fwd call    */
   int32_t launches_loss;     /* kernel launches of one grpo_loss_fwd_bwd
                                 (with a mask; one fewer without)          */
-  int32_t reserved;
+  int32_t g_in_dh_gemm;      /* 1: the stored-logit backward forms G inside
+                                the dH GEMM when dW is not requested (hidden
+                                <= 2048); 0: in a pass of its own          */
   uint64_t workspace_bytes;  /* same as grpo_workspace_size                  */
 } grpo_plan_info;
 

@@ -142,6 +142,20 @@ def test_stored_logit_workspace_is_chunk_times_vocab(clp):
     assert auto < 2 * (2 << 30) + 131072 * 400
 
 
+def test_stored_logit_workspace_single_block_up_to_2048_hidden(clp):
+    # D <= 2048: the dH GEMM forms G from the stored logits itself, so one
+    # logit block serves every chunk (no double buffering); larger chunks
+    # are allowed in exchange (4 GiB of logits instead of 2 x 2 GiB).
+    p = clp.make_params(chunk_tokens=2048, flags=1)
+    block = 2048 * 151936 * 2
+    small = clp.grpo_workspace_size(32768, 2048, 151936, 1, p)
+    assert block < small < block + 32768 * 400
+    big = clp.grpo_workspace_size(32768, 2056, 151936, 1, p)
+    assert 2 * block < big < 2 * block + 32768 * 400
+    auto = clp.grpo_workspace_size(131072, 1536, 151936, 1, clp.make_params(flags=1))
+    assert (2 << 30) < auto < (4 << 30) + 131072 * 400
+
+
 @pytest.mark.parametrize("flags", [0, 1])
 def test_workspace_budget_caps_the_chunk(clp, flags):
     n, d, v = 65536, 4096, 128256

@@ -277,10 +277,13 @@ def test_stored_logits_ragged(clp, N, T, D, V, chunk, vblock, padded):
     check(gpu_loss(clp, p, old, ref, params), want, p.mask, f"stored {N}x{D}x{V}")
 
 
+# Hidden sizes on either side of the switch between G formed inside the dH
+# GEMM (D <= 2048) and G formed in a pass of its own over the logit block.
+@pytest.mark.parametrize("D", [200, 2176])
 @pytest.mark.parametrize("kw", XFORMS)
-def test_stored_logits_transforms(clp, kw):
-    p = synth.make_problem("tiny", seed=32, T=75, prompts=1, G=4, D=200, V=3000,
-                           lengths=(20, 75), weight_std=0.2)
+def test_stored_logits_transforms(clp, kw, D):
+    p = synth.make_problem("tiny", seed=32, T=75, prompts=1, G=4, D=D, V=3000,
+                           lengths=(20, 75), weight_std=0.2 if D < 1000 else 0.06)
     xf = oracle.Transform(scale_mul=kw.get("logit_scale_multiply", 1.0),
                           scale_div=kw.get("logit_scale_divide", 1.0),
                           softcap=kw.get("logit_softcapping", 0.0),
@@ -320,6 +323,34 @@ def test_stored_and_recomputed_backward_agree(clp):
     assert np.abs(lp1 - lp2).max() <= 1e-5
     assert abs(L1 - L2) <= 1e-5 * abs(L1)
     assert np.linalg.norm(dH1 - dH2) <= 1e-2 * np.linalg.norm(dH1)
+
+
+@pytest.mark.parametrize("chunk", [0, 128])
+def test_g_in_dh_gemm_matches_separate_pass(clp, chunk):
+    # D <= 2048: without dW the dH GEMM turns the stored logits into G itself;
+    # asking for dW makes the same call form G in a pass of its own (both GEMMs
+    # read it). Same inputs, same row values: logp and loss bit-identical, dH
+    # equal up to the rounding of the target column's G value.
+    p = synth.make_problem("tiny", seed=17, prompts=2, G=4, T=96, D=512, V=3001,
+                           lengths=(10, 96))
+    old, ref, want = oracle_case(p)
+    params = clp.make_params(chunk_tokens=chunk, flags=STORED)
+    plan = clp.grpo_get_plan(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, params)
+    assert plan["g_in_dh_gemm"] == 1
+    args = [_to(x) for x in (p.hidden, p.weight, p.ids, p.mask, old, ref, p.adv)]
+    ws = clp.alloc_workspace(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, params, DEV)
+    L1, lp1, dH1 = clp.grpo_loss_fwd_bwd(*args, p.seq_len, params=params, workspace=ws)
+    st = clp.grpo_read_device_status(ws)
+    L2, lp2, dH2, dW = clp.grpo_loss_fwd_bwd(*args, p.seq_len, params=params, workspace=ws,
+                                             want_dW=True)
+    assert st == 0 and clp.grpo_read_device_status(ws) == 0
+    assert torch.equal(L1, L2) and torch.equal(lp1, lp2)
+    d1, d2 = dH1.double().cpu().numpy(), dH2.double().cpu().numpy()
+    assert np.linalg.norm(d1 - d2) <= 1e-2 * np.linalg.norm(d1)
+    m = p.mask.numpy().astype(bool)
+    assert np.all(d1[~m] == 0) and np.all(d2[~m] == 0)
+    check((L1.item(), lp1.cpu().double().numpy(), d1, st), want, p.mask,
+          f"fused G chunk={chunk}")
 
 
 def test_stored_logits_bad_id_and_all_masked(clp):
@@ -463,11 +494,13 @@ def test_lm_head_gradient_with_transform(clp):
 
 
 def test_concurrent_calls_from_two_threads(clp):
-    # Separate workspaces and streams, stored path with several chunks (so the
-    # shared side stream is used): results equal the same calls made serially.
+    # Separate workspaces and streams, stored path with several chunks and G
+    # formed in its own pass (D > 2048), so the shared side stream is used:
+    # results equal the same calls made serially.
     import threading
 
-    probs = [synth.make_problem("tiny", seed=90 + i, prompts=2, G=4, T=256, D=256, V=3000,
+    D = 2304
+    probs = [synth.make_problem("tiny", seed=90 + i, prompts=2, G=4, T=256, D=D, V=3000,
                                 lengths=(64, 256)) for i in range(2)]
     params = clp.make_params(chunk_tokens=512, flags=STORED)
 
@@ -490,7 +523,7 @@ def test_concurrent_calls_from_two_threads(clp):
         try:
             s = torch.cuda.Stream()
             with torch.cuda.stream(s):
-                ws = clp.alloc_workspace(probs[i].n_tokens, 256, 3000, probs[i].seq_len, params,
+                ws = clp.alloc_workspace(probs[i].n_tokens, D, 3000, probs[i].seq_len, params,
                                          DEV)
                 for _ in range(3):
                     r = clp.grpo_loss_fwd_bwd(*inputs[i], probs[i].seq_len, params=params,
