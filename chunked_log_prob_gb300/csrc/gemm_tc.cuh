@@ -245,10 +245,13 @@ __device__ __forceinline__ void logits_to_g_row(const TileArgs& a, uint8_t* tile
 // The pair's dH GEMM runs units of 512 D columns: two 256-column accumulators
 // fill TMEM (no double buffering; its units are whole-vocabulary K loops, so
 // the single epilogue per unit costs ~1 %), and every A tile of G feeds twice
-// the MMA work.
-template <int MODE, int CTAS>
+// the MMA work. WIDE = 1 does the same for the pair's logit GEMMs (512-column
+// vocab tiles): a quarter less operand traffic per flop, at the price of an
+// epilogue the next tile's MMAs wait for (worth it for the plain forward at
+// large hidden sizes; not for MODE_FWDS, whose epilogue also stores logits).
+template <int MODE, int CTAS, int WIDE = 0>
 struct PairCfg {
-  static constexpr int kNAcc = (is_dh(MODE) && CTAS == 2) ? 2 : 1;  // accumulators
+  static constexpr int kNAcc = ((is_dh(MODE) || WIDE) && CTAS == 2) ? 2 : 1;  // accumulators
   static constexpr int kNBuf = kNAcc == 2 ? 1 : 2;     // TMEM buffers (of kNAcc x 256)
   static constexpr int kTileN = BN * kNAcc;            // N columns per unit
   static constexpr int kBRows = BN / CTAS;             // B rows (cols) per CTA and MMA
@@ -279,11 +282,11 @@ __device__ __forceinline__ void load_box(void* dst, const CUtensorMap* map, uint
   }
 }
 
-template <int MODE, int CTAS>
-__global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
+template <int MODE, int CTAS, int WIDE = 0>
+__global__ void __launch_bounds__(PairCfg<MODE, CTAS, WIDE>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b, const TileArgs args) {
-  using C = PairCfg<MODE, CTAS>;
+  using C = PairCfg<MODE, CTAS, WIDE>;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
@@ -432,8 +435,13 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
                                               (j % kBoxes) * 64,
                                           args.v0 + k * BK);
               } else {
-                tma_load_2d_pair_nohint(b_dst, &map_b, lead, k * BK,
-                                        args.v0 + t * BN + static_cast<int>(rank) * C::kBRows);
+                // Per accumulator, this CTA's 128 of its 256 vocab rows.
+#pragma unroll
+                for (int na = 0; na < C::kNAcc; ++na)
+                  tma_load_2d_pair_nohint(b_dst + na * (C::kBRows * BK * 2), &map_b, lead,
+                                          k * BK,
+                                          args.v0 + t * C::kTileN + na * BN +
+                                              static_cast<int>(rank) * C::kBRows);
               }
             } else {
               mbar_arrive_expect_tx(&full_bar[s], C::kStageBytes);
@@ -615,8 +623,8 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
 
         if (is_fwd(MODE)) {
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            const int col0 = t * BN + c * 32;
+          for (int c = 0; c < C::kTileN / 32; ++c) {
+            const int col0 = t * C::kTileN + c * 32;
             if (col0 >= args.vocab) break;  // warp-uniform
             float v[32];
             tmem_ld32(tbase + c * 32, v);

@@ -119,8 +119,10 @@ def test_ragged_shapes(clp, N, T, D, V, chunk, vblock, padded):
     check(gpu_loss(clp, p, old, ref, params), want, p.mask, f"ragged {N}x{D}x{V}")
 
 
-def test_logp_fwd_ragged(clp):
-    p = synth.make_problem("tiny", seed=3, T=75, prompts=1, G=4, D=200, V=1000)
+# D = 2880: the pair's logit GEMM in 512-column vocab tiles (a ragged last tile).
+@pytest.mark.parametrize("D,V", [(200, 1000), (2880, 1300)])
+def test_logp_fwd_ragged(clp, D, V):
+    p = synth.make_problem("tiny", seed=3, T=75, prompts=1, G=4, D=D, V=V)
     logp, _ = clp.grpo_logp_fwd(_to(p.hidden), _to(p.weight), _to(p.ids))
     want, _ = oracle.selective_logp(p.hidden, p.weight, p.ids.numpy())
     assert np.abs(logp.cpu().double().numpy() - want).max() <= LOGP_TOL
