@@ -267,6 +267,17 @@ struct PairCfg {
   static constexpr int kThreads = 64 + 128 * kCvtGroups;
 };
 
+// MODE_DH/DHS/DW (output columns = hidden): the MMA width of accumulator na
+// of tile t, i.e. its columns inside the hidden size in whole 64-column MN
+// blocks of every CTA's share; 0 when the accumulator lies wholly past it.
+// A ragged last tile thus runs narrower MMAs and loads fewer B boxes.
+template <int CTAS>
+__device__ __forceinline__ int mn_out_cols(const TileArgs& a, int col0) {
+  const int w = a.hidden - col0;
+  constexpr int q = 64 * CTAS;
+  return w <= 0 ? 0 : min(BN, (w + q - 1) / q * q);
+}
+
 // One TMA box into this CTA's stage; its bytes are counted on the leader's
 // barrier (pair) or this CTA's own.
 template <int CTAS>
@@ -376,6 +387,15 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS, WIDE>::kThreads, 1)
             MODE == MODE_DW ? 0 : (is_dh(MODE) ? li : global_rb(args, li)) * BM;
         const int a_m0 = (ru * CTAS + static_cast<int>(rank)) * BM;  // MODE_DW: vocab row
         for (int t = t0; t < t1 && ok; ++t) {
+          // MN-major B (DH, DHS, DW): 64-column boxes per accumulator in this
+          // CTA, and their bytes.
+          int nbox[C::kNAcc];
+          uint32_t b_bytes = 0;
+#pragma unroll
+          for (int na = 0; na < C::kNAcc; ++na) {
+            nbox[na] = mn_out_cols<CTAS>(args, t * C::kTileN + na * BN) / (64 * CTAS);
+            b_bytes += static_cast<uint32_t>(nbox[na]) * (BK * 64 * 2);
+          }
           for (int k = 0; k < k_iters; ++k, ++it) {
             const int s = it % kStages;
             const uint32_t round = it / kStages;
@@ -390,22 +410,23 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS, WIDE>::kThreads, 1)
               // its own barrier: the epilogue warps turn it into G in place.
               mbar_arrive_expect_tx(&afull_bar[s], A_BYTES);
               tma_load_2d_hint(a_dst, &map_a, &afull_bar[s], k * BK, a_row, pol_a);
-              // B (W, MN-major): per accumulator, this CTA's kBRows of its 256
-              // D columns, counted on the leader's barrier (pair) or its own.
-              constexpr int kBoxes = C::kBRows / 64;
+              // B (W, MN-major): per accumulator, this CTA's share of its D
+              // columns, counted on the leader's barrier (pair) or its own.
               const uint32_t lead = CTAS == 2 ? mapa_shared(smem_u32(&full_bar[s]), 0) : 0u;
-              if (CTAS == 2) mbar_arrive_expect_tx_cluster(lead, C::kBBytes);
-              else mbar_arrive_expect_tx(&full_bar[s], C::kBBytes);
+              if (CTAS == 2) mbar_arrive_expect_tx_cluster(lead, b_bytes);
+              else mbar_arrive_expect_tx(&full_bar[s], b_bytes);
 #pragma unroll
-              for (int j = 0; j < C::kNAcc * kBoxes; ++j)
-                load_box<CTAS>(b_dst + j * (BK * 64 * 2), &map_b, &full_bar[s], lead,
-                               t * C::kTileN + (j / kBoxes) * BN +
-                                   static_cast<int>(rank) * C::kBRows + (j % kBoxes) * 64,
-                               args.v0 + k * BK, false, 0);
+              for (int na = 0; na < C::kNAcc; ++na)
+                for (int jb = 0; jb < nbox[na]; ++jb)
+                  load_box<CTAS>(b_dst + na * (C::kBRows * BK * 2) + jb * (BK * 64 * 2), &map_b,
+                                 &full_bar[s], lead,
+                                 t * C::kTileN + na * BN + static_cast<int>(rank) * nbox[na] * 64 +
+                                     jb * 64,
+                                 args.v0 + k * BK, false, 0);
             } else if (MODE == MODE_DW) {
               const uint32_t lead = CTAS == 2 ? mapa_shared(smem_u32(&full_bar[s]), 0) : 0u;
-              if (CTAS == 2) mbar_arrive_expect_tx_cluster(lead, C::kStageBytes);
-              else mbar_arrive_expect_tx(&full_bar[s], C::kStageBytes);
+              if (CTAS == 2) mbar_arrive_expect_tx_cluster(lead, A_BYTES + b_bytes);
+              else mbar_arrive_expect_tx(&full_bar[s], A_BYTES + b_bytes);
               const int kr = k * BK;  // chunk-local row of this K step
               const int grow_k = global_rb(args, kr / BM) * BM + kr % BM;
               // A = G^T: 128 vocab rows (two 64-wide MN blocks) x 64 chunk rows.
@@ -414,26 +435,26 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS, WIDE>::kThreads, 1)
                 load_box<CTAS>(a_dst + j * (BK * 64 * 2), &map_a, &full_bar[s], lead,
                                a_m0 + j * 64, kr, true, pol_a);
               // B = H: this CTA's D columns x the same 64 rows, in 64-wide blocks.
-#pragma unroll
-              for (int j = 0; j < C::kBRows / 64; ++j)
-                load_box<CTAS>(b_dst + j * (BK * 64 * 2), &map_b, &full_bar[s], lead,
-                               t * BN + static_cast<int>(rank) * C::kBRows + j * 64, grow_k,
+              for (int jb = 0; jb < nbox[0]; ++jb)
+                load_box<CTAS>(b_dst + jb * (BK * 64 * 2), &map_b, &full_bar[s], lead,
+                               t * BN + static_cast<int>(rank) * nbox[0] * 64 + jb * 64, grow_k,
                                false, 0);
             } else if (CTAS == 2) {
               // Both CTAs count their bytes on the leader's barrier.
               const uint32_t lead = mapa_shared(smem_u32(&full_bar[s]), 0);
-              mbar_arrive_expect_tx_cluster(lead, C::kStageBytes);
+              mbar_arrive_expect_tx_cluster(lead, MODE == MODE_DH ? A_BYTES + b_bytes
+                                                                  : C::kStageBytes);
               tma_load_2d_pair(a_dst, &map_a, lead, k * BK, a_row, pol_a);
               if (MODE == MODE_DH) {
-                // Per accumulator, this CTA's 128 of its 256 D columns.
-                constexpr int kBoxes = C::kBRows / 64;
+                // Per accumulator, this CTA's share of its D columns.
 #pragma unroll
-                for (int j = 0; j < C::kNAcc * kBoxes; ++j)
-                  tma_load_2d_pair_nohint(b_dst + j * (BK * 64 * 2), &map_b, lead,
-                                          t * C::kTileN + (j / kBoxes) * BN +
-                                              static_cast<int>(rank) * C::kBRows +
-                                              (j % kBoxes) * 64,
-                                          args.v0 + k * BK);
+                for (int na = 0; na < C::kNAcc; ++na)
+                  for (int jb = 0; jb < nbox[na]; ++jb)
+                    tma_load_2d_pair_nohint(
+                        b_dst + na * (C::kBRows * BK * 2) + jb * (BK * 64 * 2), &map_b, lead,
+                        t * C::kTileN + na * BN + static_cast<int>(rank) * nbox[na] * 64 +
+                            jb * 64,
+                        args.v0 + k * BK);
               } else {
                 // Per accumulator, this CTA's 128 of its 256 vocab rows.
 #pragma unroll
@@ -444,14 +465,14 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS, WIDE>::kThreads, 1)
                                               static_cast<int>(rank) * C::kBRows);
               }
             } else {
-              mbar_arrive_expect_tx(&full_bar[s], C::kStageBytes);
+              mbar_arrive_expect_tx(&full_bar[s],
+                                    MODE == MODE_DH ? A_BYTES + b_bytes : C::kStageBytes);
               tma_load_2d_hint(a_dst, &map_a, &full_bar[s], k * BK, a_row, pol_a);
               if (MODE == MODE_DH) {
-                // W[v0 + k*64 .. +64, d0 .. d0+256) as four 64x64 MN-major boxes.
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  tma_load_2d(b_dst + j * (BK * 64 * 2), &map_b, &full_bar[s],
-                              t * BN + j * 64, args.v0 + k * BK);
+                // W[v0 + k*64 .. +64, d0 .. d0+256) as up to four 64x64 MN-major boxes.
+                for (int jb = 0; jb < nbox[0]; ++jb)
+                  tma_load_2d(b_dst + jb * (BK * 64 * 2), &map_b, &full_bar[s],
+                              t * BN + jb * 64, args.v0 + k * BK);
               } else {
                 tma_load_2d(b_dst, &map_b, &full_bar[s], k * BK, args.v0 + t * BN);
               }
@@ -474,8 +495,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS, WIDE>::kThreads, 1)
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer --
     if (lane == 0 && rank == 0) {
-      constexpr uint32_t idesc =
-          idesc_bf16(BM * CTAS, BN, MODE == MODE_DW, is_dh(MODE) || MODE == MODE_DW);
+      constexpr bool kMnOut = is_dh(MODE) || MODE == MODE_DW;  // B MN-major, N = hidden
       uint32_t it = 0, tile_it = 0;
       bool ok = true;
       for (int u = cta_slot; u < n_units && ok; u += n_slots) {
@@ -491,6 +511,13 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS, WIDE>::kThreads, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + buf * BN;
+          // Instruction descriptor per accumulator (0: skipped, past the hidden size).
+          uint32_t idesc[C::kNAcc];
+#pragma unroll
+          for (int na = 0; na < C::kNAcc; ++na) {
+            const int n = kMnOut ? mn_out_cols<CTAS>(args, t * C::kTileN + na * BN) : BN;
+            idesc[na] = n == 0 ? 0u : idesc_bf16(BM * CTAS, n, MODE == MODE_DW, kMnOut);
+          }
           for (int k = 0; k < k_iters; ++k, ++it) {
             const int s = it % kStages;
             const uint32_t round = it / kStages;
@@ -526,9 +553,10 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS, WIDE>::kThreads, 1)
 #pragma unroll
               for (int na = 0; na < C::kNAcc; ++na) {
                 // Accumulator na: B columns na*256.. (its own B boxes), TMEM columns na*256..
+                if (idesc[na] == 0u) continue;
                 const uint64_t bd = bdesc + ((static_cast<uint64_t>(na) * C::kBRows * BK * 2) >> 4);
-                if (CTAS == 2) tc_mma_bf16_pair(d_tmem + na * BN, adesc, bd, idesc, acc);
-                else tc_mma_bf16(d_tmem + na * BN, adesc, bd, idesc, acc);
+                if (CTAS == 2) tc_mma_bf16_pair(d_tmem + na * BN, adesc, bd, idesc[na], acc);
+                else tc_mma_bf16(d_tmem + na * BN, adesc, bd, idesc[na], acc);
               }
             }
             if (CTAS == 2) tc_commit_pair_multicast(&empty_bar[s], 0x3);
