@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "grpo_gb300.h"
 #include "launch.h"
@@ -124,23 +125,42 @@ int stored_fwd_splits(int nrb, int nvt, int sms, double* eff_out) {
 // Row blocks per chunk for the stored-logit backward. Each chunk runs a
 // forward launch of (row blocks x splits) units and a dH launch of
 // (row blocks x D tiles) units; the score is the ideal SM time of the whole
-// schedule (every chunk, including a shorter last one) over its wave-rounded
-// time, forward and dH weighted equally. Near-ties go to the larger chunk.
-int auto_stored_chunk_blocks(long long n_rb_total, int n_dt, int nvt, int sms, int max_units) {
+// schedule (every chunk, including a shorter last one) over its modelled
+// time: forward and dH rounded up to whole waves, plus whatever of each
+// chunk's separate G pass the GEMMs around it cannot hide. exposed_g is that
+// pass's time relative to the forward GEMM of the same rows (0 when dH forms
+// G itself). In the overlapped schedule pass c runs beside dH(c-1) and the
+// forward of chunk c+1; with a single chunk it is fully exposed. Plans of
+// more than one chunk take at most max_multi row blocks per chunk (they may
+// need two chunk blocks). Near-ties go to the larger chunk.
+int auto_stored_chunk_blocks(long long n_rb_total, int n_dt, int nvt, int sms, int max_units,
+                             int max_multi, double exposed_g) {
   const int hi = static_cast<int>(std::min<long long>(n_rb_total, max_units));
-  int best = hi;
+  int best = std::min(hi, std::max(1, max_multi));
+  if (hi >= n_rb_total) best = hi;
   double best_score = -1.0;
+  std::vector<double> fwd, dh;
   for (int nrb = hi; nrb >= 1; --nrb) {
+    if (nrb < n_rb_total && nrb > max_multi) continue;
     double ideal = 0.0, actual = 0.0;
+    fwd.clear();
+    dh.clear();
     for (long long r0 = 0; r0 < n_rb_total; r0 += nrb) {
       const int n = static_cast<int>(std::min<long long>(nrb, n_rb_total - r0));
       const int sp = stored_fwd_splits(n, nvt, sms, nullptr);
       // forward: waves x tiles per unit (the longest unit sets the pace)
-      ideal += static_cast<double>(n) * nvt / sms;
-      actual += static_cast<double>(cdiv(static_cast<long long>(n) * sp, sms)) * cdiv(nvt, sp);
+      fwd.push_back(static_cast<double>(cdiv(static_cast<long long>(n) * sp, sms)) *
+                    cdiv(nvt, sp));
       // dH: units of equal K; scaled to the forward's per-row work
-      ideal += static_cast<double>(n) * nvt / sms;
-      actual += static_cast<double>(cdiv(static_cast<long long>(n) * n_dt, sms)) * nvt / n_dt;
+      dh.push_back(static_cast<double>(cdiv(static_cast<long long>(n) * n_dt, sms)) * nvt /
+                   n_dt);
+      ideal += 2.0 * n * nvt / sms;
+      actual += fwd.back() + dh.back();
+    }
+    const size_t nc = fwd.size();
+    for (size_t c = 0; c < nc; ++c) {
+      const double window = (c > 0 ? dh[c - 1] : 0.0) + (c + 1 < nc ? fwd[c + 1] : 0.0);
+      actual += std::max(0.0, exposed_g * fwd[c] - window);
     }
     const double score = ideal / actual;
     if (score > best_score + 0.005) {
@@ -226,8 +246,18 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   if (p && p->chunk_tokens > 0) {
     crows = cdiv(p->chunk_tokens, ru_rows) * ru_rows;
   } else if (L->stored) {
+    // The G pass moves 4 bytes per logit against the forward's 2 D flops:
+    // about 550 / D of the forward GEMM's time on GB300 (measured at D = 4096).
+    const double exposed_g = L->fused ? 0.0 : 550.0 / L->D;
+    // A device plan never needs more than the sizing without a device (the
+    // largest chunk): when that is one block for the whole batch, a plan of
+    // several double-buffered chunks gets half of it per chunk.
+    const long long big = std::min<long long>(n_ru_total, max_units);
+    const long long room = big * (sbufs == 2 && big < n_ru_total ? 2 : 1);
+    const int max_multi = static_cast<int>(std::max<long long>(1, room / sbufs));
     crows = (sms > 0 ? auto_stored_chunk_blocks(n_ru_total, n_dt, L->nvt, slots,
-                                                static_cast<int>(max_units))
+                                                static_cast<int>(max_units), max_multi,
+                                                exposed_g)
                      : std::min<long long>(n_ru_total, max_units)) *
             ru_rows;
   } else if (sms > 0) {

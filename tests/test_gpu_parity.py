@@ -355,6 +355,27 @@ def test_g_in_dh_gemm_matches_separate_pass(clp, chunk):
           f"fused G chunk={chunk}")
 
 
+@pytest.mark.parametrize("n", [2048, 4096, 8192])
+def test_device_plan_fits_host_sized_workspace(clp, n):
+    # grpo_workspace_size plans without a device; the call plans with the SM
+    # count (and may split a batch that fits one logit block into
+    # double-buffered chunks). The host-sized workspace must always suffice,
+    # and both backward variants must agree.
+    D, V = 2304, 3000
+    p = synth.make_problem("tiny", seed=n, prompts=n // 1024, G=4, T=256, D=D, V=V,
+                           lengths=(128, 256))
+    base, _ = oracle.selective_logp(p.hidden[:4], p.weight, p.ids.numpy()[:4])
+    old = torch.full((n,), float(base.mean()))
+    params = clp.make_params(flags=STORED)
+    plan = clp.grpo_get_plan(n, D, V, p.seq_len, params)
+    assert plan["workspace_bytes"] <= clp.grpo_workspace_size(n, D, V, p.seq_len, params)
+    L1, lp1, dH1, s1 = gpu_loss(clp, p, old, old, params)
+    L2, lp2, dH2, s2 = gpu_loss(clp, p, old, old, clp.make_params())
+    assert s1 == 0 and s2 == 0
+    assert np.abs(lp1 - lp2).max() <= 1e-5 and abs(L1 - L2) <= 1e-5 * abs(L2)
+    assert np.linalg.norm(dH1 - dH2) <= 1e-2 * np.linalg.norm(dH2)
+
+
 def test_stored_logits_bad_id_and_all_masked(clp):
     p = synth.make_problem("tiny", seed=13)
     params = clp.make_params(flags=STORED)
