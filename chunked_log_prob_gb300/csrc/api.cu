@@ -29,11 +29,6 @@ constexpr size_t kMaxStoredChunkBytes = size_t(2) << 30;    // 2 GiB of fp16 log
 // with the CTA-pair MMA operand reads). At D = 1536 fusing is 7-12 % faster
 // per call, at D = 2880 and 4096 the overlapped separate pass is faster.
 constexpr int kFusedMaxHidden = 2048;
-// Hidden sizes from which the pair's plain logit GEMM (logp forward and the
-// recomputed backward's forward) runs 512-column vocab tiles: a quarter less
-// operand traffic per flop against an epilogue the next tile waits for.
-// Measured on GB300: 5-6 % faster at D = 2880 and 4096, slower at D = 1536.
-constexpr int kWideMinHidden = 2560;
 constexpr int kSplitsTarget = 8;        // forward vocab splits per raster group
 constexpr size_t kHeaderBytes = 16384;   // status, counters, loss partials
 constexpr int kMaxDevices = 64;
@@ -60,8 +55,6 @@ struct Layout {
   long long n, nr;  // rows, rows rounded up to BM
   int T, D, V;
   int nvt;          // vocab tiles (256 columns)
-  bool fwd_wide;    // plain logit GEMM in 512-column vocab tiles (pair, D >= kWideMinHidden)
-  int nvt_f;        // vocab tiles of the plain logit GEMM (256 or 512 columns)
   int chunk_rows;   // backward chunk (multiple of BM)
   int n_sbuf;       // stored path: logit blocks (2 = double-buffered chunks)
   bool fused;       // stored path, D <= kFusedMaxHidden: G formed inside the dH
@@ -204,8 +197,6 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   L->vblock = L->stored ? static_cast<int>(L->ldS) : static_cast<int>(vb);
   L->need_acc = !L->stored && L->vblock < L->V;
   L->fused = L->stored && L->D <= kFusedMaxHidden;
-  L->fwd_wide = L->ctas == 2 && L->D >= kWideMinHidden;
-  L->nvt_f = static_cast<int>(cdiv(s->vocab, L->fwd_wide ? 2 * BN : BN));
 
   // Everything before the backward chunk block depends on N only.
   size_t off = kHeaderBytes;
@@ -509,9 +500,9 @@ int run_forward(const void* hidden, const void* W, const int32_t* ids, const uin
   a.group_rows = (prm != nullptr && prm->raster_rows > 0) ? std::min(prm->raster_rows, n_ru)
                                                          : group_rows_exact(n_ru, slots);
   int splits = std::max(1, slots / a.group_rows);
-  splits = std::min(splits, std::min(L.nvt_f, kMaxSplits));
+  splits = std::min(splits, std::min(L.nvt, kMaxSplits));
   a.n_cols = splits;
-  a.n_vtiles = L.nvt_f;
+  a.n_vtiles = L.nvt;
   a.v0 = 0;
   a.ids = ids;
   a.mask = mask;
@@ -521,8 +512,7 @@ int run_forward(const void* hidden, const void* W, const int32_t* ids, const uin
   a.part_ld = L.nr;
   const long long units = static_cast<long long>(n_ru) * a.n_cols;
   const int grid = L.ctas * static_cast<int>(std::min<long long>(units, slots));
-  if (launch_fwd_gemm(L.ctas, L.fwd_wide, map_h, map_w, a, grid, st) != cudaSuccess)
-    return GRPO_ERR_CUDA;
+  if (launch_fwd_gemm(L.ctas, map_h, map_w, a, grid, st) != cudaSuccess) return GRPO_ERR_CUDA;
   *splits_out = splits;
   return GRPO_OK;
 }
@@ -1052,7 +1042,7 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
   const int n_rb = static_cast<int>(L.nr / BM);
   const int slots = std::max(1, sms / L.ctas);
   const int grp = group_rows_exact(static_cast<int>(cdiv(n_rb, L.ctas)), slots);
-  info->fwd_splits = std::min(std::max(1, slots / grp), std::min(L.nvt_f, kMaxSplits));
+  info->fwd_splits = std::min(std::max(1, slots / grp), std::min(L.nvt, kMaxSplits));
   info->launches_logp = L.n > 0 ? 2 : 0;
   info->launches_loss = L.n <= 0 ? 0
                       : L.stored ? 3 + 3 * info->n_chunks

@@ -12,16 +12,13 @@ namespace grpo {
 
 cudaError_t prepare_fwd_gemm() {
   cudaError_t e = prepare_gemm_variant<MODE_FWD, 1>();
-  if (e == cudaSuccess) e = prepare_gemm_variant<MODE_FWD, 2>();
-  return e == cudaSuccess ? prepare_gemm_variant<MODE_FWD, 2, 1>() : e;
+  return e == cudaSuccess ? prepare_gemm_variant<MODE_FWD, 2>() : e;
 }
 
-cudaError_t launch_fwd_gemm(int ctas, bool wide, const CUtensorMap& map_a,
-                            const CUtensorMap& map_b, const TileArgs& args, int grid,
-                            cudaStream_t stream) {
-  if (ctas != 2) return launch_gemm_variant<MODE_FWD, 1>(map_a, map_b, args, grid, stream);
-  return wide ? launch_gemm_variant<MODE_FWD, 2, 1>(map_a, map_b, args, grid, stream)
-              : launch_gemm_variant<MODE_FWD, 2>(map_a, map_b, args, grid, stream);
+cudaError_t launch_fwd_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                            const TileArgs& args, int grid, cudaStream_t stream) {
+  return ctas == 2 ? launch_gemm_variant<MODE_FWD, 2>(map_a, map_b, args, grid, stream)
+                   : launch_gemm_variant<MODE_FWD, 1>(map_a, map_b, args, grid, stream);
 }
 
 __global__ void __launch_bounds__(1024) row_plan_kernel(const uint8_t* __restrict__ mask,

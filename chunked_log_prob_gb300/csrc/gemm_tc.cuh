@@ -245,18 +245,21 @@ __device__ __forceinline__ void logits_to_g_row(const TileArgs& a, uint8_t* tile
 // The pair's dH GEMM runs units of 512 D columns: two 256-column accumulators
 // fill TMEM (no double buffering; its units are whole-vocabulary K loops, so
 // the single epilogue per unit costs ~1 %), and every A tile of G feeds twice
-// the MMA work. WIDE = 1 does the same for the pair's logit GEMMs (512-column
-// vocab tiles): a quarter less operand traffic per flop, at the price of an
-// epilogue the next tile's MMAs wait for (worth it for the plain forward at
-// large hidden sizes; not for MODE_FWDS, whose epilogue also stores logits).
-template <int MODE, int CTAS, int WIDE = 0>
+// the MMA work.
+template <int MODE, int CTAS>
 struct PairCfg {
-  static constexpr int kNAcc = ((is_dh(MODE) || WIDE) && CTAS == 2) ? 2 : 1;  // accumulators
+  static constexpr int kNAcc = (is_dh(MODE) && CTAS == 2) ? 2 : 1;  // accumulators
   static constexpr int kNBuf = kNAcc == 2 ? 1 : 2;     // TMEM buffers (of kNAcc x 256)
   static constexpr int kTileN = BN * kNAcc;            // N columns per unit
   static constexpr int kBRows = BN / CTAS;             // B rows (cols) per CTA and MMA
   static constexpr int kBBytes = kNAcc * kBRows * BK * 2;
-  static constexpr int kStageBytes = A_BYTES + kBBytes;
+  // 64-wide K slices per stage: the pair's 256-column logit GEMMs (a lone
+  // accumulator) take two, so that each stage carries 8 MMAs like the dH
+  // GEMM's 512-wide units. With 4 per stage the tensor pipe idled ~18 % of the
+  // time whatever the ring depth, the operand traffic or the epilogue: a fixed
+  // cost per stage (measured 81 % -> 91 % tensor-pipe activity).
+  static constexpr int kKSub = (CTAS == 2 && kNAcc == 1 && (is_fwd(MODE) || MODE == MODE_BWDG)) ? 2 : 1;
+  static constexpr int kStageBytes = kKSub * (A_BYTES + kBBytes);
   static constexpr int kMaxDynSmem = 232448 - 1024 - 1024;  // 227 KB less slack and statics
   static constexpr int kStages =
       CTAS == 2 ? (kMaxDynSmem / kStageBytes < 7 ? kMaxDynSmem / kStageBytes : 7) : STAGES;
@@ -293,11 +296,11 @@ __device__ __forceinline__ void load_box(void* dst, const CUtensorMap* map, uint
   }
 }
 
-template <int MODE, int CTAS, int WIDE = 0>
-__global__ void __launch_bounds__(PairCfg<MODE, CTAS, WIDE>::kThreads, 1)
+template <int MODE, int CTAS>
+__global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b, const TileArgs args) {
-  using C = PairCfg<MODE, CTAS, WIDE>;
+  using C = PairCfg<MODE, CTAS>;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
@@ -367,7 +370,8 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS, WIDE>::kThreads, 1)
   const int n_ru = MODE == MODE_DW ? (args.dw_rows + BM * CTAS - 1) / (BM * CTAS)
                                    : (n_rb + CTAS - 1) / CTAS;  // units of 128*CTAS rows
   const int n_units = n_ru * args.n_cols;
-  const int k_iters = MODE == MODE_DW ? n_rb * (BM / BK) : args.k_iters;
+  // Stages per tile (k_iters counts 64-wide K slices; a stage holds kKSub).
+  const int k_iters = MODE == MODE_DW ? n_rb * (BM / BK) : (args.k_iters + C::kKSub - 1) / C::kKSub;
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
@@ -404,7 +408,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS, WIDE>::kThreads, 1)
               break;
             }
             uint8_t* a_dst = smem + s * C::kStageBytes;
-            uint8_t* b_dst = a_dst + A_BYTES;
+            uint8_t* b_dst = a_dst + C::kKSub * A_BYTES;
             if constexpr (MODE == MODE_DHS) {
               // A (the stored fp16 logits) into this CTA's stage, counted on
               // its own barrier: the epilogue warps turn it into G in place.
@@ -444,7 +448,10 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS, WIDE>::kThreads, 1)
               const uint32_t lead = mapa_shared(smem_u32(&full_bar[s]), 0);
               mbar_arrive_expect_tx_cluster(lead, MODE == MODE_DH ? A_BYTES + b_bytes
                                                                   : C::kStageBytes);
-              tma_load_2d_pair(a_dst, &map_a, lead, k * BK, a_row, pol_a);
+#pragma unroll
+              for (int ks = 0; ks < C::kKSub; ++ks)
+                tma_load_2d_pair(a_dst + ks * A_BYTES, &map_a, lead, (k * C::kKSub + ks) * BK, a_row,
+                                 pol_a);
               if (MODE == MODE_DH) {
                 // Per accumulator, this CTA's share of its D columns.
 #pragma unroll
@@ -456,13 +463,15 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS, WIDE>::kThreads, 1)
                             jb * 64,
                         args.v0 + k * BK);
               } else {
-                // Per accumulator, this CTA's 128 of its 256 vocab rows.
+                // Per K slice and accumulator, this CTA's 128 of its 256 vocab rows.
 #pragma unroll
-                for (int na = 0; na < C::kNAcc; ++na)
-                  tma_load_2d_pair_nohint(b_dst + na * (C::kBRows * BK * 2), &map_b, lead,
-                                          k * BK,
-                                          args.v0 + t * C::kTileN + na * BN +
-                                              static_cast<int>(rank) * C::kBRows);
+                for (int ks = 0; ks < C::kKSub; ++ks)
+#pragma unroll
+                  for (int na = 0; na < C::kNAcc; ++na)
+                    tma_load_2d_pair_nohint(b_dst + ks * C::kBBytes + na * (C::kBRows * BK * 2),
+                                            &map_b, lead, (k * C::kKSub + ks) * BK,
+                                            args.v0 + t * C::kTileN + na * BN +
+                                                static_cast<int>(rank) * C::kBRows);
               }
             } else {
               mbar_arrive_expect_tx(&full_bar[s],
@@ -533,23 +542,26 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS, WIDE>::kThreads, 1)
             }
             tc_fence_after();
             const uint32_t a_addr = smem_u32(smem + s * C::kStageBytes);
-            const uint32_t b_addr = a_addr + A_BYTES;
+            const uint32_t b_addr = a_addr + C::kKSub * A_BYTES;
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
+            for (int kq = 0; kq < C::kKSub * (BK / 16); ++kq) {
+              const int kk = kq % (BK / 16);                      // K step in its slice
+              const uint32_t a_sl = a_addr + (kq / (BK / 16)) * A_BYTES;  // slice base
+              const uint32_t b_sl = b_addr + (kq / (BK / 16)) * C::kBBytes;
               // K-major, 128B swizzle: K advances by 32 bytes inside the atom;
               // 8-row groups are 1024 bytes apart.
               const uint64_t adesc = MODE == MODE_DW
                                          ? sdesc_sw128(a_addr + kk * 2048, BK * 64 * 2, 1024)
-                                         : sdesc_sw128(a_addr + kk * 32, 16, 1024);
+                                         : sdesc_sw128(a_sl + kk * 32, 16, 1024);
               uint64_t bdesc;
               if (is_dh(MODE) || MODE == MODE_DW) {
                 // MN-major, 128B swizzle: 64-wide N blocks 8 KB apart (LBO),
                 // 8-deep K groups 1 KB apart (SBO); K advances 16 rows.
                 bdesc = sdesc_sw128(b_addr + kk * 2048, BK * 64 * 2, 1024);
               } else {
-                bdesc = sdesc_sw128(b_addr + kk * 32, 16, 1024);
+                bdesc = sdesc_sw128(b_sl + kk * 32, 16, 1024);
               }
-              const uint32_t acc = (k | kk) != 0 ? 1u : 0u;
+              const uint32_t acc = (k | kq) != 0 ? 1u : 0u;  // first MMA of the tile overwrites
 #pragma unroll
               for (int na = 0; na < C::kNAcc; ++na) {
                 // Accumulator na: B columns na*256.. (its own B boxes), TMEM columns na*256..

@@ -89,13 +89,13 @@ constexpr int kMaxFinalizeBlocks = 1024;
 
 // Launch of one GEMM variant; a CTA pair (CTAS = 2) runs as a 2-CTA cluster.
 // `grid` counts CTAs (a multiple of CTAS).
-template <int MODE, int CTAS, int WIDE = 0>
+template <int MODE, int CTAS>
 cudaError_t launch_gemm_variant(const CUtensorMap& map_a, const CUtensorMap& map_b,
                                 const TileArgs& args, int grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(PairCfg<MODE, CTAS, WIDE>::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = PairCfg<MODE, CTAS, WIDE>::kSmemBytes;
+  cfg.blockDim = dim3(PairCfg<MODE, CTAS>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = PairCfg<MODE, CTAS>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   if (CTAS == 2) {
@@ -106,24 +106,22 @@ cudaError_t launch_gemm_variant(const CUtensorMap& map_a, const CUtensorMap& map
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, CTAS, WIDE>, map_a, map_b, args);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, CTAS>, map_a, map_b, args);
 }
 
-template <int MODE, int CTAS, int WIDE = 0>
+template <int MODE, int CTAS>
 cudaError_t prepare_gemm_variant() {
-  return cudaFuncSetAttribute(tc_gemm_kernel<MODE, CTAS, WIDE>,
+  return cudaFuncSetAttribute(tc_gemm_kernel<MODE, CTAS>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              PairCfg<MODE, CTAS, WIDE>::kSmemBytes);
+                              PairCfg<MODE, CTAS>::kSmemBytes);
 }
 
 // Each launcher lives in the translation unit that instantiates its kernels;
 // ctas selects the single-CTA (1) or CTA-pair (2) variant.
 cudaError_t prepare_fwd_gemm();   // opt-in to the large dynamic smem
 cudaError_t prepare_bwd_gemms();
-// wide (pair only): 512-column vocab tiles (PairCfg WIDE).
-cudaError_t launch_fwd_gemm(int ctas, bool wide, const CUtensorMap& map_a,
-                            const CUtensorMap& map_b, const TileArgs& args, int grid,
-                            cudaStream_t stream);
+cudaError_t launch_fwd_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                            const TileArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_bwdg_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                              const TileArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_dh_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,

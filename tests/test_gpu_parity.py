@@ -119,7 +119,7 @@ def test_ragged_shapes(clp, N, T, D, V, chunk, vblock, padded):
     check(gpu_loss(clp, p, old, ref, params), want, p.mask, f"ragged {N}x{D}x{V}")
 
 
-# D = 2880: the pair's logit GEMM in 512-column vocab tiles (a ragged last tile).
+# D = 2880: an odd number of 64-wide K slices (the pair GEMMs' last stage is half empty).
 @pytest.mark.parametrize("D,V", [(200, 1000), (2880, 1300)])
 def test_logp_fwd_ragged(clp, D, V):
     p = synth.make_problem("tiny", seed=3, T=75, prompts=1, G=4, D=D, V=V)
