@@ -71,11 +71,15 @@ typedef struct grpo_shape {
 
 /* grpo_params.flags bit: backward without a second logit GEMM. Per chunk of
  * rows, the forward GEMM also keeps the chunk's (transformed) logits in fp16
- * in the workspace; a row-wise pass turns them into G once lse and g are
- * known, and the dH GEMM runs over the whole vocabulary. Executes 4 N D V
- * instead of 6 N D V flops, for a workspace of chunk x V x 2 bytes (capped at
- * 2 GiB) instead of chunk x vocab_block x 2 (vocab_block is then ignored).
- * Logits must stay within fp16 range (|z'| < 65504). */
+ * in the workspace, and the dH GEMM runs over the whole vocabulary once lse
+ * and g are known. The logits are turned into G in one of two ways:
+ *   - D <= 2048 without dW: the dH GEMM converts each landed tile on chip.
+ *     One block of chunk x V x 2 bytes (capped at 4 GiB) serves every chunk.
+ *   - otherwise: a row-wise pass rewrites the block in place, beside the next
+ *     chunk's GEMMs. Two blocks when there is more than one chunk (each capped
+ *     at 2 GiB).
+ * Executes 4 N D V instead of 6 N D V flops; vocab_block is ignored. Logits
+ * must stay within fp16 range (|z'| < 65504). */
 #define GRPO_FLAG_STORED_LOGITS 1u
 
 /* grpo_params.flags bit: run every GEMM as one CTA per 128-row tile instead
