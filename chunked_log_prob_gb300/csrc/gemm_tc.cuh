@@ -253,12 +253,13 @@ struct PairCfg {
   static constexpr int kTileN = BN * kNAcc;            // N columns per unit
   static constexpr int kBRows = BN / CTAS;             // B rows (cols) per CTA and MMA
   static constexpr int kBBytes = kNAcc * kBRows * BK * 2;
-  // 64-wide K slices per stage: the pair's 256-column logit GEMMs (a lone
-  // accumulator) take two, so that each stage carries 8 MMAs like the dH
+  // 64-wide K slices per stage: the pair's 256-column logit and dW GEMMs (a
+  // lone accumulator) take two, so that each stage carries 8 MMAs like the dH
   // GEMM's 512-wide units. With 4 per stage the tensor pipe idled ~18 % of the
   // time whatever the ring depth, the operand traffic or the epilogue: a fixed
   // cost per stage (measured 81 % -> 91 % tensor-pipe activity).
-  static constexpr int kKSub = (CTAS == 2 && kNAcc == 1 && (is_fwd(MODE) || MODE == MODE_BWDG)) ? 2 : 1;
+  static constexpr int kKSub =
+      (CTAS == 2 && kNAcc == 1 && (is_fwd(MODE) || MODE == MODE_BWDG || MODE == MODE_DW)) ? 2 : 1;
   static constexpr int kStageBytes = kKSub * (A_BYTES + kBBytes);
   static constexpr int kMaxDynSmem = 232448 - 1024 - 1024;  // 227 KB less slack and statics
   static constexpr int kStages =
@@ -371,7 +372,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
                                    : (n_rb + CTAS - 1) / CTAS;  // units of 128*CTAS rows
   const int n_units = n_ru * args.n_cols;
   // Stages per tile (k_iters counts 64-wide K slices; a stage holds kKSub).
-  const int k_iters = MODE == MODE_DW ? n_rb * (BM / BK) : (args.k_iters + C::kKSub - 1) / C::kKSub;
+  const int k_iters = ((MODE == MODE_DW ? n_rb * (BM / BK) : args.k_iters) + C::kKSub - 1) / C::kKSub;
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
@@ -429,20 +430,24 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
                                  args.v0 + k * BK, false, 0);
             } else if (MODE == MODE_DW) {
               const uint32_t lead = CTAS == 2 ? mapa_shared(smem_u32(&full_bar[s]), 0) : 0u;
-              if (CTAS == 2) mbar_arrive_expect_tx_cluster(lead, A_BYTES + b_bytes);
-              else mbar_arrive_expect_tx(&full_bar[s], A_BYTES + b_bytes);
-              const int kr = k * BK;  // chunk-local row of this K step
-              const int grow_k = global_rb(args, kr / BM) * BM + kr % BM;
-              // A = G^T: 128 vocab rows (two 64-wide MN blocks) x 64 chunk rows.
+              if (CTAS == 2) mbar_arrive_expect_tx_cluster(lead, C::kKSub * (A_BYTES + b_bytes));
+              else mbar_arrive_expect_tx(&full_bar[s], C::kKSub * (A_BYTES + b_bytes));
 #pragma unroll
-              for (int j = 0; j < 2; ++j)
-                load_box<CTAS>(a_dst + j * (BK * 64 * 2), &map_a, &full_bar[s], lead,
-                               a_m0 + j * 64, kr, true, pol_a);
-              // B = H: this CTA's D columns x the same 64 rows, in 64-wide blocks.
-              for (int jb = 0; jb < nbox[0]; ++jb)
-                load_box<CTAS>(b_dst + jb * (BK * 64 * 2), &map_b, &full_bar[s], lead,
-                               t * BN + static_cast<int>(rank) * nbox[0] * 64 + jb * 64, grow_k,
-                               false, 0);
+              for (int ks = 0; ks < C::kKSub; ++ks) {
+                const int kr = (k * C::kKSub + ks) * BK;  // chunk-local row of this K slice
+                const int grow_k = global_rb(args, kr / BM) * BM + kr % BM;
+                // A = G^T: 128 vocab rows (two 64-wide MN blocks) x 64 chunk rows.
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                  load_box<CTAS>(a_dst + ks * A_BYTES + j * (BK * 64 * 2), &map_a, &full_bar[s],
+                                 lead, a_m0 + j * 64, kr, true, pol_a);
+                // B = H: this CTA's D columns x the same 64 rows, in 64-wide blocks.
+                for (int jb = 0; jb < nbox[0]; ++jb)
+                  load_box<CTAS>(b_dst + ks * C::kBBytes + jb * (BK * 64 * 2), &map_b,
+                                 &full_bar[s], lead,
+                                 t * BN + static_cast<int>(rank) * nbox[0] * 64 + jb * 64, grow_k,
+                                 false, 0);
+              }
             } else if (CTAS == 2) {
               // Both CTAs count their bytes on the leader's barrier.
               const uint32_t lead = mapa_shared(smem_u32(&full_bar[s]), 0);
@@ -551,13 +556,13 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
               // K-major, 128B swizzle: K advances by 32 bytes inside the atom;
               // 8-row groups are 1024 bytes apart.
               const uint64_t adesc = MODE == MODE_DW
-                                         ? sdesc_sw128(a_addr + kk * 2048, BK * 64 * 2, 1024)
+                                         ? sdesc_sw128(a_sl + kk * 2048, BK * 64 * 2, 1024)
                                          : sdesc_sw128(a_sl + kk * 32, 16, 1024);
               uint64_t bdesc;
               if (is_dh(MODE) || MODE == MODE_DW) {
                 // MN-major, 128B swizzle: 64-wide N blocks 8 KB apart (LBO),
                 // 8-deep K groups 1 KB apart (SBO); K advances 16 rows.
-                bdesc = sdesc_sw128(b_addr + kk * 2048, BK * 64 * 2, 1024);
+                bdesc = sdesc_sw128(b_sl + kk * 2048, BK * 64 * 2, 1024);
               } else {
                 bdesc = sdesc_sw128(b_sl + kk * 32, 16, 1024);
               }

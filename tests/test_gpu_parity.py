@@ -564,3 +564,47 @@ def test_concurrent_calls_from_two_threads(clp):
     assert not errors
     for (l0, lp0, d0), (l1, lp1, d1) in zip(serial, out):
         assert torch.equal(l0, l1) and torch.equal(lp0, lp1) and torch.equal(d0, d1)
+
+
+@pytest.mark.parametrize("flags", [0, STORED])
+def test_device_memory_is_the_workspace_only(clp, flags):
+    # The memory claim ("GRPO with 7x longer context", section "Flattened
+    # sequence length chunking", Eq. 1-3): at a fixed chunk the memory a call
+    # needs grows with N only by a few words per row, never with N x V. Checked
+    # on the device: with inputs, outputs and workspace allocated beforehand,
+    # a call changes the free device memory by nothing (the library allocates
+    # nothing), and the workspace over an N sweep grows by O(N) only.
+    D, V, T, chunk = 1024, 32000, 1024, 2048
+    dev = torch.device(DEV)
+    params = clp.make_params(chunk_tokens=chunk, flags=flags)
+    sizes = {}
+    for n in (4096, 16384, 65536):
+        g = torch.Generator(device="cpu").manual_seed(n)
+        hidden = torch.randn(n, D, generator=g).to(torch.bfloat16).to(dev)
+        W = (0.02 * torch.randn(V, D, generator=g)).to(torch.bfloat16).to(dev)
+        ids = torch.randint(0, V, (n,), generator=g, dtype=torch.int32).to(dev)
+        mask = torch.ones(n, dtype=torch.uint8, device=dev)
+        old = torch.full((n,), -10.0, device=dev)
+        adv = torch.randn(n // T, generator=g).to(dev)
+        ws = clp.alloc_workspace(n, D, V, T, params, dev)
+        loss = torch.empty(1, device=dev)
+        logp = torch.empty(n, device=dev)
+        dH = torch.empty(n, D, dtype=torch.bfloat16, device=dev)
+        clp.grpo_loss_fwd_bwd(hidden, W, ids, mask, old, old, adv, T, params=params,
+                              workspace=ws, loss=loss, logp=logp, dH=dH)
+        torch.cuda.synchronize()
+        free0, _ = torch.cuda.mem_get_info(dev)
+        for _ in range(2):
+            clp.grpo_loss_fwd_bwd(hidden, W, ids, mask, old, old, adv, T, params=params,
+                                  workspace=ws, loss=loss, logp=logp, dH=dH)
+        torch.cuda.synchronize()
+        free1, _ = torch.cuda.mem_get_info(dev)
+        assert free1 == free0, (n, free0 - free1)
+        assert clp.grpo_read_device_status(ws) == 0 and math.isfinite(loss.item())
+        sizes[n] = ws.numel()
+        print(f"flags={flags} N={n}: workspace {ws.numel() / 2**20:.1f} MiB, "
+              f"fp32 N x V logits would be {n * V * 4 / 2**20:.0f} MiB")
+        del hidden, W, ids, mask, old, adv, ws, loss, logp, dH
+    per_row = (sizes[65536] - sizes[4096]) / (65536 - 4096)
+    assert per_row < 1024  # a few fp32 / fp64 words and the split partials per row
+    assert sizes[65536] < 65536 * V * 4 / 20
