@@ -608,3 +608,30 @@ def test_device_memory_is_the_workspace_only(clp, flags):
     per_row = (sizes[65536] - sizes[4096]) / (65536 - 4096)
     assert per_row < 1024  # a few fp32 / fp64 words and the split partials per row
     assert sizes[65536] < 65536 * V * 4 / 20
+
+
+# Vocabulary edges through every backward form: V = 1 (logp = 0, G = 0),
+# V = 7 (a stored row narrower than one 16-byte chunk), V = 65 (one column
+# past a 64-wide K slice); D = 256 forms G in the dH GEMM, D = 2304 in its own
+# pass; flags 0 is the recomputed backward.
+@pytest.mark.parametrize("flags", [0, STORED])
+@pytest.mark.parametrize("D", [256, 2304])
+@pytest.mark.parametrize("V", [1, 7, 65])
+def test_small_vocab_edges(clp, flags, D, V):
+    p = synth.make_problem("tiny", seed=V * 7 + D, prompts=1, G=4, T=32, D=D, V=V,
+                           lengths=(5, 32), weight_std=0.3)
+    old, ref, want = oracle_case(p)
+    params = clp.make_params(flags=flags)
+    check(gpu_loss(clp, p, old, ref, params), want, p.mask, f"V={V} D={D} flags={flags}")
+
+
+@pytest.mark.parametrize("flags", [STORED, STORED | SINGLE])
+def test_empty_batch_stored(clp, flags):
+    h = torch.empty(0, 64, dtype=torch.bfloat16, device=DEV)
+    W = torch.randn(100, 64, device=DEV).to(torch.bfloat16)
+    e = torch.empty(0, dtype=torch.int32, device=DEV)
+    f = torch.empty(0, dtype=torch.float32, device=DEV)
+    loss, logp, dH = clp.grpo_loss_fwd_bwd(h, W, e, torch.empty(0, dtype=torch.uint8, device=DEV),
+                                           f, f, torch.empty(0, dtype=torch.float32, device=DEV),
+                                           1, params=clp.make_params(flags=flags))
+    assert loss.item() == 0.0 and dH.numel() == 0
