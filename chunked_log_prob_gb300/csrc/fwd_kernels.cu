@@ -372,6 +372,43 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
     for (int i = threadIdx.x; i < n_vec; i += blockDim.x) row[i] = make_uint4(0, 0, 0, 0);
     return;
   }
+  if (a.xmode == 0) {
+    // Without a transform: -g 2^(z log2e - lse2) = -sign(g) 2^(z log2e + log2|g| - lse2),
+    // one FFMA and one exponential per logit and the sign set on each packed
+    // pair; the target column and the padding past the vocabulary are fixed
+    // up afterwards.
+    const float c = log2f(fabsf(g)) - lse2;
+    const uint32_t sgn = g > 0.f ? 0x80008000u : 0u;
+    auto fast = [&](const uint4 in) {
+      const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float z0, z1;
+        unpack_f16x2(w[k], z0, z1);
+        o[k] = pack_bf16x2(ex2(fmaf(z0, kLog2e, c)), ex2(fmaf(z1, kLog2e, c))) ^ sgn;
+      }
+      return make_uint4(o[0], o[1], o[2], o[3]);
+    };
+    const int step = 2 * blockDim.x;
+    int i = threadIdx.x;
+    for (; i + blockDim.x < n_vec; i += step) {
+      const uint4 in0 = row[i];
+      const uint4 in1 = row[i + blockDim.x];
+      row[i] = fast(in0);
+      row[i + blockDim.x] = fast(in1);
+    }
+    if (i < n_vec) row[i] = fast(row[i]);
+    __syncthreads();  // the whole row is written before the fix-ups
+    uint16_t* row16 = a.S + static_cast<long long>(lrow) * a.ldS;
+    if (threadIdx.x == 0 && y >= 0) {
+      // Target column: g (1 - p_y), from the forward's fp32 target logit.
+      const float val = g - g * ex2(fmaf(a.zy[grow], kLog2e, -lse2));
+      row16[y] = static_cast<uint16_t>(pack_bf16x2(val, 0.f) & 0xffffu);
+    }
+    if (threadIdx.x < a.ldS - a.vocab) row16[a.vocab + threadIdx.x] = 0;
+    return;
+  }
   const float ng = -g;
   // G_v from the stored z'_v: g (onehot_v(y) - exp(z'_v - lse)) f'(z_v).
   auto convert = [&](const uint4 in, int i) {
