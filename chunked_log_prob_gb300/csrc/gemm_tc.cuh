@@ -184,7 +184,7 @@ __device__ __forceinline__ int swz_offset(int r, int c) {
 template <int NCH>
 __device__ __forceinline__ void logits_to_g_row(const TileArgs& a, uint8_t* tile, int r, int jb,
                                                 int vbase, int y, float g, float lse2,
-                                                float zy) {
+                                                float zy, float c, uint32_t sgn) {
   uint4* row = reinterpret_cast<uint4*>(tile + r * 128);
   const int sw = r & 7;
   if (g == 0.f) {
@@ -203,9 +203,10 @@ __device__ __forceinline__ void logits_to_g_row(const TileArgs& a, uint8_t* tile
       uint32_t o[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
+        // -g 2^(z log2e - lse2) = -sign(g) 2^(z log2e + c), c = log2|g| - lse2
         float z0, z1;
         unpack_f16x2(w[e], z0, z1);
-        o[e] = pack_bf16x2(ng * ex2(fmaf(z0, kLog2e, -lse2)), ng * ex2(fmaf(z1, kLog2e, -lse2)));
+        o[e] = pack_bf16x2(ex2(fmaf(z0, kLog2e, c)), ex2(fmaf(z1, kLog2e, c))) ^ sgn;
       }
       row[(jb + j) ^ sw] = make_uint4(o[0], o[1], o[2], o[3]);
     }
@@ -620,6 +621,8 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
       int y = -1;
       float lse2 = 0.f, gval = 0.f;      // BWDG, DHS
       float zyv = 0.f;                   // DHS: fp32 target logit
+      float cexp = 0.f;                  // DHS: log2|g| - lse2
+      uint32_t sgn = 0u;                 // DHS: sign bits of -g on a bf16 pair
       if (is_fwd(MODE)) {
         if (valid && (args.mask == nullptr || args.mask[grow] != 0)) y = args.ids[grow];
       } else if (MODE == MODE_BWDG || MODE == MODE_DHS) {
@@ -628,7 +631,11 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
           lse2 = args.lse[grow] * kLog2e;
           if (gval != 0.f) {
             y = args.ids[grow];
-            if (MODE == MODE_DHS) zyv = args.zy[grow];
+            if (MODE == MODE_DHS) {
+              zyv = args.zy[grow];
+              cexp = log2f(fabsf(gval)) - lse2;
+              sgn = gval > 0.f ? 0x80008000u : 0u;
+            }
           }
         }
       }
@@ -644,7 +651,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
           }
           constexpr int kNch = 8 / C::kCvtGroups;
           logits_to_g_row<kNch>(args, smem + s * C::kStageBytes, lrow_in_tile, part * kNch,
-                                args.v0 + k * BK, y, gval, lse2, zyv);
+                                args.v0 + k * BK, y, gval, lse2, zyv, cexp, sgn);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
