@@ -635,3 +635,18 @@ def test_empty_batch_stored(clp, flags):
                                            f, f, torch.empty(0, dtype=torch.float32, device=DEV),
                                            1, params=clp.make_params(flags=flags))
     assert loss.item() == 0.0 and dH.numel() == 0
+
+
+# Smallest legal shapes: hidden sizes far below one 64-wide K slice (D = 8,
+# 24), a single token, and D = 2056 (just past the size up to which G is
+# formed in the dH GEMM, and not a multiple of 64); every backward form.
+@pytest.mark.parametrize("flags", [0, STORED, STORED | SINGLE])
+@pytest.mark.parametrize("N,D", [(1, 8), (3, 24), (130, 8), (70, 2056)])
+def test_tiny_hidden_and_single_token(clp, flags, N, D):
+    p = synth.make_problem("tiny", seed=N * 31 + D, prompts=1, G=1, T=N, D=D, V=300,
+                           weight_std=0.5 if D < 64 else 0.05)
+    old, ref, want = oracle_case(p)
+    params = clp.make_params(flags=flags)
+    check(gpu_loss(clp, p, old, ref, params), want, p.mask, f"N={N} D={D} flags={flags}")
+    lp, _ = clp.grpo_logp_fwd(_to(p.hidden), _to(p.weight), _to(p.ids), params=params)
+    assert np.abs(lp.cpu().double().numpy() - want["logp"]).max() <= LOGP_TOL
