@@ -195,15 +195,42 @@ def oracle_rows_per_second(p, target_s, seed, cores_note):
     return n, t
 
 
+def code_tokens(src):
+    """C/C++/CUDA source without comments and with whitespace collapsed."""
+    import re
+
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":  # string or character literal, kept verbatim
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return re.sub(r"\s+", " ", "".join(out)).strip()
+
+
 def kernel_source_hash():
-    """Hash of the CUDA sources: DRAM traffic recorded for other sources is stale."""
+    """Hash of the CUDA sources' code (comments and layout ignored): DRAM traffic
+    recorded for other code is stale."""
     import hashlib
 
     csrc = os.path.join(ROOT, "chunked_log_prob_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -25,9 +25,10 @@ constexpr size_t kMaxStoredChunkBytes = size_t(2) << 30;    // 2 GiB of fp16 log
 // GEMM (MODE_DHS) rather than in a pass of its own over the logit block.
 // Measured on GB300: the separate pass costs about 1/D of the dH GEMM and
 // mostly hides behind the next chunk's GEMMs; the in-GEMM conversion costs a
-// roughly constant share of the dH GEMM (its shared-memory traffic competes
-// with the CTA-pair MMA operand reads). At D = 1536 fusing is 7-12 % faster
-// per call, at D = 2880 and 4096 the overlapped separate pass is faster.
+// roughly constant share of the dH GEMM (the exponential and conversions per
+// logit on its converter warps, measured: not its shared-memory traffic). At
+// D = 1536 fusing is 7-12 % faster per call, at D = 2880 and 4096 the
+// overlapped separate pass is faster.
 constexpr int kFusedMaxHidden = 2048;
 constexpr int kSplitsTarget = 8;        // forward vocab splits per raster group
 constexpr size_t kHeaderBytes = 16384;   // status, counters, loss partials
