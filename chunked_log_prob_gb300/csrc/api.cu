@@ -10,6 +10,8 @@
 #include <mutex>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "grpo_gb300.h"
 #include "launch.h"
 
@@ -44,6 +46,15 @@ constexpr size_t kOffPartials = 64;    // double[kMaxFinalizeBlocks]
 static_assert(kOffPartials + kMaxFinalizeBlocks * sizeof(double) <= kHeaderBytes, "header");
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// An NVTX range around one ABI call (host side: it brackets the enqueueing of
+// the call's launches), so that profilers can attribute the kernels to it.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
 // D columns per dH unit, in units of 256: the pair kernel covers 512.
@@ -900,6 +911,7 @@ int grpo_workspace_size(const grpo_shape* shape, const grpo_params* params, size
 int grpo_logp_fwd(const void* hidden, const void* W, const int32_t* ids, float* logp,
                   float* lse_or_null, const grpo_shape* shape, const grpo_params* params,
                   void* workspace, size_t workspace_bytes, void* stream) {
+  const NvtxRange range("grpo_logp_fwd");
   int r = check_shape(shape, false);
   if (r != GRPO_OK) return r;
   if ((r = check_params(params)) != GRPO_OK) return r;
@@ -945,6 +957,7 @@ int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
                       const float* adv, float* loss, float* logp_or_null, void* dH,
                       float* dW_or_null, const grpo_shape* shape, const grpo_params* params,
                       void* workspace, size_t workspace_bytes, void* stream) {
+  const NvtxRange range("grpo_loss_fwd_bwd");
   int r = check_shape(shape, true);
   if (r != GRPO_OK) return r;
   if ((r = check_params(params)) != GRPO_OK) return r;
@@ -1142,6 +1155,7 @@ int noalloc_scratch(void** out) {
 extern "C" int grpo_logp_fwd_noalloc(const void* hidden, const void* W, const int32_t* ids,
                                      float* logp, float* lse_or_null, const grpo_shape* shape,
                                      void* stream) {
+  const NvtxRange range("grpo_logp_fwd_noalloc");
   int r = check_shape(shape, false);
   if (r != GRPO_OK) return r;
   if (shape->n_tokens > GRPO_NOALLOC_MAX_TOKENS) return GRPO_ERR_UNSUPPORTED_SHAPE;

@@ -650,3 +650,50 @@ def test_tiny_hidden_and_single_token(clp, flags, N, D):
     check(gpu_loss(clp, p, old, ref, params), want, p.mask, f"N={N} D={D} flags={flags}")
     lp, _ = clp.grpo_logp_fwd(_to(p.hidden), _to(p.weight), _to(p.ids), params=params)
     assert np.abs(lp.cpu().double().numpy() - want["logp"]).max() <= LOGP_TOL
+
+
+def _guarded(n, dtype, fill, guard):
+    # A tensor of n elements inside a buffer of guard elements on each side,
+    # everything set to `fill` (so writes outside the view can be detected).
+    buf = torch.full((n + 2 * guard,), fill, dtype=dtype, device=DEV)
+    return buf, buf[guard:guard + n]
+
+
+# No write outside the output buffers and no read of uninitialised workspace:
+# every output is a view inside a buffer of sentinels, and the workspace is
+# prefilled with 0xFF bytes (NaN in every float format) inside its own guard
+# band. Results must still match the oracle and every sentinel must survive.
+@pytest.mark.parametrize("flags", [0, STORED, STORED | SINGLE])
+@pytest.mark.parametrize("D", [256, 2304])
+@pytest.mark.parametrize("with_dw", [False, True])
+def test_guard_bands_and_poisoned_workspace(clp, flags, D, with_dw):
+    p = synth.make_problem("tiny", seed=D + flags, prompts=1, G=4, T=75, D=D, V=1000,
+                           lengths=(20, 75))
+    old, ref, want = oracle_case(p)
+    N, V = p.n_tokens, p.vocab
+    params = clp.make_params(chunk_tokens=128, flags=flags)
+    g = 4096
+    lb, loss = _guarded(1, torch.float32, 7.0, g)
+    pb, logp = _guarded(N, torch.float32, 7.0, g)
+    hb, dH = _guarded(N * D, torch.bfloat16, 7.0, g)
+    dH = dH.view(N, D)
+    wb, dW = _guarded(V * D, torch.float32, 7.0, g) if with_dw else (None, None)
+    if dW is not None:
+        dW = dW.view(V, D)
+    size = clp.grpo_workspace_size(N, D, V, p.seq_len, params)
+    wsb = torch.full((size + 2 * g,), 0xFF, dtype=torch.uint8, device=DEV)
+    ws = wsb[g:g + size]
+    out = clp.grpo_loss_fwd_bwd(_to(p.hidden), _to(p.weight), _to(p.ids), _to(p.mask), _to(old),
+                                _to(ref), _to(p.adv), p.seq_len, params=params, workspace=ws,
+                                loss=loss, logp=logp, dH=dH, dW=dW)
+    st = clp.grpo_read_device_status(ws)
+    check((loss.item(), logp.cpu().double().numpy(), dH.cpu().double().numpy(), st), want,
+          p.mask, f"guarded D={D} flags={flags} dW={with_dw}")
+    for name, buf, n in (("loss", lb, 1), ("logp", pb, N), ("dH", hb, N * D)) + (
+            (("dW", wb, V * D),) if with_dw else ()):
+        assert torch.all(buf[:g] == 7.0) and torch.all(buf[g + n:] == 7.0), name
+    assert torch.all(wsb[:g] == 0xFF) and torch.all(wsb[g + size:] == 0xFF)
+    if with_dw:
+        want_dW = oracle.grad_weight(p.hidden, p.weight, p.ids.numpy(), want["g"])
+        got = out[3].cpu().double().numpy()
+        assert np.linalg.norm(got - want_dW) <= DH_RTOL * np.linalg.norm(want_dW)
