@@ -163,8 +163,13 @@ def flops_per_token(D, V):
     return 6.0 * D * V
 
 
-def oracle_rows_per_second(p, target_s, seed, cores_note):
-    """Time the fp64 oracle on a seeded sample of valid rows of workload `p`."""
+def oracle_rows_per_second(p, target_s, seed, cores_note, gpu=None):
+    """Time the fp64 oracle on a seeded sample of valid rows of workload `p`.
+
+    gpu = (old, ref, logp, dH) of a GPU call on the same inputs: the oracle
+    then runs with that call's old/ref log-probs, and its rows are compared
+    with the call's logp and dH (each row is exact given the loss
+    denominator). Returns (rows, seconds, parity dict or None)."""
     import numpy as np
     import torch
 
@@ -175,24 +180,38 @@ def oracle_rows_per_second(p, target_s, seed, cores_note):
     W64 = p.weight.float().cpu().numpy().astype(np.float64)  # input preparation
     h = p.hidden.cpu()
     ids = p.ids.cpu().numpy()
-    base = torch.full((p.n_tokens,), -math.log(p.vocab))
-    old, ref = (x.cpu() for x in p.old_ref(base.to(p.old_noise.device)))
+    if gpu is None:
+        base = torch.full((p.n_tokens,), -math.log(p.vocab))
+        old, ref = (x.cpu() for x in p.old_ref(base.to(p.old_noise.device)))
+    else:
+        old, ref = gpu[0].cpu(), gpu[1].cpu()
     adv = p.adv.cpu()
     M = float(len(valid))
 
     def run(n_rows):
         rows = np.sort(rng.choice(valid, size=min(n_rows, len(valid)), replace=False))
         t0 = time.perf_counter()
-        oracle.rows_fwd_bwd(h, W64, ids, rows, old, ref, adv, p.seq_len, M,
-                            p.eps_low, p.eps_high, p.beta)
-        return len(rows), time.perf_counter() - t0
+        out = oracle.rows_fwd_bwd(h, W64, ids, rows, old, ref, adv, p.seq_len, M,
+                                  p.eps_low, p.eps_high, p.beta)
+        return rows, time.perf_counter() - t0, out
 
     run(4)  # the first call pays one-time costs (thread pool start-up, page-in)
-    n0, t0 = run(24)
-    per_row = t0 / n0
+    rows0, t0, _ = run(24)
+    per_row = t0 / len(rows0)
     n_rows = int(max(8, min(len(valid), target_s / max(per_row, 1e-6))))
-    n, t = run(n_rows)
-    return n, t
+    rows, t, want = run(n_rows)
+    parity = None
+    if gpu is not None:
+        idx = torch.from_numpy(rows)
+        got_lp = gpu[2].cpu().double()[idx].numpy()
+        got_dh = gpu[3][idx.to(gpu[3].device)].double().cpu().numpy()
+        parity = {
+            "rows": len(rows),
+            "max_abs_dlogp": float(np.abs(got_lp - want["logp"]).max()),
+            "rel_fro_dH": float(np.linalg.norm(got_dh - want["dH"]) /
+                                np.linalg.norm(want["dH"])),
+            "gates": "|dlogp| <= 1e-2, rel dH <= 2e-2"}
+    return len(rows), t, parity
 
 
 def code_tokens(src):
@@ -493,11 +512,15 @@ def run_ours(args):
         "cpu_baseline": None,
     }
     if world == 1 and not args.no_cpu_baseline:
-        n, t = oracle_rows_per_second(p, args.cpu_seconds, args.seed, None)
+        step()  # the outputs of one headline call, for the parity check
+        torch.cuda.synchronize(dev)
+        n, t, parity = oracle_rows_per_second(p, args.cpu_seconds, args.seed, None,
+                                              gpu=(old, ref, logp, dH))
         out["cpu_baseline"] = {
             "value": n / t, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
             "sample": f"{n} seeded valid rows of {p.name} (logp, g, dH per row; 6DV fp64 "
-                      f"flops each), {t:.1f} s on the host cores (numpy/OpenBLAS threads)"}
+                      f"flops each), {t:.1f} s on the host cores (numpy/OpenBLAS threads)",
+            "parity_vs_gpu": parity}
     print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()
