@@ -21,6 +21,7 @@ import argparse
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -59,6 +60,13 @@ def parse_args():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--record-traffic", metavar="CSV", default=None,
+                    help="no benchmark: turn an ncu launch list (--csv, with "
+                         "gpu__time_duration.sum, dram__bytes_read.sum and "
+                         "dram__bytes_write.sum) of this bench's calls into "
+                         "profiles/traffic_<workload>_<backward>.json")
+    ap.add_argument("--record-command", default="",
+                    help="the command that made --record-traffic's CSV (kept in the record)")
     return ap.parse_args()
 
 
@@ -216,7 +224,6 @@ def oracle_rows_per_second(p, target_s, seed, cores_note, gpu=None):
 
 def code_tokens(src):
     """C/C++/CUDA source without comments and with whitespace collapsed."""
-    import re
 
     out, i, n = [], 0, len(src)
     while i < n:
@@ -253,17 +260,135 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
+def traffic_path(workload, backward):
+    return os.path.join(ROOT, "profiles", f"traffic_{workload}_{backward}.json")
+
+
 def recorded_traffic(workload, backward):
-    """DRAM bytes per call from a committed ncu summary, if it matches these sources."""
-    path = os.path.join(ROOT, "profiles", f"traffic_{workload}_{backward}.json")
+    """The committed ncu DRAM record of one call, if it matches these sources."""
     try:
-        with open(path) as f:
+        with open(traffic_path(workload, backward)) as f:
             rec = json.load(f)
     except Exception:
         return None
     if rec.get("kernel_source_hash") != kernel_source_hash():
         return None
-    return rec.get("dram_bytes_per_call")
+    return rec
+
+
+_NCU_SCALE = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12,
+              "ns": 1e-6, "nsecond": 1e-6, "us": 1e-3, "usecond": 1e-3, "ms": 1.0,
+              "msecond": 1.0, "s": 1e3, "second": 1e3}
+_FIRST_KERNEL = "row_plan_kernel"  # every grpo_loss_fwd_bwd call starts with it
+
+
+def ncu_calls(csv_path):
+    """Split an ncu --csv launch list into the library's calls.
+
+    Returns a list of calls, each a list of launches {"name", "read", "write",
+    "ms"} (bytes, milliseconds). A call runs from one row_plan_kernel launch up
+    to the next; launches of other code (torch's own kernels) are dropped, and
+    so is the last call, which the capture limit may have cut short."""
+    import csv
+
+    with open(csv_path, newline="") as f:
+        rows = list(csv.reader(f))
+    head = next(i for i, r in enumerate(rows) if "Kernel Name" in r and "Metric Name" in r)
+    h = rows[head]
+    col = {k: h.index(k) for k in ("ID", "Kernel Name", "Metric Name", "Metric Unit",
+                                   "Metric Value")}
+    launches = {}
+    for r in rows[head + 1:]:
+        if len(r) < len(h):
+            continue
+        d = launches.setdefault(int(r[col["ID"]]), {"name": r[col["Kernel Name"]]})
+        d[r[col["Metric Name"]]] = (float(r[col["Metric Value"]].replace(",", ""))
+                                    * _NCU_SCALE[r[col["Metric Unit"]]])
+    seq = []
+    for i in sorted(launches):
+        d = launches[i]
+        if "grpo::" not in d["name"]:
+            continue
+        name = d["name"].replace("(int)", "").split("(")[0]
+        name = name.replace("void ", "").replace("grpo::", "").strip()
+        seq.append({"name": name, "read": d.get("dram__bytes_read.sum", 0.0),
+                    "write": d.get("dram__bytes_write.sum", 0.0),
+                    "ms": d.get("gpu__time_duration.sum", 0.0)})
+    starts = [i for i, d in enumerate(seq) if d["name"] == _FIRST_KERNEL]
+    return [seq[a:b] for a, b in zip(starts, starts[1:])]
+
+
+def record_traffic(csv_path, workload, backward, command):
+    """Write the DRAM record of the last complete call in an ncu launch list."""
+    calls = ncu_calls(csv_path)
+    if not calls:
+        raise SystemExit(f"{csv_path}: no complete grpo_loss_fwd_bwd call")
+    call = calls[-1]
+    per = {}
+    for d in call:
+        e = per.setdefault(d["name"], {"launches": 0, "read_bytes": 0.0, "write_bytes": 0.0,
+                                       "time_ms": 0.0})
+        e["launches"] += 1
+        e["read_bytes"] += d["read"]
+        e["write_bytes"] += d["write"]
+        e["time_ms"] += d["ms"]
+    rd, wr = sum(d["read"] for d in call), sum(d["write"] for d in call)
+    rec = {"workload": workload, "backward": backward, "dram_bytes_per_call": rd + wr,
+           "dram_read_bytes": rd, "dram_write_bytes": wr, "launches_per_call": len(call),
+           "ncu_time_ms_per_call": sum(d["ms"] for d in call), "per_kernel": per,
+           "command": command, "kernel_source_hash": kernel_source_hash()}
+    with open(traffic_path(workload, backward), "w") as f:
+        json.dump(rec, f, indent=1)
+    return rec
+
+
+def kernel_work(name, D, V):
+    """Algorithmic work of one kernel kind per valid token: (bound, amount, unit)."""
+    if name.startswith("tc_gemm_kernel"):
+        return "tensor", 2.0 * D * V, "flop"  # one pass of the N x V x D contraction
+    if name == "finalize_gform_kernel":
+        return "hbm", 4.0 * V, "byte"  # fp16 logit row in, bf16 G row out
+    return None
+
+
+def kernel_roofline(times, calls, D, V, valid, peaks, rec):
+    """Roofline of the kernel with the most device time over `calls` calls.
+
+    times: per-kernel sums from the library's launch timing (CUDA events on
+    each launch's own stream). A launch's algorithmic work is the kind's work
+    per valid token x the valid tokens of a call / its launches per call."""
+    if not times:
+        return None
+    summed = sum(k["total_ms"] for k in times)
+    per_kernel = [{"name": k["name"], "launches_per_call": k["launches"] / calls,
+                   "avg_launch_ms": k["total_ms"] / k["launches"],
+                   "ms_per_call": k["total_ms"] / calls,
+                   "share": k["total_ms"] / summed}
+                  for k in sorted(times, key=lambda k: -k["total_ms"])]
+    top = per_kernel[0]
+    out = {"kernel": top["name"], "avg_launch_ms": top["avg_launch_ms"],
+           "launches_per_call": top["launches_per_call"], "share": top["share"]}
+    traffic = None
+    if rec is not None and top["name"] in rec.get("per_kernel", {}):
+        e = rec["per_kernel"][top["name"]]
+        traffic = (e["read_bytes"] + e["write_bytes"]) / e["launches"]
+    work = kernel_work(top["name"], D, V)
+    if work is None:
+        out.update({"bound": None, "achieved": None, "peak": None, "unit": None,
+                    "frac": None, "traffic": traffic})
+    else:
+        bound, per_token, unit = work
+        per_launch = per_token * valid / top["launches_per_call"]
+        rate = per_launch / (top["avg_launch_ms"] / 1e3)
+        if bound == "tensor":
+            achieved, peak, u = rate / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
+        else:
+            achieved, peak, u = rate / 1e9, peaks["hbm_gbs"], "GB/s"
+        out.update({"bound": bound, "achieved": achieved, "peak": peak, "unit": u,
+                    "frac": achieved / peak, "traffic": traffic,
+                    f"algorithmic_{unit}s_per_launch": per_launch})
+    out["per_kernel"] = per_kernel
+    return out
 
 
 def cpu_cores():
@@ -334,19 +459,35 @@ def run_ours(args):
     gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
     gpu_id = f"GPU-{gpu_id}" if gpu_id is not None else str(local)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # Per-kernel device times over the timed calls: the library brackets each
+    # launch with CUDA events on that launch's own stream (the caller's or its
+    # side stream) and sums them per kernel (64K launches at most per read).
+    launches_est = plan["launches_loss"] + (plan["n_chunks"] * plan["n_vocab_blocks"]
+                                            if args.with_dw else 0)
+    timed_calls = args.steps if args.steps * launches_est <= 60000 else 0
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(gpu_id) as clocks:
         time.sleep(0.3)  # let the sampler start
+        clp.grpo_launch_timing_enable(timed_calls > 0)
         ev0.record(stream)
         for _ in range(args.steps):
             step()
         ev1.record(stream)
         torch.cuda.synchronize(dev)
+        clp.grpo_launch_timing_enable(False)
     if world > 1:
         dist.barrier()
     ms_max = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+    if timed_calls == 0:  # too many launches for one read: time 10 calls of their own
+        timed_calls = 10
+        clp.grpo_launch_timing_enable(True)
+        for _ in range(timed_calls):
+            step()
+        torch.cuda.synchronize(dev)
+        clp.grpo_launch_timing_enable(False)
+    kernel_times = clp.grpo_launch_timing_read()
 
     # The other backward variant on the same inputs (reported beside the headline).
     variant = None
@@ -460,6 +601,24 @@ def run_ours(args):
     tflops_exec = fl_exec / (ms_max / 1e3) / 1e12
     peak_sus = peaks["bf16_tflops_sustained"]
     peak_burst = peaks["bf16_tflops"]
+    rec = recorded_traffic(p.name, "stored" if stored else "recompute")
+    # The dominant kernel (most device time), timed live; its peak is the
+    # sustained one, as it runs inside a long step. The call as a whole beside it.
+    roofline = kernel_roofline(kernel_times, timed_calls, D, V, valid, peaks, rec) or {}
+    roofline["peak_source"] = "%s (%s)" % (peak_src, "bf16 sustained cuBLAS loop" if roofline.get(
+        "bound") == "tensor" else "STREAM-style copy")
+    roofline["timing"] = ("CUDA events recorded by the library around each launch on the "
+                          "launch's own stream, over the %d timed calls" % timed_calls)
+    roofline["traffic_unit"] = "DRAM bytes per launch (ncu dram__bytes_read.sum + write.sum)"
+    roofline["call"] = {
+        "scope": "grpo_loss_fwd_bwd: %d launches per call, %d chunks x %d vocab blocks" % (
+            plan["launches_loss"], plan["n_chunks"], plan["n_vocab_blocks"]),
+        "bound": "tensor", "achieved": tflops_exec, "peak": peak_sus, "unit": "TFLOP/s",
+        "frac": tflops_exec / peak_sus, "frac_of_burst_peak": tflops_exec / peak_burst,
+        "counted_tflops_6NDV": tflops, "flops_per_call": fl_exec,
+        "traffic": None if rec is None else rec.get("dram_bytes_per_call"),
+        "traffic_unit": "DRAM bytes per call"}
+    launches_per_call = sum(k["launches"] for k in kernel_times) / timed_calls
     out = {
         "metric": METRIC,
         "value": world * valid / (ms_max / 1e3),
@@ -489,25 +648,16 @@ def run_ours(args):
             and not args.with_dw else ", G formed in its own pass" if stored else "") + (
             " + lm_head dW" if args.with_dw else ""),
         "variant": variant,
-        "roofline": {
-            "bound": "tensor", "achieved": tflops_exec, "peak": peak_sus, "unit": "TFLOP/s",
-            "frac": tflops_exec / peak_sus, "frac_of_burst_peak": tflops_exec / peak_burst,
-            "counted_tflops_6NDV": tflops,
-            "peak_source": f"{peak_src} bf16 sustained (cuBLAS loop)",
-            "kernel": "grpo_loss_fwd_bwd: %d launches per call, %d chunks x %d vocab blocks" % (
-                plan["launches_loss"], plan["n_chunks"], plan["n_vocab_blocks"]),
-            "flops_per_call": fl_exec,
-            "traffic": recorded_traffic(p.name, "stored" if stored else "recompute"),
-            "traffic_unit": "DRAM bytes per call (ncu dram__bytes_read.sum + write.sum)",
-        },
+        "roofline": roofline,
         "fwd_only": None if fwd_ms is None else {
             "ms": fwd_ms, "tflops": 2.0 * D * V * N / (fwd_ms / 1e3) / 1e12,
             "frac_of_burst_peak": 2.0 * D * V * N / (fwd_ms / 1e3) / 1e12 / peak_burst,
             "scope": "grpo_logp_fwd: logit GEMM + finalize over all N rows"},
         "e2e": e2e,
         "clocks": clocks.summary(),
-        "gpu_launches": (plan["launches_loss"] + (plan["n_chunks"] * plan["n_vocab_blocks"]
-                                                  if args.with_dw else 0)) * args.steps,
+        "gpu_launches": launches_per_call * args.steps,
+        "gpu_launches_source": "counted by the library's launch timing (%g per call)" % (
+            launches_per_call),
         "workspace_bytes": plan["workspace_bytes"],
         "cpu_baseline": None,
     }
@@ -582,7 +732,11 @@ def run_reference(args):
 
 if __name__ == "__main__":
     a = parse_args()
-    if a.impl == "reference":
+    if a.record_traffic:
+        r = record_traffic(a.record_traffic, a.workload, a.backward, a.record_command)
+        print(json.dumps({k: r[k] for k in ("workload", "backward", "dram_bytes_per_call",
+                                            "launches_per_call", "ncu_time_ms_per_call")}))
+    elif a.impl == "reference":
         run_reference(a)
     else:
         run_ours(a)

@@ -13,6 +13,8 @@ from ._binding import (  # noqa: F401
     GrpoShape,
     alloc_workspace,
     grpo_get_plan,
+    grpo_launch_timing_enable,
+    grpo_launch_timing_read,
     grpo_logp_fwd,
     grpo_logp_fwd_noalloc,
     grpo_loss_fwd_bwd,

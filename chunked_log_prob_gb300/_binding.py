@@ -54,6 +54,11 @@ class GrpoError(RuntimeError):
         super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} ({status_string(code)})")
 
 
+class GrpoKernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 40), ("launches", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("total_ms", ctypes.c_double)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -78,6 +83,10 @@ def _load():
     lib.grpo_logp_fwd_noalloc.restype = ctypes.c_int
     lib.grpo_selftest_bounded_wait.argtypes = [vp, sz, vp]
     lib.grpo_selftest_bounded_wait.restype = ctypes.c_int
+    lib.grpo_launch_timing_enable.argtypes = [ctypes.c_int]
+    lib.grpo_launch_timing_enable.restype = ctypes.c_int
+    lib.grpo_launch_timing_read.argtypes = [P(GrpoKernelTime), ctypes.c_int, P(ctypes.c_int)]
+    lib.grpo_launch_timing_read.restype = ctypes.c_int
     lib.grpo_status_string.argtypes = [ctypes.c_int]
     lib.grpo_status_string.restype = ctypes.c_char_p
     return lib
@@ -87,7 +96,8 @@ lib = _load()
 
 EXPORTED = ("grpo_default_params", "grpo_workspace_size", "grpo_logp_fwd",
             "grpo_loss_fwd_bwd", "grpo_get_plan", "grpo_read_device_status",
-            "grpo_logp_fwd_noalloc", "grpo_selftest_bounded_wait", "grpo_status_string")
+            "grpo_logp_fwd_noalloc", "grpo_selftest_bounded_wait", "grpo_launch_timing_enable",
+            "grpo_launch_timing_read", "grpo_status_string")
 
 FLAG_STORED_LOGITS = 1
 FLAG_SINGLE_CTA = 2
@@ -282,3 +292,24 @@ def grpo_selftest_bounded_wait(workspace) -> int:
     if rc != GRPO_OK:
         raise GrpoError(rc, "grpo_selftest_bounded_wait")
     return grpo_read_device_status(workspace)
+
+
+def grpo_launch_timing_enable(on: bool = True) -> None:
+    """Per-launch CUDA-event timing for the calling thread (off by default)."""
+    rc = lib.grpo_launch_timing_enable(1 if on else 0)
+    if rc != GRPO_OK:
+        raise GrpoError(rc, "grpo_launch_timing_enable")
+
+
+def grpo_launch_timing_read(capacity: int = 64) -> list[dict]:
+    """Waits for the timed launches, returns and clears their per-kernel sums:
+    ``[{"name", "launches", "total_ms"}]`` in order of first launch."""
+    buf = (GrpoKernelTime * capacity)()
+    count = ctypes.c_int(0)
+    rc = lib.grpo_launch_timing_read(buf, int(capacity), ctypes.byref(count))
+    if rc != GRPO_OK:
+        raise GrpoError(rc, "grpo_launch_timing_read")
+    if count.value > capacity:
+        raise GrpoError(-1, f"grpo_launch_timing_read: {count.value} kernels > capacity {capacity}")
+    return [{"name": buf[i].name.decode(), "launches": int(buf[i].launches),
+             "total_ms": float(buf[i].total_ms)} for i in range(count.value)]

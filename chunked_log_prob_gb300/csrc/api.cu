@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <climits>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -882,6 +883,115 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
 }
 
 }  // namespace
+
+// ---- Opt-in per-launch timing ------------------------------------------------
+namespace {
+
+constexpr size_t kMaxTimedLaunches = size_t(1) << 16;  // records kept between reads
+
+struct TimedLaunch {
+  char name[sizeof(grpo_kernel_time::name)];
+  int device;
+  cudaEvent_t start, stop;
+  bool complete;  // both events recorded
+};
+
+// Per host thread: the switch, the launches recorded since the last read and
+// a per-device pool of events for reuse (an event records only on streams of
+// the device it was created on).
+struct TimingState {
+  bool on = false;
+  std::vector<TimedLaunch> pending;
+  std::vector<cudaEvent_t> pool[kMaxDevices];
+
+  cudaEvent_t take(int dev) {
+    if (!pool[dev].empty()) {
+      cudaEvent_t e = pool[dev].back();
+      pool[dev].pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
+    return e;
+  }
+  void give(int dev, cudaEvent_t e) {
+    if (e != nullptr) pool[dev].push_back(e);
+  }
+  void release_pool() {
+    for (auto& p : pool) {
+      for (cudaEvent_t e : p) (void)cudaEventDestroy(e);
+      p.clear();
+    }
+  }
+  ~TimingState() {
+    for (TimedLaunch& r : pending) {
+      (void)cudaEventDestroy(r.start);
+      (void)cudaEventDestroy(r.stop);
+    }
+    release_pool();
+  }
+};
+
+thread_local TimingState t_timing;
+
+}  // namespace
+
+bool launch_timing_on() { return t_timing.on; }
+
+void LaunchTimer::begin(const char* name, cudaStream_t stream) {
+  TimingState& st = t_timing;
+  if (st.pending.size() >= kMaxTimedLaunches) return;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    (void)cudaGetLastError();
+    return;
+  }
+  TimedLaunch r = {};
+  std::snprintf(r.name, sizeof(r.name), "%s", name);
+  r.device = dev;
+  r.start = st.take(dev);
+  r.stop = st.take(dev);
+  if (r.start == nullptr || r.stop == nullptr || cudaEventRecord(r.start, stream) != cudaSuccess) {
+    (void)cudaGetLastError();  // keep the launcher's own error check clean
+    st.give(dev, r.start);
+    st.give(dev, r.stop);
+    return;
+  }
+  st.pending.push_back(r);
+  slot_ = static_cast<int>(st.pending.size() - 1);
+  stream_ = stream;
+}
+
+LaunchTimer::LaunchTimer(const char* name, cudaStream_t stream) {
+  if (t_timing.on) begin(name, stream);
+}
+
+LaunchTimer::LaunchTimer(int mode, int ctas, cudaStream_t stream) {
+  if (!t_timing.on) return;
+  char name[sizeof(grpo_kernel_time::name)];
+  std::snprintf(name, sizeof(name), "tc_gemm_kernel<%d, %d>", mode, ctas);
+  begin(name, stream);
+}
+
+LaunchTimer::~LaunchTimer() {
+  if (slot_ < 0) return;
+  TimedLaunch& r = t_timing.pending[static_cast<size_t>(slot_)];
+  if (cudaEventRecord(r.stop, stream_) == cudaSuccess) {
+    r.complete = true;
+  } else {
+    (void)cudaGetLastError();
+  }
+}
+
 }  // namespace grpo
 
 using namespace grpo;
@@ -1099,6 +1209,58 @@ int grpo_selftest_bounded_wait(void* workspace, size_t workspace_bytes, void* st
       cudaSuccess)
     return GRPO_ERR_CUDA;
   return GRPO_OK;
+}
+
+int grpo_launch_timing_enable(int on) {
+  t_timing.on = on != 0;
+  if (!t_timing.on && t_timing.pending.empty()) t_timing.release_pool();
+  return GRPO_OK;
+}
+
+int grpo_launch_timing_read(grpo_kernel_time* out, int capacity, int* count) {
+  if (count == nullptr || capacity < 0 || (capacity > 0 && out == nullptr)) {
+    return GRPO_ERR_INVALID_ARG;
+  }
+  TimingState& st = t_timing;
+  std::vector<grpo_kernel_time> agg;
+  int rc = GRPO_OK;
+  int prev_dev = -1;
+  if (!st.pending.empty() && cudaGetDevice(&prev_dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    prev_dev = -1;
+  }
+  for (TimedLaunch& r : st.pending) {
+    float ms = 0.0f;
+    cudaError_t e = r.complete ? cudaSuccess : cudaErrorNotReady;
+    if (e == cudaSuccess) e = cudaSetDevice(r.device);
+    if (e == cudaSuccess) e = cudaEventSynchronize(r.stop);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.start, r.stop);
+    if (e == cudaSuccess) {
+      auto it = std::find_if(agg.begin(), agg.end(), [&](const grpo_kernel_time& k) {
+        return std::strncmp(k.name, r.name, sizeof(k.name)) == 0;
+      });
+      if (it == agg.end()) {
+        grpo_kernel_time k = {};
+        std::memcpy(k.name, r.name, sizeof(k.name));
+        agg.push_back(k);
+        it = agg.end() - 1;
+      }
+      it->launches += 1;
+      it->total_ms += ms;
+    } else if (r.complete) {
+      (void)cudaGetLastError();
+      rc = GRPO_ERR_CUDA;
+    }
+    st.give(r.device, r.start);
+    st.give(r.device, r.stop);
+  }
+  st.pending.clear();
+  if (prev_dev >= 0) (void)cudaSetDevice(prev_dev);
+  if (!st.on) st.release_pool();
+  *count = static_cast<int>(agg.size());
+  const int n = std::min(capacity, static_cast<int>(agg.size()));
+  for (int i = 0; i < n; ++i) out[i] = agg[static_cast<size_t>(i)];
+  return rc;
 }
 
 const char* grpo_status_string(int s) {

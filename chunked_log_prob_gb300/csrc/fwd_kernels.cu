@@ -242,6 +242,7 @@ cudaError_t launch_seq_lens(const uint8_t* mask, long long n, int seq_len, int* 
                             int* n_nonempty, cudaStream_t stream) {
   const long long n_seq = n / seq_len;
   if (n_seq <= 0) return cudaSuccess;
+  LaunchTimer timer("seq_lens_kernel", stream);
   seq_lens_kernel<<<static_cast<int>(std::min<long long>(n_seq, 4096)), 256, 0, stream>>>(
       mask, n, seq_len, lens, n_nonempty);
   return cudaGetLastError();
@@ -249,6 +250,7 @@ cudaError_t launch_seq_lens(const uint8_t* mask, long long n, int seq_len, int* 
 
 cudaError_t launch_row_plan(const uint8_t* mask, long long n, int n_rb, int* rb_list,
                             int* n_active, double* msum, cudaStream_t stream) {
+  LaunchTimer timer("row_plan_kernel", stream);
   row_plan_kernel<<<1, 1024, 0, stream>>>(mask, n, n_rb, rb_list, n_active, msum);
   return cudaGetLastError();
 }
@@ -257,6 +259,7 @@ cudaError_t launch_zero_padding_blocks(const uint8_t* mask, long long n, int n_r
                                        void* dH, int sms, cudaStream_t stream) {
   if (mask == nullptr || n_rb <= 0) return cudaSuccess;
   const int grid = std::min(n_rb, 4 * std::max(sms, 1));
+  LaunchTimer timer("zero_padding_blocks_kernel", stream);
   zero_padding_blocks_kernel<<<grid, 256, 0, stream>>>(mask, n, n_rb, hidden,
                                                        static_cast<__nv_bfloat16*>(dH));
   return cudaGetLastError();
@@ -266,6 +269,7 @@ cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t stream) {
   long long blocks = (a.n + kFinalizeThreads - 1) / kFinalizeThreads;
   if (blocks < 1) blocks = 1;
   if (blocks > kMaxFinalizeBlocks) blocks = kMaxFinalizeBlocks;
+  LaunchTimer timer("finalize_kernel", stream);
   finalize_kernel<<<static_cast<int>(blocks), kFinalizeThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
@@ -486,6 +490,7 @@ __global__ void __launch_bounds__(kFinalizeThreads) finish_loss_kernel(const Fin
 
 cudaError_t launch_finalize_gform(const GformArgs& a, int rows, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
+  LaunchTimer timer("finalize_gform_kernel", stream);
   finalize_gform_kernel<<<rows, kGformThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
@@ -507,6 +512,7 @@ __global__ void __launch_bounds__(kFinalizeThreads) finalize_rows_kernel(const G
 
 cudaError_t launch_finalize_rows(const GformArgs& a, int rows, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
+  LaunchTimer timer("finalize_rows_kernel", stream);
   finalize_rows_kernel<<<(rows + kFinalizeThreads - 1) / kFinalizeThreads, kFinalizeThreads, 0,
                          stream>>>(a, rows);
   return cudaGetLastError();
@@ -515,6 +521,7 @@ cudaError_t launch_finalize_rows(const GformArgs& a, int rows, cudaStream_t stre
 cudaError_t launch_finish_loss(const FinishArgs& a, cudaStream_t stream) {
   long long blocks = (a.n + kFinalizeThreads - 1) / kFinalizeThreads;
   blocks = std::max(1LL, std::min<long long>(blocks, kMaxFinalizeBlocks));
+  LaunchTimer timer("finish_loss_kernel", stream);
   finish_loss_kernel<<<static_cast<int>(blocks), kFinalizeThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
@@ -544,6 +551,7 @@ __global__ void bounded_wait_selftest_kernel(int* status, int* waited_out) {
 }
 
 cudaError_t launch_bounded_wait_selftest(int* status, int* waited_out, cudaStream_t stream) {
+  LaunchTimer timer("bounded_wait_selftest_kernel", stream);
   bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(status, waited_out);
   return cudaGetLastError();
 }

@@ -87,6 +87,26 @@ constexpr int kGformThreads = 256;
 constexpr int kFinalizeThreads = 256;
 constexpr int kMaxFinalizeBlocks = 1024;
 
+// Opt-in per-launch timing (grpo_launch_timing_enable). While it is on for the
+// calling host thread, each launcher brackets its launch with two CUDA events
+// recorded on the launch's own stream; grpo_launch_timing_read sums them per
+// kernel. Off (the default), a LaunchTimer costs one thread-local load. Launches
+// into a stream that is being captured are not timed. Defined in api.cu.
+bool launch_timing_on();
+class LaunchTimer {
+ public:
+  LaunchTimer(const char* name, cudaStream_t stream);
+  LaunchTimer(int mode, int ctas, cudaStream_t stream);  // "tc_gemm_kernel<mode, ctas>"
+  ~LaunchTimer();
+  LaunchTimer(const LaunchTimer&) = delete;
+  LaunchTimer& operator=(const LaunchTimer&) = delete;
+
+ private:
+  void begin(const char* name, cudaStream_t stream);
+  int slot_ = -1;
+  cudaStream_t stream_ = nullptr;
+};
+
 // Launch of one GEMM variant; a CTA pair (CTAS = 2) runs as a 2-CTA cluster.
 // `grid` counts CTAs (a multiple of CTAS).
 template <int MODE, int CTAS>
@@ -106,6 +126,7 @@ cudaError_t launch_gemm_variant(const CUtensorMap& map_a, const CUtensorMap& map
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
+  LaunchTimer timer(MODE, CTAS, stream);
   return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, CTAS>, map_a, map_b, args);
 }
 

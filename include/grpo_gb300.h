@@ -239,6 +239,43 @@ int grpo_logp_fwd_noalloc(const void* hidden, const void* W, const int32_t* ids,
  * grpo_read_device_status. Returns GRPO_OK if the launch went through. */
 int grpo_selftest_bounded_wait(void* workspace, size_t workspace_bytes, void* stream);
 
+/* Opt-in per-launch timing, for profiling without an external profiler.
+ *
+ * grpo_launch_timing_enable(1) turns it on for the calling host thread. While it
+ * is on, every kernel launch that thread makes through this library is
+ * bracketed by two CUDA events recorded on the launch's own stream. That stream
+ * is the caller's stream or the library's side stream. An event pair measures
+ * the kernel's device time, plus any idle gap on that stream between the two
+ * records. Timing adds about two event records of host time per launch, and
+ * nothing on the device.
+ *   - Off is the default. grpo_launch_timing_enable(0) stops recording; launches
+ *     already recorded stay readable.
+ *   - Launches into a stream that is being captured into a CUDA graph are not
+ *     timed.
+ *   - At most 65536 launches are kept between reads; later ones are not timed.
+ *
+ * grpo_launch_timing_read first waits for the recorded launches to finish. It
+ * then sums them per kernel, empties the record, and writes up to `capacity`
+ * entries to `out` in order of first launch. `*count` is set to the number of
+ * distinct kernels seen, which may exceed `capacity`; entries past `capacity`
+ * are lost. Kernel names are the device functions', e.g. "finalize_gform_kernel".
+ * GEMM variants are named "tc_gemm_kernel<mode, ctas>": mode 0 is the logit GEMM
+ * of the forward pass, 1 forms G from recomputed logits, 2 is G W -> dH, 3 is
+ * the logit GEMM that also stores fp16 logits, 4 is the lm_head gradient, and
+ * 5 is the dH GEMM that forms G from the stored logits; ctas is 2 for a CTA
+ * pair. Returns GRPO_OK, GRPO_ERR_INVALID_ARG (count null, capacity < 0, or out
+ * null with capacity > 0) or GRPO_ERR_CUDA (an event could not be read; the
+ * other launches are still summed). */
+typedef struct grpo_kernel_time {
+  char name[40];      /* NUL-terminated kernel name                         */
+  int32_t launches;   /* launches summed                                    */
+  int32_t reserved;
+  double total_ms;    /* summed device time between each launch's events    */
+} grpo_kernel_time;
+
+int grpo_launch_timing_enable(int on);
+int grpo_launch_timing_read(grpo_kernel_time* out, int capacity, int* count);
+
 /* Static text for a status code. */
 const char* grpo_status_string(int status);
 

@@ -186,3 +186,24 @@ def test_workspace_budget_too_small_is_an_error(clp):
 def test_sequence_mean_flag_is_accepted(clp):
     assert clp.grpo_workspace_size(1024, 64, 100, 256,
                                    clp.make_params(flags=clp._binding.FLAG_SEQUENCE_MEAN)) > 0
+
+
+def test_launch_timing_without_launches(clp):
+    # Host-only: switching the timing on and off and reading an empty record
+    # makes no CUDA call.
+    clp.grpo_launch_timing_enable(True)
+    assert clp.grpo_launch_timing_read() == []
+    clp.grpo_launch_timing_enable(False)
+    assert clp.grpo_launch_timing_read() == []
+
+
+def test_launch_timing_read_rejects_bad_arguments(clp):
+    lib = clp.lib
+    count = ctypes.c_int(-5)
+    assert lib.grpo_launch_timing_read(None, 0, ctypes.byref(count)) == 0
+    assert count.value == 0
+    assert lib.grpo_launch_timing_read(None, 0, None) == -1
+    assert lib.grpo_launch_timing_read(None, 4, ctypes.byref(count)) == -1
+    buf = (clp._binding.GrpoKernelTime * 1)()
+    assert lib.grpo_launch_timing_read(buf, -1, ctypes.byref(count)) == -1
+    assert ctypes.sizeof(clp._binding.GrpoKernelTime) == 56

@@ -1,6 +1,6 @@
 """Host-side helpers of bench.py (CPU): the source hash that ties a recorded
-DRAM-traffic figure to the code it was measured with, and the JSON keys the
-benchmark line must carry."""
+DRAM-traffic figure to the code it was measured with, the conversion of an ncu
+launch list into that record, and the roofline of the dominant kernel."""
 
 import json
 import os
@@ -30,6 +30,89 @@ def test_recorded_traffic_is_used_only_for_its_own_code():
         assert rec["dram_bytes_per_call"] == rec["dram_read_bytes"] + rec["dram_write_bytes"]
         got = bench.recorded_traffic(rec["workload"], rec["backward"])
         if rec["kernel_source_hash"] == bench.kernel_source_hash():
-            assert got == rec["dram_bytes_per_call"], name
+            assert got == rec, name
         else:
             assert got is None, name
+
+
+def _ncu_csv(path, launches):
+    """A launch list in the layout of `ncu --csv --metrics ...` (one row per metric)."""
+    head = ['"ID"', '"Process ID"', '"Kernel Name"', '"Metric Name"', '"Metric Unit"',
+            '"Metric Value"']
+    lines = ['==PROF== Connected to process 1', ",".join(head)]
+    for i, (name, rd, wr, us) in enumerate(launches):
+        for metric, unit, val in (("dram__bytes_read.sum", "Mbyte", rd),
+                                  ("dram__bytes_write.sum", "Kbyte", wr),
+                                  ("gpu__time_duration.sum", "usecond", us)):
+            lines.append(",".join(f'"{x}"' for x in (i, 1, name, metric, unit,
+                                                      f"{val:,.2f}")))
+    path.write_text("\n".join(lines) + "\n")
+
+
+def _call(scale):
+    return [("void grpo::row_plan_kernel(const unsigned char *, long long, int, int *)",
+             0.02, 0.0, 10.0),
+            ("void grpo::tc_gemm_kernel<(int)3, (int)2>(CUtensorMap, CUtensorMap, "
+             "grpo::TileArgs)", 1000.0 * scale, 800.0, 2000.0),
+            ("void at::native::vectorized_elementwise_kernel<4>(int, float)", 5.0, 5.0, 3.0),
+            ("void grpo::tc_gemm_kernel<(int)3, (int)2>(CUtensorMap, CUtensorMap, "
+             "grpo::TileArgs)", 1000.0 * scale, 800.0, 2000.0),
+            ("void grpo::finish_loss_kernel(grpo::FinishArgs)", 0.1, 0.004, 5.0)]
+
+
+def test_ncu_launch_list_split_into_calls(tmp_path):
+    csv = tmp_path / "launches.csv"
+    _ncu_csv(csv, _call(1.0) + _call(2.0) + _call(3.0)[:2])  # the last call is cut short
+    calls = bench.ncu_calls(str(csv))
+    assert len(calls) == 2  # the truncated call is dropped
+    for c, scale in zip(calls, (1.0, 2.0)):
+        # torch's own kernel is not part of the call; (int) is dropped from names
+        assert [d["name"] for d in c] == ["row_plan_kernel", "tc_gemm_kernel<3, 2>",
+                                          "tc_gemm_kernel<3, 2>", "finish_loss_kernel"]
+        assert c[1]["read"] == 1000.0 * scale * 1e6
+        assert c[1]["write"] == 800.0 * 1e3
+        assert c[1]["ms"] == 2.0
+
+
+def test_record_traffic_keeps_the_last_complete_call(tmp_path, monkeypatch):
+    csv = tmp_path / "launches.csv"
+    _ncu_csv(csv, _call(1.0) + _call(2.0) + _call(3.0)[:2])
+    monkeypatch.setattr(bench, "traffic_path",
+                        lambda w, b: str(tmp_path / f"traffic_{w}_{b}.json"))
+    rec = bench.record_traffic(str(csv), "toy", "stored", "ncu ... python bench.py")
+    gemm = rec["per_kernel"]["tc_gemm_kernel<3, 2>"]
+    assert gemm["launches"] == 2 and gemm["read_bytes"] == 2 * 2000.0e6
+    assert rec["launches_per_call"] == 4
+    assert rec["dram_bytes_per_call"] == rec["dram_read_bytes"] + rec["dram_write_bytes"]
+    assert abs(rec["ncu_time_ms_per_call"] - 4.015) < 1e-9
+    assert rec["kernel_source_hash"] == bench.kernel_source_hash()
+    assert json.loads((tmp_path / "traffic_toy_stored.json").read_text()) == rec
+
+
+def test_kernel_roofline_takes_the_kernel_with_most_time():
+    D, V, valid, calls = 4096, 128256, 16384, 5
+    times = [{"name": "row_plan_kernel", "launches": 5, "total_ms": 0.05},
+             {"name": "tc_gemm_kernel<3, 2>", "launches": 20, "total_ms": 45.0},
+             {"name": "finalize_gform_kernel", "launches": 20, "total_ms": 4.0},
+             {"name": "tc_gemm_kernel<2, 2>", "launches": 20, "total_ms": 41.0}]
+    peaks = {"hbm_gbs": 7000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1700.0}
+    rec = {"per_kernel": {"tc_gemm_kernel<3, 2>": {"launches": 4, "read_bytes": 4.0e9,
+                                                   "write_bytes": 2.0e9}}}
+    r = bench.kernel_roofline(times, calls, D, V, valid, peaks, rec)
+    assert r["kernel"] == "tc_gemm_kernel<3, 2>" and r["bound"] == "tensor"
+    assert r["launches_per_call"] == 4 and r["avg_launch_ms"] == 45.0 / 20
+    # 2 D V per valid token, over the call's 4 launches of this kernel
+    per_launch = 2.0 * D * V * valid / 4
+    assert r["algorithmic_flops_per_launch"] == per_launch
+    assert abs(r["achieved"] - per_launch / (45.0 / 20 / 1e3) / 1e12) < 1e-9
+    assert r["peak"] == 1700.0 and abs(r["frac"] - r["achieved"] / 1700.0) < 1e-12
+    assert r["traffic"] == 1.5e9
+    assert [k["name"] for k in r["per_kernel"]][:2] == ["tc_gemm_kernel<3, 2>",
+                                                          "tc_gemm_kernel<2, 2>"]
+    assert abs(sum(k["share"] for k in r["per_kernel"]) - 1.0) < 1e-12
+    # A row pass on top is HBM-bound: 4 V bytes per valid token.
+    times[2]["total_ms"] = 99.0
+    r = bench.kernel_roofline(times, calls, D, V, valid, peaks, None)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 7000.0
+    assert r["traffic"] is None
+    assert abs(r["achieved"] - 4.0 * V * valid / 4 / (99.0 / 20 / 1e3) / 1e9) < 1e-9
