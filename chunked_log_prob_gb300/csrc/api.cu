@@ -695,9 +695,13 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     a.part_ld = L.nr;
     a.S = sbuf(c);
     a.ldS = L.ldS;
+    // The pair variant stores each warp's 32 rows x 64 logits through TMA.
+    CUtensorMap map_st;
+    if (!encode_2d(&map_st, a.S, L.V, static_cast<uint64_t>(n_rb) * BM, L.ldS, 64, 32))
+      return GRPO_ERR_CUDA;
     const long long units = static_cast<long long>(n_ru) * splits;
     *splits_out = splits;
-    return launch_fwds_gemm(L.ctas, map_h, map_w_k, a,
+    return launch_fwds_gemm(L.ctas, map_h, map_w_k, map_st, a,
                             L.ctas * static_cast<int>(std::min<long long>(units, slots)),
                             st) == cudaSuccess
                ? GRPO_OK

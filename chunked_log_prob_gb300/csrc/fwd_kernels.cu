@@ -284,8 +284,9 @@ cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t stream) {
 namespace grpo {
 
 cudaError_t launch_fwds_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                             const TileArgs& args, int grid, cudaStream_t stream) {
-  return ctas == 2 ? launch_gemm_variant<MODE_FWDS, 2>(map_a, map_b, args, grid, stream)
+                             const CUtensorMap& map_s, const TileArgs& args, int grid,
+                             cudaStream_t stream) {
+  return ctas == 2 ? launch_gemm_variant<MODE_FWDS, 2>(map_a, map_b, args, grid, stream, &map_s)
                    : launch_gemm_variant<MODE_FWDS, 1>(map_a, map_b, args, grid, stream);
 }
 

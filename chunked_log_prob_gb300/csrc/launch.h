@@ -108,10 +108,12 @@ class LaunchTimer {
 };
 
 // Launch of one GEMM variant; a CTA pair (CTAS = 2) runs as a 2-CTA cluster.
-// `grid` counts CTAs (a multiple of CTAS).
+// `grid` counts CTAs (a multiple of CTAS). map_c: the store map of the
+// variants that write through TMA (PairCfg::kTmaStore), unused otherwise.
 template <int MODE, int CTAS>
 cudaError_t launch_gemm_variant(const CUtensorMap& map_a, const CUtensorMap& map_b,
-                                const TileArgs& args, int grid, cudaStream_t stream) {
+                                const TileArgs& args, int grid, cudaStream_t stream,
+                                const CUtensorMap* map_c = nullptr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(PairCfg<MODE, CTAS>::kThreads, 1, 1);
@@ -127,7 +129,8 @@ cudaError_t launch_gemm_variant(const CUtensorMap& map_a, const CUtensorMap& map
     cfg.numAttrs = 1;
   }
   LaunchTimer timer(MODE, CTAS, stream);
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, CTAS>, map_a, map_b, args);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, CTAS>, map_a, map_b,
+                            map_c != nullptr ? *map_c : map_a, args);
 }
 
 template <int MODE, int CTAS>
@@ -159,8 +162,11 @@ cudaError_t launch_zero_padding_blocks(const uint8_t* mask, long long n, int n_r
                                        void* dH, int sms, cudaStream_t stream);
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t stream);
 cudaError_t prepare_fwds_gemm();
+// map_s: the chunk's fp16 logit block [rows][ldS] as a store map, 64 x 32 boxes
+// with the 128-byte swizzle (used by the CTA-pair variant).
 cudaError_t launch_fwds_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                             const TileArgs& args, int grid, cudaStream_t stream);
+                             const CUtensorMap& map_s, const TileArgs& args, int grid,
+                             cudaStream_t stream);
 cudaError_t launch_finalize_gform(const GformArgs& a, int rows, cudaStream_t stream);
 cudaError_t launch_finalize_rows(const GformArgs& a, int rows, cudaStream_t stream);
 cudaError_t launch_finish_loss(const FinishArgs& a, cudaStream_t stream);
