@@ -351,19 +351,22 @@ def kernel_work(name, D, V):
     return None
 
 
-def kernel_roofline(times, calls, D, V, valid, peaks, rec):
+def kernel_roofline(times, calls, D, V, valid, peaks, rec, call_ms=None):
     """Roofline of the kernel with the most device time over `calls` calls.
 
     times: per-kernel sums from the library's launch timing (CUDA events on
     each launch's own stream). A launch's algorithmic work is the kind's work
-    per valid token x the valid tokens of a call / its launches per call."""
+    per valid token x the valid tokens of a call / its launches per call.
+    share: of the summed kernel time; of_call: of the call's own duration
+    (kernels on the side stream overlap the others, so these may sum past 1)."""
     if not times:
         return None
     summed = sum(k["total_ms"] for k in times)
     per_kernel = [{"name": k["name"], "launches_per_call": k["launches"] / calls,
                    "avg_launch_ms": k["total_ms"] / k["launches"],
                    "ms_per_call": k["total_ms"] / calls,
-                   "share": k["total_ms"] / summed}
+                   "share": k["total_ms"] / summed,
+                   "of_call": None if not call_ms else k["total_ms"] / calls / call_ms}
                   for k in sorted(times, key=lambda k: -k["total_ms"])]
     top = per_kernel[0]
     out = {"kernel": top["name"], "avg_launch_ms": top["avg_launch_ms"],
@@ -604,7 +607,8 @@ def run_ours(args):
     rec = recorded_traffic(p.name, "stored" if stored else "recompute")
     # The dominant kernel (most device time), timed live; its peak is the
     # sustained one, as it runs inside a long step. The call as a whole beside it.
-    roofline = kernel_roofline(kernel_times, timed_calls, D, V, valid, peaks, rec) or {}
+    roofline = kernel_roofline(kernel_times, timed_calls, D, V, valid, peaks, rec,
+                               ms_max if world == 1 else None) or {}
     roofline["peak_source"] = "%s (%s)" % (peak_src, "bf16 sustained cuBLAS loop" if roofline.get(
         "bound") == "tensor" else "STREAM-style copy")
     roofline["timing"] = ("CUDA events recorded by the library around each launch on the "

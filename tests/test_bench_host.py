@@ -110,6 +110,9 @@ def test_kernel_roofline_takes_the_kernel_with_most_time():
     assert [k["name"] for k in r["per_kernel"]][:2] == ["tc_gemm_kernel<3, 2>",
                                                           "tc_gemm_kernel<2, 2>"]
     assert abs(sum(k["share"] for k in r["per_kernel"]) - 1.0) < 1e-12
+    assert all(k["of_call"] is None for k in r["per_kernel"])
+    r = bench.kernel_roofline(times, calls, D, V, valid, peaks, rec, call_ms=18.0)
+    assert abs(r["per_kernel"][0]["of_call"] - 45.0 / calls / 18.0) < 1e-12
     # A row pass on top is HBM-bound: 4 V bytes per valid token.
     times[2]["total_ms"] = 99.0
     r = bench.kernel_roofline(times, calls, D, V, valid, peaks, None)
