@@ -433,15 +433,16 @@ DeviceInfo* current_device_info() {
 // 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows,
 // `pitch_elems` elements between rows; box {box_inner, box_outer}; 128B swizzle.
 bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-               uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer) {
+               uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+               uint64_t elem_bytes = 2) {
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {pitch_elems * 2};
+  cuuint64_t strides[1] = {pitch_elems * elem_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = g_encode(map, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -536,9 +537,11 @@ int launch_dw(const void* hidden, const __nv_bfloat16* G, long long ldG, int v0,
               int rb0, int n_rb, float* dW, bool first, const Layout& L, const Ws& w, int sms,
               cudaStream_t st) {
   const int slots = std::max(1, sms / L.ctas);
-  CUtensorMap map_gt, map_h_mn;
+  CUtensorMap map_gt, map_h_mn, map_dw;
   if (!encode_2d(&map_gt, G, width, static_cast<uint64_t>(n_rb) * BM, ldG, 64, BK) ||
-      !encode_2d(&map_h_mn, hidden, L.D, L.n, L.D, 64, BK))
+      !encode_2d(&map_h_mn, hidden, L.D, L.n, L.D, 64, BK) ||
+      !encode_2d(&map_dw, dW + static_cast<size_t>(v0) * L.D, L.D, width, L.D, 32, 32,
+                 CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4))
     return GRPO_ERR_CUDA;
   TileArgs a = base_args(L, w);
   a.n_total = L.n;
@@ -555,7 +558,7 @@ int launch_dw(const void* hidden, const __nv_bfloat16* G, long long ldG, int v0,
   a.dW = dW;
   a.first = first ? 1 : 0;
   const long long units = static_cast<long long>(n_vu) * n_dt;
-  if (launch_dw_gemm(L.ctas, map_gt, map_h_mn, a,
+  if (launch_dw_gemm(L.ctas, map_gt, map_h_mn, map_dw, a,
                      L.ctas * static_cast<int>(std::min<long long>(units, slots)),
                      st) != cudaSuccess)
     return GRPO_ERR_CUDA;

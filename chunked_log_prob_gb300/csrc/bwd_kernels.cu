@@ -19,8 +19,9 @@ cudaError_t prepare_bwd_gemms() {
 }
 
 cudaError_t launch_dw_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                           const TileArgs& args, int grid, cudaStream_t stream) {
-  return ctas == 2 ? launch_gemm_variant<MODE_DW, 2>(map_a, map_b, args, grid, stream)
+                           const CUtensorMap& map_dw, const TileArgs& args, int grid,
+                           cudaStream_t stream) {
+  return ctas == 2 ? launch_gemm_variant<MODE_DW, 2>(map_a, map_b, args, grid, stream, &map_dw)
                    : launch_gemm_variant<MODE_DW, 1>(map_a, map_b, args, grid, stream);
 }
 

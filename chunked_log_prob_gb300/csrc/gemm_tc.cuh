@@ -262,13 +262,15 @@ struct PairCfg {
   static constexpr int kKSub =
       (CTAS == 2 && kNAcc == 1 && (is_fwd(MODE) || MODE == MODE_BWDG || MODE == MODE_DW)) ? 2 : 1;
   static constexpr int kStageBytes = kKSub * (A_BYTES + kBBytes);
-  // The pair's logit-storing GEMM writes its fp16 logits through shared
-  // memory: each epilogue warp stages 32 rows x 64 columns (4 KB, 128-byte
-  // swizzle) in one of two buffers and writes them with a TMA tensor store, in
-  // whole 128-byte lines. Stored straight from registers, each warp store
-  // touched 32 rows in 16-byte pieces; at D = 1536 that cost the GEMM 15 % of
-  // its time (measured: 1.73 ms with the stores, 1.47 ms without).
-  static constexpr bool kTmaStore = MODE == MODE_FWDS && CTAS == 2;
+  // The pair's logit-storing and dW GEMMs write their outputs through shared
+  // memory: each epilogue warp stages a 32-row box of 128-byte rows (64 fp16
+  // logits or 32 fp32 dW values; 4 KB, 128-byte swizzle) in one of two buffers
+  // and writes it with a TMA tensor store (dW after its first chunk: a TMA
+  // reduce-add), in whole 128-byte lines. Written straight from registers,
+  // each warp store touched 32 rows in 16-byte pieces: that cost the logit
+  // GEMM 15 % of its time at D = 1536 (1.73 ms with the stores, 1.47 ms
+  // without) and the dW GEMM 25 % at the Llama shape (3.22 against 2.43 ms).
+  static constexpr bool kTmaStore = (MODE == MODE_FWDS || MODE == MODE_DW) && CTAS == 2;
   static constexpr int kStoreBufBytes = 32 * 128;
   static constexpr int kStoreBytes = kTmaStore ? 4 * 2 * kStoreBufBytes : 0;
   static constexpr int kMaxDynSmem = 232448 - 1024 - 1024;  // 227 KB less slack and statics
@@ -821,6 +823,40 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
 #pragma unroll
               for (int j = 0; j < 4; ++j)
                 st_global_v4(dst + j * 8, p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+            }
+          }
+        } else if (MODE == MODE_DW && C::kTmaStore) {
+          // map_c: dW[v0 : v0 + dw_rows) as fp32 [rows][hidden], 32 x 32 boxes;
+          // rows past the block and columns past D are clipped by the store.
+          const int vrow0 = ru * CTAS * BM + static_cast<int>(rank) * BM + q * 32;
+          if (vrow0 < args.dw_rows) {  // warp-uniform
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+              const int d0 = t * BN + c * 32;
+              if (d0 >= args.hidden) break;  // warp-uniform
+              float v[32];
+              tmem_ld32(tbase + c * 32, v);
+              if (k_iters == 0) {  // no row of the chunk is active: nothing accumulated
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+              }
+              uint8_t* buf = stage_out + (n_stores & 1u) * C::kStoreBufBytes;
+              if (lane == 0) bulk_wait_group_read<1>();  // this buffer's last store read it
+              __syncwarp();
+              uint4* srow = reinterpret_cast<uint4*>(buf + lane * 128);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                srow[j ^ (lane & 7)] =
+                    make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                               __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                if (args.first) tma_store_2d(&map_c, buf, d0, vrow0);
+                else tma_reduce_add_2d(&map_c, buf, d0, vrow0);
+                bulk_commit_group();
+              }
+              ++n_stores;
             }
           }
         } else if (MODE == MODE_DW) {

@@ -152,8 +152,11 @@ cudaError_t launch_dh_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap
                            const TileArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_dhs_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                             const TileArgs& args, int grid, cudaStream_t stream);
+// map_dw: dW[v0 : v0 + dw_rows) as fp32 [rows][hidden], 32 x 32 boxes with the
+// 128-byte swizzle (used by the CTA-pair variant).
 cudaError_t launch_dw_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                           const TileArgs& args, int grid, cudaStream_t stream);
+                           const CUtensorMap& map_dw, const TileArgs& args, int grid,
+                           cudaStream_t stream);
 cudaError_t launch_row_plan(const uint8_t* mask, long long n, int n_rb, int* rb_list,
                             int* n_active, double* msum, cudaStream_t stream);
 cudaError_t launch_seq_lens(const uint8_t* mask, long long n, int seq_len, int* lens,
