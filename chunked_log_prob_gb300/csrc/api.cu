@@ -605,7 +605,11 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
       a.G = w.G;
       a.ldG = L.vblock;
       long long units = static_cast<long long>(n_ru) * ntile;
-      if (launch_bwdg_gemm(L.ctas, map_h, map_w_k, a,
+      CUtensorMap map_gst;  // the pair variant stores G through TMA
+      if (!encode_2d(&map_gst, w.G, L.vblock, static_cast<uint64_t>(n_rb) * BM, L.vblock, 64,
+                     32))
+        return GRPO_ERR_CUDA;
+      if (launch_bwdg_gemm(L.ctas, map_h, map_w_k, map_gst, a,
                            L.ctas * static_cast<int>(std::min<long long>(units, slots)),
                            st) != cudaSuccess)
         return GRPO_ERR_CUDA;

@@ -26,8 +26,9 @@ cudaError_t launch_dw_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap
 }
 
 cudaError_t launch_bwdg_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                             const TileArgs& args, int grid, cudaStream_t stream) {
-  return ctas == 2 ? launch_gemm_variant<MODE_BWDG, 2>(map_a, map_b, args, grid, stream)
+                             const CUtensorMap& map_g, const TileArgs& args, int grid,
+                             cudaStream_t stream) {
+  return ctas == 2 ? launch_gemm_variant<MODE_BWDG, 2>(map_a, map_b, args, grid, stream, &map_g)
                    : launch_gemm_variant<MODE_BWDG, 1>(map_a, map_b, args, grid, stream);
 }
 

@@ -262,15 +262,17 @@ struct PairCfg {
   static constexpr int kKSub =
       (CTAS == 2 && kNAcc == 1 && (is_fwd(MODE) || MODE == MODE_BWDG || MODE == MODE_DW)) ? 2 : 1;
   static constexpr int kStageBytes = kKSub * (A_BYTES + kBBytes);
-  // The pair's logit-storing and dW GEMMs write their outputs through shared
-  // memory: each epilogue warp stages a 32-row box of 128-byte rows (64 fp16
-  // logits or 32 fp32 dW values; 4 KB, 128-byte swizzle) in one of two buffers
+  // The pair's logit-storing, G-tile and dW GEMMs write their outputs through
+  // shared memory: each epilogue warp stages a 32-row box of 128-byte rows (64
+  // fp16 logits, 64 bf16 G values or 32 fp32 dW values; 4 KB, 128-byte
+  // swizzle) in one of two buffers
   // and writes it with a TMA tensor store (dW after its first chunk: a TMA
   // reduce-add), in whole 128-byte lines. Written straight from registers,
   // each warp store touched 32 rows in 16-byte pieces: that cost the logit
   // GEMM 15 % of its time at D = 1536 (1.73 ms with the stores, 1.47 ms
   // without) and the dW GEMM 25 % at the Llama shape (3.22 against 2.43 ms).
-  static constexpr bool kTmaStore = (MODE == MODE_FWDS || MODE == MODE_DW) && CTAS == 2;
+  static constexpr bool kTmaStore =
+      (MODE == MODE_FWDS || MODE == MODE_BWDG || MODE == MODE_DW) && CTAS == 2;
   static constexpr int kStoreBufBytes = 32 * 128;
   static constexpr int kStoreBytes = kTmaStore ? 4 * 2 * kStoreBufBytes : 0;
   static constexpr int kMaxDynSmem = 232448 - 1024 - 1024;  // 227 KB less slack and statics
@@ -815,7 +817,34 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             // Rows past N in an active block come out exactly 0 (zero-filled
             // hidden rows, g = 0); they are written too, so that the G block
             // holds no stale bytes for the dW GEMM.
-            if (block_ok) {
+            if constexpr (C::kTmaStore) {
+              // map_c: the chunk's G block [rows][ldG], 64 x 32 boxes; chunk c
+              // fills 16-byte pieces 4 (c & 1) .. +3 of this row of the box.
+              if (block_ok) {
+                uint8_t* buf = stage_out + (n_stores & 1u) * C::kStoreBufBytes;
+                if ((c & 1) == 0) {
+                  if (lane == 0) bulk_wait_group_read<1>();  // this buffer's last store read it
+                  __syncwarp();
+                }
+                uint4* srow = reinterpret_cast<uint4*>(buf + lane * 128);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  srow[((c & 1) * 4 + j) ^ (lane & 7)] =
+                      make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]),
+                                 pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                                 pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                                 pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+                if ((c & 1) == 1) {
+                  fence_proxy_async_smem();
+                  __syncwarp();
+                  if (lane == 0) {
+                    tma_store_2d(&map_c, buf, t * BN + (c >> 1) * 64, li * BM + q * 32);
+                    bulk_commit_group();
+                  }
+                  ++n_stores;
+                }
+              }
+            } else if (block_ok) {
               uint32_t p[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) p[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
