@@ -17,10 +17,14 @@
 //              epilogue accumulates in fp32 and writes bf16 on the last block.
 //   MODE_DW    dW[v0 + m, n] (+)= sum over the chunk's rows of G[row, m] H[row, n]:
 //              the lm_head gradient; A (G^T) and B (H) are both MN-major, K runs
-//              over the chunk's active row blocks; fp32 RMW on the output.
+//              over the chunk's active row blocks; fp32 accumulation on the
+//              output across chunks.
 //   MODE_FWDS  MODE_FWD over the rows of one backward chunk that also stores
 //              the (transformed) logits in fp16 to the chunk workspace, for a
 //              backward that needs no second logit GEMM.
+// On CTA pairs, MODE_FWDS, MODE_BWDG and MODE_DW write their outputs through
+// shared memory and TMA stores (MODE_DW: TMA reduce-adds after the first
+// chunk), in whole 128-byte lines.
 //   MODE_DHS   MODE_DH whose A operand is that stored fp16 logit block: the
 //              epilogue warps, idle during the long vocabulary K loop, and four
 //              converter-only warps rewrite each landed A stage in place as

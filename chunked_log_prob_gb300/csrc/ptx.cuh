@@ -111,12 +111,6 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
 // -------------------------------------------------------------- tcgen05 ----
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -246,16 +240,8 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
-// Cluster-scope release: for an arrive that announces this thread's own
-// shared-memory writes to a consumer in the peer CTA.
-__device__ __forceinline__ void mbar_arrive_cluster_rel(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
-                   cluster_addr)
-               : "memory");
-}
-
 // Orders this thread's generic-proxy writes to shared memory before later
-// async-proxy reads of it (tcgen05.mma operands).
+// async-proxy reads of it (tcgen05.mma operands, TMA stores).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
