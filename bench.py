@@ -700,10 +700,12 @@ def run_reference(args):
     old, ref = p.old_ref(base)
     M = float(len(valid))
     rng = np.random.default_rng(args.seed)
-    # Rows per step: about 3 s of oracle work, calibrated on 8 rows.
+    # Rows per step: about 3 s of oracle work, calibrated on 16 rows after a
+    # first call that pays the one-time costs (thread pool start-up, page-in).
+    oracle.rows_fwd_bwd(p.hidden, W64, p.ids.numpy(), valid[:4], old, ref, p.adv, p.seq_len, M)
     t0 = time.perf_counter()
-    oracle.rows_fwd_bwd(p.hidden, W64, p.ids.numpy(), valid[:8], old, ref, p.adv, p.seq_len, M)
-    per_row = (time.perf_counter() - t0) / 8
+    oracle.rows_fwd_bwd(p.hidden, W64, p.ids.numpy(), valid[:16], old, ref, p.adv, p.seq_len, M)
+    per_row = (time.perf_counter() - t0) / 16
     rows_per_step = int(max(4, min(len(valid), 3.0 / max(per_row, 1e-6))))
 
     def step():
