@@ -119,3 +119,32 @@ def test_kernel_roofline_takes_the_kernel_with_most_time():
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 7000.0
     assert r["traffic"] is None
     assert abs(r["achieved"] - 4.0 * V * valid / 4 / (99.0 / 20 / 1e3) / 1e9) < 1e-9
+
+
+def test_record_traffic_command_line(tmp_path):
+    # The command the profiles give: bench.py --record-traffic <csv> --workload W
+    # writes profiles/traffic_W_<backward>.json. Run on a copy of bench.py so the
+    # committed profiles stay untouched.
+    import shutil
+    import subprocess
+    import sys
+
+    root = tmp_path / "repo"
+    (root / "profiles").mkdir(parents=True)
+    shutil.copy(os.path.join(ROOT, "bench.py"), root / "bench.py")
+    shutil.copytree(os.path.join(ROOT, "chunked_log_prob_gb300", "csrc"),
+                    root / "chunked_log_prob_gb300" / "csrc")
+    csv = tmp_path / "launches.csv"
+    _ncu_csv(csv, _call(1.0) + _call(2.0) + _call(3.0)[:2])
+    r = subprocess.run([sys.executable, str(root / "bench.py"), "--record-traffic", str(csv),
+                        "--workload", "toy", "--backward", "recompute",
+                        "--record-command", "ncu ..."],
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["workload"] == "toy" and line["launches_per_call"] == 4
+    with open(root / "profiles" / "traffic_toy_recompute.json") as f:
+        rec = json.load(f)
+    assert rec["command"] == "ncu ..." and rec["backward"] == "recompute"
+    assert rec["kernel_source_hash"] == bench.kernel_source_hash()
+    assert rec["per_kernel"]["tc_gemm_kernel<3, 2>"]["read_bytes"] == 2 * 2000.0e6
