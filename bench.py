@@ -47,9 +47,16 @@ def parse_args():
                     help="override tokens per completion (small profiling cases)")
     ap.add_argument("--chunk-tokens", type=int, default=0)
     ap.add_argument("--vocab-block", type=int, default=0)
-    ap.add_argument("--backward", default="stored", choices=["stored", "recompute"],
-                    help="stored: the backward reads fp16 logits kept per chunk (4NDV "
-                         "executed); recompute: it recomputes the logit tiles (6NDV)")
+    ap.add_argument("--backward", default="auto", choices=["auto", "stored", "recompute"],
+                    help="auto: the library's default choice (flags 0) for the workspace "
+                         "budget; stored: the backward reads fp16 logits kept per chunk "
+                         "(4NDV executed); recompute: it recomputes the logit tiles (6NDV)")
+    ap.add_argument("--workspace-limit-gb", type=float, default=0.0,
+                    help="workspace budget passed to the library (0 = none)")
+    ap.add_argument("--budget-sweep", default="",
+                    help="no headline line: comma-separated workspace budgets in GB; for "
+                         "each, time the automatic choice and both forced forms and print "
+                         "one JSON line per (budget, form)")
     ap.add_argument("--single-cta", action="store_true",
                     help="one CTA per 128-row GEMM tile instead of CTA pairs")
     ap.add_argument("--with-dw", action="store_true",
@@ -166,18 +173,26 @@ def max_over_ranks(x):
     return float(t.item())
 
 
+# grpo_params.flags of each backward form (GRPO_FLAG_STORED_LOGITS,
+# GRPO_FLAG_RECOMPUTE_LOGITS; 0 lets the library choose).
+FORM_FLAGS = {"auto": 0, "stored": 1, "recompute": 16}
+
+
 def flops_per_token(D, V):
     # 2DV forward + 4DV backward (recomputed logits + G W), per valid token.
     return 6.0 * D * V
 
 
-def oracle_rows_per_second(p, target_s, seed, cores_note, gpu=None):
+def oracle_rows_per_second(p, target_s, seed, cores_note, gpu=None, masked_loss=None):
     """Time the fp64 oracle on a seeded sample of valid rows of workload `p`.
 
     gpu = (old, ref, logp, dH) of a GPU call on the same inputs: the oracle
     then runs with that call's old/ref log-probs, and its rows are compared
     with the call's logp and dH (each row is exact given the loss
-    denominator). Returns (rows, seconds, parity dict or None)."""
+    denominator). masked_loss(mask) runs the same call with another mask and
+    returns its loss: with the sampled rows as the mask, the oracle's loss
+    over those rows is exact, so the loss is compared too. Returns (rows,
+    seconds, parity dict or None)."""
     import numpy as np
     import torch
 
@@ -218,7 +233,21 @@ def oracle_rows_per_second(p, target_s, seed, cores_note, gpu=None):
             "max_abs_dlogp": float(np.abs(got_lp - want["logp"]).max()),
             "rel_fro_dH": float(np.linalg.norm(got_dh - want["dH"]) /
                                 np.linalg.norm(want["dH"])),
-            "gates": "|dlogp| <= 1e-2, rel dH <= 2e-2"}
+            "gates": "|dlogp| <= 1e-2, rel loss <= 1e-3, rel dH <= 2e-2"}
+        if masked_loss is not None:
+            # Same call with only the sampled rows unmasked: its loss is the
+            # masked mean over exactly the rows the oracle computed.
+            mask2 = torch.zeros(p.n_tokens, dtype=torch.uint8)
+            mask2[idx] = 1
+            lp_full = np.zeros(p.n_tokens)
+            lp_full[rows] = want["logp"]
+            L_want = oracle.grpo_loss(lp_full, old, ref, adv, mask2, p.seq_len, p.eps_low,
+                                      p.eps_high, p.beta)[0]
+            L_got = masked_loss(mask2)
+            parity.update({"loss_rows": len(rows), "loss": L_got, "loss_oracle": L_want,
+                           "rel_loss": abs(L_got - L_want) / abs(L_want),
+                           "loss_note": "second call, same inputs, mask = the sampled rows "
+                                        "(the oracle's loss over them is exact)"})
     return len(rows), t, parity
 
 
@@ -347,7 +376,8 @@ def kernel_work(name, D, V):
     if name.startswith("tc_gemm_kernel"):
         return "tensor", 2.0 * D * V, "flop"  # one pass of the N x V x D contraction
     if name == "finalize_gform_kernel":
-        return "hbm", 4.0 * V, "byte"  # fp16 logit row in, bf16 G row out
+        # fp16 logit row in, bf16 G row out, one fp32 maximum per 64-column box
+        return "hbm", 4.0 * V + 4.0 * math.ceil(V / 64), "byte"
     return None
 
 
@@ -384,7 +414,10 @@ def kernel_roofline(times, calls, D, V, valid, peaks, rec, call_ms=None):
         per_launch = per_token * valid / top["launches_per_call"]
         rate = per_launch / (top["avg_launch_ms"] / 1e3)
         if bound == "tensor":
-            achieved, peak, u = rate / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
+            # The burst peak: a launch lasts milliseconds, not the seconds the
+            # sustained figure's loop ran for; the sustained fraction beside it.
+            achieved, peak, u = rate / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+            out["frac_of_sustained_peak"] = achieved / peaks["bf16_tflops_sustained"]
         else:
             achieved, peak, u = rate / 1e9, peaks["hbm_gbs"], "GB/s"
         out.update({"bound": bound, "achieved": achieved, "peak": peak, "unit": u,
@@ -426,15 +459,25 @@ def run_ours(args):
     p = synth.make_problem(args.workload, seed=rank_seed(args.seed, rank), device=dev, **over)
     torch.cuda.empty_cache()  # drop the generator's fp32 temporaries
     N, D, V, T = p.n_tokens, p.hidden_size, p.vocab, p.seq_len
-    stored = args.backward == "stored"
+    limit = int(args.workspace_limit_gb * (1 << 30))
 
     def make(flag):
         return clp.make_params(p.eps_low, p.eps_high, p.beta, 0.0, args.chunk_tokens,
-                               args.vocab_block, flags=flag | (2 if args.single_cta else 0))
+                               args.vocab_block, flags=flag | (2 if args.single_cta else 0),
+                               workspace_limit_bytes=limit)
 
-    params = make(1 if stored else 0)
-    other = make(0 if stored else 1)
+    params = make(FORM_FLAGS[args.backward])
     plan = clp.grpo_get_plan(N, D, V, T, params)
+    stored = bool(plan["stored_logits"])
+    other = make(FORM_FLAGS["recompute" if stored else "stored"])
+    if args.backward == "auto":
+        choice = ("library default (flags 0): the planner's automatic choice; %s" % (
+            "no workspace budget" if limit == 0 else "budget %.2f GB" % args.workspace_limit_gb)
+            + (", so the stored form fits and its modelled GEMM time is the shorter"
+               if stored else ", under which the recomputed form is the faster or the only "
+               "one that fits"))
+    else:
+        choice = "forced by --backward %s" % args.backward
     ws_bytes = max(clp.grpo_workspace_size(N, D, V, T, params),
                    0 if args.no_variant else clp.grpo_workspace_size(N, D, V, T, other))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
@@ -605,11 +648,11 @@ def run_ours(args):
     peak_sus = peaks["bf16_tflops_sustained"]
     peak_burst = peaks["bf16_tflops"]
     rec = recorded_traffic(p.name, "stored" if stored else "recompute")
-    # The dominant kernel (most device time), timed live; its peak is the
-    # sustained one, as it runs inside a long step. The call as a whole beside it.
+    # The dominant kernel (most device time), timed live; its peak is the burst
+    # one (a call lasts milliseconds). The call as a whole beside it.
     roofline = kernel_roofline(kernel_times, timed_calls, D, V, valid, peaks, rec,
                                ms_max if world == 1 else None) or {}
-    roofline["peak_source"] = "%s (%s)" % (peak_src, "bf16 sustained cuBLAS loop" if roofline.get(
+    roofline["peak_source"] = "%s (%s)" % (peak_src, "bf16 cuBLAS burst" if roofline.get(
         "bound") == "tensor" else "STREAM-style copy")
     roofline["timing"] = ("CUDA events recorded by the library around each launch on the "
                           "launch's own stream, over the %d timed calls" % timed_calls)
@@ -617,9 +660,11 @@ def run_ours(args):
     roofline["call"] = {
         "scope": "grpo_loss_fwd_bwd: %d launches per call, %d chunks x %d vocab blocks" % (
             plan["launches_loss"], plan["n_chunks"], plan["n_vocab_blocks"]),
-        "bound": "tensor", "achieved": tflops_exec, "peak": peak_sus, "unit": "TFLOP/s",
-        "frac": tflops_exec / peak_sus, "frac_of_burst_peak": tflops_exec / peak_burst,
-        "counted_tflops_6NDV": tflops, "flops_per_call": fl_exec,
+        "bound": "tensor", "achieved": tflops_exec, "peak": peak_burst, "unit": "TFLOP/s",
+        "frac": tflops_exec / peak_burst, "frac_of_sustained_peak": tflops_exec / peak_sus,
+        "counted_tflops_6NDV": tflops,
+        "counted_note": "6NDV counted flops per second; the stored backward executes 4NDV, "
+                        "so this rate is not a utilisation", "flops_per_call": fl_exec,
         "traffic": None if rec is None else rec.get("dram_bytes_per_call"),
         "traffic_unit": "DRAM bytes per call"}
     launches_per_call = sum(k["launches"] for k in kernel_times) / timed_calls
@@ -646,7 +691,9 @@ def run_ours(args):
         },
         "tflops": tflops,
         "tflops_executed": tflops_exec,
-        "pct_bf16_peak": 100.0 * tflops_exec / peak_sus,
+        "pct_bf16_peak": 100.0 * tflops_exec / peak_burst,
+        "pct_bf16_peak_note": "executed flops over the measured burst bf16 peak",
+        "backward_choice": choice,
         "backward": ("stored fp16 logits" if stored else "recomputed logits") + (
             ", G formed inside the dH GEMM" if stored and plan["g_in_dh_gemm"]
             and not args.with_dw else ", G formed in its own pass" if stored else "") + (
@@ -668,8 +715,16 @@ def run_ours(args):
     if world == 1 and not args.no_cpu_baseline:
         step()  # the outputs of one headline call, for the parity check
         torch.cuda.synchronize(dev)
+        def masked_loss(mask2):
+            loss2 = torch.empty(1, dtype=torch.float32, device=dev)
+            dH2 = torch.empty_like(dH)
+            clp.grpo_loss_fwd_bwd(p.hidden, p.weight, p.ids, mask2.to(dev), old, ref, p.adv, T,
+                                  params=params, workspace=ws, loss=loss2, logp=None, dH=dH2,
+                                  want_logp=False)
+            return float(loss2.item())
+
         n, t, parity = oracle_rows_per_second(p, args.cpu_seconds, args.seed, None,
-                                              gpu=(old, ref, logp, dH))
+                                              gpu=(old, ref, logp, dH), masked_loss=masked_loss)
         out["cpu_baseline"] = {
             "value": n / t, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
             "sample": f"{n} seeded valid rows of {p.name} (logp, g, dH per row; 6DV fp64 "
@@ -678,6 +733,72 @@ def run_ours(args):
     print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+# -------------------------------------------------------- budget sweep ----
+
+def run_budget_sweep(args):
+    """Workspace budget against call time: for each budget, the library's
+    automatic choice and both forced backward forms, each with the largest
+    plan the budget allows. One JSON line per (budget, form); a form that does
+    not fit a budget is reported as such."""
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import chunked_log_prob_gb300 as clp
+    import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    p = synth.make_problem(args.workload, seed=args.seed, device=dev)
+    torch.cuda.empty_cache()
+    N, D, V, T = p.n_tokens, p.hidden_size, p.vocab, p.seq_len
+    old = torch.full((N,), -math.log(V), device=dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    dH = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(3, args.steps)
+    for gb in [float(x) for x in args.budget_sweep.split(",") if x.strip()]:
+        limit = int(gb * (1 << 30))
+        for form in ("auto", "stored", "recompute"):
+            params = clp.make_params(p.eps_low, p.eps_high, p.beta,
+                                     flags=FORM_FLAGS[form], workspace_limit_bytes=limit)
+            row = {"workload": p.name, "budget_gb": gb, "form": form}
+            try:
+                nbytes = clp.grpo_workspace_size(N, D, V, T, params)
+                plan = clp.grpo_get_plan(N, D, V, T, params)
+            except clp.GrpoError as e:
+                row["fits"] = False
+                row["why"] = str(e)
+                print(json.dumps(row), flush=True)
+                continue
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+            def call():
+                clp.grpo_loss_fwd_bwd(p.hidden, p.weight, p.ids, p.mask, old, old, p.adv, T,
+                                      params=params, workspace=ws, loss=loss, logp=None, dH=dH,
+                                      want_logp=False)
+            for _ in range(max(args.warmup, 3)):
+                call()
+            torch.cuda.synchronize(dev)
+            assert clp.grpo_read_device_status(ws) == 0
+            ev0.record(stream)
+            for _ in range(reps):
+                call()
+            ev1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = ev0.elapsed_time(ev1) / reps
+            row.update({"fits": True, "workspace_bytes": nbytes,
+                        "backward": "stored" if plan["stored_logits"] else "recompute",
+                        "chunk_rows": plan["chunk_rows"], "n_chunks": plan["n_chunks"],
+                        "vocab_block": plan["vocab_block"], "ms_per_call": ms,
+                        "tokens_per_s": p.n_valid / (ms / 1e3)})
+            print(json.dumps(row), flush=True)
+            del ws
+            torch.cuda.empty_cache()
 
 
 # ----------------------------------------------------------- reference ----
@@ -744,5 +865,7 @@ if __name__ == "__main__":
                                             "launches_per_call", "ncu_time_ms_per_call")}))
     elif a.impl == "reference":
         run_reference(a)
+    elif a.budget_sweep:
+        run_budget_sweep(a)
     else:
         run_ours(a)

@@ -6,6 +6,9 @@ runs in the CUDA library ``libgrpo_gb300.so`` built from ``csrc/``.
 
 from ._binding import (  # noqa: F401
     EXPORTED,
+    GRPO_ERR_BAD_TOKEN_ID,
+    GRPO_ERR_DEVICE_TIMEOUT,
+    GRPO_ERR_NONFINITE,
     GRPO_OK,
     NOALLOC_MAX_TOKENS,
     GrpoError,

@@ -16,11 +16,14 @@ import torch
 from ._build import LIB_PATH
 
 GRPO_OK = 0
+GRPO_ERR_DEVICE_TIMEOUT = -7
+GRPO_ERR_BAD_TOKEN_ID = -8
+GRPO_ERR_NONFINITE = -9
 STATUS_NAMES = {
     0: "GRPO_OK", -1: "GRPO_ERR_INVALID_ARG", -2: "GRPO_ERR_MISALIGNED",
     -3: "GRPO_ERR_UNSUPPORTED_SHAPE", -4: "GRPO_ERR_WORKSPACE_TOO_SMALL",
     -5: "GRPO_ERR_UNSUPPORTED_DEVICE", -6: "GRPO_ERR_CUDA",
-    -7: "GRPO_ERR_DEVICE_TIMEOUT", -8: "GRPO_ERR_BAD_TOKEN_ID",
+    -7: "GRPO_ERR_DEVICE_TIMEOUT", -8: "GRPO_ERR_BAD_TOKEN_ID", -9: "GRPO_ERR_NONFINITE",
 }
 
 
@@ -45,6 +48,7 @@ class GrpoPlanInfo(ctypes.Structure):
                 ("n_chunks", ctypes.c_int32), ("n_vocab_blocks", ctypes.c_int32),
                 ("fwd_splits", ctypes.c_int32), ("launches_logp", ctypes.c_int32),
                 ("launches_loss", ctypes.c_int32), ("g_in_dh_gemm", ctypes.c_int32),
+                ("stored_logits", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_uint64)]
 
 
@@ -103,6 +107,7 @@ FLAG_STORED_LOGITS = 1
 FLAG_SINGLE_CTA = 2
 FLAG_SEQUENCE_MEAN = 4
 FLAG_FIT_FREE_MEMORY = 8
+FLAG_RECOMPUTE_LOGITS = 16
 
 # Largest batch of the workspace-free forward (its static device scratch).
 NOALLOC_MAX_TOKENS = 8192

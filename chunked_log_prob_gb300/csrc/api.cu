@@ -34,6 +34,10 @@ constexpr size_t kMaxStoredChunkBytes = size_t(2) << 30;    // 2 GiB of fp16 log
 // overlapped separate pass is faster.
 constexpr int kFusedMaxHidden = 2048;
 constexpr int kSplitsTarget = 8;        // forward vocab splits per raster group
+// SM count at which the automatic choice between the stored and the
+// recomputed backward is modelled (GB300's): the same choice then holds for
+// the sizing without a device and for the call's own plan.
+constexpr int kRefSms = 152;
 constexpr size_t kHeaderBytes = 16384;   // status, counters, loss partials
 constexpr int kMaxDevices = 64;
 
@@ -74,7 +78,10 @@ struct Layout {
                     // GEMM, one logit block (the dW variant then runs unoverlapped)
   int vblock;       // backward vocab block (multiple of BN)
   bool need_acc;    // more than one vocab block -> fp32 dH accumulator
-  size_t off_pm, off_ps, off_zy, off_lse, off_g, off_rbl, off_lt, off_seq, off_G, off_acc, total;
+  double model_cost;  // modelled GEMM time of the plan in forward-tile times (0: no device)
+  int nbox;         // stored path: 64-column boxes per row (their maxima are kept)
+  size_t off_pm, off_ps, off_zy, off_lse, off_g, off_rbl, off_lt, off_seq, off_G, off_bmax,
+      off_acc, total;
 };
 
 int auto_chunk_blocks(long long n_rb_total, int n_dt, int sms, int max_units) {
@@ -128,53 +135,95 @@ int stored_fwd_splits(int nrb, int nvt, int sms, double* eff_out) {
   return best;
 }
 
-// Row blocks per chunk for the stored-logit backward. Each chunk runs a
-// forward launch of (row blocks x splits) units and a dH launch of
-// (row blocks x D tiles) units; the score is the ideal SM time of the whole
-// schedule (every chunk, including a shorter last one) over its modelled
-// time: forward and dH rounded up to whole waves, plus whatever of each
-// chunk's separate G pass the GEMMs around it cannot hide. exposed_g is that
-// pass's time relative to the forward GEMM of the same rows (0 when dH forms
-// G itself). In the overlapped schedule pass c runs beside dH(c-1) and the
-// forward of chunk c+1; with a single chunk it is fully exposed. Plans of
-// more than one chunk take at most max_multi row blocks per chunk (they may
-// need two chunk blocks). Near-ties go to the larger chunk.
+// Row units per raster group: the slots in flight (one per SM pair) cover
+// group_rows row units x (slots / group_rows) vocab tiles or splits, so each
+// W tile fetched from HBM is shared through L2 by group_rows slots and each
+// row unit's hidden states by the others.
+int group_rows_for(int n_rb, int sms) {
+  return std::max(1, std::min(n_rb, std::max(1, sms) / kSplitsTarget));
+}
+
+// Same, with group_rows a divisor of the slot count (at least 4 columns per
+// group): a group is then exactly one round of the persistent grid, and the
+// slots that share a W range all run in the same round.
+int group_rows_exact(int n_ru, int slots) {
+  slots = std::max(1, slots);
+  const int cap = std::max(1, std::min(n_ru, slots / 4));
+  for (int r = cap; r > 1; --r)
+    if (slots % r == 0) return r;
+  return 1;
+}
+
+// Modelled GEMM time of the stored-logit schedule with chunks of nrb row
+// units, in forward-tile times (one 256-row x 256-column x D tile on one SM
+// pair). Each chunk runs a forward launch of (row units x splits) units and a
+// dH launch of (row units x D tiles) units, both rounded up to whole waves,
+// plus whatever of each chunk's separate G pass the GEMMs around it cannot
+// hide. exposed_g is that pass's time relative to the forward GEMM of the same
+// rows (0 when dH forms G itself). In the overlapped schedule pass c runs
+// beside dH(c-1) and the forward of chunk c+1; with a single chunk it is fully
+// exposed.
+double stored_cost(long long n_rb_total, int nrb, int n_dt, int nvt, int sms, double exposed_g) {
+  std::vector<double> fwd, dh;
+  double actual = 0.0;
+  for (long long r0 = 0; r0 < n_rb_total; r0 += nrb) {
+    const int n = static_cast<int>(std::min<long long>(nrb, n_rb_total - r0));
+    const int sp = stored_fwd_splits(n, nvt, sms, nullptr);
+    // forward: waves x tiles per unit (the longest unit sets the pace)
+    fwd.push_back(static_cast<double>(cdiv(static_cast<long long>(n) * sp, sms)) *
+                  cdiv(nvt, sp));
+    // dH: units of equal K; scaled to the forward's per-row work
+    dh.push_back(static_cast<double>(cdiv(static_cast<long long>(n) * n_dt, sms)) * nvt / n_dt);
+    actual += fwd.back() + dh.back();
+  }
+  const size_t nc = fwd.size();
+  for (size_t c = 0; c < nc; ++c) {
+    const double window = (c > 0 ? dh[c - 1] : 0.0) + (c + 1 < nc ? fwd[c + 1] : 0.0);
+    actual += std::max(0.0, exposed_g * fwd[c] - window);
+  }
+  return actual;
+}
+
+// Row units per chunk for the stored-logit backward: the best ratio of the
+// ideal SM time of the whole schedule (every chunk, including a shorter last
+// one) to its modelled time. Plans of more than one chunk take at most
+// max_multi row units per chunk (they may need two chunk blocks). Near-ties go
+// to the larger chunk.
 int auto_stored_chunk_blocks(long long n_rb_total, int n_dt, int nvt, int sms, int max_units,
                              int max_multi, double exposed_g) {
   const int hi = static_cast<int>(std::min<long long>(n_rb_total, max_units));
   int best = std::min(hi, std::max(1, max_multi));
   if (hi >= n_rb_total) best = hi;
   double best_score = -1.0;
-  std::vector<double> fwd, dh;
+  const double ideal = 2.0 * static_cast<double>(n_rb_total) * nvt / sms;
   for (int nrb = hi; nrb >= 1; --nrb) {
     if (nrb < n_rb_total && nrb > max_multi) continue;
-    double ideal = 0.0, actual = 0.0;
-    fwd.clear();
-    dh.clear();
-    for (long long r0 = 0; r0 < n_rb_total; r0 += nrb) {
-      const int n = static_cast<int>(std::min<long long>(nrb, n_rb_total - r0));
-      const int sp = stored_fwd_splits(n, nvt, sms, nullptr);
-      // forward: waves x tiles per unit (the longest unit sets the pace)
-      fwd.push_back(static_cast<double>(cdiv(static_cast<long long>(n) * sp, sms)) *
-                    cdiv(nvt, sp));
-      // dH: units of equal K; scaled to the forward's per-row work
-      dh.push_back(static_cast<double>(cdiv(static_cast<long long>(n) * n_dt, sms)) * nvt /
-                   n_dt);
-      ideal += 2.0 * n * nvt / sms;
-      actual += fwd.back() + dh.back();
-    }
-    const size_t nc = fwd.size();
-    for (size_t c = 0; c < nc; ++c) {
-      const double window = (c > 0 ? dh[c - 1] : 0.0) + (c + 1 < nc ? fwd[c + 1] : 0.0);
-      actual += std::max(0.0, exposed_g * fwd[c] - window);
-    }
-    const double score = ideal / actual;
+    const double score = ideal / stored_cost(n_rb_total, nrb, n_dt, nvt, sms, exposed_g);
     if (score > best_score + 0.005) {
       best_score = score;
       best = nrb;
     }
   }
   return best;
+}
+
+// Modelled GEMM time of the recomputed-logit schedule (same unit as
+// stored_cost): one forward over every row unit, then per chunk of nrb row
+// units and per vocab block of vb_tiles tiles a G-tile launch of (row units x
+// tiles) units and a dH launch of (row units x D tiles) units of K = the block.
+double recompute_cost(long long n_rb_total, int nrb, int n_dt, int nvt, int vb_tiles, int sms) {
+  const int grp = group_rows_exact(static_cast<int>(n_rb_total), sms);
+  const int splits = std::min(std::max(1, sms / grp), std::min(nvt, kMaxSplits));
+  double actual = static_cast<double>(cdiv(n_rb_total * splits, sms)) * cdiv(nvt, splits);
+  for (long long r0 = 0; r0 < n_rb_total; r0 += nrb) {
+    const long long n = std::min<long long>(nrb, n_rb_total - r0);
+    for (int t0 = 0; t0 < nvt; t0 += vb_tiles) {
+      const int w = std::min(vb_tiles, nvt - t0);
+      actual += static_cast<double>(cdiv(n * w, sms));
+      actual += static_cast<double>(cdiv(n * n_dt, sms)) * w / n_dt;
+    }
+  }
+  return actual;
 }
 
 // Workspace budget of a call in bytes (0 = none): the caller's limit, or half
@@ -192,9 +241,14 @@ size_t workspace_budget(const grpo_params* p) {
   return budget;
 }
 
-int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
+// Layout of a call with the backward form fixed (stored: fp16 logits kept per
+// chunk; else recomputed logit tiles). sms = 0: the sizing without a device
+// (the largest automatic chunk).
+int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, bool stored,
+                     Layout* L) {
   L->ctas = (p != nullptr && (p->flags & GRPO_FLAG_SINGLE_CTA) != 0) ? 1 : 2;
-  L->stored = p != nullptr && (p->flags & GRPO_FLAG_STORED_LOGITS) != 0;
+  L->stored = stored;
+  L->model_cost = 0.0;
   L->ldS = cdiv(std::max(s->vocab, 1), 8) * 8;
   L->n = s->n_tokens;
   L->nr = cdiv(std::max<long long>(s->n_tokens, 1), BM) * BM;
@@ -210,6 +264,7 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   L->vblock = L->stored ? static_cast<int>(L->ldS) : static_cast<int>(vb);
   L->need_acc = !L->stored && L->vblock < L->V;
   L->fused = L->stored && L->D <= kFusedMaxHidden;
+  L->nbox = static_cast<int>(cdiv(std::max(s->vocab, 1), 64));
 
   // Everything before the backward chunk block depends on N only.
   size_t off = kHeaderBytes;
@@ -236,6 +291,7 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   const int sbufs = L->stored && !L->fused ? 2 : 1;
   const size_t unit_bytes = static_cast<size_t>(ru_rows) *
                             (static_cast<size_t>(L->vblock) * 2 * sbufs +
+                             (L->stored ? static_cast<size_t>(L->nbox) * 4 * sbufs : 0) +
                              (L->need_acc ? L->D * 4 : 0));
   long long max_units = L->stored ? std::max(1, stored_max_blocks(L->ldS, sbufs) / L->ctas)
                                   : kMaxAutoChunkBlocks / L->ctas;
@@ -278,30 +334,39 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   // fp16 logits, rewritten in place as bf16 G [C x ldS] (stored path; two of
   // them when double-buffered).
   off = align_up(off + static_cast<size_t>(L->n_sbuf) * L->chunk_rows * L->vblock * 2, 256);
+  // Stored path: the maxima of each block's 64-column boxes, fp32 [nbox][chunk rows].
+  L->off_bmax = off;
+  if (L->stored)
+    off = align_up(off + static_cast<size_t>(L->n_sbuf) * L->nbox * L->chunk_rows * 4, 256);
   L->off_acc = off;
   if (L->need_acc) off = align_up(off + static_cast<size_t>(L->chunk_rows) * L->D * 4, 256);
   L->total = off;
   if (budget > 0 && L->total > budget) return GRPO_ERR_WORKSPACE_TOO_SMALL;
+  if (sms > 0) {
+    const int rb = static_cast<int>(L->chunk_rows / ru_rows);
+    L->model_cost = L->stored ? stored_cost(n_ru_total, rb, n_dt, L->nvt, slots,
+                                            L->fused ? 0.0 : 550.0 / L->D)
+                              : recompute_cost(n_ru_total, rb, n_dt, L->nvt,
+                                               static_cast<int>(cdiv(L->vblock, BN)), slots);
+  }
   return GRPO_OK;
 }
 
-// Row units per raster group: the slots in flight (one per SM pair) cover
-// group_rows row units x (slots / group_rows) vocab tiles or splits, so each
-// W tile fetched from HBM is shared through L2 by group_rows slots and each
-// row unit's hidden states by the others.
-int group_rows_for(int n_rb, int sms) {
-  return std::max(1, std::min(n_rb, std::max(1, sms) / kSplitsTarget));
-}
-
-// Same, with group_rows a divisor of the slot count (at least 4 columns per
-// group): a group is then exactly one round of the persistent grid, and the
-// slots that share a W range all run in the same round.
-int group_rows_exact(int n_ru, int slots) {
-  slots = std::max(1, slots);
-  const int cap = std::max(1, std::min(n_ru, slots / 4));
-  for (int r = cap; r > 1; --r)
-    if (slots % r == 0) return r;
-  return 1;
+// Layout of a call. GRPO_FLAG_STORED_LOGITS or GRPO_FLAG_RECOMPUTE_LOGITS fix
+// the backward form; without either the planner takes the stored form unless
+// it does not fit the workspace budget or its modelled GEMM time (at the
+// reference SM count, so that sizing and call agree) is longer than the
+// recomputed form's: chunks too small for whole SM waves of the dH GEMM.
+int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
+  const uint32_t f = p != nullptr ? p->flags : 0u;
+  if ((f & GRPO_FLAG_STORED_LOGITS) != 0) return make_layout_mode(s, p, sms, true, L);
+  if ((f & GRPO_FLAG_RECOMPUTE_LOGITS) != 0) return make_layout_mode(s, p, sms, false, L);
+  Layout ls, lr;
+  const int rs = make_layout_mode(s, p, kRefSms, true, &ls);
+  const int rr = make_layout_mode(s, p, kRefSms, false, &lr);
+  if (rs != GRPO_OK && rr != GRPO_OK) return rr;
+  const bool stored = rs == GRPO_OK && (rr != GRPO_OK || ls.model_cost <= lr.model_cost);
+  return make_layout_mode(s, p, sms, stored, L);
 }
 
 int check_shape(const grpo_shape* s, bool need_seq) {
@@ -320,8 +385,10 @@ int check_shape(const grpo_shape* s, bool need_seq) {
 int check_params(const grpo_params* p) {
   if (!p) return GRPO_OK;
   if ((p->flags & ~(GRPO_FLAG_STORED_LOGITS | GRPO_FLAG_SINGLE_CTA | GRPO_FLAG_SEQUENCE_MEAN |
-                    GRPO_FLAG_FIT_FREE_MEMORY)) != 0 || p->raster_rows < 0 || p->chunk_tokens < 0 ||
-      p->vocab_block < 0)
+                    GRPO_FLAG_FIT_FREE_MEMORY | GRPO_FLAG_RECOMPUTE_LOGITS)) != 0 ||
+      p->raster_rows < 0 || p->chunk_tokens < 0 || p->vocab_block < 0)
+    return GRPO_ERR_INVALID_ARG;
+  if ((p->flags & GRPO_FLAG_STORED_LOGITS) != 0 && (p->flags & GRPO_FLAG_RECOMPUTE_LOGITS) != 0)
     return GRPO_ERR_INVALID_ARG;
   if (!(p->eps_low >= 0.f) || !(p->eps_high >= 0.f) || !(p->beta >= 0.f))
     return GRPO_ERR_INVALID_ARG;
@@ -675,6 +742,10 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     return reinterpret_cast<uint16_t*>(w.G) +
            (overlap ? static_cast<size_t>(c & 1) * L.chunk_rows * L.ldS : 0);
   };
+  auto bmax = [&](int c) {
+    return reinterpret_cast<float*>(w.base + L.off_bmax) +
+           (overlap ? static_cast<size_t>(c & 1) * L.nbox * L.chunk_rows : 0);
+  };
   auto chunk_rbs = [&](int c) { return std::min(rb_per_chunk, n_rb_total - c * rb_per_chunk); };
 
   // (1) logits of chunk c: online LSE partials, z_y, fp16 copy.
@@ -702,6 +773,8 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     a.part_ld = L.nr;
     a.S = sbuf(c);
     a.ldS = L.ldS;
+    a.box_max = bmax(c);
+    a.ldM = L.chunk_rows;
     // The pair variant stores each warp's 32 rows x 64 logits through TMA.
     CUtensorMap map_st;
     if (!encode_2d(&map_st, a.S, L.V, static_cast<uint64_t>(n_rb) * BM, L.ldS, 64, 32))
@@ -748,6 +821,8 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     f.lt = w.lt;
     f.S = sbuf(c);
     f.ldS = L.ldS;
+    f.box_max = bmax(c);
+    f.ldM = L.chunk_rows;
     TileArgs t = base_args(L, w);
     set_transform(&t, prm);
     f.xmode = t.xmode;
@@ -825,6 +900,8 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     b.lse = w.lse;
     b.g = w.g;
     b.zy = w.zy;
+    b.box_max = bmax(c);
+    b.ldM = L.chunk_rows;
     b.dH = static_cast<__nv_bfloat16*>(dH);
     b.first = 1;
     b.last = 1;
@@ -889,6 +966,7 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
   fin.block_partials = w.partials;
   fin.counter = w.counter;
   fin.loss_out = loss;
+  fin.status = w.status;
   if (launch_finish_loss(fin, st) != cudaSuccess) return GRPO_ERR_CUDA;
   return GRPO_OK;
 }
@@ -1190,6 +1268,7 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
         stored_fwd_splits(L.chunk_rows / (BM * L.ctas), L.nvt, slots, nullptr);
   }
   info->g_in_dh_gemm = L.fused ? 1 : 0;
+  info->stored_logits = L.stored ? 1 : 0;
   info->workspace_bytes = std::max(L.total, Lmax.total);
   return GRPO_OK;
 }
@@ -1285,6 +1364,7 @@ const char* grpo_status_string(int s) {
     case GRPO_ERR_CUDA: return "CUDA runtime or driver error";
     case GRPO_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case GRPO_ERR_BAD_TOKEN_ID: return "token id outside [0, vocab) on an unmasked row";
+    case GRPO_ERR_NONFINITE: return "log-sum-exp of a row is not finite (inf/NaN inputs)";
     default: return "unknown status";
   }
 }

@@ -164,6 +164,9 @@ __global__ void __launch_bounds__(kFinalizeThreads) finalize_kernel(const Finali
   __shared__ double sh[32];
   __shared__ bool is_last;
   double local = 0.0;
+  // A wait of the logit GEMM that ran out leaves its partials incomplete:
+  // every output of the call is then NaN (the status word says why).
+  const bool aborted = *reinterpret_cast<const volatile int*>(a.status) == GRPO_ERR_DEVICE_TIMEOUT;
   for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < a.n;
        t += static_cast<long long>(gridDim.x) * blockDim.x) {
     const bool counted = !a.loss_mode || a.mask == nullptr || a.mask[t] != 0;
@@ -177,6 +180,8 @@ __global__ void __launch_bounds__(kFinalizeThreads) finalize_kernel(const Finali
       for (int s = 0; s < a.splits; ++s)
         ssum += a.part_s[s * a.part_ld + t] * exp2f(a.part_m[s * a.part_ld + t] - m2);
       lse = (m2 + log2f(ssum)) * 0.69314718055994531f;
+      if (aborted) lse = __int_as_float(0x7fc00000);
+      else if (!isfinite(lse)) atomicCAS(a.status, 0, GRPO_ERR_NONFINITE);
     }
     a.lse_ws[t] = lse;
     if (a.lse_out) a.lse_out[t] = lse;
@@ -232,7 +237,7 @@ __global__ void __launch_bounds__(kFinalizeThreads) finalize_kernel(const Finali
       v += reinterpret_cast<volatile double*>(a.block_partials)[i];
     const double tot = block_sum(v, sh);
     if (threadIdx.x == 0) {
-      *a.loss_out = static_cast<float>(tot);
+      *a.loss_out = aborted ? __int_as_float(0x7fc00000) : static_cast<float>(tot);
       *a.counter = 0;
     }
   }
@@ -316,6 +321,7 @@ __device__ __forceinline__ void finish_row(const GformArgs& a, long long grow, f
   for (int s = 0; s < a.splits; ++s)
     ssum += a.part_s[s * a.part_ld + grow] * exp2f(a.part_m[s * a.part_ld + grow] - m2);
   lse = (m2 + log2f(ssum)) * 0.69314718055994531f;
+  if (!isfinite(lse)) atomicCAS(a.status, 0, GRPO_ERR_NONFINITE);
   y = a.ids[grow];
   float logp;
   if (y < 0 || y >= a.vocab) {
@@ -377,6 +383,10 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
     for (int i = threadIdx.x; i < n_vec; i += blockDim.x) row[i] = make_uint4(0, 0, 0, 0);
     return;
   }
+  // Stored value of column v: z'_v - m_b, m_b the maximum of its 64-column box
+  // b = v / 64 (vector i of 8 columns lies in box i / 8).
+  const float* bm = a.box_max + lrow;
+  auto box_max = [&](int i) { return __ldg(bm + static_cast<long long>(i >> 3) * a.ldM); };
   if (a.xmode == 0) {
     // Without a transform: -g 2^(z log2e - lse2) = -sign(g) 2^(z log2e + log2|g| - lse2),
     // one FFMA and one exponential per logit and the sign set on each packed
@@ -384,14 +394,15 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
     // up afterwards.
     const float c = log2f(fabsf(g)) - lse2;
     const uint32_t sgn = g > 0.f ? 0x80008000u : 0u;
-    auto fast = [&](const uint4 in) {
+    auto fast = [&](const uint4 in, float mb) {
+      const float cb = fmaf(mb, kLog2e, c);
       const uint32_t w[4] = {in.x, in.y, in.z, in.w};
       uint32_t o[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         float z0, z1;
         unpack_f16x2(w[k], z0, z1);
-        o[k] = pack_bf16x2(ex2(fmaf(z0, kLog2e, c)), ex2(fmaf(z1, kLog2e, c))) ^ sgn;
+        o[k] = pack_bf16x2(ex2(fmaf(z0, kLog2e, cb)), ex2(fmaf(z1, kLog2e, cb))) ^ sgn;
       }
       return make_uint4(o[0], o[1], o[2], o[3]);
     };
@@ -400,10 +411,11 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
     for (; i + blockDim.x < n_vec; i += step) {
       const uint4 in0 = row[i];
       const uint4 in1 = row[i + blockDim.x];
-      row[i] = fast(in0);
-      row[i + blockDim.x] = fast(in1);
+      const float m0 = box_max(i), m1 = box_max(i + blockDim.x);
+      row[i] = fast(in0, m0);
+      row[i + blockDim.x] = fast(in1, m1);
     }
-    if (i < n_vec) row[i] = fast(row[i]);
+    if (i < n_vec) row[i] = fast(row[i], box_max(i));
     __syncthreads();  // the whole row is written before the fix-ups
     uint16_t* row16 = a.S + static_cast<long long>(lrow) * a.ldS;
     if (threadIdx.x == 0 && y >= 0) {
@@ -418,6 +430,7 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
   // G_v from the stored z'_v: g (onehot_v(y) - exp(z'_v - lse)) f'(z_v).
   auto convert = [&](const uint4 in, int i) {
     const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    const float mb = i * 8 < a.vocab ? box_max(i) : 0.f;
     uint32_t o[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -425,7 +438,7 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int v = i * 8 + k * 2 + h;
-        const float z = half_bits_to_float(h == 0 ? (w[k] & 0xffffu) : (w[k] >> 16));
+        const float z = half_bits_to_float(h == 0 ? (w[k] & 0xffffu) : (w[k] >> 16)) + mb;
         float d = 1.f;  // dz'/dz recovered from the stored z'
         if (a.xmode == 1) {
           d = a.k0;
@@ -459,10 +472,14 @@ __global__ void __launch_bounds__(kFinalizeThreads) finish_loss_kernel(const Fin
   __shared__ double sh[32];
   __shared__ bool is_last;
   double local = 0.0;
+  // After a wait that ran out anywhere in the call, logp and the loss are NaN.
+  const bool aborted = *reinterpret_cast<const volatile int*>(a.status) == GRPO_ERR_DEVICE_TIMEOUT;
   for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < a.n;
        t += static_cast<long long>(gridDim.x) * blockDim.x) {
     const bool counted = a.mask == nullptr || a.mask[t] != 0;
-    if (counted) {
+    if (aborted) {
+      if (a.logp_out) a.logp_out[t] = __int_as_float(0x7fc00000);
+    } else if (counted) {
       local += a.lt[t];
     } else if (a.logp_out) {
       a.logp_out[t] = 0.f;
@@ -483,7 +500,7 @@ __global__ void __launch_bounds__(kFinalizeThreads) finish_loss_kernel(const Fin
       v += reinterpret_cast<volatile double*>(a.block_partials)[i];
     const double tot = block_sum(v, sh);
     if (threadIdx.x == 0) {
-      *a.loss_out = static_cast<float>(tot);
+      *a.loss_out = aborted ? __int_as_float(0x7fc00000) : static_cast<float>(tot);
       *a.counter = 0;
     }
   }

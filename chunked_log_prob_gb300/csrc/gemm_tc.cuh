@@ -83,9 +83,12 @@ struct TileArgs {
   const float* g;        // indexed by global row
   __nv_bfloat16* G;      // [local rows][ldG] chunk workspace
   long long ldG;
-  // MODE_FWDS
-  uint16_t* S;           // [local rows][ldS] fp16 logits of the chunk
+  // MODE_FWDS (written), MODE_DHS (read)
+  uint16_t* S;           // [local rows][ldS] fp16 logits of the chunk, each 64-column
+                         // box stored relative to its own maximum
   long long ldS;
+  float* box_max;        // [ceil(V / 64)][ldM] those maxima (fp32), box-major
+  long long ldM;         // rows of the chunk block (stride between boxes)
   // MODE_DW
   float* dW;             // [V][hidden] fp32 output / accumulator
   int dw_rows;           // vocab rows of dW this launch covers (from v0)
@@ -175,9 +178,10 @@ __device__ __forceinline__ int swz_offset(int r, int c) {
 }
 
 // MODE_DHS: rewrites chunks jb..jb+NCH-1 (8 columns each) of row r of a
-// landed A stage (64 fp16 logits z' of vocab columns vbase..) in place as the
-// bf16 G values,
+// landed A stage (one stored box: 64 fp16 values z'_v - zoff of vocab columns
+// vbase.., zoff the box's maximum) in place as the bf16 G values,
 //   G_v = g (onehot_v(y) - 2^(z'_v log2e - lse2)) f'(S_v).
+// c = log2|g| - lse2 + zoff log2e folds the row's and the box's constants.
 // Rows with g = 0 (masked, padding, past N) become zeros whatever the buffer
 // held; columns at or past the vocabulary size become zeros. The main loop
 // runs over logical chunks, so the 8 lanes of a shared-memory phase (8
@@ -188,7 +192,7 @@ __device__ __forceinline__ int swz_offset(int r, int c) {
 template <int NCH>
 __device__ __forceinline__ void logits_to_g_row(const TileArgs& a, uint8_t* tile, int r, int jb,
                                                 int vbase, int y, float g, float lse2,
-                                                float zy, float c, uint32_t sgn) {
+                                                float zy, float c, uint32_t sgn, float zoff) {
   uint4* row = reinterpret_cast<uint4*>(tile + r * 128);
   const int sw = r & 7;
   if (g == 0.f) {
@@ -224,6 +228,8 @@ __device__ __forceinline__ void logits_to_g_row(const TileArgs& a, uint8_t* tile
       for (int e = 0; e < 4; ++e) {
         float z0, z1;
         unpack_f16x2(w[e], z0, z1);
+        z0 += zoff;
+        z1 += zoff;
         o[e] = pack_bf16x2(ng * ex2(fmaf(z0, kLog2e, -lse2)) * dz_of_logit(a, z0),
                            ng * ex2(fmaf(z1, kLog2e, -lse2)) * dz_of_logit(a, z1));
       }
@@ -664,7 +670,21 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
       if constexpr (MODE == MODE_DHS) {
         // Every A stage of this unit, as it lands: fp16 logits -> bf16 G in
         // place (this thread's part of its row), then tell the MMA issuer.
+        // Stage k is box (v0 / 64) + k; its maximum is loaded kPre stages
+        // ahead (rows with g = 0 need none).
+        constexpr int kPre = 4;
+        const float* bm = args.box_max + static_cast<long long>(args.v0 >> 6) * args.ldM + lrow;
+        float zq[kPre];
+#pragma unroll
+        for (int j = 0; j < kPre; ++j)
+          zq[j] = (gval != 0.f && j < k_iters) ? __ldg(bm + j * args.ldM) : 0.f;
         for (int k = 0; k < k_iters; ++k, ++cit) {
+          const float zoff = zq[0];
+#pragma unroll
+          for (int j = 0; j + 1 < kPre; ++j) zq[j] = zq[j + 1];
+          zq[kPre - 1] = (gval != 0.f && k + kPre < k_iters)
+                             ? __ldg(bm + static_cast<long long>(k + kPre) * args.ldM)
+                             : 0.f;
           const int s = static_cast<int>(cit % kStages);
           if (!mbar_wait(&afull_bar[s], (cit / kStages) & 1u, abort_flag, args.status)) {
             ok = false;
@@ -672,7 +692,8 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
           }
           constexpr int kNch = 8 / C::kCvtGroups;
           logits_to_g_row<kNch>(args, smem + s * C::kStageBytes, lrow_in_tile, part * kNch,
-                                args.v0 + k * BK, y, gval, lse2, zyv, cexp, sgn);
+                                args.v0 + k * BK, y, gval, lse2, zyv,
+                                fmaf(zoff, kLog2e, cexp), sgn, zoff);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -694,7 +715,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
         tc_fence_after();
         const uint32_t tbase = tmem_base + lane_addr + buf * BN;
 
-        if (is_fwd(MODE)) {
+        if (MODE == MODE_FWD) {
 #pragma unroll 1
           for (int c = 0; c < C::kTileN / 32; ++c) {
             const int col0 = t * C::kTileN + c * 32;
@@ -702,51 +723,6 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             float v[32];
             tmem_ld32(tbase + c * 32, v);
             logit_transform(args, v);
-            if constexpr (C::kTmaStore) {
-              if (block_ok) {
-                // Chunk c fills 16-byte pieces 4 (c & 1) .. +3 of this row of
-                // the 64-column box; a box is stored once complete or where
-                // the vocabulary ends (the store clips columns past V).
-                uint8_t* buf = stage_out + (n_stores & 1u) * C::kStoreBufBytes;
-                if ((c & 1) == 0) {
-                  if (lane == 0) bulk_wait_group_read<1>();  // this buffer's last store read it
-                  __syncwarp();
-                }
-                uint4* srow = reinterpret_cast<uint4*>(buf + lane * 128);
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  srow[((c & 1) * 4 + j) ^ (lane & 7)] =
-                      make_uint4(pack_f16x2(v[8 * j], v[8 * j + 1]),
-                                 pack_f16x2(v[8 * j + 2], v[8 * j + 3]),
-                                 pack_f16x2(v[8 * j + 4], v[8 * j + 5]),
-                                 pack_f16x2(v[8 * j + 6], v[8 * j + 7]));
-                if ((c & 1) == 1 || col0 + 32 >= args.vocab) {
-                  fence_proxy_async_smem();
-                  __syncwarp();
-                  if (lane == 0) {
-                    tma_store_2d(&map_c, buf, col0 & ~63, li * BM + q * 32);
-                    bulk_commit_group();
-                  }
-                  ++n_stores;
-                }
-              }
-            } else if (MODE == MODE_FWDS && valid) {
-              uint16_t* dst = args.S + static_cast<long long>(lrow) * args.ldS + col0;
-              if (col0 + 32 <= args.vocab) {
-                uint32_t hpk[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) hpk[j] = pack_f16x2(v[2 * j], v[2 * j + 1]);
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  st_global_v4(dst + j * 8, hpk[4 * j], hpk[4 * j + 1], hpk[4 * j + 2],
-                               hpk[4 * j + 3]);
-              } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  if (col0 + j < args.vocab)
-                    dst[j] = static_cast<uint16_t>(pack_f16x2(v[j], 0.f) & 0xffffu);
-              }
-            }
             if (col0 + 32 > args.vocab) {
 #pragma unroll
               for (int j = 0; j < 32; ++j)
@@ -778,6 +754,114 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             ssum = fmaf(ssum, ex2(m2 - mn), (s0 + s1) + (s2 + s3));
             m2 = mn;
           }
+        } else if (MODE == MODE_FWDS) {
+          // One 64-column box at a time. The box is stored in fp16 relative to
+          // its own maximum, which goes beside it in fp32 (box-major, so a warp
+          // writes 32 consecutive rows). Stored values then lie in [-inf, 0]:
+          // no logit overflows fp16, and the columns near the box maximum (the
+          // ones that carry probability) keep fp16's finest spacing whatever
+          // the logits' magnitude. Unshifted, a logit near 40 kept only
+          // 2^-6 of absolute precision, i.e. 1.6 % of its softmax term.
+#pragma unroll 1
+          for (int c = 0; c < C::kTileN / 64; ++c) {
+            const int col0 = t * C::kTileN + c * 64;
+            if (col0 >= args.vocab) break;  // warp-uniform
+            float lo[32], hi[32];
+            tmem_ld32(tbase + c * 64, lo);
+            tmem_ld32(tbase + c * 64 + 32, hi);
+            logit_transform(args, lo);
+            logit_transform(args, hi);
+            if (col0 + 64 > args.vocab) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                if (col0 + j >= args.vocab) lo[j] = -INFINITY;
+                if (col0 + 32 + j >= args.vocab) hi[j] = -INFINITY;
+              }
+            }
+            float mx0 = fmaxf(lo[0], hi[0]), mx1 = fmaxf(lo[1], hi[1]);
+#pragma unroll
+            for (int j = 2; j < 32; j += 2) {
+              mx0 = fmaxf(mx0, fmaxf(lo[j], hi[j]));
+              mx1 = fmaxf(mx1, fmaxf(lo[j + 1], hi[j + 1]));
+            }
+            const float mb = fmaxf(mx0, mx1);  // finite: col0 < V
+            const unsigned off = static_cast<unsigned>(y - col0);
+            if (off < 64u) {
+              float z = 0.f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                if (static_cast<unsigned>(j) == off) z = lo[j];
+                if (static_cast<unsigned>(j + 32) == off) z = hi[j];
+              }
+              args.zy[grow] = z;
+            }
+            if constexpr (C::kTmaStore) {
+              if (block_ok) {
+                // The box fills one 32-row x 128-byte staging buffer; the
+                // store clips the columns past V.
+                uint8_t* buf = stage_out + (n_stores & 1u) * C::kStoreBufBytes;
+                if (lane == 0) bulk_wait_group_read<1>();  // this buffer's last store read it
+                __syncwarp();
+                uint4* srow = reinterpret_cast<uint4*>(buf + lane * 128);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  srow[j ^ (lane & 7)] =
+                      make_uint4(pack_f16x2(lo[8 * j] - mb, lo[8 * j + 1] - mb),
+                                 pack_f16x2(lo[8 * j + 2] - mb, lo[8 * j + 3] - mb),
+                                 pack_f16x2(lo[8 * j + 4] - mb, lo[8 * j + 5] - mb),
+                                 pack_f16x2(lo[8 * j + 6] - mb, lo[8 * j + 7] - mb));
+                  srow[(4 + j) ^ (lane & 7)] =
+                      make_uint4(pack_f16x2(hi[8 * j] - mb, hi[8 * j + 1] - mb),
+                                 pack_f16x2(hi[8 * j + 2] - mb, hi[8 * j + 3] - mb),
+                                 pack_f16x2(hi[8 * j + 4] - mb, hi[8 * j + 5] - mb),
+                                 pack_f16x2(hi[8 * j + 6] - mb, hi[8 * j + 7] - mb));
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                  tma_store_2d(&map_c, buf, col0, li * BM + q * 32);
+                  bulk_commit_group();
+                }
+                ++n_stores;
+                args.box_max[static_cast<long long>(col0 >> 6) * args.ldM + lrow] = mb;
+              }
+            } else if (valid) {
+              uint16_t* dst = args.S + static_cast<long long>(lrow) * args.ldS + col0;
+              if (col0 + 64 <= args.vocab) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  st_global_v4(dst + j * 8, pack_f16x2(lo[8 * j] - mb, lo[8 * j + 1] - mb),
+                               pack_f16x2(lo[8 * j + 2] - mb, lo[8 * j + 3] - mb),
+                               pack_f16x2(lo[8 * j + 4] - mb, lo[8 * j + 5] - mb),
+                               pack_f16x2(lo[8 * j + 6] - mb, lo[8 * j + 7] - mb));
+                  st_global_v4(dst + 32 + j * 8, pack_f16x2(hi[8 * j] - mb, hi[8 * j + 1] - mb),
+                               pack_f16x2(hi[8 * j + 2] - mb, hi[8 * j + 3] - mb),
+                               pack_f16x2(hi[8 * j + 4] - mb, hi[8 * j + 5] - mb),
+                               pack_f16x2(hi[8 * j + 6] - mb, hi[8 * j + 7] - mb));
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  if (col0 + j < args.vocab)
+                    dst[j] = static_cast<uint16_t>(pack_f16x2(lo[j] - mb, 0.f) & 0xffffu);
+                  if (col0 + 32 + j < args.vocab)
+                    dst[32 + j] = static_cast<uint16_t>(pack_f16x2(hi[j] - mb, 0.f) & 0xffffu);
+                }
+              }
+              args.box_max[static_cast<long long>(col0 >> 6) * args.ldM + lrow] = mb;
+            }
+            const float mn = fmaxf(m2, mb * kLog2e);
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              s0 += ex2(fmaf(lo[j], kLog2e, -mn));
+              s1 += ex2(fmaf(lo[j + 1], kLog2e, -mn));
+              s2 += ex2(fmaf(hi[j], kLog2e, -mn));
+              s3 += ex2(fmaf(hi[j + 1], kLog2e, -mn));
+            }
+            ssum = fmaf(ssum, ex2(m2 - mn), (s0 + s1) + (s2 + s3));
+            m2 = mn;
+          }
         } else if (MODE == MODE_BWDG) {
           __nv_bfloat16* grow_ptr = args.G + static_cast<long long>(lrow) * args.ldG + t * BN;
 #pragma unroll 1
@@ -787,7 +871,13 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             tmem_ld32(tbase + c * 32, v);
             const float ng = -gval;
             const unsigned off = static_cast<unsigned>(y - col0);
-            if (args.xmode != 2) {
+            if (gval == 0.f) {
+              // Rows that do not count (masked, padding, past N): exact zeros.
+              // Their lse is 0, so the exponential below could overflow and
+              // 0 * inf would leave NaN in G.
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            } else if (args.xmode != 2) {
               // z' = k S (k = 1 without a transform): G = k g (onehot - p).
               const float k = args.xmode == 1 ? args.k0 : 1.f;
               const float kl = k * kLog2e;

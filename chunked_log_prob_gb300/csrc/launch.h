@@ -66,8 +66,11 @@ struct GformArgs {
   double* lt;            // [N] weighted token loss w_t l_t of unmasked rows
   float* lse_out;        // finalize_rows: [rows] lse (natural log), by global row
   float* g_out;          // finalize_rows: [rows] dL/dlogp (0 for rows that do not count)
-  uint16_t* S;           // [chunk rows][ldS]: fp16 logits in, bf16 G out
+  uint16_t* S;           // [chunk rows][ldS]: fp16 logits in (each 64-column box
+                         // relative to its maximum), bf16 G out
   long long ldS;
+  const float* box_max;  // [ceil(V / 64)][ldM] the boxes' maxima
+  long long ldM;
   int xmode;
   float k0, k2;
   int* status;
@@ -75,6 +78,7 @@ struct GformArgs {
 
 struct FinishArgs {
   long long n;
+  const int* status;     // the call's status word (a timed-out wait -> NaN outputs)
   const uint8_t* mask;
   const double* lt;
   float* logp_out;

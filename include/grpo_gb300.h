@@ -15,8 +15,10 @@
  * old policy and a beta-weighted k3 reverse-KL term against the reference
  * policy ("Unsloth internals", section "The relationship to TRL"; "Train
  * reasoning models with 5GB VRAM", section "Under the Hood"), and its
- * gradient to the hidden states, obtained by recomputing the logit tiles
- * (same Unsloth docs page, section "Offloading activations for log-softmax").
+ * gradient to the hidden states, obtained either by recomputing the logit
+ * tiles as the pages' backward does (same Unsloth docs page, section
+ * "Offloading activations for log-softmax") or from each chunk's logits kept
+ * in fp16, which saves that second logit GEMM.
  *
  * Conventions shared by every entry point:
  *   - All tensor arguments are DEVICE pointers on the current CUDA device,
@@ -30,8 +32,10 @@
  *     (a cudaStream_t; NULL = the legacy default stream).
  *   - Return value: GRPO_OK (0) or a negative grpo_status. Argument checks
  *     happen on the host before anything is launched; problems found on the
- *     device (out-of-range token ids, a timed-out wait) are recorded in the
- *     workspace's status word, read back with grpo_read_device_status.
+ *     device (out-of-range token ids, a non-finite log-sum-exp, a timed-out
+ *     wait) are recorded in the workspace's status word, read back with
+ *     grpo_read_device_status. After a timed-out wait the call's logp, lse
+ *     and loss are NaN, and its dH (and dW) are undefined.
  *   - Two calls that share a workspace must not overlap on the GPU. Calls
  *     with separate workspaces may run concurrently from several host
  *     threads; the stored-logit path's side stream (one per device, created
@@ -58,7 +62,10 @@ typedef enum grpo_status {
   GRPO_ERR_UNSUPPORTED_DEVICE = -5, /* not an sm_103 GPU                      */
   GRPO_ERR_CUDA = -6,               /* a CUDA runtime/driver call failed      */
   GRPO_ERR_DEVICE_TIMEOUT = -7,     /* (device) a bounded wait ran out        */
-  GRPO_ERR_BAD_TOKEN_ID = -8        /* (device) unmasked id outside [0, V)   */
+  GRPO_ERR_BAD_TOKEN_ID = -8,       /* (device) unmasked id outside [0, V)   */
+  GRPO_ERR_NONFINITE = -9           /* (device) a row's log-sum-exp is inf or
+                                       NaN: the inputs hold inf/NaN or logits
+                                       beyond the fp32 range                 */
 } grpo_status;
 
 typedef struct grpo_shape {
@@ -69,17 +76,33 @@ typedef struct grpo_shape {
   int32_t reserved; /* must be 0                                              */
 } grpo_shape;
 
-/* grpo_params.flags bit: backward without a second logit GEMM. Per chunk of
+/* The backward form. Two exist; without either of the two flags below the
+ * call chooses (the default):
+ *   - stored logits (GRPO_FLAG_STORED_LOGITS): 4 N D V flops, a workspace
+ *     of chunk x V x 2 bytes (and twice that at D > 2048, see below);
+ *   - recomputed logit tiles (GRPO_FLAG_RECOMPUTE_LOGITS): 6 N D V flops
+ *     (the pages' backward, which re-runs the forward), a workspace of
+ *     chunk x vocab_block x 2 bytes plus a chunk x D fp32 accumulator.
+ * The automatic choice is the stored form unless it does not fit the
+ * workspace budget (workspace_limit_bytes, or half the free device memory
+ * with GRPO_FLAG_FIT_FREE_MEMORY), or its modelled GEMM time within that
+ * budget is longer than the recomputed form's (chunks too small for whole SM
+ * waves of the dH GEMM). The choice is made at GB300's SM count, so that
+ * grpo_workspace_size and the call agree; grpo_get_plan reports it.
+ *
+ * grpo_params.flags bit: backward without a second logit GEMM. Per chunk of
  * rows, the forward GEMM also keeps the chunk's (transformed) logits in fp16
  * in the workspace, and the dH GEMM runs over the whole vocabulary once lse
- * and g are known. The logits are turned into G in one of two ways:
+ * and g are known. Each 64-column box of a row is stored relative to its own
+ * maximum (kept beside it in fp32), so any finite logit is stored without
+ * overflow and the box's largest terms keep fp16's finest spacing. The logits
+ * are turned into G in one of two ways:
  *   - D <= 2048 without dW: the dH GEMM converts each landed tile on chip.
  *     One block of chunk x V x 2 bytes (capped at 4 GiB) serves every chunk.
  *   - otherwise: a row-wise pass rewrites the block in place, beside the next
  *     chunk's GEMMs. Two blocks when there is more than one chunk (each capped
  *     at 2 GiB).
- * Executes 4 N D V instead of 6 N D V flops; vocab_block is ignored. Logits
- * must stay within fp16 range (|z'| < 65504). */
+ * Executes 4 N D V instead of 6 N D V flops; vocab_block is ignored. */
 #define GRPO_FLAG_STORED_LOGITS 1u
 
 /* grpo_params.flags bit: run every GEMM as one CTA per 128-row tile instead
@@ -99,6 +122,12 @@ typedef struct grpo_shape {
  * smaller) - the pages' "adjust to the available VRAM". With this flag
  * grpo_workspace_size queries the current device (no allocation, no launch). */
 #define GRPO_FLAG_FIT_FREE_MEMORY 8u
+
+/* grpo_params.flags bit: the backward recomputes the logit tiles chunk by
+ * chunk and vocab block by vocab block (G = g (onehot - softmax) formed in
+ * the GEMM's epilogue, then dH += G W[block]): the smallest workspace.
+ * Setting it together with GRPO_FLAG_STORED_LOGITS is GRPO_ERR_INVALID_ARG. */
+#define GRPO_FLAG_RECOMPUTE_LOGITS 16u
 
 typedef struct grpo_params {
   float eps_low;          /* ratio clip: lower bound 1 - eps_low (0.2)         */
@@ -129,7 +158,8 @@ typedef struct grpo_params {
 
 /* Defaults: eps 0.2/0.2, beta 0.001 (the pages' corrected GRPO default,
  * "How does Unsloth implement GRPO", section "Corrected hyperparameters"),
- * token-mean denominator, automatic chunking, no logit transform. Host only. */
+ * token-mean denominator, automatic chunking and backward form, no workspace
+ * budget, no logit transform. Host only. */
 void grpo_default_params(grpo_params* params);
 
 /* Bytes of device workspace that grpo_loss_fwd_bwd needs for this shape and
@@ -192,6 +222,10 @@ typedef struct grpo_plan_info {
   int32_t g_in_dh_gemm;      /* 1: the stored-logit backward forms G inside
                                 the dH GEMM when dW is not requested (hidden
                                 <= 2048); 0: in a pass of its own          */
+  int32_t stored_logits;     /* 1: the stored-logit backward; 0: recomputed
+                                logit tiles (the flags' or the automatic
+                                choice)                                    */
+  int32_t reserved;
   uint64_t workspace_bytes;  /* same as grpo_workspace_size                  */
 } grpo_plan_info;
 
@@ -220,6 +254,9 @@ int grpo_read_device_status(const void* workspace, int* device_status, void* str
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture begins.
+ *   - If a wait inside the call runs out (GRPO_ERR_DEVICE_TIMEOUT, which the
+ *     workspace calls report in their status word), every logp and lse of
+ *     the call is NaN: this call has no status word the caller can read.
  *   - All calls share the one array, which keeps the previous call's
  *     contents; each call clears the parts that must start at zero. Two calls
  *     that overlap on the GPU (different streams, no ordering between them)

@@ -42,7 +42,7 @@ def test_library_is_loaded_in_process(clp):
 
 
 def test_status_strings(clp):
-    for code in range(0, -9, -1):
+    for code in range(0, -10, -1):
         assert clp.status_string(code) != "unknown status"
     assert clp.status_string(-99) == "unknown status"
 
@@ -54,8 +54,9 @@ def test_default_params(clp):
 
 
 def test_workspace_independent_of_vocab_times_tokens(clp):
-    # Grows with N (a few fp32 per row) and with chunk x vocab block, never N x V.
-    p = clp.make_params(chunk_tokens=1024, vocab_block=8192)
+    # Recomputed backward: grows with N (a few fp32 per row) and with chunk x
+    # vocab block, never N x V.
+    p = clp.make_params(chunk_tokens=1024, vocab_block=8192, flags=16)
     sizes = [clp.grpo_workspace_size(n, 4096, 128256, 1, p) for n in (4096, 16384, 65536)]
     per_row = (sizes[2] - sizes[1]) / (65536 - 16384)
     assert per_row < 64 * 4 * 2 + 64  # split partials + a few fp32 per row
@@ -71,10 +72,10 @@ def test_workspace_grows_with_chunk(clp):
 
 
 def test_single_vocab_block_needs_no_accumulator(clp):
-    big = clp.grpo_workspace_size(1024, 4096, 4096, 1, clp.make_params(chunk_tokens=1024,
-                                                                       vocab_block=4096))
-    small = clp.grpo_workspace_size(1024, 4096, 4096, 1, clp.make_params(chunk_tokens=1024,
-                                                                         vocab_block=2048))
+    big = clp.grpo_workspace_size(1024, 4096, 4096, 1, clp.make_params(
+        chunk_tokens=1024, vocab_block=4096, flags=16))
+    small = clp.grpo_workspace_size(1024, 4096, 4096, 1, clp.make_params(
+        chunk_tokens=1024, vocab_block=2048, flags=16))
     assert small - big > 1024 * 4096 * 4 - 1024 * 2048 * 2 - 4096
 
 
@@ -91,10 +92,35 @@ def test_workspace_size_rejects_bad_shapes(clp, n, d, v, want):
 
 def test_bad_params_rejected(clp):
     p = clp.make_params()
-    p.flags = 16  # not a defined flag bit
+    p.flags = 32  # not a defined flag bit
     with pytest.raises(clp.GrpoError) as e:
         clp.grpo_workspace_size(10, 16, 50, 1, p)
     assert e.value.code == -1
+    p.flags = 1 | 16  # both backward forms at once
+    with pytest.raises(clp.GrpoError) as e:
+        clp.grpo_workspace_size(10, 16, 50, 1, p)
+    assert e.value.code == -1
+
+
+def test_automatic_backward_form_follows_the_budget(clp):
+    # Flags 0 (the default) choose the backward form: the stored one when the
+    # workspace budget leaves room for chunks that fill the SMs, the
+    # recomputed one under a tight budget. The choice is made at a fixed SM
+    # count, so the sizing here (no device) is the call's own.
+    STORED, RECOMPUTE = 1, 16
+    n, d, v, t = 16384, 4096, 128256, 4096
+
+    def ws(flags, limit=0):
+        return clp.grpo_workspace_size(n, d, v, t, clp.make_params(
+            flags=flags, workspace_limit_bytes=limit))
+    assert ws(0) == ws(STORED)
+    assert ws(0, 8 << 30) == ws(STORED, 8 << 30)
+    assert ws(0, 512 << 20) == ws(RECOMPUTE, 512 << 20) < ws(STORED, 512 << 20)
+    # Below the stored form's smallest chunk (two logit blocks of 256 rows),
+    # only the recomputed form fits.
+    with pytest.raises(clp.GrpoError):
+        ws(STORED, 128 << 20)
+    assert ws(0, 128 << 20) == ws(RECOMPUTE, 128 << 20) <= 128 << 20
 
 
 def test_null_pointers_rejected_before_launch(clp):
@@ -126,20 +152,27 @@ def test_misaligned_pointers_rejected(clp):
     assert rc == -2
 
 
+def stored_block(chunk, V):
+    """One stored-logit block: fp16 logits of chunk x V (V padded to 8) and the
+    fp32 maximum of every 64-column box of each row."""
+    return chunk * (-(-V // 8) * 8 * 2 + -(-V // 64) * 4)
+
+
 def test_stored_logit_workspace_is_chunk_times_vocab(clp):
-    # Stored-logit backward: two fp16 logit blocks of chunk x V (V padded to 8;
-    # double-buffered when there is more than one chunk), independent of N.
+    # Stored-logit backward: two blocks of chunk x V (double-buffered when
+    # there is more than one chunk), independent of N.
     p = clp.make_params(chunk_tokens=2048, flags=1)
     a = clp.grpo_workspace_size(16384, 4096, 128256, 1, p)
     b = clp.grpo_workspace_size(65536, 4096, 128256, 1, p)
-    block = 2048 * 128256 * 2
+    block = stored_block(2048, 128256)
     assert 2 * block < a < 2 * block + 16384 * 400
     one = clp.grpo_workspace_size(2048, 4096, 128256, 1, p)  # a single chunk: one block
     assert block < one < block + 2048 * 400
     assert (b - a) / (65536 - 16384) < 64 * 4 * 2 + 64
-    # Automatic chunk without a device: bounded by 2 GiB of logits.
+    # Automatic chunk without a device: bounded by 2 GiB of fp16 logits per
+    # block (plus their box maxima, 1/32 of that).
     auto = clp.grpo_workspace_size(131072, 2880, 201088, 1, clp.make_params(flags=1))
-    assert auto < 2 * (2 << 30) + 131072 * 400
+    assert auto < 2 * (2 << 30) * (1 + 1 / 32) + 131072 * 400
 
 
 def test_stored_logit_workspace_single_block_up_to_2048_hidden(clp):
@@ -147,16 +180,16 @@ def test_stored_logit_workspace_single_block_up_to_2048_hidden(clp):
     # logit block serves every chunk (no double buffering); larger chunks
     # are allowed in exchange (4 GiB of logits instead of 2 x 2 GiB).
     p = clp.make_params(chunk_tokens=2048, flags=1)
-    block = 2048 * 151936 * 2
+    block = stored_block(2048, 151936)
     small = clp.grpo_workspace_size(32768, 2048, 151936, 1, p)
     assert block < small < block + 32768 * 400
     big = clp.grpo_workspace_size(32768, 2056, 151936, 1, p)
     assert 2 * block < big < 2 * block + 32768 * 400
     auto = clp.grpo_workspace_size(131072, 1536, 151936, 1, clp.make_params(flags=1))
-    assert (2 << 30) < auto < (4 << 30) + 131072 * 400
+    assert (2 << 30) < auto < (4 << 30) * (1 + 1 / 32) + 131072 * 400
 
 
-@pytest.mark.parametrize("flags", [0, 1])
+@pytest.mark.parametrize("flags", [16, 1, 0])
 def test_workspace_budget_caps_the_chunk(clp, flags):
     n, d, v = 65536, 4096, 128256
     free = clp.grpo_workspace_size(n, d, v, 1, clp.make_params(flags=flags))

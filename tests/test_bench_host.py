@@ -105,7 +105,9 @@ def test_kernel_roofline_takes_the_kernel_with_most_time():
     per_launch = 2.0 * D * V * valid / 4
     assert r["algorithmic_flops_per_launch"] == per_launch
     assert abs(r["achieved"] - per_launch / (45.0 / 20 / 1e3) / 1e12) < 1e-9
-    assert r["peak"] == 1700.0 and abs(r["frac"] - r["achieved"] / 1700.0) < 1e-12
+    # Launches last milliseconds: the burst peak, with the sustained fraction beside it.
+    assert r["peak"] == 2000.0 and abs(r["frac"] - r["achieved"] / 2000.0) < 1e-12
+    assert abs(r["frac_of_sustained_peak"] - r["achieved"] / 1700.0) < 1e-12
     assert r["traffic"] == 1.5e9
     assert [k["name"] for k in r["per_kernel"]][:2] == ["tc_gemm_kernel<3, 2>",
                                                           "tc_gemm_kernel<2, 2>"]
@@ -113,12 +115,14 @@ def test_kernel_roofline_takes_the_kernel_with_most_time():
     assert all(k["of_call"] is None for k in r["per_kernel"])
     r = bench.kernel_roofline(times, calls, D, V, valid, peaks, rec, call_ms=18.0)
     assert abs(r["per_kernel"][0]["of_call"] - 45.0 / calls / 18.0) < 1e-12
-    # A row pass on top is HBM-bound: 4 V bytes per valid token.
+    # A row pass on top is HBM-bound: 4 V bytes per valid token (fp16 logits in,
+    # bf16 G out) and 4 bytes per 64-column box (its maximum).
     times[2]["total_ms"] = 99.0
     r = bench.kernel_roofline(times, calls, D, V, valid, peaks, None)
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 7000.0
     assert r["traffic"] is None
-    assert abs(r["achieved"] - 4.0 * V * valid / 4 / (99.0 / 20 / 1e3) / 1e9) < 1e-9
+    per_token = 4.0 * V + 4.0 * (-(-V // 64))
+    assert abs(r["achieved"] - per_token * valid / 4 / (99.0 / 20 / 1e3) / 1e9) < 1e-9
 
 
 def test_record_traffic_command_line(tmp_path):

@@ -22,6 +22,7 @@ GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
                       "grpo7x_memory_example.txt")
 GIB = 1024.0 ** 3
 STORED = 1
+RECOMPUTE = 16  # GRPO_FLAG_RECOMPUTE_LOGITS
 
 
 @pytest.fixture(scope="module")
@@ -83,9 +84,12 @@ def test_stored_logit_block_is_eq3_elements_in_fp16(clp, ex, hidden, blocks):
     def ws(n, chunk):
         return clp.grpo_workspace_size(n, hidden, V, T, clp.make_params(chunk_tokens=chunk,
                                                                         flags=STORED))
-    # Halving the chunk frees exactly half of Eq. 3's elements at 2 bytes, per
-    # logit block (two blocks when G is formed in a pass of its own, D > 2048).
-    assert ws(b * T, rows) - ws(b * T, rows // 2) == blocks * 2 * (eq3_elements // 2)
+    # Halving the chunk frees exactly half of Eq. 3's elements at 2 bytes, plus
+    # one fp32 maximum per 64 of them (1/32 more), per logit block (two blocks
+    # when G is formed in a pass of its own, D > 2048).
+    half = eq3_elements // 2
+    assert V % 64 == 0
+    assert ws(b * T, rows) - ws(b * T, rows // 2) == blocks * (2 * half + 4 * (half // 64))
     # Eq. 2's point: the block does not grow with the batch; only per-row
     # vectors do (a few hundred bytes per token).
     grow = ws(2 * b * T, rows) - ws(b * T, rows)
@@ -98,5 +102,6 @@ def test_recompute_g_block_is_eq3_elements_in_bf16(clp, ex):
 
     def ws(chunk):
         return clp.grpo_workspace_size(b * T, 4096, V, T,
-                                       clp.make_params(chunk_tokens=chunk, vocab_block=V))
+                                       clp.make_params(chunk_tokens=chunk, vocab_block=V,
+                                                       flags=RECOMPUTE))
     assert ws(rows) - ws(rows // 2) == 2 * (rows // 2) * V

@@ -1,0 +1,204 @@
+"""GPU parity at the logit magnitudes real lm_heads produce.
+
+The synthetic workloads draw W ~ N(0, 0.02^2), so their logits have a standard
+deviation of 0.02 sqrt(D) (0.8 to 1.3) and never leave |z| < 12. Trained heads
+put the top logits of a row at 30 to 60. That is where fp16 storage of a logit
+would lose precision (its spacing is 2^-6 to 2^-5 there), so these cases check
+both backward forms against the fp64 oracle there:
+
+  * logit std about 10 (row maxima 35-50), at D = 4096 (G formed in a pass of
+    its own) and D = 1536 (G formed inside the dH GEMM), with half of the rows
+    sampling their own top token (a peaked softmax on the target) and half a
+    uniform token;
+  * softcapping at 30 with raw logits far beyond the cap;
+  * logits beyond the fp16 range (|z| > 65504), which the stored form handles
+    like any other (each 64-column box is stored relative to its maximum);
+  * non-finite inputs, which give GRPO_ERR_NONFINITE in the status word.
+
+Each case prints the relative dH error of both backward forms, so the cost of
+storing logits in fp16 is a number. Gates: |d logp| <= 1e-2, relative loss
+error <= 1e-3, relative Frobenius dH error <= 2e-2 (spec tolerances);
+besides, the stored form's dH error must stay within a small factor of the
+recomputed form's (both round G to bf16; the stored form adds only the fp16
+rounding of values within a box of their maximum).
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+LOGP_TOL = 1e-2
+LOSS_RTOL = 1e-3
+DH_RTOL = 2e-2
+DEV = "cuda:0"
+STORED, RECOMPUTE = 1, 16  # GRPO_FLAG_STORED_LOGITS, GRPO_FLAG_RECOMPUTE_LOGITS
+
+
+@pytest.fixture(scope="module")
+def clp():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import chunked_log_prob_gb300 as m
+
+    return m
+
+
+def _problem(seed, D, V, N=512, T=128, logit_std=10.0, peaked=True):
+    """Rows of h ~ N(0, 1) and W ~ N(0, (logit_std / sqrt(D))^2): logits of std
+    about logit_std. With `peaked`, even rows sample their own top token."""
+    p = synth.make_problem("tiny", seed=seed, prompts=N // T // 4, G=4, T=T, D=D, V=V,
+                           lengths=(T // 2, T), weight_std=logit_std / math.sqrt(D))
+    if peaked:
+        z = oracle.logits_rows(p.hidden[::2].double().numpy(), p.weight.double().numpy())
+        ids = p.ids.clone()
+        ids[::2] = torch.from_numpy(z.argmax(axis=1).astype(np.int32))
+        p.ids = ids
+    return p
+
+
+def _oracle(p, xf=oracle.IDENTITY, with_dw=False):
+    base, _ = oracle.selective_logp(p.hidden, p.weight, p.ids.numpy(), xf=xf)
+    old, ref = p.old_ref(torch.from_numpy(base))
+    want = oracle.loss_fwd_bwd(p.hidden, p.weight, p.ids.numpy(), p.mask.numpy(), old, ref,
+                               p.adv, p.seq_len, p.eps_low, p.eps_high, p.beta, xf=xf)
+    if with_dw:
+        want["dW"] = oracle.grad_weight(p.hidden, p.weight, p.ids.numpy(), want["g"], xf=xf)
+    return old, ref, want
+
+
+def _gpu(clp, p, old, ref, flags, with_dw=False, **kw):
+    params = clp.make_params(flags=flags, **kw)
+    dev = torch.device(DEV)
+    ws = clp.alloc_workspace(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, params, dev)
+    out = clp.grpo_loss_fwd_bwd(*[t.to(dev) for t in (p.hidden, p.weight, p.ids, p.mask, old,
+                                                      ref, p.adv)],
+                                p.seq_len, params=params, workspace=ws, want_dW=with_dw)
+    st = clp.grpo_read_device_status(ws)
+    return out, st
+
+
+def _errors(out, want, mask):
+    m = mask.numpy().astype(bool)
+    L = out[0].item()
+    logp = out[1].cpu().double().numpy()
+    dH = out[2].cpu().double().numpy()
+    e = {"dlogp": float(np.abs(logp - want["logp"]).max()),
+         "rel_loss": abs(L - want["L"]) / abs(want["L"]),
+         "rel_dH": float(np.linalg.norm(dH[m] - want["dH"][m]) / np.linalg.norm(want["dH"][m])),
+         "masked_zero": bool(np.all(logp[~m] == 0) and np.all(dH[~m] == 0))}
+    if len(out) > 3:
+        dW = out[3].cpu().double().numpy()
+        e["rel_dW"] = float(np.linalg.norm(dW - want["dW"]) / np.linalg.norm(want["dW"]))
+    return e
+
+
+def _compare_forms(clp, p, want, old, ref, tag, with_dw=False, **kw):
+    errs = {}
+    for name, flags in (("recompute", RECOMPUTE), ("stored", STORED)):
+        out, st = _gpu(clp, p, old, ref, flags, with_dw=with_dw, chunk_tokens=256, **kw)
+        assert st == 0, f"{tag} {name}: device status {st}"
+        errs[name] = _errors(out, want, p.mask)
+    print(f"{tag}: " + "; ".join(f"{k}: " + ", ".join(f"{a}={b:.3e}" for a, b in v.items()
+                                                        if a != "masked_zero")
+                                 for k, v in errs.items()))
+    for name, e in errs.items():
+        assert e["masked_zero"], f"{tag} {name}: masked rows not zero"
+        assert e["dlogp"] <= LOGP_TOL and e["rel_loss"] <= LOSS_RTOL, f"{tag} {name}: {e}"
+        assert e["rel_dH"] <= DH_RTOL, f"{tag} {name}: {e}"
+        if with_dw:
+            assert e["rel_dW"] <= DH_RTOL, f"{tag} {name}: {e}"
+    # Storing logits costs no accuracy beyond the bf16 rounding of G that both
+    # forms share (unshifted fp16 logits near 40 gave about 4x the error).
+    assert errs["stored"]["rel_dH"] <= 1.5 * errs["recompute"]["rel_dH"] + 1e-3, errs
+    return errs
+
+
+# D = 4096: G in its own pass; D = 1536: G formed inside the dH GEMM.
+@pytest.mark.parametrize("D,V", [(4096, 20000), (1536, 30000)])
+def test_large_logits_both_backwards(clp, D, V):
+    p = _problem(11, D, V)
+    old, ref, want = _oracle(p)
+    zmax = want["lse"].max()
+    assert zmax > 30.0  # the regime this test is for
+    _compare_forms(clp, p, want, old, ref, f"logit std 10, D={D}, max lse {zmax:.1f}")
+
+
+def test_large_logits_lm_head_gradient(clp):
+    # dW requested: the stored form rewrites the logits as G in a pass of its
+    # own even at D <= 2048, and the dW GEMM reads that G.
+    p = _problem(12, 1536, 8000)
+    old, ref, want = _oracle(p, with_dw=True)
+    _compare_forms(clp, p, want, old, ref, "logit std 10 with dW", with_dw=True)
+
+
+@pytest.mark.parametrize("D", [4096, 1536])
+def test_softcap_beyond_the_cap(clp, D):
+    # Raw logits of std 40 against a cap of 30: most large logits saturate.
+    p = _problem(13, D, 12000, logit_std=40.0)
+    xf = oracle.Transform(softcap=30.0)
+    old, ref, want = _oracle(p, xf=xf)
+    _compare_forms(clp, p, want, old, ref, f"softcap 30, raw std 40, D={D}",
+                   logit_softcapping=30.0)
+
+
+@pytest.mark.parametrize("flags", [STORED, RECOMPUTE], ids=["stored", "recompute"])
+def test_logits_beyond_fp16_range(clp, flags):
+    # Logits of std ~2e4 (|z| well past fp16's 65504): the softmax is one-hot
+    # on each row's top token. No inf or NaN may appear, and the results must
+    # match the oracle. At that magnitude fp32 itself (the pages' precision)
+    # rounds a logit by about 2^-20 of the largest one, so logp is compared
+    # within that; and since the loss derivative g carries exp(logp - old),
+    # dH is compared with the oracle's dH for the call's own logp, which
+    # checks the softmax Jacobian and the dH GEMM on their own.
+    p = _problem(14, 256, 4096, N=256, T=64, logit_std=2.0e4, peaked=False)
+    old, ref, want = _oracle(p)
+    zmax = float(np.abs(oracle.logits_rows(p.hidden.double().numpy(),
+                                           p.weight.double().numpy())).max())
+    assert zmax > 65504.0
+    out, st = _gpu(clp, p, old, ref, flags)
+    assert st == 0
+    logp = out[1].cpu().double().numpy()
+    dH = out[2].cpu().double().numpy()
+    m = p.mask.numpy().astype(bool)
+    assert np.all(np.isfinite(logp)) and np.all(np.isfinite(dH))
+    assert np.all(logp[~m] == 0) and np.all(dH[~m] == 0)
+    dl = np.abs(logp - want["logp"]).max()
+    _, g_own, _, _ = oracle.grpo_loss(logp, old, ref, p.adv, p.mask, p.seq_len,
+                                      p.eps_low, p.eps_high, p.beta)
+    want_dh = oracle.grad_hidden(p.hidden, p.weight, p.ids.numpy(), g_own)
+    rel_dh = np.linalg.norm(dH[m] - want_dh[m]) / np.linalg.norm(want_dh[m])
+    print(f"|z| up to {zmax:.3e} (flags {flags}): max|dlogp|={dl:.3e} "
+          f"rel_dH (given logp)={rel_dh:.3e}")
+    assert dl <= LOGP_TOL + zmax * 2.0 ** -20
+    assert rel_dh <= DH_RTOL
+
+
+def test_nonfinite_inputs_set_status(clp):
+    # One hidden row holding +inf: its logits are inf or NaN (plain IEEE
+    # arithmetic), so its log-sum-exp is not finite. Every path flags that.
+    p = synth.make_problem("tiny", seed=15)
+    h = p.hidden.clone()
+    h[5, 3] = float("inf")
+    dev = torch.device(DEV)
+    old = torch.full((p.n_tokens,), -8.0)
+    args = [t.to(dev) for t in (h, p.weight, p.ids, p.mask, old, old, p.adv)]
+    ws = clp.alloc_workspace(p.n_tokens, p.hidden_size, p.vocab, p.seq_len,
+                             clp.make_params(flags=STORED), dev)
+    clp.grpo_logp_fwd(args[0], args[1], args[2], workspace=ws)
+    assert clp.grpo_read_device_status(ws) == clp.GRPO_ERR_NONFINITE
+    for flags in (STORED, RECOMPUTE):
+        clp.grpo_loss_fwd_bwd(*args, p.seq_len, params=clp.make_params(flags=flags),
+                              workspace=ws)
+        assert clp.grpo_read_device_status(ws) == clp.GRPO_ERR_NONFINITE
+    # The same workspace then serves a clean call.
+    args[0] = p.hidden.to(dev)
+    clp.grpo_loss_fwd_bwd(*args, p.seq_len, params=clp.make_params(flags=STORED), workspace=ws)
+    assert clp.grpo_read_device_status(ws) == 0

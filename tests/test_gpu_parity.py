@@ -20,6 +20,9 @@ pytestmark = pytest.mark.gpu
 LOGP_TOL = 1e-2
 LOSS_RTOL = 1e-3
 DH_RTOL = 2e-2
+# Backward forms (grpo_params.flags): without either bit the call chooses.
+STORED = 1      # GRPO_FLAG_STORED_LOGITS
+RECOMPUTE = 16  # GRPO_FLAG_RECOMPUTE_LOGITS
 
 
 @pytest.fixture(scope="module")
@@ -115,7 +118,7 @@ def test_ragged_shapes(clp, N, T, D, V, chunk, vblock, padded):
     p = synth.make_problem("tiny", seed=N + D + V, prompts=(N // T) // G, G=G, T=T, D=D, V=V,
                            lengths=(max(1, T // 3), T) if padded else None)
     old, ref, want = oracle_case(p)
-    params = clp.make_params(chunk_tokens=chunk, vocab_block=vblock)
+    params = clp.make_params(chunk_tokens=chunk, vocab_block=vblock, flags=RECOMPUTE)
     check(gpu_loss(clp, p, old, ref, params), want, p.mask, f"ragged {N}x{D}x{V}")
 
 
@@ -138,7 +141,8 @@ def test_chunking_does_not_change_results(clp):
     runs = {}
     for chunk, vb in ((128, 0), (256, 0), (512, 0), (0, 256), (0, 1024), (128, 512)):
         runs[(chunk, vb)] = gpu_loss(clp, p, old, ref, clp.make_params(chunk_tokens=chunk,
-                                                                      vocab_block=vb))
+                                                                      vocab_block=vb,
+                                                                      flags=RECOMPUTE))
     L0, lp0, dH0, _ = runs[(128, 0)]
     for key, (L, lp, dH, st) in runs.items():
         assert st == 0
@@ -223,7 +227,7 @@ def test_padding_blocks_are_skipped_and_zeroed(clp, chunk):
     p = synth.make_problem("tiny", seed=21 + chunk, prompts=2, G=4, T=512, D=256, V=3000,
                            lengths=(1, 512))
     old, ref, want = oracle_case(p)
-    params = clp.make_params(chunk_tokens=chunk, vocab_block=1024)
+    params = clp.make_params(chunk_tokens=chunk, vocab_block=1024, flags=RECOMPUTE)
     ws = clp.alloc_workspace(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, params, DEV)
     dH = torch.full((p.n_tokens, p.hidden_size), float("nan"), dtype=torch.bfloat16, device=DEV)
     logp = torch.full((p.n_tokens,), float("nan"), device=DEV)
@@ -258,7 +262,7 @@ def test_logit_transforms(clp, kw):
     old, ref = p.old_ref(torch.from_numpy(base))
     want = oracle.loss_fwd_bwd(p.hidden, p.weight, p.ids.numpy(), p.mask.numpy(), old, ref,
                                p.adv, p.seq_len, p.eps_low, p.eps_high, p.beta, xf=xf)
-    params = clp.make_params(chunk_tokens=128, vocab_block=1024, **kw)
+    params = clp.make_params(chunk_tokens=128, vocab_block=1024, flags=RECOMPUTE, **kw)
     check(gpu_loss(clp, p, old, ref, params), want, p.mask, f"transform {kw}")
     lp, _ = clp.grpo_logp_fwd(_to(p.hidden), _to(p.weight), _to(p.ids), params=params)
     assert np.abs(lp.cpu().double().numpy() - base).max() <= LOGP_TOL
@@ -266,7 +270,6 @@ def test_logit_transforms(clp, kw):
 
 # ---------------------------------------------- stored-logit backward ------
 
-STORED = 1  # GRPO_FLAG_STORED_LOGITS
 
 
 @pytest.mark.parametrize("N,T,D,V,chunk,vblock,padded", RAGGED)
@@ -319,7 +322,7 @@ def test_stored_and_recomputed_backward_agree(clp):
     p = synth.make_problem("tiny", seed=12, T=128, prompts=2, G=4, D=256, V=5000,
                            lengths=(30, 128))
     old, ref, _ = oracle_case(p)
-    L1, lp1, dH1, s1 = gpu_loss(clp, p, old, ref, clp.make_params(flags=0))
+    L1, lp1, dH1, s1 = gpu_loss(clp, p, old, ref, clp.make_params(flags=RECOMPUTE))
     L2, lp2, dH2, s2 = gpu_loss(clp, p, old, ref, clp.make_params(flags=STORED))
     assert s1 == 0 and s2 == 0
     assert np.abs(lp1 - lp2).max() <= 1e-5
@@ -370,7 +373,7 @@ def test_device_plan_fits_host_sized_workspace(clp, n):
     plan = clp.grpo_get_plan(n, D, V, p.seq_len, params)
     assert plan["workspace_bytes"] <= clp.grpo_workspace_size(n, D, V, p.seq_len, params)
     L1, lp1, dH1, s1 = gpu_loss(clp, p, old, old, params)
-    L2, lp2, dH2, s2 = gpu_loss(clp, p, old, old, clp.make_params())
+    L2, lp2, dH2, s2 = gpu_loss(clp, p, old, old, clp.make_params(flags=RECOMPUTE))
     assert s1 == 0 and s2 == 0
     assert np.abs(lp1 - lp2).max() <= 1e-5 and abs(L1 - L2) <= 1e-5 * abs(L2)
     assert np.linalg.norm(dH1 - dH2) <= 1e-2 * np.linalg.norm(dH2)
@@ -393,7 +396,7 @@ def test_stored_logits_bad_id_and_all_masked(clp):
 SINGLE = 2  # GRPO_FLAG_SINGLE_CTA
 
 
-@pytest.mark.parametrize("flags", [SINGLE, SINGLE | STORED])
+@pytest.mark.parametrize("flags", [SINGLE | RECOMPUTE, SINGLE | STORED])
 @pytest.mark.parametrize("N,T,D,V,chunk,vblock,padded", RAGGED[:4])
 def test_single_cta_gemms(clp, flags, N, T, D, V, chunk, vblock, padded):
     G = 4 if (N // T) % 4 == 0 else 1
@@ -408,7 +411,7 @@ def test_pair_and_single_cta_agree(clp):
     # Odd number of 128-row blocks: the last CTA pair has one real row block.
     p = synth.make_problem("tiny", seed=14, T=640, prompts=1, G=1, D=256, V=3000)
     old, ref, _ = oracle_case(p)
-    for extra in (0, STORED):
+    for extra in (RECOMPUTE, STORED):
         L1, lp1, dH1, s1 = gpu_loss(clp, p, old, ref, clp.make_params(flags=extra))
         L2, lp2, dH2, s2 = gpu_loss(clp, p, old, ref, clp.make_params(flags=extra | SINGLE))
         assert s1 == 0 and s2 == 0
@@ -422,7 +425,8 @@ SEQMEAN = 4  # GRPO_FLAG_SEQUENCE_MEAN
 FITFREE = 8  # GRPO_FLAG_FIT_FREE_MEMORY
 
 
-@pytest.mark.parametrize("flags", [SEQMEAN, SEQMEAN | STORED, SEQMEAN | SINGLE])
+@pytest.mark.parametrize("flags", [SEQMEAN | RECOMPUTE, SEQMEAN | STORED,
+                                   SEQMEAN | SINGLE | RECOMPUTE, SEQMEAN])
 def test_sequence_mean_aggregation(clp, flags):
     p = synth.make_problem("tiny", seed=60, T=100, prompts=2, G=4, D=256, V=3000,
                            lengths=(5, 100))
@@ -437,7 +441,8 @@ def test_sequence_mean_aggregation(clp, flags):
 
 
 @pytest.mark.parametrize("flags,limit", [(FITFREE, 0), (STORED | FITFREE, 0),
-                                         (STORED, 24 << 20), (0, 24 << 20)])
+                                         (STORED, 24 << 20), (RECOMPUTE, 24 << 20),
+                                         (RECOMPUTE | FITFREE, 0), (0, 24 << 20)])
 def test_workspace_budget_plans_give_same_results(clp, flags, limit):
     p = synth.make_problem("tiny", seed=61, T=512, prompts=2, G=4, D=512, V=6000,
                            lengths=(100, 512))
@@ -453,14 +458,14 @@ def test_workspace_budget_plans_give_same_results(clp, flags, limit):
 
 DW_CASES = [
     # N, T, D, V, chunk, vblock, padded, flags
-    (256, 64, 256, 4096, 0, 0, False, 0),
+    (256, 64, 256, 4096, 0, 0, False, RECOMPUTE),
     (256, 64, 256, 4096, 0, 0, False, STORED),
-    (300, 75, 200, 1000, 128, 512, True, 0),
+    (300, 75, 200, 1000, 128, 512, True, RECOMPUTE),
     (300, 75, 200, 1000, 128, 512, True, STORED),
-    (300, 75, 200, 1000, 128, 512, True, SINGLE),
+    (300, 75, 200, 1000, 128, 512, True, SINGLE | RECOMPUTE),
     (300, 75, 200, 1000, 128, 512, True, SINGLE | STORED),
     (4096, 512, 256, 3000, 256, 1024, True, STORED),   # many skipped blocks, empty chunks
-    (4096, 512, 256, 3000, 256, 1024, True, 0),
+    (4096, 512, 256, 3000, 256, 1024, True, RECOMPUTE),
 ]
 
 
@@ -489,7 +494,7 @@ def test_lm_head_gradient(clp, N, T, D, V, chunk, vblock, padded, flags):
 def test_lm_head_gradient_all_masked_is_zero(clp):
     p = synth.make_problem("tiny", seed=62)
     dW = torch.full((p.vocab, p.hidden_size), float("nan"), device=DEV)
-    for flags in (0, STORED):
+    for flags in (RECOMPUTE, STORED):
         _, _, _, dW = clp.grpo_loss_fwd_bwd(
             _to(p.hidden), _to(p.weight), _to(p.ids), _to(torch.zeros_like(p.mask)),
             _to(torch.zeros(p.n_tokens)), _to(torch.zeros(p.n_tokens)), _to(p.adv), p.seq_len,
@@ -506,7 +511,7 @@ def test_lm_head_gradient_with_transform(clp):
     want = oracle.loss_fwd_bwd(p.hidden, p.weight, p.ids.numpy(), p.mask.numpy(), old, ref,
                                p.adv, p.seq_len, p.eps_low, p.eps_high, p.beta, xf=xf)
     want_dW = oracle.grad_weight(p.hidden, p.weight, p.ids.numpy(), want["g"], xf=xf)
-    for flags in (0, STORED):
+    for flags in (RECOMPUTE, STORED):
         params = clp.make_params(chunk_tokens=128, flags=flags, logit_softcapping=2.0,
                                  temperature=0.8)
         _, _, _, dW = clp.grpo_loss_fwd_bwd(
@@ -566,7 +571,7 @@ def test_concurrent_calls_from_two_threads(clp):
         assert torch.equal(l0, l1) and torch.equal(lp0, lp1) and torch.equal(d0, d1)
 
 
-@pytest.mark.parametrize("flags", [0, STORED])
+@pytest.mark.parametrize("flags", [RECOMPUTE, STORED])
 def test_device_memory_is_the_workspace_only(clp, flags):
     # The memory claim ("GRPO with 7x longer context", section "Flattened
     # sequence length chunking", Eq. 1-3): at a fixed chunk the memory a call
@@ -613,8 +618,8 @@ def test_device_memory_is_the_workspace_only(clp, flags):
 # Vocabulary edges through every backward form: V = 1 (logp = 0, G = 0),
 # V = 7 (a stored row narrower than one 16-byte chunk), V = 65 (one column
 # past a 64-wide K slice); D = 256 forms G in the dH GEMM, D = 2304 in its own
-# pass; flags 0 is the recomputed backward.
-@pytest.mark.parametrize("flags", [0, STORED])
+# pass; RECOMPUTE is the recomputed backward.
+@pytest.mark.parametrize("flags", [RECOMPUTE, STORED])
 @pytest.mark.parametrize("D", [256, 2304])
 @pytest.mark.parametrize("V", [1, 7, 65])
 def test_small_vocab_edges(clp, flags, D, V):
@@ -640,7 +645,7 @@ def test_empty_batch_stored(clp, flags):
 # Smallest legal shapes: hidden sizes far below one 64-wide K slice (D = 8,
 # 24), a single token, and D = 2056 (just past the size up to which G is
 # formed in the dH GEMM, and not a multiple of 64); every backward form.
-@pytest.mark.parametrize("flags", [0, STORED, STORED | SINGLE])
+@pytest.mark.parametrize("flags", [RECOMPUTE, STORED, STORED | SINGLE])
 @pytest.mark.parametrize("N,D", [(1, 8), (3, 24), (130, 8), (70, 2056)])
 def test_tiny_hidden_and_single_token(clp, flags, N, D):
     p = synth.make_problem("tiny", seed=N * 31 + D, prompts=1, G=1, T=N, D=D, V=300,
@@ -663,7 +668,7 @@ def _guarded(n, dtype, fill, guard):
 # every output is a view inside a buffer of sentinels, and the workspace is
 # prefilled with 0xFF bytes (NaN in every float format) inside its own guard
 # band. Results must still match the oracle and every sentinel must survive.
-@pytest.mark.parametrize("flags", [0, STORED, STORED | SINGLE])
+@pytest.mark.parametrize("flags", [RECOMPUTE, STORED, STORED | SINGLE])
 @pytest.mark.parametrize("D", [256, 2304])
 @pytest.mark.parametrize("with_dw", [False, True])
 def test_guard_bands_and_poisoned_workspace(clp, flags, D, with_dw):
@@ -697,3 +702,27 @@ def test_guard_bands_and_poisoned_workspace(clp, flags, D, with_dw):
         want_dW = oracle.grad_weight(p.hidden, p.weight, p.ids.numpy(), want["g"])
         got = out[3].cpu().double().numpy()
         assert np.linalg.norm(got - want_dW) <= DH_RTOL * np.linalg.norm(want_dW)
+
+
+# --------------------------------------------- automatic backward form -----
+
+def test_automatic_backward_form_is_the_forced_one(clp):
+    # Flags 0: without a budget the call takes the stored form; under a budget
+    # too small for one stored chunk of 256 rows (32000 fp16 logits each) it
+    # takes the recomputed one, with vocab blocks of 4096. Either way its
+    # results are bitwise those of the form forced by its flag.
+    p = synth.make_problem("tiny", seed=71, T=1024, prompts=2, G=4, D=1024, V=32000,
+                           lengths=(256, 1024))
+    old, ref, want = oracle_case(p)
+    for limit, form in ((0, STORED), (12 << 20, RECOMPUTE)):
+        auto = clp.make_params(workspace_limit_bytes=limit, vocab_block=4096)
+        plan = clp.grpo_get_plan(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, auto)
+        assert plan["stored_logits"] == (1 if form == STORED else 0), (limit, plan)
+        forced = clp.make_params(flags=form, workspace_limit_bytes=limit, vocab_block=4096)
+        assert clp.grpo_workspace_size(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, auto) == \
+            clp.grpo_workspace_size(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, forced)
+        got = gpu_loss(clp, p, old, ref, auto)
+        check(got, want, p.mask, f"automatic, budget {limit}")
+        ref_run = gpu_loss(clp, p, old, ref, forced)
+        assert got[0] == ref_run[0] and np.array_equal(got[1], ref_run[1])
+        assert np.array_equal(got[2], ref_run[2])
