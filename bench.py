@@ -47,10 +47,13 @@ def parse_args():
                     help="override tokens per completion (small profiling cases)")
     ap.add_argument("--chunk-tokens", type=int, default=0)
     ap.add_argument("--vocab-block", type=int, default=0)
-    ap.add_argument("--backward", default="auto", choices=["auto", "stored", "recompute"],
+    ap.add_argument("--backward", default="auto",
+                    choices=["auto", "stored", "single_pass", "recompute"],
                     help="auto: the library's default choice (flags 0) for the workspace "
                          "budget; stored: the backward reads fp16 logits kept per chunk "
-                         "(4NDV executed); recompute: it recomputes the logit tiles (6NDV)")
+                         "(4NDV executed); single_pass: one vocabulary block of logits at a "
+                         "time, rescaled U accumulator (4NDV); recompute: it recomputes "
+                         "the logit tiles (6NDV)")
     ap.add_argument("--workspace-limit-gb", type=float, default=0.0,
                     help="workspace budget passed to the library (0 = none)")
     ap.add_argument("--budget-sweep", default="",
@@ -62,7 +65,7 @@ def parse_args():
     ap.add_argument("--with-dw", action="store_true",
                     help="also compute the lm_head gradient dW (full fine-tuning; +2NDV)")
     ap.add_argument("--no-variant", action="store_true",
-                    help="skip timing the other backward variant")
+                    help="skip timing the other backward forms")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -174,8 +177,20 @@ def max_over_ranks(x):
 
 
 # grpo_params.flags of each backward form (GRPO_FLAG_STORED_LOGITS,
-# GRPO_FLAG_RECOMPUTE_LOGITS; 0 lets the library choose).
-FORM_FLAGS = {"auto": 0, "stored": 1, "recompute": 16}
+# GRPO_FLAG_SINGLE_PASS, GRPO_FLAG_RECOMPUTE_LOGITS; 0 lets the library choose).
+FORM_FLAGS = {"auto": 0, "stored": 1, "single_pass": 32, "recompute": 16}
+FORM_NAMES = {"stored": "stored fp16 logits", "single_pass": "single pass over vocab blocks",
+              "recompute": "recomputed logits"}
+# Executed tensor work per valid token in units of D V (without dW): the
+# stored and single-pass forms compute each logit once, the recomputed form twice.
+EXECUTED_NDV = {"stored": 4.0, "single_pass": 4.0, "recompute": 6.0}
+
+
+def form_of(plan):
+    """The backward form a plan (grpo_get_plan) uses."""
+    if plan["stored_logits"]:
+        return "stored"
+    return "single_pass" if plan.get("single_pass") else "recompute"
 
 
 def flops_per_token(D, V):
@@ -311,13 +326,10 @@ _NCU_SCALE = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e
 _FIRST_KERNEL = "row_plan_kernel"  # every grpo_loss_fwd_bwd call starts with it
 
 
-def ncu_calls(csv_path):
-    """Split an ncu --csv launch list into the library's calls.
-
-    Returns a list of calls, each a list of launches {"name", "read", "write",
-    "ms"} (bytes, milliseconds). A call runs from one row_plan_kernel launch up
-    to the next; launches of other code (torch's own kernels) are dropped, and
-    so is the last call, which the capture limit may have cut short."""
+def ncu_launches(csv_path):
+    """The library's launches in an ncu --csv capture, in launch order:
+    {"name", "read", "write", "ms"} (bytes, milliseconds); launches of other
+    code (torch's own kernels) are dropped."""
     import csv
 
     with open(csv_path, newline="") as f:
@@ -343,15 +355,44 @@ def ncu_calls(csv_path):
         seq.append({"name": name, "read": d.get("dram__bytes_read.sum", 0.0),
                     "write": d.get("dram__bytes_write.sum", 0.0),
                     "ms": d.get("gpu__time_duration.sum", 0.0)})
+    return seq
+
+
+def ncu_calls(csv_path):
+    """Split an ncu --csv launch list into the library's calls: lists of
+    launches as ncu_launches gives them. A call runs from one row_plan_kernel
+    launch up to the next; the last call, which the capture limit may have cut
+    short, is dropped."""
+    seq = ncu_launches(csv_path)
     starts = [i for i, d in enumerate(seq) if d["name"] == _FIRST_KERNEL]
     return [seq[a:b] for a, b in zip(starts, starts[1:])]
 
 
 def record_traffic(csv_path, workload, backward, command):
-    """Write the DRAM record of the last complete call in an ncu launch list."""
+    """Write the DRAM record of an ncu capture: of the last complete call in a
+    launch list, or, when the capture holds no whole call (one kernel, a few
+    launches, -k/-c), of each captured kernel per launch. The bench reads the
+    dominant kernel's bytes per launch from either."""
     calls = ncu_calls(csv_path)
     if not calls:
-        raise SystemExit(f"{csv_path}: no complete grpo_loss_fwd_bwd call")
+        seq = ncu_launches(csv_path)
+        if not seq:
+            raise SystemExit(f"{csv_path}: no launch of the library")
+        per = {}
+        for d in seq:
+            e = per.setdefault(d["name"], {"launches": 0, "read_bytes": 0.0,
+                                           "write_bytes": 0.0, "time_ms": 0.0})
+            e["launches"] += 1
+            e["read_bytes"] += d["read"]
+            e["write_bytes"] += d["write"]
+            e["time_ms"] += d["ms"]
+        rec = {"workload": workload, "backward": backward, "dram_bytes_per_call": None,
+               "scope": "captured launches of single kernels (no whole call); per_kernel "
+                        "sums over them", "per_kernel": per, "command": command,
+               "kernel_source_hash": kernel_source_hash()}
+        with open(traffic_path(workload, backward), "w") as f:
+            json.dump(rec, f, indent=1)
+        return rec
     call = calls[-1]
     per = {}
     for d in call:
@@ -469,17 +510,18 @@ def run_ours(args):
     params = make(FORM_FLAGS[args.backward])
     plan = clp.grpo_get_plan(N, D, V, T, params)
     stored = bool(plan["stored_logits"])
-    other = make(FORM_FLAGS["recompute" if stored else "stored"])
+    form = form_of(plan)
+    others = {f: make(FORM_FLAGS[f]) for f in ("stored", "single_pass", "recompute") if f != form}
     if args.backward == "auto":
-        choice = ("library default (flags 0): the planner's automatic choice; %s" % (
-            "no workspace budget" if limit == 0 else "budget %.2f GB" % args.workspace_limit_gb)
-            + (", so the stored form fits and its modelled GEMM time is the shorter"
-               if stored else ", under which the recomputed form is the faster or the only "
-               "one that fits"))
+        choice = ("library default (flags 0): the planner's automatic choice; %s; among the "
+                  "forms that fit, %s has the shortest modelled GEMM time" % (
+                      "no workspace budget" if limit == 0
+                      else "budget %.2f GB" % args.workspace_limit_gb, FORM_NAMES[form]))
     else:
         choice = "forced by --backward %s" % args.backward
     ws_bytes = max(clp.grpo_workspace_size(N, D, V, T, params),
-                   0 if args.no_variant else clp.grpo_workspace_size(N, D, V, T, other))
+                   0 if args.no_variant else max(clp.grpo_workspace_size(N, D, V, T, o)
+                                                 for o in others.values()))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     # old/ref: the policy's own log-probs (as a GRPO trainer gets them) + noise.
     base, _ = clp.grpo_logp_fwd(p.hidden, p.weight, p.ids, params=params, workspace=ws)
@@ -535,27 +577,31 @@ def run_ours(args):
         clp.grpo_launch_timing_enable(False)
     kernel_times = clp.grpo_launch_timing_read()
 
-    # The other backward variant on the same inputs (reported beside the headline).
-    variant = None
+    # The other backward forms on the same inputs (reported beside the headline).
+    variants = []
     if not args.no_variant:
-        for _ in range(3):
-            step(other)
-        torch.cuda.synchronize(dev)
-        if world > 1:
-            dist.barrier()
-        ev0.record(stream)
-        for _ in range(args.steps):
-            step(other)
-        ev1.record(stream)
-        torch.cuda.synchronize(dev)
-        v_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
-        v_exec = ((6.0 if stored else 4.0) + (2.0 if args.with_dw else 0.0)) * D * V * p.n_valid
-        variant = {"backward": "recomputed logits" if stored else "stored fp16 logits",
-                   "ms_per_step": v_ms, "value": world * p.n_valid / (v_ms / 1e3),
-                   "tflops_executed": v_exec / (v_ms / 1e3) / 1e12,
-                   "launches_per_call": clp.grpo_get_plan(N, D, V, T, other)["launches_loss"]
-            + (clp.grpo_get_plan(N, D, V, T, other)["n_chunks"]
-               * clp.grpo_get_plan(N, D, V, T, other)["n_vocab_blocks"] if args.with_dw else 0)}
+        for f, prm in others.items():
+            for _ in range(3):
+                step(prm)
+            torch.cuda.synchronize(dev)
+            if world > 1:
+                dist.barrier()
+            ev0.record(stream)
+            for _ in range(args.steps):
+                step(prm)
+            ev1.record(stream)
+            torch.cuda.synchronize(dev)
+            v_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+            v_plan = clp.grpo_get_plan(N, D, V, T, prm)
+            v_exec = (EXECUTED_NDV[f] + (2.0 if args.with_dw else 0.0)) * D * V * p.n_valid
+            variants.append({
+                "backward": FORM_NAMES[f], "ms_per_step": v_ms,
+                "value": world * p.n_valid / (v_ms / 1e3),
+                "tflops_executed": v_exec / (v_ms / 1e3) / 1e12,
+                "workspace_bytes": v_plan["workspace_bytes"], "chunk_rows": v_plan["chunk_rows"],
+                "vocab_block": v_plan["vocab_block"],
+                "launches_per_call": v_plan["launches_loss"] + (
+                    v_plan["n_chunks"] * v_plan["n_vocab_blocks"] if args.with_dw else 0)})
 
     # Forward alone (one logit GEMM launch + finalize), timed on the same stream.
     fwd_ms = None
@@ -643,11 +689,13 @@ def run_ours(args):
     tflops = fl / (ms_max / 1e3) / 1e12
     # Executed tensor work: 6NDV with the recomputed backward, 4NDV when the
     # backward reads the stored fp16 logits instead of a second logit GEMM.
-    fl_exec = ((4.0 if stored else 6.0) + (2.0 if args.with_dw else 0.0)) * D * V * valid
+    # With dW the single pass runs as the recomputed form (it never forms G).
+    run_form = "recompute" if (form == "single_pass" and args.with_dw) else form
+    fl_exec = (EXECUTED_NDV[run_form] + (2.0 if args.with_dw else 0.0)) * D * V * valid
     tflops_exec = fl_exec / (ms_max / 1e3) / 1e12
     peak_sus = peaks["bf16_tflops_sustained"]
     peak_burst = peaks["bf16_tflops"]
-    rec = recorded_traffic(p.name, "stored" if stored else "recompute")
+    rec = recorded_traffic(p.name, run_form)
     # The dominant kernel (most device time), timed live; its peak is the burst
     # one (a call lasts milliseconds). The call as a whole beside it.
     roofline = kernel_roofline(kernel_times, timed_calls, D, V, valid, peaks, rec,
@@ -694,11 +742,11 @@ def run_ours(args):
         "pct_bf16_peak": 100.0 * tflops_exec / peak_burst,
         "pct_bf16_peak_note": "executed flops over the measured burst bf16 peak",
         "backward_choice": choice,
-        "backward": ("stored fp16 logits" if stored else "recomputed logits") + (
+        "backward": FORM_NAMES[run_form] + (
             ", G formed inside the dH GEMM" if stored and plan["g_in_dh_gemm"]
             and not args.with_dw else ", G formed in its own pass" if stored else "") + (
             " + lm_head dW" if args.with_dw else ""),
-        "variant": variant,
+        "variants": variants,
         "roofline": roofline,
         "fwd_only": None if fwd_ms is None else {
             "ms": fwd_ms, "tflops": 2.0 * D * V * N / (fwd_ms / 1e3) / 1e12,
@@ -792,7 +840,7 @@ def run_budget_sweep(args):
             torch.cuda.synchronize(dev)
             ms = ev0.elapsed_time(ev1) / reps
             row.update({"fits": True, "workspace_bytes": nbytes,
-                        "backward": "stored" if plan["stored_logits"] else "recompute",
+                        "backward": form_of(plan),
                         "chunk_rows": plan["chunk_rows"], "n_chunks": plan["n_chunks"],
                         "vocab_block": plan["vocab_block"], "ms_per_call": ms,
                         "tokens_per_s": p.n_valid / (ms / 1e3)})
@@ -860,9 +908,11 @@ def run_reference(args):
 if __name__ == "__main__":
     a = parse_args()
     if a.record_traffic:
-        r = record_traffic(a.record_traffic, a.workload, a.backward, a.record_command)
-        print(json.dumps({k: r[k] for k in ("workload", "backward", "dram_bytes_per_call",
-                                            "launches_per_call", "ncu_time_ms_per_call")}))
+        # "auto" names the form a call takes without a budget: stored.
+        r = record_traffic(a.record_traffic, a.workload,
+                           "stored" if a.backward == "auto" else a.backward, a.record_command)
+        print(json.dumps({k: r.get(k) for k in ("workload", "backward", "dram_bytes_per_call",
+                                                "launches_per_call", "ncu_time_ms_per_call")}))
     elif a.impl == "reference":
         run_reference(a)
     elif a.budget_sweep:

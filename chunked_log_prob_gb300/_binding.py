@@ -48,7 +48,7 @@ class GrpoPlanInfo(ctypes.Structure):
                 ("n_chunks", ctypes.c_int32), ("n_vocab_blocks", ctypes.c_int32),
                 ("fwd_splits", ctypes.c_int32), ("launches_logp", ctypes.c_int32),
                 ("launches_loss", ctypes.c_int32), ("g_in_dh_gemm", ctypes.c_int32),
-                ("stored_logits", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("stored_logits", ctypes.c_int32), ("single_pass", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_uint64)]
 
 
@@ -108,6 +108,7 @@ FLAG_SINGLE_CTA = 2
 FLAG_SEQUENCE_MEAN = 4
 FLAG_FIT_FREE_MEMORY = 8
 FLAG_RECOMPUTE_LOGITS = 16
+FLAG_SINGLE_PASS = 32
 
 # Largest batch of the workspace-free forward (its static device scratch).
 NOALLOC_MAX_TOKENS = 8192

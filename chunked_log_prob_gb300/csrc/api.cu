@@ -23,6 +23,7 @@ constexpr int kMaxSplits = 32;          // forward vocab splits (per-row partial
 constexpr int kMaxAutoChunkBlocks = 32;  // automatic backward chunk <= 4096 rows
 constexpr int kAutoVocabBlock = 32768;   // automatic backward vocab block
 constexpr int kMaxStoredChunkBlocks = 64;                   // stored-logit chunk bound
+constexpr int kMaxSinglePassChunkBlocks = 64;               // single-pass chunk <= 8192 rows
 constexpr size_t kMaxStoredChunkBytes = size_t(2) << 30;    // 2 GiB of fp16 logits
 // Hidden sizes up to which the stored-logit backward forms G inside the dH
 // GEMM (MODE_DHS) rather than in a pass of its own over the logit block.
@@ -65,9 +66,14 @@ long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 // D columns per dH unit, in units of 256: the pair kernel covers 512.
 int dh_accumulators(int ctas) { return ctas == 2 ? 2 : 1; }
 
+// Backward forms (grpo_params.flags, or the automatic choice).
+enum Form { kFormRecompute = 0, kFormStored = 1, kFormSinglePass = 2 };
+
 struct Layout {
   int ctas;         // 2: CTA-pair GEMMs (default); 1: single-CTA GEMMs
   bool stored;      // stored-logit backward (GRPO_FLAG_STORED_LOGITS)
+  bool single_pass; // single-pass backward (GRPO_FLAG_SINGLE_PASS)
+  int nvb;          // single pass: vocab blocks (each one logit GEMM + one U GEMM)
   long long ldS;    // stored mode: elements per row of the chunk logit block
   long long n, nr;  // rows, rows rounded up to BM
   int T, D, V;
@@ -226,6 +232,46 @@ double recompute_cost(long long n_rb_total, int nrb, int n_dt, int nvt, int vb_t
   return actual;
 }
 
+// Forward vocab splits of one block of the single-pass backward: whole waves
+// of (row unit x split) units, at most `cap` splits (every block's splits
+// share the kMaxSplits partial slots of a row).
+int single_pass_fwd_splits(int nrb, int tiles, int cap, int sms) {
+  int best = 1;
+  double best_eff = -1.0;
+  for (int sp = 1; sp <= std::min(tiles, cap); ++sp) {
+    const double even = (static_cast<double>(tiles) / sp) / static_cast<double>(cdiv(tiles, sp));
+    const double eff = wave_eff(static_cast<long long>(nrb) * sp, sms) * even;
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = sp;
+    }
+  }
+  return best;
+}
+
+// Modelled GEMM time of the single-pass schedule (same unit as stored_cost):
+// per chunk of nrb row units and per vocab block of `tiles` tiles, a logit
+// GEMM of (row units x splits) units and a U GEMM of (row units x D tiles)
+// units of K = the block. The U GEMM converts every landed logit stage on chip
+// (measured: about a fifth of its time on GB300) and, with several blocks,
+// reads and rewrites its fp32 accumulator once per block.
+double single_pass_cost(long long n_rb_total, int nrb, int n_dt, int nvt, int vb_tiles, int nvb,
+                        int sms) {
+  const double uac_factor = 1.2 + (nvb > 1 ? 0.03 : 0.0);
+  double actual = 0.0;
+  for (long long r0 = 0; r0 < n_rb_total; r0 += nrb) {
+    const int n = static_cast<int>(std::min<long long>(nrb, n_rb_total - r0));
+    for (int t0 = 0; t0 < nvt; t0 += vb_tiles) {
+      const int w = std::min(vb_tiles, nvt - t0);
+      const int sp = single_pass_fwd_splits(n, w, kMaxSplits / nvb, sms);
+      actual += static_cast<double>(cdiv(static_cast<long long>(n) * sp, sms)) * cdiv(w, sp);
+      actual += static_cast<double>(cdiv(static_cast<long long>(n) * n_dt, sms)) * w / n_dt *
+                uac_factor;
+    }
+  }
+  return actual;
+}
+
 // Workspace budget of a call in bytes (0 = none): the caller's limit, or half
 // of the device's free memory with GRPO_FLAG_FIT_FREE_MEMORY.
 size_t workspace_budget(const grpo_params* p) {
@@ -241,13 +287,15 @@ size_t workspace_budget(const grpo_params* p) {
   return budget;
 }
 
-// Layout of a call with the backward form fixed (stored: fp16 logits kept per
-// chunk; else recomputed logit tiles). sms = 0: the sizing without a device
-// (the largest automatic chunk).
-int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, bool stored,
+// Layout of a call with the backward form fixed (stored: fp16 logits of the
+// whole vocabulary kept per chunk; single pass: one vocabulary block's logits
+// at a time and an fp32 U accumulator; recompute: recomputed logit tiles).
+// sms = 0: the sizing without a device (the largest automatic chunk).
+int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, Form form,
                      Layout* L) {
   L->ctas = (p != nullptr && (p->flags & GRPO_FLAG_SINGLE_CTA) != 0) ? 1 : 2;
-  L->stored = stored;
+  L->stored = form == kFormStored;
+  L->single_pass = form == kFormSinglePass;
   L->model_cost = 0.0;
   L->ldS = cdiv(std::max(s->vocab, 1), 8) * 8;
   L->n = s->n_tokens;
@@ -259,12 +307,27 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, bool st
   L->ctas = (p != nullptr && (p->flags & GRPO_FLAG_SINGLE_CTA) != 0) ? 1 : 2;
   const int n_dt = static_cast<int>(cdiv(s->hidden, BN * dh_accumulators(L->ctas)));
   long long vb = (p && p->vocab_block > 0) ? p->vocab_block : kAutoVocabBlock;
+  if (L->single_pass) {
+    // Equal blocks (the automatic size split evenly), at most kMaxSplits of
+    // them: every block's forward splits need partial slots of their own.
+    long long nb = cdiv(s->vocab, cdiv(vb, BN) * BN);
+    if (p == nullptr || p->vocab_block <= 0) vb = cdiv(s->vocab, nb);
+    nb = cdiv(s->vocab, cdiv(vb, BN) * BN);
+    if (nb > kMaxSplits) vb = cdiv(s->vocab, kMaxSplits);
+  }
   vb = cdiv(vb, BN) * BN;
   vb = std::min<long long>(vb, static_cast<long long>(L->nvt) * BN);
-  L->vblock = L->stored ? static_cast<int>(L->ldS) : static_cast<int>(vb);
+  L->nvb = static_cast<int>(cdiv(s->vocab, vb));
+  if (L->stored) {
+    L->vblock = static_cast<int>(L->ldS);
+  } else {
+    L->vblock = static_cast<int>(vb);
+  }
+  if (L->single_pass) L->ldS = L->vblock;
   L->need_acc = !L->stored && L->vblock < L->V;
   L->fused = L->stored && L->D <= kFusedMaxHidden;
-  L->nbox = static_cast<int>(cdiv(std::max(s->vocab, 1), 64));
+  // 64-column boxes of a stored row (the whole vocabulary, or one block).
+  L->nbox = static_cast<int>(cdiv(L->single_pass ? L->vblock : std::max(s->vocab, 1), 64));
 
   // Everything before the backward chunk block depends on N only.
   size_t off = kHeaderBytes;
@@ -289,12 +352,14 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, bool st
   // (one being turned into G while the next chunk's logits are computed),
   // one when the dH GEMM forms G itself.
   const int sbufs = L->stored && !L->fused ? 2 : 1;
+  const bool boxes = L->stored || L->single_pass;  // fp16 logits with box maxima
   const size_t unit_bytes = static_cast<size_t>(ru_rows) *
                             (static_cast<size_t>(L->vblock) * 2 * sbufs +
-                             (L->stored ? static_cast<size_t>(L->nbox) * 4 * sbufs : 0) +
+                             (boxes ? static_cast<size_t>(L->nbox) * 4 * sbufs : 0) +
                              (L->need_acc ? L->D * 4 : 0));
-  long long max_units = L->stored ? std::max(1, stored_max_blocks(L->ldS, sbufs) / L->ctas)
-                                  : kMaxAutoChunkBlocks / L->ctas;
+  long long max_units = L->stored        ? std::max(1, stored_max_blocks(L->ldS, sbufs) / L->ctas)
+                        : L->single_pass ? kMaxSinglePassChunkBlocks / L->ctas
+                                         : kMaxAutoChunkBlocks / L->ctas;
   const size_t budget = workspace_budget(p);
   if (budget > 0) {
     const long long fit =
@@ -320,6 +385,20 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, bool st
                                                 exposed_g)
                      : std::min<long long>(n_ru_total, max_units)) *
             ru_rows;
+  } else if (sms > 0 && L->single_pass) {
+    // The best modelled schedule (near-ties to the larger chunk).
+    const int hi = static_cast<int>(std::min<long long>(n_ru_total, max_units));
+    const int vbt = static_cast<int>(cdiv(L->vblock, BN));
+    int best = hi;
+    double best_cost = 0.0;
+    for (int nrb = hi; nrb >= 1; --nrb) {
+      const double cost = single_pass_cost(n_ru_total, nrb, n_dt, L->nvt, vbt, L->nvb, slots);
+      if (nrb == hi || cost < best_cost * 0.995) {
+        best_cost = cost;
+        best = nrb;
+      }
+    }
+    crows = static_cast<long long>(best) * ru_rows;
   } else if (sms > 0) {
     crows = auto_chunk_blocks(n_ru_total, n_dt, slots, static_cast<int>(max_units)) * ru_rows;
   } else {  // sizing without a device: the largest automatic chunk
@@ -334,9 +413,10 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, bool st
   // fp16 logits, rewritten in place as bf16 G [C x ldS] (stored path; two of
   // them when double-buffered).
   off = align_up(off + static_cast<size_t>(L->n_sbuf) * L->chunk_rows * L->vblock * 2, 256);
-  // Stored path: the maxima of each block's 64-column boxes, fp32 [nbox][chunk rows].
+  // Stored and single-pass paths: the maxima of each block's 64-column boxes,
+  // fp32 [nbox][chunk rows].
   L->off_bmax = off;
-  if (L->stored)
+  if (boxes)
     off = align_up(off + static_cast<size_t>(L->n_sbuf) * L->nbox * L->chunk_rows * 4, 256);
   L->off_acc = off;
   if (L->need_acc) off = align_up(off + static_cast<size_t>(L->chunk_rows) * L->D * 4, 256);
@@ -344,29 +424,46 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, bool st
   if (budget > 0 && L->total > budget) return GRPO_ERR_WORKSPACE_TOO_SMALL;
   if (sms > 0) {
     const int rb = static_cast<int>(L->chunk_rows / ru_rows);
-    L->model_cost = L->stored ? stored_cost(n_ru_total, rb, n_dt, L->nvt, slots,
-                                            L->fused ? 0.0 : 550.0 / L->D)
-                              : recompute_cost(n_ru_total, rb, n_dt, L->nvt,
-                                               static_cast<int>(cdiv(L->vblock, BN)), slots);
+    const int vbt = static_cast<int>(cdiv(L->vblock, BN));
+    L->model_cost = L->stored        ? stored_cost(n_ru_total, rb, n_dt, L->nvt, slots,
+                                                   L->fused ? 0.0 : 550.0 / L->D)
+                    : L->single_pass ? single_pass_cost(n_ru_total, rb, n_dt, L->nvt, vbt,
+                                                        L->nvb, slots)
+                                     : recompute_cost(n_ru_total, rb, n_dt, L->nvt, vbt, slots);
   }
   return GRPO_OK;
 }
 
-// Layout of a call. GRPO_FLAG_STORED_LOGITS or GRPO_FLAG_RECOMPUTE_LOGITS fix
-// the backward form; without either the planner takes the stored form unless
-// it does not fit the workspace budget or its modelled GEMM time (at the
-// reference SM count, so that sizing and call agree) is longer than the
-// recomputed form's: chunks too small for whole SM waves of the dH GEMM.
+// Layout of a call. GRPO_FLAG_STORED_LOGITS, GRPO_FLAG_SINGLE_PASS or
+// GRPO_FLAG_RECOMPUTE_LOGITS fix the backward form; without any of them the
+// planner takes, among the forms that fit the workspace budget, the one with
+// the shortest modelled GEMM time at the reference SM count (so that sizing
+// and call agree); ties go to the form listed first: stored, single pass,
+// recompute.
 int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
   const uint32_t f = p != nullptr ? p->flags : 0u;
-  if ((f & GRPO_FLAG_STORED_LOGITS) != 0) return make_layout_mode(s, p, sms, true, L);
-  if ((f & GRPO_FLAG_RECOMPUTE_LOGITS) != 0) return make_layout_mode(s, p, sms, false, L);
-  Layout ls, lr;
-  const int rs = make_layout_mode(s, p, kRefSms, true, &ls);
-  const int rr = make_layout_mode(s, p, kRefSms, false, &lr);
-  if (rs != GRPO_OK && rr != GRPO_OK) return rr;
-  const bool stored = rs == GRPO_OK && (rr != GRPO_OK || ls.model_cost <= lr.model_cost);
-  return make_layout_mode(s, p, sms, stored, L);
+  if ((f & GRPO_FLAG_STORED_LOGITS) != 0) return make_layout_mode(s, p, sms, kFormStored, L);
+  if ((f & GRPO_FLAG_SINGLE_PASS) != 0) return make_layout_mode(s, p, sms, kFormSinglePass, L);
+  if ((f & GRPO_FLAG_RECOMPUTE_LOGITS) != 0)
+    return make_layout_mode(s, p, sms, kFormRecompute, L);
+  const Form order[3] = {kFormStored, kFormSinglePass, kFormRecompute};
+  int rc = GRPO_OK;
+  int best = -1;
+  double best_cost = 0.0;
+  for (int i = 0; i < 3; ++i) {
+    Layout t;
+    const int r = make_layout_mode(s, p, kRefSms, order[i], &t);
+    if (r != GRPO_OK) {
+      rc = r;
+      continue;
+    }
+    if (best < 0 || t.model_cost < best_cost) {
+      best = i;
+      best_cost = t.model_cost;
+    }
+  }
+  if (best < 0) return rc;
+  return make_layout_mode(s, p, sms, order[best], L);
 }
 
 int check_shape(const grpo_shape* s, bool need_seq) {
@@ -385,11 +482,13 @@ int check_shape(const grpo_shape* s, bool need_seq) {
 int check_params(const grpo_params* p) {
   if (!p) return GRPO_OK;
   if ((p->flags & ~(GRPO_FLAG_STORED_LOGITS | GRPO_FLAG_SINGLE_CTA | GRPO_FLAG_SEQUENCE_MEAN |
-                    GRPO_FLAG_FIT_FREE_MEMORY | GRPO_FLAG_RECOMPUTE_LOGITS)) != 0 ||
+                    GRPO_FLAG_FIT_FREE_MEMORY | GRPO_FLAG_RECOMPUTE_LOGITS |
+                    GRPO_FLAG_SINGLE_PASS)) != 0 ||
       p->raster_rows < 0 || p->chunk_tokens < 0 || p->vocab_block < 0)
     return GRPO_ERR_INVALID_ARG;
-  if ((p->flags & GRPO_FLAG_STORED_LOGITS) != 0 && (p->flags & GRPO_FLAG_RECOMPUTE_LOGITS) != 0)
-    return GRPO_ERR_INVALID_ARG;
+  const uint32_t forms =
+      p->flags & (GRPO_FLAG_STORED_LOGITS | GRPO_FLAG_RECOMPUTE_LOGITS | GRPO_FLAG_SINGLE_PASS);
+  if ((forms & (forms - 1)) != 0) return GRPO_ERR_INVALID_ARG;  // at most one form
   if (!(p->eps_low >= 0.f) || !(p->eps_high >= 0.f) || !(p->beta >= 0.f))
     return GRPO_ERR_INVALID_ARG;
   if (!(p->logit_scale_multiply >= 0.f) || !(p->logit_scale_divide >= 0.f) ||
@@ -971,6 +1070,164 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
   return GRPO_OK;
 }
 
+// Single-pass backward of a loss call, chunk by chunk over the active row
+// blocks and, within a chunk, vocabulary block by vocabulary block, all on the
+// caller's stream:
+//   FWDS(c, 0) UAC(c, 0) FWDS(c, 1) UAC(c, 1) ... FWDS(c, nb-1) ROWS(c) UAC(c, nb-1)
+// FWDS(c, b) computes the block's logits once: online LSE partials in slots
+// of their own, z_y, and the block's fp16 logits (box-shifted) in the chunk
+// block. UAC(c, b) turns them into P on chip and adds P W[block] to the fp32
+// accumulator U, rescaled to the running maximum. ROWS finishes each row (lse,
+// logp, token loss, g) once every block's partials are in, and the last UAC
+// turns U into dH. Each logit is computed once: 4 N D V flops in all.
+int run_single_pass(const void* hidden, const void* W, const int32_t* ids, const uint8_t* mask,
+                    const float* old_logp, const float* ref_logp, const float* adv, float* loss,
+                    float* logp_out, void* dH, const grpo_params* prm, const Layout& L,
+                    const Ws& w, int sms, cudaStream_t st) {
+  CUtensorMap map_h, map_w_k, map_w_mn;
+  const int slots = std::max(1, sms / L.ctas);
+  if (!encode_2d(&map_h, hidden, L.D, L.n, L.D, BK, BM) ||
+      !encode_2d(&map_w_k, W, L.D, L.V, L.D, BK, BN / L.ctas) ||
+      !encode_2d(&map_w_mn, W, L.D, L.V, L.D, 64, BK))
+    return GRPO_ERR_CUDA;
+  const int n_dt_dh = static_cast<int>(cdiv(L.D, BN * dh_accumulators(L.ctas)));
+  const int n_rb_total = static_cast<int>(L.nr / BM);
+  const int rb_per_chunk = L.chunk_rows / BM;
+  uint16_t* const S = reinterpret_cast<uint16_t*>(w.G);
+  float* const bmax = reinterpret_cast<float*>(w.base + L.off_bmax);
+  const int vbt = static_cast<int>(cdiv(L.vblock, BN));
+  for (int rb0 = 0; rb0 < n_rb_total; rb0 += rb_per_chunk) {
+    const int n_rb = std::min(rb_per_chunk, n_rb_total - rb0);
+    const int n_ru = static_cast<int>(cdiv(n_rb, L.ctas));
+    int slot0 = 0;
+    for (int b = 0; b < L.nvb; ++b) {
+      const int v0 = b * L.vblock;
+      const int width = std::min(L.vblock, L.V - v0);
+      const int tiles = static_cast<int>(cdiv(width, BN));
+      const int splits = single_pass_fwd_splits(n_ru, tiles, kMaxSplits / L.nvb, slots);
+      // (1) the block's logits.
+      TileArgs a = base_args(L, w);
+      set_transform(&a, prm);
+      a.n_total = L.n;
+      a.n_rb = n_rb;
+      a.rb_offset = rb0;
+      a.rb_list = w.rb_list;
+      a.n_active = w.n_active;
+      a.k_iters = static_cast<int>(cdiv(L.D, BK));
+      a.group_rows = n_ru;
+      a.n_cols = splits;
+      a.n_vtiles = tiles;
+      a.v0 = v0;
+      a.ids = ids;
+      a.mask = mask;
+      a.part_m = w.pm;
+      a.part_s = w.ps;
+      a.zy = w.zy;
+      a.part_ld = L.nr;
+      a.part_slot0 = slot0;
+      a.S = S;
+      a.ldS = L.ldS;
+      a.box_max = bmax;
+      a.ldM = L.chunk_rows;
+      CUtensorMap map_st;
+      if (!encode_2d(&map_st, S, width, static_cast<uint64_t>(n_rb) * BM, L.ldS, 64, 32))
+        return GRPO_ERR_CUDA;
+      if (launch_fwds_gemm(L.ctas, map_h, map_w_k, map_st, a,
+                           L.ctas * static_cast<int>(std::min<long long>(
+                                        static_cast<long long>(n_ru) * splits, slots)),
+                           st) != cudaSuccess)
+        return GRPO_ERR_CUDA;
+      const bool last = b + 1 == L.nvb;
+      // (2) after the last block: lse, logp, token loss and g of every row.
+      if (last) {
+        GformArgs f;
+        std::memset(&f, 0, sizeof(f));
+        f.n_total = L.n;
+        f.n_rb = n_rb;
+        f.rb_offset = rb0;
+        f.rb_list = w.rb_list;
+        f.n_active = w.n_active;
+        f.splits = slot0 + splits;
+        f.part_ld = L.nr;
+        f.vocab = L.V;
+        f.seq_len = L.T;
+        f.part_m = w.pm;
+        f.part_s = w.ps;
+        f.zy = w.zy;
+        f.ids = ids;
+        f.mask = mask;
+        f.old_logp = old_logp;
+        f.ref_logp = ref_logp;
+        f.adv = adv;
+        f.eps_low = prm->eps_low;
+        f.eps_high = prm->eps_high;
+        f.beta = prm->beta;
+        f.loss_den = prm->loss_denominator;
+        f.msum = w.msum;
+        f.seq_mode = (prm->flags & GRPO_FLAG_SEQUENCE_MEAN) != 0;
+        f.seq_lens = w.seq_lens;
+        f.n_nonempty = w.n_nonempty;
+        f.logp_out = logp_out;
+        f.lt = w.lt;
+        f.status = w.status;
+        f.lse_out = w.lse;
+        f.g_out = w.g;
+        if (launch_finalize_rows(f, n_rb * BM, st) != cudaSuccess) return GRPO_ERR_CUDA;
+      }
+      // (3) U (+)= P W[block]; dH on the last block.
+      CUtensorMap map_s;
+      if (!encode_2d(&map_s, S, width, static_cast<uint64_t>(n_rb) * BM, L.ldS, BK, BM))
+        return GRPO_ERR_CUDA;
+      TileArgs u = base_args(L, w);
+      set_transform(&u, prm);
+      u.n_total = L.n;
+      u.n_rb = n_rb;
+      u.rb_offset = rb0;
+      u.rb_list = w.rb_list;
+      u.n_active = w.n_active;
+      u.k_iters = static_cast<int>(cdiv(width, BK));
+      u.group_rows = group_rows_for(n_ru, slots);
+      u.n_cols = n_dt_dh;
+      u.v0 = v0;
+      u.ids = ids;
+      u.mask = mask;
+      u.lse = w.lse;
+      u.g = w.g;
+      u.zy = w.zy;
+      u.part_m = w.pm;
+      u.part_ld = L.nr;
+      u.slots_prev = slot0;
+      u.slots_cur = slot0 + splits;
+      u.W = static_cast<const __nv_bfloat16*>(W);
+      u.box_max = bmax;
+      u.ldM = L.chunk_rows;
+      u.acc = w.acc;
+      u.dH = static_cast<__nv_bfloat16*>(dH);
+      u.first = b == 0;
+      u.last = last;
+      if (launch_uac_gemm(L.ctas, map_s, map_w_mn, u,
+                          L.ctas * static_cast<int>(std::min<long long>(
+                                       static_cast<long long>(n_ru) * n_dt_dh, slots)),
+                          st) != cudaSuccess)
+        return GRPO_ERR_CUDA;
+      slot0 += splits;
+    }
+    (void)vbt;
+  }
+  FinishArgs fin;
+  std::memset(&fin, 0, sizeof(fin));
+  fin.n = L.n;
+  fin.mask = mask;
+  fin.lt = w.lt;
+  fin.logp_out = logp_out;
+  fin.block_partials = w.partials;
+  fin.counter = w.counter;
+  fin.loss_out = loss;
+  fin.status = w.status;
+  if (launch_finish_loss(fin, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  return GRPO_OK;
+}
+
 }  // namespace
 
 // ---- Opt-in per-launch timing ------------------------------------------------
@@ -1198,6 +1455,24 @@ int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
   if (L.stored)
     return run_stored(hidden, W, ids, mask, old_logp, ref_logp, adv, loss, logp_or_null, dH,
                       dW_or_null, &prm, L, w, sms, st);
+  if (L.single_pass && dW_or_null == nullptr)
+    return run_single_pass(hidden, W, ids, mask, old_logp, ref_logp, adv, loss, logp_or_null, dH,
+                           &prm, L, w, sms, st);
+  if (L.single_pass) {
+    // The lm_head gradient needs G explicitly, which the single pass never
+    // forms: recompute the logit tiles instead, with the same chunk and vocab
+    // block, whose workspace lies within the single pass's.
+    grpo_params p2 = prm;
+    p2.flags = (p2.flags & ~GRPO_FLAG_SINGLE_PASS) | GRPO_FLAG_RECOMPUTE_LOGITS;
+    p2.chunk_tokens = L.chunk_rows;
+    p2.vocab_block = L.vblock;
+    p2.workspace_limit_bytes = 0;
+    Layout L2;
+    if ((r = make_layout_mode(shape, &p2, sms, kFormRecompute, &L2)) != GRPO_OK) return r;
+    if (L2.total > workspace_bytes) return GRPO_ERR_WORKSPACE_TOO_SMALL;
+    L = L2;
+    w = carve(workspace, L);
+  }
   int splits = 1;
   if ((r = run_forward(hidden, W, ids, mask, w.rb_list, w.n_active, &prm, L, w, sms, &splits,
                        st)) != GRPO_OK)
@@ -1257,9 +1532,10 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
   const int grp = group_rows_exact(static_cast<int>(cdiv(n_rb, L.ctas)), slots);
   info->fwd_splits = std::min(std::max(1, slots / grp), std::min(L.nvt, kMaxSplits));
   info->launches_logp = L.n > 0 ? 2 : 0;
-  info->launches_loss = L.n <= 0 ? 0
-                      : L.stored ? 3 + 3 * info->n_chunks
-                                 : 4 + 2 * info->n_chunks * info->n_vocab_blocks;
+  info->launches_loss = L.n <= 0        ? 0
+                        : L.stored      ? 3 + 3 * info->n_chunks
+                        : L.single_pass ? 3 + info->n_chunks * (2 * L.nvb + 1)
+                                        : 4 + 2 * info->n_chunks * info->n_vocab_blocks;
   if (L.n > 0 && params != nullptr && (params->flags & GRPO_FLAG_SEQUENCE_MEAN) != 0)
     info->launches_loss += 1;
   if (L.stored) {
@@ -1269,6 +1545,7 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
   }
   info->g_in_dh_gemm = L.fused ? 1 : 0;
   info->stored_logits = L.stored ? 1 : 0;
+  info->single_pass = L.single_pass ? 1 : 0;
   info->workspace_bytes = std::max(L.total, Lmax.total);
   return GRPO_OK;
 }

@@ -1,7 +1,10 @@
-// Backward-side GEMM launchers: the G tile (recomputed logits -> bf16
-// softmax-Jacobian rows), the dH accumulation from a G block or straight
-// from a stored fp16 logit block, and the lm_head gradient, each in the
-// single-CTA and the CTA-pair variant.
+// Launchers of the backward GEMM variants, and the translation unit that
+// instantiates them (the kernel template itself is tc_gemm_kernel in
+// gemm_tc.cuh): the G tile (recomputed logits -> bf16 softmax-Jacobian rows),
+// the dH accumulation from a G block or straight from a stored fp16 logit
+// block, the single pass's U accumulation, and the lm_head gradient, each in
+// the single-CTA and the CTA-pair variant. No kernel is defined here; the file
+// exists so that these instantiations compile in parallel with the others.
 #include "launch.h"
 
 namespace grpo {
@@ -15,6 +18,8 @@ cudaError_t prepare_bwd_gemms() {
   if (e == cudaSuccess) e = prepare_gemm_variant<MODE_DW, 2>();
   if (e == cudaSuccess) e = prepare_gemm_variant<MODE_DHS, 1>();
   if (e == cudaSuccess) e = prepare_gemm_variant<MODE_DHS, 2>();
+  if (e == cudaSuccess) e = prepare_gemm_variant<MODE_UAC, 1>();
+  if (e == cudaSuccess) e = prepare_gemm_variant<MODE_UAC, 2>();
   return e;
 }
 
@@ -42,6 +47,12 @@ cudaError_t launch_dhs_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMa
                             const TileArgs& args, int grid, cudaStream_t stream) {
   return ctas == 2 ? launch_gemm_variant<MODE_DHS, 2>(map_a, map_b, args, grid, stream)
                    : launch_gemm_variant<MODE_DHS, 1>(map_a, map_b, args, grid, stream);
+}
+
+cudaError_t launch_uac_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                            const TileArgs& args, int grid, cudaStream_t stream) {
+  return ctas == 2 ? launch_gemm_variant<MODE_UAC, 2>(map_a, map_b, args, grid, stream)
+                   : launch_gemm_variant<MODE_UAC, 1>(map_a, map_b, args, grid, stream);
 }
 
 }  // namespace grpo

@@ -1,9 +1,9 @@
 // Persistent, warp-specialised tcgen05 GEMM for sm_103a with fused
-// epilogues. One CTA per SM, 192 threads (320 for MODE_DHS):
+// epilogues. One CTA per SM, 192 threads (320 for MODE_DHS and MODE_UAC):
 //   warp 0      TMA producer (one elected thread) filling the smem stage ring
 //   warp 1      TMEM allocator + MMA issuer (one elected thread)
 //   warps 2..5  epilogue: 128 threads <-> the 128 TMEM lanes (= tile rows)
-//   warps 6..9  MODE_DHS only: converter warps (the second half of each row)
+//   warps 6..9  MODE_DHS, MODE_UAC: converter warps (the second half of each row)
 // The fp32 accumulator lives in TMEM, double buffered (2 x 256 columns), so
 // the epilogue of tile j overlaps the MMAs of tile j+1.
 //
@@ -30,6 +30,13 @@
 //              converter-only warps rewrite each landed A stage in place as
 //              bf16 G (the softmax-Jacobian row, scaled by dL/dlogp) before the
 //              MMA reads it, so G never goes through HBM.
+//   MODE_UAC   the single-pass backward's second GEMM over one vocabulary block:
+//              like MODE_DHS, but the landed logits become P_v = 2^(z'_v log2e
+//              - M) f'(S_v) (M the row's running maximum after this block, the
+//              target column excluded), and the epilogue keeps the fp32
+//              accumulator U = sum_v P_v W_v across blocks, rescaled by
+//              2^(M_prev - M) whenever the maximum grows; the last block turns
+//              it into dH = g (1 - p_y) f'_y W_y - g 2^(M - lse2) U.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -48,10 +55,14 @@ constexpr int TMEM_COLS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum GemmMode { MODE_FWD = 0, MODE_BWDG = 1, MODE_DH = 2, MODE_FWDS = 3, MODE_DW = 4,
-                MODE_DHS = 5 };
+                MODE_DHS = 5, MODE_UAC = 6 };
 
 __host__ __device__ constexpr bool is_fwd(int mode) { return mode == MODE_FWD || mode == MODE_FWDS; }
-__host__ __device__ constexpr bool is_dh(int mode) { return mode == MODE_DH || mode == MODE_DHS; }
+__host__ __device__ constexpr bool is_dh(int mode) {
+  return mode == MODE_DH || mode == MODE_DHS || mode == MODE_UAC;
+}
+// Modes whose A operand is stored fp16 logits, converted on chip before the MMA.
+__host__ __device__ constexpr bool has_cvt(int mode) { return mode == MODE_DHS || mode == MODE_UAC; }
 
 struct TileArgs {
   long long n_total;     // N: rows of hidden / dH; global rows >= N are padding
@@ -73,11 +84,17 @@ struct TileArgs {
   float k0, k1, k2;
   const int32_t* ids;    // indexed by global row
   const uint8_t* mask;   // FWD: optional; masked rows' ids are never read
-  // MODE_FWD
-  float* part_m;         // [n_cols][part_ld] running max (log2 units)
-  float* part_s;         // [n_cols][part_ld] running sum of 2^(x - max)
+  // MODE_FWD (written; MODE_UAC reads part_m)
+  float* part_m;         // [slots][part_ld] running max (log2 units)
+  float* part_s;         // [slots][part_ld] running sum of 2^(x - max)
   float* zy;             // [N] target logit, indexed by global row
   long long part_ld;
+  int part_slot0;        // slot of this launch's first vocab split
+  // MODE_UAC: the split partials of the blocks so far (slots_cur) and before
+  // this block (slots_prev) give the row's running maximum now and before;
+  // W (bf16 [V][hidden]) gives W_y on the last block.
+  int slots_cur, slots_prev;
+  const __nv_bfloat16* W;
   // MODE_BWDG, MODE_DHS
   const float* lse;      // indexed by global row
   const float* g;        // indexed by global row
@@ -92,7 +109,7 @@ struct TileArgs {
   // MODE_DW
   float* dW;             // [V][hidden] fp32 output / accumulator
   int dw_rows;           // vocab rows of dW this launch covers (from v0)
-  // MODE_DH, MODE_DHS
+  // MODE_DH, MODE_DHS, MODE_UAC
   float* acc;            // [local rows][hidden] fp32 accumulator
   __nv_bfloat16* dH;     // [N][hidden] output, indexed by global row
   int first;
@@ -177,31 +194,60 @@ __device__ __forceinline__ int swz_offset(int r, int c) {
   return r * 128 + ((((c >> 3) ^ r) & 7) << 4) + (c & 7) * 2;
 }
 
-// MODE_DHS: rewrites chunks jb..jb+NCH-1 (8 columns each) of row r of a
-// landed A stage (one stored box: 64 fp16 values z'_v - zoff of vocab columns
-// vbase.., zoff the box's maximum) in place as the bf16 G values,
-//   G_v = g (onehot_v(y) - 2^(z'_v log2e - lse2)) f'(S_v).
-// c = log2|g| - lse2 + zoff log2e folds the row's and the box's constants.
-// Rows with g = 0 (masked, padding, past N) become zeros whatever the buffer
-// held; columns at or past the vocabulary size become zeros. The main loop
+// Two stored fp16 values of a box-shifted row (both <= 0) as fp32 magnitudes
+// scaled by 2^-112: the sign bits are dropped, and the exponent and mantissa
+// fields move to their fp32 positions, where fp16's exponent bias (15) reads
+// as fp32's (127) less 112. Exact for every finite fp16, subnormals included
+// (an fp16 subnormal lands on the fp32 subnormal of the same scaled value).
+// Integer shifts and masks instead of two conversions on the pipe that also
+// runs the exponentials.
+__device__ __forceinline__ void f16x2_nonpos_magnitudes(uint32_t w, float& lo, float& hi) {
+  lo = __uint_as_float((w << 13) & 0x0FFFE000u);
+  hi = __uint_as_float((w >> 3) & 0x0FFFE000u);
+}
+// -log2(e) 2^112: with f16x2_nonpos_magnitudes, fmaf(m, kNegLog2eScaled, c)
+// equals fmaf(z, log2e, c) for the stored value z = -m 2^112, bit for bit
+// (scaling by a power of two is exact).
+constexpr float kNegLog2eScaled = -kLog2e * 5192296858534827628530496329220096.0f;
+
+// Per-row constants of the in-GEMM conversion of stored logits (MODE_DHS,
+// MODE_UAC). A stored value s of column v is z'_v - zoff, zoff the maximum of
+// the column's 64-column box (one pipeline stage), and becomes the bf16
+//   without a transform:  sign * 2^(s log2e + c + zoff log2e)
+//   with one:             scale * 2^((s + zoff) log2e + shift2) f'(S_v)
+// (f' recovered from z', as in dz_of_logit); the target column gets ytarget.
+//   MODE_DHS (G):  c = log2|g| - lse2, sign = -sign(g), scale = -g,
+//                  shift2 = -lse2, ytarget = g (1 - p_y) f'_y
+//   MODE_UAC (P):  c = -M, sign = +, scale = 1, shift2 = -M, ytarget = 0
+// with M the row's running maximum (log2 units).
+struct RowCvt {
+  bool zero;        // the row contributes nothing: zeros whatever the buffer held
+  int y;            // target column (vocabulary index), or -1
+  float c;          // see above (without the box maximum)
+  uint32_t sgn;     // sign bits XORed into each packed bf16 pair
+  float scale, shift2;
+  float ytarget;
+};
+
+// Rewrites chunks jb..jb+NCH-1 (8 columns each) of row r of a landed A stage
+// (64 stored values of vocab columns vbase.., box maximum zoff) in place as
+// bf16. Columns at or past the vocabulary size become zeros. The main loop
 // runs over logical chunks, so the 8 lanes of a shared-memory phase (8
 // consecutive rows, same chunk) touch 8 different physical chunks: no bank
 // conflicts. The target column (at most once per row and unit) and the
-// vocabulary edge (the last stage) are fixed up afterwards, off the hot path;
-// the target uses the fp32 z'_y the logit GEMM recorded.
+// vocabulary edge (the last stage) are fixed up afterwards, off the hot path.
 template <int NCH>
-__device__ __forceinline__ void logits_to_g_row(const TileArgs& a, uint8_t* tile, int r, int jb,
-                                                int vbase, int y, float g, float lse2,
-                                                float zy, float c, uint32_t sgn, float zoff) {
+__device__ __forceinline__ void stage_row_to_bf16(const TileArgs& a, uint8_t* tile, int r, int jb,
+                                                  int vbase, const RowCvt& rc, float zoff) {
   uint4* row = reinterpret_cast<uint4*>(tile + r * 128);
   const int sw = r & 7;
-  if (g == 0.f) {
+  if (rc.zero) {
 #pragma unroll
     for (int j = 0; j < NCH; ++j) row[(jb + j) ^ sw] = make_uint4(0u, 0u, 0u, 0u);
     return;
   }
-  const float ng = -g;
   if (a.xmode == 0) {
+    const float c = fmaf(zoff, kLog2e, rc.c);
     uint4 in[NCH];
 #pragma unroll
     for (int j = 0; j < NCH; ++j) in[j] = row[(jb + j) ^ sw];
@@ -211,10 +257,10 @@ __device__ __forceinline__ void logits_to_g_row(const TileArgs& a, uint8_t* tile
       uint32_t o[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        // -g 2^(z log2e - lse2) = -sign(g) 2^(z log2e + c), c = log2|g| - lse2
-        float z0, z1;
-        unpack_f16x2(w[e], z0, z1);
-        o[e] = pack_bf16x2(ex2(fmaf(z0, kLog2e, c)), ex2(fmaf(z1, kLog2e, c))) ^ sgn;
+        float m0, m1;
+        f16x2_nonpos_magnitudes(w[e], m0, m1);
+        o[e] = pack_bf16x2(ex2(fmaf(m0, kNegLog2eScaled, c)), ex2(fmaf(m1, kNegLog2eScaled, c))) ^
+               rc.sgn;
       }
       row[(jb + j) ^ sw] = make_uint4(o[0], o[1], o[2], o[3]);
     }
@@ -230,17 +276,16 @@ __device__ __forceinline__ void logits_to_g_row(const TileArgs& a, uint8_t* tile
         unpack_f16x2(w[e], z0, z1);
         z0 += zoff;
         z1 += zoff;
-        o[e] = pack_bf16x2(ng * ex2(fmaf(z0, kLog2e, -lse2)) * dz_of_logit(a, z0),
-                           ng * ex2(fmaf(z1, kLog2e, -lse2)) * dz_of_logit(a, z1));
+        o[e] = pack_bf16x2(rc.scale * ex2(fmaf(z0, kLog2e, rc.shift2)) * dz_of_logit(a, z0),
+                           rc.scale * ex2(fmaf(z1, kLog2e, rc.shift2)) * dz_of_logit(a, z1));
       }
       row[j ^ sw] = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
-  const unsigned yoff = static_cast<unsigned>(y - vbase - jb * 8);
-  if (yoff < static_cast<unsigned>(NCH * 8) && y < a.vocab) {
-    const float val = (ng * ex2(fmaf(zy, kLog2e, -lse2)) + g) * dz_of_logit(a, zy);
+  const unsigned yoff = static_cast<unsigned>(rc.y - vbase - jb * 8);
+  if (yoff < static_cast<unsigned>(NCH * 8) && rc.y < a.vocab) {
     *reinterpret_cast<uint16_t*>(tile + swz_offset(r, jb * 8 + static_cast<int>(yoff))) =
-        static_cast<uint16_t>(pack_bf16x2(val, 0.f) & 0xffffu);
+        static_cast<uint16_t>(pack_bf16x2(rc.ytarget, 0.f) & 0xffffu);
   }
   if (vbase + (jb + NCH) * 8 > a.vocab) {
 #pragma unroll 1
@@ -291,7 +336,7 @@ struct PairCfg {
   static constexpr int kSmemBytes = kStages * kStageBytes + kStoreBytes + 1024;
   // Warp groups that convert A stages (MODE_DHS): the epilogue warps and a
   // second group of converter-only warps, each group half of every row.
-  static constexpr int kCvtGroups = MODE == MODE_DHS ? 2 : 1;
+  static constexpr int kCvtGroups = has_cvt(MODE) ? 2 : 1;
   static constexpr int kThreads = 64 + 128 * kCvtGroups;
 };
 
@@ -334,10 +379,10 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
   __shared__ __align__(8) uint64_t tfull_bar[2];
   __shared__ __align__(8) uint64_t tempty_bar[2];
   __shared__ __align__(8) uint64_t drain_bar;
-  // MODE_DHS: this CTA's A stage has landed (its own barrier); the stage has
-  // been converted to G by the pair's epilogue warps (the leader's barrier).
-  __shared__ __align__(8) uint64_t afull_bar[MODE == MODE_DHS ? kStages : 1];
-  __shared__ __align__(8) uint64_t cvt_bar[MODE == MODE_DHS ? kStages : 1];
+  // MODE_DHS, MODE_UAC: this CTA's A stage has landed (its own barrier); the
+  // stage has been converted by the pair's converter warps (the leader's barrier).
+  __shared__ __align__(8) uint64_t afull_bar[has_cvt(MODE) ? kStages : 1];
+  __shared__ __align__(8) uint64_t cvt_bar[has_cvt(MODE) ? kStages : 1];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -363,7 +408,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
       mbar_init(&tempty_bar[b], 4 * CTAS);  // every epilogue warp of the pair
     }
     mbar_init(&drain_bar, 1);
-    if constexpr (MODE == MODE_DHS) {
+    if constexpr (has_cvt(MODE)) {
       for (int s = 0; s < kStages; ++s) {
         mbar_init(&afull_bar[s], 1);
         mbar_init(&cvt_bar[s], 4 * C::kCvtGroups * CTAS);  // every converter warp of the pair
@@ -435,7 +480,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             }
             uint8_t* a_dst = smem + s * C::kStageBytes;
             uint8_t* b_dst = a_dst + C::kKSub * A_BYTES;
-            if constexpr (MODE == MODE_DHS) {
+            if constexpr (has_cvt(MODE)) {
               // A (the stored fp16 logits) into this CTA's stage, counted on
               // its own barrier: the epilogue warps turn it into G in place.
               mbar_arrive_expect_tx(&afull_bar[s], A_BYTES);
@@ -526,7 +571,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
         // CTA's A copies on its own barriers.
         for (uint32_t j = (it >= kStages ? it - kStages : 0); j < it; ++j) {
           if (rank == 0) drain_wait(&full_bar[j % kStages], (j / kStages) & 1u);
-          if constexpr (MODE == MODE_DHS)
+          if constexpr (has_cvt(MODE))
             drain_wait(&afull_bar[j % kStages], (j / kStages) & 1u);
         }
       }
@@ -564,7 +609,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
               ok = false;
               break;
             }
-            if constexpr (MODE == MODE_DHS) {
+            if constexpr (has_cvt(MODE)) {
               if (!mbar_wait(&cvt_bar[s], round & 1u, abort_flag, args.status)) {
                 ok = false;
                 break;
@@ -618,7 +663,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
     // ---------------------------------------------------------- epilogue --
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int lrow_in_tile = q * 32 + lane;
-    const int part = (warp - 2) >> 2;  // 0: epilogue warps; 1: converter-only (MODE_DHS)
+    const int part = (warp - 2) >> 2;  // 0: epilogue warps; 1: converter-only (has_cvt)
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     uint32_t tile_it = 0;
     bool ok = true;
@@ -628,7 +673,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
         CTAS == 2 ? mapa_shared(smem_u32(&tempty_bar[0]), 0) : smem_u32(&tempty_bar[0]);
     const uint32_t cvt_addr0 =
         CTAS == 2 ? mapa_shared(smem_u32(&cvt_bar[0]), 0) : smem_u32(&cvt_bar[0]);
-    uint32_t cit = 0;  // MODE_DHS: A stages converted so far
+    uint32_t cit = 0;  // has_cvt: A stages converted so far
     // kTmaStore: this warp's two staging buffers and the boxes it has stored.
     uint8_t* const stage_out = smem + C::kStages * C::kStageBytes + q * 2 * C::kStoreBufBytes;
     uint32_t n_stores = 0;
@@ -646,43 +691,86 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
       // Per-row state.
       float m2 = -INFINITY, ssum = 0.f;  // FWD
       int y = -1;
-      float lse2 = 0.f, gval = 0.f;      // BWDG, DHS
-      float zyv = 0.f;                   // DHS: fp32 target logit
-      float cexp = 0.f;                  // DHS: log2|g| - lse2
-      uint32_t sgn = 0u;                 // DHS: sign bits of -g on a bf16 pair
+      float lse2 = 0.f, gval = 0.f;      // BWDG
+      RowCvt rc;                         // DHS, UAC: conversion constants
+      rc.zero = true;
+      rc.y = -1;
+      rc.c = 0.f;
+      rc.sgn = 0u;
+      rc.scale = 1.f;
+      rc.shift2 = 0.f;
+      rc.ytarget = 0.f;
+      float u_alpha = 0.f, u_cu = 0.f, u_cw = 0.f;  // UAC epilogue: rescale, dH factors
       if (is_fwd(MODE)) {
         if (valid && (args.mask == nullptr || args.mask[grow] != 0)) y = args.ids[grow];
-      } else if (MODE == MODE_BWDG || MODE == MODE_DHS) {
+      } else if (MODE == MODE_BWDG) {
         if (valid) {
           gval = args.g[grow];
           lse2 = args.lse[grow] * kLog2e;
+          if (gval != 0.f) y = args.ids[grow];
+        }
+      } else if (MODE == MODE_DHS) {
+        if (valid) {
+          gval = args.g[grow];
           if (gval != 0.f) {
-            y = args.ids[grow];
-            if (MODE == MODE_DHS) {
-              zyv = args.zy[grow];
-              cexp = log2f(fabsf(gval)) - lse2;
-              sgn = gval > 0.f ? 0x80008000u : 0u;
+            lse2 = args.lse[grow] * kLog2e;
+            const float zy = args.zy[grow];  // fp32 target logit
+            rc.zero = false;
+            rc.y = args.ids[grow];
+            rc.c = log2f(fabsf(gval)) - lse2;
+            rc.sgn = gval > 0.f ? 0x80008000u : 0u;  // -g: the sign of each bf16
+            rc.scale = -gval;
+            rc.shift2 = -lse2;
+            rc.ytarget = (gval - gval * ex2(fmaf(zy, kLog2e, -lse2))) * dz_of_logit(args, zy);
+          }
+        }
+      } else if (MODE == MODE_UAC) {
+        if (valid && (args.mask == nullptr || args.mask[grow] != 0)) {
+          // Running maxima (log2 units) from the forward's split partials.
+          float mcur = -INFINITY;
+          for (int sl = 0; sl < args.slots_cur; ++sl)
+            mcur = fmaxf(mcur, args.part_m[sl * args.part_ld + grow]);
+          const int yy = args.ids[grow];
+          rc.zero = false;
+          rc.y = (yy >= 0 && yy < args.vocab) ? yy : -1;  // bad ids: status set by the row finish
+          rc.c = -mcur;
+          rc.shift2 = -mcur;
+          if (part == 0) {
+            if (!args.first) {
+              float mprev = -INFINITY;
+              for (int sl = 0; sl < args.slots_prev; ++sl)
+                mprev = fmaxf(mprev, args.part_m[sl * args.part_ld + grow]);
+              u_alpha = ex2(mprev - mcur);
+            }
+            if (args.last) {
+              const float g = args.g[grow];
+              const float l2 = args.lse[grow] * kLog2e;
+              u_cu = g * ex2(mcur - l2);
+              if (rc.y >= 0) {
+                const float zy = args.zy[grow];
+                u_cw = (g - g * ex2(fmaf(zy, kLog2e, -l2))) * dz_of_logit(args, zy);
+              }
             }
           }
         }
       }
 
-      if constexpr (MODE == MODE_DHS) {
-        // Every A stage of this unit, as it lands: fp16 logits -> bf16 G in
+      if constexpr (has_cvt(MODE)) {
+        // Every A stage of this unit, as it lands: fp16 logits -> bf16 in
         // place (this thread's part of its row), then tell the MMA issuer.
-        // Stage k is box (v0 / 64) + k; its maximum is loaded kPre stages
-        // ahead (rows with g = 0 need none).
+        // Stage k is box k of the stored block; its maximum is loaded kPre
+        // stages ahead (rows that contribute nothing need none).
         constexpr int kPre = 4;
-        const float* bm = args.box_max + static_cast<long long>(args.v0 >> 6) * args.ldM + lrow;
+        const float* bm = args.box_max + lrow;
         float zq[kPre];
 #pragma unroll
         for (int j = 0; j < kPre; ++j)
-          zq[j] = (gval != 0.f && j < k_iters) ? __ldg(bm + j * args.ldM) : 0.f;
+          zq[j] = (!rc.zero && j < k_iters) ? __ldg(bm + j * args.ldM) : 0.f;
         for (int k = 0; k < k_iters; ++k, ++cit) {
           const float zoff = zq[0];
 #pragma unroll
           for (int j = 0; j + 1 < kPre; ++j) zq[j] = zq[j + 1];
-          zq[kPre - 1] = (gval != 0.f && k + kPre < k_iters)
+          zq[kPre - 1] = (!rc.zero && k + kPre < k_iters)
                              ? __ldg(bm + static_cast<long long>(k + kPre) * args.ldM)
                              : 0.f;
           const int s = static_cast<int>(cit % kStages);
@@ -691,9 +779,8 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             break;
           }
           constexpr int kNch = 8 / C::kCvtGroups;
-          logits_to_g_row<kNch>(args, smem + s * C::kStageBytes, lrow_in_tile, part * kNch,
-                                args.v0 + k * BK, y, gval, lse2, zyv,
-                                fmaf(zoff, kLog2e, cexp), sgn, zoff);
+          stage_row_to_bf16<kNch>(args, smem + s * C::kStageBytes, lrow_in_tile, part * kNch,
+                                  args.v0 + k * BK, rc, zoff);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -718,7 +805,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
         if (MODE == MODE_FWD) {
 #pragma unroll 1
           for (int c = 0; c < C::kTileN / 32; ++c) {
-            const int col0 = t * C::kTileN + c * 32;
+            const int col0 = args.v0 + t * C::kTileN + c * 32;
             if (col0 >= args.vocab) break;  // warp-uniform
             float v[32];
             tmem_ld32(tbase + c * 32, v);
@@ -764,7 +851,8 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
           // 2^-6 of absolute precision, i.e. 1.6 % of its softmax term.
 #pragma unroll 1
           for (int c = 0; c < C::kTileN / 64; ++c) {
-            const int col0 = t * C::kTileN + c * 64;
+            const int lcol = t * C::kTileN + c * 64;  // column of the stored block
+            const int col0 = args.v0 + lcol;           // vocabulary column
             if (col0 >= args.vocab) break;  // warp-uniform
             float lo[32], hi[32];
             tmem_ld32(tbase + c * 64, lo);
@@ -819,14 +907,14 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                  tma_store_2d(&map_c, buf, col0, li * BM + q * 32);
+                  tma_store_2d(&map_c, buf, lcol, li * BM + q * 32);
                   bulk_commit_group();
                 }
                 ++n_stores;
-                args.box_max[static_cast<long long>(col0 >> 6) * args.ldM + lrow] = mb;
+                args.box_max[static_cast<long long>(lcol >> 6) * args.ldM + lrow] = mb;
               }
             } else if (valid) {
-              uint16_t* dst = args.S + static_cast<long long>(lrow) * args.ldS + col0;
+              uint16_t* dst = args.S + static_cast<long long>(lrow) * args.ldS + lcol;
               if (col0 + 64 <= args.vocab) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -848,7 +936,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
                     dst[32 + j] = static_cast<uint16_t>(pack_f16x2(hi[j] - mb, 0.f) & 0xffffu);
                 }
               }
-              args.box_max[static_cast<long long>(col0 >> 6) * args.ldM + lrow] = mb;
+              args.box_max[static_cast<long long>(lcol >> 6) * args.ldM + lrow] = mb;
             }
             const float mn = fmaxf(m2, mb * kLog2e);
             float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
@@ -1020,6 +1108,59 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
               }
             }
           }
+        } else if (MODE == MODE_UAC) {
+          // U (+)= this block's P W, rescaled to the running maximum; on the
+          // last block dH = g (1 - p_y) f'_y W_y - g 2^(M - lse2) U.
+#pragma unroll 1
+          for (int c = 0; c < C::kTileN / 32; ++c) {
+            const int d0 = t * C::kTileN + c * 32;
+            if (d0 >= args.hidden) break;  // warp-uniform
+            float v[32];
+            tmem_ld32(tbase + c * 32, v);
+            if (valid) {
+              float* accp = args.acc + static_cast<long long>(lrow) * args.hidden + d0;
+              __nv_bfloat16* outp = args.dH + static_cast<long long>(grow) * args.hidden + d0;
+              const __nv_bfloat16* wy =
+                  args.W + static_cast<long long>(rc.y < 0 ? 0 : rc.y) * args.hidden + d0;
+#pragma unroll
+              for (int j8 = 0; j8 < 4; ++j8) {
+                if (d0 + j8 * 8 >= args.hidden) break;
+                float* x = v + j8 * 8;
+                if (rc.zero) {
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) x[e] = 0.f;
+                } else if (!args.first) {
+                  const float4 a0 = *reinterpret_cast<const float4*>(accp + j8 * 8);
+                  const float4 a1 = *reinterpret_cast<const float4*>(accp + j8 * 8 + 4);
+                  const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) x[e] = fmaf(u_alpha, av[e], x[e]);
+                }
+                if (args.last) {
+                  if (!rc.zero) {
+                    float wv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    if (rc.y >= 0) {
+                      const uint4 wb = *reinterpret_cast<const uint4*>(wy + j8 * 8);
+                      const uint32_t ww[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                      for (int e = 0; e < 4; ++e) {
+                        wv[2 * e] = __uint_as_float(ww[e] << 16);
+                        wv[2 * e + 1] = __uint_as_float(ww[e] & 0xffff0000u);
+                      }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = fmaf(u_cw, wv[e], -u_cu * x[e]);
+                  }
+                  st_global_v4(outp + j8 * 8, pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
+                               pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+                } else {
+                  *reinterpret_cast<float4*>(accp + j8 * 8) = make_float4(x[0], x[1], x[2], x[3]);
+                  *reinterpret_cast<float4*>(accp + j8 * 8 + 4) =
+                      make_float4(x[4], x[5], x[6], x[7]);
+                }
+              }
+            }
+          }
         } else {  // MODE_DH
 #pragma unroll 1
           for (int c = 0; c < C::kTileN / 32; ++c) {
@@ -1070,8 +1211,8 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
         }
       }
       if (is_fwd(MODE) && ok && valid) {
-        args.part_m[static_cast<long long>(col) * args.part_ld + grow] = m2;
-        args.part_s[static_cast<long long>(col) * args.part_ld + grow] = ssum;
+        args.part_m[static_cast<long long>(args.part_slot0 + col) * args.part_ld + grow] = m2;
+        args.part_s[static_cast<long long>(args.part_slot0 + col) * args.part_ld + grow] = ssum;
       }
     }
     if constexpr (C::kTmaStore) {

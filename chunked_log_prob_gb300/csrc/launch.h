@@ -159,6 +159,10 @@ cudaError_t launch_dh_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap
                            const TileArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_dhs_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                             const TileArgs& args, int grid, cudaStream_t stream);
+// map_a: one vocabulary block of stored fp16 logits [rows][width] (64 x 128
+// boxes, 128-byte swizzle); map_b: W MN-major (64 x 64 boxes).
+cudaError_t launch_uac_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                            const TileArgs& args, int grid, cudaStream_t stream);
 // map_dw: dW[v0 : v0 + dw_rows) as fp32 [rows][hidden], 32 x 32 boxes with the
 // 128-byte swizzle (used by the CTA-pair variant).
 cudaError_t launch_dw_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,

@@ -76,19 +76,23 @@ typedef struct grpo_shape {
   int32_t reserved; /* must be 0                                              */
 } grpo_shape;
 
-/* The backward form. Two exist; without either of the two flags below the
+/* The backward form. Three exist; without any of the three flags below the
  * call chooses (the default):
  *   - stored logits (GRPO_FLAG_STORED_LOGITS): 4 N D V flops, a workspace
  *     of chunk x V x 2 bytes (and twice that at D > 2048, see below);
+ *   - single pass (GRPO_FLAG_SINGLE_PASS): 4 N D V flops, a workspace of
+ *     chunk x vocab_block x 2 bytes plus a chunk x D fp32 accumulator;
  *   - recomputed logit tiles (GRPO_FLAG_RECOMPUTE_LOGITS): 6 N D V flops
  *     (the pages' backward, which re-runs the forward), a workspace of
  *     chunk x vocab_block x 2 bytes plus a chunk x D fp32 accumulator.
- * The automatic choice is the stored form unless it does not fit the
- * workspace budget (workspace_limit_bytes, or half the free device memory
- * with GRPO_FLAG_FIT_FREE_MEMORY), or its modelled GEMM time within that
- * budget is longer than the recomputed form's (chunks too small for whole SM
- * waves of the dH GEMM). The choice is made at GB300's SM count, so that
- * grpo_workspace_size and the call agree; grpo_get_plan reports it.
+ * The automatic choice is, among the forms that fit the workspace budget
+ * (workspace_limit_bytes, or half the free device memory with
+ * GRPO_FLAG_FIT_FREE_MEMORY; none by default), the one whose modelled GEMM
+ * time is shortest (whole SM waves of each launch, the separate G pass the
+ * stored form cannot hide, the single pass's on-chip conversion). It is made
+ * at GB300's SM count, so that grpo_workspace_size and the call agree;
+ * grpo_get_plan reports it. Setting more than one of the three flags is
+ * GRPO_ERR_INVALID_ARG.
  *
  * grpo_params.flags bit: backward without a second logit GEMM. Per chunk of
  * rows, the forward GEMM also keeps the chunk's (transformed) logits in fp16
@@ -125,9 +129,21 @@ typedef struct grpo_shape {
 
 /* grpo_params.flags bit: the backward recomputes the logit tiles chunk by
  * chunk and vocab block by vocab block (G = g (onehot - softmax) formed in
- * the GEMM's epilogue, then dH += G W[block]): the smallest workspace.
- * Setting it together with GRPO_FLAG_STORED_LOGITS is GRPO_ERR_INVALID_ARG. */
+ * the GEMM's epilogue, then dH += G W[block]): the smallest workspace. */
 #define GRPO_FLAG_RECOMPUTE_LOGITS 16u
+
+/* grpo_params.flags bit: the single-pass backward. Per chunk of rows and per
+ * vocabulary block of vocab_block columns (automatic: blocks of about 32768,
+ * at most 32 of them), one logit GEMM keeps the block's logits in fp16
+ * (box-shifted as above) and one GEMM converts them on chip to
+ * P_v = exp(z'_v - M) f'(S_v), M the row's running maximum, the target column
+ * left out, and adds P W[block] into an fp32 accumulator U, rescaled whenever
+ * the maximum grows. After the last block, dH = g (1 - p_y) f'_y W[y]
+ * - g exp(M - lse) U. Each logit is computed once (4 N D V flops, like the
+ * stored form), while the workspace holds one block: chunk x vocab_block x
+ * 2 bytes plus the chunk x D fp32 accumulator. With dW requested the call
+ * recomputes the logit tiles instead (same chunk and vocab block). */
+#define GRPO_FLAG_SINGLE_PASS 32u
 
 typedef struct grpo_params {
   float eps_low;          /* ratio clip: lower bound 1 - eps_low (0.2)         */
@@ -164,9 +180,14 @@ void grpo_default_params(grpo_params* params);
 
 /* Bytes of device workspace that grpo_loss_fwd_bwd needs for this shape and
  * these params (enough for grpo_logp_fwd too, which needs only the part that
- * does not depend on the chunking). Host only, touches no GPU. The size grows with
- * N (a few fp32 per token) and with chunk_tokens x vocab_block, never with
- * N x V. Returns GRPO_OK or GRPO_ERR_INVALID_ARG / _UNSUPPORTED_SHAPE. */
+ * does not depend on the chunking). Host only, touches no GPU (except with
+ * GRPO_FLAG_FIT_FREE_MEMORY, which reads the free memory). The size grows
+ * with N (a few fp32 per token) and with the chunk (chunk x V for the stored
+ * form, chunk x vocab_block otherwise), never with N x V: the point of
+ * "GRPO with 7x longer context", section "Flattened sequence length
+ * chunking", Eq. 1-3, where the logit memory follows the chunk, not the
+ * batch. Returns GRPO_OK or GRPO_ERR_INVALID_ARG / _UNSUPPORTED_SHAPE /
+ * _WORKSPACE_TOO_SMALL (a budget below what any plan needs). */
 int grpo_workspace_size(const grpo_shape* shape, const grpo_params* params, size_t* bytes);
 
 /* Selective log-softmax ("GRPO with 7x longer context", section "Flattened
@@ -222,10 +243,10 @@ typedef struct grpo_plan_info {
   int32_t g_in_dh_gemm;      /* 1: the stored-logit backward forms G inside
                                 the dH GEMM when dW is not requested (hidden
                                 <= 2048); 0: in a pass of its own          */
-  int32_t stored_logits;     /* 1: the stored-logit backward; 0: recomputed
-                                logit tiles (the flags' or the automatic
-                                choice)                                    */
-  int32_t reserved;
+  int32_t stored_logits;     /* 1: the stored-logit backward              */
+  int32_t single_pass;       /* 1: the single-pass backward (neither: the
+                                recomputed logit tiles); the flags' or the
+                                automatic choice                          */
   uint64_t workspace_bytes;  /* same as grpo_workspace_size                  */
 } grpo_plan_info;
 
@@ -298,9 +319,10 @@ int grpo_selftest_bounded_wait(void* workspace, size_t workspace_bytes, void* st
  * are lost. Kernel names are the device functions', e.g. "finalize_gform_kernel".
  * GEMM variants are named "tc_gemm_kernel<mode, ctas>": mode 0 is the logit GEMM
  * of the forward pass, 1 forms G from recomputed logits, 2 is G W -> dH, 3 is
- * the logit GEMM that also stores fp16 logits, 4 is the lm_head gradient, and
- * 5 is the dH GEMM that forms G from the stored logits; ctas is 2 for a CTA
- * pair. Returns GRPO_OK, GRPO_ERR_INVALID_ARG (count null, capacity < 0, or out
+ * the logit GEMM that also stores fp16 logits, 4 is the lm_head gradient,
+ * 5 is the dH GEMM that forms G from the stored logits, and 6 is the single
+ * pass's GEMM that forms P from one block's stored logits and accumulates U;
+ * ctas is 2 for a CTA pair. Returns GRPO_OK, GRPO_ERR_INVALID_ARG (count null, capacity < 0, or out
  * null with capacity > 0) or GRPO_ERR_CUDA (an event could not be read; the
  * other launches are still summed). */
 typedef struct grpo_kernel_time {

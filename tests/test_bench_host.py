@@ -152,3 +152,21 @@ def test_record_traffic_command_line(tmp_path):
     assert rec["command"] == "ncu ..." and rec["backward"] == "recompute"
     assert rec["kernel_source_hash"] == bench.kernel_source_hash()
     assert rec["per_kernel"]["tc_gemm_kernel<3, 2>"]["read_bytes"] == 2 * 2000.0e6
+
+
+def test_record_traffic_of_single_kernel_captures(tmp_path, monkeypatch):
+    # A capture of one kernel, a few launches (-k, -c) holds no whole call: the
+    # record keeps each kernel's bytes per launch, which is what the roofline reads.
+    csv = tmp_path / "one_kernel.csv"
+    name = "void grpo::tc_gemm_kernel<(int)3, (int)2>(CUtensorMap, CUtensorMap, grpo::TileArgs)"
+    _ncu_csv(csv, [(name, 1000.0, 0.5e6, 2000.0),    # MB read, KB written, us
+                   (name, 1200.0, 0.5e6, 2200.0)])
+    monkeypatch.setattr(bench, "traffic_path", lambda w, b: str(tmp_path / f"t_{w}_{b}.json"))
+    rec = bench.record_traffic(str(csv), "toy", "stored", "ncu -k ...")
+    e = rec["per_kernel"]["tc_gemm_kernel<3, 2>"]
+    assert e["launches"] == 2 and rec["dram_bytes_per_call"] is None
+    assert abs((e["read_bytes"] + e["write_bytes"]) / e["launches"] - 1.6e9) < 1.0
+    r = bench.kernel_roofline([{"name": "tc_gemm_kernel<3, 2>", "launches": 4, "total_ms": 8.0}],
+                              1, 4096, 128256, 16384, {"hbm_gbs": 7000.0, "bf16_tflops": 2000.0,
+                                                       "bf16_tflops_sustained": 1700.0}, rec)
+    assert abs(r["traffic"] - 1.6e9) < 1.0

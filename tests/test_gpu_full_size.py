@@ -1,7 +1,8 @@
 """Full-size GPU parity on the four large workloads, for both backward forms
 (flags 1 = stored fp16 logits, the form the library chooses by default when
-no workspace budget is set and the form bench.py times; flags 16 = recomputed
-logit tiles), each with its automatic plan as bench.py launches it.
+no workspace budget is set and the form bench.py times; flags 32 = the single
+pass over vocabulary blocks; flags 16 = recomputed logit tiles), each with its
+automatic plan as bench.py launches it.
 
 The oracle cannot afford all N x V logits in fp64 at these sizes, so:
   * logp and dH are compared on a seeded sample of rows. Given the loss
@@ -65,7 +66,7 @@ def _run(clp, p, mask, old, ref, flags=16):
     return loss.item(), logp.cpu(), dH, st
 
 
-@pytest.mark.parametrize("flags", [16, 1], ids=["recompute", "stored"])
+@pytest.mark.parametrize("flags", [16, 1, 32], ids=["recompute", "stored", "single_pass"])
 @pytest.mark.parametrize("name", ["qwen2.5-1.5b", "llama-3.1-8b", "qwen3-8b-long",
                                   "gpt-oss-20b-long"])
 def test_full_size_sampled_rows(clp, name, flags):
@@ -125,7 +126,7 @@ def llama_full_oracle():
     return p, lp
 
 
-@pytest.mark.parametrize("flags", [1, 16], ids=["stored", "recompute"])
+@pytest.mark.parametrize("flags", [1, 16, 32], ids=["stored", "recompute", "single_pass"])
 def test_llama_full_loss_exact(clp, llama_full_oracle, flags):
     # The loss of the bench's own workload, exactly, with old/ref = oracle logp
     # + noise: every row's logp enters it.
@@ -158,7 +159,7 @@ def test_llama_lm_head_gradient_column_sums(clp):
         assert torch.isfinite(dW).all() and colsum <= 2e-2 * scale
 
 
-@pytest.mark.parametrize("flags", [1, 16], ids=["stored", "recompute"])
+@pytest.mark.parametrize("flags", [1, 16, 32], ids=["stored", "recompute", "single_pass"])
 def test_qwen3_head_chunk_sweep(clp, flags):
     # The Qwen3-8B long-context head (D = 4096, V = 151936) with the workload's
     # chunk sweep of 1K, 4K and 16K rows, on a reduced batch (3 completions in
@@ -207,7 +208,8 @@ def test_qwen3_head_chunk_sweep(clp, flags):
             # nothing depends on the chunk.
             assert torch.equal(L0, L1) and torch.equal(lp0, lp1) and torch.equal(dh0, dh1)
         else:
-            # Stored logits: each chunk's forward splits the vocabulary to fill
-            # whole SM waves, so the fp32 sums run in a chunk-dependent order.
+            # Stored logits or the single pass: each chunk's forward splits the
+            # vocabulary to fill whole SM waves, so the fp32 sums run in a
+            # chunk-dependent order.
             assert (lp0 - lp1).abs().max().item() <= 1e-4
             assert abs(L0.item() - L1.item()) <= 1e-5 * abs(L0.item())

@@ -38,7 +38,8 @@ LOGP_TOL = 1e-2
 LOSS_RTOL = 1e-3
 DH_RTOL = 2e-2
 DEV = "cuda:0"
-STORED, RECOMPUTE = 1, 16  # GRPO_FLAG_STORED_LOGITS, GRPO_FLAG_RECOMPUTE_LOGITS
+# GRPO_FLAG_STORED_LOGITS, GRPO_FLAG_RECOMPUTE_LOGITS, GRPO_FLAG_SINGLE_PASS
+STORED, RECOMPUTE, SINGLE_PASS = 1, 16, 32
 
 
 @pytest.fixture(scope="module")
@@ -102,8 +103,9 @@ def _errors(out, want, mask):
 
 def _compare_forms(clp, p, want, old, ref, tag, with_dw=False, **kw):
     errs = {}
-    for name, flags in (("recompute", RECOMPUTE), ("stored", STORED)):
-        out, st = _gpu(clp, p, old, ref, flags, with_dw=with_dw, chunk_tokens=256, **kw)
+    for name, flags, extra in (("recompute", RECOMPUTE, {}), ("stored", STORED, {}),
+                               ("single_pass", SINGLE_PASS, {"vocab_block": 4096})):
+        out, st = _gpu(clp, p, old, ref, flags, with_dw=with_dw, chunk_tokens=256, **extra, **kw)
         assert st == 0, f"{tag} {name}: device status {st}"
         errs[name] = _errors(out, want, p.mask)
     print(f"{tag}: " + "; ".join(f"{k}: " + ", ".join(f"{a}={b:.3e}" for a, b in v.items()
@@ -115,9 +117,10 @@ def _compare_forms(clp, p, want, old, ref, tag, with_dw=False, **kw):
         assert e["rel_dH"] <= DH_RTOL, f"{tag} {name}: {e}"
         if with_dw:
             assert e["rel_dW"] <= DH_RTOL, f"{tag} {name}: {e}"
-    # Storing logits costs no accuracy beyond the bf16 rounding of G that both
-    # forms share (unshifted fp16 logits near 40 gave about 4x the error).
-    assert errs["stored"]["rel_dH"] <= 1.5 * errs["recompute"]["rel_dH"] + 1e-3, errs
+    # Storing logits costs no accuracy beyond the bf16 rounding of G (or P)
+    # that the forms share (unshifted fp16 logits near 40 gave about 4x the error).
+    for name in ("stored", "single_pass"):
+        assert errs[name]["rel_dH"] <= 1.5 * errs["recompute"]["rel_dH"] + 1e-3, errs
     return errs
 
 
@@ -149,7 +152,8 @@ def test_softcap_beyond_the_cap(clp, D):
                    logit_softcapping=30.0)
 
 
-@pytest.mark.parametrize("flags", [STORED, RECOMPUTE], ids=["stored", "recompute"])
+@pytest.mark.parametrize("flags", [STORED, RECOMPUTE, SINGLE_PASS],
+                         ids=["stored", "recompute", "single_pass"])
 def test_logits_beyond_fp16_range(clp, flags):
     # Logits of std ~2e4 (|z| well past fp16's 65504): the softmax is one-hot
     # on each row's top token. No inf or NaN may appear, and the results must
@@ -194,7 +198,7 @@ def test_nonfinite_inputs_set_status(clp):
                              clp.make_params(flags=STORED), dev)
     clp.grpo_logp_fwd(args[0], args[1], args[2], workspace=ws)
     assert clp.grpo_read_device_status(ws) == clp.GRPO_ERR_NONFINITE
-    for flags in (STORED, RECOMPUTE):
+    for flags in (STORED, RECOMPUTE, SINGLE_PASS):
         clp.grpo_loss_fwd_bwd(*args, p.seq_len, params=clp.make_params(flags=flags),
                               workspace=ws)
         assert clp.grpo_read_device_status(ws) == clp.GRPO_ERR_NONFINITE

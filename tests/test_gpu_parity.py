@@ -21,8 +21,9 @@ LOGP_TOL = 1e-2
 LOSS_RTOL = 1e-3
 DH_RTOL = 2e-2
 # Backward forms (grpo_params.flags): without either bit the call chooses.
-STORED = 1      # GRPO_FLAG_STORED_LOGITS
-RECOMPUTE = 16  # GRPO_FLAG_RECOMPUTE_LOGITS
+STORED = 1        # GRPO_FLAG_STORED_LOGITS
+RECOMPUTE = 16    # GRPO_FLAG_RECOMPUTE_LOGITS
+SINGLE_PASS = 32  # GRPO_FLAG_SINGLE_PASS
 
 
 @pytest.fixture(scope="module")
@@ -318,6 +319,88 @@ def test_stored_logits_padding_blocks(clp, chunk):
     check(got, want, p.mask, f"stored padding chunk={chunk}")
 
 
+# ------------------------------------------------ single-pass backward -----
+
+# vocab_block: the vocabulary in several blocks (their logits, partial slots
+# and the rescaled U accumulator), with a ragged last block.
+@pytest.mark.parametrize("N,T,D,V,chunk,vblock,padded", RAGGED)
+def test_single_pass_ragged(clp, N, T, D, V, chunk, vblock, padded):
+    G = 4 if (N // T) % 4 == 0 else 1
+    p = synth.make_problem("tiny", seed=N + D + V + 5, prompts=(N // T) // G, G=G, T=T, D=D,
+                           V=V, lengths=(max(1, T // 3), T) if padded else None)
+    old, ref, want = oracle_case(p)
+    params = clp.make_params(chunk_tokens=chunk, vocab_block=vblock, flags=SINGLE_PASS)
+    plan = clp.grpo_get_plan(p.n_tokens, D, V, T, params)
+    assert plan["single_pass"] == 1 and plan["stored_logits"] == 0
+    check(gpu_loss(clp, p, old, ref, params), want, p.mask,
+          f"single pass {N}x{D}x{V} ({plan['n_vocab_blocks']} blocks)")
+
+
+@pytest.mark.parametrize("vblock", [256, 768, 0])
+@pytest.mark.parametrize("kw", XFORMS)
+def test_single_pass_transforms(clp, kw, vblock):
+    # Logit std ~2.8 so that softcaps of 2-3 saturate; 12, 4 or 1 vocab blocks.
+    p = synth.make_problem("tiny", seed=33, T=75, prompts=1, G=4, D=200, V=3000,
+                           lengths=(20, 75), weight_std=0.2)
+    xf = oracle.Transform(scale_mul=kw.get("logit_scale_multiply", 1.0),
+                          scale_div=kw.get("logit_scale_divide", 1.0),
+                          softcap=kw.get("logit_softcapping", 0.0),
+                          temperature=kw.get("temperature", 1.0))
+    base, _ = oracle.selective_logp(p.hidden, p.weight, p.ids.numpy(), xf=xf)
+    old, ref = p.old_ref(torch.from_numpy(base))
+    want = oracle.loss_fwd_bwd(p.hidden, p.weight, p.ids.numpy(), p.mask.numpy(), old, ref,
+                               p.adv, p.seq_len, p.eps_low, p.eps_high, p.beta, xf=xf)
+    params = clp.make_params(chunk_tokens=128, vocab_block=vblock, flags=SINGLE_PASS, **kw)
+    check(gpu_loss(clp, p, old, ref, params), want, p.mask, f"single pass transform {kw}")
+
+
+@pytest.mark.parametrize("chunk", [256, 0])
+def test_single_pass_padding_blocks(clp, chunk):
+    p = synth.make_problem("tiny", seed=42 + chunk, prompts=2, G=4, T=512, D=256, V=3000,
+                           lengths=(1, 512))
+    old, ref, want = oracle_case(p)
+    params = clp.make_params(chunk_tokens=chunk, vocab_block=1024, flags=SINGLE_PASS)
+    ws = clp.alloc_workspace(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, params, DEV)
+    dH = torch.full((p.n_tokens, p.hidden_size), float("nan"), dtype=torch.bfloat16, device=DEV)
+    logp = torch.full((p.n_tokens,), float("nan"), device=DEV)
+    loss, logp, dH = clp.grpo_loss_fwd_bwd(
+        _to(p.hidden), _to(p.weight), _to(p.ids), _to(p.mask), _to(old), _to(ref), _to(p.adv),
+        p.seq_len, params=params, workspace=ws, dH=dH, logp=logp)
+    st = clp.grpo_read_device_status(ws)
+    got = (loss.item(), logp.cpu().double().numpy(), dH.cpu().double().numpy(), st)
+    check(got, want, p.mask, f"single pass padding chunk={chunk}")
+
+
+def test_three_backward_forms_agree(clp):
+    # Same inputs through the three forms: same forward values up to fp32
+    # summation order, dH within bf16 rounding of G (or P) of each other.
+    p = synth.make_problem("tiny", seed=53, T=500, prompts=1, G=4, D=320, V=5000,
+                           lengths=(100, 500))
+    old, ref, want = oracle_case(p)
+    runs = {f: gpu_loss(clp, p, old, ref, clp.make_params(chunk_tokens=512, vocab_block=1280,
+                                                          flags=f))
+            for f in (STORED, SINGLE_PASS, RECOMPUTE)}
+    for f, got in runs.items():
+        check(got, want, p.mask, f"form {f}")
+    L0, lp0, dH0, _ = runs[RECOMPUTE]
+    for f in (STORED, SINGLE_PASS):
+        L1, lp1, dH1, _ = runs[f]
+        assert np.abs(lp1 - lp0).max() <= 1e-5 and abs(L1 - L0) <= 1e-5 * abs(L0)
+        assert np.linalg.norm(dH1 - dH0) <= 1e-2 * np.linalg.norm(dH0)
+
+
+def test_single_pass_bad_id_and_all_masked(clp):
+    p = synth.make_problem("tiny", seed=17)
+    params = clp.make_params(flags=SINGLE_PASS, vocab_block=1024)
+    ids = p.ids.clone()
+    ids[9] = p.vocab + 5
+    old = torch.full((p.n_tokens,), -8.0)
+    L, logp, dH, st = gpu_loss(clp, p, old, old, params, ids=ids)
+    assert st == -8 and math.isnan(logp[9]) and math.isnan(L)
+    L, logp, dH, st = gpu_loss(clp, p, old, old, params, mask=torch.zeros_like(p.mask))
+    assert st == 0 and L == 0.0 and np.all(logp == 0) and np.all(dH == 0)
+
+
 def test_stored_and_recomputed_backward_agree(clp):
     p = synth.make_problem("tiny", seed=12, T=128, prompts=2, G=4, D=256, V=5000,
                            lengths=(30, 128))
@@ -396,7 +479,7 @@ def test_stored_logits_bad_id_and_all_masked(clp):
 SINGLE = 2  # GRPO_FLAG_SINGLE_CTA
 
 
-@pytest.mark.parametrize("flags", [SINGLE | RECOMPUTE, SINGLE | STORED])
+@pytest.mark.parametrize("flags", [SINGLE | RECOMPUTE, SINGLE | STORED, SINGLE | SINGLE_PASS])
 @pytest.mark.parametrize("N,T,D,V,chunk,vblock,padded", RAGGED[:4])
 def test_single_cta_gemms(clp, flags, N, T, D, V, chunk, vblock, padded):
     G = 4 if (N // T) % 4 == 0 else 1
@@ -411,7 +494,7 @@ def test_pair_and_single_cta_agree(clp):
     # Odd number of 128-row blocks: the last CTA pair has one real row block.
     p = synth.make_problem("tiny", seed=14, T=640, prompts=1, G=1, D=256, V=3000)
     old, ref, _ = oracle_case(p)
-    for extra in (RECOMPUTE, STORED):
+    for extra in (RECOMPUTE, STORED, SINGLE_PASS):
         L1, lp1, dH1, s1 = gpu_loss(clp, p, old, ref, clp.make_params(flags=extra))
         L2, lp2, dH2, s2 = gpu_loss(clp, p, old, ref, clp.make_params(flags=extra | SINGLE))
         assert s1 == 0 and s2 == 0
@@ -426,7 +509,8 @@ FITFREE = 8  # GRPO_FLAG_FIT_FREE_MEMORY
 
 
 @pytest.mark.parametrize("flags", [SEQMEAN | RECOMPUTE, SEQMEAN | STORED,
-                                   SEQMEAN | SINGLE | RECOMPUTE, SEQMEAN])
+                                   SEQMEAN | SINGLE | RECOMPUTE, SEQMEAN,
+                                   SEQMEAN | SINGLE_PASS])
 def test_sequence_mean_aggregation(clp, flags):
     p = synth.make_problem("tiny", seed=60, T=100, prompts=2, G=4, D=256, V=3000,
                            lengths=(5, 100))
@@ -442,7 +526,8 @@ def test_sequence_mean_aggregation(clp, flags):
 
 @pytest.mark.parametrize("flags,limit", [(FITFREE, 0), (STORED | FITFREE, 0),
                                          (STORED, 24 << 20), (RECOMPUTE, 24 << 20),
-                                         (RECOMPUTE | FITFREE, 0), (0, 24 << 20)])
+                                         (RECOMPUTE | FITFREE, 0), (0, 24 << 20),
+                                         (SINGLE_PASS, 24 << 20), (SINGLE_PASS | FITFREE, 0)])
 def test_workspace_budget_plans_give_same_results(clp, flags, limit):
     p = synth.make_problem("tiny", seed=61, T=512, prompts=2, G=4, D=512, V=6000,
                            lengths=(100, 512))
@@ -466,6 +551,8 @@ DW_CASES = [
     (300, 75, 200, 1000, 128, 512, True, SINGLE | STORED),
     (4096, 512, 256, 3000, 256, 1024, True, STORED),   # many skipped blocks, empty chunks
     (4096, 512, 256, 3000, 256, 1024, True, RECOMPUTE),
+    # dW with the single pass: the call recomputes the logit tiles instead.
+    (300, 75, 200, 1000, 128, 512, True, SINGLE_PASS),
 ]
 
 
@@ -571,7 +658,7 @@ def test_concurrent_calls_from_two_threads(clp):
         assert torch.equal(l0, l1) and torch.equal(lp0, lp1) and torch.equal(d0, d1)
 
 
-@pytest.mark.parametrize("flags", [RECOMPUTE, STORED])
+@pytest.mark.parametrize("flags", [RECOMPUTE, STORED, SINGLE_PASS])
 def test_device_memory_is_the_workspace_only(clp, flags):
     # The memory claim ("GRPO with 7x longer context", section "Flattened
     # sequence length chunking", Eq. 1-3): at a fixed chunk the memory a call
@@ -619,7 +706,7 @@ def test_device_memory_is_the_workspace_only(clp, flags):
 # V = 7 (a stored row narrower than one 16-byte chunk), V = 65 (one column
 # past a 64-wide K slice); D = 256 forms G in the dH GEMM, D = 2304 in its own
 # pass; RECOMPUTE is the recomputed backward.
-@pytest.mark.parametrize("flags", [RECOMPUTE, STORED])
+@pytest.mark.parametrize("flags", [RECOMPUTE, STORED, SINGLE_PASS])
 @pytest.mark.parametrize("D", [256, 2304])
 @pytest.mark.parametrize("V", [1, 7, 65])
 def test_small_vocab_edges(clp, flags, D, V):
@@ -645,7 +732,8 @@ def test_empty_batch_stored(clp, flags):
 # Smallest legal shapes: hidden sizes far below one 64-wide K slice (D = 8,
 # 24), a single token, and D = 2056 (just past the size up to which G is
 # formed in the dH GEMM, and not a multiple of 64); every backward form.
-@pytest.mark.parametrize("flags", [RECOMPUTE, STORED, STORED | SINGLE])
+@pytest.mark.parametrize("flags", [RECOMPUTE, STORED, STORED | SINGLE, SINGLE_PASS,
+                                   SINGLE_PASS | SINGLE])
 @pytest.mark.parametrize("N,D", [(1, 8), (3, 24), (130, 8), (70, 2056)])
 def test_tiny_hidden_and_single_token(clp, flags, N, D):
     p = synth.make_problem("tiny", seed=N * 31 + D, prompts=1, G=1, T=N, D=D, V=300,
@@ -668,7 +756,8 @@ def _guarded(n, dtype, fill, guard):
 # every output is a view inside a buffer of sentinels, and the workspace is
 # prefilled with 0xFF bytes (NaN in every float format) inside its own guard
 # band. Results must still match the oracle and every sentinel must survive.
-@pytest.mark.parametrize("flags", [RECOMPUTE, STORED, STORED | SINGLE])
+@pytest.mark.parametrize("flags", [RECOMPUTE, STORED, STORED | SINGLE, SINGLE_PASS,
+                                   SINGLE_PASS | SINGLE])
 @pytest.mark.parametrize("D", [256, 2304])
 @pytest.mark.parametrize("with_dw", [False, True])
 def test_guard_bands_and_poisoned_workspace(clp, flags, D, with_dw):
