@@ -324,6 +324,11 @@ _NCU_SCALE = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e
               "ns": 1e-6, "nsecond": 1e-6, "us": 1e-3, "usecond": 1e-3, "ms": 1.0,
               "msecond": 1.0, "s": 1e3, "second": 1e3}
 _FIRST_KERNEL = "row_plan_kernel"  # every grpo_loss_fwd_bwd call starts with it
+# The library's kernels (any other launch in a capture is torch's own).
+LIBRARY_KERNELS = ("tc_gemm_kernel", "finalize_kernel", "finalize_gform_kernel",
+                   "finalize_rows_kernel", "finish_loss_kernel", "row_plan_kernel",
+                   "zero_padding_blocks_kernel", "seq_lens_kernel",
+                   "bounded_wait_selftest_kernel")
 
 
 def ncu_launches(csv_path):
@@ -348,10 +353,12 @@ def ncu_launches(csv_path):
     seq = []
     for i in sorted(launches):
         d = launches[i]
-        if "grpo::" not in d["name"]:
-            continue
+        # ncu prints "void grpo::tc_gemm_kernel<(int)3, (int)2>(...)" or, with
+        # other name bases, "void tc_gemm_kernel<3, 2>(...)".
         name = d["name"].replace("(int)", "").split("(")[0]
         name = name.replace("void ", "").replace("grpo::", "").strip()
+        if name.split("<")[0] not in LIBRARY_KERNELS:
+            continue
         seq.append({"name": name, "read": d.get("dram__bytes_read.sum", 0.0),
                     "write": d.get("dram__bytes_write.sum", 0.0),
                     "ms": d.get("gpu__time_duration.sum", 0.0)})
@@ -371,11 +378,13 @@ def ncu_calls(csv_path):
 def record_traffic(csv_path, workload, backward, command):
     """Write the DRAM record of an ncu capture: of the last complete call in a
     launch list, or, when the capture holds no whole call (one kernel, a few
-    launches, -k/-c), of each captured kernel per launch. The bench reads the
-    dominant kernel's bytes per launch from either."""
-    calls = ncu_calls(csv_path)
+    launches, -k/-c; several such captures may be given, comma-separated), of
+    each captured kernel per launch. The bench reads the dominant kernel's
+    bytes per launch from either."""
+    paths = csv_path.split(",")
+    calls = ncu_calls(paths[0]) if len(paths) == 1 else []
     if not calls:
-        seq = ncu_launches(csv_path)
+        seq = [d for pth in paths for d in ncu_launches(pth)]
         if not seq:
             raise SystemExit(f"{csv_path}: no launch of the library")
         per = {}

@@ -63,8 +63,38 @@ struct NvtxRange {
 };
 long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
-// D columns per dH unit, in units of 256: the pair kernel covers 512.
-int dh_accumulators(int ctas) { return ctas == 2 ? 2 : 1; }
+// Hidden columns per accumulator of the dH-type GEMMs. A CTA pair's unit
+// holds two accumulators (TMEM's 512 columns); 256 wide each unless a
+// narrower width (a multiple of 16, down to 192) tiles the hidden size with
+// less padding: D = 2880 takes 6 units of 2 x 240 instead of 6 of 2 x 256,
+// one of them filled to 62.5 %. A single CTA's unit is one 256-wide
+// accumulator.
+int dh_acc_width(int hidden, int ctas) {
+  if (ctas != 2) return BN;
+  // MMA columns issued over the hidden size with accumulators of width w: a
+  // ragged accumulator runs in whole 128-column steps, one wholly past the
+  // hidden size not at all.
+  auto issued = [hidden](int w) {
+    long long cols = 0;
+    for (int c0 = 0; c0 < hidden; c0 += w) cols += std::min(w, (hidden - c0 + 127) / 128 * 128);
+    return cols;
+  };
+  int best = BN;
+  long long best_cols = issued(BN);
+  for (int w = BN - 16; w >= 192; w -= 16) {
+    const long long cols = issued(w);
+    if (cols < best_cols) {
+      best_cols = cols;
+      best = w;
+    }
+  }
+  return best;
+}
+
+// Hidden-dimension units of a dH-type launch.
+int dh_tiles(int hidden, int ctas) {
+  return static_cast<int>(cdiv(hidden, ctas == 2 ? 2 * dh_acc_width(hidden, 2) : BN));
+}
 
 // Backward forms (grpo_params.flags, or the automatic choice).
 enum Form { kFormRecompute = 0, kFormStored = 1, kFormSinglePass = 2 };
@@ -74,6 +104,7 @@ struct Layout {
   bool stored;      // stored-logit backward (GRPO_FLAG_STORED_LOGITS)
   bool single_pass; // single-pass backward (GRPO_FLAG_SINGLE_PASS)
   int nvb;          // single pass: vocab blocks (each one logit GEMM + one U GEMM)
+  int acc_w;        // hidden columns per accumulator of the dH-type GEMMs
   long long ldS;    // stored mode: elements per row of the chunk logit block
   long long n, nr;  // rows, rows rounded up to BM
   int T, D, V;
@@ -305,7 +336,8 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, Form fo
   L->V = s->vocab;
   L->nvt = static_cast<int>(cdiv(s->vocab, BN));
   L->ctas = (p != nullptr && (p->flags & GRPO_FLAG_SINGLE_CTA) != 0) ? 1 : 2;
-  const int n_dt = static_cast<int>(cdiv(s->hidden, BN * dh_accumulators(L->ctas)));
+  const int n_dt = dh_tiles(s->hidden, L->ctas);
+  L->acc_w = dh_acc_width(s->hidden, L->ctas);
   long long vb = (p && p->vocab_block > 0) ? p->vocab_block : kAutoVocabBlock;
   if (L->single_pass) {
     // Equal blocks (the automatic size split evenly), at most kMaxSplits of
@@ -743,7 +775,7 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
       !encode_2d(&map_w_k, W, L.D, L.V, L.D, BK, BN / L.ctas) ||
       !encode_2d(&map_w_mn, W, L.D, L.V, L.D, 64, BK))
     return GRPO_ERR_CUDA;
-  const int n_dt_dh = static_cast<int>(cdiv(L.D, BN * dh_accumulators(L.ctas)));
+  const int n_dt_dh = dh_tiles(L.D, L.ctas);
   const int n_rb_total = static_cast<int>(L.nr / BM);
   const int rb_per_chunk = L.chunk_rows / BM;
   for (int rb0 = 0; rb0 < n_rb_total; rb0 += rb_per_chunk) {
@@ -795,6 +827,7 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
       b.v0 = static_cast<int>(v0);
       b.acc = w.acc;
       b.dH = static_cast<__nv_bfloat16*>(dH);
+      b.acc_w = L.acc_w;
       b.first = v0 == 0;
       b.last = v0 + L.vblock >= L.V;
       units = static_cast<long long>(n_ru) * n_dt_dh;
@@ -833,7 +866,7 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
   DeviceInfo* di = current_device_info();
   if (di == nullptr) return GRPO_ERR_CUDA;
   const bool overlap = L.n_sbuf == 2;
-  const int n_dt_dh = static_cast<int>(cdiv(L.D, BN * dh_accumulators(L.ctas)));
+  const int n_dt_dh = dh_tiles(L.D, L.ctas);
   const int n_rb_total = static_cast<int>(L.nr / BM);
   const int rb_per_chunk = L.chunk_rows / BM;
   const int n_chunks = static_cast<int>(cdiv(n_rb_total, rb_per_chunk));
@@ -963,6 +996,7 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     b.n_cols = n_dt_dh;
     b.v0 = 0;
     b.dH = static_cast<__nv_bfloat16*>(dH);
+    b.acc_w = L.acc_w;
     b.first = 1;
     b.last = 1;
     const long long units = static_cast<long long>(n_ru) * n_dt_dh;
@@ -1002,6 +1036,7 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     b.box_max = bmax(c);
     b.ldM = L.chunk_rows;
     b.dH = static_cast<__nv_bfloat16*>(dH);
+    b.acc_w = L.acc_w;
     b.first = 1;
     b.last = 1;
     const long long units = static_cast<long long>(n_ru) * n_dt_dh;
@@ -1090,7 +1125,7 @@ int run_single_pass(const void* hidden, const void* W, const int32_t* ids, const
       !encode_2d(&map_w_k, W, L.D, L.V, L.D, BK, BN / L.ctas) ||
       !encode_2d(&map_w_mn, W, L.D, L.V, L.D, 64, BK))
     return GRPO_ERR_CUDA;
-  const int n_dt_dh = static_cast<int>(cdiv(L.D, BN * dh_accumulators(L.ctas)));
+  const int n_dt_dh = dh_tiles(L.D, L.ctas);
   const int n_rb_total = static_cast<int>(L.nr / BM);
   const int rb_per_chunk = L.chunk_rows / BM;
   uint16_t* const S = reinterpret_cast<uint16_t*>(w.G);
@@ -1203,6 +1238,7 @@ int run_single_pass(const void* hidden, const void* W, const int32_t* ids, const
       u.ldM = L.chunk_rows;
       u.acc = w.acc;
       u.dH = static_cast<__nv_bfloat16*>(dH);
+      u.acc_w = L.acc_w;
       u.first = b == 0;
       u.last = last;
       if (launch_uac_gemm(L.ctas, map_s, map_w_mn, u,

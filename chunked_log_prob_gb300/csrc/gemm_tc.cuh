@@ -110,6 +110,9 @@ struct TileArgs {
   float* dW;             // [V][hidden] fp32 output / accumulator
   int dw_rows;           // vocab rows of dW this launch covers (from v0)
   // MODE_DH, MODE_DHS, MODE_UAC
+  int acc_w;             // CTA pairs: hidden columns per accumulator (a multiple of 16,
+                         // <= 256); a unit covers two. Narrower than 256 when that
+                         // tiles the hidden size with less padding (2880 = 6 x 480)
   float* acc;            // [local rows][hidden] fp32 accumulator
   __nv_bfloat16* dH;     // [N][hidden] output, indexed by global row
   int first;
@@ -340,15 +343,23 @@ struct PairCfg {
   static constexpr int kThreads = 64 + 128 * kCvtGroups;
 };
 
-// MODE_DH/DHS/DW (output columns = hidden): the MMA width of accumulator na
-// of tile t, i.e. its columns inside the hidden size in whole 64-column MN
-// blocks of every CTA's share; 0 when the accumulator lies wholly past it.
-// A ragged last tile thus runs narrower MMAs and loads fewer B boxes.
+// Hidden columns per accumulator: the launch's acc_w for the dH modes on CTA
+// pairs, BN otherwise.
+template <int MODE, int CTAS>
+__device__ __forceinline__ int acc_cols(const TileArgs& a) {
+  return (is_dh(MODE) && CTAS == 2) ? a.acc_w : BN;
+}
+
+// MODE_DH/DHS/UAC/DW (output columns = hidden): the MMA width of an
+// accumulator of aw columns starting at hidden column col0, i.e. its columns
+// inside the hidden size, in whole 64-column MN blocks of every CTA's share
+// when it is ragged; 0 when it lies wholly past the hidden size. A ragged
+// last tile thus runs narrower MMAs and loads fewer B boxes.
 template <int CTAS>
-__device__ __forceinline__ int mn_out_cols(const TileArgs& a, int col0) {
+__device__ __forceinline__ int mn_out_cols(const TileArgs& a, int col0, int aw) {
   const int w = a.hidden - col0;
   constexpr int q = 64 * CTAS;
-  return w <= 0 ? 0 : min(BN, (w + q - 1) / q * q);
+  return w <= 0 ? 0 : min(aw, (w + q - 1) / q * q);
 }
 
 // One TMA box into this CTA's stage; its bytes are counted on the leader's
@@ -462,13 +473,17 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             MODE == MODE_DW ? 0 : (is_dh(MODE) ? li : global_rb(args, li)) * BM;
         const int a_m0 = (ru * CTAS + static_cast<int>(rank)) * BM;  // MODE_DW: vocab row
         for (int t = t0; t < t1 && ok; ++t) {
-          // MN-major B (DH, DHS, DW): 64-column boxes per accumulator in this
-          // CTA, and their bytes.
-          int nbox[C::kNAcc];
+          // MN-major B (DH, DHS, UAC, DW): this CTA's share of each
+          // accumulator's columns (ncol, from column offset rank * ncol), in
+          // 64-column boxes (the last one may reach into the next share:
+          // loaded, not used), and their bytes.
+          const int aw = acc_cols<MODE, CTAS>(args);
+          int nbox[C::kNAcc], ncol[C::kNAcc];
           uint32_t b_bytes = 0;
 #pragma unroll
           for (int na = 0; na < C::kNAcc; ++na) {
-            nbox[na] = mn_out_cols<CTAS>(args, t * C::kTileN + na * BN) / (64 * CTAS);
+            ncol[na] = mn_out_cols<CTAS>(args, t * C::kNAcc * aw + na * aw, aw) / CTAS;
+            nbox[na] = (ncol[na] + 63) / 64;
             b_bytes += static_cast<uint32_t>(nbox[na]) * (BK * 64 * 2);
           }
           for (int k = 0; k < k_iters; ++k, ++it) {
@@ -495,7 +510,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
                 for (int jb = 0; jb < nbox[na]; ++jb)
                   load_box<CTAS>(b_dst + na * (C::kBRows * BK * 2) + jb * (BK * 64 * 2), &map_b,
                                  &full_bar[s], lead,
-                                 t * C::kTileN + na * BN + static_cast<int>(rank) * nbox[na] * 64 +
+                                 t * C::kNAcc * aw + na * aw + static_cast<int>(rank) * ncol[na] +
                                      jb * 64,
                                  args.v0 + k * BK, false, 0);
             } else if (MODE == MODE_DW) {
@@ -534,7 +549,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
                   for (int jb = 0; jb < nbox[na]; ++jb)
                     tma_load_2d_pair_nohint(
                         b_dst + na * (C::kBRows * BK * 2) + jb * (BK * 64 * 2), &map_b, lead,
-                        t * C::kTileN + na * BN + static_cast<int>(rank) * nbox[na] * 64 +
+                        t * C::kNAcc * aw + na * aw + static_cast<int>(rank) * ncol[na] +
                             jb * 64,
                         args.v0 + k * BK);
               } else {
@@ -599,7 +614,8 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
           uint32_t idesc[C::kNAcc];
 #pragma unroll
           for (int na = 0; na < C::kNAcc; ++na) {
-            const int n = kMnOut ? mn_out_cols<CTAS>(args, t * C::kTileN + na * BN) : BN;
+            const int aw = acc_cols<MODE, CTAS>(args);
+            const int n = kMnOut ? mn_out_cols<CTAS>(args, t * C::kNAcc * aw + na * aw, aw) : BN;
             idesc[na] = n == 0 ? 0u : idesc_bf16(BM * CTAS, n, MODE == MODE_DW, kMnOut);
           }
           for (int k = 0; k < k_iters; ++k, ++it) {
@@ -758,35 +774,45 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
       if constexpr (has_cvt(MODE)) {
         // Every A stage of this unit, as it lands: fp16 logits -> bf16 in
         // place (this thread's part of its row), then tell the MMA issuer.
-        // Stage k is box k of the stored block; its maximum is loaded kPre
-        // stages ahead (rows that contribute nothing need none).
+        // Stage k is box k of the stored block. The box maxima of the next
+        // kPre stages are loaded at the start of each group of kPre stages,
+        // into registers that no instruction touches until the group after
+        // (a register move of a load in flight would wait for it); rows that
+        // contribute nothing need none.
         constexpr int kPre = 4;
         const float* bm = args.box_max + lrow;
-        float zq[kPre];
+        auto box_max_of = [&](int k) {
+          return (!rc.zero && k < k_iters) ? __ldg(bm + static_cast<long long>(k) * args.ldM)
+                                           : 0.f;
+        };
+        float zc[kPre], zn[kPre];
 #pragma unroll
-        for (int j = 0; j < kPre; ++j)
-          zq[j] = (!rc.zero && j < k_iters) ? __ldg(bm + j * args.ldM) : 0.f;
-        for (int k = 0; k < k_iters; ++k, ++cit) {
-          const float zoff = zq[0];
+        for (int j = 0; j < kPre; ++j) zc[j] = box_max_of(j);
+        for (int k0 = 0; k0 < k_iters && ok; k0 += kPre) {
 #pragma unroll
-          for (int j = 0; j + 1 < kPre; ++j) zq[j] = zq[j + 1];
-          zq[kPre - 1] = (!rc.zero && k + kPre < k_iters)
-                             ? __ldg(bm + static_cast<long long>(k + kPre) * args.ldM)
-                             : 0.f;
-          const int s = static_cast<int>(cit % kStages);
-          if (!mbar_wait(&afull_bar[s], (cit / kStages) & 1u, abort_flag, args.status)) {
-            ok = false;
-            break;
+          for (int j = 0; j < kPre; ++j) zn[j] = box_max_of(k0 + kPre + j);
+#pragma unroll
+          for (int j = 0; j < kPre; ++j) {
+            const int k = k0 + j;
+            if (k >= k_iters || !ok) break;
+            const int s = static_cast<int>(cit % kStages);
+            if (!mbar_wait(&afull_bar[s], (cit / kStages) & 1u, abort_flag, args.status)) {
+              ok = false;
+              break;
+            }
+            constexpr int kNch = 8 / C::kCvtGroups;
+            stage_row_to_bf16<kNch>(args, smem + s * C::kStageBytes, lrow_in_tile, part * kNch,
+                                    args.v0 + k * BK, rc, zc[j]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (CTAS == 2) mbar_arrive_cluster(cvt_addr0 + static_cast<uint32_t>(s) * 8u);
+              else mbar_arrive(&cvt_bar[s]);
+            }
+            ++cit;
           }
-          constexpr int kNch = 8 / C::kCvtGroups;
-          stage_row_to_bf16<kNch>(args, smem + s * C::kStageBytes, lrow_in_tile, part * kNch,
-                                  args.v0 + k * BK, rc, zoff);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            if (CTAS == 2) mbar_arrive_cluster(cvt_addr0 + static_cast<uint32_t>(s) * 8u);
-            else mbar_arrive(&cvt_bar[s]);
-          }
+#pragma unroll
+          for (int j = 0; j < kPre; ++j) zc[j] = zn[j];
         }
         if (!ok) break;
         if (part != 0) continue;  // converter-only warps: no epilogue
@@ -1111,9 +1137,13 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
         } else if (MODE == MODE_UAC) {
           // U (+)= this block's P W, rescaled to the running maximum; on the
           // last block dH = g (1 - p_y) f'_y W_y - g 2^(M - lse2) U.
+          const int aw = acc_cols<MODE, CTAS>(args);
 #pragma unroll 1
           for (int c = 0; c < C::kTileN / 32; ++c) {
-            const int d0 = t * C::kTileN + c * 32;
+            // TMEM columns c*32.. hold accumulator c / 8, its columns (c % 8)*32..
+            const int cc = (c & 7) * 32;
+            if (cc >= aw) continue;  // past this accumulator's width (warp-uniform)
+            const int d0 = t * C::kNAcc * aw + (c >> 3) * aw + cc;
             if (d0 >= args.hidden) break;  // warp-uniform
             float v[32];
             tmem_ld32(tbase + c * 32, v);
@@ -1124,7 +1154,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
                   args.W + static_cast<long long>(rc.y < 0 ? 0 : rc.y) * args.hidden + d0;
 #pragma unroll
               for (int j8 = 0; j8 < 4; ++j8) {
-                if (d0 + j8 * 8 >= args.hidden) break;
+                if (d0 + j8 * 8 >= args.hidden || cc + j8 * 8 >= aw) break;
                 float* x = v + j8 * 8;
                 if (rc.zero) {
 #pragma unroll
@@ -1162,9 +1192,14 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             }
           }
         } else {  // MODE_DH
+          const int aw = acc_cols<MODE, CTAS>(args);
 #pragma unroll 1
           for (int c = 0; c < C::kTileN / 32; ++c) {
-            const int d0 = t * C::kTileN + c * 32;
+            // TMEM columns c*32.. hold accumulator c / 8 (c / 8 = 0 on single
+            // CTAs), its columns (c % 8)*32..
+            const int cc = (c & 7) * 32;
+            if (cc >= aw) continue;  // past this accumulator's width (warp-uniform)
+            const int d0 = t * C::kNAcc * aw + (c >> 3) * aw + cc;
             if (d0 >= args.hidden) break;  // warp-uniform
             float v[32];
             tmem_ld32(tbase + c * 32, v);
@@ -1174,7 +1209,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
                   args.dH + static_cast<long long>(grow) * args.hidden + d0;
 #pragma unroll
               for (int j8 = 0; j8 < 4; ++j8) {
-                if (d0 + j8 * 8 >= args.hidden) break;
+                if (d0 + j8 * 8 >= args.hidden || cc + j8 * 8 >= aw) break;
                 float* a8 = accp + j8 * 8;
                 if (!args.first) {
                   const float4 x0 = *reinterpret_cast<const float4*>(a8);
