@@ -63,37 +63,13 @@ struct NvtxRange {
 };
 long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
-// Hidden columns per accumulator of the dH-type GEMMs. A CTA pair's unit
-// holds two accumulators (TMEM's 512 columns); 256 wide each unless a
-// narrower width (a multiple of 16, down to 192) tiles the hidden size with
-// less padding: D = 2880 takes 6 units of 2 x 240 instead of 6 of 2 x 256,
-// one of them filled to 62.5 %. A single CTA's unit is one 256-wide
-// accumulator.
-int dh_acc_width(int hidden, int ctas) {
-  if (ctas != 2) return BN;
-  // MMA columns issued over the hidden size with accumulators of width w: a
-  // ragged accumulator runs in whole 128-column steps, one wholly past the
-  // hidden size not at all.
-  auto issued = [hidden](int w) {
-    long long cols = 0;
-    for (int c0 = 0; c0 < hidden; c0 += w) cols += std::min(w, (hidden - c0 + 127) / 128 * 128);
-    return cols;
-  };
-  int best = BN;
-  long long best_cols = issued(BN);
-  for (int w = BN - 16; w >= 192; w -= 16) {
-    const long long cols = issued(w);
-    if (cols < best_cols) {
-      best_cols = cols;
-      best = w;
-    }
-  }
-  return best;
-}
+// D columns per dH unit, in units of 256: the pair kernel covers 512 (two
+// 256-column accumulators, TMEM's 512 columns).
+int dh_accumulators(int ctas) { return ctas == 2 ? 2 : 1; }
 
 // Hidden-dimension units of a dH-type launch.
 int dh_tiles(int hidden, int ctas) {
-  return static_cast<int>(cdiv(hidden, ctas == 2 ? 2 * dh_acc_width(hidden, 2) : BN));
+  return static_cast<int>(cdiv(hidden, BN * dh_accumulators(ctas)));
 }
 
 // Backward forms (grpo_params.flags, or the automatic choice).
@@ -104,7 +80,6 @@ struct Layout {
   bool stored;      // stored-logit backward (GRPO_FLAG_STORED_LOGITS)
   bool single_pass; // single-pass backward (GRPO_FLAG_SINGLE_PASS)
   int nvb;          // single pass: vocab blocks (each one logit GEMM + one U GEMM)
-  int acc_w;        // hidden columns per accumulator of the dH-type GEMMs
   long long ldS;    // stored mode: elements per row of the chunk logit block
   long long n, nr;  // rows, rows rounded up to BM
   int T, D, V;
@@ -337,7 +312,6 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, Form fo
   L->nvt = static_cast<int>(cdiv(s->vocab, BN));
   L->ctas = (p != nullptr && (p->flags & GRPO_FLAG_SINGLE_CTA) != 0) ? 1 : 2;
   const int n_dt = dh_tiles(s->hidden, L->ctas);
-  L->acc_w = dh_acc_width(s->hidden, L->ctas);
   long long vb = (p && p->vocab_block > 0) ? p->vocab_block : kAutoVocabBlock;
   if (L->single_pass) {
     // Equal blocks (the automatic size split evenly), at most kMaxSplits of
@@ -827,7 +801,6 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
       b.v0 = static_cast<int>(v0);
       b.acc = w.acc;
       b.dH = static_cast<__nv_bfloat16*>(dH);
-      b.acc_w = L.acc_w;
       b.first = v0 == 0;
       b.last = v0 + L.vblock >= L.V;
       units = static_cast<long long>(n_ru) * n_dt_dh;
@@ -996,7 +969,6 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     b.n_cols = n_dt_dh;
     b.v0 = 0;
     b.dH = static_cast<__nv_bfloat16*>(dH);
-    b.acc_w = L.acc_w;
     b.first = 1;
     b.last = 1;
     const long long units = static_cast<long long>(n_ru) * n_dt_dh;
@@ -1036,7 +1008,6 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     b.box_max = bmax(c);
     b.ldM = L.chunk_rows;
     b.dH = static_cast<__nv_bfloat16*>(dH);
-    b.acc_w = L.acc_w;
     b.first = 1;
     b.last = 1;
     const long long units = static_cast<long long>(n_ru) * n_dt_dh;
@@ -1238,7 +1209,6 @@ int run_single_pass(const void* hidden, const void* W, const int32_t* ids, const
       u.ldM = L.chunk_rows;
       u.acc = w.acc;
       u.dH = static_cast<__nv_bfloat16*>(dH);
-      u.acc_w = L.acc_w;
       u.first = b == 0;
       u.last = last;
       if (launch_uac_gemm(L.ctas, map_s, map_w_mn, u,

@@ -110,9 +110,6 @@ struct TileArgs {
   float* dW;             // [V][hidden] fp32 output / accumulator
   int dw_rows;           // vocab rows of dW this launch covers (from v0)
   // MODE_DH, MODE_DHS, MODE_UAC
-  int acc_w;             // CTA pairs: hidden columns per accumulator (a multiple of 16,
-                         // <= 256); a unit covers two. Narrower than 256 when that
-                         // tiles the hidden size with less padding (2880 = 6 x 480)
   float* acc;            // [local rows][hidden] fp32 accumulator
   __nv_bfloat16* dH;     // [N][hidden] output, indexed by global row
   int first;
@@ -197,22 +194,6 @@ __device__ __forceinline__ int swz_offset(int r, int c) {
   return r * 128 + ((((c >> 3) ^ r) & 7) << 4) + (c & 7) * 2;
 }
 
-// Two stored fp16 values of a box-shifted row (both <= 0) as fp32 magnitudes
-// scaled by 2^-112: the sign bits are dropped, and the exponent and mantissa
-// fields move to their fp32 positions, where fp16's exponent bias (15) reads
-// as fp32's (127) less 112. Exact for every finite fp16, subnormals included
-// (an fp16 subnormal lands on the fp32 subnormal of the same scaled value).
-// Integer shifts and masks instead of two conversions on the pipe that also
-// runs the exponentials.
-__device__ __forceinline__ void f16x2_nonpos_magnitudes(uint32_t w, float& lo, float& hi) {
-  lo = __uint_as_float((w << 13) & 0x0FFFE000u);
-  hi = __uint_as_float((w >> 3) & 0x0FFFE000u);
-}
-// -log2(e) 2^112: with f16x2_nonpos_magnitudes, fmaf(m, kNegLog2eScaled, c)
-// equals fmaf(z, log2e, c) for the stored value z = -m 2^112, bit for bit
-// (scaling by a power of two is exact).
-constexpr float kNegLog2eScaled = -kLog2e * 5192296858534827628530496329220096.0f;
-
 // Per-row constants of the in-GEMM conversion of stored logits (MODE_DHS,
 // MODE_UAC). A stored value s of column v is z'_v - zoff, zoff the maximum of
 // the column's 64-column box (one pipeline stage), and becomes the bf16
@@ -260,10 +241,9 @@ __device__ __forceinline__ void stage_row_to_bf16(const TileArgs& a, uint8_t* ti
       uint32_t o[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        float m0, m1;
-        f16x2_nonpos_magnitudes(w[e], m0, m1);
-        o[e] = pack_bf16x2(ex2(fmaf(m0, kNegLog2eScaled, c)), ex2(fmaf(m1, kNegLog2eScaled, c))) ^
-               rc.sgn;
+        float z0, z1;
+        unpack_f16x2(w[e], z0, z1);
+        o[e] = pack_bf16x2(ex2(fmaf(z0, kLog2e, c)), ex2(fmaf(z1, kLog2e, c))) ^ rc.sgn;
       }
       row[(jb + j) ^ sw] = make_uint4(o[0], o[1], o[2], o[3]);
     }
@@ -343,23 +323,16 @@ struct PairCfg {
   static constexpr int kThreads = 64 + 128 * kCvtGroups;
 };
 
-// Hidden columns per accumulator: the launch's acc_w for the dH modes on CTA
-// pairs, BN otherwise.
-template <int MODE, int CTAS>
-__device__ __forceinline__ int acc_cols(const TileArgs& a) {
-  return (is_dh(MODE) && CTAS == 2) ? a.acc_w : BN;
-}
-
-// MODE_DH/DHS/UAC/DW (output columns = hidden): the MMA width of an
-// accumulator of aw columns starting at hidden column col0, i.e. its columns
-// inside the hidden size, in whole 64-column MN blocks of every CTA's share
-// when it is ragged; 0 when it lies wholly past the hidden size. A ragged
-// last tile thus runs narrower MMAs and loads fewer B boxes.
+// MODE_DH/DHS/UAC/DW (output columns = hidden): the MMA width of the
+// accumulator starting at hidden column col0, i.e. its columns inside the
+// hidden size in whole 64-column MN blocks of every CTA's share; 0 when the
+// accumulator lies wholly past it. A ragged last tile thus runs narrower MMAs
+// and loads fewer B boxes.
 template <int CTAS>
-__device__ __forceinline__ int mn_out_cols(const TileArgs& a, int col0, int aw) {
+__device__ __forceinline__ int mn_out_cols(const TileArgs& a, int col0) {
   const int w = a.hidden - col0;
   constexpr int q = 64 * CTAS;
-  return w <= 0 ? 0 : min(aw, (w + q - 1) / q * q);
+  return w <= 0 ? 0 : min(BN, (w + q - 1) / q * q);
 }
 
 // One TMA box into this CTA's stage; its bytes are counted on the leader's
@@ -473,17 +446,13 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             MODE == MODE_DW ? 0 : (is_dh(MODE) ? li : global_rb(args, li)) * BM;
         const int a_m0 = (ru * CTAS + static_cast<int>(rank)) * BM;  // MODE_DW: vocab row
         for (int t = t0; t < t1 && ok; ++t) {
-          // MN-major B (DH, DHS, UAC, DW): this CTA's share of each
-          // accumulator's columns (ncol, from column offset rank * ncol), in
-          // 64-column boxes (the last one may reach into the next share:
-          // loaded, not used), and their bytes.
-          const int aw = acc_cols<MODE, CTAS>(args);
-          int nbox[C::kNAcc], ncol[C::kNAcc];
+          // MN-major B (DH, DHS, UAC, DW): 64-column boxes per accumulator in
+          // this CTA, and their bytes.
+          int nbox[C::kNAcc];
           uint32_t b_bytes = 0;
 #pragma unroll
           for (int na = 0; na < C::kNAcc; ++na) {
-            ncol[na] = mn_out_cols<CTAS>(args, t * C::kNAcc * aw + na * aw, aw) / CTAS;
-            nbox[na] = (ncol[na] + 63) / 64;
+            nbox[na] = mn_out_cols<CTAS>(args, t * C::kTileN + na * BN) / (64 * CTAS);
             b_bytes += static_cast<uint32_t>(nbox[na]) * (BK * 64 * 2);
           }
           for (int k = 0; k < k_iters; ++k, ++it) {
@@ -510,7 +479,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
                 for (int jb = 0; jb < nbox[na]; ++jb)
                   load_box<CTAS>(b_dst + na * (C::kBRows * BK * 2) + jb * (BK * 64 * 2), &map_b,
                                  &full_bar[s], lead,
-                                 t * C::kNAcc * aw + na * aw + static_cast<int>(rank) * ncol[na] +
+                                 t * C::kTileN + na * BN + static_cast<int>(rank) * nbox[na] * 64 +
                                      jb * 64,
                                  args.v0 + k * BK, false, 0);
             } else if (MODE == MODE_DW) {
@@ -549,7 +518,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
                   for (int jb = 0; jb < nbox[na]; ++jb)
                     tma_load_2d_pair_nohint(
                         b_dst + na * (C::kBRows * BK * 2) + jb * (BK * 64 * 2), &map_b, lead,
-                        t * C::kNAcc * aw + na * aw + static_cast<int>(rank) * ncol[na] +
+                        t * C::kTileN + na * BN + static_cast<int>(rank) * nbox[na] * 64 +
                             jb * 64,
                         args.v0 + k * BK);
               } else {
@@ -614,8 +583,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
           uint32_t idesc[C::kNAcc];
 #pragma unroll
           for (int na = 0; na < C::kNAcc; ++na) {
-            const int aw = acc_cols<MODE, CTAS>(args);
-            const int n = kMnOut ? mn_out_cols<CTAS>(args, t * C::kNAcc * aw + na * aw, aw) : BN;
+            const int n = kMnOut ? mn_out_cols<CTAS>(args, t * C::kTileN + na * BN) : BN;
             idesc[na] = n == 0 ? 0u : idesc_bf16(BM * CTAS, n, MODE == MODE_DW, kMnOut);
           }
           for (int k = 0; k < k_iters; ++k, ++it) {
@@ -1137,13 +1105,9 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
         } else if (MODE == MODE_UAC) {
           // U (+)= this block's P W, rescaled to the running maximum; on the
           // last block dH = g (1 - p_y) f'_y W_y - g 2^(M - lse2) U.
-          const int aw = acc_cols<MODE, CTAS>(args);
 #pragma unroll 1
           for (int c = 0; c < C::kTileN / 32; ++c) {
-            // TMEM columns c*32.. hold accumulator c / 8, its columns (c % 8)*32..
-            const int cc = (c & 7) * 32;
-            if (cc >= aw) continue;  // past this accumulator's width (warp-uniform)
-            const int d0 = t * C::kNAcc * aw + (c >> 3) * aw + cc;
+            const int d0 = t * C::kTileN + c * 32;
             if (d0 >= args.hidden) break;  // warp-uniform
             float v[32];
             tmem_ld32(tbase + c * 32, v);
@@ -1154,7 +1118,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
                   args.W + static_cast<long long>(rc.y < 0 ? 0 : rc.y) * args.hidden + d0;
 #pragma unroll
               for (int j8 = 0; j8 < 4; ++j8) {
-                if (d0 + j8 * 8 >= args.hidden || cc + j8 * 8 >= aw) break;
+                if (d0 + j8 * 8 >= args.hidden) break;
                 float* x = v + j8 * 8;
                 if (rc.zero) {
 #pragma unroll
@@ -1192,14 +1156,9 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             }
           }
         } else {  // MODE_DH
-          const int aw = acc_cols<MODE, CTAS>(args);
 #pragma unroll 1
           for (int c = 0; c < C::kTileN / 32; ++c) {
-            // TMEM columns c*32.. hold accumulator c / 8 (c / 8 = 0 on single
-            // CTAs), its columns (c % 8)*32..
-            const int cc = (c & 7) * 32;
-            if (cc >= aw) continue;  // past this accumulator's width (warp-uniform)
-            const int d0 = t * C::kNAcc * aw + (c >> 3) * aw + cc;
+            const int d0 = t * C::kTileN + c * 32;
             if (d0 >= args.hidden) break;  // warp-uniform
             float v[32];
             tmem_ld32(tbase + c * 32, v);
@@ -1209,7 +1168,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
                   args.dH + static_cast<long long>(grow) * args.hidden + d0;
 #pragma unroll
               for (int j8 = 0; j8 < 4; ++j8) {
-                if (d0 + j8 * 8 >= args.hidden || cc + j8 * 8 >= aw) break;
+                if (d0 + j8 * 8 >= args.hidden) break;
                 float* a8 = accp + j8 * 8;
                 if (!args.first) {
                   const float4 x0 = *reinterpret_cast<const float4*>(a8);
