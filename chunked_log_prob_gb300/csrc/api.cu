@@ -72,8 +72,11 @@ int dh_tiles(int hidden, int ctas) {
   return static_cast<int>(cdiv(hidden, BN * dh_accumulators(ctas)));
 }
 
-// Backward forms (grpo_params.flags, or the automatic choice).
-enum Form { kFormRecompute = 0, kFormStored = 1, kFormSinglePass = 2 };
+// Backward forms (grpo_params.flags, or the automatic choice). The single pass
+// comes in two placements of its P conversion: on chip in the U GEMM (one
+// logit block), or a row-wise pass beside the next block's logit GEMM (two
+// blocks; hidden sizes above kFusedMaxHidden only).
+enum Form { kFormRecompute = 0, kFormStored = 1, kFormSinglePass = 2, kFormSinglePassPass = 3 };
 
 struct Layout {
   int ctas;         // 2: CTA-pair GEMMs (default); 1: single-CTA GEMMs
@@ -262,17 +265,34 @@ int single_pass_fwd_splits(int nrb, int tiles, int cap, int sms) {
 // (measured: about a fifth of its time on GB300) and, with several blocks,
 // reads and rewrites its fp32 accumulator once per block.
 double single_pass_cost(long long n_rb_total, int nrb, int n_dt, int nvt, int vb_tiles, int nvb,
-                        int sms) {
-  const double uac_factor = 1.2 + (nvb > 1 ? 0.03 : 0.0);
+                        int sms, double exposed_p) {
+  // exposed_p = 0: P formed on chip; otherwise the P pass's time relative to
+  // the block's forward GEMM, of which the neighbouring GEMMs hide what they
+  // can (as in stored_cost). Measured on GB300 against the stored form's GEMMs
+  // over the same rows: the U GEMM takes 1.07-1.12x the dH GEMM reading P
+  // (Llama-3.1-8B, gpt-oss-20b heads), 1.24x forming P on chip (Llama); the
+  // per-block logit GEMMs 0.99-1.05x the whole-vocabulary one.
+  const double uac_factor = exposed_p > 0.0 ? 1.10 : 1.22;
+  const double fwd_factor = 1.03;
+  std::vector<double> fwd, uac;
   double actual = 0.0;
   for (long long r0 = 0; r0 < n_rb_total; r0 += nrb) {
     const int n = static_cast<int>(std::min<long long>(nrb, n_rb_total - r0));
     for (int t0 = 0; t0 < nvt; t0 += vb_tiles) {
       const int w = std::min(vb_tiles, nvt - t0);
       const int sp = single_pass_fwd_splits(n, w, kMaxSplits / nvb, sms);
-      actual += static_cast<double>(cdiv(static_cast<long long>(n) * sp, sms)) * cdiv(w, sp);
-      actual += static_cast<double>(cdiv(static_cast<long long>(n) * n_dt, sms)) * w / n_dt *
-                uac_factor;
+      fwd.push_back(static_cast<double>(cdiv(static_cast<long long>(n) * sp, sms)) * cdiv(w, sp) *
+                    fwd_factor);
+      uac.push_back(static_cast<double>(cdiv(static_cast<long long>(n) * n_dt, sms)) * w / n_dt *
+                    uac_factor);
+      actual += fwd.back() + uac.back();
+    }
+  }
+  if (exposed_p > 0.0) {
+    const size_t nb = fwd.size();
+    for (size_t b = 0; b < nb; ++b) {
+      const double window = (b > 0 ? uac[b - 1] : 0.0) + (b + 1 < nb ? fwd[b + 1] : 0.0);
+      actual += std::max(0.0, exposed_p * fwd[b] - window);
     }
   }
   return actual;
@@ -301,7 +321,7 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, Form fo
                      Layout* L) {
   L->ctas = (p != nullptr && (p->flags & GRPO_FLAG_SINGLE_CTA) != 0) ? 1 : 2;
   L->stored = form == kFormStored;
-  L->single_pass = form == kFormSinglePass;
+  L->single_pass = form == kFormSinglePass || form == kFormSinglePassPass;
   L->model_cost = 0.0;
   L->ldS = cdiv(std::max(s->vocab, 1), 8) * 8;
   L->n = s->n_tokens;
@@ -331,7 +351,10 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, Form fo
   }
   if (L->single_pass) L->ldS = L->vblock;
   L->need_acc = !L->stored && L->vblock < L->V;
-  L->fused = L->stored && L->D <= kFusedMaxHidden;
+  // Stored form and single pass at D <= kFusedMaxHidden: the dH-type GEMM forms
+  // G (or P) from the stored logits itself; above it a row-wise pass does,
+  // beside the next GEMMs, on a second block.
+  L->fused = (L->stored && L->D <= kFusedMaxHidden) || form == kFormSinglePass;
   // 64-column boxes of a stored row (the whole vocabulary, or one block).
   L->nbox = static_cast<int>(cdiv(L->single_pass ? L->vblock : std::max(s->vocab, 1), 64));
 
@@ -357,7 +380,7 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, Form fo
   // The stored path keeps two chunk blocks when there is more than one chunk
   // (one being turned into G while the next chunk's logits are computed),
   // one when the dH GEMM forms G itself.
-  const int sbufs = L->stored && !L->fused ? 2 : 1;
+  const int sbufs = (L->stored || L->single_pass) && !L->fused ? 2 : 1;
   const bool boxes = L->stored || L->single_pass;  // fp16 logits with box maxima
   const size_t unit_bytes = static_cast<size_t>(ru_rows) *
                             (static_cast<size_t>(L->vblock) * 2 * sbufs +
@@ -392,16 +415,26 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, Form fo
                      : std::min<long long>(n_ru_total, max_units)) *
             ru_rows;
   } else if (sms > 0 && L->single_pass) {
-    // The best modelled schedule (near-ties to the larger chunk).
+    // The best modelled schedule (near-ties to the larger chunk). With a
+    // separate P pass and one vocabulary block, a plan of several chunks
+    // needs two blocks: like the stored form, it then gets half of what the
+    // sizing without a device (one chunk of the largest size) holds.
     const int hi = static_cast<int>(std::min<long long>(n_ru_total, max_units));
     const int vbt = static_cast<int>(cdiv(L->vblock, BN));
-    int best = hi;
+    const long long room = static_cast<long long>(hi) * (hi < n_ru_total ? 2 : 1);
+    const int max_multi =
+        (sbufs == 2 && L->nvb == 1) ? static_cast<int>(std::max<long long>(1, room / 2)) : hi;
+    int best = (hi < n_ru_total) ? std::min(hi, max_multi) : hi;
     double best_cost = 0.0;
+    bool have = false;
     for (int nrb = hi; nrb >= 1; --nrb) {
-      const double cost = single_pass_cost(n_ru_total, nrb, n_dt, L->nvt, vbt, L->nvb, slots);
-      if (nrb == hi || cost < best_cost * 0.995) {
+      if (nrb < n_ru_total && nrb > max_multi) continue;
+      const double cost = single_pass_cost(n_ru_total, nrb, n_dt, L->nvt, vbt, L->nvb, slots,
+                                           L->fused ? 0.0 : 550.0 / L->D);
+      if (!have || cost < best_cost * 0.995) {
         best_cost = cost;
         best = nrb;
+        have = true;
       }
     }
     crows = static_cast<long long>(best) * ru_rows;
@@ -413,7 +446,10 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, Form fo
   crows = std::min(crows, n_ru_total * ru_rows);
   if (crows > INT_MAX / 2) return GRPO_ERR_UNSUPPORTED_SHAPE;
   L->chunk_rows = static_cast<int>(crows);
-  L->n_sbuf = (sbufs == 2 && cdiv(L->nr, L->chunk_rows) > 1) ? 2 : 1;
+  // Two blocks when one can be converted while the next is written: more than
+  // one chunk (stored form), more than one chunk x vocab block (single pass).
+  L->n_sbuf = (sbufs == 2 && cdiv(L->nr, L->chunk_rows) * (L->single_pass ? L->nvb : 1) > 1)
+                  ? 2 : 1;
 
   // Backward chunk block: bf16 G [C x V_b] (recompute path) or the chunk's
   // fp16 logits, rewritten in place as bf16 G [C x ldS] (stored path; two of
@@ -434,31 +470,24 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, Form fo
     L->model_cost = L->stored        ? stored_cost(n_ru_total, rb, n_dt, L->nvt, slots,
                                                    L->fused ? 0.0 : 550.0 / L->D)
                     : L->single_pass ? single_pass_cost(n_ru_total, rb, n_dt, L->nvt, vbt,
-                                                        L->nvb, slots)
+                                                        L->nvb, slots,
+                                                        L->fused ? 0.0 : 550.0 / L->D)
                                      : recompute_cost(n_ru_total, rb, n_dt, L->nvt, vbt, slots);
   }
   return GRPO_OK;
 }
 
-// Layout of a call. GRPO_FLAG_STORED_LOGITS, GRPO_FLAG_SINGLE_PASS or
-// GRPO_FLAG_RECOMPUTE_LOGITS fix the backward form; without any of them the
-// planner takes, among the forms that fit the workspace budget, the one with
-// the shortest modelled GEMM time at the reference SM count (so that sizing
-// and call agree); ties go to the form listed first: stored, single pass,
-// recompute.
-int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
-  const uint32_t f = p != nullptr ? p->flags : 0u;
-  if ((f & GRPO_FLAG_STORED_LOGITS) != 0) return make_layout_mode(s, p, sms, kFormStored, L);
-  if ((f & GRPO_FLAG_SINGLE_PASS) != 0) return make_layout_mode(s, p, sms, kFormSinglePass, L);
-  if ((f & GRPO_FLAG_RECOMPUTE_LOGITS) != 0)
-    return make_layout_mode(s, p, sms, kFormRecompute, L);
-  const Form order[3] = {kFormStored, kFormSinglePass, kFormRecompute};
+// The form with the shortest modelled GEMM time among `forms` that fit the
+// workspace budget, modelled at the reference SM count (so that sizing and
+// call agree); ties go to the earlier one. Returns its layout at `sms`.
+int best_layout(const grpo_shape* s, const grpo_params* p, int sms, const Form* forms, int n,
+                Layout* L) {
   int rc = GRPO_OK;
   int best = -1;
   double best_cost = 0.0;
-  for (int i = 0; i < 3; ++i) {
+  for (int i = 0; i < n; ++i) {
     Layout t;
-    const int r = make_layout_mode(s, p, kRefSms, order[i], &t);
+    const int r = make_layout_mode(s, p, kRefSms, forms[i], &t);
     if (r != GRPO_OK) {
       rc = r;
       continue;
@@ -469,7 +498,30 @@ int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
     }
   }
   if (best < 0) return rc;
-  return make_layout_mode(s, p, sms, order[best], L);
+  return make_layout_mode(s, p, sms, forms[best], L);
+}
+
+// Layout of a call. GRPO_FLAG_STORED_LOGITS, GRPO_FLAG_SINGLE_PASS or
+// GRPO_FLAG_RECOMPUTE_LOGITS fix the backward form; without any of them the
+// planner takes, among the forms that fit the workspace budget, the one with
+// the shortest modelled GEMM time; ties go to the form listed first: stored,
+// single pass, recompute. Above kFusedMaxHidden the single pass's P
+// placement (on chip, one block; or a pass of its own, two blocks) is chosen
+// the same way.
+int make_layout(const grpo_shape* s, const grpo_params* p, int sms, Layout* L) {
+  const uint32_t f = p != nullptr ? p->flags : 0u;
+  const bool p_pass = s->hidden > kFusedMaxHidden;
+  if ((f & GRPO_FLAG_STORED_LOGITS) != 0) return make_layout_mode(s, p, sms, kFormStored, L);
+  if ((f & GRPO_FLAG_RECOMPUTE_LOGITS) != 0)
+    return make_layout_mode(s, p, sms, kFormRecompute, L);
+  if ((f & GRPO_FLAG_SINGLE_PASS) != 0) {
+    const Form sp[2] = {kFormSinglePassPass, kFormSinglePass};
+    return p_pass ? best_layout(s, p, sms, sp, 2, L)
+                  : make_layout_mode(s, p, sms, kFormSinglePass, L);
+  }
+  const Form all[4] = {kFormStored, kFormSinglePassPass, kFormSinglePass, kFormRecompute};
+  const Form fused[3] = {kFormStored, kFormSinglePass, kFormRecompute};
+  return p_pass ? best_layout(s, p, sms, all, 4, L) : best_layout(s, p, sms, fused, 3, L);
 }
 
 int check_shape(const grpo_shape* s, bool need_seq) {
@@ -1077,15 +1129,20 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
 }
 
 // Single-pass backward of a loss call, chunk by chunk over the active row
-// blocks and, within a chunk, vocabulary block by vocabulary block, all on the
-// caller's stream:
-//   FWDS(c, 0) UAC(c, 0) FWDS(c, 1) UAC(c, 1) ... FWDS(c, nb-1) ROWS(c) UAC(c, nb-1)
-// FWDS(c, b) computes the block's logits once: online LSE partials in slots
-// of their own, z_y, and the block's fp16 logits (box-shifted) in the chunk
-// block. UAC(c, b) turns them into P on chip and adds P W[block] to the fp32
-// accumulator U, rescaled to the running maximum. ROWS finishes each row (lse,
-// logp, token loss, g) once every block's partials are in, and the last UAC
-// turns U into dH. Each logit is computed once: 4 N D V flops in all.
+// blocks and, within a chunk, vocabulary block by vocabulary block. Per block
+// b of chunk c:
+//   FWDS(c, b)  the block's logits, once: online LSE partials in slots of
+//               their own, z_y, and the block's box-shifted fp16 logits;
+//   P(c, b)     (D > kFusedMaxHidden) a row-wise pass rewriting them in place
+//               as bf16 P on the side stream, beside the next block's FWDS;
+//   U(c, b)     U (+)= P W[block], rescaled to the running maximum: MODE_UAC
+//               forms P from the logits on chip, MODE_UAP reads P.
+// ROWS(c) finishes each row (lse, logp, token loss, g) once every block's
+// partials are in, and the chunk's last U launch turns U into dH. Each logit
+// is computed once: 4 N D V flops in all. On the caller's stream:
+//   on chip:  FWDS(c,0) U(c,0) ... FWDS(c,nb-1) ROWS(c) U(c,nb-1) ...
+//   P pass:   FWDS(0) FWDS(1) U(0) FWDS(2) U(1) ... over the (chunk, block)
+//             sequence, with P(i) on the side stream between FWDS(i) and U(i).
 int run_single_pass(const void* hidden, const void* W, const int32_t* ids, const uint8_t* mask,
                     const float* old_logp, const float* ref_logp, const float* adv, float* loss,
                     float* logp_out, void* dH, const grpo_params* prm, const Layout& L,
@@ -1096,130 +1153,215 @@ int run_single_pass(const void* hidden, const void* W, const int32_t* ids, const
       !encode_2d(&map_w_k, W, L.D, L.V, L.D, BK, BN / L.ctas) ||
       !encode_2d(&map_w_mn, W, L.D, L.V, L.D, 64, BK))
     return GRPO_ERR_CUDA;
+  DeviceInfo* di = current_device_info();
+  if (di == nullptr) return GRPO_ERR_CUDA;
   const int n_dt_dh = dh_tiles(L.D, L.ctas);
   const int n_rb_total = static_cast<int>(L.nr / BM);
   const int rb_per_chunk = L.chunk_rows / BM;
-  uint16_t* const S = reinterpret_cast<uint16_t*>(w.G);
-  float* const bmax = reinterpret_cast<float*>(w.base + L.off_bmax);
-  const int vbt = static_cast<int>(cdiv(L.vblock, BN));
-  for (int rb0 = 0; rb0 < n_rb_total; rb0 += rb_per_chunk) {
-    const int n_rb = std::min(rb_per_chunk, n_rb_total - rb0);
+  const int n_chunks = static_cast<int>(cdiv(n_rb_total, rb_per_chunk));
+  const int n_steps = n_chunks * L.nvb;  // (chunk, block) pairs
+  const bool overlap = L.n_sbuf == 2;
+  auto chunk_rbs = [&](int c) { return std::min(rb_per_chunk, n_rb_total - c * rb_per_chunk); };
+  auto buf = [&](int i) {
+    return reinterpret_cast<uint16_t*>(w.G) +
+           (overlap ? static_cast<size_t>(i & 1) * L.chunk_rows * L.ldS : 0);
+  };
+  auto bmax = [&](int i) {
+    return reinterpret_cast<float*>(w.base + L.off_bmax) +
+           (overlap ? static_cast<size_t>(i & 1) * L.nbox * L.chunk_rows : 0);
+  };
+  auto width_of = [&](int b) { return std::min(L.vblock, L.V - b * L.vblock); };
+  // Forward splits of block b of chunk c, and the partial slots before it.
+  auto splits_of = [&](int c, int b) {
+    const int n_ru = static_cast<int>(cdiv(chunk_rbs(c), L.ctas));
+    return single_pass_fwd_splits(n_ru, static_cast<int>(cdiv(width_of(b), BN)),
+                                  kMaxSplits / L.nvb, slots);
+  };
+  auto slot0_of = [&](int c, int b) {
+    int s0 = 0;
+    for (int j = 0; j < b; ++j) s0 += splits_of(c, j);
+    return s0;
+  };
+  auto row_args = [&](int c) {
+    GformArgs f;
+    std::memset(&f, 0, sizeof(f));
+    f.n_total = L.n;
+    f.n_rb = chunk_rbs(c);
+    f.rb_offset = c * rb_per_chunk;
+    f.rb_list = w.rb_list;
+    f.n_active = w.n_active;
+    f.part_ld = L.nr;
+    f.vocab = L.V;
+    f.seq_len = L.T;
+    f.part_m = w.pm;
+    f.part_s = w.ps;
+    f.zy = w.zy;
+    f.ids = ids;
+    f.mask = mask;
+    f.old_logp = old_logp;
+    f.ref_logp = ref_logp;
+    f.adv = adv;
+    f.eps_low = prm->eps_low;
+    f.eps_high = prm->eps_high;
+    f.beta = prm->beta;
+    f.loss_den = prm->loss_denominator;
+    f.msum = w.msum;
+    f.seq_mode = (prm->flags & GRPO_FLAG_SEQUENCE_MEAN) != 0;
+    f.seq_lens = w.seq_lens;
+    f.n_nonempty = w.n_nonempty;
+    f.logp_out = logp_out;
+    f.lt = w.lt;
+    f.status = w.status;
+    f.lse_out = w.lse;
+    f.g_out = w.g;
+    f.ldS = L.ldS;
+    f.ldM = L.chunk_rows;
+    TileArgs t = base_args(L, w);
+    set_transform(&t, prm);
+    f.xmode = t.xmode;
+    f.k0 = t.k0;
+    f.k2 = t.k2;
+    return f;
+  };
+  // (1) the logits of step i = (chunk c, block b).
+  auto fwds = [&](int i) -> int {
+    const int c = i / L.nvb, b = i % L.nvb;
+    const int n_rb = chunk_rbs(c);
     const int n_ru = static_cast<int>(cdiv(n_rb, L.ctas));
-    int slot0 = 0;
-    for (int b = 0; b < L.nvb; ++b) {
-      const int v0 = b * L.vblock;
-      const int width = std::min(L.vblock, L.V - v0);
-      const int tiles = static_cast<int>(cdiv(width, BN));
-      const int splits = single_pass_fwd_splits(n_ru, tiles, kMaxSplits / L.nvb, slots);
-      // (1) the block's logits.
-      TileArgs a = base_args(L, w);
-      set_transform(&a, prm);
-      a.n_total = L.n;
-      a.n_rb = n_rb;
-      a.rb_offset = rb0;
-      a.rb_list = w.rb_list;
-      a.n_active = w.n_active;
-      a.k_iters = static_cast<int>(cdiv(L.D, BK));
-      a.group_rows = n_ru;
-      a.n_cols = splits;
-      a.n_vtiles = tiles;
-      a.v0 = v0;
-      a.ids = ids;
-      a.mask = mask;
-      a.part_m = w.pm;
-      a.part_s = w.ps;
-      a.zy = w.zy;
-      a.part_ld = L.nr;
-      a.part_slot0 = slot0;
-      a.S = S;
-      a.ldS = L.ldS;
-      a.box_max = bmax;
-      a.ldM = L.chunk_rows;
-      CUtensorMap map_st;
-      if (!encode_2d(&map_st, S, width, static_cast<uint64_t>(n_rb) * BM, L.ldS, 64, 32))
-        return GRPO_ERR_CUDA;
-      if (launch_fwds_gemm(L.ctas, map_h, map_w_k, map_st, a,
-                           L.ctas * static_cast<int>(std::min<long long>(
-                                        static_cast<long long>(n_ru) * splits, slots)),
-                           st) != cudaSuccess)
-        return GRPO_ERR_CUDA;
-      const bool last = b + 1 == L.nvb;
-      // (2) after the last block: lse, logp, token loss and g of every row.
-      if (last) {
-        GformArgs f;
-        std::memset(&f, 0, sizeof(f));
-        f.n_total = L.n;
-        f.n_rb = n_rb;
-        f.rb_offset = rb0;
-        f.rb_list = w.rb_list;
-        f.n_active = w.n_active;
-        f.splits = slot0 + splits;
-        f.part_ld = L.nr;
-        f.vocab = L.V;
-        f.seq_len = L.T;
-        f.part_m = w.pm;
-        f.part_s = w.ps;
-        f.zy = w.zy;
-        f.ids = ids;
-        f.mask = mask;
-        f.old_logp = old_logp;
-        f.ref_logp = ref_logp;
-        f.adv = adv;
-        f.eps_low = prm->eps_low;
-        f.eps_high = prm->eps_high;
-        f.beta = prm->beta;
-        f.loss_den = prm->loss_denominator;
-        f.msum = w.msum;
-        f.seq_mode = (prm->flags & GRPO_FLAG_SEQUENCE_MEAN) != 0;
-        f.seq_lens = w.seq_lens;
-        f.n_nonempty = w.n_nonempty;
-        f.logp_out = logp_out;
-        f.lt = w.lt;
-        f.status = w.status;
-        f.lse_out = w.lse;
-        f.g_out = w.g;
-        if (launch_finalize_rows(f, n_rb * BM, st) != cudaSuccess) return GRPO_ERR_CUDA;
-      }
-      // (3) U (+)= P W[block]; dH on the last block.
-      CUtensorMap map_s;
-      if (!encode_2d(&map_s, S, width, static_cast<uint64_t>(n_rb) * BM, L.ldS, BK, BM))
-        return GRPO_ERR_CUDA;
-      TileArgs u = base_args(L, w);
-      set_transform(&u, prm);
-      u.n_total = L.n;
-      u.n_rb = n_rb;
-      u.rb_offset = rb0;
-      u.rb_list = w.rb_list;
-      u.n_active = w.n_active;
-      u.k_iters = static_cast<int>(cdiv(width, BK));
-      u.group_rows = group_rows_for(n_ru, slots);
-      u.n_cols = n_dt_dh;
-      u.v0 = v0;
-      u.ids = ids;
-      u.mask = mask;
-      u.lse = w.lse;
-      u.g = w.g;
-      u.zy = w.zy;
-      u.part_m = w.pm;
-      u.part_ld = L.nr;
-      u.slots_prev = slot0;
-      u.slots_cur = slot0 + splits;
-      u.W = static_cast<const __nv_bfloat16*>(W);
-      u.box_max = bmax;
-      u.ldM = L.chunk_rows;
-      u.acc = w.acc;
-      u.dH = static_cast<__nv_bfloat16*>(dH);
-      u.first = b == 0;
-      u.last = last;
-      if (launch_uac_gemm(L.ctas, map_s, map_w_mn, u,
-                          L.ctas * static_cast<int>(std::min<long long>(
-                                       static_cast<long long>(n_ru) * n_dt_dh, slots)),
-                          st) != cudaSuccess)
-        return GRPO_ERR_CUDA;
-      slot0 += splits;
+    const int width = width_of(b);
+    const int splits = splits_of(c, b);
+    TileArgs a = base_args(L, w);
+    set_transform(&a, prm);
+    a.n_total = L.n;
+    a.n_rb = n_rb;
+    a.rb_offset = c * rb_per_chunk;
+    a.rb_list = w.rb_list;
+    a.n_active = w.n_active;
+    a.k_iters = static_cast<int>(cdiv(L.D, BK));
+    a.group_rows = n_ru;
+    a.n_cols = splits;
+    a.n_vtiles = static_cast<int>(cdiv(width, BN));
+    a.v0 = b * L.vblock;
+    a.ids = ids;
+    a.mask = mask;
+    a.part_m = w.pm;
+    a.part_s = w.ps;
+    a.zy = w.zy;
+    a.part_ld = L.nr;
+    a.part_slot0 = slot0_of(c, b);
+    a.S = buf(i);
+    a.ldS = L.ldS;
+    a.box_max = bmax(i);
+    a.ldM = L.chunk_rows;
+    CUtensorMap map_st;
+    if (!encode_2d(&map_st, a.S, width, static_cast<uint64_t>(n_rb) * BM, L.ldS, 64, 32))
+      return GRPO_ERR_CUDA;
+    return launch_fwds_gemm(L.ctas, map_h, map_w_k, map_st, a,
+                            L.ctas * static_cast<int>(std::min<long long>(
+                                         static_cast<long long>(n_ru) * splits, slots)),
+                            st) == cudaSuccess
+               ? GRPO_OK
+               : GRPO_ERR_CUDA;
+  };
+  // (2) the block's logits rewritten in place as bf16 P (not on chip).
+  auto ppass = [&](int i, cudaStream_t s2) -> int {
+    const int c = i / L.nvb, b = i % L.nvb;
+    GformArgs f = row_args(c);
+    f.splits = slot0_of(c, b) + splits_of(c, b);
+    f.S = buf(i);
+    f.box_max = bmax(i);
+    f.v0 = b * L.vblock;
+    f.width = width_of(b);
+    return launch_single_pass_p(f, chunk_rbs(c) * BM, s2) == cudaSuccess ? GRPO_OK
+                                                                          : GRPO_ERR_CUDA;
+  };
+  // (3) lse, logp, token loss and g of chunk c's rows, after its last block.
+  auto rowfin = [&](int c) -> int {
+    GformArgs f = row_args(c);
+    f.splits = slot0_of(c, L.nvb - 1) + splits_of(c, L.nvb - 1);
+    return launch_finalize_rows(f, chunk_rbs(c) * BM, st) == cudaSuccess ? GRPO_OK
+                                                                          : GRPO_ERR_CUDA;
+  };
+  // (4) U (+)= P W[block]; dH on the chunk's last block.
+  auto uacc = [&](int i) -> int {
+    const int c = i / L.nvb, b = i % L.nvb;
+    const int n_rb = chunk_rbs(c);
+    const int n_ru = static_cast<int>(cdiv(n_rb, L.ctas));
+    const int width = width_of(b);
+    CUtensorMap map_s;
+    if (!encode_2d(&map_s, buf(i), width, static_cast<uint64_t>(n_rb) * BM, L.ldS, BK, BM))
+      return GRPO_ERR_CUDA;
+    TileArgs u = base_args(L, w);
+    set_transform(&u, prm);
+    u.n_total = L.n;
+    u.n_rb = n_rb;
+    u.rb_offset = c * rb_per_chunk;
+    u.rb_list = w.rb_list;
+    u.n_active = w.n_active;
+    u.k_iters = static_cast<int>(cdiv(width, BK));
+    u.group_rows = group_rows_for(n_ru, slots);
+    u.n_cols = n_dt_dh;
+    u.v0 = b * L.vblock;
+    u.ids = ids;
+    u.mask = mask;
+    u.lse = w.lse;
+    u.g = w.g;
+    u.zy = w.zy;
+    u.part_m = w.pm;
+    u.part_ld = L.nr;
+    u.slots_prev = slot0_of(c, b);
+    u.slots_cur = u.slots_prev + splits_of(c, b);
+    u.W = static_cast<const __nv_bfloat16*>(W);
+    u.box_max = bmax(i);
+    u.ldM = L.chunk_rows;
+    u.acc = w.acc;
+    u.dH = static_cast<__nv_bfloat16*>(dH);
+    u.first = b == 0;
+    u.last = b + 1 == L.nvb;
+    const int grid =
+        L.ctas * static_cast<int>(std::min<long long>(static_cast<long long>(n_ru) * n_dt_dh, slots));
+    const cudaError_t e = L.fused ? launch_uac_gemm(L.ctas, map_s, map_w_mn, u, grid, st)
+                                  : launch_uap_gemm(L.ctas, map_s, map_w_mn, u, grid, st);
+    return e == cudaSuccess ? GRPO_OK : GRPO_ERR_CUDA;
+  };
+
+  int r = GRPO_OK;
+  if (L.fused || !overlap) {
+    for (int i = 0; i < n_steps && r == GRPO_OK; ++i) {
+      const int c = i / L.nvb, b = i % L.nvb;
+      r = fwds(i);
+      if (r == GRPO_OK && !L.fused) r = ppass(i, st);
+      if (r == GRPO_OK && b + 1 == L.nvb) r = rowfin(c);
+      if (r == GRPO_OK) r = uacc(i);
     }
-    (void)vbt;
-  }
+  } else {
+    std::lock_guard<std::mutex> side_lock(di->side_mu);
+    // The side stream starts after everything already on the caller's stream.
+    if (cudaEventRecord(di->ev_main, st) != cudaSuccess ||
+        cudaStreamWaitEvent(di->side, di->ev_main, 0) != cudaSuccess)
+      return GRPO_ERR_CUDA;
+    auto fwd_then_p = [&](int i) -> int {
+      int rr = fwds(i);
+      if (rr != GRPO_OK) return rr;
+      if (cudaEventRecord(di->ev_fwd[i & 1], st) != cudaSuccess ||
+          cudaStreamWaitEvent(di->side, di->ev_fwd[i & 1], 0) != cudaSuccess)
+        return GRPO_ERR_CUDA;
+      rr = ppass(i, di->side);
+      if (rr != GRPO_OK) return rr;
+      return cudaEventRecord(di->ev_g[i & 1], di->side) == cudaSuccess ? GRPO_OK
+                                                                        : GRPO_ERR_CUDA;
+    };
+    r = fwd_then_p(0);
+    for (int i = 0; i < n_steps && r == GRPO_OK; ++i) {
+      // Block (i+1) & 1 was last read by U(i-1), enqueued before this FWDS.
+      if (i + 1 < n_steps) r = fwd_then_p(i + 1);
+      if (r != GRPO_OK) break;
+      if (cudaStreamWaitEvent(st, di->ev_g[i & 1], 0) != cudaSuccess) return GRPO_ERR_CUDA;
+      if (i % L.nvb + 1 == L.nvb) r = rowfin(i / L.nvb);
+      if (r == GRPO_OK) r = uacc(i);
+    }
+  }  // side_lock released: this call's records and waits are all enqueued
+  if (r != GRPO_OK) return r;
   FinishArgs fin;
   std::memset(&fin, 0, sizeof(fin));
   fin.n = L.n;
@@ -1540,7 +1682,7 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
   info->launches_logp = L.n > 0 ? 2 : 0;
   info->launches_loss = L.n <= 0        ? 0
                         : L.stored      ? 3 + 3 * info->n_chunks
-                        : L.single_pass ? 3 + info->n_chunks * (2 * L.nvb + 1)
+                        : L.single_pass ? 3 + info->n_chunks * ((L.fused ? 2 : 3) * L.nvb + 1)
                                         : 4 + 2 * info->n_chunks * info->n_vocab_blocks;
   if (L.n > 0 && params != nullptr && (params->flags & GRPO_FLAG_SEQUENCE_MEAN) != 0)
     info->launches_loss += 1;

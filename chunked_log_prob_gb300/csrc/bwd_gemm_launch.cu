@@ -20,6 +20,8 @@ cudaError_t prepare_bwd_gemms() {
   if (e == cudaSuccess) e = prepare_gemm_variant<MODE_DHS, 2>();
   if (e == cudaSuccess) e = prepare_gemm_variant<MODE_UAC, 1>();
   if (e == cudaSuccess) e = prepare_gemm_variant<MODE_UAC, 2>();
+  if (e == cudaSuccess) e = prepare_gemm_variant<MODE_UAP, 1>();
+  if (e == cudaSuccess) e = prepare_gemm_variant<MODE_UAP, 2>();
   return e;
 }
 
@@ -53,6 +55,12 @@ cudaError_t launch_uac_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMa
                             const TileArgs& args, int grid, cudaStream_t stream) {
   return ctas == 2 ? launch_gemm_variant<MODE_UAC, 2>(map_a, map_b, args, grid, stream)
                    : launch_gemm_variant<MODE_UAC, 1>(map_a, map_b, args, grid, stream);
+}
+
+cudaError_t launch_uap_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                            const TileArgs& args, int grid, cudaStream_t stream) {
+  return ctas == 2 ? launch_gemm_variant<MODE_UAP, 2>(map_a, map_b, args, grid, stream)
+                   : launch_gemm_variant<MODE_UAP, 1>(map_a, map_b, args, grid, stream);
 }
 
 }  // namespace grpo

@@ -528,6 +528,97 @@ __global__ void __launch_bounds__(kFinalizeThreads) finalize_rows_kernel(const G
   a.g_out[grow] = g;
 }
 
+// Single pass at hidden sizes above 2048: one vocabulary block of a chunk's
+// stored logits rewritten in place as the bf16
+//   P_v = 2^(z'_v log2e - M) f'(S_v),
+// M the row's running maximum (log2 units) over the forward's split partials
+// of the blocks so far (slots [0, splits)); the target column and rows that do
+// not count become zeros. The U GEMM then reads P through TMA, so each logit
+// is converted once rather than once per hidden tile. Columns past the
+// block's width are never read (the U GEMM's tensor map ends there). One CTA
+// per row.
+__global__ void __launch_bounds__(kGformThreads) single_pass_p_kernel(const GformArgs a) {
+  __shared__ float sh_m2;
+  __shared__ int sh_y, sh_on;
+  const int lrow = blockIdx.x;
+  const long long grow = chunk_row(a, lrow);
+  if (grow < 0) return;  // whole block: uniform
+  if (threadIdx.x == 0) {
+    const bool on = grow < a.n_total && (a.mask == nullptr || a.mask[grow] != 0);
+    float m2 = -INFINITY;
+    int y = -1;
+    if (on) {
+      for (int s = 0; s < a.splits; ++s) m2 = fmaxf(m2, a.part_m[s * a.part_ld + grow]);
+      const int yy = a.ids[grow];
+      if (yy >= a.v0 && yy < a.v0 + a.width) y = yy - a.v0;
+    }
+    sh_m2 = m2;
+    sh_y = y;
+    sh_on = on ? 1 : 0;
+  }
+  __syncthreads();
+  uint4* row = reinterpret_cast<uint4*>(a.S + static_cast<long long>(lrow) * a.ldS);
+  const int n_vec = static_cast<int>(a.ldS / 8);
+  if (!sh_on) {
+    for (int i = threadIdx.x; i < n_vec; i += blockDim.x) row[i] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const float m2 = sh_m2;
+  const float* bm = a.box_max + lrow;
+  auto box_max = [&](int i) { return __ldg(bm + static_cast<long long>(i >> 3) * a.ldM); };
+  auto convert = [&](const uint4 in, int i) {
+    const float mb = box_max(i);
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    uint32_t o[4];
+    if (a.xmode == 0) {
+      const float c = fmaf(mb, kLog2e, -m2);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float z0, z1;
+        unpack_f16x2(w[k], z0, z1);
+        o[k] = pack_bf16x2(ex2(fmaf(z0, kLog2e, c)), ex2(fmaf(z1, kLog2e, c)));
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float z0, z1;
+        unpack_f16x2(w[k], z0, z1);
+        z0 += mb;
+        z1 += mb;
+        float d0 = 1.f, d1 = 1.f;  // dz'/dz recovered from the stored z'
+        if (a.xmode == 1) {
+          d0 = d1 = a.k0;
+        } else {
+          const float u0 = z0 / a.k2, u1 = z1 / a.k2;
+          d0 = a.k0 * fmaf(-u0, u0, 1.f);
+          d1 = a.k0 * fmaf(-u1, u1, 1.f);
+        }
+        o[k] = pack_bf16x2(ex2(fmaf(z0, kLog2e, -m2)) * d0, ex2(fmaf(z1, kLog2e, -m2)) * d1);
+      }
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  };
+  // Two 16-byte vectors per thread per step keep more loads in flight.
+  const int step = 2 * blockDim.x;
+  int i = threadIdx.x;
+  for (; i + blockDim.x < n_vec; i += step) {
+    const uint4 in0 = row[i];
+    const uint4 in1 = row[i + blockDim.x];
+    row[i] = convert(in0, i);
+    row[i + blockDim.x] = convert(in1, i + blockDim.x);
+  }
+  if (i < n_vec) row[i] = convert(row[i], i);
+  __syncthreads();  // the whole row is written before the target column is cleared
+  if (threadIdx.x == 0 && sh_y >= 0) a.S[static_cast<long long>(lrow) * a.ldS + sh_y] = 0;
+}
+
+cudaError_t launch_single_pass_p(const GformArgs& a, int rows, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  LaunchTimer timer("single_pass_p_kernel", stream);
+  single_pass_p_kernel<<<rows, kGformThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_finalize_rows(const GformArgs& a, int rows, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
   LaunchTimer timer("finalize_rows_kernel", stream);

@@ -37,6 +37,9 @@
 //              accumulator U = sum_v P_v W_v across blocks, rescaled by
 //              2^(M_prev - M) whenever the maximum grows; the last block turns
 //              it into dH = g (1 - p_y) f'_y W_y - g 2^(M - lse2) U.
+//   MODE_UAP   MODE_UAC for hidden sizes above 2048: the block's P was formed
+//              by a row-wise pass of its own, so A arrives through TMA as bf16
+//              like MODE_DH's G, and no converter warps run.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -55,12 +58,18 @@ constexpr int TMEM_COLS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum GemmMode { MODE_FWD = 0, MODE_BWDG = 1, MODE_DH = 2, MODE_FWDS = 3, MODE_DW = 4,
-                MODE_DHS = 5, MODE_UAC = 6 };
+                MODE_DHS = 5, MODE_UAC = 6, MODE_UAP = 7 };
 
 __host__ __device__ constexpr bool is_fwd(int mode) { return mode == MODE_FWD || mode == MODE_FWDS; }
 __host__ __device__ constexpr bool is_dh(int mode) {
-  return mode == MODE_DH || mode == MODE_DHS || mode == MODE_UAC;
+  return mode == MODE_DH || mode == MODE_DHS || mode == MODE_UAC || mode == MODE_UAP;
 }
+// dH-type modes whose A operand arrives ready for the MMA (bf16 G or P via TMA).
+__host__ __device__ constexpr bool is_dh_plain(int mode) {
+  return mode == MODE_DH || mode == MODE_UAP;
+}
+// Modes whose epilogue keeps the single pass's U accumulator.
+__host__ __device__ constexpr bool is_uacc(int mode) { return mode == MODE_UAC || mode == MODE_UAP; }
 // Modes whose A operand is stored fp16 logits, converted on chip before the MMA.
 __host__ __device__ constexpr bool has_cvt(int mode) { return mode == MODE_DHS || mode == MODE_UAC; }
 
@@ -505,13 +514,13 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             } else if (CTAS == 2) {
               // Both CTAs count their bytes on the leader's barrier.
               const uint32_t lead = mapa_shared(smem_u32(&full_bar[s]), 0);
-              mbar_arrive_expect_tx_cluster(lead, MODE == MODE_DH ? A_BYTES + b_bytes
+              mbar_arrive_expect_tx_cluster(lead, is_dh_plain(MODE) ? A_BYTES + b_bytes
                                                                   : C::kStageBytes);
 #pragma unroll
               for (int ks = 0; ks < C::kKSub; ++ks)
                 tma_load_2d_pair(a_dst + ks * A_BYTES, &map_a, lead, (k * C::kKSub + ks) * BK, a_row,
                                  pol_a);
-              if (MODE == MODE_DH) {
+              if (is_dh_plain(MODE)) {
                 // Per accumulator, this CTA's share of its D columns.
 #pragma unroll
                 for (int na = 0; na < C::kNAcc; ++na)
@@ -534,9 +543,9 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
               }
             } else {
               mbar_arrive_expect_tx(&full_bar[s],
-                                    MODE == MODE_DH ? A_BYTES + b_bytes : C::kStageBytes);
+                                    is_dh_plain(MODE) ? A_BYTES + b_bytes : C::kStageBytes);
               tma_load_2d_hint(a_dst, &map_a, &full_bar[s], k * BK, a_row, pol_a);
-              if (MODE == MODE_DH) {
+              if (is_dh_plain(MODE)) {
                 // W[v0 + k*64 .. +64, d0 .. d0+256) as up to four 64x64 MN-major boxes.
                 for (int jb = 0; jb < nbox[0]; ++jb)
                   tma_load_2d(b_dst + jb * (BK * 64 * 2), &map_b, &full_bar[s],
@@ -708,7 +717,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             rc.ytarget = (gval - gval * ex2(fmaf(zy, kLog2e, -lse2))) * dz_of_logit(args, zy);
           }
         }
-      } else if (MODE == MODE_UAC) {
+      } else if (is_uacc(MODE)) {
         if (valid && (args.mask == nullptr || args.mask[grow] != 0)) {
           // Running maxima (log2 units) from the forward's split partials.
           float mcur = -INFINITY;
@@ -1102,7 +1111,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
               }
             }
           }
-        } else if (MODE == MODE_UAC) {
+        } else if (is_uacc(MODE)) {
           // U (+)= this block's P W, rescaled to the running maximum; on the
           // last block dH = g (1 - p_y) f'_y W_y - g 2^(M - lse2) U.
 #pragma unroll 1

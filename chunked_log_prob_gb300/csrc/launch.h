@@ -71,6 +71,7 @@ struct GformArgs {
   long long ldS;
   const float* box_max;  // [ceil(V / 64)][ldM] the boxes' maxima
   long long ldM;
+  int v0, width;         // single_pass_p: the vocabulary block of S (splits = slots so far)
   int xmode;
   float k0, k2;
   int* status;
@@ -163,6 +164,10 @@ cudaError_t launch_dhs_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMa
 // boxes, 128-byte swizzle); map_b: W MN-major (64 x 64 boxes).
 cudaError_t launch_uac_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                             const TileArgs& args, int grid, cudaStream_t stream);
+// map_a: one vocabulary block of bf16 P [rows][width] (64 x 128 boxes), as
+// single_pass_p_kernel leaves it; map_b: W MN-major.
+cudaError_t launch_uap_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                            const TileArgs& args, int grid, cudaStream_t stream);
 // map_dw: dW[v0 : v0 + dw_rows) as fp32 [rows][hidden], 32 x 32 boxes with the
 // 128-byte swizzle (used by the CTA-pair variant).
 cudaError_t launch_dw_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
@@ -183,6 +188,7 @@ cudaError_t launch_fwds_gemm(int ctas, const CUtensorMap& map_a, const CUtensorM
                              cudaStream_t stream);
 cudaError_t launch_finalize_gform(const GformArgs& a, int rows, cudaStream_t stream);
 cudaError_t launch_finalize_rows(const GformArgs& a, int rows, cudaStream_t stream);
+cudaError_t launch_single_pass_p(const GformArgs& a, int rows, cudaStream_t stream);
 cudaError_t launch_finish_loss(const FinishArgs& a, cudaStream_t stream);
 cudaError_t launch_bounded_wait_selftest(int* status, int* waited_out, cudaStream_t stream);
 

@@ -135,14 +135,16 @@ typedef struct grpo_shape {
 /* grpo_params.flags bit: the single-pass backward. Per chunk of rows and per
  * vocabulary block of vocab_block columns (automatic: blocks of about 32768,
  * at most 32 of them), one logit GEMM keeps the block's logits in fp16
- * (box-shifted as above) and one GEMM converts them on chip to
- * P_v = exp(z'_v - M) f'(S_v), M the row's running maximum, the target column
- * left out, and adds P W[block] into an fp32 accumulator U, rescaled whenever
- * the maximum grows. After the last block, dH = g (1 - p_y) f'_y W[y]
- * - g exp(M - lse) U. Each logit is computed once (4 N D V flops, like the
- * stored form), while the workspace holds one block: chunk x vocab_block x
- * 2 bytes plus the chunk x D fp32 accumulator. With dW requested the call
- * recomputes the logit tiles instead (same chunk and vocab block). */
+ * (box-shifted as above); they become P_v = exp(z'_v - M) f'(S_v), M the
+ * row's running maximum, the target column left out (on chip in the next
+ * GEMM at D <= 2048, else by a row-wise pass beside the next block's logit
+ * GEMM, on a second block), and one GEMM adds P W[block] into an fp32
+ * accumulator U, rescaled whenever the maximum grows. After the last block,
+ * dH = g (1 - p_y) f'_y W[y] - g exp(M - lse) U. Each logit is computed once
+ * (4 N D V flops, like the stored form), while the workspace holds one or two
+ * blocks of chunk x vocab_block x 2 bytes plus the chunk x D fp32
+ * accumulator. With dW requested the call recomputes the logit tiles instead
+ * (same chunk and vocab block). */
 #define GRPO_FLAG_SINGLE_PASS 32u
 
 typedef struct grpo_params {
@@ -240,9 +242,10 @@ typedef struct grpo_plan_info {
   int32_t launches_logp;     /* kernel launches of one grpo_logp_fwd call    */
   int32_t launches_loss;     /* kernel launches of one grpo_loss_fwd_bwd
                                 (with a mask; one fewer without)          */
-  int32_t g_in_dh_gemm;      /* 1: the stored-logit backward forms G inside
-                                the dH GEMM when dW is not requested (hidden
-                                <= 2048); 0: in a pass of its own          */
+  int32_t g_in_dh_gemm;      /* 1: the stored-logit backward forms G (the
+                                single pass P) inside the dH-type GEMM
+                                (hidden <= 2048; not with dW); 0: in a
+                                row-wise pass of its own beside the GEMMs  */
   int32_t stored_logits;     /* 1: the stored-logit backward              */
   int32_t single_pass;       /* 1: the single-pass backward (neither: the
                                 recomputed logit tiles); the flags' or the

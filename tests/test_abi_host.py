@@ -118,9 +118,9 @@ def test_automatic_backward_form_follows_the_budget(clp):
     assert ws(0) == ws(STORED)
     assert ws(0, 8 << 30) == ws(STORED, 8 << 30)
     # Between about 0.3 and 1.5 GB the stored form's chunks are too small for
-    # whole SM waves: the single pass, which holds one vocabulary block of a
-    # larger chunk, is modelled faster.
-    assert ws(0, 1 << 30) == ws(SINGLE_PASS, 1 << 30) < ws(STORED, 1 << 30)
+    # whole SM waves: the single pass, which holds one or two vocabulary blocks
+    # of a larger chunk, is modelled faster.
+    assert ws(0, 1 << 30) == ws(SINGLE_PASS, 1 << 30) <= 1 << 30
     # Below the stored form's smallest chunk (two logit blocks of 256 rows),
     # it does not fit at all.
     with pytest.raises(clp.GrpoError):

@@ -336,12 +336,15 @@ def test_single_pass_ragged(clp, N, T, D, V, chunk, vblock, padded):
           f"single pass {N}x{D}x{V} ({plan['n_vocab_blocks']} blocks)")
 
 
+# D = 200: P formed on chip; D = 2176: by a pass of its own, double-buffered
+# beside the next block's logit GEMM (12 or 4 blocks) or not (1 block).
+@pytest.mark.parametrize("D", [200, 2176])
 @pytest.mark.parametrize("vblock", [256, 768, 0])
 @pytest.mark.parametrize("kw", XFORMS)
-def test_single_pass_transforms(clp, kw, vblock):
-    # Logit std ~2.8 so that softcaps of 2-3 saturate; 12, 4 or 1 vocab blocks.
-    p = synth.make_problem("tiny", seed=33, T=75, prompts=1, G=4, D=200, V=3000,
-                           lengths=(20, 75), weight_std=0.2)
+def test_single_pass_transforms(clp, kw, vblock, D):
+    # Logit std ~2.8 so that softcaps of 2-3 saturate.
+    p = synth.make_problem("tiny", seed=33, T=75, prompts=1, G=4, D=D, V=3000,
+                           lengths=(20, 75), weight_std=0.2 if D < 1000 else 0.06)
     xf = oracle.Transform(scale_mul=kw.get("logit_scale_multiply", 1.0),
                           scale_div=kw.get("logit_scale_divide", 1.0),
                           softcap=kw.get("logit_softcapping", 0.0),
@@ -369,6 +372,44 @@ def test_single_pass_padding_blocks(clp, chunk):
     st = clp.grpo_read_device_status(ws)
     got = (loss.item(), logp.cpu().double().numpy(), dH.cpu().double().numpy(), st)
     check(got, want, p.mask, f"single pass padding chunk={chunk}")
+
+
+@pytest.mark.parametrize("D", [320, 2304])
+def test_single_pass_many_chunks_and_blocks(clp, D):
+    # 4 chunks x 3 vocab blocks, padded: at D = 2304 the P pass of each
+    # (chunk, block) runs on the side stream beside the next one's logit GEMM,
+    # alternating two blocks, across chunk boundaries.
+    p = synth.make_problem("tiny", seed=57 + D, T=256, prompts=1, G=4, D=D, V=3000,
+                           lengths=(60, 256))
+    old, ref, want = oracle_case(p)
+    params = clp.make_params(chunk_tokens=256, vocab_block=1024, flags=SINGLE_PASS)
+    plan = clp.grpo_get_plan(p.n_tokens, D, p.vocab, p.seq_len, params)
+    assert plan["n_chunks"] == 4 and plan["n_vocab_blocks"] == 3
+    assert plan["g_in_dh_gemm"] == (1 if D <= 2048 else 0)
+    check(gpu_loss(clp, p, old, ref, params), want, p.mask, f"single pass D={D} 4x3 steps")
+
+
+def test_single_pass_both_placements_above_2048(clp):
+    # Above D = 2048 the planner places the single pass's P conversion on chip
+    # (one logit block) or in a pass of its own (two blocks), whichever is
+    # modelled faster within the budget: a range of budgets reaches both, and
+    # each gives the oracle's results.
+    p = synth.make_problem("tiny", seed=58, T=512, prompts=1, G=4, D=2304, V=6000,
+                           lengths=(100, 512))
+    old, ref, want = oracle_case(p)
+    full = clp.grpo_workspace_size(p.n_tokens, p.hidden_size, p.vocab, p.seq_len,
+                                   clp.make_params(flags=SINGLE_PASS, vocab_block=2048))
+    seen = {}
+    for frac in (0, 1.0, 0.8, 0.6, 0.5, 0.4, 0.3):
+        params = clp.make_params(flags=SINGLE_PASS, vocab_block=2048,
+                                 workspace_limit_bytes=int(full * frac))
+        plan = clp.grpo_get_plan(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, params)
+        assert plan["single_pass"] == 1
+        seen.setdefault(plan["g_in_dh_gemm"], params)
+    assert set(seen) == {0, 1}, seen
+    for on_chip, params in seen.items():
+        check(gpu_loss(clp, p, old, ref, params), want, p.mask,
+              f"single pass D=2304, P {'on chip' if on_chip else 'in its own pass'}")
 
 
 def test_three_backward_forms_agree(clp):
