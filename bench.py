@@ -326,8 +326,8 @@ _NCU_SCALE = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e
 _FIRST_KERNEL = "row_plan_kernel"  # every grpo_loss_fwd_bwd call starts with it
 # The library's kernels (any other launch in a capture is torch's own).
 LIBRARY_KERNELS = ("tc_gemm_kernel", "finalize_kernel", "finalize_gform_kernel",
-                   "finalize_rows_kernel", "finish_loss_kernel", "row_plan_kernel",
-                   "zero_padding_blocks_kernel", "seq_lens_kernel",
+                   "finalize_rows_kernel", "single_pass_p_kernel", "finish_loss_kernel",
+                   "row_plan_kernel", "zero_padding_blocks_kernel", "seq_lens_kernel",
                    "bounded_wait_selftest_kernel")
 
 
@@ -425,8 +425,9 @@ def kernel_work(name, D, V):
     """Algorithmic work of one kernel kind per valid token: (bound, amount, unit)."""
     if name.startswith("tc_gemm_kernel"):
         return "tensor", 2.0 * D * V, "flop"  # one pass of the N x V x D contraction
-    if name == "finalize_gform_kernel":
-        # fp16 logit row in, bf16 G row out, one fp32 maximum per 64-column box
+    if name in ("finalize_gform_kernel", "single_pass_p_kernel"):
+        # fp16 logit row in, bf16 G (or P) row out, one fp32 maximum per 64-column
+        # box: over a call, every vocabulary column of every valid token once
         return "hbm", 4.0 * V + 4.0 * math.ceil(V / 64), "byte"
     return None
 
