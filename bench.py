@@ -797,8 +797,8 @@ def run_ours(args):
 
 def run_budget_sweep(args):
     """Workspace budget against call time: for each budget, the library's
-    automatic choice and both forced backward forms, each with the largest
-    plan the budget allows. One JSON line per (budget, form); a form that does
+    automatic choice and the three forced backward forms, each with the
+    largest plan the budget allows. One JSON line per (budget, form); a form that does
     not fit a budget is reported as such."""
     import torch
 
@@ -821,7 +821,7 @@ def run_budget_sweep(args):
     reps = max(3, args.steps)
     for gb in [float(x) for x in args.budget_sweep.split(",") if x.strip()]:
         limit = int(gb * (1 << 30))
-        for form in ("auto", "stored", "recompute"):
+        for form in ("auto", "stored", "single_pass", "recompute"):
             params = clp.make_params(p.eps_low, p.eps_high, p.beta,
                                      flags=FORM_FLAGS[form], workspace_limit_bytes=limit)
             row = {"workload": p.name, "budget_gb": gb, "form": form}

@@ -81,15 +81,17 @@ typedef struct grpo_shape {
  *   - stored logits (GRPO_FLAG_STORED_LOGITS): 4 N D V flops, a workspace
  *     of chunk x V x 2 bytes (and twice that at D > 2048, see below);
  *   - single pass (GRPO_FLAG_SINGLE_PASS): 4 N D V flops, a workspace of
- *     chunk x vocab_block x 2 bytes plus a chunk x D fp32 accumulator;
+ *     one or two blocks of chunk x vocab_block x 2 bytes plus a chunk x D
+ *     fp32 accumulator;
  *   - recomputed logit tiles (GRPO_FLAG_RECOMPUTE_LOGITS): 6 N D V flops
  *     (the pages' backward, which re-runs the forward), a workspace of
  *     chunk x vocab_block x 2 bytes plus a chunk x D fp32 accumulator.
  * The automatic choice is, among the forms that fit the workspace budget
  * (workspace_limit_bytes, or half the free device memory with
  * GRPO_FLAG_FIT_FREE_MEMORY; none by default), the one whose modelled GEMM
- * time is shortest (whole SM waves of each launch, the separate G pass the
- * stored form cannot hide, the single pass's on-chip conversion). It is made
+ * time is shortest (whole SM waves of each launch, the part of a separate G or
+ * P pass the neighbouring GEMMs cannot hide, the cost of forming P on chip,
+ * with factors measured on GB300). It is made
  * at GB300's SM count, so that grpo_workspace_size and the call agree;
  * grpo_get_plan reports it. Setting more than one of the three flags is
  * GRPO_ERR_INVALID_ARG.
@@ -137,8 +139,9 @@ typedef struct grpo_shape {
  * at most 32 of them), one logit GEMM keeps the block's logits in fp16
  * (box-shifted as above); they become P_v = exp(z'_v - M) f'(S_v), M the
  * row's running maximum, the target column left out (on chip in the next
- * GEMM at D <= 2048, else by a row-wise pass beside the next block's logit
- * GEMM, on a second block), and one GEMM adds P W[block] into an fp32
+ * GEMM; or, at D > 2048 when the planner models it faster within the budget,
+ * by a row-wise pass beside the next block's logit GEMM, on a second block),
+ * and one GEMM adds P W[block] into an fp32
  * accumulator U, rescaled whenever the maximum grows. After the last block,
  * dH = g (1 - p_y) f'_y W[y] - g exp(M - lse) U. Each logit is computed once
  * (4 N D V flops, like the stored form), while the workspace holds one or two
@@ -323,9 +326,10 @@ int grpo_selftest_bounded_wait(void* workspace, size_t workspace_bytes, void* st
  * GEMM variants are named "tc_gemm_kernel<mode, ctas>": mode 0 is the logit GEMM
  * of the forward pass, 1 forms G from recomputed logits, 2 is G W -> dH, 3 is
  * the logit GEMM that also stores fp16 logits, 4 is the lm_head gradient,
- * 5 is the dH GEMM that forms G from the stored logits, and 6 is the single
- * pass's GEMM that forms P from one block's stored logits and accumulates U;
- * ctas is 2 for a CTA pair. Returns GRPO_OK, GRPO_ERR_INVALID_ARG (count null, capacity < 0, or out
+ * 5 is the dH GEMM that forms G from the stored logits, 6 is the single
+ * pass's GEMM that forms P from one block's stored logits and accumulates U,
+ * and 7 the same GEMM reading P formed by single_pass_p_kernel; ctas is 2
+ * for a CTA pair. Returns GRPO_OK, GRPO_ERR_INVALID_ARG (count null, capacity < 0, or out
  * null with capacity > 0) or GRPO_ERR_CUDA (an event could not be read; the
  * other launches are still summed). */
 typedef struct grpo_kernel_time {
