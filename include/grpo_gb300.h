@@ -235,7 +235,10 @@ int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* How a call with this shape and these params is carried out on the current
- * device (host only; reads the device's SM count, launches nothing). */
+ * device (host only; reads the device's SM count, launches nothing): the
+ * chunking whose memory the pages size by the chunk rather than the batch
+ * ("GRPO with 7x longer context", section "Flattened sequence length
+ * chunking", Eq. 1-3), and the backward form chosen for the budget. */
 typedef struct grpo_plan_info {
   int32_t chunk_rows;        /* rows per backward chunk                      */
   int32_t vocab_block;       /* vocab columns per backward block             */

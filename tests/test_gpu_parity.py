@@ -482,8 +482,9 @@ def test_g_in_dh_gemm_matches_separate_pass(clp, chunk):
           f"fused G chunk={chunk}")
 
 
+@pytest.mark.parametrize("flags", [STORED, SINGLE_PASS])
 @pytest.mark.parametrize("n", [2048, 4096, 8192])
-def test_device_plan_fits_host_sized_workspace(clp, n):
+def test_device_plan_fits_host_sized_workspace(clp, n, flags):
     # grpo_workspace_size plans without a device; the call plans with the SM
     # count (and may split a batch that fits one logit block into
     # double-buffered chunks). The host-sized workspace must always suffice,
@@ -493,7 +494,7 @@ def test_device_plan_fits_host_sized_workspace(clp, n):
                            lengths=(128, 256))
     base, _ = oracle.selective_logp(p.hidden[:4], p.weight, p.ids.numpy()[:4])
     old = torch.full((n,), float(base.mean()))
-    params = clp.make_params(flags=STORED)
+    params = clp.make_params(flags=flags)
     plan = clp.grpo_get_plan(n, D, V, p.seq_len, params)
     assert plan["workspace_bytes"] <= clp.grpo_workspace_size(n, D, V, p.seq_len, params)
     L1, lp1, dH1, s1 = gpu_loss(clp, p, old, old, params)
@@ -649,16 +650,29 @@ def test_lm_head_gradient_with_transform(clp):
         assert rel <= DH_RTOL, (flags, rel)
 
 
-def test_concurrent_calls_from_two_threads(clp):
-    # Separate workspaces and streams, stored path with several chunks and G
-    # formed in its own pass (D > 2048), so the shared side stream is used:
-    # results equal the same calls made serially.
+def _side_stream_params(clp, flags, n, D, V, T):
+    """Params under which a call of this shape runs its G (stored form) or P
+    (single pass) pass on the side stream, in more than one step."""
+    for chunk, vb in ((512, 1024), (256, 1024), (512, 0), (1024, 1024)):
+        params = clp.make_params(chunk_tokens=chunk, vocab_block=vb, flags=flags)
+        plan = clp.grpo_get_plan(n, D, V, T, params)
+        steps = plan["n_chunks"] * (plan["n_vocab_blocks"] if flags == SINGLE_PASS else 1)
+        if plan["g_in_dh_gemm"] == 0 and steps > 1:
+            return params
+    raise AssertionError("no plan with a side-stream pass")
+
+
+@pytest.mark.parametrize("flags", [STORED, SINGLE_PASS])
+def test_concurrent_calls_from_two_threads(clp, flags):
+    # Separate workspaces and streams, several chunks (and vocabulary blocks)
+    # with G or P formed in a pass of their own (D > 2048), so the shared side
+    # stream is used: results equal the same calls made serially.
     import threading
 
     D = 2304
     probs = [synth.make_problem("tiny", seed=90 + i, prompts=2, G=4, T=256, D=D, V=3000,
                                 lengths=(64, 256)) for i in range(2)]
-    params = clp.make_params(chunk_tokens=512, flags=STORED)
+    params = _side_stream_params(clp, flags, probs[0].n_tokens, D, 3000, probs[0].seq_len)
 
     def args_of(p):
         base, _ = oracle.selective_logp(p.hidden, p.weight, p.ids.numpy())
