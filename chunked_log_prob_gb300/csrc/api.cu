@@ -95,9 +95,27 @@ struct Layout {
   bool need_acc;    // more than one vocab block -> fp32 dH accumulator
   double model_cost;  // modelled GEMM time of the plan in forward-tile times (0: no device)
   int nbox;         // stored path: 64-column boxes per row (their maxima are kept)
-  size_t off_pm, off_ps, off_zy, off_lse, off_g, off_rbl, off_lt, off_seq, off_G, off_bmax,
-      off_acc, total;
+  int sk_slots;     // stored path: pairs of the tail-split dH launches (0: no split)
+  size_t off_pm, off_ps, off_zy, off_lse, off_g, off_rbl, off_lt, off_seq, off_sk, off_G,
+      off_bmax, off_acc, total;
 };
+
+// Stored form: a dH launch whose last round has fewer units than SM pairs
+// splits that round's units between their own pairs and idle ones (the tail
+// split, see SkSplit in gemm_tc.cuh) when the vocabulary K loop is long enough
+// to cut and no G pass runs beside it. The pairs are the device's, at most kRefSms / ctas, so that the slot
+// region of the sizing without a device holds. The chunk planner models whole
+// rounds all the same: the split only makes a plan's last round shorter.
+int stored_sk_slots(int vocab, int ctas, int sms) {
+  if (cdiv(vocab, BK) < 2 * kSkMinStages) return 0;
+  return std::min(sms > 0 ? sms : kRefSms, kRefSms) / ctas;
+}
+
+// Bytes of the tail split's partial slots: two fp32 tiles of a unit per pair.
+size_t stored_sk_bytes(int sk_slots, int ctas) {
+  return static_cast<size_t>(2) * sk_slots * ctas * BM * (BN * dh_accumulators(ctas)) *
+         sizeof(float);
+}
 
 int auto_chunk_blocks(long long n_rb_total, int n_dt, int sms, int max_units) {
   // Row blocks per backward chunk: keep the dH GEMM's (row block x D tile)
@@ -369,6 +387,9 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, Form fo
   L->off_rbl = off; off = align_up(off + (L->nr / BM) * sizeof(int), 256);
   L->off_lt = off; off = align_up(off + L->nr * sizeof(double), 256);
   L->off_seq = off; off = align_up(off + L->nr * sizeof(int), 256);  // >= N / T lengths
+  L->sk_slots = L->stored ? stored_sk_slots(s->vocab, L->ctas, sms) : 0;
+  L->off_sk = off;
+  if (L->sk_slots > 0) off = align_up(off + stored_sk_bytes(L->sk_slots, L->ctas), 256);
   L->off_G = off;
 
   // Chunks are whole row units (BM * ctas rows: what one CTA pair covers).
@@ -681,7 +702,7 @@ struct Ws {
   int* n_nonempty;
   int* seq_lens;
   int* rb_list;
-  float *pm, *ps, *zy, *lse, *g, *acc;
+  float *pm, *ps, *zy, *lse, *g, *acc, *sk;
   __nv_bfloat16* G;
 };
 
@@ -704,6 +725,7 @@ Ws carve(void* ws, const Layout& L) {
   w.g = reinterpret_cast<float*>(w.base + L.off_g);
   w.G = reinterpret_cast<__nv_bfloat16*>(w.base + L.off_G);
   w.acc = reinterpret_cast<float*>(w.base + L.off_acc);
+  w.sk = L.sk_slots > 0 ? reinterpret_cast<float*>(w.base + L.off_sk) : nullptr;
   return w;
 }
 
@@ -904,6 +926,22 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
            (overlap ? static_cast<size_t>(c & 1) * L.nbox * L.chunk_rows : 0);
   };
   auto chunk_rbs = [&](int c) { return std::min(rb_per_chunk, n_rb_total - c * rb_per_chunk); };
+  // dH launches: with the tail split every pair of the launch takes part (the
+  // device decides from the active row blocks which units are cut), and a
+  // fixup pass adds the cut units' pieces. Without a mask every row block is
+  // active, so a unit count of whole rounds is known here to cut nothing. The
+  // overlapped schedule does without it: there the next chunk's G pass runs
+  // on the pairs that a dH launch's last round leaves idle (measured at the
+  // gpt-oss-20b head: the split made that pass 19 % slower and the call 0.5 %).
+  auto dh_grid = [&](long long units, bool split) {
+    return L.ctas * (split ? L.sk_slots : static_cast<int>(std::min<long long>(units, slots)));
+  };
+  auto sk_fixup = [&](const TileArgs& b, long long units) -> int {
+    if (b.sk_part == nullptr || (mask == nullptr && units % L.sk_slots == 0)) return GRPO_OK;
+    return launch_sk_fixup(L.ctas, b, static_cast<int>(units), st) == cudaSuccess
+               ? GRPO_OK
+               : GRPO_ERR_CUDA;
+  };
 
   // (1) logits of chunk c: online LSE partials, z_y, fp16 copy.
   auto fwds = [&](int c, int* splits_out) -> int {
@@ -1004,7 +1042,7 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
                : GRPO_ERR_CUDA;
   };
   // (3) dH rows of chunk c = G W over the whole vocabulary; (4) dW.
-  auto dh = [&](int c) -> int {
+  auto dh = [&](int c, bool split) -> int {
     const int n_rb = chunk_rbs(c);
     const int n_ru = static_cast<int>(cdiv(n_rb, L.ctas));
     CUtensorMap map_g;
@@ -1023,11 +1061,13 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     b.dH = static_cast<__nv_bfloat16*>(dH);
     b.first = 1;
     b.last = 1;
+    split = split && L.sk_slots > 0;
+    b.sk_part = split ? w.sk : nullptr;
+    b.sk_slots = split ? L.sk_slots : 0;
     const long long units = static_cast<long long>(n_ru) * n_dt_dh;
-    if (launch_dh_gemm(L.ctas, map_g, map_w_mn, b,
-                       L.ctas * static_cast<int>(std::min<long long>(units, slots)),
-                       st) != cudaSuccess)
+    if (launch_dh_gemm(L.ctas, map_g, map_w_mn, b, dh_grid(units, split), st) != cudaSuccess)
       return GRPO_ERR_CUDA;
+    if (const int rr = sk_fixup(b, units); rr != GRPO_OK) return rr;
     if (dW != nullptr)
       return launch_dw(hidden, reinterpret_cast<const __nv_bfloat16*>(sbuf(c)), L.ldS, 0, L.V,
                        c * rb_per_chunk, n_rb, dW, c == 0, L, w, sms, st);
@@ -1062,12 +1102,13 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     b.dH = static_cast<__nv_bfloat16*>(dH);
     b.first = 1;
     b.last = 1;
+    const bool split = L.sk_slots > 0;
+    b.sk_part = split ? w.sk : nullptr;
+    b.sk_slots = split ? L.sk_slots : 0;
     const long long units = static_cast<long long>(n_ru) * n_dt_dh;
-    return launch_dhs_gemm(L.ctas, map_s, map_w_mn, b,
-                           L.ctas * static_cast<int>(std::min<long long>(units, slots)),
-                           st) == cudaSuccess
-               ? GRPO_OK
-               : GRPO_ERR_CUDA;
+    if (launch_dhs_gemm(L.ctas, map_s, map_w_mn, b, dh_grid(units, split), st) != cudaSuccess)
+      return GRPO_ERR_CUDA;
+    return sk_fixup(b, units);
   };
 
   int r = GRPO_OK;
@@ -1085,7 +1126,7 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
       int splits = 1;
       r = fwds(c, &splits);
       if (r == GRPO_OK) r = gform(c, splits, st);
-      if (r == GRPO_OK) r = dh(c);
+      if (r == GRPO_OK) r = dh(c, true);
     }
   } else {
     std::lock_guard<std::mutex> side_lock(di->side_mu);
@@ -1110,7 +1151,7 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
       if (c + 1 < n_chunks) r = fwd_then_gform(c + 1);  // buffer (c+1)&1: free after dh(c-1)
       if (r != GRPO_OK) break;
       if (cudaStreamWaitEvent(st, di->ev_g[c & 1], 0) != cudaSuccess) return GRPO_ERR_CUDA;
-      r = dh(c);
+      r = dh(c, false);
     }
   }  // side_lock released: this call's records and waits are all enqueued
   if (r != GRPO_OK) return r;
@@ -1680,8 +1721,11 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
   const int grp = group_rows_exact(static_cast<int>(cdiv(n_rb, L.ctas)), slots);
   info->fwd_splits = std::min(std::max(1, slots / grp), std::min(L.nvt, kMaxSplits));
   info->launches_logp = L.n > 0 ? 2 : 0;
+  // The stored form's tail-split dH launches (a fused dH GEMM, or chunks that
+  // run one after another) are each followed by a fixup pass.
+  const bool tail_split = L.stored && L.sk_slots > 0 && (L.fused || L.n_sbuf == 1);
   info->launches_loss = L.n <= 0        ? 0
-                        : L.stored      ? 3 + 3 * info->n_chunks
+                        : L.stored      ? 3 + (tail_split ? 4 : 3) * info->n_chunks
                         : L.single_pass ? 3 + info->n_chunks * ((L.fused ? 2 : 3) * L.nvb + 1)
                                         : 4 + 2 * info->n_chunks * info->n_vocab_blocks;
   if (L.n > 0 && params != nullptr && (params->flags & GRPO_FLAG_SEQUENCE_MEAN) != 0)

@@ -3,8 +3,9 @@
 // gemm_tc.cuh): the G tile (recomputed logits -> bf16 softmax-Jacobian rows),
 // the dH accumulation from a G block or straight from a stored fp16 logit
 // block, the single pass's U accumulation, and the lm_head gradient, each in
-// the single-CTA and the CTA-pair variant. No kernel is defined here; the file
-// exists so that these instantiations compile in parallel with the others.
+// the single-CTA and the CTA-pair variant, and the fixup pass of the
+// tail-split dH launches. No kernel is defined here; the file exists so that these
+// instantiations compile in parallel with the others.
 #include "launch.h"
 
 namespace grpo {
@@ -49,6 +50,16 @@ cudaError_t launch_dhs_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMa
                             const TileArgs& args, int grid, cudaStream_t stream) {
   return ctas == 2 ? launch_gemm_variant<MODE_DHS, 2>(map_a, map_b, args, grid, stream)
                    : launch_gemm_variant<MODE_DHS, 1>(map_a, map_b, args, grid, stream);
+}
+
+cudaError_t launch_sk_fixup(int ctas, const TileArgs& args, int units, cudaStream_t stream) {
+  if (units <= 0) return cudaSuccess;
+  LaunchTimer timer("sk_fixup_kernel", stream);
+  if (ctas == 2)
+    sk_fixup_kernel<2><<<dim3(units, PairCfg<MODE_DH, 2>::kTileN / 32), BM * 2, 0, stream>>>(args);
+  else
+    sk_fixup_kernel<1><<<dim3(units, PairCfg<MODE_DH, 1>::kTileN / 32), BM, 0, stream>>>(args);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_uac_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,

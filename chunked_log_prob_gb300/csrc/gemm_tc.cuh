@@ -123,6 +123,13 @@ struct TileArgs {
   __nv_bfloat16* dH;     // [N][hidden] output, indexed by global row
   int first;
   int last;
+  // MODE_DH, MODE_DHS over the whole vocabulary (first and last): the tail
+  // split of the last round (see SkSplit). sk_part: 2 slots per SM pair of
+  // fp32 partial tiles, or null (units run whole, one per pair and round);
+  // sk_slots: the pairs of the launch (its grid / CTAS), which the fixup
+  // kernel must be given too.
+  float* sk_part;
+  int sk_slots;
   int* status;
 };
 
@@ -344,6 +351,253 @@ __device__ __forceinline__ int mn_out_cols(const TileArgs& a, int col0) {
   return w <= 0 ? 0 : min(BN, (w + q - 1) / q * q);
 }
 
+// ---------------------------------------------------------------------------
+// Tail split of a dH launch (MODE_DH, MODE_DHS over the whole vocabulary).
+// Its units (row unit x hidden tile) each run a K loop over the vocabulary,
+// and the pairs run them whole, one per pair and round. When the last round
+// has fewer units (U) than pairs, the pairs without one would idle (66 units
+// on 76 pairs: 13 % of the launch). Instead, each of those U units runs on its
+// own pair only up to a balance point m of its K loop (its main piece), and Q
+// of the idle pairs share the units' tails [m, K) among them, laid end to end
+// in unit order and cut at K-stage boundaries, so that every pair of the round
+// does about the same work. The U main pieces all start at K = 0 together and
+// the tails all lie in the last part of the vocabulary: at any moment the
+// pairs read W and the logit rows from two narrow K windows, which stay in L2
+// (cuts at arbitrary K offsets, one contiguous share of all units per pair,
+// left every pair at its own place in the vocabulary and made the launch
+// DRAM-bound). Q is at most a third of the pairs, whose tail reads may come
+// from DRAM. Each cut piece leaves its fp32 partial tile in a slot of its own;
+// sk_fixup_kernel adds a unit's pieces in a fixed order (the main piece, then
+// the tails in pair order), so the result does not depend on timing.
+constexpr int kSkMinStages = 64;  // least K stages of full width per tail pair
+// What a cut piece costs beyond its stages (its partial tile leaves TMEM
+// before the next piece's MMAs can start, and the pipeline refills), in cost
+// units: about 8 full-width stages (6 us per piece measured on GB300 against
+// 0.7 us per stage).
+constexpr int kSkPieceCost = 8 * 4;
+
+struct SkSplit {
+  int w_dp;          // units [0, w_dp) run whole, round-robin (the whole rounds)
+  int n_main;        // U: units of the last round; pair p < U runs unit w_dp + p
+  int n_tail;        // Q: pairs U .. U+Q-1 share the tails; 0: no split
+  int k;             // K stages of a unit
+  int cs_f, cs_l;    // cost per stage: units of the other tiles, of the last tile
+  int m_f, m_l;      // main stages of each
+  long long t_f, t_l;   // tail cost of each
+  long long tail_total;
+};
+
+// MMA column blocks (of 64 columns per CTA) per K stage of a dH unit of
+// hidden tile `col`: its cost per stage.
+template <int CTAS>
+__device__ __forceinline__ int sk_blocks(const TileArgs& a, int col) {
+  constexpr int kNAcc = CTAS == 2 ? 2 : 1;
+  int b = 0;
+#pragma unroll
+  for (int na = 0; na < kNAcc; ++na)
+    b += mn_out_cols<CTAS>(a, col * (BN * kNAcc) + na * BN) / (64 * CTAS);
+  return b;
+}
+
+// Units in [u0, u1) of the last hidden tile, in the raster order of
+// decode_unit (groups of group_rows row units, tile-major within a group).
+__device__ __forceinline__ int sk_count_last(const TileArgs& a, int n_ru, int u0, int u1) {
+  if (u1 <= u0) return 0;
+  const int per_group = a.group_rows * a.n_cols;
+  int n = 0;
+  for (int g = u0 / per_group; g * per_group < u1; ++g) {
+    const int rig = min(a.group_rows, n_ru - g * a.group_rows);
+    const int lo = g * per_group + (a.n_cols - 1) * rig, hi = lo + rig;
+    n += max(0, min(hi, u1) - max(lo, u0));
+  }
+  return n;
+}
+
+template <int CTAS>
+__device__ __forceinline__ SkSplit sk_split(const TileArgs& a, int n_ru, int n_units, int slots) {
+  SkSplit s;
+  s.w_dp = n_units;
+  s.n_main = 0;
+  s.n_tail = 0;
+  s.k = a.k_iters;
+  s.cs_f = s.cs_l = 1;
+  s.m_f = s.m_l = a.k_iters;
+  s.t_f = s.t_l = 0;
+  s.tail_total = 0;
+  const int rem = slots > 0 ? n_units % slots : 0;
+  if (a.sk_part == nullptr || !a.first || !a.last || rem == 0 || a.k_iters < 2 * kSkMinStages)
+    return s;
+  const int U = rem;
+  const int w_dp = n_units - rem;
+  const int k = a.k_iters;
+  s.cs_f = sk_blocks<CTAS>(a, 0);
+  s.cs_l = sk_blocks<CTAS>(a, a.n_cols - 1);
+  const int n_l = a.n_cols == 1 ? U : sk_count_last(a, n_ru, w_dp, n_units);
+  const int n_f = U - n_l;
+  if (a.n_cols == 1) s.cs_f = s.cs_l;
+  const long long c_f = static_cast<long long>(k) * s.cs_f, c_l = static_cast<long long>(k) * s.cs_l;
+  const long long total = n_f * c_f + n_l * c_l;
+  const long long min_cost = static_cast<long long>(kSkMinStages) * 4;
+  const int Q = static_cast<int>(min(static_cast<long long>(min(slots - U, slots / 3)),
+                                     total / min_cost - U));
+  if (Q <= 0) return s;
+  // Balance: every pair of the round takes about T of cost, the tail pairs'
+  // pieces (about (U + Q) / Q each) counted with their overhead. A unit
+  // cheaper than T (a narrow last tile) keeps no tail.
+  const long long ovh = kSkPieceCost;
+  long long T = (total + (U + Q) * ovh + U + Q - 1) / (U + Q);
+  if (T > c_l && n_f > 0)
+    T = max(c_l, (n_f * c_f + (n_f + Q) * ovh + n_f + Q - 1) / (n_f + Q));
+  // No gain unless the round gets shorter by more than the pieces cost.
+  if (T + 2 * ovh >= c_f) return s;
+  s.m_f = static_cast<int>(min(static_cast<long long>(k), T / s.cs_f));
+  s.m_l = static_cast<int>(min(static_cast<long long>(k), T / s.cs_l));
+  s.t_f = static_cast<long long>(k - s.m_f) * s.cs_f;
+  s.t_l = static_cast<long long>(k - s.m_l) * s.cs_l;
+  s.tail_total = n_f * s.t_f + n_l * s.t_l;
+  if (s.tail_total == 0) return s;
+  s.w_dp = w_dp;
+  s.n_main = U;
+  s.n_tail = Q;
+  return s;
+}
+
+__device__ __forceinline__ bool sk_is_last(const TileArgs& a, int n_ru, int u) {
+  int ru, col;
+  decode_unit(u, n_ru, a.n_cols, a.group_rows, ru, col);
+  return col == a.n_cols - 1;
+}
+
+// Tail cost of the last round's units before u.
+__device__ __forceinline__ long long sk_tail_prefix(const TileArgs& a, int n_ru, const SkSplit& s,
+                                                    int u) {
+  const int nl = sk_count_last(a, n_ru, s.w_dp, u);
+  return static_cast<long long>(u - s.w_dp - nl) * s.t_f + static_cast<long long>(nl) * s.t_l;
+}
+
+// First tail cost of tail pair q (q = n_tail: the end).
+__device__ __forceinline__ long long sk_tail_start(const SkSplit& s, int q) {
+  return s.tail_total * q / s.n_tail;
+}
+
+// The tail pair whose share holds tail cost x (0 <= x < tail_total).
+__device__ __forceinline__ int sk_tail_pair_of(const SkSplit& s, long long x) {
+  int q = static_cast<int>(x * s.n_tail / s.tail_total);
+  q = min(max(q, 0), s.n_tail - 1);
+  while (q + 1 < s.n_tail && sk_tail_start(s, q + 1) <= x) ++q;
+  while (q > 0 && sk_tail_start(s, q) > x) --q;
+  return q;
+}
+
+// The last unit u of the last round with tail prefix <= x.
+__device__ __forceinline__ int sk_tail_unit_at(const TileArgs& a, int n_ru, const SkSplit& s,
+                                               int lo, long long x) {
+  int hi = s.w_dp + s.n_main - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (sk_tail_prefix(a, n_ru, s, mid) <= x) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Stages [kb, ke) of unit u's tail that tail pair q runs (kb >= ke: none).
+__device__ __forceinline__ void sk_tail_piece(const TileArgs& a, int n_ru, const SkSplit& s, int q,
+                                              int u, int& kb, int& ke) {
+  const bool last = sk_is_last(a, n_ru, u);
+  const int cs = last ? s.cs_l : s.cs_f;
+  const int m = last ? s.m_l : s.m_f;
+  const long long t = last ? s.t_l : s.t_f;
+  const long long p0 = sk_tail_prefix(a, n_ru, s, u);
+  const long long q0 = sk_tail_start(s, q), q1 = sk_tail_start(s, q + 1);
+  kb = m + static_cast<int>((max(q0, p0) - p0) / cs);
+  ke = m + static_cast<int>((min(q1, p0 + t) - p0) / cs);
+}
+
+// Slot of a cut piece: main pieces 0 .. U-1, tail pieces U + (u - w_dp) + q
+// (unique: along the units in order and the tail pairs in order, u + q grows).
+__device__ __forceinline__ int sk_main_slot(const SkSplit& s, int u) { return u - s.w_dp; }
+__device__ __forceinline__ int sk_tail_slot(const SkSplit& s, int u, int q) {
+  return s.n_main + (u - s.w_dp) + q;
+}
+
+// One work item of a pair: unit u over K stages [kb, ke). A cut piece (not the
+// whole K range) writes its fp32 partial tile to slot `slot` instead of dH.
+struct WorkItem {
+  int u, kb, ke, slot;
+  bool cut;
+  // A piece of the split that rounding left without stages: no role touches it.
+  __device__ __forceinline__ bool empty() const { return slot >= 0 && ke <= kb; }
+};
+
+// The work items of one pair, in order: its round-robin units, then its main
+// piece or its tail pieces of the last round.
+template <int CTAS>
+struct WorkList {
+  SkSplit s;
+  int slot, n_slots, n_dp;
+  int n_extra;       // items after the round-robin ones
+  int u_first;       // tail pair: first unit whose tail it meets
+  int q;             // tail pair index, or -1 (main pair or none)
+
+  __device__ __forceinline__ void init(const TileArgs& a, int n_ru, int n_units, int slot_,
+                                       int n_slots_, bool dh_mode) {
+    slot = slot_;
+    n_slots = n_slots_;
+    n_extra = 0;
+    u_first = 0;
+    q = -1;
+    s = sk_split<CTAS>(a, n_ru, dh_mode ? n_units : 0, n_slots);
+    if (!dh_mode) s.w_dp = n_units;
+    if (s.n_tail > 0) {
+      if (slot < s.n_main) {
+        n_extra = 1;
+      } else if (slot < s.n_main + s.n_tail) {
+        q = slot - s.n_main;
+        const long long x0 = sk_tail_start(s, q), x1 = sk_tail_start(s, q + 1);
+        u_first = sk_tail_unit_at(a, n_ru, s, s.w_dp, x0);
+        const int u_last = sk_tail_unit_at(a, n_ru, s, u_first, x1 - 1);
+        n_extra = u_last - u_first + 1;
+      }
+    }
+    n_dp = slot < s.w_dp ? (s.w_dp - slot + n_slots - 1) / n_slots : 0;
+  }
+
+  // Item i (false past the end).
+  __device__ __forceinline__ bool get(const TileArgs& a, int n_ru, int k_iters, int i,
+                                      WorkItem& w) const {
+    if (i < n_dp) {
+      w.u = slot + i * n_slots;
+      w.kb = 0;
+      w.ke = k_iters;
+      w.slot = -1;
+      w.cut = false;
+      return true;
+    }
+    const int j = i - n_dp;
+    if (j >= n_extra) return false;
+    if (q < 0) {  // main piece
+      w.u = s.w_dp + slot;
+      w.kb = 0;
+      w.ke = sk_is_last(a, n_ru, w.u) ? s.m_l : s.m_f;
+      w.slot = sk_main_slot(s, w.u);
+    } else {
+      w.u = u_first + j;
+      sk_tail_piece(a, n_ru, s, q, w.u, w.kb, w.ke);
+      w.slot = sk_tail_slot(s, w.u, q);
+    }
+    w.cut = w.kb != 0 || w.ke != k_iters;
+    return true;
+  }
+};
+
+// fp32 partial tile of slot `slot`, CTA `rank`: [32-column chunk][8][BM rows][4],
+// so that a warp's 32 rows write (and the fixup reads) 512 contiguous bytes.
+__device__ __forceinline__ float* sk_slot_ptr(const TileArgs& a, int slot, int rank, int ctas,
+                                              int tile_n) {
+  return a.sk_part + (static_cast<long long>(slot) * ctas + rank) * (static_cast<long long>(BM) * tile_n);
+}
+
 // One TMA box into this CTA's stage; its bytes are counted on the leader's
 // barrier (pair) or this CTA's own.
 template <int CTAS>
@@ -436,6 +690,9 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
   const int n_units = n_ru * args.n_cols;
   // Stages per tile (k_iters counts 64-wide K slices; a stage holds kKSub).
   const int k_iters = ((MODE == MODE_DW ? n_rb * (BM / BK) : args.k_iters) + C::kKSub - 1) / C::kKSub;
+  // This pair's units, and with a tail split its part of the last round.
+  WorkList<CTAS> wl;
+  wl.init(args, n_ru, n_units, cta_slot, n_slots, MODE == MODE_DH || MODE == MODE_DHS);
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
@@ -443,9 +700,12 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
       uint32_t it = 0;
       bool ok = true;
       const uint64_t pol_a = policy_evict_last();
-      for (int u = cta_slot; u < n_units && ok; u += n_slots) {
+      for (int i = 0; ok; ++i) {
+        WorkItem wk;
+        if (!wl.get(args, n_ru, k_iters, i, wk)) break;
+        if (wk.empty()) continue;
         int ru, col, t0, t1;
-        decode_unit(u, n_ru, args.n_cols, args.group_rows, ru, col);
+        decode_unit(wk.u, n_ru, args.n_cols, args.group_rows, ru, col);
         unit_tiles<MODE>(args, col, t0, t1);
         // A CTA whose row block lies past the list computes its partner's rows
         // again and stores nothing.
@@ -464,7 +724,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             nbox[na] = mn_out_cols<CTAS>(args, t * C::kTileN + na * BN) / (64 * CTAS);
             b_bytes += static_cast<uint32_t>(nbox[na]) * (BK * 64 * 2);
           }
-          for (int k = 0; k < k_iters; ++k, ++it) {
+          for (int k = wk.kb; k < wk.ke; ++k, ++it) {
             const int s = it % kStages;
             const uint32_t round = it / kStages;
             if (!mbar_wait(&empty_bar[s], (round & 1u) ^ 1u, abort_flag, args.status)) {
@@ -575,9 +835,12 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
       constexpr bool kMnOut = is_dh(MODE) || MODE == MODE_DW;  // B MN-major, N = hidden
       uint32_t it = 0, tile_it = 0;
       bool ok = true;
-      for (int u = cta_slot; u < n_units && ok; u += n_slots) {
+      for (int i = 0; ok; ++i) {
+        WorkItem wk;
+        if (!wl.get(args, n_ru, k_iters, i, wk)) break;
+        if (wk.empty()) continue;
         int ru, col, t0, t1;
-        decode_unit(u, n_ru, args.n_cols, args.group_rows, ru, col);
+        decode_unit(wk.u, n_ru, args.n_cols, args.group_rows, ru, col);
         unit_tiles<MODE>(args, col, t0, t1);
         for (int t = t0; t < t1 && ok; ++t, ++tile_it) {
           const uint32_t buf = tile_it % C::kNBuf;
@@ -595,7 +858,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             const int n = kMnOut ? mn_out_cols<CTAS>(args, t * C::kTileN + na * BN) : BN;
             idesc[na] = n == 0 ? 0u : idesc_bf16(BM * CTAS, n, MODE == MODE_DW, kMnOut);
           }
-          for (int k = 0; k < k_iters; ++k, ++it) {
+          for (int k = wk.kb; k < wk.ke; ++k, ++it) {
             const int s = it % kStages;
             const uint32_t round = it / kStages;
             if (!mbar_wait(&full_bar[s], round & 1u, abort_flag, args.status)) {
@@ -629,7 +892,8 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
               } else {
                 bdesc = sdesc_sw128(b_sl + kk * 32, 16, 1024);
               }
-              const uint32_t acc = (k | kq) != 0 ? 1u : 0u;  // first MMA of the tile overwrites
+              // The first MMA of the tile (or piece) overwrites the accumulator.
+              const uint32_t acc = (k != wk.kb || kq != 0) ? 1u : 0u;
 #pragma unroll
               for (int na = 0; na < C::kNAcc; ++na) {
                 // Accumulator na: B columns na*256.. (its own B boxes), TMEM columns na*256..
@@ -670,9 +934,12 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
     // kTmaStore: this warp's two staging buffers and the boxes it has stored.
     uint8_t* const stage_out = smem + C::kStages * C::kStageBytes + q * 2 * C::kStoreBufBytes;
     uint32_t n_stores = 0;
-    for (int u = cta_slot; u < n_units && ok; u += n_slots) {
+    for (int i = 0; ok; ++i) {
+      WorkItem wk;
+      if (!wl.get(args, n_ru, k_iters, i, wk)) break;
+      if (wk.empty()) continue;
       int ru, col, t0, t1;
-      decode_unit(u, n_ru, args.n_cols, args.group_rows, ru, col);
+      decode_unit(wk.u, n_ru, args.n_cols, args.group_rows, ru, col);
       unit_tiles<MODE>(args, col, t0, t1);
       const int li = ru * CTAS + static_cast<int>(rank);
       const bool block_ok = li < n_rb;
@@ -759,19 +1026,19 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
         constexpr int kPre = 4;
         const float* bm = args.box_max + lrow;
         auto box_max_of = [&](int k) {
-          return (!rc.zero && k < k_iters) ? __ldg(bm + static_cast<long long>(k) * args.ldM)
-                                           : 0.f;
+          return (!rc.zero && k < wk.ke) ? __ldg(bm + static_cast<long long>(k) * args.ldM)
+                                         : 0.f;
         };
         float zc[kPre], zn[kPre];
 #pragma unroll
-        for (int j = 0; j < kPre; ++j) zc[j] = box_max_of(j);
-        for (int k0 = 0; k0 < k_iters && ok; k0 += kPre) {
+        for (int j = 0; j < kPre; ++j) zc[j] = box_max_of(wk.kb + j);
+        for (int k0 = wk.kb; k0 < wk.ke && ok; k0 += kPre) {
 #pragma unroll
           for (int j = 0; j < kPre; ++j) zn[j] = box_max_of(k0 + kPre + j);
 #pragma unroll
           for (int j = 0; j < kPre; ++j) {
             const int k = k0 + j;
-            if (k >= k_iters || !ok) break;
+            if (k >= wk.ke || !ok) break;
             const int s = static_cast<int>(cit % kStages);
             if (!mbar_wait(&afull_bar[s], (cit / kStages) & 1u, abort_flag, args.status)) {
               ok = false;
@@ -1171,6 +1438,19 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             if (d0 >= args.hidden) break;  // warp-uniform
             float v[32];
             tmem_ld32(tbase + c * 32, v);
+            if (wk.cut) {
+              // A piece of a split unit: its fp32 partial tile goes to its slot.
+              if (valid) {
+                float* sp = sk_slot_ptr(args, wk.slot, static_cast<int>(rank), CTAS, C::kTileN) +
+                            (c * 8 * BM + lrow_in_tile) * 4;
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj)
+                  st_global_v4(sp + jj * BM * 4, __float_as_uint(v[4 * jj]),
+                               __float_as_uint(v[4 * jj + 1]), __float_as_uint(v[4 * jj + 2]),
+                               __float_as_uint(v[4 * jj + 3]));
+              }
+              continue;
+            }
             if (valid) {
               float* accp = args.acc + static_cast<long long>(lrow) * args.hidden + d0;
               __nv_bfloat16* outp =
@@ -1229,6 +1509,96 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
   if (warp == 1) {
     if (CTAS == 2) tmem_dealloc_pair(tmem_base, TMEM_COLS);
     else tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// Adds the pieces of every dH unit that the tail split cut (see SkSplit) in a
+// fixed order, its main piece and then its tails in pair order, and writes the
+// unit's bf16 dH rows. Grid: (the launch's host-side bound on units) x (32-
+// column chunks of a unit); one thread per row of the unit. Units that ran
+// whole return at once. `a` is the dH launch's own TileArgs.
+template <int CTAS>
+__global__ void __launch_bounds__(BM * CTAS) sk_fixup_kernel(const TileArgs a) {
+  constexpr int kTileN = PairCfg<MODE_DH, CTAS>::kTileN;
+  __shared__ SkSplit sp_sh;
+  __shared__ long long p0_sh;
+  const int n_rb = launch_row_blocks(a);
+  const int n_ru = (n_rb + CTAS - 1) / CTAS;
+  const int n_units = n_ru * a.n_cols;
+  const int u = static_cast<int>(blockIdx.x);
+  // Only units of a last round with fewer units than pairs can be cut.
+  if (a.sk_slots <= 0 || u >= n_units || u < n_units - n_units % a.sk_slots) return;
+  int ru, col;
+  decode_unit(u, n_ru, a.n_cols, a.group_rows, ru, col);
+  const int c = static_cast<int>(blockIdx.y);
+  const int d0 = col * kTileN + c * 32;
+  if (d0 >= a.hidden) return;
+  if (threadIdx.x == 0) {
+    sp_sh = sk_split<CTAS>(a, n_ru, n_units, a.sk_slots);
+    p0_sh = sp_sh.n_tail > 0 ? sk_tail_prefix(a, n_ru, sp_sh, u) : 0;
+  }
+  __syncthreads();
+  const SkSplit& sp = sp_sh;
+  if (sp.n_tail == 0) return;
+  const bool last = col == a.n_cols - 1;
+  const int m = last ? sp.m_l : sp.m_f;
+  const int cs = last ? sp.cs_l : sp.cs_f;
+  const long long t = last ? sp.t_l : sp.t_f;
+  if (t == 0) return;  // the main piece was the whole unit
+  const long long p0 = p0_sh;
+  const int qa = sk_tail_pair_of(sp, p0);
+  const int qb = sk_tail_pair_of(sp, p0 + t - 1);
+  // Stages of tail pair q's piece of this unit (as sk_tail_piece).
+  auto piece = [&](int q, int& kb, int& ke) {
+    const long long q0 = sk_tail_start(sp, q), q1 = sk_tail_start(sp, q + 1);
+    kb = m + static_cast<int>((max(q0, p0) - p0) / cs);
+    ke = m + static_cast<int>((min(q1, p0 + t) - p0) / cs);
+  };
+  if (m == 0) {
+    // No main piece: a single tail piece then covered the whole unit.
+    int n = 0;
+    for (int q = qa; q <= qb; ++q) {
+      int kb, ke;
+      piece(q, kb, ke);
+      n += ke > kb;
+    }
+    if (n <= 1) return;
+  }
+
+  const int rank = static_cast<int>(threadIdx.x) / BM;
+  const int lrow = static_cast<int>(threadIdx.x) % BM;
+  const int li = ru * CTAS + rank;
+  if (li >= n_rb) return;
+  const long long grow = static_cast<long long>(global_rb(a, li)) * BM + lrow;
+  if (grow >= a.n_total) return;
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = 0.f;
+  auto add_slot = [&](int slot) {
+    const float* src = sk_slot_ptr(a, slot, rank, CTAS, kTileN) + (c * 8 * BM + lrow) * 4;
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const float4 x = *reinterpret_cast<const float4*>(src + jj * BM * 4);
+      v[4 * jj] += x.x;
+      v[4 * jj + 1] += x.y;
+      v[4 * jj + 2] += x.z;
+      v[4 * jj + 3] += x.w;
+    }
+  };
+  if (m > 0) add_slot(sk_main_slot(sp, u));
+  for (int q = qa; q <= qb; ++q) {
+    int kb, ke;
+    piece(q, kb, ke);
+    if (ke > kb) add_slot(sk_tail_slot(sp, u, q));
+  }
+  __nv_bfloat16* out = a.dH + grow * a.hidden + d0;
+#pragma unroll
+  for (int j8 = 0; j8 < 4; ++j8) {
+    if (d0 + j8 * 8 >= a.hidden) break;
+    st_global_v4(out + j8 * 8, pack_bf16x2(v[j8 * 8], v[j8 * 8 + 1]),
+                 pack_bf16x2(v[j8 * 8 + 2], v[j8 * 8 + 3]),
+                 pack_bf16x2(v[j8 * 8 + 4], v[j8 * 8 + 5]),
+                 pack_bf16x2(v[j8 * 8 + 6], v[j8 * 8 + 7]));
   }
 }
 

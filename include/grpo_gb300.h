@@ -99,7 +99,12 @@ typedef struct grpo_shape {
  * grpo_params.flags bit: backward without a second logit GEMM. Per chunk of
  * rows, the forward GEMM also keeps the chunk's (transformed) logits in fp16
  * in the workspace, and the dH GEMM runs over the whole vocabulary once lse
- * and g are known. Each 64-column box of a row is stored relative to its own
+ * and g are known. When the last round of a dH launch has fewer units (256
+ * rows x 512 hidden columns) than the device has SM pairs, and no G pass runs
+ * beside it, idle pairs take over the tails of that round's vocabulary loops;
+ * a fixup pass adds the pieces in a fixed order (results do not depend on
+ * timing). Its fp32 partial tiles take a fixed 76 MiB of the workspace (38 MiB
+ * with GRPO_FLAG_SINGLE_CTA; vocabularies of at least 8129 columns). Each 64-column box of a row is stored relative to its own
  * maximum (kept beside it in fp32), so any finite logit is stored without
  * overflow and the box's largest terms keep fp16's finest spacing. The logits
  * are turned into G in one of two ways:
@@ -247,7 +252,9 @@ typedef struct grpo_plan_info {
   int32_t fwd_splits;        /* forward vocab splits (partials per row)      */
   int32_t launches_logp;     /* kernel launches of one grpo_logp_fwd call    */
   int32_t launches_loss;     /* kernel launches of one grpo_loss_fwd_bwd
-                                (with a mask; one fewer without)          */
+                                with a mask (without one: one fewer, and
+                                no fixup pass after a dH launch whose
+                                units fill whole rounds of the SM pairs)  */
   int32_t g_in_dh_gemm;      /* 1: the stored-logit backward forms G (the
                                 single pass P) inside the dH-type GEMM
                                 (hidden <= 2048; not with dW); 0: in a

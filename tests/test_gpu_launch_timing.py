@@ -43,10 +43,14 @@ def _call(clp, p, old, params, ws):
     return loss.item(), logp.cpu(), dH.cpu()
 
 
-@pytest.mark.parametrize("D, want_g", [(2304, "finalize_gform_kernel"),
-                                       (1536, "finalize_rows_kernel")])
-def test_timing_records_every_launch_of_a_call(clp, D, want_g):
-    p, old = _problem(D)
+@pytest.mark.parametrize("D, V, want_g", [(2304, 3000, "finalize_gform_kernel"),
+                                          (1536, 3000, "finalize_rows_kernel"),
+                                          (1536, 9000, "sk_fixup_kernel")])
+def test_timing_records_every_launch_of_a_call(clp, D, V, want_g):
+    # V = 9000: a vocabulary loop long enough for the tail split, so the fused
+    # dH launch (at most 8 pair row units x 3 hidden tiles, fewer than the SM
+    # pairs) is followed by its fixup pass.
+    p, old = _problem(D, V=V)
     params = clp.make_params(flags=STORED)
     ws = clp.alloc_workspace(p.n_tokens, D, p.vocab, p.seq_len, params, DEV)
     plan = clp.grpo_get_plan(p.n_tokens, D, p.vocab, p.seq_len, params)
