@@ -108,7 +108,7 @@ def test_tail_split_against_oracle(clp, name, prompts, G, T, D, V, lengths, flag
 
 def test_tail_split_whole_rounds_then_a_split_round(clp):
     # 20 row units x 8 hidden tiles = 160 units on 76 pairs: units 0..151 run
-    # whole in two rounds, the last 8 are split with 25 tail pairs. The oracle
+    # whole in two rounds, the last 8 are split with 9 tail pairs. The oracle
     # checks a seeded sample of rows (each row's dH depends on that row alone,
     # given the loss denominator), among them the first and last rows.
     p = synth.make_problem("tiny", seed=7, prompts=1, G=4, T=1280, D=4096, V=9000,
@@ -162,3 +162,39 @@ def test_tail_split_whole_rounds_without_a_mask(clp):
     got_dh = dH[torch.from_numpy(rows).to(DEV)].double().cpu().numpy()
     rel_dh = np.linalg.norm(got_dh - want["dH"]) / np.linalg.norm(want["dH"])
     assert rel_dh <= DH_RTOL
+
+
+def test_tail_split_with_the_lm_head_gradient(clp):
+    # With dW the stored form forms G in a pass of its own and the dW GEMM reads
+    # the same G block after the dH launch, its tail split and the fixup (one
+    # chunk: the unoverlapped schedule). 2 pair row units x 3 hidden tiles = 6
+    # units, cut with 11 tail pairs (tail shares of at least 64 full stages).
+    p = synth.make_problem("tiny", seed=11, prompts=1, G=4, T=128, D=1536, V=12000,
+                           lengths=(40, 128))
+    base, _ = oracle.selective_logp(p.hidden, p.weight, p.ids.numpy())
+    old, ref = p.old_ref(torch.from_numpy(np.asarray(base)))
+    want = oracle.loss_fwd_bwd(p.hidden, p.weight, p.ids.numpy(), p.mask.numpy(), old, ref,
+                               p.adv, p.seq_len, p.eps_low, p.eps_high, p.beta)
+    want_dW = oracle.grad_weight(p.hidden, p.weight, p.ids.numpy(), want["g"])
+    dev = torch.device(DEV)
+    params = clp.make_params(flags=STORED)
+    ws = clp.alloc_workspace(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, params, dev)
+    outs = []
+    for _ in range(2):
+        dW = torch.full((p.vocab, p.hidden_size), float("nan"), device=dev)
+        loss, logp, dH, dW = clp.grpo_loss_fwd_bwd(
+            p.hidden.to(dev), p.weight.to(dev), p.ids.to(dev), p.mask.to(dev), old.to(dev),
+            ref.to(dev), p.adv.to(dev), p.seq_len, params=params, workspace=ws, dW=dW)
+        assert clp.grpo_read_device_status(ws) == 0
+        outs.append((loss.item(), logp.cpu(), dH.cpu(), dW.cpu()))
+    L, logp, dH, dW = outs[0]
+    m = p.mask.numpy().astype(bool)
+    dh = dH.double().numpy()
+    rel_dh = np.linalg.norm(dh[m] - want["dH"][m]) / np.linalg.norm(want["dH"][m])
+    rel_dw = np.linalg.norm(dW.double().numpy() - want_dW) / np.linalg.norm(want_dW)
+    print(f"with dW: rel_dH={rel_dh:.3e} rel_dW={rel_dw:.3e}")
+    assert np.abs(logp.double().numpy() - want["logp"]).max() <= LOGP_TOL
+    assert abs(L - want["L"]) / abs(want["L"]) <= LOSS_RTOL
+    assert rel_dh <= DH_RTOL and rel_dw <= DH_RTOL and np.all(dh[~m] == 0.0)
+    L2, logp2, dH2, dW2 = outs[1]
+    assert L2 == L and torch.equal(dH2, dH) and torch.equal(logp2, logp)
