@@ -100,19 +100,21 @@ struct Layout {
       off_bmax, off_acc, total;
 };
 
-// Stored form: a dH launch whose last round has fewer units than SM pairs
-// splits that round's units between their own pairs and idle ones (the tail
-// split, see SkSplit in gemm_tc.cuh) when the vocabulary K loop is long enough
-// to cut and no G pass runs beside it. The pairs are the device's, at most kRefSms / ctas, so that the slot
-// region of the sizing without a device holds. The chunk planner models whole
-// rounds all the same: the split only makes a plan's last round shorter.
-int stored_sk_slots(int vocab, int ctas, int sms) {
-  if (cdiv(vocab, BK) < 2 * kSkMinStages) return 0;
+// Tail split (see SkSplit in gemm_tc.cuh): a dH-type launch whose last round
+// has fewer units than SM pairs splits that round's units between their own
+// pairs and idle ones, when its K loop (the vocabulary, or the single pass's
+// vocabulary block) is long enough to cut and nothing runs beside it. The
+// stored form and the single pass with P formed on chip reserve its slots. The
+// pairs are the device's, at most kRefSms / ctas, so that the slot region of
+// the sizing without a device holds. The chunk planner models whole rounds all
+// the same: the split only makes a launch's last round shorter.
+int tail_split_slots(int k_cols, int ctas, int sms) {
+  if (cdiv(k_cols, BK) < 2 * kSkMinStages) return 0;
   return std::min(sms > 0 ? sms : kRefSms, kRefSms) / ctas;
 }
 
 // Bytes of the tail split's partial slots: two fp32 tiles of a unit per pair.
-size_t stored_sk_bytes(int sk_slots, int ctas) {
+size_t tail_split_bytes(int sk_slots, int ctas) {
   return static_cast<size_t>(2) * sk_slots * ctas * BM * (BN * dh_accumulators(ctas)) *
          sizeof(float);
 }
@@ -387,9 +389,16 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, Form fo
   L->off_rbl = off; off = align_up(off + (L->nr / BM) * sizeof(int), 256);
   L->off_lt = off; off = align_up(off + L->nr * sizeof(double), 256);
   L->off_seq = off; off = align_up(off + L->nr * sizeof(int), 256);  // >= N / T lengths
-  L->sk_slots = L->stored ? stored_sk_slots(s->vocab, L->ctas, sms) : 0;
+  // Tail-split slots: stored form, single pass with P on chip; not under a
+  // budget they would take more than an eighth of.
+  const size_t budget = workspace_budget(p);
+  L->sk_slots = L->stored ? tail_split_slots(s->vocab, L->ctas, sms)
+                : form == kFormSinglePass ? tail_split_slots(static_cast<int>(L->vblock), L->ctas, sms)
+                                          : 0;
+  if (L->sk_slots > 0 && budget > 0 && tail_split_bytes(L->sk_slots, L->ctas) * 8 > budget)
+    L->sk_slots = 0;
   L->off_sk = off;
-  if (L->sk_slots > 0) off = align_up(off + stored_sk_bytes(L->sk_slots, L->ctas), 256);
+  if (L->sk_slots > 0) off = align_up(off + tail_split_bytes(L->sk_slots, L->ctas), 256);
   L->off_G = off;
 
   // Chunks are whole row units (BM * ctas rows: what one CTA pair covers).
@@ -410,7 +419,6 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, Form fo
   long long max_units = L->stored        ? std::max(1, stored_max_blocks(L->ldS, sbufs) / L->ctas)
                         : L->single_pass ? kMaxSinglePassChunkBlocks / L->ctas
                                          : kMaxAutoChunkBlocks / L->ctas;
-  const size_t budget = workspace_budget(p);
   if (budget > 0) {
     const long long fit =
         budget > off + 512 ? static_cast<long long>((budget - off - 512) / unit_bytes) : 0;
@@ -938,7 +946,7 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
   };
   auto sk_fixup = [&](const TileArgs& b, long long units) -> int {
     if (b.sk_part == nullptr || (mask == nullptr && units % L.sk_slots == 0)) return GRPO_OK;
-    return launch_sk_fixup(L.ctas, b, static_cast<int>(units), st) == cudaSuccess
+    return launch_sk_fixup(L.ctas, b, static_cast<int>(units), false, st) == cudaSuccess
                ? GRPO_OK
                : GRPO_ERR_CUDA;
   };
@@ -1323,8 +1331,10 @@ int run_single_pass(const void* hidden, const void* W, const int32_t* ids, const
     return launch_finalize_rows(f, chunk_rbs(c) * BM, st) == cudaSuccess ? GRPO_OK
                                                                           : GRPO_ERR_CUDA;
   };
-  // (4) U (+)= P W[block]; dH on the chunk's last block.
-  auto uacc = [&](int i) -> int {
+  // (4) U (+)= P W[block]; dH on the chunk's last block. With the tail split
+  // (split: nothing runs beside the launch) a fixup pass applies the U update
+  // to the units it cut.
+  auto uacc = [&](int i, bool split) -> int {
     const int c = i / L.nvb, b = i % L.nvb;
     const int n_rb = chunk_rbs(c);
     const int n_ru = static_cast<int>(cdiv(n_rb, L.ctas));
@@ -1359,11 +1369,19 @@ int run_single_pass(const void* hidden, const void* W, const int32_t* ids, const
     u.dH = static_cast<__nv_bfloat16*>(dH);
     u.first = b == 0;
     u.last = b + 1 == L.nvb;
+    split = split && L.sk_slots > 0;
+    u.sk_part = split ? w.sk : nullptr;
+    u.sk_slots = split ? L.sk_slots : 0;
+    const long long units = static_cast<long long>(n_ru) * n_dt_dh;
     const int grid =
-        L.ctas * static_cast<int>(std::min<long long>(static_cast<long long>(n_ru) * n_dt_dh, slots));
+        L.ctas * (split ? L.sk_slots : static_cast<int>(std::min<long long>(units, slots)));
     const cudaError_t e = L.fused ? launch_uac_gemm(L.ctas, map_s, map_w_mn, u, grid, st)
                                   : launch_uap_gemm(L.ctas, map_s, map_w_mn, u, grid, st);
-    return e == cudaSuccess ? GRPO_OK : GRPO_ERR_CUDA;
+    if (e != cudaSuccess) return GRPO_ERR_CUDA;
+    if (!split || (mask == nullptr && units % L.sk_slots == 0)) return GRPO_OK;
+    return launch_sk_fixup(L.ctas, u, static_cast<int>(units), true, st) == cudaSuccess
+               ? GRPO_OK
+               : GRPO_ERR_CUDA;
   };
 
   int r = GRPO_OK;
@@ -1373,7 +1391,7 @@ int run_single_pass(const void* hidden, const void* W, const int32_t* ids, const
       r = fwds(i);
       if (r == GRPO_OK && !L.fused) r = ppass(i, st);
       if (r == GRPO_OK && b + 1 == L.nvb) r = rowfin(c);
-      if (r == GRPO_OK) r = uacc(i);
+      if (r == GRPO_OK) r = uacc(i, true);
     }
   } else {
     std::lock_guard<std::mutex> side_lock(di->side_mu);
@@ -1399,7 +1417,7 @@ int run_single_pass(const void* hidden, const void* W, const int32_t* ids, const
       if (r != GRPO_OK) break;
       if (cudaStreamWaitEvent(st, di->ev_g[i & 1], 0) != cudaSuccess) return GRPO_ERR_CUDA;
       if (i % L.nvb + 1 == L.nvb) r = rowfin(i / L.nvb);
-      if (r == GRPO_OK) r = uacc(i);
+      if (r == GRPO_OK) r = uacc(i, false);
     }
   }  // side_lock released: this call's records and waits are all enqueued
   if (r != GRPO_OK) return r;
@@ -1721,12 +1739,16 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
   const int grp = group_rows_exact(static_cast<int>(cdiv(n_rb, L.ctas)), slots);
   info->fwd_splits = std::min(std::max(1, slots / grp), std::min(L.nvt, kMaxSplits));
   info->launches_logp = L.n > 0 ? 2 : 0;
-  // The stored form's tail-split dH launches (a fused dH GEMM, or chunks that
-  // run one after another) are each followed by a fixup pass.
-  const bool tail_split = L.stored && L.sk_slots > 0 && (L.fused || L.n_sbuf == 1);
+  // Tail-split dH-type launches (the stored form's fused dH GEMM or chunks that
+  // run one after another; the single pass's U GEMMs that nothing runs beside)
+  // are each followed by a fixup pass.
+  const bool tail_split = L.sk_slots > 0 && (L.fused || L.n_sbuf == 1);
   info->launches_loss = L.n <= 0        ? 0
                         : L.stored      ? 3 + (tail_split ? 4 : 3) * info->n_chunks
-                        : L.single_pass ? 3 + info->n_chunks * ((L.fused ? 2 : 3) * L.nvb + 1)
+                        : L.single_pass ? 3 + info->n_chunks *
+                                                  (((L.fused ? 2 : 3) + (tail_split ? 1 : 0)) *
+                                                       L.nvb +
+                                                   1)
                                         : 4 + 2 * info->n_chunks * info->n_vocab_blocks;
   if (L.n > 0 && params != nullptr && (params->flags & GRPO_FLAG_SEQUENCE_MEAN) != 0)
     info->launches_loss += 1;

@@ -229,6 +229,88 @@ struct RowCvt {
   float ytarget;
 };
 
+// Per-row constants of the single pass's U accumulator (MODE_UAC, MODE_UAP):
+// the row's running maximum M after this block (log2 units, from the split
+// partials of the blocks so far), the rescale of U from the blocks before,
+// alpha = 2^(M_prev - M), and on the last block the factors of
+// dH = cw W_y - cu U: cu = g 2^(M - lse2), cw = g (1 - p_y) f'_y.
+struct UaccRow {
+  bool zero;        // masked or outside the batch: U and dH get zeros
+  int y;            // target column, or -1 (bad ids: the row finish sets the status)
+  float mcur, alpha, cu, cw;
+};
+
+__device__ __forceinline__ UaccRow uacc_row(const TileArgs& a, long long grow, bool valid) {
+  UaccRow r;
+  r.zero = true;
+  r.y = -1;
+  r.mcur = 0.f;
+  r.alpha = 0.f;
+  r.cu = 0.f;
+  r.cw = 0.f;
+  if (!valid || (a.mask != nullptr && a.mask[grow] == 0)) return r;
+  float mcur = -INFINITY;
+  for (int sl = 0; sl < a.slots_cur; ++sl) mcur = fmaxf(mcur, a.part_m[sl * a.part_ld + grow]);
+  const int yy = a.ids[grow];
+  r.zero = false;
+  r.y = (yy >= 0 && yy < a.vocab) ? yy : -1;
+  r.mcur = mcur;
+  if (!a.first) {
+    float mprev = -INFINITY;
+    for (int sl = 0; sl < a.slots_prev; ++sl) mprev = fmaxf(mprev, a.part_m[sl * a.part_ld + grow]);
+    r.alpha = ex2(mprev - mcur);
+  }
+  if (a.last) {
+    const float g = a.g[grow];
+    const float l2 = a.lse[grow] * kLog2e;
+    r.cu = g * ex2(mcur - l2);
+    if (r.y >= 0) {
+      const float zy = a.zy[grow];
+      r.cw = (g - g * ex2(fmaf(zy, kLog2e, -l2))) * dz_of_logit(a, zy);
+    }
+  }
+  return r;
+}
+
+// U update of 8 hidden columns of one row, x = this block's P W for them:
+// U = alpha U_prev + x (U_prev read from accp unless this is the first block),
+// then stored back to accp, or on the last block turned into dH (bf16, outp).
+__device__ __forceinline__ void uacc_update8(const TileArgs& a, const UaccRow& r, float (&x)[8],
+                                             float* accp, __nv_bfloat16* outp,
+                                             const __nv_bfloat16* wy) {
+  if (r.zero) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = 0.f;
+  } else if (!a.first) {
+    const float4 a0 = *reinterpret_cast<const float4*>(accp);
+    const float4 a1 = *reinterpret_cast<const float4*>(accp + 4);
+    const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = fmaf(r.alpha, av[e], x[e]);
+  }
+  if (a.last) {
+    if (!r.zero) {
+      float wv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (r.y >= 0) {
+        const uint4 wb = *reinterpret_cast<const uint4*>(wy);
+        const uint32_t ww[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          wv[2 * e] = __uint_as_float(ww[e] << 16);
+          wv[2 * e + 1] = __uint_as_float(ww[e] & 0xffff0000u);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = fmaf(r.cw, wv[e], -r.cu * x[e]);
+    }
+    st_global_v4(outp, pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
+                 pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+  } else {
+    *reinterpret_cast<float4*>(accp) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4*>(accp + 4) = make_float4(x[4], x[5], x[6], x[7]);
+  }
+}
+
 // Rewrites chunks jb..jb+NCH-1 (8 columns each) of row r of a landed A stage
 // (64 stored values of vocab columns vbase.., box maximum zoff) in place as
 // bf16. Columns at or past the vocabulary size become zeros. The main loop
@@ -425,8 +507,7 @@ __device__ __forceinline__ SkSplit sk_split(const TileArgs& a, int n_ru, int n_u
   s.t_f = s.t_l = 0;
   s.tail_total = 0;
   const int rem = slots > 0 ? n_units % slots : 0;
-  if (a.sk_part == nullptr || !a.first || !a.last || rem == 0 || a.k_iters < 2 * kSkMinStages)
-    return s;
+  if (a.sk_part == nullptr || rem == 0 || a.k_iters < 2 * kSkMinStages) return s;
   const int U = rem;
   const int w_dp = n_units - rem;
   const int k = a.k_iters;
@@ -692,7 +773,8 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
   const int k_iters = ((MODE == MODE_DW ? n_rb * (BM / BK) : args.k_iters) + C::kKSub - 1) / C::kKSub;
   // This pair's units, and with a tail split its part of the last round.
   WorkList<CTAS> wl;
-  wl.init(args, n_ru, n_units, cta_slot, n_slots, MODE == MODE_DH || MODE == MODE_DHS);
+  wl.init(args, n_ru, n_units, cta_slot, n_slots,
+          MODE == MODE_DH || MODE == MODE_DHS || is_uacc(MODE));
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
@@ -960,7 +1042,8 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
       rc.scale = 1.f;
       rc.shift2 = 0.f;
       rc.ytarget = 0.f;
-      float u_alpha = 0.f, u_cu = 0.f, u_cw = 0.f;  // UAC epilogue: rescale, dH factors
+      UaccRow ur;                        // UAC, UAP: the U update's row constants
+      ur.zero = true;
       if (is_fwd(MODE)) {
         if (valid && (args.mask == nullptr || args.mask[grow] != 0)) y = args.ids[grow];
       } else if (MODE == MODE_BWDG) {
@@ -985,33 +1068,12 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
           }
         }
       } else if (is_uacc(MODE)) {
-        if (valid && (args.mask == nullptr || args.mask[grow] != 0)) {
-          // Running maxima (log2 units) from the forward's split partials.
-          float mcur = -INFINITY;
-          for (int sl = 0; sl < args.slots_cur; ++sl)
-            mcur = fmaxf(mcur, args.part_m[sl * args.part_ld + grow]);
-          const int yy = args.ids[grow];
+        ur = uacc_row(args, grow, valid);
+        if (!ur.zero) {
           rc.zero = false;
-          rc.y = (yy >= 0 && yy < args.vocab) ? yy : -1;  // bad ids: status set by the row finish
-          rc.c = -mcur;
-          rc.shift2 = -mcur;
-          if (part == 0) {
-            if (!args.first) {
-              float mprev = -INFINITY;
-              for (int sl = 0; sl < args.slots_prev; ++sl)
-                mprev = fmaxf(mprev, args.part_m[sl * args.part_ld + grow]);
-              u_alpha = ex2(mprev - mcur);
-            }
-            if (args.last) {
-              const float g = args.g[grow];
-              const float l2 = args.lse[grow] * kLog2e;
-              u_cu = g * ex2(mcur - l2);
-              if (rc.y >= 0) {
-                const float zy = args.zy[grow];
-                u_cw = (g - g * ex2(fmaf(zy, kLog2e, -l2))) * dz_of_logit(args, zy);
-              }
-            }
-          }
+          rc.y = ur.y;
+          rc.c = -ur.mcur;
+          rc.shift2 = -ur.mcur;
         }
       }
 
@@ -1380,54 +1442,38 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
           }
         } else if (is_uacc(MODE)) {
           // U (+)= this block's P W, rescaled to the running maximum; on the
-          // last block dH = g (1 - p_y) f'_y W_y - g 2^(M - lse2) U.
+          // last block dH = g (1 - p_y) f'_y W_y - g 2^(M - lse2) U. A cut piece
+          // of the tail split leaves its partial tile for the fixup instead.
 #pragma unroll 1
           for (int c = 0; c < C::kTileN / 32; ++c) {
             const int d0 = t * C::kTileN + c * 32;
             if (d0 >= args.hidden) break;  // warp-uniform
             float v[32];
             tmem_ld32(tbase + c * 32, v);
+            if (wk.cut) {
+              if (valid) {
+                float* sp = sk_slot_ptr(args, wk.slot, static_cast<int>(rank), CTAS, C::kTileN) +
+                            (c * 8 * BM + lrow_in_tile) * 4;
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj)
+                  st_global_v4(sp + jj * BM * 4, __float_as_uint(v[4 * jj]),
+                               __float_as_uint(v[4 * jj + 1]), __float_as_uint(v[4 * jj + 2]),
+                               __float_as_uint(v[4 * jj + 3]));
+              }
+              continue;
+            }
             if (valid) {
               float* accp = args.acc + static_cast<long long>(lrow) * args.hidden + d0;
               __nv_bfloat16* outp = args.dH + static_cast<long long>(grow) * args.hidden + d0;
               const __nv_bfloat16* wy =
-                  args.W + static_cast<long long>(rc.y < 0 ? 0 : rc.y) * args.hidden + d0;
+                  args.W + static_cast<long long>(ur.y < 0 ? 0 : ur.y) * args.hidden + d0;
 #pragma unroll
               for (int j8 = 0; j8 < 4; ++j8) {
                 if (d0 + j8 * 8 >= args.hidden) break;
-                float* x = v + j8 * 8;
-                if (rc.zero) {
+                float x[8];
 #pragma unroll
-                  for (int e = 0; e < 8; ++e) x[e] = 0.f;
-                } else if (!args.first) {
-                  const float4 a0 = *reinterpret_cast<const float4*>(accp + j8 * 8);
-                  const float4 a1 = *reinterpret_cast<const float4*>(accp + j8 * 8 + 4);
-                  const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-                  for (int e = 0; e < 8; ++e) x[e] = fmaf(u_alpha, av[e], x[e]);
-                }
-                if (args.last) {
-                  if (!rc.zero) {
-                    float wv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                    if (rc.y >= 0) {
-                      const uint4 wb = *reinterpret_cast<const uint4*>(wy + j8 * 8);
-                      const uint32_t ww[4] = {wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-                      for (int e = 0; e < 4; ++e) {
-                        wv[2 * e] = __uint_as_float(ww[e] << 16);
-                        wv[2 * e + 1] = __uint_as_float(ww[e] & 0xffff0000u);
-                      }
-                    }
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = fmaf(u_cw, wv[e], -u_cu * x[e]);
-                  }
-                  st_global_v4(outp + j8 * 8, pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
-                               pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
-                } else {
-                  *reinterpret_cast<float4*>(accp + j8 * 8) = make_float4(x[0], x[1], x[2], x[3]);
-                  *reinterpret_cast<float4*>(accp + j8 * 8 + 4) =
-                      make_float4(x[4], x[5], x[6], x[7]);
-                }
+                for (int e = 0; e < 8; ++e) x[e] = v[j8 * 8 + e];
+                uacc_update8(args, ur, x, accp + j8 * 8, outp + j8 * 8, wy + j8 * 8);
               }
             }
           }
@@ -1512,12 +1558,13 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
   }
 }
 
-// Adds the pieces of every dH unit that the tail split cut (see SkSplit) in a
-// fixed order, its main piece and then its tails in pair order, and writes the
-// unit's bf16 dH rows. Grid: (the launch's host-side bound on units) x (32-
+// Adds the pieces of every dH-type unit that the tail split cut (see SkSplit)
+// in a fixed order, its main piece and then its tails in pair order, and
+// writes the unit's bf16 dH rows (kUacc: applies the single pass's U update to
+// the sum instead, as the U GEMM's epilogue does). Grid: (the launch's host-side bound on units) x (32-
 // column chunks of a unit); one thread per row of the unit. Units that ran
 // whole return at once. `a` is the dH launch's own TileArgs.
-template <int CTAS>
+template <int CTAS, bool kUacc>
 __global__ void __launch_bounds__(BM * CTAS) sk_fixup_kernel(const TileArgs a) {
   constexpr int kTileN = PairCfg<MODE_DH, CTAS>::kTileN;
   __shared__ SkSplit sp_sh;
@@ -1592,6 +1639,21 @@ __global__ void __launch_bounds__(BM * CTAS) sk_fixup_kernel(const TileArgs a) {
     if (ke > kb) add_slot(sk_tail_slot(sp, u, q));
   }
   __nv_bfloat16* out = a.dH + grow * a.hidden + d0;
+  if constexpr (kUacc) {
+    // The single pass's U update, as the U GEMM's epilogue does it.
+    const UaccRow ur = uacc_row(a, grow, true);
+    float* accp = a.acc + (static_cast<long long>(li) * BM + lrow) * a.hidden + d0;
+    const __nv_bfloat16* wy = a.W + static_cast<long long>(ur.y < 0 ? 0 : ur.y) * a.hidden + d0;
+#pragma unroll
+    for (int j8 = 0; j8 < 4; ++j8) {
+      if (d0 + j8 * 8 >= a.hidden) break;
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = v[j8 * 8 + e];
+      uacc_update8(a, ur, x, accp + j8 * 8, out + j8 * 8, wy + j8 * 8);
+    }
+    return;
+  }
 #pragma unroll
   for (int j8 = 0; j8 < 4; ++j8) {
     if (d0 + j8 * 8 >= a.hidden) break;

@@ -96,15 +96,20 @@ typedef struct grpo_shape {
  * grpo_get_plan reports it. Setting more than one of the three flags is
  * GRPO_ERR_INVALID_ARG.
  *
+ * Tail split (stored form; single pass with P formed on chip): when the last
+ * round of a dH-type GEMM launch has fewer units (256 rows x 512 hidden
+ * columns) than the device has SM pairs, and no G or P pass runs beside it,
+ * idle pairs take over the tails of that round's vocabulary loops, and a fixup
+ * pass adds each cut unit's pieces in a fixed order (results do not depend on
+ * timing). Its fp32 partial tiles take a fixed 76 MiB of the workspace (38 MiB
+ * with GRPO_FLAG_SINGLE_CTA) when the K loop has at least 8129 columns (the
+ * vocabulary, or the single pass's block), and none under a workspace budget
+ * below 8 times that.
+ *
  * grpo_params.flags bit: backward without a second logit GEMM. Per chunk of
  * rows, the forward GEMM also keeps the chunk's (transformed) logits in fp16
  * in the workspace, and the dH GEMM runs over the whole vocabulary once lse
- * and g are known. When the last round of a dH launch has fewer units (256
- * rows x 512 hidden columns) than the device has SM pairs, and no G pass runs
- * beside it, idle pairs take over the tails of that round's vocabulary loops;
- * a fixup pass adds the pieces in a fixed order (results do not depend on
- * timing). Its fp32 partial tiles take a fixed 76 MiB of the workspace (38 MiB
- * with GRPO_FLAG_SINGLE_CTA; vocabularies of at least 8129 columns). Each 64-column box of a row is stored relative to its own
+ * and g are known. Each 64-column box of a row is stored relative to its own
  * maximum (kept beside it in fp32), so any finite logit is stored without
  * overflow and the box's largest terms keep fp16's finest spacing. The logits
  * are turned into G in one of two ways:

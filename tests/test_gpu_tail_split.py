@@ -198,3 +198,62 @@ def test_tail_split_with_the_lm_head_gradient(clp):
     assert rel_dh <= DH_RTOL and rel_dw <= DH_RTOL and np.all(dh[~m] == 0.0)
     L2, logp2, dH2, dW2 = outs[1]
     assert L2 == L and torch.equal(dH2, dH) and torch.equal(logp2, logp)
+
+
+SINGLE_PASS = 32  # GRPO_FLAG_SINGLE_PASS
+
+# name, prompts, G, T, D, V, lengths, chunk tokens, vocab block
+SINGLE_PASS_CASES = [
+    # 4 pair row units x 3 hidden tiles per U GEMM launch, 4 vocabulary blocks
+    # (the first, middle and last U updates all go through the fixup when cut).
+    ("sp_blocks", 1, 4, 256, 1536, 40000, (40, 256), 0, 12800),
+    # two chunks, ragged last block, a hidden size with a narrow last tile
+    ("sp_chunks", 1, 4, 256, 1280, 30000, (100, 256), 512, 9728),
+]
+
+
+@pytest.mark.parametrize("name,prompts,G,T,D,V,lengths,chunk,vblock", SINGLE_PASS_CASES,
+                         ids=[c[0] for c in SINGLE_PASS_CASES])
+def test_tail_split_single_pass(clp, name, prompts, G, T, D, V, lengths, chunk, vblock):
+    # The single pass with P formed on chip: its U GEMM launches split like the
+    # stored form's dH launches, and the fixup applies the U update (the
+    # rescale by the running maximum, and dH on the last block) to the sum of
+    # a cut unit's pieces.
+    p = synth.make_problem("tiny", seed=D + V + 1, prompts=prompts, G=G, T=T, D=D, V=V,
+                           lengths=lengths)
+    base, _ = oracle.selective_logp(p.hidden, p.weight, p.ids.numpy())
+    old, ref = p.old_ref(torch.from_numpy(np.asarray(base)))
+    want = oracle.loss_fwd_bwd(p.hidden, p.weight, p.ids.numpy(), p.mask.numpy(), old, ref,
+                               p.adv, p.seq_len, p.eps_low, p.eps_high, p.beta)
+    dev = torch.device(DEV)
+    params = clp.make_params(flags=SINGLE_PASS, chunk_tokens=chunk, vocab_block=vblock)
+    plan = clp.grpo_get_plan(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, params)
+    assert plan["single_pass"] == 1 and plan["g_in_dh_gemm"] == 1 and plan["n_vocab_blocks"] > 2
+    ws = clp.alloc_workspace(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, params, dev)
+    args = [t.to(dev) for t in (p.hidden, p.weight, p.ids, p.mask)] + [old.to(dev), ref.to(dev),
+                                                                       p.adv.to(dev)]
+    outs = []
+    clp.grpo_launch_timing_enable(True)
+    try:
+        for _ in range(2):
+            loss, logp, dH = clp.grpo_loss_fwd_bwd(*args, p.seq_len, params=params, workspace=ws)
+            assert clp.grpo_read_device_status(ws) == 0
+            outs.append((loss.item(), logp.cpu(), dH.cpu()))
+    finally:
+        clp.grpo_launch_timing_enable(False)
+    times = {k["name"]: k["launches"] for k in clp.grpo_launch_timing_read()}
+    assert times.get("sk_fixup_kernel", 0) == 2 * plan["n_chunks"] * plan["n_vocab_blocks"]
+    assert sum(times.values()) == 2 * plan["launches_loss"]
+    L, logp, dH = outs[0]
+    m = p.mask.numpy().astype(bool)
+    dh = dH.double().numpy()
+    dl = np.abs(logp.double().numpy() - want["logp"]).max()
+    rel_loss = abs(L - want["L"]) / abs(want["L"])
+    rel_dh = np.linalg.norm(dh[m] - want["dH"][m]) / np.linalg.norm(want["dH"][m])
+    print(f"{name}: max|dlogp|={dl:.3e} rel_loss={rel_loss:.3e} rel_dH={rel_dh:.3e}")
+    assert dl <= LOGP_TOL and rel_loss <= LOSS_RTOL and rel_dh <= DH_RTOL
+    assert np.all(dh[~m] == 0.0)
+    row_err = np.linalg.norm(dh[m] - want["dH"][m], axis=1)
+    assert np.all(row_err <= 0.05 * np.linalg.norm(want["dH"][m], axis=1) + 1e-6)
+    L2, logp2, dH2 = outs[1]
+    assert L2 == L and torch.equal(logp2, logp) and torch.equal(dH2, dH)
