@@ -938,9 +938,10 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
   // device decides from the active row blocks which units are cut), and a
   // fixup pass adds the cut units' pieces. Without a mask every row block is
   // active, so a unit count of whole rounds is known here to cut nothing. The
-  // overlapped schedule does without it: there the next chunk's G pass runs
-  // on the pairs that a dH launch's last round leaves idle (measured at the
-  // gpt-oss-20b head: the split made that pass 19 % slower and the call 0.5 %).
+  // overlapped schedule splits only its last chunk's launch: before that the
+  // next chunk's G pass runs on the pairs that a dH launch's last round leaves
+  // idle (measured at the gpt-oss-20b head: splitting every launch made that
+  // pass 19 % slower and the call 0.5 %).
   auto dh_grid = [&](long long units, bool split) {
     return L.ctas * (split ? L.sk_slots : static_cast<int>(std::min<long long>(units, slots)));
   };
@@ -1159,7 +1160,8 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
       if (c + 1 < n_chunks) r = fwd_then_gform(c + 1);  // buffer (c+1)&1: free after dh(c-1)
       if (r != GRPO_OK) break;
       if (cudaStreamWaitEvent(st, di->ev_g[c & 1], 0) != cudaSuccess) return GRPO_ERR_CUDA;
-      r = dh(c, false);
+      // Only the last chunk's dH launch has no G pass beside it.
+      r = dh(c, c + 1 == n_chunks);
     }
   }  // side_lock released: this call's records and waits are all enqueued
   if (r != GRPO_OK) return r;
@@ -1739,12 +1741,13 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
   const int grp = group_rows_exact(static_cast<int>(cdiv(n_rb, L.ctas)), slots);
   info->fwd_splits = std::min(std::max(1, slots / grp), std::min(L.nvt, kMaxSplits));
   info->launches_logp = L.n > 0 ? 2 : 0;
-  // Tail-split dH-type launches (the stored form's fused dH GEMM or chunks that
-  // run one after another; the single pass's U GEMMs that nothing runs beside)
-  // are each followed by a fixup pass.
+  // Tail-split dH-type launches (the stored form's fused dH GEMM, chunks that
+  // run one after another, or the overlapped schedule's last chunk; the single
+  // pass's U GEMMs that nothing runs beside) are each followed by a fixup pass.
   const bool tail_split = L.sk_slots > 0 && (L.fused || L.n_sbuf == 1);
+  const int stored_fixups = L.sk_slots == 0 ? 0 : tail_split ? info->n_chunks : 1;
   info->launches_loss = L.n <= 0        ? 0
-                        : L.stored      ? 3 + (tail_split ? 4 : 3) * info->n_chunks
+                        : L.stored      ? 3 + 3 * info->n_chunks + stored_fixups
                         : L.single_pass ? 3 + info->n_chunks *
                                                   (((L.fused ? 2 : 3) + (tail_split ? 1 : 0)) *
                                                        L.nvb +

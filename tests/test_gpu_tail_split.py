@@ -257,3 +257,48 @@ def test_tail_split_single_pass(clp, name, prompts, G, T, D, V, lengths, chunk, 
     assert np.all(row_err <= 0.05 * np.linalg.norm(want["dH"][m], axis=1) + 1e-6)
     L2, logp2, dH2 = outs[1]
     assert L2 == L and torch.equal(logp2, logp) and torch.equal(dH2, dH)
+
+
+def test_tail_split_overlapped_schedule_last_chunk(clp):
+    # D > 2048 with several chunks: each chunk's G pass runs on a side stream
+    # beside the previous chunk's dH launch, which therefore keeps whole units;
+    # only the last chunk's dH launch, with nothing beside it, is split.
+    # Lengths over 128 keep both row blocks of every completion active, so the
+    # last chunk has units to split (trailing padding inside them).
+    p = synth.make_problem("tiny", seed=13, prompts=1, G=4, T=256, D=2304, V=9000,
+                           lengths=(200, 256))
+    base, _ = oracle.selective_logp(p.hidden, p.weight, p.ids.numpy())
+    old, ref = p.old_ref(torch.from_numpy(np.asarray(base)))
+    want = oracle.loss_fwd_bwd(p.hidden, p.weight, p.ids.numpy(), p.mask.numpy(), old, ref,
+                               p.adv, p.seq_len, p.eps_low, p.eps_high, p.beta)
+    dev = torch.device(DEV)
+    params = clp.make_params(flags=STORED, chunk_tokens=256)
+    plan = clp.grpo_get_plan(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, params)
+    assert plan["g_in_dh_gemm"] == 0 and plan["n_chunks"] >= 3
+    ws = clp.alloc_workspace(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, params, dev)
+    args = [t.to(dev) for t in (p.hidden, p.weight, p.ids, p.mask)] + [old.to(dev), ref.to(dev),
+                                                                       p.adv.to(dev)]
+    outs = []
+    clp.grpo_launch_timing_enable(True)
+    try:
+        for _ in range(2):
+            loss, logp, dH = clp.grpo_loss_fwd_bwd(*args, p.seq_len, params=params, workspace=ws)
+            assert clp.grpo_read_device_status(ws) == 0
+            outs.append((loss.item(), logp.cpu(), dH.cpu()))
+    finally:
+        clp.grpo_launch_timing_enable(False)
+    times = {k["name"]: k["launches"] for k in clp.grpo_launch_timing_read()}
+    assert times.get("sk_fixup_kernel", 0) == 2
+    assert sum(times.values()) == 2 * plan["launches_loss"]
+    L, logp, dH = outs[0]
+    m = p.mask.numpy().astype(bool)
+    dh = dH.double().numpy()
+    rel_dh = np.linalg.norm(dh[m] - want["dH"][m]) / np.linalg.norm(want["dH"][m])
+    print(f"overlapped, last chunk split: rel_dH={rel_dh:.3e}")
+    assert np.abs(logp.double().numpy() - want["logp"]).max() <= LOGP_TOL
+    assert abs(L - want["L"]) / abs(want["L"]) <= LOSS_RTOL and rel_dh <= DH_RTOL
+    row_err = np.linalg.norm(dh[m] - want["dH"][m], axis=1)
+    assert np.all(row_err <= 0.05 * np.linalg.norm(want["dH"][m], axis=1) + 1e-6)
+    assert np.all(dh[~m] == 0.0)
+    L2, logp2, dH2 = outs[1]
+    assert L2 == L and torch.equal(logp2, logp) and torch.equal(dH2, dH)
