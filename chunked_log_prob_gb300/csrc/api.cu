@@ -95,12 +95,12 @@ struct Layout {
   bool need_acc;    // more than one vocab block -> fp32 dH accumulator
   double model_cost;  // modelled GEMM time of the plan in forward-tile times (0: no device)
   int nbox;         // stored path: 64-column boxes per row (their maxima are kept)
-  int sk_slots;     // stored path: pairs of the tail-split dH launches (0: no split)
+  int ts_slots;     // stored path: pairs of the tail-split dH launches (0: no split)
   size_t off_pm, off_ps, off_zy, off_lse, off_g, off_rbl, off_lt, off_seq, off_sk, off_G,
       off_bmax, off_acc, total;
 };
 
-// Tail split (see SkSplit in gemm_tc.cuh): a dH-type launch whose last round
+// Tail split (see TailSplit in gemm_tc.cuh): a dH-type launch whose last round
 // has fewer units than SM pairs splits that round's units between their own
 // pairs and idle ones, when its K loop (the vocabulary, or the single pass's
 // vocabulary block) is long enough to cut and nothing runs beside it. The
@@ -109,13 +109,13 @@ struct Layout {
 // the sizing without a device holds. The chunk planner models whole rounds all
 // the same: the split only makes a launch's last round shorter.
 int tail_split_slots(int k_cols, int ctas, int sms) {
-  if (cdiv(k_cols, BK) < 2 * kSkMinStages) return 0;
+  if (cdiv(k_cols, BK) < 2 * kTailMinStages) return 0;
   return std::min(sms > 0 ? sms : kRefSms, kRefSms) / ctas;
 }
 
 // Bytes of the tail split's partial slots: two fp32 tiles of a unit per pair.
-size_t tail_split_bytes(int sk_slots, int ctas) {
-  return static_cast<size_t>(2) * sk_slots * ctas * BM * (BN * dh_accumulators(ctas)) *
+size_t tail_split_bytes(int ts_slots, int ctas) {
+  return static_cast<size_t>(2) * ts_slots * ctas * BM * (BN * dh_accumulators(ctas)) *
          sizeof(float);
 }
 
@@ -392,13 +392,13 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, Form fo
   // Tail-split slots: stored form, single pass with P on chip; not under a
   // budget they would take more than an eighth of.
   const size_t budget = workspace_budget(p);
-  L->sk_slots = L->stored ? tail_split_slots(s->vocab, L->ctas, sms)
+  L->ts_slots = L->stored ? tail_split_slots(s->vocab, L->ctas, sms)
                 : form == kFormSinglePass ? tail_split_slots(static_cast<int>(L->vblock), L->ctas, sms)
                                           : 0;
-  if (L->sk_slots > 0 && budget > 0 && tail_split_bytes(L->sk_slots, L->ctas) * 8 > budget)
-    L->sk_slots = 0;
+  if (L->ts_slots > 0 && budget > 0 && tail_split_bytes(L->ts_slots, L->ctas) * 8 > budget)
+    L->ts_slots = 0;
   L->off_sk = off;
-  if (L->sk_slots > 0) off = align_up(off + tail_split_bytes(L->sk_slots, L->ctas), 256);
+  if (L->ts_slots > 0) off = align_up(off + tail_split_bytes(L->ts_slots, L->ctas), 256);
   L->off_G = off;
 
   // Chunks are whole row units (BM * ctas rows: what one CTA pair covers).
@@ -733,7 +733,7 @@ Ws carve(void* ws, const Layout& L) {
   w.g = reinterpret_cast<float*>(w.base + L.off_g);
   w.G = reinterpret_cast<__nv_bfloat16*>(w.base + L.off_G);
   w.acc = reinterpret_cast<float*>(w.base + L.off_acc);
-  w.sk = L.sk_slots > 0 ? reinterpret_cast<float*>(w.base + L.off_sk) : nullptr;
+  w.sk = L.ts_slots > 0 ? reinterpret_cast<float*>(w.base + L.off_sk) : nullptr;
   return w;
 }
 
@@ -943,11 +943,11 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
   // idle (measured at the gpt-oss-20b head: splitting every launch made that
   // pass 19 % slower and the call 0.5 %).
   auto dh_grid = [&](long long units, bool split) {
-    return L.ctas * (split ? L.sk_slots : static_cast<int>(std::min<long long>(units, slots)));
+    return L.ctas * (split ? L.ts_slots : static_cast<int>(std::min<long long>(units, slots)));
   };
-  auto sk_fixup = [&](const TileArgs& b, long long units) -> int {
-    if (b.sk_part == nullptr || (mask == nullptr && units % L.sk_slots == 0)) return GRPO_OK;
-    return launch_sk_fixup(L.ctas, b, static_cast<int>(units), false, st) == cudaSuccess
+  auto ts_fixup = [&](const TileArgs& b, long long units) -> int {
+    if (b.ts_part == nullptr || (mask == nullptr && units % L.ts_slots == 0)) return GRPO_OK;
+    return launch_tail_fixup(L.ctas, b, static_cast<int>(units), false, st) == cudaSuccess
                ? GRPO_OK
                : GRPO_ERR_CUDA;
   };
@@ -1070,13 +1070,13 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     b.dH = static_cast<__nv_bfloat16*>(dH);
     b.first = 1;
     b.last = 1;
-    split = split && L.sk_slots > 0;
-    b.sk_part = split ? w.sk : nullptr;
-    b.sk_slots = split ? L.sk_slots : 0;
+    split = split && L.ts_slots > 0;
+    b.ts_part = split ? w.sk : nullptr;
+    b.ts_slots = split ? L.ts_slots : 0;
     const long long units = static_cast<long long>(n_ru) * n_dt_dh;
     if (launch_dh_gemm(L.ctas, map_g, map_w_mn, b, dh_grid(units, split), st) != cudaSuccess)
       return GRPO_ERR_CUDA;
-    if (const int rr = sk_fixup(b, units); rr != GRPO_OK) return rr;
+    if (const int rr = ts_fixup(b, units); rr != GRPO_OK) return rr;
     if (dW != nullptr)
       return launch_dw(hidden, reinterpret_cast<const __nv_bfloat16*>(sbuf(c)), L.ldS, 0, L.V,
                        c * rb_per_chunk, n_rb, dW, c == 0, L, w, sms, st);
@@ -1111,13 +1111,13 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     b.dH = static_cast<__nv_bfloat16*>(dH);
     b.first = 1;
     b.last = 1;
-    const bool split = L.sk_slots > 0;
-    b.sk_part = split ? w.sk : nullptr;
-    b.sk_slots = split ? L.sk_slots : 0;
+    const bool split = L.ts_slots > 0;
+    b.ts_part = split ? w.sk : nullptr;
+    b.ts_slots = split ? L.ts_slots : 0;
     const long long units = static_cast<long long>(n_ru) * n_dt_dh;
     if (launch_dhs_gemm(L.ctas, map_s, map_w_mn, b, dh_grid(units, split), st) != cudaSuccess)
       return GRPO_ERR_CUDA;
-    return sk_fixup(b, units);
+    return ts_fixup(b, units);
   };
 
   int r = GRPO_OK;
@@ -1371,17 +1371,17 @@ int run_single_pass(const void* hidden, const void* W, const int32_t* ids, const
     u.dH = static_cast<__nv_bfloat16*>(dH);
     u.first = b == 0;
     u.last = b + 1 == L.nvb;
-    split = split && L.sk_slots > 0;
-    u.sk_part = split ? w.sk : nullptr;
-    u.sk_slots = split ? L.sk_slots : 0;
+    split = split && L.ts_slots > 0;
+    u.ts_part = split ? w.sk : nullptr;
+    u.ts_slots = split ? L.ts_slots : 0;
     const long long units = static_cast<long long>(n_ru) * n_dt_dh;
     const int grid =
-        L.ctas * (split ? L.sk_slots : static_cast<int>(std::min<long long>(units, slots)));
+        L.ctas * (split ? L.ts_slots : static_cast<int>(std::min<long long>(units, slots)));
     const cudaError_t e = L.fused ? launch_uac_gemm(L.ctas, map_s, map_w_mn, u, grid, st)
                                   : launch_uap_gemm(L.ctas, map_s, map_w_mn, u, grid, st);
     if (e != cudaSuccess) return GRPO_ERR_CUDA;
-    if (!split || (mask == nullptr && units % L.sk_slots == 0)) return GRPO_OK;
-    return launch_sk_fixup(L.ctas, u, static_cast<int>(units), true, st) == cudaSuccess
+    if (!split || (mask == nullptr && units % L.ts_slots == 0)) return GRPO_OK;
+    return launch_tail_fixup(L.ctas, u, static_cast<int>(units), true, st) == cudaSuccess
                ? GRPO_OK
                : GRPO_ERR_CUDA;
   };
@@ -1744,8 +1744,8 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
   // Tail-split dH-type launches (the stored form's fused dH GEMM, chunks that
   // run one after another, or the overlapped schedule's last chunk; the single
   // pass's U GEMMs that nothing runs beside) are each followed by a fixup pass.
-  const bool tail_split = L.sk_slots > 0 && (L.fused || L.n_sbuf == 1);
-  const int stored_fixups = L.sk_slots == 0 ? 0 : tail_split ? info->n_chunks : 1;
+  const bool tail_split = L.ts_slots > 0 && (L.fused || L.n_sbuf == 1);
+  const int stored_fixups = L.ts_slots == 0 ? 0 : tail_split ? info->n_chunks : 1;
   info->launches_loss = L.n <= 0        ? 0
                         : L.stored      ? 3 + 3 * info->n_chunks + stored_fixups
                         : L.single_pass ? 3 + info->n_chunks *

@@ -52,17 +52,17 @@ cudaError_t launch_dhs_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMa
                    : launch_gemm_variant<MODE_DHS, 1>(map_a, map_b, args, grid, stream);
 }
 
-cudaError_t launch_sk_fixup(int ctas, const TileArgs& args, int units, bool uacc,
+cudaError_t launch_tail_fixup(int ctas, const TileArgs& args, int units, bool uacc,
                             cudaStream_t stream) {
   if (units <= 0) return cudaSuccess;
-  LaunchTimer timer("sk_fixup_kernel", stream);
+  LaunchTimer timer("tail_fixup_kernel", stream);
   const dim3 grid2(units, PairCfg<MODE_DH, 2>::kTileN / 32), grid1(units, PairCfg<MODE_DH, 1>::kTileN / 32);
   if (ctas == 2) {
-    if (uacc) sk_fixup_kernel<2, true><<<grid2, BM * 2, 0, stream>>>(args);
-    else sk_fixup_kernel<2, false><<<grid2, BM * 2, 0, stream>>>(args);
+    if (uacc) tail_fixup_kernel<2, true><<<grid2, BM * 2, 0, stream>>>(args);
+    else tail_fixup_kernel<2, false><<<grid2, BM * 2, 0, stream>>>(args);
   } else {
-    if (uacc) sk_fixup_kernel<1, true><<<grid1, BM, 0, stream>>>(args);
-    else sk_fixup_kernel<1, false><<<grid1, BM, 0, stream>>>(args);
+    if (uacc) tail_fixup_kernel<1, true><<<grid1, BM, 0, stream>>>(args);
+    else tail_fixup_kernel<1, false><<<grid1, BM, 0, stream>>>(args);
   }
   return cudaGetLastError();
 }

@@ -124,12 +124,12 @@ struct TileArgs {
   int first;
   int last;
   // MODE_DH, MODE_DHS over the whole vocabulary (first and last): the tail
-  // split of the last round (see SkSplit). sk_part: 2 slots per SM pair of
+  // split of the last round (see TailSplit). ts_part: 2 slots per SM pair of
   // fp32 partial tiles, or null (units run whole, one per pair and round);
-  // sk_slots: the pairs of the launch (its grid / CTAS), which the fixup
+  // ts_slots: the pairs of the launch (its grid / CTAS), which the fixup
   // kernel must be given too.
-  float* sk_part;
-  int sk_slots;
+  float* ts_part;
+  int ts_slots;
   int* status;
 };
 
@@ -449,16 +449,16 @@ __device__ __forceinline__ int mn_out_cols(const TileArgs& a, int col0) {
 // left every pair at its own place in the vocabulary and made the launch
 // DRAM-bound). Q is at most a third of the pairs, whose tail reads may come
 // from DRAM. Each cut piece leaves its fp32 partial tile in a slot of its own;
-// sk_fixup_kernel adds a unit's pieces in a fixed order (the main piece, then
+// tail_fixup_kernel adds a unit's pieces in a fixed order (the main piece, then
 // the tails in pair order), so the result does not depend on timing.
-constexpr int kSkMinStages = 64;  // least K stages of full width per tail pair
+constexpr int kTailMinStages = 64;  // least K stages of full width per tail pair
 // What a cut piece costs beyond its stages (its partial tile leaves TMEM
 // before the next piece's MMAs can start, and the pipeline refills), in cost
 // units: about 8 full-width stages (6 us per piece measured on GB300 against
 // 0.7 us per stage).
-constexpr int kSkPieceCost = 8 * 4;
+constexpr int kTailPieceCost = 8 * 4;
 
-struct SkSplit {
+struct TailSplit {
   int w_dp;          // units [0, w_dp) run whole, round-robin (the whole rounds)
   int n_main;        // U: units of the last round; pair p < U runs unit w_dp + p
   int n_tail;        // Q: pairs U .. U+Q-1 share the tails; 0: no split
@@ -472,7 +472,7 @@ struct SkSplit {
 // MMA column blocks (of 64 columns per CTA) per K stage of a dH unit of
 // hidden tile `col`: its cost per stage.
 template <int CTAS>
-__device__ __forceinline__ int sk_blocks(const TileArgs& a, int col) {
+__device__ __forceinline__ int ts_blocks(const TileArgs& a, int col) {
   constexpr int kNAcc = CTAS == 2 ? 2 : 1;
   int b = 0;
 #pragma unroll
@@ -483,7 +483,7 @@ __device__ __forceinline__ int sk_blocks(const TileArgs& a, int col) {
 
 // Units in [u0, u1) of the last hidden tile, in the raster order of
 // decode_unit (groups of group_rows row units, tile-major within a group).
-__device__ __forceinline__ int sk_count_last(const TileArgs& a, int n_ru, int u0, int u1) {
+__device__ __forceinline__ int ts_count_last(const TileArgs& a, int n_ru, int u0, int u1) {
   if (u1 <= u0) return 0;
   const int per_group = a.group_rows * a.n_cols;
   int n = 0;
@@ -496,8 +496,8 @@ __device__ __forceinline__ int sk_count_last(const TileArgs& a, int n_ru, int u0
 }
 
 template <int CTAS>
-__device__ __forceinline__ SkSplit sk_split(const TileArgs& a, int n_ru, int n_units, int slots) {
-  SkSplit s;
+__device__ __forceinline__ TailSplit tail_split(const TileArgs& a, int n_ru, int n_units, int slots) {
+  TailSplit s;
   s.w_dp = n_units;
   s.n_main = 0;
   s.n_tail = 0;
@@ -507,25 +507,25 @@ __device__ __forceinline__ SkSplit sk_split(const TileArgs& a, int n_ru, int n_u
   s.t_f = s.t_l = 0;
   s.tail_total = 0;
   const int rem = slots > 0 ? n_units % slots : 0;
-  if (a.sk_part == nullptr || rem == 0 || a.k_iters < 2 * kSkMinStages) return s;
+  if (a.ts_part == nullptr || rem == 0 || a.k_iters < 2 * kTailMinStages) return s;
   const int U = rem;
   const int w_dp = n_units - rem;
   const int k = a.k_iters;
-  s.cs_f = sk_blocks<CTAS>(a, 0);
-  s.cs_l = sk_blocks<CTAS>(a, a.n_cols - 1);
-  const int n_l = a.n_cols == 1 ? U : sk_count_last(a, n_ru, w_dp, n_units);
+  s.cs_f = ts_blocks<CTAS>(a, 0);
+  s.cs_l = ts_blocks<CTAS>(a, a.n_cols - 1);
+  const int n_l = a.n_cols == 1 ? U : ts_count_last(a, n_ru, w_dp, n_units);
   const int n_f = U - n_l;
   if (a.n_cols == 1) s.cs_f = s.cs_l;
   const long long c_f = static_cast<long long>(k) * s.cs_f, c_l = static_cast<long long>(k) * s.cs_l;
   const long long total = n_f * c_f + n_l * c_l;
-  const long long min_cost = static_cast<long long>(kSkMinStages) * 4;
+  const long long min_cost = static_cast<long long>(kTailMinStages) * 4;
   const int Q = static_cast<int>(min(static_cast<long long>(min(slots - U, slots / 3)),
                                      total / min_cost - U));
   if (Q <= 0) return s;
   // Balance: every pair of the round takes about T of cost, the tail pairs'
   // pieces (about (U + Q) / Q each) counted with their overhead. A unit
   // cheaper than T (a narrow last tile) keeps no tail.
-  const long long ovh = kSkPieceCost;
+  const long long ovh = kTailPieceCost;
   long long T = (total + (U + Q) * ovh + U + Q - 1) / (U + Q);
   if (T > c_l && n_f > 0)
     T = max(c_l, (n_f * c_f + (n_f + Q) * ovh + n_f + Q - 1) / (n_f + Q));
@@ -543,62 +543,62 @@ __device__ __forceinline__ SkSplit sk_split(const TileArgs& a, int n_ru, int n_u
   return s;
 }
 
-__device__ __forceinline__ bool sk_is_last(const TileArgs& a, int n_ru, int u) {
+__device__ __forceinline__ bool ts_is_last(const TileArgs& a, int n_ru, int u) {
   int ru, col;
   decode_unit(u, n_ru, a.n_cols, a.group_rows, ru, col);
   return col == a.n_cols - 1;
 }
 
 // Tail cost of the last round's units before u.
-__device__ __forceinline__ long long sk_tail_prefix(const TileArgs& a, int n_ru, const SkSplit& s,
+__device__ __forceinline__ long long ts_tail_prefix(const TileArgs& a, int n_ru, const TailSplit& s,
                                                     int u) {
-  const int nl = sk_count_last(a, n_ru, s.w_dp, u);
+  const int nl = ts_count_last(a, n_ru, s.w_dp, u);
   return static_cast<long long>(u - s.w_dp - nl) * s.t_f + static_cast<long long>(nl) * s.t_l;
 }
 
 // First tail cost of tail pair q (q = n_tail: the end).
-__device__ __forceinline__ long long sk_tail_start(const SkSplit& s, int q) {
+__device__ __forceinline__ long long ts_tail_start(const TailSplit& s, int q) {
   return s.tail_total * q / s.n_tail;
 }
 
 // The tail pair whose share holds tail cost x (0 <= x < tail_total).
-__device__ __forceinline__ int sk_tail_pair_of(const SkSplit& s, long long x) {
+__device__ __forceinline__ int ts_tail_pair_of(const TailSplit& s, long long x) {
   int q = static_cast<int>(x * s.n_tail / s.tail_total);
   q = min(max(q, 0), s.n_tail - 1);
-  while (q + 1 < s.n_tail && sk_tail_start(s, q + 1) <= x) ++q;
-  while (q > 0 && sk_tail_start(s, q) > x) --q;
+  while (q + 1 < s.n_tail && ts_tail_start(s, q + 1) <= x) ++q;
+  while (q > 0 && ts_tail_start(s, q) > x) --q;
   return q;
 }
 
 // The last unit u of the last round with tail prefix <= x.
-__device__ __forceinline__ int sk_tail_unit_at(const TileArgs& a, int n_ru, const SkSplit& s,
+__device__ __forceinline__ int ts_tail_unit_at(const TileArgs& a, int n_ru, const TailSplit& s,
                                                int lo, long long x) {
   int hi = s.w_dp + s.n_main - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (sk_tail_prefix(a, n_ru, s, mid) <= x) lo = mid;
+    if (ts_tail_prefix(a, n_ru, s, mid) <= x) lo = mid;
     else hi = mid - 1;
   }
   return lo;
 }
 
 // Stages [kb, ke) of unit u's tail that tail pair q runs (kb >= ke: none).
-__device__ __forceinline__ void sk_tail_piece(const TileArgs& a, int n_ru, const SkSplit& s, int q,
+__device__ __forceinline__ void ts_tail_piece(const TileArgs& a, int n_ru, const TailSplit& s, int q,
                                               int u, int& kb, int& ke) {
-  const bool last = sk_is_last(a, n_ru, u);
+  const bool last = ts_is_last(a, n_ru, u);
   const int cs = last ? s.cs_l : s.cs_f;
   const int m = last ? s.m_l : s.m_f;
   const long long t = last ? s.t_l : s.t_f;
-  const long long p0 = sk_tail_prefix(a, n_ru, s, u);
-  const long long q0 = sk_tail_start(s, q), q1 = sk_tail_start(s, q + 1);
+  const long long p0 = ts_tail_prefix(a, n_ru, s, u);
+  const long long q0 = ts_tail_start(s, q), q1 = ts_tail_start(s, q + 1);
   kb = m + static_cast<int>((max(q0, p0) - p0) / cs);
   ke = m + static_cast<int>((min(q1, p0 + t) - p0) / cs);
 }
 
 // Slot of a cut piece: main pieces 0 .. U-1, tail pieces U + (u - w_dp) + q
 // (unique: along the units in order and the tail pairs in order, u + q grows).
-__device__ __forceinline__ int sk_main_slot(const SkSplit& s, int u) { return u - s.w_dp; }
-__device__ __forceinline__ int sk_tail_slot(const SkSplit& s, int u, int q) {
+__device__ __forceinline__ int ts_main_slot(const TailSplit& s, int u) { return u - s.w_dp; }
+__device__ __forceinline__ int ts_tail_slot(const TailSplit& s, int u, int q) {
   return s.n_main + (u - s.w_dp) + q;
 }
 
@@ -615,7 +615,7 @@ struct WorkItem {
 // piece or its tail pieces of the last round.
 template <int CTAS>
 struct WorkList {
-  SkSplit s;
+  TailSplit s;
   int slot, n_slots, n_dp;
   int n_extra;       // items after the round-robin ones
   int u_first;       // tail pair: first unit whose tail it meets
@@ -628,16 +628,16 @@ struct WorkList {
     n_extra = 0;
     u_first = 0;
     q = -1;
-    s = sk_split<CTAS>(a, n_ru, dh_mode ? n_units : 0, n_slots);
+    s = tail_split<CTAS>(a, n_ru, dh_mode ? n_units : 0, n_slots);
     if (!dh_mode) s.w_dp = n_units;
     if (s.n_tail > 0) {
       if (slot < s.n_main) {
         n_extra = 1;
       } else if (slot < s.n_main + s.n_tail) {
         q = slot - s.n_main;
-        const long long x0 = sk_tail_start(s, q), x1 = sk_tail_start(s, q + 1);
-        u_first = sk_tail_unit_at(a, n_ru, s, s.w_dp, x0);
-        const int u_last = sk_tail_unit_at(a, n_ru, s, u_first, x1 - 1);
+        const long long x0 = ts_tail_start(s, q), x1 = ts_tail_start(s, q + 1);
+        u_first = ts_tail_unit_at(a, n_ru, s, s.w_dp, x0);
+        const int u_last = ts_tail_unit_at(a, n_ru, s, u_first, x1 - 1);
         n_extra = u_last - u_first + 1;
       }
     }
@@ -660,12 +660,12 @@ struct WorkList {
     if (q < 0) {  // main piece
       w.u = s.w_dp + slot;
       w.kb = 0;
-      w.ke = sk_is_last(a, n_ru, w.u) ? s.m_l : s.m_f;
-      w.slot = sk_main_slot(s, w.u);
+      w.ke = ts_is_last(a, n_ru, w.u) ? s.m_l : s.m_f;
+      w.slot = ts_main_slot(s, w.u);
     } else {
       w.u = u_first + j;
-      sk_tail_piece(a, n_ru, s, q, w.u, w.kb, w.ke);
-      w.slot = sk_tail_slot(s, w.u, q);
+      ts_tail_piece(a, n_ru, s, q, w.u, w.kb, w.ke);
+      w.slot = ts_tail_slot(s, w.u, q);
     }
     w.cut = w.kb != 0 || w.ke != k_iters;
     return true;
@@ -674,9 +674,9 @@ struct WorkList {
 
 // fp32 partial tile of slot `slot`, CTA `rank`: [32-column chunk][8][BM rows][4],
 // so that a warp's 32 rows write (and the fixup reads) 512 contiguous bytes.
-__device__ __forceinline__ float* sk_slot_ptr(const TileArgs& a, int slot, int rank, int ctas,
+__device__ __forceinline__ float* ts_slot_ptr(const TileArgs& a, int slot, int rank, int ctas,
                                               int tile_n) {
-  return a.sk_part + (static_cast<long long>(slot) * ctas + rank) * (static_cast<long long>(BM) * tile_n);
+  return a.ts_part + (static_cast<long long>(slot) * ctas + rank) * (static_cast<long long>(BM) * tile_n);
 }
 
 // One TMA box into this CTA's stage; its bytes are counted on the leader's
@@ -1452,7 +1452,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             tmem_ld32(tbase + c * 32, v);
             if (wk.cut) {
               if (valid) {
-                float* sp = sk_slot_ptr(args, wk.slot, static_cast<int>(rank), CTAS, C::kTileN) +
+                float* sp = ts_slot_ptr(args, wk.slot, static_cast<int>(rank), CTAS, C::kTileN) +
                             (c * 8 * BM + lrow_in_tile) * 4;
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj)
@@ -1487,7 +1487,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             if (wk.cut) {
               // A piece of a split unit: its fp32 partial tile goes to its slot.
               if (valid) {
-                float* sp = sk_slot_ptr(args, wk.slot, static_cast<int>(rank), CTAS, C::kTileN) +
+                float* sp = ts_slot_ptr(args, wk.slot, static_cast<int>(rank), CTAS, C::kTileN) +
                             (c * 8 * BM + lrow_in_tile) * 4;
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj)
@@ -1558,34 +1558,34 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
   }
 }
 
-// Adds the pieces of every dH-type unit that the tail split cut (see SkSplit)
+// Adds the pieces of every dH-type unit that the tail split cut (see TailSplit)
 // in a fixed order, its main piece and then its tails in pair order, and
 // writes the unit's bf16 dH rows (kUacc: applies the single pass's U update to
 // the sum instead, as the U GEMM's epilogue does). Grid: (the launch's host-side bound on units) x (32-
 // column chunks of a unit); one thread per row of the unit. Units that ran
 // whole return at once. `a` is the dH launch's own TileArgs.
 template <int CTAS, bool kUacc>
-__global__ void __launch_bounds__(BM * CTAS) sk_fixup_kernel(const TileArgs a) {
+__global__ void __launch_bounds__(BM * CTAS) tail_fixup_kernel(const TileArgs a) {
   constexpr int kTileN = PairCfg<MODE_DH, CTAS>::kTileN;
-  __shared__ SkSplit sp_sh;
+  __shared__ TailSplit sp_sh;
   __shared__ long long p0_sh;
   const int n_rb = launch_row_blocks(a);
   const int n_ru = (n_rb + CTAS - 1) / CTAS;
   const int n_units = n_ru * a.n_cols;
   const int u = static_cast<int>(blockIdx.x);
   // Only units of a last round with fewer units than pairs can be cut.
-  if (a.sk_slots <= 0 || u >= n_units || u < n_units - n_units % a.sk_slots) return;
+  if (a.ts_slots <= 0 || u >= n_units || u < n_units - n_units % a.ts_slots) return;
   int ru, col;
   decode_unit(u, n_ru, a.n_cols, a.group_rows, ru, col);
   const int c = static_cast<int>(blockIdx.y);
   const int d0 = col * kTileN + c * 32;
   if (d0 >= a.hidden) return;
   if (threadIdx.x == 0) {
-    sp_sh = sk_split<CTAS>(a, n_ru, n_units, a.sk_slots);
-    p0_sh = sp_sh.n_tail > 0 ? sk_tail_prefix(a, n_ru, sp_sh, u) : 0;
+    sp_sh = tail_split<CTAS>(a, n_ru, n_units, a.ts_slots);
+    p0_sh = sp_sh.n_tail > 0 ? ts_tail_prefix(a, n_ru, sp_sh, u) : 0;
   }
   __syncthreads();
-  const SkSplit& sp = sp_sh;
+  const TailSplit& sp = sp_sh;
   if (sp.n_tail == 0) return;
   const bool last = col == a.n_cols - 1;
   const int m = last ? sp.m_l : sp.m_f;
@@ -1593,11 +1593,11 @@ __global__ void __launch_bounds__(BM * CTAS) sk_fixup_kernel(const TileArgs a) {
   const long long t = last ? sp.t_l : sp.t_f;
   if (t == 0) return;  // the main piece was the whole unit
   const long long p0 = p0_sh;
-  const int qa = sk_tail_pair_of(sp, p0);
-  const int qb = sk_tail_pair_of(sp, p0 + t - 1);
-  // Stages of tail pair q's piece of this unit (as sk_tail_piece).
+  const int qa = ts_tail_pair_of(sp, p0);
+  const int qb = ts_tail_pair_of(sp, p0 + t - 1);
+  // Stages of tail pair q's piece of this unit (as ts_tail_piece).
   auto piece = [&](int q, int& kb, int& ke) {
-    const long long q0 = sk_tail_start(sp, q), q1 = sk_tail_start(sp, q + 1);
+    const long long q0 = ts_tail_start(sp, q), q1 = ts_tail_start(sp, q + 1);
     kb = m + static_cast<int>((max(q0, p0) - p0) / cs);
     ke = m + static_cast<int>((min(q1, p0 + t) - p0) / cs);
   };
@@ -1622,7 +1622,7 @@ __global__ void __launch_bounds__(BM * CTAS) sk_fixup_kernel(const TileArgs a) {
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = 0.f;
   auto add_slot = [&](int slot) {
-    const float* src = sk_slot_ptr(a, slot, rank, CTAS, kTileN) + (c * 8 * BM + lrow) * 4;
+    const float* src = ts_slot_ptr(a, slot, rank, CTAS, kTileN) + (c * 8 * BM + lrow) * 4;
 #pragma unroll
     for (int jj = 0; jj < 8; ++jj) {
       const float4 x = *reinterpret_cast<const float4*>(src + jj * BM * 4);
@@ -1632,11 +1632,11 @@ __global__ void __launch_bounds__(BM * CTAS) sk_fixup_kernel(const TileArgs a) {
       v[4 * jj + 3] += x.w;
     }
   };
-  if (m > 0) add_slot(sk_main_slot(sp, u));
+  if (m > 0) add_slot(ts_main_slot(sp, u));
   for (int q = qa; q <= qb; ++q) {
     int kb, ke;
     piece(q, kb, ke);
-    if (ke > kb) add_slot(sk_tail_slot(sp, u, q));
+    if (ke > kb) add_slot(ts_tail_slot(sp, u, q));
   }
   __nv_bfloat16* out = a.dH + grow * a.hidden + d0;
   if constexpr (kUacc) {

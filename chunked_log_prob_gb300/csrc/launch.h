@@ -160,10 +160,10 @@ cudaError_t launch_dh_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap
                            const TileArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_dhs_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                             const TileArgs& args, int grid, cudaStream_t stream);
-// After a tail-split dH-type launch (args.sk_part set): adds the pieces of its
+// After a tail-split dH-type launch (args.ts_part set): adds the pieces of its
 // cut units and writes their dH rows (uacc: a U GEMM's units, whose sum goes
 // through the single pass's U update). `units`: the launch's host-side bound.
-cudaError_t launch_sk_fixup(int ctas, const TileArgs& args, int units, bool uacc,
+cudaError_t launch_tail_fixup(int ctas, const TileArgs& args, int units, bool uacc,
                             cudaStream_t stream);
 // map_a: one vocabulary block of stored fp16 logits [rows][width] (64 x 128
 // boxes, 128-byte swizzle); map_b: W MN-major (64 x 64 boxes).

@@ -45,7 +45,7 @@ def _call(clp, p, old, params, ws):
 
 @pytest.mark.parametrize("D, V, want_g", [(2304, 3000, "finalize_gform_kernel"),
                                           (1536, 3000, "finalize_rows_kernel"),
-                                          (1536, 9000, "sk_fixup_kernel")])
+                                          (1536, 9000, "tail_fixup_kernel")])
 def test_timing_records_every_launch_of_a_call(clp, D, V, want_g):
     # V = 9000: a vocabulary loop long enough for the tail split, so the fused
     # dH launch (at most 8 pair row units x 3 hidden tiles, fewer than the SM

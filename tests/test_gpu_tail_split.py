@@ -242,7 +242,7 @@ def test_tail_split_single_pass(clp, name, prompts, G, T, D, V, lengths, chunk, 
     finally:
         clp.grpo_launch_timing_enable(False)
     times = {k["name"]: k["launches"] for k in clp.grpo_launch_timing_read()}
-    assert times.get("sk_fixup_kernel", 0) == 2 * plan["n_chunks"] * plan["n_vocab_blocks"]
+    assert times.get("tail_fixup_kernel", 0) == 2 * plan["n_chunks"] * plan["n_vocab_blocks"]
     assert sum(times.values()) == 2 * plan["launches_loss"]
     L, logp, dH = outs[0]
     m = p.mask.numpy().astype(bool)
@@ -288,7 +288,7 @@ def test_tail_split_overlapped_schedule_last_chunk(clp):
     finally:
         clp.grpo_launch_timing_enable(False)
     times = {k["name"]: k["launches"] for k in clp.grpo_launch_timing_read()}
-    assert times.get("sk_fixup_kernel", 0) == 2
+    assert times.get("tail_fixup_kernel", 0) == 2
     assert sum(times.values()) == 2 * plan["launches_loss"]
     L, logp, dH = outs[0]
     m = p.mask.numpy().astype(bool)
