@@ -434,9 +434,11 @@ __device__ __forceinline__ int mn_out_cols(const TileArgs& a, int col0) {
 }
 
 // ---------------------------------------------------------------------------
-// Tail split of a dH launch (MODE_DH, MODE_DHS over the whole vocabulary).
-// Its units (row unit x hidden tile) each run a K loop over the vocabulary,
-// and the pairs run them whole, one per pair and round. When the last round
+// Tail split of a dH-type launch (MODE_DH, MODE_DHS over the whole vocabulary;
+// MODE_UAC, MODE_UAP over one vocabulary block, whose cut units the fixup
+// passes through the U update). Its units (row unit x hidden tile) each run a
+// K loop over the vocabulary, and the pairs run them whole, one per pair and
+// round. When the last round
 // has fewer units (U) than pairs, the pairs without one would idle (66 units
 // on 76 pairs: 13 % of the launch). Instead, each of those U units runs on its
 // own pair only up to a balance point m of its K loop (its main piece), and Q

@@ -163,10 +163,10 @@ def stored_block(chunk, V):
     return chunk * (-(-V // 8) * 8 * 2 + -(-V // 64) * 4)
 
 
-# The stored form's stream-K partial slots (vocabularies of at least 128 K
+# The stored form's tail-split partial slots (vocabularies of at least 128 K
 # stages): two fp32 tiles of 256 rows x 512 hidden columns for each of the 76
 # SM pairs the sizing assumes. Fixed: independent of N, the chunk and V.
-SK_BYTES = 2 * 76 * 256 * 512 * 4
+TAIL_SPLIT_BYTES = 2 * 76 * 256 * 512 * 4
 
 
 def test_stored_logit_workspace_is_chunk_times_vocab(clp):
@@ -175,15 +175,15 @@ def test_stored_logit_workspace_is_chunk_times_vocab(clp):
     p = clp.make_params(chunk_tokens=2048, flags=1)
     a = clp.grpo_workspace_size(16384, 4096, 128256, 1, p)
     b = clp.grpo_workspace_size(65536, 4096, 128256, 1, p)
-    block = stored_block(2048, 128256) + SK_BYTES
-    assert 2 * block - SK_BYTES < a < 2 * block - SK_BYTES + 16384 * 400
+    block = stored_block(2048, 128256) + TAIL_SPLIT_BYTES
+    assert 2 * block - TAIL_SPLIT_BYTES < a < 2 * block - TAIL_SPLIT_BYTES + 16384 * 400
     one = clp.grpo_workspace_size(2048, 4096, 128256, 1, p)  # a single chunk: one block
     assert block < one < block + 2048 * 400
     assert (b - a) / (65536 - 16384) < 64 * 4 * 2 + 64
     # Automatic chunk without a device: bounded by 2 GiB of fp16 logits per
     # block (plus their box maxima, 1/32 of that).
     auto = clp.grpo_workspace_size(131072, 2880, 201088, 1, clp.make_params(flags=1))
-    assert auto < 2 * (2 << 30) * (1 + 1 / 32) + SK_BYTES + 131072 * 400
+    assert auto < 2 * (2 << 30) * (1 + 1 / 32) + TAIL_SPLIT_BYTES + 131072 * 400
 
 
 def test_stored_logit_workspace_single_block_up_to_2048_hidden(clp):
@@ -193,11 +193,11 @@ def test_stored_logit_workspace_single_block_up_to_2048_hidden(clp):
     p = clp.make_params(chunk_tokens=2048, flags=1)
     block = stored_block(2048, 151936)
     small = clp.grpo_workspace_size(32768, 2048, 151936, 1, p)
-    assert block + SK_BYTES < small < block + SK_BYTES + 32768 * 400
+    assert block + TAIL_SPLIT_BYTES < small < block + TAIL_SPLIT_BYTES + 32768 * 400
     big = clp.grpo_workspace_size(32768, 2056, 151936, 1, p)
-    assert 2 * block + SK_BYTES < big < 2 * block + SK_BYTES + 32768 * 400
+    assert 2 * block + TAIL_SPLIT_BYTES < big < 2 * block + TAIL_SPLIT_BYTES + 32768 * 400
     auto = clp.grpo_workspace_size(131072, 1536, 151936, 1, clp.make_params(flags=1))
-    assert (2 << 30) < auto < (4 << 30) * (1 + 1 / 32) + SK_BYTES + 131072 * 400
+    assert (2 << 30) < auto < (4 << 30) * (1 + 1 / 32) + TAIL_SPLIT_BYTES + 131072 * 400
 
 
 @pytest.mark.parametrize("flags", [16, 1, 0])
