@@ -328,7 +328,7 @@ _FIRST_KERNEL = "row_plan_kernel"  # every grpo_loss_fwd_bwd call starts with it
 LIBRARY_KERNELS = ("tc_gemm_kernel", "finalize_kernel", "finalize_gform_kernel",
                    "finalize_rows_kernel", "single_pass_p_kernel", "finish_loss_kernel",
                    "row_plan_kernel", "zero_padding_blocks_kernel", "seq_lens_kernel",
-                   "tail_fixup_kernel", "bounded_wait_selftest_kernel")
+                   "tail_fixup_kernel", "gather_blocks_kernel", "bounded_wait_selftest_kernel")
 
 
 def ncu_launches(csv_path):

@@ -96,8 +96,9 @@ struct Layout {
   double model_cost;  // modelled GEMM time of the plan in forward-tile times (0: no device)
   int nbox;         // stored path: 64-column boxes per row (their maxima are kept)
   int ts_slots;     // stored path: pairs of the tail-split dH launches (0: no split)
+  int n_hc;         // chunk copies of h (the rows of non-consecutive row blocks): 1
   size_t off_pm, off_ps, off_zy, off_lse, off_g, off_rbl, off_lt, off_seq, off_sk, off_G,
-      off_bmax, off_acc, total;
+      off_bmax, off_acc, off_hc, total;
 };
 
 // Tail split (see TailSplit in gemm_tc.cuh): a dH-type launch whose last round
@@ -386,7 +387,7 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, Form fo
   L->off_zy = off; off = align_up(off + L->nr * sizeof(float), 256);
   L->off_lse = off; off = align_up(off + L->nr * sizeof(float), 256);
   L->off_g = off; off = align_up(off + L->nr * sizeof(float), 256);
-  L->off_rbl = off; off = align_up(off + (L->nr / BM) * sizeof(int), 256);
+  L->off_rbl = off; off = align_up(off + (L->nr / SEG) * sizeof(int), 256);
   L->off_lt = off; off = align_up(off + L->nr * sizeof(double), 256);
   L->off_seq = off; off = align_up(off + L->nr * sizeof(int), 256);  // >= N / T lengths
   // Tail-split slots: stored form, single pass with P on chip; not under a
@@ -412,10 +413,14 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, Form fo
   // one when the dH GEMM forms G itself.
   const int sbufs = (L->stored || L->single_pass) && !L->fused ? 2 : 1;
   const bool boxes = L->stored || L->single_pass;  // fp16 logits with box maxima
+  // A chunk's copy of h for the row blocks whose active segments are not
+  // consecutive rows (read by its logit or G-tile GEMMs, which run one chunk
+  // after another on the caller's stream; the dW GEMM reads h itself).
+  const int hc_bufs = 1;
   const size_t unit_bytes = static_cast<size_t>(ru_rows) *
                             (static_cast<size_t>(L->vblock) * 2 * sbufs +
                              (boxes ? static_cast<size_t>(L->nbox) * 4 * sbufs : 0) +
-                             (L->need_acc ? L->D * 4 : 0));
+                             (L->need_acc ? L->D * 4 : 0) + static_cast<size_t>(L->D) * 2 * hc_bufs);
   long long max_units = L->stored        ? std::max(1, stored_max_blocks(L->ldS, sbufs) / L->ctas)
                         : L->single_pass ? kMaxSinglePassChunkBlocks / L->ctas
                                          : kMaxAutoChunkBlocks / L->ctas;
@@ -491,6 +496,9 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, Form fo
     off = align_up(off + static_cast<size_t>(L->n_sbuf) * L->nbox * L->chunk_rows * 4, 256);
   L->off_acc = off;
   if (L->need_acc) off = align_up(off + static_cast<size_t>(L->chunk_rows) * L->D * 4, 256);
+  L->n_hc = hc_bufs;
+  L->off_hc = off;
+  off = align_up(off + static_cast<size_t>(L->n_hc) * L->chunk_rows * L->D * 2, 256);
   L->total = off;
   if (budget > 0 && L->total > budget) return GRPO_ERR_WORKSPACE_TOO_SMALL;
   if (sms > 0) {
@@ -706,11 +714,12 @@ struct Ws {
   double* msum;
   double* partials;
   double* lt;
-  int* n_active;
+  int* n_seg;     // length of the active-segment list
   int* n_nonempty;
   int* seq_lens;
-  int* rb_list;
+  int* seg_list;  // the active 16-row segments (row plan)
   float *pm, *ps, *zy, *lse, *g, *acc, *sk;
+  __nv_bfloat16* hc;  // chunk copies of h's rows (Layout::n_hc of chunk_rows x D)
   __nv_bfloat16* G;
 };
 
@@ -721,10 +730,10 @@ Ws carve(void* ws, const Layout& L) {
   w.counter = reinterpret_cast<unsigned*>(w.base + kOffCounter);
   w.msum = reinterpret_cast<double*>(w.base + kOffMsum);
   w.partials = reinterpret_cast<double*>(w.base + kOffPartials);
-  w.n_active = reinterpret_cast<int*>(w.base + kOffActive);
+  w.n_seg = reinterpret_cast<int*>(w.base + kOffActive);
   w.n_nonempty = reinterpret_cast<int*>(w.base + kOffNonempty);
   w.seq_lens = reinterpret_cast<int*>(w.base + L.off_seq);
-  w.rb_list = reinterpret_cast<int*>(w.base + L.off_rbl);
+  w.seg_list = reinterpret_cast<int*>(w.base + L.off_rbl);
   w.lt = reinterpret_cast<double*>(w.base + L.off_lt);
   w.pm = reinterpret_cast<float*>(w.base + L.off_pm);
   w.ps = reinterpret_cast<float*>(w.base + L.off_ps);
@@ -734,6 +743,7 @@ Ws carve(void* ws, const Layout& L) {
   w.G = reinterpret_cast<__nv_bfloat16*>(w.base + L.off_G);
   w.acc = reinterpret_cast<float*>(w.base + L.off_acc);
   w.sk = L.ts_slots > 0 ? reinterpret_cast<float*>(w.base + L.off_sk) : nullptr;
+  w.hc = reinterpret_cast<__nv_bfloat16*>(w.base + L.off_hc);
   return w;
 }
 
@@ -747,13 +757,14 @@ TileArgs base_args(const Layout& L, const Ws& w) {
 }
 
 // Forward logit GEMM: per-split (max, sum-exp) and z_y for every row of the
-// row blocks in `rb_list` (all row blocks when it is null).
+// active segments in `seg_list` (every row when it is null).
 int run_forward(const void* hidden, const void* W, const int32_t* ids, const uint8_t* mask,
-                const int* rb_list, const int* n_active, const grpo_params* prm,
+                const int* seg_list, const int* n_seg, const grpo_params* prm,
                 const Layout& L, const Ws& w, int sms, int* splits_out, cudaStream_t st) {
-  CUtensorMap map_h, map_w;
+  CUtensorMap map_h, map_h16, map_w;
   const int slots = std::max(1, sms / L.ctas);
   if (!encode_2d(&map_h, hidden, L.D, L.n, L.D, BK, BM) ||
+      !encode_2d(&map_h16, hidden, L.D, L.n, L.D, BK, SEG) ||
       !encode_2d(&map_w, W, L.D, L.V, L.D, BK, BN / L.ctas))
     return GRPO_ERR_CUDA;
   TileArgs a = base_args(L, w);
@@ -761,8 +772,8 @@ int run_forward(const void* hidden, const void* W, const int32_t* ids, const uin
   a.n_total = L.n;
   a.n_rb = static_cast<int>(L.nr / BM);
   a.rb_offset = 0;
-  a.rb_list = rb_list;
-  a.n_active = n_active;
+  a.seg_list = seg_list;
+  a.n_seg = n_seg;
   a.k_iters = static_cast<int>(cdiv(L.D, BK));
   const int n_ru = static_cast<int>(cdiv(a.n_rb, L.ctas));
   a.group_rows = (prm != nullptr && prm->raster_rows > 0) ? std::min(prm->raster_rows, n_ru)
@@ -780,7 +791,8 @@ int run_forward(const void* hidden, const void* W, const int32_t* ids, const uin
   a.part_ld = L.nr;
   const long long units = static_cast<long long>(n_ru) * a.n_cols;
   const int grid = L.ctas * static_cast<int>(std::min<long long>(units, slots));
-  if (launch_fwd_gemm(L.ctas, map_h, map_w, a, grid, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  if (launch_fwd_gemm(L.ctas, map_h, map_w, map_h16, a, grid, st) != cudaSuccess)
+    return GRPO_ERR_CUDA;
   *splits_out = splits;
   return GRPO_OK;
 }
@@ -791,9 +803,10 @@ int launch_dw(const void* hidden, const __nv_bfloat16* G, long long ldG, int v0,
               int rb0, int n_rb, float* dW, bool first, const Layout& L, const Ws& w, int sms,
               cudaStream_t st) {
   const int slots = std::max(1, sms / L.ctas);
-  CUtensorMap map_gt, map_h_mn, map_dw;
+  CUtensorMap map_gt, map_h_mn, map_h16, map_dw;
   if (!encode_2d(&map_gt, G, width, static_cast<uint64_t>(n_rb) * BM, ldG, 64, BK) ||
       !encode_2d(&map_h_mn, hidden, L.D, L.n, L.D, 64, BK) ||
+      !encode_2d(&map_h16, hidden, L.D, L.n, L.D, 64, SEG) ||
       !encode_2d(&map_dw, dW + static_cast<size_t>(v0) * L.D, L.D, width, L.D, 32, 32,
                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4))
     return GRPO_ERR_CUDA;
@@ -801,8 +814,8 @@ int launch_dw(const void* hidden, const __nv_bfloat16* G, long long ldG, int v0,
   a.n_total = L.n;
   a.n_rb = n_rb;
   a.rb_offset = rb0;
-  a.rb_list = w.rb_list;
-  a.n_active = w.n_active;
+  a.seg_list = w.seg_list;
+  a.n_seg = w.n_seg;
   const int n_vu = static_cast<int>(cdiv(width, static_cast<long long>(BM) * L.ctas));
   const int n_dt = static_cast<int>(cdiv(L.D, BN));
   a.group_rows = group_rows_for(n_vu, slots);
@@ -812,7 +825,7 @@ int launch_dw(const void* hidden, const __nv_bfloat16* G, long long ldG, int v0,
   a.dW = dW;
   a.first = first ? 1 : 0;
   const long long units = static_cast<long long>(n_vu) * n_dt;
-  if (launch_dw_gemm(L.ctas, map_gt, map_h_mn, map_dw, a,
+  if (launch_dw_gemm(L.ctas, map_gt, map_h_mn, map_h16, map_dw, a,
                      L.ctas * static_cast<int>(std::min<long long>(units, slots)),
                      st) != cudaSuccess)
     return GRPO_ERR_CUDA;
@@ -825,9 +838,10 @@ int launch_dw(const void* hidden, const __nv_bfloat16* G, long long ldG, int v0,
 int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH, float* dW,
                  const grpo_params* prm, const Layout& L, const Ws& w, int sms,
                  cudaStream_t st) {
-  CUtensorMap map_h, map_w_k, map_w_mn;
+  CUtensorMap map_h, map_h16, map_w_k, map_w_mn;
   const int slots = std::max(1, sms / L.ctas);
   if (!encode_2d(&map_h, hidden, L.D, L.n, L.D, BK, BM) ||
+      !encode_2d(&map_h16, hidden, L.D, L.n, L.D, BK, SEG) ||
       !encode_2d(&map_w_k, W, L.D, L.V, L.D, BK, BN / L.ctas) ||
       !encode_2d(&map_w_mn, W, L.D, L.V, L.D, 64, BK))
     return GRPO_ERR_CUDA;
@@ -837,6 +851,20 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
   for (int rb0 = 0; rb0 < n_rb_total; rb0 += rb_per_chunk) {
     const int n_rb = std::min(rb_per_chunk, n_rb_total - rb0);
     const int n_ru = static_cast<int>(cdiv(n_rb, L.ctas));
+    // The chunk's non-consecutive row blocks of h, copied once for every
+    // vocab block's G-tile GEMM.
+    CUtensorMap map_hc;
+    if (!encode_2d(&map_hc, w.hc, L.D, static_cast<uint64_t>(n_rb) * BM, L.D, BK, BM))
+      return GRPO_ERR_CUDA;
+    {
+      TileArgs gh = base_args(L, w);
+      gh.n_total = L.n;
+      gh.n_rb = n_rb;
+      gh.rb_offset = rb0;
+      gh.seg_list = w.seg_list;
+      gh.n_seg = w.n_seg;
+      if (launch_gather_blocks(hidden, w.hc, gh, st) != cudaSuccess) return GRPO_ERR_CUDA;
+    }
     for (long long v0 = 0; v0 < L.V; v0 += L.vblock) {
       const int width = static_cast<int>(std::min<long long>(L.vblock, L.V - v0));
       const int ntile = static_cast<int>(cdiv(width, BN));
@@ -846,8 +874,8 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
       a.n_total = L.n;
       a.n_rb = n_rb;
       a.rb_offset = rb0;
-      a.rb_list = w.rb_list;
-      a.n_active = w.n_active;
+      a.seg_list = w.seg_list;
+      a.n_seg = w.n_seg;
       a.k_iters = static_cast<int>(cdiv(L.D, BK));
       a.group_rows = (prm != nullptr && prm->raster_rows > 0) ? std::min(prm->raster_rows, n_ru)
                                                              : group_rows_exact(n_ru, slots);
@@ -858,14 +886,15 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
       a.g = w.g;
       a.G = w.G;
       a.ldG = L.vblock;
+      a.hc = 1;
       long long units = static_cast<long long>(n_ru) * ntile;
       CUtensorMap map_gst;  // the pair variant stores G through TMA
       if (!encode_2d(&map_gst, w.G, L.vblock, static_cast<uint64_t>(n_rb) * BM, L.vblock, 64,
                      32))
         return GRPO_ERR_CUDA;
-      if (launch_bwdg_gemm(L.ctas, map_h, map_w_k, map_gst, a,
-                           L.ctas * static_cast<int>(std::min<long long>(units, slots)),
-                           st) != cudaSuccess)
+      if (launch_bwdg_gemm(L.ctas, map_h, map_w_k, map_h16, map_gst, a,
+                           L.ctas * static_cast<int>(std::min<long long>(units, slots)), st,
+                           &map_hc) != cudaSuccess)
         return GRPO_ERR_CUDA;
       // (2) dH_chunk (+)= G W[v0 : v0 + width].
       CUtensorMap map_g;
@@ -875,8 +904,8 @@ int run_backward(const void* hidden, const void* W, const int32_t* ids, void* dH
       b.n_total = L.n;
       b.n_rb = n_rb;
       b.rb_offset = rb0;
-      b.rb_list = w.rb_list;
-      b.n_active = w.n_active;
+      b.seg_list = w.seg_list;
+      b.n_seg = w.n_seg;
       b.k_iters = static_cast<int>(cdiv(width, BK));
       b.group_rows = group_rows_for(n_ru, slots);
       b.n_cols = n_dt_dh;
@@ -912,9 +941,10 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
                const float* old_logp, const float* ref_logp, const float* adv, float* loss,
                float* logp_out, void* dH, float* dW, const grpo_params* prm, const Layout& L,
                const Ws& w, int sms, cudaStream_t st) {
-  CUtensorMap map_h, map_w_k, map_w_mn;
+  CUtensorMap map_h, map_h16, map_w_k, map_w_mn;
   const int slots = std::max(1, sms / L.ctas);
   if (!encode_2d(&map_h, hidden, L.D, L.n, L.D, BK, BM) ||
+      !encode_2d(&map_h16, hidden, L.D, L.n, L.D, BK, SEG) ||
       !encode_2d(&map_w_k, W, L.D, L.V, L.D, BK, BN / L.ctas) ||
       !encode_2d(&map_w_mn, W, L.D, L.V, L.D, 64, BK))
     return GRPO_ERR_CUDA;
@@ -962,8 +992,8 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     a.n_total = L.n;
     a.n_rb = n_rb;
     a.rb_offset = c * rb_per_chunk;
-    a.rb_list = w.rb_list;
-    a.n_active = w.n_active;
+    a.seg_list = w.seg_list;
+    a.n_seg = w.n_seg;
     a.k_iters = static_cast<int>(cdiv(L.D, BK));
     a.group_rows = n_ru;
     a.n_cols = splits;
@@ -980,14 +1010,18 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     a.box_max = bmax(c);
     a.ldM = L.chunk_rows;
     // The pair variant stores each warp's 32 rows x 64 logits through TMA.
-    CUtensorMap map_st;
-    if (!encode_2d(&map_st, a.S, L.V, static_cast<uint64_t>(n_rb) * BM, L.ldS, 64, 32))
+    CUtensorMap map_st, map_hc;
+    if (!encode_2d(&map_st, a.S, L.V, static_cast<uint64_t>(n_rb) * BM, L.ldS, 64, 32) ||
+        !encode_2d(&map_hc, w.hc, L.D, static_cast<uint64_t>(n_rb) * BM, L.D, BK, BM))
       return GRPO_ERR_CUDA;
+    // The chunk's non-consecutive row blocks of h, copied for the GEMM.
+    a.hc = 1;
+    if (launch_gather_blocks(hidden, w.hc, a, st) != cudaSuccess) return GRPO_ERR_CUDA;
     const long long units = static_cast<long long>(n_ru) * splits;
     *splits_out = splits;
-    return launch_fwds_gemm(L.ctas, map_h, map_w_k, map_st, a,
-                            L.ctas * static_cast<int>(std::min<long long>(units, slots)),
-                            st) == cudaSuccess
+    return launch_fwds_gemm(L.ctas, map_h, map_w_k, map_h16, map_st, a,
+                            L.ctas * static_cast<int>(std::min<long long>(units, slots)), st,
+                            &map_hc) == cudaSuccess
                ? GRPO_OK
                : GRPO_ERR_CUDA;
   };
@@ -999,8 +1033,8 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     f.n_total = L.n;
     f.n_rb = n_rb;
     f.rb_offset = c * rb_per_chunk;
-    f.rb_list = w.rb_list;
-    f.n_active = w.n_active;
+    f.seg_list = w.seg_list;
+    f.n_seg = w.n_seg;
     f.splits = splits;
     f.part_ld = L.nr;
     f.vocab = L.V;
@@ -1061,8 +1095,8 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     b.n_total = L.n;
     b.n_rb = n_rb;
     b.rb_offset = c * rb_per_chunk;
-    b.rb_list = w.rb_list;
-    b.n_active = w.n_active;
+    b.seg_list = w.seg_list;
+    b.n_seg = w.n_seg;
     b.k_iters = static_cast<int>(cdiv(L.V, BK));
     b.group_rows = group_rows_for(n_ru, slots);
     b.n_cols = n_dt_dh;
@@ -1096,8 +1130,8 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     b.n_total = L.n;
     b.n_rb = n_rb;
     b.rb_offset = c * rb_per_chunk;
-    b.rb_list = w.rb_list;
-    b.n_active = w.n_active;
+    b.seg_list = w.seg_list;
+    b.n_seg = w.n_seg;
     b.k_iters = static_cast<int>(cdiv(L.V, BK));
     b.group_rows = group_rows_for(n_ru, slots);
     b.n_cols = n_dt_dh;
@@ -1198,9 +1232,10 @@ int run_single_pass(const void* hidden, const void* W, const int32_t* ids, const
                     const float* old_logp, const float* ref_logp, const float* adv, float* loss,
                     float* logp_out, void* dH, const grpo_params* prm, const Layout& L,
                     const Ws& w, int sms, cudaStream_t st) {
-  CUtensorMap map_h, map_w_k, map_w_mn;
+  CUtensorMap map_h, map_h16, map_w_k, map_w_mn;
   const int slots = std::max(1, sms / L.ctas);
   if (!encode_2d(&map_h, hidden, L.D, L.n, L.D, BK, BM) ||
+      !encode_2d(&map_h16, hidden, L.D, L.n, L.D, BK, SEG) ||
       !encode_2d(&map_w_k, W, L.D, L.V, L.D, BK, BN / L.ctas) ||
       !encode_2d(&map_w_mn, W, L.D, L.V, L.D, 64, BK))
     return GRPO_ERR_CUDA;
@@ -1239,8 +1274,8 @@ int run_single_pass(const void* hidden, const void* W, const int32_t* ids, const
     f.n_total = L.n;
     f.n_rb = chunk_rbs(c);
     f.rb_offset = c * rb_per_chunk;
-    f.rb_list = w.rb_list;
-    f.n_active = w.n_active;
+    f.seg_list = w.seg_list;
+    f.n_seg = w.n_seg;
     f.part_ld = L.nr;
     f.vocab = L.V;
     f.seq_len = L.T;
@@ -1286,8 +1321,8 @@ int run_single_pass(const void* hidden, const void* W, const int32_t* ids, const
     a.n_total = L.n;
     a.n_rb = n_rb;
     a.rb_offset = c * rb_per_chunk;
-    a.rb_list = w.rb_list;
-    a.n_active = w.n_active;
+    a.seg_list = w.seg_list;
+    a.n_seg = w.n_seg;
     a.k_iters = static_cast<int>(cdiv(L.D, BK));
     a.group_rows = n_ru;
     a.n_cols = splits;
@@ -1304,13 +1339,18 @@ int run_single_pass(const void* hidden, const void* W, const int32_t* ids, const
     a.ldS = L.ldS;
     a.box_max = bmax(i);
     a.ldM = L.chunk_rows;
-    CUtensorMap map_st;
-    if (!encode_2d(&map_st, a.S, width, static_cast<uint64_t>(n_rb) * BM, L.ldS, 64, 32))
+    CUtensorMap map_st, map_hc;
+    if (!encode_2d(&map_st, a.S, width, static_cast<uint64_t>(n_rb) * BM, L.ldS, 64, 32) ||
+        !encode_2d(&map_hc, w.hc, L.D, static_cast<uint64_t>(n_rb) * BM, L.D, BK, BM))
       return GRPO_ERR_CUDA;
-    return launch_fwds_gemm(L.ctas, map_h, map_w_k, map_st, a,
+    // The chunk's non-consecutive row blocks of h, copied once before its
+    // first block's logit GEMM (the blocks of a chunk run in a row).
+    a.hc = 1;
+    if (b == 0 && launch_gather_blocks(hidden, w.hc, a, st) != cudaSuccess) return GRPO_ERR_CUDA;
+    return launch_fwds_gemm(L.ctas, map_h, map_w_k, map_h16, map_st, a,
                             L.ctas * static_cast<int>(std::min<long long>(
                                          static_cast<long long>(n_ru) * splits, slots)),
-                            st) == cudaSuccess
+                            st, &map_hc) == cudaSuccess
                ? GRPO_OK
                : GRPO_ERR_CUDA;
   };
@@ -1349,8 +1389,8 @@ int run_single_pass(const void* hidden, const void* W, const int32_t* ids, const
     u.n_total = L.n;
     u.n_rb = n_rb;
     u.rb_offset = c * rb_per_chunk;
-    u.rb_list = w.rb_list;
-    u.n_active = w.n_active;
+    u.seg_list = w.seg_list;
+    u.n_seg = w.n_seg;
     u.k_iters = static_cast<int>(cdiv(width, BK));
     u.group_rows = group_rows_for(n_ru, slots);
     u.n_cols = n_dt_dh;
@@ -1655,7 +1695,8 @@ int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
   }
   Ws w = carve(workspace, L);
   const int n_rb_total = static_cast<int>(L.nr / BM);
-  if (launch_row_plan(mask, L.n, n_rb_total, w.rb_list, w.n_active, w.msum, st) != cudaSuccess ||
+  if (launch_row_plan(mask, L.n, static_cast<int>(L.nr / SEG), w.seg_list, w.n_seg, w.msum, st) !=
+          cudaSuccess ||
       launch_zero_padding_blocks(mask, L.n, n_rb_total, L.D, dH, sms, st) != cudaSuccess)
     return GRPO_ERR_CUDA;
   if ((prm.flags & GRPO_FLAG_SEQUENCE_MEAN) != 0 &&
@@ -1683,7 +1724,7 @@ int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
     w = carve(workspace, L);
   }
   int splits = 1;
-  if ((r = run_forward(hidden, W, ids, mask, w.rb_list, w.n_active, &prm, L, w, sms, &splits,
+  if ((r = run_forward(hidden, W, ids, mask, w.seg_list, w.n_seg, &prm, L, w, sms, &splits,
                        st)) != GRPO_OK)
     return r;
   FinalizeArgs f;
@@ -1746,13 +1787,14 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
   // pass's U GEMMs that nothing runs beside) are each followed by a fixup pass.
   const bool tail_split = L.ts_slots > 0 && (L.fused || L.n_sbuf == 1);
   const int stored_fixups = L.ts_slots == 0 ? 0 : tail_split ? info->n_chunks : 1;
+  // Every form gathers each chunk's non-consecutive row blocks of h once.
   info->launches_loss = L.n <= 0        ? 0
-                        : L.stored      ? 3 + 3 * info->n_chunks + stored_fixups
+                        : L.stored      ? 3 + 4 * info->n_chunks + stored_fixups
                         : L.single_pass ? 3 + info->n_chunks *
                                                   (((L.fused ? 2 : 3) + (tail_split ? 1 : 0)) *
                                                        L.nvb +
-                                                   1)
-                                        : 4 + 2 * info->n_chunks * info->n_vocab_blocks;
+                                                   2)
+                                        : 4 + (2 * info->n_vocab_blocks + 1) * info->n_chunks;
   if (L.n > 0 && params != nullptr && (params->flags & GRPO_FLAG_SEQUENCE_MEAN) != 0)
     info->launches_loss += 1;
   if (L.stored) {
@@ -1914,8 +1956,9 @@ extern "C" int grpo_logp_fwd_noalloc(const void* hidden, const void* W, const in
   if ((r = device_setup(&sms)) != GRPO_OK) return r;
   Layout L;
   if ((r = make_layout(shape, nullptr, sms, &L)) != GRPO_OK) return r;
-  // The forward uses the workspace only up to the backward's G block.
-  if (L.off_G > GRPO_NOALLOC_SCRATCH_BYTES) return GRPO_ERR_UNSUPPORTED_SHAPE;
+  // The forward uses the workspace only up to the backward's part (the tail
+  // split's slots, then the chunk block), which depends on the vocabulary.
+  if (L.off_sk > GRPO_NOALLOC_SCRATCH_BYTES) return GRPO_ERR_UNSUPPORTED_SHAPE;
   void* scratch = nullptr;
   if ((r = noalloc_scratch(&scratch)) != GRPO_OK) return r;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1926,6 +1969,8 @@ extern "C" int grpo_logp_fwd_noalloc(const void* hidden, const void* W, const in
   Ws w = carve(scratch, L);
   w.G = nullptr;  // beyond the forward's part of the scratch; never used here
   w.acc = nullptr;
+  w.sk = nullptr;
+  w.hc = nullptr;
   int splits = 1;
   if ((r = run_forward(hidden, W, ids, nullptr, nullptr, nullptr, nullptr, L, w, sms, &splits, st)) != GRPO_OK) return r;
   FinalizeArgs f;

@@ -27,17 +27,20 @@ cudaError_t prepare_bwd_gemms() {
 }
 
 cudaError_t launch_dw_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                            const CUtensorMap& map_h16,
                            const CUtensorMap& map_dw, const TileArgs& args, int grid,
                            cudaStream_t stream) {
-  return ctas == 2 ? launch_gemm_variant<MODE_DW, 2>(map_a, map_b, args, grid, stream, &map_dw)
-                   : launch_gemm_variant<MODE_DW, 1>(map_a, map_b, args, grid, stream);
+  return ctas == 2 ? launch_gemm_variant<MODE_DW, 2>(map_a, map_b, args, grid, stream, &map_dw, &map_h16)
+                   : launch_gemm_variant<MODE_DW, 1>(map_a, map_b, args, grid, stream, nullptr, &map_h16);
 }
 
 cudaError_t launch_bwdg_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                            const CUtensorMap& map_h16,
                              const CUtensorMap& map_g, const TileArgs& args, int grid,
-                             cudaStream_t stream) {
-  return ctas == 2 ? launch_gemm_variant<MODE_BWDG, 2>(map_a, map_b, args, grid, stream, &map_g)
-                   : launch_gemm_variant<MODE_BWDG, 1>(map_a, map_b, args, grid, stream);
+                             cudaStream_t stream,
+                             const CUtensorMap* map_hc) {
+  return ctas == 2 ? launch_gemm_variant<MODE_BWDG, 2>(map_a, map_b, args, grid, stream, &map_g, &map_h16, map_hc)
+                   : launch_gemm_variant<MODE_BWDG, 1>(map_a, map_b, args, grid, stream, nullptr, &map_h16, map_hc);
 }
 
 cudaError_t launch_dh_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,

@@ -16,15 +16,18 @@ cudaError_t prepare_fwd_gemm() {
 }
 
 cudaError_t launch_fwd_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                            const CUtensorMap& map_h16,
                             const TileArgs& args, int grid, cudaStream_t stream) {
-  return ctas == 2 ? launch_gemm_variant<MODE_FWD, 2>(map_a, map_b, args, grid, stream)
-                   : launch_gemm_variant<MODE_FWD, 1>(map_a, map_b, args, grid, stream);
+  return ctas == 2 ? launch_gemm_variant<MODE_FWD, 2>(map_a, map_b, args, grid, stream, nullptr, &map_h16)
+                   : launch_gemm_variant<MODE_FWD, 1>(map_a, map_b, args, grid, stream, nullptr, &map_h16);
 }
 
+// The active-row list of a loss call: the 16-row segments that hold any
+// unmasked row, in order (seg_list, n_seg), and the mask's sum.
 __global__ void __launch_bounds__(1024) row_plan_kernel(const uint8_t* __restrict__ mask,
-                                                        long long n, int n_rb,
-                                                        int* __restrict__ rb_list,
-                                                        int* __restrict__ n_active,
+                                                        long long n, int n_segs,
+                                                        int* __restrict__ seg_list,
+                                                        int* __restrict__ n_seg,
                                                         double* __restrict__ msum) {
   __shared__ int warp_off[32];
   __shared__ int chunk_total;
@@ -34,12 +37,12 @@ __global__ void __launch_bounds__(1024) row_plan_kernel(const uint8_t* __restric
   const int n_warps = blockDim.x >> 5;
   int base = 0;
   unsigned long long tokens = 0;
-  for (int b0 = 0; b0 < n_rb; b0 += blockDim.x) {
-    const int rb = b0 + threadIdx.x;
+  for (int b0 = 0; b0 < n_segs; b0 += blockDim.x) {
+    const int sg = b0 + threadIdx.x;
     int cnt = 0;
-    if (rb < n_rb) {
-      const long long r0 = static_cast<long long>(rb) * BM;
-      const long long r1 = min(r0 + BM, n);
+    if (sg < n_segs) {
+      const long long r0 = static_cast<long long>(sg) * SEG;
+      const long long r1 = min(r0 + SEG, n);
       if (mask == nullptr) {
         cnt = static_cast<int>(r1 - r0);
       } else {
@@ -63,7 +66,7 @@ __global__ void __launch_bounds__(1024) row_plan_kernel(const uint8_t* __restric
       if (lane == 31) chunk_total = incl;
     }
     __syncthreads();
-    if (active) rb_list[base + warp_off[w] + pre] = rb;
+    if (active) seg_list[base + warp_off[w] + pre] = sg;
     base += chunk_total;
     __syncthreads();
   }
@@ -74,29 +77,31 @@ __global__ void __launch_bounds__(1024) row_plan_kernel(const uint8_t* __restric
     unsigned long long t = 0;
     for (int i = 0; i < n_warps; ++i) t += warp_tok[i];
     *msum = static_cast<double>(t);
-    *n_active = base;
+    *n_seg = base;
   }
 }
 
 // dH rows of row blocks without any unmasked token are never touched by the
 // backward GEMMs; they are written as exact zeros here.
+// dH rows of the 16-row segments without an unmasked row (no GEMM computes
+// them): zeros. Per 128-row block, the inactive segments' rows.
 __global__ void __launch_bounds__(256) zero_padding_blocks_kernel(
     const uint8_t* __restrict__ mask, long long n, int n_rb, int hidden,
     __nv_bfloat16* __restrict__ dH) {
-  __shared__ int any;
+  __shared__ int any[kSegs];
   for (int rb = blockIdx.x; rb < n_rb; rb += gridDim.x) {
-    if (threadIdx.x == 0) any = 0;
+    if (threadIdx.x < kSegs) any[threadIdx.x] = 0;
     __syncthreads();
     const long long r0 = static_cast<long long>(rb) * BM;
     const long long r1 = min(r0 + BM, n);
-    if (r0 + threadIdx.x < r1 && mask[r0 + threadIdx.x] != 0) any = 1;
+    if (r0 + threadIdx.x < r1 && mask[r0 + threadIdx.x] != 0) any[threadIdx.x / SEG] = 1;
     __syncthreads();
-    if (!any) {
-      // hidden % 8 == 0: 16-byte stores of 8 bf16.
-      const long long vecs = (r1 - r0) * (hidden / 8);
-      uint4* dst = reinterpret_cast<uint4*>(dH + r0 * hidden);
-      for (long long i = threadIdx.x; i < vecs; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
-    }
+    // hidden % 8 == 0: 16-byte stores of 8 bf16.
+    const int vecs_row = hidden / 8;
+    const long long vecs = (r1 - r0) * vecs_row;
+    uint4* dst = reinterpret_cast<uint4*>(dH + r0 * hidden);
+    for (long long i = threadIdx.x; i < vecs; i += blockDim.x)
+      if (!any[static_cast<int>(i / vecs_row) / SEG]) dst[i] = make_uint4(0, 0, 0, 0);
     __syncthreads();
   }
 }
@@ -253,10 +258,45 @@ cudaError_t launch_seq_lens(const uint8_t* mask, long long n, int seq_len, int* 
   return cudaGetLastError();
 }
 
-cudaError_t launch_row_plan(const uint8_t* mask, long long n, int n_rb, int* rb_list,
-                            int* n_active, double* msum, cudaStream_t stream) {
+// Copies the rows of h of every row block of one chunk whose segments are not
+// consecutive rows (a block that spans the end of a completion) into the
+// chunk's copy of h, at the block's local rows li * BM, with zeros for rows
+// past the active list or past N; the GEMMs then read every block in one TMA
+// box (a block of consecutive rows from h itself). One CTA per segment (16
+// rows) of each row block of the chunk's host-side bound; those of blocks of
+// consecutive rows return at once.
+__global__ void __launch_bounds__(256) gather_blocks_kernel(const __nv_bfloat16* __restrict__ h,
+                                                            __nv_bfloat16* __restrict__ out,
+                                                            const TileArgs a) {
+  const int li = static_cast<int>(blockIdx.x);
+  const int j = static_cast<int>(blockIdx.y);  // segment of the block
+  if (li >= launch_row_blocks(a)) return;
+  int rows[kSegs];
+  if (h_rows(a, li, rows)) return;
+  const int vecs = a.hidden / 8;  // 16-byte vectors per row (hidden % 8 == 0)
+  uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<long long>(li) * BM + j * SEG) *
+                                                  a.hidden);
+  for (int r = 0; r < SEG; ++r) {
+    const long long src = static_cast<long long>(rows[j]) + r;
+    const uint4* s = reinterpret_cast<const uint4*>(h + src * a.hidden);
+    for (int v = threadIdx.x; v < vecs; v += blockDim.x)
+      dst[r * vecs + v] = src < a.n_total ? s[v] : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+cudaError_t launch_gather_blocks(const void* h, void* out, const TileArgs& args,
+                                 cudaStream_t stream) {
+  if (args.n_rb <= 0 || args.seg_list == nullptr) return cudaSuccess;
+  LaunchTimer timer("gather_blocks_kernel", stream);
+  gather_blocks_kernel<<<dim3(args.n_rb, kSegs), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(h), static_cast<__nv_bfloat16*>(out), args);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_row_plan(const uint8_t* mask, long long n, int n_segs, int* seg_list,
+                            int* n_seg, double* msum, cudaStream_t stream) {
   LaunchTimer timer("row_plan_kernel", stream);
-  row_plan_kernel<<<1, 1024, 0, stream>>>(mask, n, n_rb, rb_list, n_active, msum);
+  row_plan_kernel<<<1, 1024, 0, stream>>>(mask, n, n_segs, seg_list, n_seg, msum);
   return cudaGetLastError();
 }
 
@@ -289,10 +329,12 @@ cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t stream) {
 namespace grpo {
 
 cudaError_t launch_fwds_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                            const CUtensorMap& map_h16,
                              const CUtensorMap& map_s, const TileArgs& args, int grid,
-                             cudaStream_t stream) {
-  return ctas == 2 ? launch_gemm_variant<MODE_FWDS, 2>(map_a, map_b, args, grid, stream, &map_s)
-                   : launch_gemm_variant<MODE_FWDS, 1>(map_a, map_b, args, grid, stream);
+                             cudaStream_t stream,
+                             const CUtensorMap* map_hc) {
+  return ctas == 2 ? launch_gemm_variant<MODE_FWDS, 2>(map_a, map_b, args, grid, stream, &map_s, &map_h16, map_hc)
+                   : launch_gemm_variant<MODE_FWDS, 1>(map_a, map_b, args, grid, stream, nullptr, &map_h16, map_hc);
 }
 
 cudaError_t prepare_fwds_gemm() {
@@ -349,14 +391,22 @@ __device__ __forceinline__ void finish_row(const GformArgs& a, long long grow, f
   if (a.logp_out) a.logp_out[grow] = logp;
 }
 
-// Global row of local row `lrow` of the chunk, or -1 past the active list.
+// Row blocks of the chunk that the GEMMs compute (the active list may be
+// shorter than the host-side bound).
+__device__ __forceinline__ int chunk_blocks(const GformArgs& a) {
+  if (a.n_seg == nullptr) return a.n_rb;
+  const int segs = *a.n_seg - a.rb_offset * kSegs;
+  return max(0, min(a.n_rb, (segs + kSegs - 1) / kSegs));
+}
+
+// Global row of local row `lrow` of the chunk, or -1 past the active list
+// (inside the chunk's last computed block, or past it).
 __device__ __forceinline__ long long chunk_row(const GformArgs& a, int lrow) {
-  const int li = lrow / BM;
-  int n_rb = a.n_rb;
-  if (a.n_active != nullptr) n_rb = max(0, min(a.n_rb, *a.n_active - a.rb_offset));
-  if (li >= n_rb) return -1;
-  const int rb = a.rb_list != nullptr ? a.rb_list[a.rb_offset + li] : a.rb_offset + li;
-  return static_cast<long long>(rb) * BM + (lrow - li * BM);
+  if (lrow / BM >= chunk_blocks(a)) return -1;
+  if (a.seg_list == nullptr) return static_cast<long long>(a.rb_offset) * BM + lrow;
+  const int s = a.rb_offset * kSegs + lrow / SEG;
+  if (a.n_seg != nullptr && s >= *a.n_seg) return -1;
+  return static_cast<long long>(a.seg_list[s]) * SEG + lrow % SEG;
 }
 
 __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const GformArgs a) {
@@ -364,7 +414,16 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
   __shared__ int sh_y;
   const int lrow = blockIdx.x;
   const long long grow = chunk_row(a, lrow);
-  if (grow < 0) return;  // whole block: uniform
+  uint4* row = reinterpret_cast<uint4*>(a.S + static_cast<long long>(lrow) * a.ldS);
+  const int n_vec = static_cast<int>(a.ldS / 8);
+  if (grow < 0) {
+    // Past the active list. In the chunk's last computed block the row is
+    // zeroed, so that the dW GEMM, which sums over the block's rows, reads no
+    // stale bytes; past it no GEMM reads the row.
+    if (lrow / BM < chunk_blocks(a))
+      for (int i = threadIdx.x; i < n_vec; i += blockDim.x) row[i] = make_uint4(0, 0, 0, 0);
+    return;  // whole block: uniform
+  }
 
   if (threadIdx.x == 0) {
     float lse, g;
@@ -377,8 +436,6 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
   __syncthreads();
   const float lse2 = sh_lse2, g = sh_g;
   const int y = sh_y;
-  uint4* row = reinterpret_cast<uint4*>(a.S + static_cast<long long>(lrow) * a.ldS);
-  const int n_vec = static_cast<int>(a.ldS / 8);
   if (g == 0.f) {
     for (int i = threadIdx.x; i < n_vec; i += blockDim.x) row[i] = make_uint4(0, 0, 0, 0);
     return;

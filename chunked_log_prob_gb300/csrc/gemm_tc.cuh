@@ -51,6 +51,12 @@ namespace grpo {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
+// Rows of a segment of the active-row list: a loss call computes the 16-row
+// segments that hold any unmasked row, packed into row blocks of kSegs
+// segments, so that trailing padding costs at most 15 rows per completion
+// rather than a part-filled 128-row block.
+constexpr int SEG = 16;
+constexpr int kSegs = BM / SEG;
 constexpr int STAGES = 4;                 // pipeline depth of the single-CTA kernels
 constexpr int A_BYTES = BM * BK * 2;      // 16 KB
 constexpr int GEMM_THREADS = 192;
@@ -76,10 +82,15 @@ __host__ __device__ constexpr bool has_cvt(int mode) { return mode == MODE_DHS |
 struct TileArgs {
   long long n_total;     // N: rows of hidden / dH; global rows >= N are padding
   int n_rb;              // row blocks this launch may cover (host-side bound)
-  int rb_offset;         // first entry of the row-block list this launch covers
-  const int* rb_list;    // global indices of the row blocks to compute, or null
-                         // (then local block i is global block rb_offset + i)
-  const int* n_active;   // device-side length of rb_list, or null (= all)
+  int rb_offset;         // the launch's first row block (of kSegs list entries each)
+  const int* seg_list;   // global indices of the active 16-row segments, in order,
+                         // or null (then local row r is global row rb_offset*BM + r)
+  const int* n_seg;      // device-side length of seg_list, or null (= all)
+  // The launch's row blocks whose segments are not consecutive rows were
+  // copied into a chunk-sized copy of h (gather_blocks_kernel; map_hc, rows
+  // li * BM..): read them from there in one box. 0: read those blocks from h
+  // in boxes of SEG rows (map_h16).
+  int hc;
   int k_iters;     // ceil(K / BK)
   int group_rows;  // row blocks per raster group
   int n_cols;      // FWD: vocab splits; BWDG: vocab tiles in block; DH: D tiles
@@ -143,16 +154,43 @@ __device__ __forceinline__ void decode_unit(int u, int n_rb, int n_cols, int R, 
   rb = grp * R + (rem - col * rows_in_g);
 }
 
-// Global row block of the launch's local row block `li`.
-__device__ __forceinline__ int global_rb(const TileArgs& a, int li) {
-  return a.rb_list != nullptr ? a.rb_list[a.rb_offset + li] : a.rb_offset + li;
+// Global row of the launch's local row `lr` (row lr % BM of its local row
+// block lr / BM), or -1 past the active list.
+__device__ __forceinline__ long long row_of(const TileArgs& a, int lr) {
+  if (a.seg_list == nullptr) return static_cast<long long>(a.rb_offset) * BM + lr;
+  const int s = a.rb_offset * kSegs + lr / SEG;
+  if (a.n_seg != nullptr && s >= *a.n_seg) return -1;
+  return static_cast<long long>(a.seg_list[s]) * SEG + lr % SEG;
 }
 
 // Row blocks this launch actually covers (the active list may be shorter
 // than the host-side bound).
 __device__ __forceinline__ int launch_row_blocks(const TileArgs& a) {
-  if (a.n_active == nullptr) return a.n_rb;
-  return max(0, min(a.n_rb, *a.n_active - a.rb_offset));
+  if (a.n_seg == nullptr) return a.n_rb;
+  const int segs = *a.n_seg - a.rb_offset * kSegs;
+  return max(0, min(a.n_rb, (segs + kSegs - 1) / kSegs));
+}
+
+// Rows of the hidden states that local row block `li` reads, for the TMA
+// loads of h: rows[j] is the first row of its j-th segment (past the list:
+// n_total, a coordinate the load fills with zeros). Returns true when the
+// segments are consecutive rows, so that one box of BM rows at rows[0] loads
+// the block; otherwise each segment is a box of SEG rows of its own.
+__device__ __forceinline__ bool h_rows(const TileArgs& a, int li, int (&rows)[kSegs]) {
+  if (a.seg_list == nullptr) {
+#pragma unroll
+    for (int j = 0; j < kSegs; ++j) rows[j] = (a.rb_offset + li) * BM + j * SEG;
+    return true;
+  }
+  const int s0 = (a.rb_offset + li) * kSegs;
+  const int n = a.n_seg != nullptr ? *a.n_seg : s0 + kSegs;
+  bool consecutive = true;
+#pragma unroll
+  for (int j = 0; j < kSegs; ++j) {
+    rows[j] = s0 + j < n ? a.seg_list[s0 + j] * SEG : static_cast<int>(a.n_total);
+    consecutive = consecutive && rows[j] == rows[0] + j * SEG;
+  }
+  return consecutive;
 }
 
 template <int MODE>
@@ -700,7 +738,9 @@ template <int MODE, int CTAS>
 __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b,
-                   const __grid_constant__ CUtensorMap map_c, const TileArgs args) {
+                   const __grid_constant__ CUtensorMap map_c,
+                   const __grid_constant__ CUtensorMap map_h16,
+                   const __grid_constant__ CUtensorMap map_hc, const TileArgs args) {
   using C = PairCfg<MODE, CTAS>;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -795,8 +835,21 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
         // again and stores nothing.
         int li = ru * CTAS + static_cast<int>(rank);
         if (li >= n_rb) li = ru * CTAS;
-        const int a_row =
-            MODE == MODE_DW ? 0 : (is_dh(MODE) ? li : global_rb(args, li)) * BM;
+        // The logit and G-tile GEMMs read rows of h: one box of BM rows when
+        // the block's segments are consecutive rows, else one of SEG rows per
+        // segment (map_h16); the dH-type GEMMs read chunk-local rows.
+        int hr[kSegs];
+        bool h_one = true;
+        const CUtensorMap* map_h1 = &map_a;  // where a block of h is one box
+        if constexpr (!is_dh(MODE) && MODE != MODE_DW) {
+          h_one = h_rows(args, li, hr);
+          if (!h_one && args.hc) {
+            h_one = true;
+            hr[0] = li * BM;  // the block's rows, copied in order
+            map_h1 = &map_hc;
+          }
+        }
+        const int a_row = MODE == MODE_DW ? 0 : (is_dh(MODE) ? li * BM : hr[0]);
         const int a_m0 = (ru * CTAS + static_cast<int>(rank)) * BM;  // MODE_DW: vocab row
         for (int t = t0; t < t1 && ok; ++t) {
           // MN-major B (DH, DHS, UAC, DW): 64-column boxes per accumulator in
@@ -840,20 +893,33 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
               if (CTAS == 2) mbar_arrive_expect_tx_cluster(lead, C::kKSub * (A_BYTES + b_bytes));
               else mbar_arrive_expect_tx(&full_bar[s], C::kKSub * (A_BYTES + b_bytes));
 #pragma unroll
+              int hk[kSegs];  // the rows of h of this stage's row block
+              h_rows(args, (k * C::kKSub * BK) / BM, hk);
               for (int ks = 0; ks < C::kKSub; ++ks) {
                 const int kr = (k * C::kKSub + ks) * BK;  // chunk-local row of this K slice
-                const int grow_k = global_rb(args, kr / BM) * BM + kr % BM;
+                const int j0 = (kr % BM) / SEG;            // its first segment in the block
+                bool one = true;
+#pragma unroll
+                for (int j = 1; j < BK / SEG; ++j) one = one && hk[j0 + j] == hk[j0] + j * SEG;
                 // A = G^T: 128 vocab rows (two 64-wide MN blocks) x 64 chunk rows.
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
                   load_box<CTAS>(a_dst + ks * A_BYTES + j * (BK * 64 * 2), &map_a, &full_bar[s],
                                  lead, a_m0 + j * 64, kr, true, pol_a);
-                // B = H: this CTA's D columns x the same 64 rows, in 64-wide blocks.
-                for (int jb = 0; jb < nbox[0]; ++jb)
-                  load_box<CTAS>(b_dst + ks * C::kBBytes + jb * (BK * 64 * 2), &map_b,
-                                 &full_bar[s], lead,
-                                 t * BN + static_cast<int>(rank) * nbox[0] * 64 + jb * 64, grow_k,
-                                 false, 0);
+                // B = H: this CTA's D columns x the same 64 rows, in 64-wide
+                // blocks (each a box of 64 rows, or one of SEG rows per segment).
+                for (int jb = 0; jb < nbox[0]; ++jb) {
+                  uint8_t* dst = b_dst + ks * C::kBBytes + jb * (BK * 64 * 2);
+                  const int col = t * BN + static_cast<int>(rank) * nbox[0] * 64 + jb * 64;
+                  if (one) {
+                    load_box<CTAS>(dst, &map_b, &full_bar[s], lead, col, hk[j0], false, 0);
+                  } else {
+#pragma unroll
+                    for (int j = 0; j < BK / SEG; ++j)
+                      load_box<CTAS>(dst + j * (SEG * 64 * 2), &map_h16, &full_bar[s], lead, col,
+                                     hk[j0 + j], false, 0);
+                  }
+                }
               }
             } else if (CTAS == 2) {
               // Both CTAs count their bytes on the leader's barrier.
@@ -861,9 +927,17 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
               mbar_arrive_expect_tx_cluster(lead, is_dh_plain(MODE) ? A_BYTES + b_bytes
                                                                   : C::kStageBytes);
 #pragma unroll
-              for (int ks = 0; ks < C::kKSub; ++ks)
-                tma_load_2d_pair(a_dst + ks * A_BYTES, &map_a, lead, (k * C::kKSub + ks) * BK, a_row,
-                                 pol_a);
+              for (int ks = 0; ks < C::kKSub; ++ks) {
+                const int kc = (k * C::kKSub + ks) * BK;
+                if (h_one) {
+                  tma_load_2d_pair(a_dst + ks * A_BYTES, map_h1, lead, kc, a_row, pol_a);
+                } else {
+#pragma unroll
+                  for (int j = 0; j < kSegs; ++j)
+                    tma_load_2d_pair(a_dst + ks * A_BYTES + j * (SEG * BK * 2), &map_h16, lead, kc,
+                                     hr[j], pol_a);
+                }
+              }
               if (is_dh_plain(MODE)) {
                 // Per accumulator, this CTA's share of its D columns.
 #pragma unroll
@@ -888,7 +962,14 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             } else {
               mbar_arrive_expect_tx(&full_bar[s],
                                     is_dh_plain(MODE) ? A_BYTES + b_bytes : C::kStageBytes);
-              tma_load_2d_hint(a_dst, &map_a, &full_bar[s], k * BK, a_row, pol_a);
+              if (h_one) {
+                tma_load_2d_hint(a_dst, map_h1, &full_bar[s], k * BK, a_row, pol_a);
+              } else {
+#pragma unroll
+                for (int j = 0; j < kSegs; ++j)
+                  tma_load_2d_hint(a_dst + j * (SEG * BK * 2), &map_h16, &full_bar[s], k * BK,
+                                   hr[j], pol_a);
+              }
               if (is_dh_plain(MODE)) {
                 // W[v0 + k*64 .. +64, d0 .. d0+256) as up to four 64x64 MN-major boxes.
                 for (int jb = 0; jb < nbox[0]; ++jb)
@@ -1028,9 +1109,9 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
       const int li = ru * CTAS + static_cast<int>(rank);
       const bool block_ok = li < n_rb;
       const int lrow = li * BM + lrow_in_tile;  // row of the chunk workspace
-      const long long grow =
-          block_ok ? static_cast<long long>(global_rb(args, li)) * BM + lrow_in_tile : 0;
-      const bool valid = block_ok && grow < args.n_total;
+      const long long grow_l = block_ok ? row_of(args, li * BM + lrow_in_tile) : -1;
+      const bool valid = grow_l >= 0 && grow_l < args.n_total;
+      const long long grow = valid ? grow_l : 0;
 
       // Per-row state.
       float m2 = -INFINITY, ssum = 0.f;  // FWD
@@ -1618,8 +1699,8 @@ __global__ void __launch_bounds__(BM * CTAS) tail_fixup_kernel(const TileArgs a)
   const int lrow = static_cast<int>(threadIdx.x) % BM;
   const int li = ru * CTAS + rank;
   if (li >= n_rb) return;
-  const long long grow = static_cast<long long>(global_rb(a, li)) * BM + lrow;
-  if (grow >= a.n_total) return;
+  const long long grow = row_of(a, li * BM + lrow);
+  if (grow < 0 || grow >= a.n_total) return;
   float v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = 0.f;

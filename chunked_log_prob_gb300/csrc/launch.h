@@ -43,9 +43,9 @@ struct FinalizeArgs {
 // the dH GEMM that converts the logits itself (finalize_rows).
 struct GformArgs {
   long long n_total;
-  int n_rb, rb_offset;
-  const int* rb_list;
-  const int* n_active;
+  int n_rb, rb_offset;   // as TileArgs: row blocks of kSegs entries of seg_list
+  const int* seg_list;
+  const int* n_seg;
   int splits;
   long long part_ld;
   int vocab, seq_len;
@@ -115,10 +115,16 @@ class LaunchTimer {
 // Launch of one GEMM variant; a CTA pair (CTAS = 2) runs as a 2-CTA cluster.
 // `grid` counts CTAs (a multiple of CTAS). map_c: the store map of the
 // variants that write through TMA (PairCfg::kTmaStore), unused otherwise.
+// map_h16: the hidden states in boxes of SEG rows (64 x 16, 128-byte swizzle),
+// for the variants that read h by segments of the active-row list (the logit,
+// G-tile and dW GEMMs), unused otherwise. map_hc: the chunk's copy of the rows
+// of its non-consecutive row blocks (64 x 128 boxes; with args.hc set).
 template <int MODE, int CTAS>
 cudaError_t launch_gemm_variant(const CUtensorMap& map_a, const CUtensorMap& map_b,
                                 const TileArgs& args, int grid, cudaStream_t stream,
-                                const CUtensorMap* map_c = nullptr) {
+                                const CUtensorMap* map_c = nullptr,
+                                const CUtensorMap* map_h16 = nullptr,
+                                const CUtensorMap* map_hc = nullptr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(PairCfg<MODE, CTAS>::kThreads, 1, 1);
@@ -135,7 +141,9 @@ cudaError_t launch_gemm_variant(const CUtensorMap& map_a, const CUtensorMap& map
   }
   LaunchTimer timer(MODE, CTAS, stream);
   return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, CTAS>, map_a, map_b,
-                            map_c != nullptr ? *map_c : map_a, args);
+                            map_c != nullptr ? *map_c : map_a,
+                            map_h16 != nullptr ? *map_h16 : map_a,
+                            map_hc != nullptr ? *map_hc : map_a, args);
 }
 
 template <int MODE, int CTAS>
@@ -150,12 +158,15 @@ cudaError_t prepare_gemm_variant() {
 cudaError_t prepare_fwd_gemm();   // opt-in to the large dynamic smem
 cudaError_t prepare_bwd_gemms();
 cudaError_t launch_fwd_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                            const CUtensorMap& map_h16,
                             const TileArgs& args, int grid, cudaStream_t stream);
 // map_g: the chunk's bf16 G block [rows][ldG] as a store map, 64 x 32 boxes with
 // the 128-byte swizzle (used by the CTA-pair variant).
 cudaError_t launch_bwdg_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                            const CUtensorMap& map_h16,
                              const CUtensorMap& map_g, const TileArgs& args, int grid,
-                             cudaStream_t stream);
+                             cudaStream_t stream,
+                            const CUtensorMap* map_hc = nullptr);
 cudaError_t launch_dh_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                            const TileArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_dhs_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
@@ -176,10 +187,16 @@ cudaError_t launch_uap_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMa
 // map_dw: dW[v0 : v0 + dw_rows) as fp32 [rows][hidden], 32 x 32 boxes with the
 // 128-byte swizzle (used by the CTA-pair variant).
 cudaError_t launch_dw_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                            const CUtensorMap& map_h16,
                            const CUtensorMap& map_dw, const TileArgs& args, int grid,
                            cudaStream_t stream);
-cudaError_t launch_row_plan(const uint8_t* mask, long long n, int n_rb, int* rb_list,
-                            int* n_active, double* msum, cudaStream_t stream);
+// Before a chunk's logit, G-tile or dW GEMM: the rows of its row blocks whose
+// segments are not consecutive rows, copied into `out` (chunk rows x hidden).
+// `args`: the chunk's TileArgs (rb_offset, n_rb, seg_list, n_seg, hidden, n_total).
+cudaError_t launch_gather_blocks(const void* h, void* out, const TileArgs& args,
+                                 cudaStream_t stream);
+cudaError_t launch_row_plan(const uint8_t* mask, long long n, int n_segs, int* seg_list,
+                            int* n_seg, double* msum, cudaStream_t stream);
 cudaError_t launch_seq_lens(const uint8_t* mask, long long n, int seq_len, int* lens,
                             int* n_nonempty, cudaStream_t stream);
 cudaError_t launch_zero_padding_blocks(const uint8_t* mask, long long n, int n_rb, int hidden,
@@ -189,8 +206,10 @@ cudaError_t prepare_fwds_gemm();
 // map_s: the chunk's fp16 logit block [rows][ldS] as a store map, 64 x 32 boxes
 // with the 128-byte swizzle (used by the CTA-pair variant).
 cudaError_t launch_fwds_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                            const CUtensorMap& map_h16,
                              const CUtensorMap& map_s, const TileArgs& args, int grid,
-                             cudaStream_t stream);
+                             cudaStream_t stream,
+                            const CUtensorMap* map_hc = nullptr);
 cudaError_t launch_finalize_gform(const GformArgs& a, int rows, cudaStream_t stream);
 cudaError_t launch_finalize_rows(const GformArgs& a, int rows, cudaStream_t stream);
 cudaError_t launch_single_pass_p(const GformArgs& a, int rows, cudaStream_t stream);

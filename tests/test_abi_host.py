@@ -60,7 +60,8 @@ def test_workspace_independent_of_vocab_times_tokens(clp):
     sizes = [clp.grpo_workspace_size(n, 4096, 128256, 1, p) for n in (4096, 16384, 65536)]
     per_row = (sizes[2] - sizes[1]) / (65536 - 16384)
     assert per_row < 64 * 4 * 2 + 64  # split partials + a few fp32 per row
-    fixed = 1024 * 8192 * 2 + 1024 * 4096 * 4
+    # G block, fp32 dH accumulator, the chunk's copy of h (chunk x D in bf16)
+    fixed = 1024 * 8192 * 2 + 1024 * 4096 * 4 + 1024 * 4096 * 2
     assert sizes[0] < fixed + 4096 * 300 + 65536
     assert sizes[2] < 65536 * 128256 * 4 / 100  # far below the N x V fp32 logits
 
@@ -169,14 +170,21 @@ def stored_block(chunk, V):
 TAIL_SPLIT_BYTES = 2 * 76 * 256 * 512 * 4
 
 
+def H_COPY(chunk, hidden):  # noqa: N802
+    """The chunk's copy of h (rows x D in bf16) for the row blocks whose active
+    16-row segments are not consecutive rows."""
+    return chunk * hidden * 2
+
+
 def test_stored_logit_workspace_is_chunk_times_vocab(clp):
     # Stored-logit backward: two blocks of chunk x V (double-buffered when
     # there is more than one chunk), independent of N.
     p = clp.make_params(chunk_tokens=2048, flags=1)
     a = clp.grpo_workspace_size(16384, 4096, 128256, 1, p)
     b = clp.grpo_workspace_size(65536, 4096, 128256, 1, p)
-    block = stored_block(2048, 128256) + TAIL_SPLIT_BYTES
-    assert 2 * block - TAIL_SPLIT_BYTES < a < 2 * block - TAIL_SPLIT_BYTES + 16384 * 400
+    block = stored_block(2048, 128256) + TAIL_SPLIT_BYTES + H_COPY(2048, 4096)
+    extra = TAIL_SPLIT_BYTES + H_COPY(2048, 4096)
+    assert 2 * block - extra < a < 2 * block - extra + 16384 * 400
     one = clp.grpo_workspace_size(2048, 4096, 128256, 1, p)  # a single chunk: one block
     assert block < one < block + 2048 * 400
     assert (b - a) / (65536 - 16384) < 64 * 4 * 2 + 64
@@ -193,11 +201,14 @@ def test_stored_logit_workspace_single_block_up_to_2048_hidden(clp):
     p = clp.make_params(chunk_tokens=2048, flags=1)
     block = stored_block(2048, 151936)
     small = clp.grpo_workspace_size(32768, 2048, 151936, 1, p)
-    assert block + TAIL_SPLIT_BYTES < small < block + TAIL_SPLIT_BYTES + 32768 * 400
+    extra = TAIL_SPLIT_BYTES + H_COPY(2048, 2048)
+    assert block + extra < small < block + extra + 32768 * 400
     big = clp.grpo_workspace_size(32768, 2056, 151936, 1, p)
-    assert 2 * block + TAIL_SPLIT_BYTES < big < 2 * block + TAIL_SPLIT_BYTES + 32768 * 400
+    extra = TAIL_SPLIT_BYTES + H_COPY(2048, 2056)
+    assert 2 * block + extra < big < 2 * block + extra + 32768 * 400
     auto = clp.grpo_workspace_size(131072, 1536, 151936, 1, clp.make_params(flags=1))
-    assert (2 << 30) < auto < (4 << 30) * (1 + 1 / 32) + TAIL_SPLIT_BYTES + 131072 * 400
+    assert (2 << 30) < auto < ((4 << 30) * (1 + 1 / 32) + TAIL_SPLIT_BYTES + H_COPY(16384, 1536) +
+                               131072 * 400)
 
 
 @pytest.mark.parametrize("flags", [16, 1, 0])

@@ -86,10 +86,12 @@ def test_stored_logit_block_is_eq3_elements_in_fp16(clp, ex, hidden, blocks):
                                                                         flags=STORED))
     # Halving the chunk frees exactly half of Eq. 3's elements at 2 bytes, plus
     # one fp32 maximum per 64 of them (1/32 more), per logit block (two blocks
-    # when G is formed in a pass of its own, D > 2048).
+    # when G is formed in a pass of its own, D > 2048), and the chunk's copy of
+    # h (its rows x D in bf16: the row blocks that span a completion's end).
     half = eq3_elements // 2
     assert V % 64 == 0
-    assert ws(b * T, rows) - ws(b * T, rows // 2) == blocks * (2 * half + 4 * (half // 64))
+    assert ws(b * T, rows) - ws(b * T, rows // 2) == (blocks * (2 * half + 4 * (half // 64)) +
+                                                      (rows // 2) * hidden * 2)
     # Eq. 2's point: the block does not grow with the batch; only per-row
     # vectors do (a few hundred bytes per token).
     grow = ws(2 * b * T, rows) - ws(b * T, rows)
@@ -104,4 +106,5 @@ def test_recompute_g_block_is_eq3_elements_in_bf16(clp, ex):
         return clp.grpo_workspace_size(b * T, 4096, V, T,
                                        clp.make_params(chunk_tokens=chunk, vocab_block=V,
                                                        flags=RECOMPUTE))
-    assert ws(rows) - ws(rows // 2) == 2 * (rows // 2) * V
+    # Eq. 3's elements in bf16, and the chunk's copy of h (rows x D in bf16).
+    assert ws(rows) - ws(rows // 2) == 2 * (rows // 2) * V + (rows // 2) * 4096 * 2

@@ -48,6 +48,9 @@ def _cases(clp):
         _problem(2, T=n_max // 4, prompts=1, G=4),      # 8192 x 256 x 4096: the limit
         _problem(1, T=75, prompts=1, G=4, D=200, V=1000),  # 300 rows, ragged in every dim
         _problem(0),                                    # 256 x 256 x 4096
+        # a large vocabulary: the workspace's backward part (tail-split slots,
+        # logit block) is far beyond the scratch, the forward's part is not
+        _problem(3, T=128, prompts=1, G=4, D=256, V=128256),
     ]
 
 
