@@ -120,24 +120,6 @@ size_t tail_split_bytes(int ts_slots, int ctas) {
          sizeof(float);
 }
 
-int auto_chunk_blocks(long long n_rb_total, int n_dt, int sms, int max_units) {
-  // Row blocks per backward chunk: keep the dH GEMM's (row block x D tile)
-  // grid close to whole waves of the SMs; prefer larger chunks on ties.
-  const int hi = static_cast<int>(std::min<long long>(n_rb_total, max_units));
-  int best = hi;
-  double best_eff = -1.0;
-  for (int nrb = hi; nrb >= 1; --nrb) {
-    const long long units = static_cast<long long>(nrb) * n_dt;
-    const long long waves = cdiv(units, sms);
-    const double eff = static_cast<double>(units) / static_cast<double>(waves * sms);
-    if (eff > best_eff + 0.02) {
-      best_eff = eff;
-      best = nrb;
-    }
-  }
-  return best;
-}
-
 // Stored-logit backward: largest chunk (row blocks) whose fp16 logit block
 // stays within kMaxStoredChunkBytes (twice that when there is only one block).
 int stored_max_blocks(long long ldS, int n_sbuf) {
@@ -244,15 +226,17 @@ int auto_stored_chunk_blocks(long long n_rb_total, int n_dt, int nvt, int sms, i
 }
 
 // Modelled GEMM time of the recomputed-logit schedule (same unit as
-// stored_cost): one forward over every row unit, then per chunk of nrb row
-// units and per vocab block of vb_tiles tiles a G-tile launch of (row units x
-// tiles) units and a dH launch of (row units x D tiles) units of K = the block.
+// stored_cost): per chunk of nrb row units a forward of (row units x splits)
+// units, the splits those of a full chunk's whole waves, then per vocab block
+// of vb_tiles tiles a G-tile launch of (row units x tiles) units and a dH
+// launch of (row units x D tiles) units of K = the block.
 double recompute_cost(long long n_rb_total, int nrb, int n_dt, int nvt, int vb_tiles, int sms) {
-  const int grp = group_rows_exact(static_cast<int>(n_rb_total), sms);
-  const int splits = std::min(std::max(1, sms / grp), std::min(nvt, kMaxSplits));
-  double actual = static_cast<double>(cdiv(n_rb_total * splits, sms)) * cdiv(nvt, splits);
+  const int splits =
+      stored_fwd_splits(static_cast<int>(std::min<long long>(nrb, n_rb_total)), nvt, sms, nullptr);
+  double actual = 0.0;
   for (long long r0 = 0; r0 < n_rb_total; r0 += nrb) {
     const long long n = std::min<long long>(nrb, n_rb_total - r0);
+    actual += static_cast<double>(cdiv(n * splits, sms)) * cdiv(nvt, splits);
     for (int t0 = 0; t0 < nvt; t0 += vb_tiles) {
       const int w = std::min(vb_tiles, nvt - t0);
       actual += static_cast<double>(cdiv(n * w, sms));
@@ -473,7 +457,20 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, Form fo
     }
     crows = static_cast<long long>(best) * ru_rows;
   } else if (sms > 0) {
-    crows = auto_chunk_blocks(n_ru_total, n_dt, slots, static_cast<int>(max_units)) * ru_rows;
+    // Recomputed logits: the best modelled schedule (per-chunk forward, G-tile
+    // and dH launches), near-ties to the larger chunk.
+    const int hi = static_cast<int>(std::min<long long>(n_ru_total, max_units));
+    const int vbt = static_cast<int>(cdiv(L->vblock, BN));
+    int best = hi;
+    double best_cost = 0.0;
+    for (int nrb = hi; nrb >= 1; --nrb) {
+      const double cost = recompute_cost(n_ru_total, nrb, n_dt, L->nvt, vbt, slots);
+      if (nrb == hi || cost < best_cost * 0.995) {
+        best_cost = cost;
+        best = nrb;
+      }
+    }
+    crows = static_cast<long long>(best) * ru_rows;
   } else {  // sizing without a device: the largest automatic chunk
     crows = std::min<long long>(n_ru_total, max_units) * ru_rows;
   }
@@ -793,6 +790,63 @@ int run_forward(const void* hidden, const void* W, const int32_t* ids, const uin
   const int grid = L.ctas * static_cast<int>(std::min<long long>(units, slots));
   if (launch_fwd_gemm(L.ctas, map_h, map_w, map_h16, a, grid, st) != cudaSuccess)
     return GRPO_ERR_CUDA;
+  *splits_out = splits;
+  return GRPO_OK;
+}
+
+// The recomputed form's forward of a loss call, one logit GEMM per chunk of
+// the backward's chunking, after the chunk's non-consecutive row blocks of h
+// are gathered (so that every row block loads in one box). Every chunk splits
+// the vocabulary into the count that makes a full chunk's units whole waves of
+// the SM pairs (a count set by the whole batch leaves most pairs idle on a
+// chunk of a few row units), and the row finish reads that many partial slots
+// for every row. A row's partial sums, and so its last bits, depend on the
+// chunk size.
+int run_forward_chunks(const void* hidden, const void* W, const int32_t* ids,
+                       const uint8_t* mask, const grpo_params* prm, const Layout& L,
+                       const Ws& w, int sms, int* splits_out, cudaStream_t st) {
+  CUtensorMap map_h, map_h16, map_w;
+  const int slots = std::max(1, sms / L.ctas);
+  if (!encode_2d(&map_h, hidden, L.D, L.n, L.D, BK, BM) ||
+      !encode_2d(&map_h16, hidden, L.D, L.n, L.D, BK, SEG) ||
+      !encode_2d(&map_w, W, L.D, L.V, L.D, BK, BN / L.ctas))
+    return GRPO_ERR_CUDA;
+  const int n_rb_total = static_cast<int>(L.nr / BM);
+  const int rb_per_chunk = L.chunk_rows / BM;
+  const int n_ru_full = static_cast<int>(cdiv(std::min(rb_per_chunk, n_rb_total), L.ctas));
+  const int splits = stored_fwd_splits(n_ru_full, L.nvt, slots, nullptr);
+  for (int rb0 = 0; rb0 < n_rb_total; rb0 += rb_per_chunk) {
+    const int n_rb = std::min(rb_per_chunk, n_rb_total - rb0);
+    const int n_ru = static_cast<int>(cdiv(n_rb, L.ctas));
+    TileArgs a = base_args(L, w);
+    set_transform(&a, prm);
+    a.n_total = L.n;
+    a.n_rb = n_rb;
+    a.rb_offset = rb0;
+    a.seg_list = w.seg_list;
+    a.n_seg = w.n_seg;
+    a.hc = 1;
+    a.k_iters = static_cast<int>(cdiv(L.D, BK));
+    a.group_rows = (prm != nullptr && prm->raster_rows > 0) ? std::min(prm->raster_rows, n_ru)
+                                                            : n_ru;
+    a.n_cols = splits;
+    a.n_vtiles = L.nvt;
+    a.v0 = 0;
+    a.ids = ids;
+    a.mask = mask;
+    a.part_m = w.pm;
+    a.part_s = w.ps;
+    a.zy = w.zy;
+    a.part_ld = L.nr;
+    CUtensorMap map_hc;
+    if (!encode_2d(&map_hc, w.hc, L.D, static_cast<uint64_t>(n_rb) * BM, L.D, BK, BM))
+      return GRPO_ERR_CUDA;
+    if (launch_gather_blocks(hidden, w.hc, a, st) != cudaSuccess) return GRPO_ERR_CUDA;
+    const long long units = static_cast<long long>(n_ru) * splits;
+    const int grid = L.ctas * static_cast<int>(std::min<long long>(units, slots));
+    if (launch_fwd_gemm(L.ctas, map_h, map_w, map_h16, a, grid, st, &map_hc) != cudaSuccess)
+      return GRPO_ERR_CUDA;
+  }
   *splits_out = splits;
   return GRPO_OK;
 }
@@ -1724,7 +1778,7 @@ int grpo_loss_fwd_bwd(const void* hidden, const void* W, const int32_t* ids,
     w = carve(workspace, L);
   }
   int splits = 1;
-  if ((r = run_forward(hidden, W, ids, mask, w.seg_list, w.n_seg, &prm, L, w, sms, &splits,
+  if ((r = run_forward_chunks(hidden, W, ids, mask, &prm, L, w, sms, &splits,
                        st)) != GRPO_OK)
     return r;
   FinalizeArgs f;
@@ -1794,14 +1848,14 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
                                                   (((L.fused ? 2 : 3) + (tail_split ? 1 : 0)) *
                                                        L.nvb +
                                                    2)
-                                        : 4 + (2 * info->n_vocab_blocks + 1) * info->n_chunks;
+                                        : 3 + (2 * info->n_vocab_blocks + 3) * info->n_chunks;
   if (L.n > 0 && params != nullptr && (params->flags & GRPO_FLAG_SEQUENCE_MEAN) != 0)
     info->launches_loss += 1;
-  if (L.stored) {
-    info->n_vocab_blocks = 1;
+  if (L.stored) info->n_vocab_blocks = 1;
+  // The loss call's forward of the stored and recomputed forms runs per chunk.
+  if (!L.single_pass)
     info->fwd_splits =
         stored_fwd_splits(L.chunk_rows / (BM * L.ctas), L.nvt, slots, nullptr);
-  }
   info->g_in_dh_gemm = L.fused ? 1 : 0;
   info->stored_logits = L.stored ? 1 : 0;
   info->single_pass = L.single_pass ? 1 : 0;

@@ -17,9 +17,10 @@ cudaError_t prepare_fwd_gemm() {
 
 cudaError_t launch_fwd_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                             const CUtensorMap& map_h16,
-                            const TileArgs& args, int grid, cudaStream_t stream) {
-  return ctas == 2 ? launch_gemm_variant<MODE_FWD, 2>(map_a, map_b, args, grid, stream, nullptr, &map_h16)
-                   : launch_gemm_variant<MODE_FWD, 1>(map_a, map_b, args, grid, stream, nullptr, &map_h16);
+                            const TileArgs& args, int grid, cudaStream_t stream,
+                            const CUtensorMap* map_hc) {
+  return ctas == 2 ? launch_gemm_variant<MODE_FWD, 2>(map_a, map_b, args, grid, stream, nullptr, &map_h16, map_hc)
+                   : launch_gemm_variant<MODE_FWD, 1>(map_a, map_b, args, grid, stream, nullptr, &map_h16, map_hc);
 }
 
 // The active-row list of a loss call: the 16-row segments that hold any

@@ -861,6 +861,8 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             nbox[na] = mn_out_cols<CTAS>(args, t * C::kTileN + na * BN) / (64 * CTAS);
             b_bytes += static_cast<uint32_t>(nbox[na]) * (BK * 64 * 2);
           }
+          int hk_next[kSegs];  // MODE_DW: rows of h of the next stage's row block
+          if constexpr (MODE == MODE_DW) h_rows(args, (wk.kb * C::kKSub * BK) / BM, hk_next);
           for (int k = wk.kb; k < wk.ke; ++k, ++it) {
             const int s = it % kStages;
             const uint32_t round = it / kStages;
@@ -892,15 +894,22 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
               const uint32_t lead = CTAS == 2 ? mapa_shared(smem_u32(&full_bar[s]), 0) : 0u;
               if (CTAS == 2) mbar_arrive_expect_tx_cluster(lead, C::kKSub * (A_BYTES + b_bytes));
               else mbar_arrive_expect_tx(&full_bar[s], C::kKSub * (A_BYTES + b_bytes));
+              // The rows of h of this stage's row block were looked up a stage
+              // ahead, so that the lookup's loads do not hold up the ring.
+              int hk[kSegs];
 #pragma unroll
-              int hk[kSegs];  // the rows of h of this stage's row block
-              h_rows(args, (k * C::kKSub * BK) / BM, hk);
+              for (int j = 0; j < kSegs; ++j) hk[j] = hk_next[j];
+              if (k + 1 < wk.ke) h_rows(args, ((k + 1) * C::kKSub * BK) / BM, hk_next);
+#pragma unroll
               for (int ks = 0; ks < C::kKSub; ++ks) {
                 const int kr = (k * C::kKSub + ks) * BK;  // chunk-local row of this K slice
-                const int j0 = (kr % BM) / SEG;            // its first segment in the block
+                const bool second = (kr % BM) >= BK;       // its half of the block's segments
+                int h4[BK / SEG];
+#pragma unroll
+                for (int j = 0; j < BK / SEG; ++j) h4[j] = second ? hk[BK / SEG + j] : hk[j];
                 bool one = true;
 #pragma unroll
-                for (int j = 1; j < BK / SEG; ++j) one = one && hk[j0 + j] == hk[j0] + j * SEG;
+                for (int j = 1; j < BK / SEG; ++j) one = one && h4[j] == h4[0] + j * SEG;
                 // A = G^T: 128 vocab rows (two 64-wide MN blocks) x 64 chunk rows.
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
@@ -912,12 +921,12 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
                   uint8_t* dst = b_dst + ks * C::kBBytes + jb * (BK * 64 * 2);
                   const int col = t * BN + static_cast<int>(rank) * nbox[0] * 64 + jb * 64;
                   if (one) {
-                    load_box<CTAS>(dst, &map_b, &full_bar[s], lead, col, hk[j0], false, 0);
+                    load_box<CTAS>(dst, &map_b, &full_bar[s], lead, col, h4[0], false, 0);
                   } else {
 #pragma unroll
                     for (int j = 0; j < BK / SEG; ++j)
                       load_box<CTAS>(dst + j * (SEG * 64 * 2), &map_h16, &full_bar[s], lead, col,
-                                     hk[j0 + j], false, 0);
+                                     h4[j], false, 0);
                   }
                 }
               }

@@ -159,7 +159,8 @@ cudaError_t prepare_fwd_gemm();   // opt-in to the large dynamic smem
 cudaError_t prepare_bwd_gemms();
 cudaError_t launch_fwd_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,
                             const CUtensorMap& map_h16,
-                            const TileArgs& args, int grid, cudaStream_t stream);
+                            const TileArgs& args, int grid, cudaStream_t stream,
+                            const CUtensorMap* map_hc = nullptr);
 // map_g: the chunk's bf16 G block [rows][ldG] as a store map, 64 x 32 boxes with
 // the 128-byte swizzle (used by the CTA-pair variant).
 cudaError_t launch_bwdg_gemm(int ctas, const CUtensorMap& map_a, const CUtensorMap& map_b,

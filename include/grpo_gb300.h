@@ -198,7 +198,9 @@ void grpo_default_params(grpo_params* params);
  * does not depend on the chunking). Host only, touches no GPU (except with
  * GRPO_FLAG_FIT_FREE_MEMORY, which reads the free memory). The size grows
  * with N (a few fp32 per token) and with the chunk (chunk x V for the stored
- * form, chunk x vocab_block otherwise), never with N x V: the point of
+ * form, chunk x vocab_block otherwise, and chunk x D for a copy of the rows
+ * of h whose 16-row segments of active rows do not form consecutive rows),
+ * never with N x V: the point of
  * "GRPO with 7x longer context", section "Flattened sequence length
  * chunking", Eq. 1-3, where the logit memory follows the chunk, not the
  * batch. Returns GRPO_OK or GRPO_ERR_INVALID_ARG / _UNSUPPORTED_SHAPE /
@@ -254,7 +256,10 @@ typedef struct grpo_plan_info {
   int32_t vocab_block;       /* vocab columns per backward block             */
   int32_t n_chunks;          /* backward chunks                              */
   int32_t n_vocab_blocks;    /* backward vocab blocks per chunk              */
-  int32_t fwd_splits;        /* forward vocab splits (partials per row)      */
+  int32_t fwd_splits;        /* forward vocab splits (partials per row):
+                                of the loss call's logit GEMMs in the stored
+                                and recomputed forms, else of the one
+                                logit GEMM of grpo_logp_fwd                */
   int32_t launches_logp;     /* kernel launches of one grpo_logp_fwd call    */
   int32_t launches_loss;     /* kernel launches of one grpo_loss_fwd_bwd
                                 with a mask (without one: one fewer, and

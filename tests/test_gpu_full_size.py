@@ -202,14 +202,8 @@ def test_qwen3_head_chunk_sweep(clp, flags):
     L0, lp0, dh0, _ = out[1024]
     for chunk in (4096, 16384):
         L1, lp1, dh1, _ = out[chunk]
-        if flags == 16:
-            # Recomputed logits: the forward runs over the whole batch at once
-            # and dH sums the same vocabulary blocks in the same order, so
-            # nothing depends on the chunk.
-            assert torch.equal(L0, L1) and torch.equal(lp0, lp1) and torch.equal(dh0, dh1)
-        else:
-            # Stored logits or the single pass: each chunk's forward splits the
-            # vocabulary to fill whole SM waves, so the fp32 sums run in a
-            # chunk-dependent order.
-            assert (lp0 - lp1).abs().max().item() <= 1e-4
-            assert abs(L0.item() - L1.item()) <= 1e-5 * abs(L0.item())
+        # Every form's forward splits the vocabulary to fill whole rounds of SM
+        # pairs at its chunk size, so the fp32 sums run in a chunk-dependent
+        # order: the results agree to rounding, not bit for bit.
+        assert (lp0 - lp1).abs().max().item() <= 1e-4
+        assert abs(L0.item() - L1.item()) <= 1e-5 * abs(L0.item())
