@@ -441,13 +441,13 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
     for (int i = threadIdx.x; i < n_vec; i += blockDim.x) row[i] = make_uint4(0, 0, 0, 0);
     return;
   }
-  // Stored value of column v: z'_v - m_b, m_b the maximum of its 64-column box
-  // b = v / 64 (vector i of 8 columns lies in box i / 8).
+  // Stored value of column v: (z'_v - m_b) log2e, m_b the maximum of its
+  // 64-column box b = v / 64 (vector i of 8 columns lies in box i / 8).
   const float* bm = a.box_max + lrow;
   auto box_max = [&](int i) { return __ldg(bm + static_cast<long long>(i >> 3) * a.ldM); };
   if (a.xmode == 0) {
     // Without a transform: -g 2^(z log2e - lse2) = -sign(g) 2^(z log2e + log2|g| - lse2),
-    // one FFMA and one exponential per logit and the sign set on each packed
+    // one add and one exponential per logit and the sign set on each packed
     // pair; the target column and the padding past the vocabulary are fixed
     // up afterwards.
     const float c = log2f(fabsf(g)) - lse2;
@@ -458,9 +458,9 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
       uint32_t o[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        float z0, z1;
-        unpack_f16x2(w[k], z0, z1);
-        o[k] = pack_bf16x2(ex2(fmaf(z0, kLog2e, cb)), ex2(fmaf(z1, kLog2e, cb))) ^ sgn;
+        float t0, t1;
+        add_f16x2_f32(w[k], cb, t0, t1);
+        o[k] = pack_bf16x2(ex2(t0), ex2(t1)) ^ sgn;
       }
       return make_uint4(o[0], o[1], o[2], o[3]);
     };
@@ -489,6 +489,7 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
   auto convert = [&](const uint4 in, int i) {
     const uint32_t w[4] = {in.x, in.y, in.z, in.w};
     const float mb = i * 8 < a.vocab ? box_max(i) : 0.f;
+    const float cb = fmaf(mb, kLog2e, -lse2);
     uint32_t o[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -496,7 +497,8 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int v = i * 8 + k * 2 + h;
-        const float z = half_bits_to_float(h == 0 ? (w[k] & 0xffffu) : (w[k] >> 16)) + mb;
+        const float sv = half_bits_to_float(h == 0 ? (w[k] & 0xffffu) : (w[k] >> 16));
+        const float z = fmaf(sv, kLn2, mb);
         float d = 1.f;  // dz'/dz recovered from the stored z'
         if (a.xmode == 1) {
           d = a.k0;
@@ -504,7 +506,7 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
           const float u = z / a.k2;
           d = a.k0 * fmaf(-u, u, 1.f);
         }
-        float val = ng * ex2(fmaf(z, kLog2e, -lse2));
+        float val = ng * ex2(sv + cb);
         if (v == y) val += g;
         gv[h] = v < a.vocab ? val * d : 0.f;
       }
@@ -628,21 +630,20 @@ __global__ void __launch_bounds__(kGformThreads) single_pass_p_kernel(const Gfor
     const float mb = box_max(i);
     const uint32_t w[4] = {in.x, in.y, in.z, in.w};
     uint32_t o[4];
+    const float c = fmaf(mb, kLog2e, -m2);
     if (a.xmode == 0) {
-      const float c = fmaf(mb, kLog2e, -m2);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        float z0, z1;
-        unpack_f16x2(w[k], z0, z1);
-        o[k] = pack_bf16x2(ex2(fmaf(z0, kLog2e, c)), ex2(fmaf(z1, kLog2e, c)));
+        float t0, t1;
+        add_f16x2_f32(w[k], c, t0, t1);
+        o[k] = pack_bf16x2(ex2(t0), ex2(t1));
       }
     } else {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        float z0, z1;
-        unpack_f16x2(w[k], z0, z1);
-        z0 += mb;
-        z1 += mb;
+        float s0, s1;
+        unpack_f16x2(w[k], s0, s1);
+        const float z0 = fmaf(s0, kLn2, mb), z1 = fmaf(s1, kLn2, mb);
         float d0 = 1.f, d1 = 1.f;  // dz'/dz recovered from the stored z'
         if (a.xmode == 1) {
           d0 = d1 = a.k0;
@@ -651,7 +652,7 @@ __global__ void __launch_bounds__(kGformThreads) single_pass_p_kernel(const Gfor
           d0 = a.k0 * fmaf(-u0, u0, 1.f);
           d1 = a.k0 * fmaf(-u1, u1, 1.f);
         }
-        o[k] = pack_bf16x2(ex2(fmaf(z0, kLog2e, -m2)) * d0, ex2(fmaf(z1, kLog2e, -m2)) * d1);
+        o[k] = pack_bf16x2(ex2(s0 + c) * d0, ex2(s1 + c) * d1);
       }
     }
     return make_uint4(o[0], o[1], o[2], o[3]);

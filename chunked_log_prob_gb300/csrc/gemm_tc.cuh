@@ -62,6 +62,7 @@ constexpr int A_BYTES = BM * BK * 2;      // 16 KB
 constexpr int GEMM_THREADS = 192;
 constexpr int TMEM_COLS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 enum GemmMode { MODE_FWD = 0, MODE_BWDG = 1, MODE_DH = 2, MODE_FWDS = 3, MODE_DW = 4,
                 MODE_DHS = 5, MODE_UAC = 6, MODE_UAP = 7 };
@@ -122,7 +123,7 @@ struct TileArgs {
   long long ldG;
   // MODE_FWDS (written), MODE_DHS (read)
   uint16_t* S;           // [local rows][ldS] fp16 logits of the chunk, each 64-column
-                         // box stored relative to its own maximum
+                         // box stored relative to its own maximum, in log2 units
   long long ldS;
   float* box_max;        // [ceil(V / 64)][ldM] those maxima (fp32), box-major
   long long ldM;         // rows of the chunk block (stride between boxes)
@@ -249,20 +250,24 @@ __device__ __forceinline__ int swz_offset(int r, int c) {
 }
 
 // Per-row constants of the in-GEMM conversion of stored logits (MODE_DHS,
-// MODE_UAC). A stored value s of column v is z'_v - zoff, zoff the maximum of
-// the column's 64-column box (one pipeline stage), and becomes the bf16
-//   without a transform:  sign * 2^(s log2e + c + zoff log2e)
-//   with one:             scale * 2^((s + zoff) log2e + shift2) f'(S_v)
-// (f' recovered from z', as in dz_of_logit); the target column gets ytarget.
-//   MODE_DHS (G):  c = log2|g| - lse2, sign = -sign(g), scale = -g,
-//                  shift2 = -lse2, ytarget = g (1 - p_y) f'_y
-//   MODE_UAC (P):  c = -M, sign = +, scale = 1, shift2 = -M, ytarget = 0
+// MODE_UAC). A stored value s of column v is (z'_v - zoff) log2e, zoff the
+// maximum of the column's 64-column box (one pipeline stage), and becomes the
+// bf16
+//   without a transform:  2^(s + c + zoff log2e)
+//   with one:             scale * 2^(s + zoff log2e + shift2) f'(S_v)
+// (f' recovered from z'_v = s ln2 + zoff, as in dz_of_logit); the target
+// column gets ytarget.
+//   MODE_DHS (G / sigma, sigma = -sign(g) the same for the whole row, so that
+//             the epilogue applies it to the row of dH once instead of to
+//             every element): c = log2|g| - lse2, scale = |g|, shift2 = -lse2,
+//             ytarget = sigma g (1 - p_y) f'_y
+//   MODE_UAC (P):  c = -M, scale = 1, shift2 = -M, ytarget = 0
 // with M the row's running maximum (log2 units).
 struct RowCvt {
   bool zero;        // the row contributes nothing: zeros whatever the buffer held
   int y;            // target column (vocabulary index), or -1
   float c;          // see above (without the box maximum)
-  uint32_t sgn;     // sign bits XORed into each packed bf16 pair
+  bool neg;         // MODE_DHS: sigma = -1 (g > 0), the row of dH is negated
   float scale, shift2;
   float ytarget;
 };
@@ -377,13 +382,14 @@ __device__ __forceinline__ void stage_row_to_bf16(const TileArgs& a, uint8_t* ti
       uint32_t o[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        float z0, z1;
-        unpack_f16x2(w[e], z0, z1);
-        o[e] = pack_bf16x2(ex2(fmaf(z0, kLog2e, c)), ex2(fmaf(z1, kLog2e, c))) ^ rc.sgn;
+        float t0, t1;
+        add_f16x2_f32(w[e], c, t0, t1);
+        o[e] = pack_bf16x2(ex2(t0), ex2(t1));
       }
       row[(jb + j) ^ sw] = make_uint4(o[0], o[1], o[2], o[3]);
     }
   } else {
+    const float c2 = fmaf(zoff, kLog2e, rc.shift2);
 #pragma unroll 1
     for (int j = jb; j < jb + NCH; ++j) {
       const uint4 x = row[j ^ sw];
@@ -391,12 +397,11 @@ __device__ __forceinline__ void stage_row_to_bf16(const TileArgs& a, uint8_t* ti
       uint32_t o[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        float z0, z1;
-        unpack_f16x2(w[e], z0, z1);
-        z0 += zoff;
-        z1 += zoff;
-        o[e] = pack_bf16x2(rc.scale * ex2(fmaf(z0, kLog2e, rc.shift2)) * dz_of_logit(a, z0),
-                           rc.scale * ex2(fmaf(z1, kLog2e, rc.shift2)) * dz_of_logit(a, z1));
+        float s0, s1;
+        unpack_f16x2(w[e], s0, s1);
+        const float z0 = fmaf(s0, kLn2, zoff), z1 = fmaf(s1, kLn2, zoff);
+        o[e] = pack_bf16x2(rc.scale * ex2(s0 + c2) * dz_of_logit(a, z0),
+                           rc.scale * ex2(s1 + c2) * dz_of_logit(a, z1));
       }
       row[j ^ sw] = make_uint4(o[0], o[1], o[2], o[3]);
     }
@@ -1130,7 +1135,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
       rc.zero = true;
       rc.y = -1;
       rc.c = 0.f;
-      rc.sgn = 0u;
+      rc.neg = false;
       rc.scale = 1.f;
       rc.shift2 = 0.f;
       rc.ytarget = 0.f;
@@ -1153,10 +1158,11 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             rc.zero = false;
             rc.y = args.ids[grow];
             rc.c = log2f(fabsf(gval)) - lse2;
-            rc.sgn = gval > 0.f ? 0x80008000u : 0u;  // -g: the sign of each bf16
-            rc.scale = -gval;
+            rc.neg = gval > 0.f;
+            rc.scale = fabsf(gval);
             rc.shift2 = -lse2;
-            rc.ytarget = (gval - gval * ex2(fmaf(zy, kLog2e, -lse2))) * dz_of_logit(args, zy);
+            const float yt = (gval - gval * ex2(fmaf(zy, kLog2e, -lse2))) * dz_of_logit(args, zy);
+            rc.ytarget = rc.neg ? -yt : yt;
           }
         }
       } else if (is_uacc(MODE)) {
@@ -1297,6 +1303,9 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
               mx1 = fmaxf(mx1, fmaxf(lo[j + 1], hi[j + 1]));
             }
             const float mb = fmaxf(mx0, mx1);  // finite: col0 < V
+            // Stored: (z - mb) log2e in fp16, so that every reader's exponent
+            // is the stored value plus one fp32 constant per box.
+            const float nmb2 = -mb * kLog2e;
             const unsigned off = static_cast<unsigned>(y - col0);
             if (off < 64u) {
               float z = 0.f;
@@ -1318,15 +1327,15 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                   srow[j ^ (lane & 7)] =
-                      make_uint4(pack_f16x2(lo[8 * j] - mb, lo[8 * j + 1] - mb),
-                                 pack_f16x2(lo[8 * j + 2] - mb, lo[8 * j + 3] - mb),
-                                 pack_f16x2(lo[8 * j + 4] - mb, lo[8 * j + 5] - mb),
-                                 pack_f16x2(lo[8 * j + 6] - mb, lo[8 * j + 7] - mb));
+                      make_uint4(pack_f16x2(fmaf(lo[8 * j], kLog2e, nmb2), fmaf(lo[8 * j + 1], kLog2e, nmb2)),
+                                 pack_f16x2(fmaf(lo[8 * j + 2], kLog2e, nmb2), fmaf(lo[8 * j + 3], kLog2e, nmb2)),
+                                 pack_f16x2(fmaf(lo[8 * j + 4], kLog2e, nmb2), fmaf(lo[8 * j + 5], kLog2e, nmb2)),
+                                 pack_f16x2(fmaf(lo[8 * j + 6], kLog2e, nmb2), fmaf(lo[8 * j + 7], kLog2e, nmb2)));
                   srow[(4 + j) ^ (lane & 7)] =
-                      make_uint4(pack_f16x2(hi[8 * j] - mb, hi[8 * j + 1] - mb),
-                                 pack_f16x2(hi[8 * j + 2] - mb, hi[8 * j + 3] - mb),
-                                 pack_f16x2(hi[8 * j + 4] - mb, hi[8 * j + 5] - mb),
-                                 pack_f16x2(hi[8 * j + 6] - mb, hi[8 * j + 7] - mb));
+                      make_uint4(pack_f16x2(fmaf(hi[8 * j], kLog2e, nmb2), fmaf(hi[8 * j + 1], kLog2e, nmb2)),
+                                 pack_f16x2(fmaf(hi[8 * j + 2], kLog2e, nmb2), fmaf(hi[8 * j + 3], kLog2e, nmb2)),
+                                 pack_f16x2(fmaf(hi[8 * j + 4], kLog2e, nmb2), fmaf(hi[8 * j + 5], kLog2e, nmb2)),
+                                 pack_f16x2(fmaf(hi[8 * j + 6], kLog2e, nmb2), fmaf(hi[8 * j + 7], kLog2e, nmb2)));
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -1342,27 +1351,27 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
               if (col0 + 64 <= args.vocab) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                  st_global_v4(dst + j * 8, pack_f16x2(lo[8 * j] - mb, lo[8 * j + 1] - mb),
-                               pack_f16x2(lo[8 * j + 2] - mb, lo[8 * j + 3] - mb),
-                               pack_f16x2(lo[8 * j + 4] - mb, lo[8 * j + 5] - mb),
-                               pack_f16x2(lo[8 * j + 6] - mb, lo[8 * j + 7] - mb));
-                  st_global_v4(dst + 32 + j * 8, pack_f16x2(hi[8 * j] - mb, hi[8 * j + 1] - mb),
-                               pack_f16x2(hi[8 * j + 2] - mb, hi[8 * j + 3] - mb),
-                               pack_f16x2(hi[8 * j + 4] - mb, hi[8 * j + 5] - mb),
-                               pack_f16x2(hi[8 * j + 6] - mb, hi[8 * j + 7] - mb));
+                  st_global_v4(dst + j * 8, pack_f16x2(fmaf(lo[8 * j], kLog2e, nmb2), fmaf(lo[8 * j + 1], kLog2e, nmb2)),
+                               pack_f16x2(fmaf(lo[8 * j + 2], kLog2e, nmb2), fmaf(lo[8 * j + 3], kLog2e, nmb2)),
+                               pack_f16x2(fmaf(lo[8 * j + 4], kLog2e, nmb2), fmaf(lo[8 * j + 5], kLog2e, nmb2)),
+                               pack_f16x2(fmaf(lo[8 * j + 6], kLog2e, nmb2), fmaf(lo[8 * j + 7], kLog2e, nmb2)));
+                  st_global_v4(dst + 32 + j * 8, pack_f16x2(fmaf(hi[8 * j], kLog2e, nmb2), fmaf(hi[8 * j + 1], kLog2e, nmb2)),
+                               pack_f16x2(fmaf(hi[8 * j + 2], kLog2e, nmb2), fmaf(hi[8 * j + 3], kLog2e, nmb2)),
+                               pack_f16x2(fmaf(hi[8 * j + 4], kLog2e, nmb2), fmaf(hi[8 * j + 5], kLog2e, nmb2)),
+                               pack_f16x2(fmaf(hi[8 * j + 6], kLog2e, nmb2), fmaf(hi[8 * j + 7], kLog2e, nmb2)));
                 }
               } else {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                   if (col0 + j < args.vocab)
-                    dst[j] = static_cast<uint16_t>(pack_f16x2(lo[j] - mb, 0.f) & 0xffffu);
+                    dst[j] = static_cast<uint16_t>(pack_f16x2(fmaf(lo[j], kLog2e, nmb2), 0.f) & 0xffffu);
                   if (col0 + 32 + j < args.vocab)
-                    dst[32 + j] = static_cast<uint16_t>(pack_f16x2(hi[j] - mb, 0.f) & 0xffffu);
+                    dst[32 + j] = static_cast<uint16_t>(pack_f16x2(fmaf(hi[j], kLog2e, nmb2), 0.f) & 0xffffu);
                 }
               }
               args.box_max[static_cast<long long>(lcol >> 6) * args.ldM + lrow] = mb;
             }
-            const float mn = fmaxf(m2, mb * kLog2e);
+            const float mn = fmaxf(m2, -nmb2);
             float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
@@ -1576,6 +1585,12 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             if (d0 >= args.hidden) break;  // warp-uniform
             float v[32];
             tmem_ld32(tbase + c * 32, v);
+            if constexpr (MODE == MODE_DHS) {
+              if (rc.neg) {  // the converter wrote G / sigma
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = -v[e];
+              }
+            }
             if (wk.cut) {
               // A piece of a split unit: its fp32 partial tile goes to its slot.
               if (valid) {

@@ -67,7 +67,7 @@ struct GformArgs {
   float* lse_out;        // finalize_rows: [rows] lse (natural log), by global row
   float* g_out;          // finalize_rows: [rows] dL/dlogp (0 for rows that do not count)
   uint16_t* S;           // [chunk rows][ldS]: fp16 logits in (each 64-column box
-                         // relative to its maximum), bf16 G out
+                         // relative to its maximum, in log2 units), bf16 G out
   long long ldS;
   const float* box_max;  // [ceil(V / 64)][ldM] the boxes' maxima
   long long ldM;

@@ -376,6 +376,17 @@ __device__ __forceinline__ void unpack_f16x2(uint32_t w, float& lo, float& hi) {
       : "r"(w));
 }
 
+// Two fp16 (low half first) each added to the fp32 c, in fp32: one
+// mixed-precision add per value instead of a widening and an add.
+__device__ __forceinline__ void add_f16x2_f32(uint32_t w, float c, float& lo, float& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "add.rn.f32.f16 %0, l, %3;\n\t"
+      "add.rn.f32.f16 %1, h, %3;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(w), "f"(c));
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
