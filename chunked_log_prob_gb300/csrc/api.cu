@@ -153,6 +153,15 @@ int stored_fwd_splits(int nrb, int nvt, int sms, double* eff_out) {
   return best;
 }
 
+// Row units per raster group of a logit GEMM launch: all of its row units, as
+// long as their hidden rows (re-read for every vocab tile) stay within a
+// third of L2; past that the slots in flight would evict each other's rows.
+int fwd_group_rows(int n_ru, int D, int ctas) {
+  constexpr long long kHBudget = 40LL << 20;
+  const long long per_ru = static_cast<long long>(BM) * ctas * D * 2;
+  return static_cast<int>(std::max<long long>(1, std::min<long long>(n_ru, kHBudget / per_ru)));
+}
+
 // Row units per raster group: the slots in flight (one per SM pair) cover
 // group_rows row units x (slots / group_rows) vocab tiles or splits, so each
 // W tile fetched from HBM is shared through L2 by group_rows slots and each
@@ -170,6 +179,23 @@ int group_rows_exact(int n_ru, int slots) {
   for (int r = cap; r > 1; --r)
     if (slots % r == 0) return r;
   return 1;
+}
+
+// Raster and vocab splits of a logit GEMM over n_ru row units in one launch:
+// one round of the slots per raster group (group_rows_exact, slots / group
+// splits, long units) when that fills its rounds to 90 %; otherwise the splits
+// that fill whole waves, over L2-sized groups (measured: at 512 row units the
+// first is 10-20 % faster, at 32 the second 12 %).
+void whole_batch_raster(int n_ru, int nvt, int D, int ctas, int slots, int* group, int* splits) {
+  const int r = group_rows_exact(n_ru, slots);
+  const int sp = std::min(std::max(1, slots / r), std::min(nvt, kMaxSplits));
+  if (wave_eff(static_cast<long long>(n_ru) * sp, slots) >= 0.9) {
+    *group = r;
+    *splits = sp;
+  } else {
+    *group = fwd_group_rows(n_ru, D, ctas);
+    *splits = stored_fwd_splits(n_ru, nvt, slots, nullptr);
+  }
 }
 
 // Modelled GEMM time of the stored-logit schedule with chunks of nrb row
@@ -754,7 +780,9 @@ TileArgs base_args(const Layout& L, const Ws& w) {
 }
 
 // Forward logit GEMM: per-split (max, sum-exp) and z_y for every row of the
-// active segments in `seg_list` (every row when it is null).
+// active segments in `seg_list` (every row when it is null), in the raster of
+// whole_batch_raster; with a segment list the kernel sets the splits from the
+// active row units (whole waves), and the row finish reads every partial slot.
 int run_forward(const void* hidden, const void* W, const int32_t* ids, const uint8_t* mask,
                 const int* seg_list, const int* n_seg, const grpo_params* prm,
                 const Layout& L, const Ws& w, int sms, int* splits_out, cudaStream_t st) {
@@ -773,11 +801,12 @@ int run_forward(const void* hidden, const void* W, const int32_t* ids, const uin
   a.n_seg = n_seg;
   a.k_iters = static_cast<int>(cdiv(L.D, BK));
   const int n_ru = static_cast<int>(cdiv(a.n_rb, L.ctas));
+  int group = 1, splits = 1;
+  whole_batch_raster(n_ru, L.nvt, L.D, L.ctas, slots, &group, &splits);
   a.group_rows = (prm != nullptr && prm->raster_rows > 0) ? std::min(prm->raster_rows, n_ru)
-                                                         : group_rows_exact(n_ru, slots);
-  int splits = std::max(1, slots / a.group_rows);
-  splits = std::min(splits, std::min(L.nvt, kMaxSplits));
+                                                         : group;
   a.n_cols = splits;
+  if (seg_list != nullptr) a.max_cols = std::min(L.nvt, kMaxSplits);
   a.n_vtiles = L.nvt;
   a.v0 = 0;
   a.ids = ids;
@@ -787,21 +816,22 @@ int run_forward(const void* hidden, const void* W, const int32_t* ids, const uin
   a.zy = w.zy;
   a.part_ld = L.nr;
   const long long units = static_cast<long long>(n_ru) * a.n_cols;
-  const int grid = L.ctas * static_cast<int>(std::min<long long>(units, slots));
+  const int grid =
+      L.ctas * (a.max_cols > 0 ? slots : static_cast<int>(std::min<long long>(units, slots)));
   if (launch_fwd_gemm(L.ctas, map_h, map_w, map_h16, a, grid, st) != cudaSuccess)
     return GRPO_ERR_CUDA;
-  *splits_out = splits;
+  *splits_out = a.max_cols > 0 ? a.max_cols : splits;
   return GRPO_OK;
 }
 
 // The recomputed form's forward of a loss call, one logit GEMM per chunk of
 // the backward's chunking, after the chunk's non-consecutive row blocks of h
-// are gathered (so that every row block loads in one box). Every chunk splits
-// the vocabulary into the count that makes a full chunk's units whole waves of
-// the SM pairs (a count set by the whole batch leaves most pairs idle on a
-// chunk of a few row units), and the row finish reads that many partial slots
-// for every row. A row's partial sums, and so its last bits, depend on the
-// chunk size.
+// are gathered (so that every row block loads in one box). Each launch splits
+// the vocabulary into the count that makes its active row units whole waves
+// of the SM pairs (set by the kernel; a count set by the whole batch leaves
+// most pairs idle on a chunk of a few row units), and the row finish reads
+// every partial slot. A row's partial sums, and so its last bits, depend on
+// the chunk size.
 int run_forward_chunks(const void* hidden, const void* W, const int32_t* ids,
                        const uint8_t* mask, const grpo_params* prm, const Layout& L,
                        const Ws& w, int sms, int* splits_out, cudaStream_t st) {
@@ -828,8 +858,9 @@ int run_forward_chunks(const void* hidden, const void* W, const int32_t* ids,
     a.hc = 1;
     a.k_iters = static_cast<int>(cdiv(L.D, BK));
     a.group_rows = (prm != nullptr && prm->raster_rows > 0) ? std::min(prm->raster_rows, n_ru)
-                                                            : n_ru;
+                                                            : fwd_group_rows(n_ru, L.D, L.ctas);
     a.n_cols = splits;
+    a.max_cols = std::min(L.nvt, kMaxSplits);
     a.n_vtiles = L.nvt;
     a.v0 = 0;
     a.ids = ids;
@@ -842,12 +873,11 @@ int run_forward_chunks(const void* hidden, const void* W, const int32_t* ids,
     if (!encode_2d(&map_hc, w.hc, L.D, static_cast<uint64_t>(n_rb) * BM, L.D, BK, BM))
       return GRPO_ERR_CUDA;
     if (launch_gather_blocks(hidden, w.hc, a, st) != cudaSuccess) return GRPO_ERR_CUDA;
-    const long long units = static_cast<long long>(n_ru) * splits;
-    const int grid = L.ctas * static_cast<int>(std::min<long long>(units, slots));
-    if (launch_fwd_gemm(L.ctas, map_h, map_w, map_h16, a, grid, st, &map_hc) != cudaSuccess)
+    if (launch_fwd_gemm(L.ctas, map_h, map_w, map_h16, a, L.ctas * slots, st, &map_hc) !=
+        cudaSuccess)
       return GRPO_ERR_CUDA;
   }
-  *splits_out = splits;
+  *splits_out = std::min(L.nvt, kMaxSplits);
   return GRPO_OK;
 }
 
@@ -1036,7 +1066,9 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
                : GRPO_ERR_CUDA;
   };
 
-  // (1) logits of chunk c: online LSE partials, z_y, fp16 copy.
+  // (1) logits of chunk c: online LSE partials, z_y, fp16 copy. The kernel
+  // splits the vocabulary for the chunk's active row units (whole waves of
+  // the SM pairs); the row finish reads every partial slot.
   auto fwds = [&](int c, int* splits_out) -> int {
     const int n_rb = chunk_rbs(c);
     const int n_ru = static_cast<int>(cdiv(n_rb, L.ctas));
@@ -1049,8 +1081,9 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     a.seg_list = w.seg_list;
     a.n_seg = w.n_seg;
     a.k_iters = static_cast<int>(cdiv(L.D, BK));
-    a.group_rows = n_ru;
+    a.group_rows = fwd_group_rows(n_ru, L.D, L.ctas);
     a.n_cols = splits;
+    a.max_cols = std::min(L.nvt, kMaxSplits);
     a.n_vtiles = L.nvt;
     a.v0 = 0;
     a.ids = ids;
@@ -1071,10 +1104,8 @@ int run_stored(const void* hidden, const void* W, const int32_t* ids, const uint
     // The chunk's non-consecutive row blocks of h, copied for the GEMM.
     a.hc = 1;
     if (launch_gather_blocks(hidden, w.hc, a, st) != cudaSuccess) return GRPO_ERR_CUDA;
-    const long long units = static_cast<long long>(n_ru) * splits;
-    *splits_out = splits;
-    return launch_fwds_gemm(L.ctas, map_h, map_w_k, map_h16, map_st, a,
-                            L.ctas * static_cast<int>(std::min<long long>(units, slots)), st,
+    *splits_out = a.max_cols;
+    return launch_fwds_gemm(L.ctas, map_h, map_w_k, map_h16, map_st, a, L.ctas * slots, st,
                             &map_hc) == cudaSuccess
                ? GRPO_OK
                : GRPO_ERR_CUDA;
@@ -1833,8 +1864,9 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
   info->n_vocab_blocks = static_cast<int32_t>(cdiv(L.V, L.vblock));
   const int n_rb = static_cast<int>(L.nr / BM);
   const int slots = std::max(1, sms / L.ctas);
-  const int grp = group_rows_exact(static_cast<int>(cdiv(n_rb, L.ctas)), slots);
-  info->fwd_splits = std::min(std::max(1, slots / grp), std::min(L.nvt, kMaxSplits));
+  int group = 1;
+  whole_batch_raster(static_cast<int>(cdiv(n_rb, L.ctas)), L.nvt, L.D, L.ctas, slots, &group,
+                     &info->fwd_splits);
   info->launches_logp = L.n > 0 ? 2 : 0;
   // Tail-split dH-type launches (the stored form's fused dH GEMM, chunks that
   // run one after another, or the overlapped schedule's last chunk; the single
@@ -1852,7 +1884,8 @@ int grpo_get_plan(const grpo_shape* shape, const grpo_params* params, grpo_plan_
   if (L.n > 0 && params != nullptr && (params->flags & GRPO_FLAG_SEQUENCE_MEAN) != 0)
     info->launches_loss += 1;
   if (L.stored) info->n_vocab_blocks = 1;
-  // The loss call's forward of the stored and recomputed forms runs per chunk.
+  // The loss call's forward of the stored and recomputed forms runs per chunk
+  // (with padding, the kernels set the splits from the active rows).
   if (!L.single_pass)
     info->fwd_splits =
         stored_fwd_splits(L.chunk_rows / (BM * L.ctas), L.nvt, slots, nullptr);

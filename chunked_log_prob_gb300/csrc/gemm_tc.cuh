@@ -95,6 +95,9 @@ struct TileArgs {
   int k_iters;     // ceil(K / BK)
   int group_rows;  // row blocks per raster group
   int n_cols;      // FWD: vocab splits; BWDG: vocab tiles in block; DH: D tiles
+  int max_cols;    // FWD, FWDS: > 0: the kernel sets the vocab splits (at most this
+                   // many) from its active row units, and each row's split 0
+                   // fills the row's unused partial slots below it with (-inf, 0)
   int n_vtiles;    // FWD: vocab tiles in total
   int v0;          // BWDG/DH: first vocab column of the block (0 for FWD)
   int vocab;
@@ -194,11 +197,34 @@ __device__ __forceinline__ bool h_rows(const TileArgs& a, int li, int (&rows)[kS
   return consecutive;
 }
 
+// Vocab splits of a logit GEMM launch over n_ru row units: the count (at most
+// cap) whose units fill the slots' rounds best, the longest split setting the
+// pace; ties go to fewer splits. Exact integer comparison of
+// units / (rounds * slots) * (nvt / sp) / ceil(nvt / sp).
+__device__ __forceinline__ int fwd_splits_for(int n_ru, int nvt, int slots, int cap) {
+  int best = 1;
+  long long bn = 0, bd = 1;  // best efficiency as bn / bd
+  const int hi = min(nvt, cap);
+  for (int sp = 1; sp <= hi; ++sp) {
+    const long long units = static_cast<long long>(n_ru) * sp;
+    const long long rounds = (units + slots - 1) / slots;
+    const long long per = (nvt + sp - 1) / sp;
+    const long long num = units * nvt, den = rounds * slots * sp * per;
+    if (sp == 1 || static_cast<__int128>(num) * bd > static_cast<__int128>(bn) * den) {
+      best = sp;
+      bn = num;
+      bd = den;
+    }
+  }
+  return best;
+}
+
 template <int MODE>
-__device__ __forceinline__ void unit_tiles(const TileArgs& a, int col, int& t0, int& t1) {
+__device__ __forceinline__ void unit_tiles(const TileArgs& a, int n_cols, int col, int& t0,
+                                           int& t1) {
   if (is_fwd(MODE)) {
-    t0 = static_cast<int>((static_cast<long long>(col) * a.n_vtiles) / a.n_cols);
-    t1 = static_cast<int>((static_cast<long long>(col + 1) * a.n_vtiles) / a.n_cols);
+    t0 = static_cast<int>((static_cast<long long>(col) * a.n_vtiles) / n_cols);
+    t1 = static_cast<int>((static_cast<long long>(col + 1) * a.n_vtiles) / n_cols);
   } else {
     t0 = col;
     t1 = col + 1;
@@ -815,7 +841,13 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
   const int n_rb = launch_row_blocks(args);
   const int n_ru = MODE == MODE_DW ? (args.dw_rows + BM * CTAS - 1) / (BM * CTAS)
                                    : (n_rb + CTAS - 1) / CTAS;  // units of 128*CTAS rows
-  const int n_units = n_ru * args.n_cols;
+  // Units per row unit: FWD vocab splits (set here from the active row units
+  // when max_cols > 0), BWDG vocab tiles, dH-type D tiles.
+  int n_cols = args.n_cols;
+  if constexpr (is_fwd(MODE)) {
+    if (args.max_cols > 0) n_cols = fwd_splits_for(n_ru, args.n_vtiles, n_slots, args.max_cols);
+  }
+  const int n_units = n_ru * n_cols;
   // Stages per tile (k_iters counts 64-wide K slices; a stage holds kKSub).
   const int k_iters = ((MODE == MODE_DW ? n_rb * (BM / BK) : args.k_iters) + C::kKSub - 1) / C::kKSub;
   // This pair's units, and with a tail split its part of the last round.
@@ -834,8 +866,8 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
         if (!wl.get(args, n_ru, k_iters, i, wk)) break;
         if (wk.empty()) continue;
         int ru, col, t0, t1;
-        decode_unit(wk.u, n_ru, args.n_cols, args.group_rows, ru, col);
-        unit_tiles<MODE>(args, col, t0, t1);
+        decode_unit(wk.u, n_ru, n_cols, args.group_rows, ru, col);
+        unit_tiles<MODE>(args, n_cols, col, t0, t1);
         // A CTA whose row block lies past the list computes its partner's rows
         // again and stores nothing.
         int li = ru * CTAS + static_cast<int>(rank);
@@ -1019,8 +1051,8 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
         if (!wl.get(args, n_ru, k_iters, i, wk)) break;
         if (wk.empty()) continue;
         int ru, col, t0, t1;
-        decode_unit(wk.u, n_ru, args.n_cols, args.group_rows, ru, col);
-        unit_tiles<MODE>(args, col, t0, t1);
+        decode_unit(wk.u, n_ru, n_cols, args.group_rows, ru, col);
+        unit_tiles<MODE>(args, n_cols, col, t0, t1);
         for (int t = t0; t < t1 && ok; ++t, ++tile_it) {
           const uint32_t buf = tile_it % C::kNBuf;
           const uint32_t use = tile_it / C::kNBuf;
@@ -1118,8 +1150,8 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
       if (!wl.get(args, n_ru, k_iters, i, wk)) break;
       if (wk.empty()) continue;
       int ru, col, t0, t1;
-      decode_unit(wk.u, n_ru, args.n_cols, args.group_rows, ru, col);
-      unit_tiles<MODE>(args, col, t0, t1);
+      decode_unit(wk.u, n_ru, n_cols, args.group_rows, ru, col);
+      unit_tiles<MODE>(args, n_cols, col, t0, t1);
       const int li = ru * CTAS + static_cast<int>(rank);
       const bool block_ok = li < n_rb;
       const int lrow = li * BM + lrow_in_tile;  // row of the chunk workspace
@@ -1649,6 +1681,12 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
       if (is_fwd(MODE) && ok && valid) {
         args.part_m[static_cast<long long>(args.part_slot0 + col) * args.part_ld + grow] = m2;
         args.part_s[static_cast<long long>(args.part_slot0 + col) * args.part_ld + grow] = ssum;
+        if (col == 0) {  // slots no split of this launch writes: merge as nothing
+          for (int sl = n_cols; sl < args.max_cols; ++sl) {
+            args.part_m[static_cast<long long>(args.part_slot0 + sl) * args.part_ld + grow] = -INFINITY;
+            args.part_s[static_cast<long long>(args.part_slot0 + sl) * args.part_ld + grow] = 0.f;
+          }
+        }
       }
     }
     if constexpr (C::kTmaStore) {

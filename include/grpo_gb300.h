@@ -258,10 +258,12 @@ typedef struct grpo_plan_info {
   int32_t vocab_block;       /* vocab columns per backward block             */
   int32_t n_chunks;          /* backward chunks                              */
   int32_t n_vocab_blocks;    /* backward vocab blocks per chunk              */
-  int32_t fwd_splits;        /* forward vocab splits (partials per row):
-                                of the loss call's logit GEMMs in the stored
-                                and recomputed forms, else of the one
-                                logit GEMM of grpo_logp_fwd                */
+  int32_t fwd_splits;        /* forward vocab splits (partials per row) when
+                                every row is active: of the loss call's
+                                logit GEMMs in the stored and recomputed
+                                forms, else of grpo_logp_fwd's one logit
+                                GEMM (with masked rows the kernels set them
+                                from the active rows, at most 32)          */
   int32_t launches_logp;     /* kernel launches of one grpo_logp_fwd call    */
   int32_t launches_loss;     /* kernel launches of one grpo_loss_fwd_bwd
                                 with a mask (without one: one fewer, and
