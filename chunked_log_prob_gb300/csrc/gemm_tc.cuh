@@ -158,12 +158,22 @@ __device__ __forceinline__ void decode_unit(int u, int n_rb, int n_cols, int R, 
   rb = grp * R + (rem - col * rows_in_g);
 }
 
+// True when every segment of the batch is active: the list (ascending) is
+// then the identity, and a row's place needs no lookup.
+__device__ __forceinline__ bool all_segs_active(const TileArgs& a, int n) {
+  return static_cast<long long>(n) * SEG >= a.n_total;
+}
+
 // Global row of the launch's local row `lr` (row lr % BM of its local row
 // block lr / BM), or -1 past the active list.
 __device__ __forceinline__ long long row_of(const TileArgs& a, int lr) {
   if (a.seg_list == nullptr) return static_cast<long long>(a.rb_offset) * BM + lr;
   const int s = a.rb_offset * kSegs + lr / SEG;
-  if (a.n_seg != nullptr && s >= *a.n_seg) return -1;
+  if (a.n_seg != nullptr) {
+    const int n = *a.n_seg;
+    if (s >= n) return -1;
+    if (all_segs_active(a, n)) return static_cast<long long>(a.rb_offset) * BM + lr;
+  }
   return static_cast<long long>(a.seg_list[s]) * SEG + lr % SEG;
 }
 
@@ -188,6 +198,12 @@ __device__ __forceinline__ bool h_rows(const TileArgs& a, int li, int (&rows)[kS
   }
   const int s0 = (a.rb_offset + li) * kSegs;
   const int n = a.n_seg != nullptr ? *a.n_seg : s0 + kSegs;
+  if (a.n_seg != nullptr && all_segs_active(a, n)) {
+    // Rows past the batch read as zeros (the load's fill), as past the list.
+#pragma unroll
+    for (int j = 0; j < kSegs; ++j) rows[j] = s0 * SEG + j * SEG;
+    return true;
+  }
   bool consecutive = true;
 #pragma unroll
   for (int j = 0; j < kSegs; ++j) {
@@ -861,6 +877,9 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
       uint32_t it = 0;
       bool ok = true;
       const uint64_t pol_a = policy_evict_last();
+      // MODE_DW: every segment active, so that h's rows are in order.
+      const bool h_dense =
+          args.seg_list == nullptr || (args.n_seg != nullptr && all_segs_active(args, *args.n_seg));
       for (int i = 0; ok; ++i) {
         WorkItem wk;
         if (!wl.get(args, n_ru, k_iters, i, wk)) break;
@@ -899,7 +918,9 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             b_bytes += static_cast<uint32_t>(nbox[na]) * (BK * 64 * 2);
           }
           int hk_next[kSegs];  // MODE_DW: rows of h of the next stage's row block
-          if constexpr (MODE == MODE_DW) h_rows(args, (wk.kb * C::kKSub * BK) / BM, hk_next);
+          if constexpr (MODE == MODE_DW) {
+            if (!h_dense) h_rows(args, (wk.kb * C::kKSub * BK) / BM, hk_next);
+          }
           for (int k = wk.kb; k < wk.ke; ++k, ++it) {
             const int s = it % kStages;
             const uint32_t round = it / kStages;
@@ -931,12 +952,19 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
               const uint32_t lead = CTAS == 2 ? mapa_shared(smem_u32(&full_bar[s]), 0) : 0u;
               if (CTAS == 2) mbar_arrive_expect_tx_cluster(lead, C::kKSub * (A_BYTES + b_bytes));
               else mbar_arrive_expect_tx(&full_bar[s], C::kKSub * (A_BYTES + b_bytes));
-              // The rows of h of this stage's row block were looked up a stage
-              // ahead, so that the lookup's loads do not hold up the ring.
+              // The rows of h of this stage's row block: in order when every
+              // segment is active, else looked up a stage ahead, so that the
+              // lookup's loads do not hold up the ring.
               int hk[kSegs];
+              if (h_dense) {
+                const int r0 = (args.rb_offset + (k * C::kKSub * BK) / BM) * BM;
 #pragma unroll
-              for (int j = 0; j < kSegs; ++j) hk[j] = hk_next[j];
-              if (k + 1 < wk.ke) h_rows(args, ((k + 1) * C::kKSub * BK) / BM, hk_next);
+                for (int j = 0; j < kSegs; ++j) hk[j] = r0 + j * SEG;
+              } else {
+#pragma unroll
+                for (int j = 0; j < kSegs; ++j) hk[j] = hk_next[j];
+                if (k + 1 < wk.ke) h_rows(args, ((k + 1) * C::kKSub * BK) / BM, hk_next);
+              }
 #pragma unroll
               for (int ks = 0; ks < C::kKSub; ++ks) {
                 const int kr = (k * C::kKSub + ks) * BK;  // chunk-local row of this K slice
