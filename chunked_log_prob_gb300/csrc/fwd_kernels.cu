@@ -441,8 +441,9 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
     for (int i = threadIdx.x; i < n_vec; i += blockDim.x) row[i] = make_uint4(0, 0, 0, 0);
     return;
   }
-  // Stored value of column v: (z'_v - m_b) log2e, m_b the maximum of its
-  // 64-column box b = v / 64 (vector i of 8 columns lies in box i / 8).
+  // Stored value of column v: z'_v log2e - m_b, m_b the maximum of its
+  // 64-column box b = v / 64 times log2 e (vector i of 8 columns lies in box
+  // i / 8), as kept beside the block.
   const float* bm = a.box_max + lrow;
   auto box_max = [&](int i) { return __ldg(bm + static_cast<long long>(i >> 3) * a.ldM); };
   if (a.xmode == 0) {
@@ -453,7 +454,7 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
     const float c = log2f(fabsf(g)) - lse2;
     const uint32_t sgn = g > 0.f ? 0x80008000u : 0u;
     auto fast = [&](const uint4 in, float mb) {
-      const float cb = fmaf(mb, kLog2e, c);
+      const float cb = mb + c;
       const uint32_t w[4] = {in.x, in.y, in.z, in.w};
       uint32_t o[4];
 #pragma unroll
@@ -489,7 +490,7 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
   auto convert = [&](const uint4 in, int i) {
     const uint32_t w[4] = {in.x, in.y, in.z, in.w};
     const float mb = i * 8 < a.vocab ? box_max(i) : 0.f;
-    const float cb = fmaf(mb, kLog2e, -lse2);
+    const float cb = mb - lse2;
     uint32_t o[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -498,7 +499,7 @@ __global__ void __launch_bounds__(kGformThreads) finalize_gform_kernel(const Gfo
       for (int h = 0; h < 2; ++h) {
         const int v = i * 8 + k * 2 + h;
         const float sv = half_bits_to_float(h == 0 ? (w[k] & 0xffffu) : (w[k] >> 16));
-        const float z = fmaf(sv, kLn2, mb);
+        const float z = (sv + mb) * kLn2;
         float d = 1.f;  // dz'/dz recovered from the stored z'
         if (a.xmode == 1) {
           d = a.k0;
@@ -630,7 +631,7 @@ __global__ void __launch_bounds__(kGformThreads) single_pass_p_kernel(const Gfor
     const float mb = box_max(i);
     const uint32_t w[4] = {in.x, in.y, in.z, in.w};
     uint32_t o[4];
-    const float c = fmaf(mb, kLog2e, -m2);
+    const float c = mb - m2;
     if (a.xmode == 0) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -643,7 +644,7 @@ __global__ void __launch_bounds__(kGformThreads) single_pass_p_kernel(const Gfor
       for (int k = 0; k < 4; ++k) {
         float s0, s1;
         unpack_f16x2(w[k], s0, s1);
-        const float z0 = fmaf(s0, kLn2, mb), z1 = fmaf(s1, kLn2, mb);
+        const float z0 = (s0 + mb) * kLn2, z1 = (s1 + mb) * kLn2;
         float d0 = 1.f, d1 = 1.f;  // dz'/dz recovered from the stored z'
         if (a.xmode == 1) {
           d0 = d1 = a.k0;

@@ -128,7 +128,7 @@ struct TileArgs {
   uint16_t* S;           // [local rows][ldS] fp16 logits of the chunk, each 64-column
                          // box stored relative to its own maximum, in log2 units
   long long ldS;
-  float* box_max;        // [ceil(V / 64)][ldM] those maxima (fp32), box-major
+  float* box_max;        // [ceil(V / 64)][ldM] those maxima times log2 e (fp32), box-major
   long long ldM;         // rows of the chunk block (stride between boxes)
   // MODE_DW
   float* dW;             // [V][hidden] fp32 output / accumulator
@@ -292,12 +292,14 @@ __device__ __forceinline__ int swz_offset(int r, int c) {
 }
 
 // Per-row constants of the in-GEMM conversion of stored logits (MODE_DHS,
-// MODE_UAC). A stored value s of column v is (z'_v - zoff) log2e, zoff the
-// maximum of the column's 64-column box (one pipeline stage), and becomes the
+// MODE_UAC). A stored value s of column v is z'_v log2e - zoff, zoff the
+// maximum of the column's 64-column box (one pipeline stage) times log2 e, as
+// kept in fp32 beside the box (the value subtracted, so that adding it back
+// restores z'_v log2e exactly up to the fp16 rounding of s), and becomes the
 // bf16
-//   without a transform:  2^(s + c + zoff log2e)
-//   with one:             scale * 2^(s + zoff log2e + shift2) f'(S_v)
-// (f' recovered from z'_v = s ln2 + zoff, as in dz_of_logit); the target
+//   without a transform:  2^(s + zoff + c)
+//   with one:             scale * 2^(s + zoff + shift2) f'(S_v)
+// (f' recovered from z'_v = (s + zoff) ln2, as in dz_of_logit); the target
 // column gets ytarget.
 //   MODE_DHS (G / sigma, sigma = -sign(g) the same for the whole row, so that
 //             the epilogue applies it to the row of dH once instead of to
@@ -397,7 +399,7 @@ __device__ __forceinline__ void uacc_update8(const TileArgs& a, const UaccRow& r
 }
 
 // Rewrites chunks jb..jb+NCH-1 (8 columns each) of row r of a landed A stage
-// (64 stored values of vocab columns vbase.., box maximum zoff) in place as
+// (64 stored values of vocab columns vbase.., box maximum zoff in log2 units) in place as
 // bf16. Columns at or past the vocabulary size become zeros. The main loop
 // runs over logical chunks, so the 8 lanes of a shared-memory phase (8
 // consecutive rows, same chunk) touch 8 different physical chunks: no bank
@@ -414,7 +416,7 @@ __device__ __forceinline__ void stage_row_to_bf16(const TileArgs& a, uint8_t* ti
     return;
   }
   if (a.xmode == 0) {
-    const float c = fmaf(zoff, kLog2e, rc.c);
+    const float c = zoff + rc.c;
     uint4 in[NCH];
 #pragma unroll
     for (int j = 0; j < NCH; ++j) in[j] = row[(jb + j) ^ sw];
@@ -431,7 +433,7 @@ __device__ __forceinline__ void stage_row_to_bf16(const TileArgs& a, uint8_t* ti
       row[(jb + j) ^ sw] = make_uint4(o[0], o[1], o[2], o[3]);
     }
   } else {
-    const float c2 = fmaf(zoff, kLog2e, rc.shift2);
+    const float c2 = zoff + rc.shift2;
 #pragma unroll 1
     for (int j = jb; j < jb + NCH; ++j) {
       const uint4 x = row[j ^ sw];
@@ -441,7 +443,7 @@ __device__ __forceinline__ void stage_row_to_bf16(const TileArgs& a, uint8_t* ti
       for (int e = 0; e < 4; ++e) {
         float s0, s1;
         unpack_f16x2(w[e], s0, s1);
-        const float z0 = fmaf(s0, kLn2, zoff), z1 = fmaf(s1, kLn2, zoff);
+        const float z0 = (s0 + zoff) * kLn2, z1 = (s1 + zoff) * kLn2;
         o[e] = pack_bf16x2(rc.scale * ex2(s0 + c2) * dz_of_logit(a, z0),
                            rc.scale * ex2(s1 + c2) * dz_of_logit(a, z1));
       }
@@ -1363,8 +1365,9 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
               mx1 = fmaxf(mx1, fmaxf(lo[j + 1], hi[j + 1]));
             }
             const float mb = fmaxf(mx0, mx1);  // finite: col0 < V
-            // Stored: (z - mb) log2e in fp16, so that every reader's exponent
-            // is the stored value plus one fp32 constant per box.
+            // Stored: z log2e - mb2 in fp16 with mb2 = mb log2e beside it in
+            // fp32, so that every reader's exponent is the stored value plus
+            // fp32 constants, and adding mb2 back cancels its rounding.
             const float nmb2 = -mb * kLog2e;
             const unsigned off = static_cast<unsigned>(y - col0);
             if (off < 64u) {
@@ -1404,7 +1407,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
                   bulk_commit_group();
                 }
                 ++n_stores;
-                args.box_max[static_cast<long long>(lcol >> 6) * args.ldM + lrow] = mb;
+                args.box_max[static_cast<long long>(lcol >> 6) * args.ldM + lrow] = -nmb2;
               }
             } else if (valid) {
               uint16_t* dst = args.S + static_cast<long long>(lrow) * args.ldS + lcol;
@@ -1429,7 +1432,7 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
                     dst[32 + j] = static_cast<uint16_t>(pack_f16x2(fmaf(hi[j], kLog2e, nmb2), 0.f) & 0xffffu);
                 }
               }
-              args.box_max[static_cast<long long>(lcol >> 6) * args.ldM + lrow] = mb;
+              args.box_max[static_cast<long long>(lcol >> 6) * args.ldM + lrow] = -nmb2;
             }
             const float mn = fmaxf(m2, -nmb2);
             float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;

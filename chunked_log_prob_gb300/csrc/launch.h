@@ -69,7 +69,7 @@ struct GformArgs {
   uint16_t* S;           // [chunk rows][ldS]: fp16 logits in (each 64-column box
                          // relative to its maximum, in log2 units), bf16 G out
   long long ldS;
-  const float* box_max;  // [ceil(V / 64)][ldM] the boxes' maxima
+  const float* box_max;  // [ceil(V / 64)][ldM] the boxes' maxima times log2 e
   long long ldM;
   int v0, width;         // single_pass_p: the vocabulary block of S (splits = slots so far)
   int xmode;
