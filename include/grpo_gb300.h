@@ -110,10 +110,10 @@ typedef struct grpo_shape {
  * rows, the forward GEMM also keeps the chunk's (transformed) logits in fp16
  * in the workspace, and the dH GEMM runs over the whole vocabulary once lse
  * and g are known. Each 64-column box of a row is stored relative to its own
- * maximum (kept beside it in fp32), in log2 units ((z - max) log2 e), so any
- * finite logit is stored without overflow, the box's largest terms keep fp16's
- * finest spacing, and every exponential of G takes the stored value plus one
- * constant. The logits
+ * maximum, in log2 units (z log2 e - m, with m = max log2 e kept beside it in
+ * fp32), so any finite logit is stored without overflow, the box's largest
+ * terms keep fp16's finest spacing, and every exponential of G takes the
+ * stored value plus fp32 constants. The logits
  * are turned into G in one of two ways:
  *   - D <= 2048 without dW: the dH GEMM converts each landed tile on chip.
  *     One block of chunk x V x 2 bytes (capped at 4 GiB) serves every chunk.
