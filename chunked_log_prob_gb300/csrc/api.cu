@@ -198,6 +198,17 @@ void whole_batch_raster(int n_ru, int nvt, int D, int ctas, int slots, int* grou
   }
 }
 
+// Rounds of a dH-type launch of `units` units on `slots` SM pairs: whole
+// rounds, or with the tail split the last round's U units spread over the U
+// pairs and min(slots - U, slots / 3) tail pairs.
+double dh_rounds(long long units, int slots, bool split) {
+  const long long full = units / slots, u = units % slots;
+  if (u == 0) return static_cast<double>(full);
+  if (!split) return static_cast<double>(full + 1);
+  return static_cast<double>(full) +
+         static_cast<double>(u) / static_cast<double>(u + std::min<long long>(slots - u, slots / 3));
+}
+
 // Modelled GEMM time of the stored-logit schedule with chunks of nrb row
 // units, in forward-tile times (one 256-row x 256-column x D tile on one SM
 // pair). Each chunk runs a forward launch of (row units x splits) units and a
@@ -206,8 +217,9 @@ void whole_batch_raster(int n_ru, int nvt, int D, int ctas, int slots, int* grou
 // hide. exposed_g is that pass's time relative to the forward GEMM of the same
 // rows (0 when dH forms G itself). In the overlapped schedule pass c runs
 // beside dH(c-1) and the forward of chunk c+1; with a single chunk it is fully
-// exposed.
-double stored_cost(long long n_rb_total, int nrb, int n_dt, int nvt, int sms, double exposed_g) {
+// exposed. split: every dH launch has the tail split (dh_rounds).
+double stored_cost(long long n_rb_total, int nrb, int n_dt, int nvt, int sms, double exposed_g,
+                   bool split = false) {
   std::vector<double> fwd, dh;
   double actual = 0.0;
   for (long long r0 = 0; r0 < n_rb_total; r0 += nrb) {
@@ -217,7 +229,7 @@ double stored_cost(long long n_rb_total, int nrb, int n_dt, int nvt, int sms, do
     fwd.push_back(static_cast<double>(cdiv(static_cast<long long>(n) * sp, sms)) *
                   cdiv(nvt, sp));
     // dH: units of equal K; scaled to the forward's per-row work
-    dh.push_back(static_cast<double>(cdiv(static_cast<long long>(n) * n_dt, sms)) * nvt / n_dt);
+    dh.push_back(dh_rounds(static_cast<long long>(n) * n_dt, sms, split) * nvt / n_dt);
     actual += fwd.back() + dh.back();
   }
   const size_t nc = fwd.size();
@@ -296,7 +308,7 @@ int single_pass_fwd_splits(int nrb, int tiles, int cap, int sms) {
 // (measured: about a fifth of its time on GB300) and, with several blocks,
 // reads and rewrites its fp32 accumulator once per block.
 double single_pass_cost(long long n_rb_total, int nrb, int n_dt, int nvt, int vb_tiles, int nvb,
-                        int sms, double exposed_p) {
+                        int sms, double exposed_p, bool split = false) {
   // exposed_p = 0: P formed on chip; otherwise the P pass's time relative to
   // the block's forward GEMM, of which the neighbouring GEMMs hide what they
   // can (as in stored_cost). Measured on GB300 against the stored form's GEMMs
@@ -314,7 +326,7 @@ double single_pass_cost(long long n_rb_total, int nrb, int n_dt, int nvt, int vb
       const int sp = single_pass_fwd_splits(n, w, kMaxSplits / nvb, sms);
       fwd.push_back(static_cast<double>(cdiv(static_cast<long long>(n) * sp, sms)) * cdiv(w, sp) *
                     fwd_factor);
-      uac.push_back(static_cast<double>(cdiv(static_cast<long long>(n) * n_dt, sms)) * w / n_dt *
+      uac.push_back(dh_rounds(static_cast<long long>(n) * n_dt, sms, split) * w / n_dt *
                     uac_factor);
       actual += fwd.back() + uac.back();
     }
@@ -527,11 +539,19 @@ int make_layout_mode(const grpo_shape* s, const grpo_params* p, int sms, Form fo
   if (sms > 0) {
     const int rb = static_cast<int>(L->chunk_rows / ru_rows);
     const int vbt = static_cast<int>(cdiv(L->vblock, BN));
+    // The forms compared at D <= kFusedMaxHidden (the stored form's fused dH
+    // GEMM, the single pass with P on chip) split every dH-type launch when the
+    // slots are reserved: counted here, when forms are compared. Chunk sizes
+    // are still chosen counting whole rounds: with padding the device runs
+    // fewer row units than planned, and the larger chunks that this favours
+    // measured faster. Above kFusedMaxHidden the split covers at most a last
+    // launch and is not counted.
+    const bool split = L->ts_slots > 0 && L->fused && L->D <= kFusedMaxHidden;
     L->model_cost = L->stored        ? stored_cost(n_ru_total, rb, n_dt, L->nvt, slots,
-                                                   L->fused ? 0.0 : 550.0 / L->D)
+                                                   L->fused ? 0.0 : 550.0 / L->D, split)
                     : L->single_pass ? single_pass_cost(n_ru_total, rb, n_dt, L->nvt, vbt,
                                                         L->nvb, slots,
-                                                        L->fused ? 0.0 : 550.0 / L->D)
+                                                        L->fused ? 0.0 : 550.0 / L->D, split)
                                      : recompute_cost(n_ru_total, rb, n_dt, L->nvt, vbt, slots);
   }
   return GRPO_OK;
