@@ -129,6 +129,25 @@ def test_automatic_backward_form_follows_the_budget(clp):
     assert ws(0, 128 << 20) <= 128 << 20
 
 
+def test_automatic_form_at_the_qwen25_head_counts_the_tail_split(clp):
+    # D <= 2048: the stored form's fused dH GEMM and the single pass with P on
+    # chip both split the last round of their dH-type launches once a budget
+    # leaves room for the split's slots (from 608 MiB). Measured at this shape
+    # on GB300: 1 GB, stored 3.55-3.65 ms against the single pass's 4.36-4.38;
+    # 0.5 GB (no split), the single pass 5.64-5.69 against 7.65-7.69.
+    STORED, SINGLE_PASS = 1, 32
+    n, d, v, t = 8192, 1536, 151936, 1024
+
+    def ws(flags, limit=0):
+        return clp.grpo_workspace_size(n, d, v, t, clp.make_params(
+            flags=flags, workspace_limit_bytes=limit))
+    assert ws(0) == ws(STORED)
+    for limit in (1 << 30, 2 << 30):
+        assert ws(0, limit) == ws(STORED, limit) <= limit
+    for limit in (256 << 20, 512 << 20):
+        assert ws(0, limit) == ws(SINGLE_PASS, limit) <= limit
+
+
 def test_null_pointers_rejected_before_launch(clp):
     shape = clp.make_shape(10, 5, 16, 50)
     rc = clp.lib.grpo_loss_fwd_bwd(None, None, None, None, None, None, None, None, None, None,
