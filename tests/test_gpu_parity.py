@@ -240,6 +240,27 @@ def test_padding_blocks_are_skipped_and_zeroed(clp, chunk):
     check(got, want, p.mask, f"padding chunk={chunk}")
 
 
+@pytest.mark.parametrize("flags", [STORED, RECOMPUTE], ids=["stored", "recompute"])
+@pytest.mark.parametrize("D", [256, 2304])
+def test_splits_chosen_from_the_active_rows(clp, flags, D):
+    # 16 row units of slots, about 2 of them active after padding: the logit
+    # GEMM picks its vocab splits on the device from the active ones (not the
+    # count the host plans for), and the row finish reads all 32 partial
+    # slots of a row, the unused ones filled with (-inf, 0) by split 0.
+    # Results match the oracle and repeat bit for bit.
+    p = synth.make_problem("tiny", seed=71 + D, prompts=1, G=4, T=1024, D=D, V=9000,
+                           lengths=(1, 150))
+    old, ref, want = oracle_case(p)
+    params = clp.make_params(flags=flags)
+    plan = clp.grpo_get_plan(p.n_tokens, p.hidden_size, p.vocab, p.seq_len, params)
+    assert plan["n_chunks"] >= 1
+    got = gpu_loss(clp, p, old, ref, params)
+    check(got, want, p.mask, f"active-row splits flags={flags} D={D}")
+    again = gpu_loss(clp, p, old, ref, params)
+    assert got[0] == again[0]
+    assert np.array_equal(got[1], again[1]) and np.array_equal(got[2], again[2])
+
+
 XFORMS = [
     dict(temperature=0.7),
     dict(logit_softcapping=30.0),
