@@ -907,7 +907,9 @@ __global__ void __launch_bounds__(PairCfg<MODE, CTAS>::kThreads, 1)
             map_h1 = &map_hc;
           }
         }
-        const int a_row = MODE == MODE_DW ? 0 : (is_dh(MODE) ? li * BM : hr[0]);
+        int a_row = 0;  // MODE_DW: unused (its A rows are vocab rows)
+        if constexpr (is_dh(MODE)) a_row = li * BM;
+        else if constexpr (MODE != MODE_DW) a_row = hr[0];
         const int a_m0 = (ru * CTAS + static_cast<int>(rank)) * BM;  // MODE_DW: vocab row
         for (int t = t0; t < t1 && ok; ++t) {
           // MN-major B (DH, DHS, UAC, DW): 64-column boxes per accumulator in
@@ -1828,15 +1830,15 @@ __global__ void __launch_bounds__(BM * CTAS) tail_fixup_kernel(const TileArgs a)
       for (int e = 0; e < 8; ++e) x[e] = v[j8 * 8 + e];
       uacc_update8(a, ur, x, accp + j8 * 8, out + j8 * 8, wy + j8 * 8);
     }
-    return;
-  }
+  } else {
 #pragma unroll
-  for (int j8 = 0; j8 < 4; ++j8) {
-    if (d0 + j8 * 8 >= a.hidden) break;
-    st_global_v4(out + j8 * 8, pack_bf16x2(v[j8 * 8], v[j8 * 8 + 1]),
-                 pack_bf16x2(v[j8 * 8 + 2], v[j8 * 8 + 3]),
-                 pack_bf16x2(v[j8 * 8 + 4], v[j8 * 8 + 5]),
-                 pack_bf16x2(v[j8 * 8 + 6], v[j8 * 8 + 7]));
+    for (int j8 = 0; j8 < 4; ++j8) {
+      if (d0 + j8 * 8 >= a.hidden) break;
+      st_global_v4(out + j8 * 8, pack_bf16x2(v[j8 * 8], v[j8 * 8 + 1]),
+                   pack_bf16x2(v[j8 * 8 + 2], v[j8 * 8 + 3]),
+                   pack_bf16x2(v[j8 * 8 + 4], v[j8 * 8 + 5]),
+                   pack_bf16x2(v[j8 * 8 + 6], v[j8 * 8 + 7]));
+    }
   }
 }
 
