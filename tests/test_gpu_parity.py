@@ -133,9 +133,13 @@ def test_logp_fwd_ragged(clp, D, V):
 
 
 def test_chunking_does_not_change_results(clp):
-    # "No loss of accuracy" from chunking: the forward never depends on the
-    # backward chunking; dH rows depend on the chunk size not at all, and on
-    # the vocab block only through fp32 accumulation order.
+    # "No loss of accuracy" from chunking. At this vocabulary (12 tiles) every
+    # forward launch splits it into single tiles, whatever its chunk, so the
+    # forward does not depend on the chunking (with more tiles the splits
+    # follow each chunk's row units and results agree to rounding, as the
+    # Qwen3-8B head's chunk sweep checks); dH rows depend on the chunk size
+    # not at all, and on the vocab block only through fp32 accumulation
+    # order.
     p = synth.make_problem("tiny", seed=11, T=128, prompts=1, G=4, D=256, V=3000,
                            lengths=(40, 128))
     old, ref, _ = oracle_case(p)
